@@ -1,0 +1,321 @@
+/*
+ * xt.h — C ABI of libxt: forward kernels and analytic backward kernels of the ops of a
+ * pre-norm transformer block, for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [AE] xtrain "Phase: Autograd Engine + Op Backward — Design Document": op table
+ *        (forward / backward of each op), RMSNorm, RoPE, softmax and cross-entropy
+ *        derivations, composed attention, tape and gradient accumulation.
+ *   [BP] unhomeschool "Träna en språkmodell: Backprop i anpassad CUDA": forward pass of
+ *        the GPT-style stack, forward/backward kernel pairs, saved tensors, gradient
+ *        buffers with += semantics.
+ *   [DO] xtrain "Phase T18: Dropout (device RNG + mask) — Design Document": counter-based
+ *        RNG, per-site seeds, train/eval switch, residual-path wiring.
+ *
+ * Conventions shared by every entry point
+ *   - Return value: XT_OK (0) or an xt_status code; xt_last_error() gives a message
+ *     (thread-local, valid until the next call on the same thread).
+ *   - Pointers: DEVICE pointers owned by the caller, unless a comment says "host".
+ *     The library never allocates or frees memory.  Scratch space ("ws") is caller
+ *     memory of at least the size the matching *_workspace_size() reports; its contents
+ *     on entry do not matter.
+ *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns; nothing synchronises, except
+ *     xt_get_device_errors().
+ *   - Layout: row-major, contiguous unless a leading dimension (ld, in elements) is given.
+ *     "rows, cols": x is [rows, cols].  Weights are [in, out] and a linear layer is y = x @ W.
+ *   - dtype: XT_F32 or XT_BF16 storage; arithmetic is float32 (GEMMs: tf32 or bf16
+ *     tensor-core products with float32 accumulation).  Saved statistics (inv_rms, mean,
+ *     rstd, lse) are always float32.  Token ids and targets are int32.
+ *   - accumulate flags: 0 ⇒ dst = g; 1 ⇒ dst += g ([AE] § 梯度累加: first push sets,
+ *     later pushes add; [BP] § Ackumulation över mikrobatcher: backward adds into the
+ *     gradient buffers).
+ *   - Vector paths need 16-byte aligned pointers; misaligned pointers are still handled
+ *     (a scalar path) unless a function says otherwise.  Sizes are validated on the host;
+ *     invalid arguments return XT_ERR_INVALID_ARG before anything is launched.
+ *   - Errors detected on the device (an id or target outside [0, V), a bounded wait that
+ *     gave up) set bits in a device flag word read by xt_get_device_errors(); the offending
+ *     element is skipped (its output row is written as NaN where one exists).
+ */
+#ifndef XT_H
+#define XT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  XT_OK = 0,
+  XT_ERR_INVALID_ARG = 1,
+  XT_ERR_UNSUPPORTED = 2,
+  XT_ERR_ALIGNMENT = 3,
+  XT_ERR_CUDA = 4,
+  XT_ERR_TIMEOUT = 5
+} xt_status;
+
+typedef enum { XT_F32 = 0, XT_BF16 = 1 } xt_dtype;
+
+/* device error flag bits */
+#define XT_DEVERR_INDEX 1u   /* a token id or target outside [0, V) */
+#define XT_DEVERR_TIMEOUT 2u /* a bounded mbarrier wait in a GEMM gave up */
+
+const char* xt_last_error(void);
+const char* xt_version(void);
+
+/* Synchronises `stream`, then copies the device flag word to *out (host pointer).
+ * Returns XT_ERR_TIMEOUT if the timeout bit is set, XT_OK otherwise. */
+int xt_get_device_errors(uint32_t* out, void* stream);
+int xt_clear_device_errors(void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Gradient accumulation ([AE] § 梯度累加, push_grad/accumulate): dst[i] += src[i].
+ * dst and src may have different dtypes (e.g. bf16 src into an f32 dst).
+ * ------------------------------------------------------------------------------- */
+int xt_accumulate(void* dst, int dt_dst, const void* src, int dt_src, int64_t n, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Elementwise ops, [AE] op table rows add / mul / scale.  n elements, one dtype.
+ * Backward grads may be NULL to skip them.
+ * ------------------------------------------------------------------------------- */
+int xt_add_fwd(const void* a, const void* b, void* y, int64_t n, int dt, void* stream);
+/* da = d, db = d (copy or accumulate) */
+int xt_add_bwd(const void* d, void* da, void* db, int64_t n, int dt, int acc_a, int acc_b,
+               void* stream);
+int xt_mul_fwd(const void* a, const void* b, void* y, int64_t n, int dt, void* stream);
+/* da = d∘b, db = d∘a.  a and b may be the same pointer (mul(x, x)). */
+int xt_mul_bwd(const void* d, const void* a, const void* b, void* da, void* db, int64_t n,
+               int dt, int acc_a, int acc_b, void* stream);
+int xt_scale_fwd(const void* x, void* y, int64_t n, float alpha, int dt, void* stream);
+/* dx = d·alpha */
+int xt_scale_bwd(const void* d, void* dx, int64_t n, float alpha, int dt, int acc, void* stream);
+
+/* Full sum to one float32 (device pointer `out`), deterministic two-stage reduction.
+ * Needed by the validation loss L = Σ W∘out ([AE] § 验证方法). */
+int xt_sum_workspace_size(int64_t n, size_t* bytes);
+int xt_sum_fwd(const void* x, int64_t n, int dt, float* out, void* ws, void* stream);
+/* dx[i] = *upstream (device float32 scalar) */
+int xt_sum_bwd(const float* upstream, void* dx, int64_t n, int dt, int acc, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * add_bias ([AE] op table row add_bias): y[r,c] = x[r,c] + bias[c];
+ * backward dx = d (if dx != NULL), dbias[c] = Σ_r d[r,c], summed in a fixed order
+ * (per-CTA partials in ws, then one ordered pass).  bias / dbias have dtype dt_bias.
+ * ------------------------------------------------------------------------------- */
+int xt_colsum_workspace_size(int64_t rows, int64_t cols, size_t* bytes);
+int xt_add_bias_fwd(const void* x, const void* bias, void* y, int64_t rows, int64_t cols, int dt,
+                    void* stream);
+int xt_add_bias_bwd(const void* d, void* dx, void* dbias, int64_t rows, int64_t cols, int dt,
+                    int dt_bias, void* ws, int acc_dx, int acc_dbias, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Activations.  silu ([AE] op table row silu): y = x·σ(x), dx = d·(σ + x·σ·(1−σ)).
+ * swiglu ([AE] op table row swiglu): y = silu(g)∘u with g the gate; g and u may be
+ * column blocks of one buffer (row strides ld_in), grads likewise (ld_grad).
+ * gelu (exact, erf form; [BP] § kernel-pair table, k_mlp_fwd/bwd; backward reads the saved
+ * pre-activation, [BP] § Sparade tensorer): y = x·Φ(x), dx = d·(Φ(x) + x·φ(x)).
+ * ------------------------------------------------------------------------------- */
+int xt_silu_fwd(const void* x, void* y, int64_t n, int dt, void* stream);
+int xt_silu_bwd(const void* d, const void* x, void* dx, int64_t n, int dt, int acc, void* stream);
+int xt_swiglu_fwd(const void* g, const void* u, int64_t ld_in, void* y, int64_t ld_out,
+                  int64_t rows, int64_t cols, int dt, void* stream);
+int xt_swiglu_bwd(const void* d, int64_t ld_d, const void* g, const void* u, int64_t ld_in,
+                  void* dg, void* du, int64_t ld_grad, int64_t rows, int64_t cols, int dt,
+                  int acc, void* stream);
+int xt_gelu_fwd(const void* x, void* y, int64_t n, int dt, void* stream);
+int xt_gelu_bwd(const void* d, const void* x, void* dx, int64_t n, int dt, int acc, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * RMSNorm ([AE] § RMSNorm): ir = 1/√(mean_c x² + eps), y = x·ir·γ, inv_rms[r] = ir saved.
+ * Backward, g = d∘γ: dx = ir·g − x·ir³/n·Σ_c g·x; dγ[c] = Σ_r d·x·ir.
+ * gamma has dtype dt; dgamma has dtype dt_param.  dx or dgamma may be NULL.
+ * ------------------------------------------------------------------------------- */
+int xt_norm_bwd_workspace_size(int64_t rows, int64_t cols, size_t* bytes);
+int xt_rms_norm_fwd(const void* x, const void* gamma, void* y, float* inv_rms, int64_t rows,
+                    int64_t cols, float eps, int dt, void* stream);
+int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float* inv_rms,
+                    void* dx, void* dgamma, int64_t rows, int64_t cols, int dt, int dt_param,
+                    void* ws, int acc_dx, int acc_param, void* stream);
+
+/* LayerNorm (standard definition; [BP] § kernel-pair table k_layernorm_fwd/bwd and
+ * § Sparade tensorer: mean and variance saved — saved here as mean and rstd):
+ * μ = mean x, var = mean (x−μ)², rstd = 1/√(var+eps), x̂ = (x−μ)·rstd, y = x̂·γ + β.
+ * Backward, g = d∘γ: dx = rstd·(g − mean g − x̂·mean(g∘x̂)); dγ = Σ_r d∘x̂; dβ = Σ_r d. */
+int xt_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                     float* rstd, int64_t rows, int64_t cols, float eps, int dt, void* stream);
+int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const float* mean,
+                     const float* rstd, void* dx, void* dgamma, void* dbeta, int64_t rows,
+                     int64_t cols, int dt, int dt_param, void* ws, int acc_dx, int acc_param,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * RoPE ([AE] op table row rope and § RoPE 反向推导): for each pair (i, i+h), h = hd/2,
+ * θ = s·base^(−2i/hd):  y_i = x_i cos θ − x_{i+h} sin θ;  y_{i+h} = x_{i+h} cos θ + x_i sin θ.
+ * Backward is the transposed rotation: dx_i = d_i cos + d_{i+h} sin, dx_{i+h} = d_{i+h} cos − d_i sin.
+ * xt_rope_table fills table[2][S][hd/2] (cos then sin, float32, angles in float64) for
+ * positions pos_offset + s.  Token (b, s) head h lives at x + (b·S + s)·ld + h·hd.
+ * x and y may alias (in place).  hd must be even.
+ * ------------------------------------------------------------------------------- */
+int xt_rope_table(float* table, int S, int hd, double base, int pos_offset, void* stream);
+int xt_rope_fwd(const void* x, void* y, const float* table, int B, int S, int H, int hd,
+                int64_t ld, int dt, void* stream);
+int xt_rope_bwd(const void* d, void* dx, const float* table, int B, int S, int H, int hd,
+                int64_t ld, int dt, int acc, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Row-wise safe softmax ([AE] op table row softmax and § Softmax 反向推导):
+ * y = exp(x − max)/Σ exp(x − max); dx = y∘(d − Σ_c d∘y).
+ * causal: 0 = no mask; 1 = row r is query s = r mod q_len and columns c > s are masked
+ * (y = 0 there, written); 2 = as 1, but only columns c < min(cols, 128·(⌊s/128⌋+1)) are
+ * read or written (the layout the causal attention GEMMs consume; entries beyond are
+ * left untouched).
+ * ------------------------------------------------------------------------------- */
+int xt_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int causal, int64_t q_len,
+                   int dt, void* stream);
+int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t cols, int causal,
+                   int64_t q_len, int dt, int acc, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Cross-entropy, mean over rows ([AE] op table row cross_entropy, § Cross-entropy 反向推导):
+ * loss = (1/R) Σ_r (lse_r − x[r, t_r]);  dx = upstream·(softmax(x_r) − onehot(t_r))/R.
+ * lse (float32 [rows]) is saved by the forward; `loss` and `upstream` are device float32
+ * scalars.  dlogits may alias logits (in place) when dt_grad == dt.
+ * ------------------------------------------------------------------------------- */
+int xt_cross_entropy_workspace_size(int64_t rows, size_t* bytes);
+int xt_cross_entropy_fwd(const void* logits, const int32_t* targets, float* lse, float* loss,
+                         int64_t rows, int64_t V, int dt, void* ws, void* stream);
+int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float* lse,
+                         const float* upstream, void* dlogits, int64_t rows, int64_t V, int dt,
+                         int dt_grad, int acc, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Inverted dropout with a counter-based mask ([DO] § RNG：counter-based, § dropout 节点的
+ * backward): for flat element index i (uint64),
+ *   key = seed ⊕ (i·0x9E3779B97F4A7C15), h = splitmix64(key), u = (h>>40)·2⁻²⁴ (float32),
+ *   keep = u ≥ p, y = keep ? x·scale : 0 with scale = float32(1/(1−p)).
+ * The backward regenerates the same mask from (seed, i).  p == 0 or training == 0 is an
+ * exact copy.  p must be in [0, 1).  xt_dropout_mask writes the keep mask (1/0 bytes).
+ * xt_dropout_add_fwd fuses the residual: out = h + dropout(a) (out may alias h).
+ * ------------------------------------------------------------------------------- */
+int xt_dropout_fwd(const void* x, void* y, int64_t n, float p, uint64_t seed, int training,
+                   int dt, void* stream);
+int xt_dropout_bwd(const void* d, void* dx, int64_t n, float p, uint64_t seed, int training,
+                   int dt, int acc, void* stream);
+int xt_dropout_mask(uint8_t* mask, int64_t n, float p, uint64_t seed, void* stream);
+int xt_dropout_add_fwd(const void* h, const void* a, void* out, int64_t n, float p,
+                       uint64_t seed, int training, int dt, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Embedding ([BP] § kernel-pair table k_embed_fwd/bwd; § Var gradienter lever i minnet):
+ * h[t] = E[ids[t]] (+ P[t mod S] when P != NULL).  Backward: dE[v] = Σ_{t: ids[t]=v} dh[t]
+ * summed in ascending t (deterministic), dP[s] = Σ_b dh[b·S+s].  With acc == 0 the rows
+ * of dE that no token touches are zeroed.  T ≤ 65536.
+ * ------------------------------------------------------------------------------- */
+int xt_embedding_workspace_size(int64_t T, size_t* bytes);
+int xt_embedding_fwd(const int32_t* ids, const void* E, const void* P, void* h, int64_t T, int S,
+                     int64_t d, int64_t V, int dt, void* stream);
+int xt_embedding_bwd(const int32_t* ids, const void* dh, void* dE, void* dP, int64_t T, int S,
+                     int64_t d, int64_t V, int dt_dh, int dt_grad, void* ws, int acc,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Matmul on the tensor cores ([AE] op table row matmul: C = A@B; dA = d@Bᵀ, dB = Aᵀ@d).
+ *   op(A) is M×K: trans_a = 0 ⇒ A stored [M, K] (ld lda); 1 ⇒ A stored [K, M].
+ *   op(B) is K×N: trans_b = 0 ⇒ B stored [K, N] (ld ldb); 1 ⇒ B stored [N, K].
+ *   C [M, N] (ld ldc) = alpha·op(A)@op(B)  (+ C when accumulate).
+ * Two batch levels (outer × inner) with element strides, e.g. (batch, head) for attention.
+ * dtype_ab: XT_BF16 (bf16 products) or XT_F32 (tf32 products); dtype_c: XT_F32 or XT_BF16.
+ * Requirements (else XT_ERR_ALIGNMENT): A, B 16-byte aligned; lda, ldb and the A/B batch
+ * strides are multiples of 16 bytes; C 16-byte aligned and ldc a multiple of 16 bytes.
+ * causal (square attention blocks, 128-row granularity): 0 none; 1 skip output tiles
+ * entirely above the diagonal block (n0 ≥ m0+128); 2 stop the K loop at m0+128 (A is a
+ * causal probability block); 3 start the K loop at m0 (A is a transposed causal block).
+ * ------------------------------------------------------------------------------- */
+typedef struct xt_matmul_desc {
+  int32_t M, N, K;
+  int32_t trans_a, trans_b;
+  int32_t batch_outer, batch_inner;
+  int32_t dtype_ab, dtype_c;
+  int32_t accumulate;
+  int32_t causal;
+  float alpha;
+  int64_t lda, ldb, ldc;
+  int64_t stride_a_outer, stride_a_inner;
+  int64_t stride_b_outer, stride_b_inner;
+  int64_t stride_c_outer, stride_c_inner;
+} xt_matmul_desc;
+
+int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C,
+                  void* stream);
+/* Backward of C = alpha·op(A)@op(B) given dC (layout of C, dtype dtype_ab):
+ * dA = alpha·dC@op(B)ᵀ into A's layout, dB = alpha·op(A)ᵀ@dC into B's layout; dA/dB have
+ * dtype dt_grad_a / dt_grad_b; either may be NULL.  causal must be 0. */
+int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* dC,
+                  void* dA, void* dB, int dt_grad_a, int dt_grad_b, int acc_a, int acc_b,
+                  void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Native block stack ([BP] § Framåtgåendet; [DO] § dropout 接在哪（wiring）):
+ *   h = E[ids] (+ P);  per layer l:  h += dropout(attn(norm1 h), seed ⊕ l ⊕ 0xA77),
+ *                                    h += dropout(mlp(norm2 h),  seed ⊕ l ⊕ 0xF70);
+ *   logits = norm_f(h) @ Eᵀ;  loss = cross_entropy(logits, targets).
+ * attn: q,k,v = x@W_qkv (W_qkv = [W_Q | W_K | W_V], [d, 3d]); optional RoPE on q, k;
+ * per (b, head) P = softmax_causal(q kᵀ/√hd), o = P v; attn = o @ W_O.
+ * mlp: SWIGLU: (silu(x@W_g) ∘ x@W_u) @ W_d with W_gu = [W_g | W_u] ([d, 2F]);
+ *      GELU:   gelu(x@W_1) @ W_2.
+ * xt_block_fwd runs the forward and keeps the saved tensors in ws; xt_block_bwd then adds
+ * every parameter gradient into the grad buffers (+=, [BP] § Ackumulation över mikrobatcher);
+ * call xt_block_zero_grads first for a fresh step.  No host synchronisation; the pair can
+ * be captured in a CUDA graph.
+ * ------------------------------------------------------------------------------- */
+enum { XT_NORM_RMS = 0, XT_NORM_LN = 1 };
+enum { XT_MLP_SWIGLU = 0, XT_MLP_GELU = 1 };
+
+typedef struct xt_block_config {
+  int32_t B, S, d, H, hd, F, V, n_layers;
+  int32_t norm;       /* XT_NORM_RMS or XT_NORM_LN */
+  int32_t mlp;        /* XT_MLP_SWIGLU or XT_MLP_GELU */
+  int32_t rope;       /* 1: rotate q and k */
+  int32_t learned_pos;/* 1: P [S, d] added to the embedding */
+  int32_t causal;     /* must be 1 */
+  int32_t training;   /* 0: dropout is the identity */
+  int32_t dtype;      /* activation and weight storage: XT_F32 or XT_BF16 */
+  int32_t grad_dtype; /* parameter-gradient storage: XT_F32 or XT_BF16 */
+  float eps;
+  float p;            /* residual dropout probability */
+  double rope_base;
+  uint64_t base_seed;
+} xt_block_config;
+
+/* Per-layer parameter (and gradient) pointers; arrays of n_layers device pointers,
+ * held in HOST memory.  Fields unused by the configuration may be NULL. */
+typedef struct xt_block_params {
+  const void* E;      /* [V, d] */
+  const void* P;      /* [S, d] or NULL */
+  const void* const* g1; const void* const* b1;
+  const void* const* Wqkv; const void* const* Wo;
+  const void* const* g2; const void* const* b2;
+  const void* const* W_up;   /* [d, 2F] (SWIGLU) or [d, F] (GELU) */
+  const void* const* W_down; /* [F, d] */
+  const void* gf; const void* bf;
+  void* dE; void* dP;
+  void* const* dg1; void* const* db1;
+  void* const* dWqkv; void* const* dWo;
+  void* const* dg2; void* const* db2;
+  void* const* dW_up; void* const* dW_down;
+  void* dgf; void* dbf;
+} xt_block_params;
+
+int xt_block_workspace_size(const xt_block_config* cfg, size_t* bytes);
+int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const int32_t* ids,
+                 const int32_t* targets, float* loss, void* ws, void* stream);
+int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const int32_t* ids,
+                 const int32_t* targets, void* ws, void* stream);
+int xt_block_zero_grads(const xt_block_config* cfg, const xt_block_params* prm, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XT_H */

@@ -1,0 +1,69 @@
+"""Helpers for the GPU parity tests: moving synthetic inputs to the device and comparing
+device results with the oracle under the tolerances the tests use.
+
+Tolerances:
+  * fp32 row / elementwise ops: max_i |g − r| / max(|r_i|, 1e-6·max|r|) ≤ 1e-5;
+  * bf16 ops (oracle run on the same bf16-rounded inputs): |g − r| ≤ 1 bf16 ulp of |r_i|
+    (2^(⌊log2 |r_i|⌋ − 7)) + 1e-5·max|r|;
+  * GEMM paths and whole-block gradients: ‖g − r‖ / ‖r‖ ≤ 2e-2.
+"""
+import numpy as np
+import torch
+
+DEV = "cuda"
+
+
+def dev(a, dtype="f32"):
+    t = torch.tensor(np.asarray(a, dtype=np.float32))
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+    return t.to(DEV)
+
+
+def host(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def empty(shape, dtype="f32", fill=None):
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    if fill is None:
+        return torch.empty(shape, dtype=td, device=DEV)
+    return torch.full(shape, fill, dtype=td, device=DEV)
+
+
+def rel_err_floor(g, r, floor=1e-6):
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    den = np.maximum(np.abs(r), floor * max(np.max(np.abs(r)), 1e-30))
+    return float(np.max(np.abs(g - r) / den))
+
+
+def bf16_ulp_excess(g, r, floor=1e-5):
+    """max over elements of |g − r| / (1 ulp(r) + floor·max|r|); ≤ 1 passes."""
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    a = np.abs(r)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1e-300)))
+    ulp = np.where(a > 0, 2.0 ** (e - 7), 0.0)
+    tol = ulp + floor * max(np.max(a), 1e-30)
+    return float(np.max(np.abs(g - r) / tol))
+
+
+def norm_err(g, r):
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    return float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300))
+
+
+def check(g, r, dtype, what=""):
+    if dtype == "f32":
+        e = rel_err_floor(g, r)
+        assert e <= 1e-5, f"{what}: fp32 rel err {e:.3e}"
+    else:
+        e = bf16_ulp_excess(g, r)
+        assert e <= 1.0, f"{what}: bf16 error {e:.3f} ulp-units"
+
+
+def sync():
+    torch.cuda.synchronize()

@@ -1,0 +1,61 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry point that
+include/xt.h declares, the binding declares them all, and host-side validation rejects bad
+arguments before anything touches the device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xt.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(xt_\w+)\s*\(", src, re.M)))
+
+
+@pytest.fixture(scope="module")
+def xt():
+    from transformer_fwd_bwd_gb300 import build
+    build.build()
+    from transformer_fwd_bwd_gb300 import xt as m
+    m.lib()
+    return m
+
+
+def test_header_parses():
+    fns = header_functions()
+    assert "xt_matmul_fwd" in fns and "xt_rms_norm_bwd" in fns and len(fns) > 40
+
+
+def test_exports_every_declared_symbol(xt):
+    L = xt.lib()
+    missing = [f for f in header_functions() if not hasattr(L, f)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_binding_declares_every_symbol(xt):
+    declared = set(xt.exported_symbols())
+    missing = [f for f in header_functions() if f not in declared]
+    assert not missing, f"binding lacks: {missing}"
+
+
+def test_host_validation(xt):
+    L = xt.lib()
+    assert L.xt_matmul_fwd(None, None, None, None, None) == xt.XT_ERR_INVALID_ARG
+    assert b"desc is NULL" in L.xt_last_error()
+    assert L.xt_dropout_fwd(None, None, 10, C.c_float(1.5), 1, 1, 0, None) == xt.XT_ERR_INVALID_ARG
+    assert L.xt_rope_table(None, 4, 7, C.c_double(1e4), 0, None) == xt.XT_ERR_INVALID_ARG
+    assert L.xt_softmax_fwd(None, None, 4, 8, 5, 0, 0, None) == xt.XT_ERR_INVALID_ARG
+    assert L.xt_rms_norm_fwd(None, None, None, None, -1, 8, C.c_float(1e-5), 0, None) == xt.XT_ERR_INVALID_ARG
+    assert L.xt_accumulate(None, 7, None, 0, 4, None) == xt.XT_ERR_INVALID_ARG
+    d = xt.matmul_desc(64, 64, 60, lda=60, ldb=64)
+    assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None) == xt.XT_ERR_ALIGNMENT
+    d = xt.matmul_desc(64, 64, 64, lda=8)
+    assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None) == xt.XT_ERR_INVALID_ARG
+    sz = C.c_size_t(0)
+    assert L.xt_embedding_workspace_size(1000, C.byref(sz)) == 0 and sz.value == 8000
+    assert L.xt_sum_workspace_size(-1, C.byref(sz)) == xt.XT_ERR_INVALID_ARG
+    assert xt.version().startswith("xt")

@@ -1,0 +1,177 @@
+"""GPU parity of the tensor-core matmul against the oracle (NumPy float64 on the same
+bf16 / fp32 inputs), through the C ABI.
+
+Bounds: the contract is ‖g − r‖/‖r‖ ≤ 2e-2.  The tests also hold each case to what its
+arithmetic allows: bf16 operands are exact in the fp32 products, so only fp32 accumulation
+and output rounding remain (≤ 1e-5 normalised for fp32 C, ≤ 4e-3 for bf16 C); tf32 keeps
+10 mantissa bits of each operand (≤ 2e-3 normalised).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import ops as O
+from tests.gpu_util import dev, host, norm_err, sync
+
+pytestmark = pytest.mark.gpu
+
+xt = pytest.importorskip("transformer_fwd_bwd_gb300.xt")
+
+
+def bound(ab, c):
+    if ab == "f32":
+        return 2e-3
+    return 1e-5 if c == "f32" else 4e-3
+
+
+def stored(M, N, K, ta, tb, ab, seed):
+    A = synth.normal((K, M) if ta else (M, K), seed, dtype=ab)
+    B = synth.normal((N, K) if tb else (K, N), seed + 1, dtype=ab)
+    return A, B
+
+
+def op(X, t):
+    return X.T if t else X
+
+
+CASES = [(128, 64, 64), (200, 96, 72), (256, 256, 128), (1000, 776, 328), (64, 40, 16), (384, 512, 1024)]
+
+
+@pytest.mark.parametrize("ab", ["bf16", "f32"])
+@pytest.mark.parametrize("c", ["f32", "bf16"])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", CASES)
+def test_matmul_fwd(ab, c, ta, tb, M, N, K):
+    A, B = stored(M, N, K, ta, tb, ab, 40)
+    want = O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5
+    C = torch.empty((M, N), dtype=torch.float32 if c == "f32" else torch.bfloat16, device="cuda")
+    d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_ab=xt.XT_BF16 if ab == "bf16" else xt.XT_F32,
+                       dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, alpha=0.5)
+    xt.xt_matmul_fwd(d, dev(A, ab), dev(B, ab), C); sync()
+    e = norm_err(host(C), want)
+    assert e <= min(2e-2, bound(ab, c)), f"normalised error {e:.2e}"
+    assert xt.device_errors() == 0
+
+
+@pytest.mark.parametrize("ab", ["bf16", "f32"])
+def test_matmul_accumulate_and_k0(ab):
+    M, N, K = 300, 136, 200
+    A, B = stored(M, N, K, 0, 0, ab, 41)
+    C0 = synth.normal((M, N), 43)
+    Cd = dev(C0, "f32")
+    d = xt.matmul_desc(M, N, K, dtype_ab=xt.XT_BF16 if ab == "bf16" else xt.XT_F32, accumulate=1)
+    xt.xt_matmul_fwd(d, dev(A, ab), dev(B, ab), Cd); sync()
+    assert norm_err(host(Cd), C0 + A @ B) <= bound(ab, "f32")
+    # K = 0: C = 0 without accumulate, unchanged with
+    d0 = xt.matmul_desc(M, N, 0, dtype_ab=d.dtype_ab, accumulate=0, lda=8, ldb=N)
+    xt.xt_matmul_fwd(d0, dev(A, ab), dev(B, ab), Cd); sync()
+    assert np.all(host(Cd) == 0)
+
+
+@pytest.mark.parametrize("ab", ["bf16", "f32"])
+@pytest.mark.parametrize("S,hd", [(256, 64), (200, 64), (16, 16)])
+def test_matmul_batched_heads(ab, S, hd):
+    """Attention layout: q, k, v are column blocks of a [B·S, 3·H·hd] buffer; per (b, h)
+    scores = q kᵀ · scale into [B, H, S, S]; o = P v into [B·S, H·hd]."""
+    Bn, H = 2, 3
+    dm = H * hd
+    qkv = synth.normal((Bn * S, 3 * dm), 44, dtype=ab)
+    q = qkv[:, :dm].reshape(Bn, S, H, hd).transpose(0, 2, 1, 3)
+    k = qkv[:, dm:2 * dm].reshape(Bn, S, H, hd).transpose(0, 2, 1, 3)
+    v = qkv[:, 2 * dm:].reshape(Bn, S, H, hd).transpose(0, 2, 1, 3)
+    QKV = dev(qkv, ab)
+    dab = xt.XT_BF16 if ab == "bf16" else xt.XT_F32
+    e = 2 if ab == "bf16" else 4
+    sc = 1.0 / np.sqrt(hd)
+    scores = torch.empty((Bn, H, S, S), dtype=torch.float32, device="cuda")
+    d = xt.matmul_desc(S, S, hd, trans_a=0, trans_b=1, lda=3 * dm, ldb=3 * dm, ldc=S, batch_outer=Bn,
+                       batch_inner=H, dtype_ab=dab, dtype_c=xt.XT_F32, alpha=sc,
+                       strides=(S * 3 * dm, hd, S * 3 * dm, hd, H * S * S, S * S))
+    xt.xt_matmul_fwd(d, QKV, QKV[:, dm:], scores); sync()
+    want = np.einsum("bhsd,bhtd->bhst", q, k) * sc
+    assert norm_err(host(scores), want) <= bound(ab, "f32")
+    # o = P v with P from the oracle, written into the head-interleaved [B·S, H·hd] layout
+    P = synth.to_storage(O.softmax_fwd(want, causal=True), ab)
+    out = torch.zeros((Bn * S, dm), dtype=torch.float32, device="cuda")
+    d2 = xt.matmul_desc(S, hd, S, trans_a=0, trans_b=0, lda=S, ldb=3 * dm, ldc=dm, batch_outer=Bn, batch_inner=H,
+                        dtype_ab=dab, dtype_c=xt.XT_F32, strides=(H * S * S, S * S, S * 3 * dm, hd, S * dm, hd))
+    xt.xt_matmul_fwd(d2, dev(P, ab), QKV[:, 2 * dm:], out); sync()
+    wo = np.einsum("bhst,bhtd->bhsd", P, v).transpose(0, 2, 1, 3).reshape(Bn * S, dm)
+    assert norm_err(host(out), wo) <= bound(ab, "f32")
+    del e
+
+
+@pytest.mark.parametrize("S", [384, 200, 1024])
+def test_matmul_causal_modes(S):
+    """Mode 1 skips output tiles above the diagonal block; mode 2 stops K at the block
+    diagonal (probabilities are 0 beyond); mode 3 starts K at the block diagonal."""
+    hd = 64
+    rng = np.random.default_rng(45)
+    q = synth.normal((S, hd), 46, dtype="bf16")
+    k = synth.normal((S, hd), 47, dtype="bf16")
+    full = q @ k.T
+    C = torch.full((S, S), float("nan"), dtype=torch.float32, device="cuda")
+    d = xt.matmul_desc(S, S, hd, trans_b=1, causal=1)
+    xt.xt_matmul_fwd(d, dev(q, "bf16"), dev(k, "bf16"), C); sync()
+    g = host(C)
+    s_idx, c_idx = np.meshgrid(np.arange(S), np.arange(S), indexing="ij")
+    need = c_idx < np.minimum((s_idx // 128 + 1) * 128, S)   # what the causal softmax reads
+    assert norm_err(g[need], full[need]) <= 1e-5
+    # mode 2: A is a causal probability block (zero beyond each row's 128-aligned extent)
+    P = np.where(c_idx <= s_idx, synth.normal((S, S), 48, dtype="bf16"), 0.0)
+    Pd = dev(np.where(need, P, np.nan), "bf16")   # beyond the extent: never read
+    v = synth.normal((S, hd), 49, dtype="bf16")
+    O2 = torch.empty((S, hd), dtype=torch.float32, device="cuda")
+    d2 = xt.matmul_desc(S, hd, S, causal=2)
+    xt.xt_matmul_fwd(d2, Pd, dev(v, "bf16"), O2); sync()
+    assert norm_err(host(O2), P @ v) <= 1e-5
+    # mode 3: dV = Pᵀ dO with P stored [S_q, S_k] read transposed
+    dO = synth.normal((S, hd), 50, dtype="bf16")
+    dV = torch.empty((S, hd), dtype=torch.float32, device="cuda")
+    d3 = xt.matmul_desc(S, hd, S, trans_a=1, causal=3)
+    xt.xt_matmul_fwd(d3, Pd, dev(dO, "bf16"), dV); sync()
+    assert norm_err(host(dV), P.T @ dO) <= 1e-5
+    del rng
+
+
+@pytest.mark.parametrize("ab", ["bf16", "f32"])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_matmul_bwd(ab, ta, tb):
+    M, N, K = 264, 200, 136
+    A, B = stored(M, N, K, ta, tb, ab, 51)
+    dC = synth.normal((M, N), 53, dtype=ab)
+    dA_r, dB_r = O.matmul_bwd(dC, op(A, ta), op(B, tb))
+    dA_r, dB_r = op(dA_r, ta) * 2.0, op(dB_r, tb) * 2.0   # back into the stored layouts, alpha = 2
+    dab = xt.XT_BF16 if ab == "bf16" else xt.XT_F32
+    d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_ab=dab, alpha=2.0)
+    dA = torch.empty(A.shape, dtype=torch.float32, device="cuda")
+    dB = torch.ones(B.shape, dtype=torch.float32, device="cuda")
+    xt.xt_matmul_bwd(d, dev(A, ab), dev(B, ab), dev(dC, ab), dA, dB, 0, 1); sync()
+    assert norm_err(host(dA), dA_r) <= bound(ab, "f32")
+    assert norm_err(host(dB), dB_r + 1) <= bound(ab, "f32")
+
+
+def test_matmul_large_sampled():
+    """Transformer-sized projections (QKV of the 12-layer stack: 8192 × 2304 × 768) and the
+    tied logits (8192 × 50304 × 768, NT), checked on sampled rows against the oracle."""
+    for (M, N, K, tb) in [(8192, 2304, 768, 0), (8192, 50304, 768, 1)]:
+        A = synth.normal((M, K), 54, dtype="bf16")
+        B = synth.normal((N, K) if tb else (K, N), 55, std=0.02, dtype="bf16")
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        d = xt.matmul_desc(M, N, K, trans_b=tb, dtype_c=xt.XT_BF16)
+        xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), C); sync()
+        rows = np.random.default_rng(0).choice(M, 24, replace=False)
+        rows = np.concatenate([rows, [0, 127, 128, M - 1]])
+        want = A[rows] @ op(B, tb)
+        assert norm_err(host(C[torch.tensor(rows, device="cuda")]), want) <= 4e-3
+        assert xt.device_errors() == 0
+
+
+def test_matmul_alignment_rejected():
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    d = xt.matmul_desc(64, 64, 60, lda=60, ldb=64)   # 120-byte rows: not 16-byte aligned
+    with pytest.raises(xt.XtError) as ei:
+        xt.xt_matmul_fwd(d, A, A, C)
+    assert ei.value.code == xt.XT_ERR_ALIGNMENT

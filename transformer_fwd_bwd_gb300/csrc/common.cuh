@@ -1,0 +1,173 @@
+// Shared helpers of libxt: status reporting, dtype conversion, 16-byte vector access,
+// warp / row-group reductions, device facts.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "../../include/xt.h"
+
+namespace xt {
+
+// ------------------------------------------------------------------------------ host status
+
+// Records the message for xt_last_error() and returns `code`.
+int fail(int code, const char* fmt, ...);
+// Maps the last CUDA launch error (if any) to XT_ERR_CUDA.
+int check_launch(const char* what);
+// Device address of the error flag word on the current device.
+uint32_t* errflag();
+// Multiprocessor count of the current device (cached per device).
+int num_sms();
+
+#define XT_REQUIRE(cond, ...)                                      \
+  do {                                                             \
+    if (!(cond)) return ::xt::fail(XT_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+#define XT_TRY(expr)              \
+  do {                            \
+    int _st = (expr);             \
+    if (_st != XT_OK) return _st; \
+  } while (0)
+
+inline bool valid_dtype(int dt) { return dt == XT_F32 || dt == XT_BF16; }
+inline size_t dtype_size(int dt) { return dt == XT_BF16 ? 2 : 4; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------------------ device: dtype
+
+typedef __nv_bfloat16 bf16;
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// 16-byte vector of T: VW = 4 floats or 8 bf16.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int W = 4;
+  __device__ __forceinline__ static void load(const float* p, float (&v)[4]) {
+    float4 q = *reinterpret_cast<const float4*>(p);
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  }
+  __device__ __forceinline__ static void load_nc(const float* p, float (&v)[4]) {
+    float4 q = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  }
+  __device__ __forceinline__ static void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <> struct Vec<bf16> {
+  static constexpr int W = 8;
+  __device__ __forceinline__ static void unpack(const uint4& q, float (&v)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ static void load(const bf16* p, float (&v)[8]) {
+    unpack(*reinterpret_cast<const uint4*>(p), v);
+  }
+  __device__ __forceinline__ static void load_nc(const bf16* p, float (&v)[8]) {
+    unpack(__ldg(reinterpret_cast<const uint4*>(p)), v);
+  }
+  __device__ __forceinline__ static void store(bf16* p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// 8 elements at a time for any storage type (fp32: two 16-byte loads, bf16: one).
+template <typename T> struct V8;
+template <> struct V8<float> {
+  __device__ __forceinline__ static void load(const float* p, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  __device__ __forceinline__ static void store(float* p, const float (&v)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+};
+template <> struct V8<bf16> {
+  __device__ __forceinline__ static void load(const bf16* p, float (&v)[8]) { Vec<bf16>::load(p, v); }
+  __device__ __forceinline__ static void store(bf16* p, const float (&v)[8]) { Vec<bf16>::store(p, v); }
+};
+
+// Generic access with a vector width VW of 1 (scalar path for ragged or misaligned data),
+// 4 (fp32, one 16-byte access) or 8 (any type; 16-byte aligned).
+template <typename T, int VW> struct Acc {
+  __device__ __forceinline__ static void load(const T* p, float (&v)[VW]) {
+    if constexpr (VW == 1) v[0] = to_f(p[0]);
+    else if constexpr (VW == 8) V8<T>::load(p, v);
+    else Vec<T>::load(p, v);
+  }
+  __device__ __forceinline__ static void store(T* p, const float (&v)[VW]) {
+    if constexpr (VW == 1) p[0] = from_f<T>(v[0]);
+    else if constexpr (VW == 8) V8<T>::store(p, v);
+    else Vec<T>::store(p, v);
+  }
+};
+
+// ------------------------------------------------------------------------------ reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Reduction over a row group of `tpr` consecutive threads (tpr a power of two, 32..1024;
+// groups are warp aligned).  `red` is shared scratch of blockDim/32 floats.  Every thread
+// of the group gets the result.  All threads of the block must call it together.
+template <bool MAX>
+__device__ __forceinline__ float group_reduce(float v, int tpr, float* red) {
+  v = MAX ? warp_max(v) : warp_sum(v);
+  if (tpr <= 32) return v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpg = tpr >> 5;                 // warps per group
+  const int g0 = (warp / wpg) * wpg;        // first warp of this group
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[g0];
+  for (int w = 1; w < wpg; ++w) r = MAX ? fmaxf(r, red[g0 + w]) : r + red[g0 + w];
+  return r;
+}
+
+// Online-softmax pair (running max m, running Σ exp(x − m)).
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) { m = mm; s = 0.f; return; }
+  s = s * expf(m - mm) + s2 * expf(m2 - mm);
+  m = mm;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t* flag, uint32_t bit) {
+  if (flag) atomicOr(flag, bit);
+}
+
+}  // namespace xt

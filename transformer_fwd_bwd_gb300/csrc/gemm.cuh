@@ -1,0 +1,57 @@
+// Internal interface between the GEMM host code and its kernel instantiations.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemm_kernel.cuh"
+
+namespace xt {
+namespace gemm {
+
+// One operand as the kernel reads it: `mn` rows (M for A, N for B) by K.
+// mn_major = false: K contiguous (element (i, k) at ptr + i·ld + k);
+// mn_major = true:  MN contiguous (element (i, k) at ptr + k·ld + i).
+struct Operand {
+  const void* ptr;
+  bool mn_major;
+  int64_t mn, K, ld, s_inner, s_outer;
+  int batch_inner, batch_outer;
+};
+
+struct Problem {
+  bool tf32;
+  int64_t M, N, K;
+  int batch_inner, batch_outer;
+  Operand A, B;
+  void* C;
+  int64_t ldc, sc_inner, sc_outer;
+  int c_bf16;
+  float alpha;
+  int accumulate;
+  int causal;
+};
+
+int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn);
+int run(const Problem& pb, cudaStream_t s);
+int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                int grid, cudaStream_t s);
+int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                int grid, cudaStream_t s);
+
+template <bool TF32, int BN, bool A_MN, bool B_MN>
+int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t s) {
+  auto k = gemm_kernel<TF32, BN, A_MN, B_MN>;
+  constexpr int smem = Cfg<TF32, BN>::SMEM;
+  static bool attr_set = false;  // per instantiation; idempotent if raced
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return check_launch("gemm: shared memory attribute");
+    attr_set = true;
+  }
+  k<<<grid, kThreads, smem, s>>>(ta, tb, p);
+  return check_launch("gemm kernel");
+}
+
+}  // namespace gemm
+}  // namespace xt

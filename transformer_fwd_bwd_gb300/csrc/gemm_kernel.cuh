@@ -1,0 +1,444 @@
+// Tensor-core GEMM for sm_103a: tcgen05.mma with the accumulator in tensor memory (TMEM),
+// operands staged in shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle),
+// an mbarrier pipeline of STAGES slots, and a persistent tile loop.
+//
+// Roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 allocates TMEM and its
+// lane 0 issues the MMAs; warps 2..5 drain the accumulator (tcgen05.ld) and store C.
+// TMEM holds two accumulators of BN fp32 columns so the epilogue of tile i overlaps the
+// MMAs of tile i+1.
+//
+// Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
+// XT_DEVERR_TIMEOUT in the device flag, every role stops issuing work, the producer waits
+// (bounded) for its copies in flight, and TMEM is released before the CTA exits.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace xt {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int kThreads = 192;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct Params {
+  int M, N, K;
+  int num_m, num_n;
+  int batch_inner, batches;  // batches = outer × inner
+  int causal;
+  int accumulate;
+  int c_bf16;
+  float alpha;
+  void* C;
+  int64_t ldc, sc_inner, sc_outer;
+  uint32_t* flag;
+};
+
+// ------------------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase of parity `parity`; false when the time limit expired.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kTimeoutNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrives on `bar` once every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+template <bool TF32>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accum) {
+  if constexpr (TF32) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+  }
+}
+// 32 lanes × 32 consecutive fp32 columns: thread t of the warp receives row (lane base + t).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (sm_100 format): start address, leading- and stride-
+// dimension byte offsets (all >> 4), descriptor version 1 at bit 46, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor for kind::f16 / kind::tf32: fp32 accumulator, A/B types (bf16 = 1,
+// tf32 = 2), operand majorness (1 = MN-major), N >> 3, M >> 4.
+template <bool TF32, int N, bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | ((TF32 ? 2u : 1u) << 7) | ((TF32 ? 2u : 1u) << 10) | ((A_MN ? 1u : 0u) << 15) |
+         ((B_MN ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
+
+template <int BN>
+constexpr uint32_t tmem_cols() {
+  return 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+}
+
+template <bool TF32, int BN>
+struct Cfg {
+  static constexpr int E = TF32 ? 4 : 2;
+  static constexpr int BK = 128 / E;         // K elements per stage (one 128-byte row)
+  static constexpr int ATOM = 128 / E;       // MN elements per 128-byte swizzle row
+  static constexpr int UK = TF32 ? 8 : 16;   // K per MMA instruction
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+};
+
+struct TileInfo {
+  int m0, n0, zi, zo, kb_begin, kb_end;
+  bool skip;
+};
+
+template <int BK>
+__device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
+  TileInfo ti;
+  const int per = p.num_m * p.num_n;
+  const int z = t / per;
+  const int r = t - z * per;
+  const int nb = r / p.num_m;
+  const int mb = r - nb * p.num_m;  // m fastest: concurrent CTAs share B tiles
+  ti.m0 = mb * BM;
+  ti.n0 = nb * 0;  // set by caller (BN known there)
+  ti.zo = z / p.batch_inner;
+  ti.zi = z - ti.zo * p.batch_inner;
+  ti.kb_begin = 0;
+  ti.kb_end = (p.K + BK - 1) / BK;
+  if (p.causal == 2) {
+    const int e = (ti.m0 + BM + BK - 1) / BK;
+    if (e < ti.kb_end) ti.kb_end = e;
+  } else if (p.causal == 3) {
+    ti.kb_begin = ti.m0 / BK;
+  }
+  ti.skip = false;
+  (void)nb;
+  return ti;
+}
+
+template <bool TF32, int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using C_ = Cfg<TF32, BN>;
+  constexpr int BK = C_::BK, ATOM = C_::ATOM, UK = C_::UK, STAGES = C_::STAGES;
+  constexpr uint32_t IDESC = instr_desc<TF32, BN, A_MN, B_MN>();
+  constexpr uint32_t TCOLS = tmem_cols<BN>();
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C_::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const int total = p.num_m * p.num_n * p.batches;
+
+  auto info = [&](int t) {
+    TileInfo ti = tile_info<BK>(t, p);
+    const int per = p.num_m * p.num_n;
+    const int r = t - (t / per) * per;
+    ti.n0 = (r / p.num_m) * BN;
+    if (p.causal == 1 && ti.n0 >= ti.m0 + BM) ti.skip = true;
+    return ti;
+  };
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_error(p.flag, XT_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileInfo ti = info(t);
+        if (ti.skip) continue;
+        for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (*abort_flag) break;
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1)) { give_up(); break; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_expect_tx(fb, C_::STAGE_BYTES);
+          const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
+          const uint32_t b_s = a_s + C_::A_BYTES;
+          const int k0 = kb * BK;
+          if constexpr (!A_MN) {
+            tma_load_4d(a_s, &tmA, fb, k0, ti.m0, ti.zi, ti.zo);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / ATOM; ++j) tma_load_4d(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.zi, ti.zo);
+          }
+          if constexpr (!B_MN) {
+            tma_load_4d(b_s, &tmB, fb, k0, ti.n0, ti.zi, ti.zo);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / ATOM; ++j) tma_load_4d(b_s + j * (BK * 128), &tmB, fb, ti.n0 + j * ATOM, k0, ti.zi, ti.zo);
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // Wait (bounded) for the copies that may still be in flight: the last min(STAGES, issued)
+      // fills, so no TMA write lands in shared memory after the CTA exits.
+      const int pending = issued < STAGES ? issued : STAGES;
+      for (int i = 0; i < pending; ++i) {
+        if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
+        if (!mbar_wait(smem_u32(&full[stage]), phase)) { give_up(); break; }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileInfo ti = info(t);
+        if (ti.skip || ti.kb_end <= ti.kb_begin) continue;
+        if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1)) { give_up(); break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tbase + uint32_t(ab * BN);
+        bool ok = true;
+        for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (*abort_flag || !mbar_wait(smem_u32(&full[stage]), phase)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
+          const uint32_t b_s = a_s + C_::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc(a_s + kk * UK * 128, BK * 128, 1024)
+                                     : smem_desc(a_s + kk * UK * C_::E, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc(b_s + kk * UK * 128, BK * 128, 1024)
+                                     : smem_desc(b_s + kk * UK * C_::E, 16, 1024);
+            tc_mma<TF32>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[stage]));  // frees the smem slot once these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) { give_up(); break; }
+        tc_commit(smem_u32(&tfull[ab]));  // accumulator ready for the epilogue
+        if (++ab == 2) { ab = 0; aphase ^= 1; }
+      }
+    }
+  } else {
+    // -------------------------------------------------------------------- epilogue
+    // Every decision below is warp-uniform: tcgen05.ld is a .sync.aligned instruction.
+    const int q = warp & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
+    int ab = 0;
+    uint32_t aphase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const TileInfo ti = info(t);
+      if (ti.skip) continue;
+      const int row = ti.m0 + q * 32 + lane;
+      const bool empty_k = ti.kb_end <= ti.kb_begin;
+      if (!empty_k) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[ab]), aphase));
+        if (!ok) {
+          if (lane == 0) give_up();
+          break;
+        }
+        tc_fence_after();
+      }
+      const int64_t cbase = int64_t(ti.zo) * p.sc_outer + int64_t(ti.zi) * p.sc_inner + int64_t(row) * p.ldc;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        if (!empty_k) {
+          tmem_ld32(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN + c * 32), r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = 0u;
+        }
+        const int col0 = ti.n0 + c * 32;
+        if (row >= p.M || col0 >= p.N) continue;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.alpha;
+        const bool full_cols = col0 + 32 <= p.N;
+        if (!p.c_bf16) {
+          float* cp = static_cast<float*>(p.C) + cbase + col0;
+          if (full_cols) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              if (p.accumulate) {
+                const float4 old = *reinterpret_cast<const float4*>(cp + j);
+                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+              }
+              *reinterpret_cast<float4*>(cp + j) = o;
+            }
+          } else {
+            const int nrem = p.N - col0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nrem) cp[j] = v[j] + (p.accumulate ? cp[j] : 0.f);
+          }
+        } else {
+          bf16* cp = static_cast<bf16*>(p.C) + cbase + col0;
+          if (full_cols) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              float o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] = v[j + e];
+              if (p.accumulate) {
+                float old[8];
+                Vec<bf16>::load(cp + j, old);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] += old[e];
+              }
+              Vec<bf16>::store(cp + j, o);
+            }
+          } else {
+            const int nrem = p.N - col0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nrem) cp[j] = __float2bfloat16_rn(v[j] + (p.accumulate ? __bfloat162float(cp[j]) : 0.f));
+          }
+        }
+      }
+      if (!empty_k) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+        if (++ab == 2) { ab = 0; aphase ^= 1; }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TCOLS);
+  }
+}
+
+}  // namespace gemm
+}  // namespace xt

@@ -1,0 +1,26 @@
+// fp32 operands read as tf32, fp32-accumulated GEMM instantiations (tcgen05 kind::tf32).
+#include "gemm.cuh"
+
+namespace xt {
+namespace gemm {
+
+template <int BN>
+static int pick_major(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid,
+                      cudaStream_t s) {
+  if (!a_mn && !b_mn) return launch_one<true, BN, false, false>(ta, tb, p, grid, s);
+  if (!a_mn && b_mn) return launch_one<true, BN, false, true>(ta, tb, p, grid, s);
+  if (a_mn && !b_mn) return launch_one<true, BN, true, false>(ta, tb, p, grid, s);
+  return launch_one<true, BN, true, true>(ta, tb, p, grid, s);
+}
+
+int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                int grid, cudaStream_t s) {
+  switch (bn) {
+    case 64: return pick_major<64>(a_mn, b_mn, ta, tb, p, grid, s);
+    case 128: return pick_major<128>(a_mn, b_mn, ta, tb, p, grid, s);
+    default: return fail(XT_ERR_UNSUPPORTED, "gemm: tile width %d", bn);
+  }
+}
+
+}  // namespace gemm
+}  // namespace xt

@@ -1,0 +1,1133 @@
+// Row-wise ops: RMSNorm, LayerNorm, softmax, cross-entropy; RoPE; embedding; column sums.
+//
+// Row-resident kernels keep a thread's share of one row in registers as packed 16-byte
+// vectors (4 registers per vector for both fp32 and bf16): a row of `cols` elements is split
+// over a row group of `tpr` threads (power of two, 32..1024), each holding up to NV = 4
+// vectors, so one global read feeds the reductions and the outputs.  Several row groups
+// share a block when rows are short.  Column reductions (dγ, dβ, dbias) are deterministic:
+// per-block partial rows in the workspace, then one ordered pass.
+#include "common.cuh"
+
+namespace xt {
+
+constexpr int NV = 4;  // vectors per thread in row-resident kernels
+
+// Packed storage of one vector (VW elements) of T.
+template <typename T, int VW> struct Raw;
+template <typename T> struct Raw<T, 1> {
+  float v;
+  __device__ __forceinline__ void load(const T* p) { v = to_f(*p); }
+  __device__ __forceinline__ float get(int) const { return v; }
+  __device__ __forceinline__ void zero() { v = 0.f; }
+};
+template <> struct Raw<float, 4> {
+  float4 q;
+  __device__ __forceinline__ void load(const float* p) { q = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ float get(int e) const {
+    return e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
+  }
+  __device__ __forceinline__ void zero() { q = make_float4(0.f, 0.f, 0.f, 0.f); }
+};
+template <> struct Raw<bf16, 8> {
+  uint4 q;
+  __device__ __forceinline__ void load(const bf16* p) { q = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ float get(int e) const {
+    const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
+    return (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+  }
+  __device__ __forceinline__ void zero() { q = make_uint4(0, 0, 0, 0); }
+};
+
+template <typename T, int VW>
+__device__ __forceinline__ void store_vec(T* p, const float (&v)[VW]) {
+  Acc<T, VW>::store(p, v);
+}
+template <typename T, int VW>
+__device__ __forceinline__ void load_vec(const T* p, float (&v)[VW]) {
+  Acc<T, VW>::load(p, v);
+}
+
+struct RowPlan {
+  int vw, tpr, threads, rpb;
+  bool ok;
+};
+
+static int next_pow2(int64_t v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// Plans a row-resident launch: vector width, threads per row, block size, rows per block.
+static RowPlan plan_rows(int64_t cols, int vw, int max_tpr = 1024) {
+  RowPlan pl{};
+  pl.vw = vw;
+  const int64_t nvec = ceil_div(cols, vw);
+  if (nvec > int64_t(NV) * max_tpr) { pl.ok = false; return pl; }
+  int tpr = next_pow2(ceil_div(nvec, NV));
+  if (tpr < 32) tpr = 32;
+  pl.tpr = tpr;
+  pl.threads = tpr < 256 ? 256 : tpr;
+  pl.rpb = pl.threads / tpr;
+  pl.ok = true;
+  return pl;
+}
+
+static bool rows_vec_ok(int64_t cols, int dt, std::initializer_list<const void*> ptrs) {
+  const int vw = dt == XT_BF16 ? 8 : 4;
+  if (cols % vw) return false;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return false;
+  return true;
+}
+
+static int row_grid(int64_t rows, int rpb, int cap_per_sm = 32) {
+  int64_t g = ceil_div(rows, rpb);
+  const int64_t cap = int64_t(num_sms()) * cap_per_sm;
+  if (g > cap) g = cap;
+  return int(g < 1 ? 1 : g);
+}
+
+// Fixed number of blocks of the column-reducing backward kernels (one partial row each).
+static int bwd_blocks(int64_t rows, int rpb) {
+  int64_t g = ceil_div(rows, rpb);
+  const int64_t cap = int64_t(num_sms()) * 2;
+  if (g > cap) g = cap;
+  return int(g < 1 ? 1 : g);
+}
+
+// ============================================================================== RMSNorm
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(1024) rms_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                                                      T* __restrict__ y, float* __restrict__ inv_rms,
+                                                      int64_t rows, int64_t cols, float eps, int tpr) {
+  __shared__ float red[32];
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    Raw<T, VW> v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) v[k].load(x + r * cols + j * VW); else v[k].zero();
+#pragma unroll
+      for (int e = 0; e < VW; ++e) ss += v[k].get(e) * v[k].get(e);
+    }
+    ss = group_reduce<false>(ss, tpr, red);
+    const float ir = 1.f / sqrtf(ss / float(cols) + eps);
+    if (act && l == 0) inv_rms[r] = ir;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        float gm[VW], o[VW];
+        load_vec<T, VW>(gamma + j * VW, gm);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) o[e] = v[k].get(e) * ir * gm[e];
+        store_vec<T, VW>(y + r * cols + j * VW, o);
+      }
+    }
+  }
+}
+
+// Sequentially folds each row group's per-column partials into smem `acc` (cols floats) and
+// writes the block's partial row to part[blockIdx.x].  Deterministic.
+template <int VW>
+__device__ __forceinline__ void fold_partials(const float (&p)[NV][VW], float* acc, float* part, int tpr,
+                                              int64_t nvec, int64_t cols) {
+  const int rpb = blockDim.x / tpr, grp = threadIdx.x / tpr, l = threadIdx.x % tpr;
+  for (int g = 0; g < rpb; ++g) {
+    if (grp == g) {
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int64_t j = l + int64_t(k) * tpr;
+        if (j < nvec)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) acc[j * VW + e] = (g == 0 ? 0.f : acc[j * VW + e]) + p[k][e];
+      }
+    }
+    __syncthreads();
+  }
+  for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) part[int64_t(blockIdx.x) * cols + c] = acc[c];
+}
+
+template <typename T, int VW, int MAXT>
+__global__ void __launch_bounds__(MAXT) rms_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
+                                                      const T* __restrict__ gamma, const float* __restrict__ inv_rms,
+                                                      T* dx, float* __restrict__ part, int64_t rows, int64_t cols,
+                                                      int tpr, int acc_dx) {
+  extern __shared__ float smem[];
+  float* red = smem;          // 32
+  float* colacc = smem + 32;  // cols
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  float pg[NV][VW];
+  Raw<T, VW> gm[NV];  // this thread's columns of γ, the same for every row
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t j = l + int64_t(k) * tpr;
+    if (j < nvec) gm[k].load(gamma + j * VW); else gm[k].zero();
+#pragma unroll
+    for (int e = 0; e < VW; ++e) pg[k][e] = 0.f;
+  }
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    Raw<T, VW> vd[NV], vx[NV];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        vd[k].load(d + r * cols + j * VW);
+        vx[k].load(x + r * cols + j * VW);
+      } else {
+        vd[k].zero(); vx[k].zero();
+      }
+#pragma unroll
+      for (int e = 0; e < VW; ++e) s += vd[k].get(e) * gm[k].get(e) * vx[k].get(e);
+    }
+    s = group_reduce<false>(s, tpr, red);
+    const float ir = act ? inv_rms[r] : 0.f;
+    const float c2 = ir * ir * ir / float(cols) * s;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        float o[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float xv = vx[k].get(e), dv = vd[k].get(e);
+          o[e] = ir * dv * gm[k].get(e) - xv * c2;
+          pg[k][e] += dv * xv * ir;
+        }
+        if (dx) {
+          T* p = dx + r * cols + j * VW;
+          if (acc_dx) {
+            float old[VW];
+            load_vec<T, VW>(p, old);
+#pragma unroll
+            for (int e = 0; e < VW; ++e) o[e] += old[e];
+          }
+          store_vec<T, VW>(p, o);
+        }
+      }
+    }
+  }
+  if (part) fold_partials<VW>(pg, colacc, part, tpr, nvec, cols);
+}
+
+// ============================================================================== LayerNorm
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                                                     const T* __restrict__ beta, T* __restrict__ y,
+                                                     float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                                                     int64_t rows, int64_t cols, float eps, int tpr) {
+  __shared__ float red[32];
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    Raw<T, VW> v[NV];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) v[k].load(x + r * cols + j * VW); else v[k].zero();
+#pragma unroll
+      for (int e = 0; e < VW; ++e) s += v[k].get(e);
+    }
+    const float mu = group_reduce<false>(s, tpr, red) / float(cols);
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (j < nvec)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float c = v[k].get(e) - mu;
+          q += c * c;
+        }
+    }
+    const float var = group_reduce<false>(q, tpr, red) / float(cols);
+    const float rs = 1.f / sqrtf(var + eps);
+    if (act && l == 0) { mean_out[r] = mu; rstd_out[r] = rs; }
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        float gm[VW], bt[VW], o[VW];
+        load_vec<T, VW>(gamma + j * VW, gm);
+        load_vec<T, VW>(beta + j * VW, bt);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) o[e] = (v[k].get(e) - mu) * rs * gm[e] + bt[e];
+        store_vec<T, VW>(y + r * cols + j * VW, o);
+      }
+    }
+  }
+}
+
+template <typename T, int VW, int MAXT>
+__global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
+                                                     const T* __restrict__ gamma, const float* __restrict__ mean,
+                                                     const float* __restrict__ rstd, T* dx, float* __restrict__ part_g,
+                                                     float* __restrict__ part_b, int64_t rows, int64_t cols,
+                                                     int tpr, int acc_dx) {
+  extern __shared__ float smem[];
+  float* red = smem;
+  float* colacc = smem + 32;
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  float pg[NV][VW], pb[NV][VW];
+  Raw<T, VW> gm[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t j = l + int64_t(k) * tpr;
+    if (j < nvec) gm[k].load(gamma + j * VW); else gm[k].zero();
+#pragma unroll
+    for (int e = 0; e < VW; ++e) { pg[k][e] = 0.f; pb[k][e] = 0.f; }
+  }
+  const float inv_n = 1.f / float(cols);
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    const float mu = act ? mean[r] : 0.f, rs = act ? rstd[r] : 0.f;
+    Raw<T, VW> vd[NV], vx[NV];
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        vd[k].load(d + r * cols + j * VW);
+        vx[k].load(x + r * cols + j * VW);
+      } else {
+        vd[k].zero(); vx[k].zero();
+      }
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        const float g = vd[k].get(e) * gm[k].get(e);
+        sg += g;
+        sgx += g * (vx[k].get(e) - mu) * rs;
+      }
+    }
+    const float mg = group_reduce<false>(sg, tpr, red) * inv_n;
+    const float mgx = group_reduce<false>(sgx, tpr, red) * inv_n;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        float o[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float xh = (vx[k].get(e) - mu) * rs, dv = vd[k].get(e);
+          o[e] = rs * (dv * gm[k].get(e) - mg - xh * mgx);
+          pg[k][e] += dv * xh;
+          pb[k][e] += dv;
+        }
+        if (dx) {
+          T* p = dx + r * cols + j * VW;
+          if (acc_dx) {
+            float old[VW];
+            load_vec<T, VW>(p, old);
+#pragma unroll
+            for (int e = 0; e < VW; ++e) o[e] += old[e];
+          }
+          store_vec<T, VW>(p, o);
+        }
+      }
+    }
+  }
+  if (part_g) fold_partials<VW>(pg, colacc, part_g, tpr, nvec, cols);
+  __syncthreads();
+  if (part_b) fold_partials<VW>(pb, colacc, part_b, tpr, nvec, cols);
+}
+
+// ============================================================================== column sums
+
+// part[nb][cols] → out[cols] (dtype TO), summing partial rows in order.
+template <typename TO>
+__global__ void colsum_finalize(const float* __restrict__ part, int nb, int64_t cols, TO* out, int acc) {
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < cols; c += int64_t(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < nb; ++b) s += part[int64_t(b) * cols + c];
+    if (acc) s += to_f(out[c]);
+    out[c] = from_f<TO>(s);
+  }
+}
+
+static int finalize(const float* part, int nb, int64_t cols, void* out, int dt, int acc, cudaStream_t s) {
+  const int grid = int(ceil_div(cols, 256));
+  if (dt == XT_F32) colsum_finalize<float><<<grid, 256, 0, s>>>(part, nb, cols, static_cast<float*>(out), acc);
+  else colsum_finalize<bf16><<<grid, 256, 0, s>>>(part, nb, cols, static_cast<bf16*>(out), acc);
+  return check_launch("column-sum finalize");
+}
+
+constexpr int kColChunkRows = 16;  // rows per partial in the plain column sum
+
+static int colsum_chunks(int64_t rows) { return int(ceil_div(rows, kColChunkRows)); }
+
+// Plain column sum of d [rows, cols] into per-chunk partials (and an optional copy dx = d).
+template <typename T>
+__global__ void colsum_stage1(const T* __restrict__ d, T* dx, int acc_dx, float* __restrict__ part, int64_t rows,
+                              int64_t cols) {
+  const int64_t chunk = blockIdx.y;
+  const int64_t r_begin = chunk * kColChunkRows;
+  const int64_t r_end = r_begin + kColChunkRows < rows ? r_begin + kColChunkRows : rows;
+  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < cols; c += int64_t(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int64_t r = r_begin; r < r_end; ++r) {
+      const float v = to_f(d[r * cols + c]);
+      s += v;
+      if (dx) dx[r * cols + c] = from_f<T>(acc_dx ? to_f(dx[r * cols + c]) + v : v);
+    }
+    part[chunk * cols + c] = s;
+  }
+}
+
+// ============================================================================== softmax
+
+// causal extent of row with query index s: columns read / written
+__device__ __forceinline__ int64_t causal_visible(int64_t s, int64_t cols) { return s + 1 < cols ? s + 1 : cols; }
+__device__ __forceinline__ int64_t causal_extent(int causal, int64_t s, int64_t cols) {
+  if (causal == 2) {
+    const int64_t e = (s / 128 + 1) * 128;
+    return e < cols ? e : cols;
+  }
+  return cols;
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(1024) softmax_fwd_kernel(const T* __restrict__ x, T* __restrict__ y, int64_t rows,
+                                                          int64_t cols, int causal, int64_t q_len, int tpr) {
+  __shared__ float red[32];
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    const int64_t vis = causal ? causal_visible(r % q_len, cols) : cols;
+    Raw<T, VW> v[NV];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec && j * VW < vis) v[k].load(x + r * cols + j * VW); else v[k].zero();
+#pragma unroll
+      for (int e = 0; e < VW; ++e)
+        if (act && j < nvec && j * VW + e < vis) m = fmaxf(m, v[k].get(e));
+    }
+    m = group_reduce<true>(m, tpr, red);
+    float ex[NV][VW];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        ex[k][e] = (act && j < nvec && j * VW + e < vis) ? expf(v[k].get(e) - m) : 0.f;
+        s += ex[k][e];
+      }
+    }
+    s = group_reduce<false>(s, tpr, red);
+    const float inv = 1.f / s;
+    const int64_t ext = causal ? causal_extent(causal, r % q_len, cols) : cols;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec && j * VW < ext) {
+        float o[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) o[e] = ex[k][e] * inv;
+        store_vec<T, VW>(y + r * cols + j * VW, o);
+      }
+    }
+  }
+}
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(1024) softmax_bwd_kernel(const T* __restrict__ d, const T* __restrict__ y, T* dx,
+                                                          int64_t rows, int64_t cols, int causal, int64_t q_len,
+                                                          int tpr, int acc) {
+  __shared__ float red[32];
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    const int64_t vis = causal ? causal_visible(r % q_len, cols) : cols;
+    Raw<T, VW> vd[NV], vy[NV];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec && j * VW < vis) {
+        vd[k].load(d + r * cols + j * VW);
+        vy[k].load(y + r * cols + j * VW);
+      } else {
+        vd[k].zero(); vy[k].zero();
+      }
+#pragma unroll
+      for (int e = 0; e < VW; ++e)
+        if (j * VW + e < vis) s += vd[k].get(e) * vy[k].get(e);
+    }
+    s = group_reduce<false>(s, tpr, red);
+    const int64_t ext = causal ? causal_extent(causal, r % q_len, cols) : cols;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec && j * VW < ext) {
+        float o[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e)
+          o[e] = (j * VW + e < vis) ? vy[k].get(e) * (vd[k].get(e) - s) : 0.f;
+        T* p = dx + r * cols + j * VW;
+        if (acc) {
+          float old[VW];
+          load_vec<T, VW>(p, old);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) o[e] += old[e];
+        }
+        store_vec<T, VW>(p, o);
+      }
+    }
+  }
+}
+
+// ============================================================================== cross-entropy
+
+// Streaming online log-sum-exp over one row per row group; writes lse[r] and nll[r].
+template <typename T, int VW>
+__global__ void __launch_bounds__(1024) ce_fwd_kernel(const T* __restrict__ x, const int32_t* __restrict__ tgt,
+                                                     float* __restrict__ lse, float* __restrict__ nll, int64_t rows,
+                                                     int64_t V, int tpr, uint32_t* flag) {
+  __shared__ float red_m[32], red_s[32];
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = V / VW;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    float m = -INFINITY, s = 0.f;
+    if (act) {
+      const T* row = x + r * V;
+      for (int64_t j = l; j < nvec; j += tpr) {
+        float v[VW];
+        load_vec<T, VW>(row + j * VW, v);
+        float vm = v[0];
+#pragma unroll
+        for (int e = 1; e < VW; ++e) vm = fmaxf(vm, v[e]);
+        float vs = 0.f;
+#pragma unroll
+        for (int e = 0; e < VW; ++e) vs += expf(v[e] - vm);
+        lse_merge(m, s, vm, vs);
+      }
+    }
+    // row-group merge of (m, s): warp shuffle, then shared memory across warps
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_merge(m, s, m2, s2);
+    }
+    if (tpr > 32) {
+      const int warp = threadIdx.x >> 5, wpg = tpr >> 5, g0 = (warp / wpg) * wpg;
+      __syncthreads();
+      if ((threadIdx.x & 31) == 0) { red_m[warp] = m; red_s[warp] = s; }
+      __syncthreads();
+      m = red_m[g0]; s = red_s[g0];
+      for (int w = 1; w < wpg; ++w) lse_merge(m, s, red_m[g0 + w], red_s[g0 + w]);
+    }
+    if (act && l == 0) {
+      const float L = m + logf(s);
+      lse[r] = L;
+      const int32_t t = tgt[r];
+      if (t < 0 || int64_t(t) >= V) {
+        flag_error(flag, XT_DEVERR_INDEX);
+        nll[r] = __int_as_float(0x7fc00000);
+      } else {
+        nll[r] = L - to_f(x[r * V + t]);
+      }
+    }
+  }
+}
+
+// loss = Σ nll / rows in a fixed order (one block).
+__global__ void ce_loss_kernel(const float* __restrict__ nll, int64_t rows, float* loss) {
+  __shared__ float red[32];
+  float acc = 0.f;
+  for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) acc += nll[i];
+  acc = warp_sum(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) s += red[w];
+    *loss = s / float(rows);
+  }
+}
+
+// dx = (upstream / rows)·(exp(x − lse) − onehot(t))
+template <typename T, typename TG, int VW>
+__global__ void __launch_bounds__(256) ce_bwd_kernel(const T* x, const int32_t* __restrict__ tgt,
+                                                    const float* __restrict__ lse, const float* __restrict__ upstream,
+                                                    TG* dx, int64_t rows, int64_t V, int acc, uint32_t* flag) {
+  const float sc = *upstream / float(rows);
+  const int64_t nvec = V / VW;
+  const int64_t total = rows * nvec;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = v / nvec, c = (v - r * nvec) * VW;
+    const float L = lse[r];
+    const int32_t t = tgt[r];
+    const bool bad = t < 0 || int64_t(t) >= V;
+    float xv[VW], o[VW];
+    load_vec<T, VW>(x + r * V + c, xv);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      const float p = expf(xv[e] - L);
+      o[e] = bad ? __int_as_float(0x7fc00000) : sc * (p - (c + e == t ? 1.f : 0.f));
+    }
+    if (bad && c == 0) flag_error(flag, XT_DEVERR_INDEX);
+    TG* p = dx + r * V + c;
+    if (acc) {
+      float old[VW];
+      load_vec<TG, VW>(p, old);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) o[e] += old[e];
+    }
+    store_vec<TG, VW>(p, o);
+  }
+}
+
+// ============================================================================== RoPE
+
+__global__ void rope_table_kernel(float* table, int S, int hd, double base, int pos_offset) {
+  const int h = hd / 2;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < S * h; idx += gridDim.x * blockDim.x) {
+    const int s = idx / h, i = idx - s * h;
+    const double th = double(pos_offset + s) * pow(base, -2.0 * double(i) / double(hd));
+    double sn, cs;
+    sincos(th, &sn, &cs);
+    table[idx] = float(cs);
+    table[S * h + idx] = float(sn);
+  }
+}
+
+// BWD = false: y_i = x_i c − x_{i+h} s; y_{i+h} = x_{i+h} c + x_i s
+// BWD = true:  dx_i = d_i c + d_{i+h} s; dx_{i+h} = d_{i+h} c − d_i s
+template <typename T, bool BWD, int VW>
+__global__ void __launch_bounds__(256) rope_kernel(const T* x, T* y, const float* __restrict__ table, int B, int S,
+                                                  int H, int hd, int64_t ld, int acc) {
+  const int h = hd / 2;
+  const int per_head = h / VW;
+  const int64_t total = int64_t(B) * S * H * per_head;
+  const float* ct = table;
+  const float* st = table + int64_t(S) * h;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t tok_head = v / per_head;
+    const int i0 = int(v - tok_head * per_head) * VW;
+    const int64_t tok = tok_head / H;
+    const int head = int(tok_head - tok * H);
+    const int s = int(tok % S);
+    const int64_t off = tok * ld + int64_t(head) * hd + i0;
+    float a[VW], b[VW], c[VW], sn[VW], o1[VW], o2[VW];
+    load_vec<T, VW>(x + off, a);
+    load_vec<T, VW>(x + off + h, b);
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      c[e] = ct[int64_t(s) * h + i0 + e];
+      sn[e] = st[int64_t(s) * h + i0 + e];
+    }
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      if (BWD) {
+        o1[e] = a[e] * c[e] + b[e] * sn[e];
+        o2[e] = b[e] * c[e] - a[e] * sn[e];
+      } else {
+        o1[e] = a[e] * c[e] - b[e] * sn[e];
+        o2[e] = b[e] * c[e] + a[e] * sn[e];
+      }
+    }
+    if (acc) {
+      float p1[VW], p2[VW];
+      load_vec<T, VW>(y + off, p1);
+      load_vec<T, VW>(y + off + h, p2);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) { o1[e] += p1[e]; o2[e] += p2[e]; }
+    }
+    store_vec<T, VW>(y + off, o1);
+    store_vec<T, VW>(y + off + h, o2);
+  }
+}
+
+// ============================================================================== embedding
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(256) embed_fwd_kernel(const int32_t* __restrict__ ids, const T* __restrict__ E,
+                                                       const T* __restrict__ P, T* __restrict__ h, int64_t T_,
+                                                       int S, int64_t d, int64_t V, uint32_t* flag) {
+  const int64_t per = d / VW;
+  const int64_t total = T_ * per;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t t = v / per, c = (v - t * per) * VW;
+    const int32_t id = ids[t];
+    float o[VW];
+    if (id < 0 || int64_t(id) >= V) {
+      if (c == 0) flag_error(flag, XT_DEVERR_INDEX);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) o[e] = __int_as_float(0x7fc00000);
+    } else {
+      load_vec<T, VW>(E + int64_t(id) * d + c, o);
+      if (P) {
+        float p[VW];
+        load_vec<T, VW>(P + int64_t(t % S) * d + c, p);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) o[e] += p[e];
+      }
+    }
+    store_vec<T, VW>(h + t * d + c, o);
+  }
+}
+
+constexpr int kSortMax = 16384;
+
+// One block sorts keys (id << 32 | t) ascending (bitonic, in shared memory); ids outside
+// [0, V) get the key (V << 32 | t) so they sort last and are skipped.
+__global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restrict__ ids, int64_t T_, int64_t V,
+                                                         uint64_t* __restrict__ sorted, uint32_t* flag) {
+  extern __shared__ uint64_t keys[];
+  int n = 1;
+  while (n < T_) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    if (i < T_) {
+      const int32_t id = ids[i];
+      const bool bad = id < 0 || int64_t(id) >= V;
+      if (bad) flag_error(flag, XT_DEVERR_INDEX);
+      keys[i] = (uint64_t(bad ? uint64_t(V) : uint64_t(id)) << 32) | uint64_t(i);
+    } else {
+      keys[i] = ~uint64_t(0);
+    }
+  }
+  __syncthreads();
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int p = i ^ j;
+        if (p > i) {
+          const uint64_t a = keys[i], b = keys[p];
+          const bool up = (i & k) == 0;
+          if ((a > b) == up) { keys[i] = b; keys[p] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < T_; i += blockDim.x) sorted[i] = keys[i];
+}
+
+// Block i: if sorted position i starts a run of equal ids, sums that run's dh rows in
+// ascending t and adds the sum into dE[id].
+template <typename TH, typename TG>
+__global__ void __launch_bounds__(256) embed_scatter_kernel(const uint64_t* __restrict__ sorted, const TH* __restrict__ dh,
+                                                           TG* dE, int64_t T_, int64_t d, int64_t V) {
+  const int64_t i = blockIdx.x;
+  const uint64_t key = sorted[i];
+  const int64_t id = int64_t(key >> 32);
+  if (id >= V) return;
+  if (i > 0 && int64_t(sorted[i - 1] >> 32) == id) return;
+  int64_t end = i + 1;
+  while (end < T_ && int64_t(sorted[end] >> 32) == id) ++end;
+  for (int64_t c = threadIdx.x; c < d; c += blockDim.x) {
+    float s = 0.f;
+    for (int64_t k = i; k < end; ++k) s += to_f(dh[int64_t(uint32_t(sorted[k])) * d + c]);
+    TG* p = dE + id * d + c;
+    *p = from_f<TG>(to_f(*p) + s);
+  }
+}
+
+// dP[s] (+)= Σ_b dh[b·S + s]
+template <typename TH, typename TG>
+__global__ void __launch_bounds__(256) embed_pos_kernel(const TH* __restrict__ dh, TG* dP, int64_t T_, int S, int64_t d,
+                                                       int acc) {
+  const int64_t nb = T_ / S;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < int64_t(S) * d; v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t s = v / d, c = v - s * d;
+    float a = 0.f;
+    for (int64_t b = 0; b < nb; ++b) a += to_f(dh[(b * S + s) * d + c]);
+    if (acc) a += to_f(dP[v]);
+    dP[v] = from_f<TG>(a);
+  }
+}
+
+// ============================================================================== launch helpers
+
+#define XT_ROW_DISPATCH(dt, vec, ...)                         \
+  do {                                                        \
+    if ((dt) == XT_F32) {                                     \
+      using T = float;                                        \
+      if (vec) { constexpr int VW = 4; __VA_ARGS__; }         \
+      else { constexpr int VW = 1; __VA_ARGS__; }             \
+    } else {                                                  \
+      using T = bf16;                                         \
+      if (vec) { constexpr int VW = 8; __VA_ARGS__; }         \
+      else { constexpr int VW = 1; __VA_ARGS__; }             \
+    }                                                         \
+  } while (0)
+
+constexpr int kBwdMaxTpr = 512;  // backward row kernels hold two rows + partials in registers
+
+static size_t norm_ws_floats(int64_t rows, int64_t cols, int vw) {
+  RowPlan pl = plan_rows(cols, vw, kBwdMaxTpr);
+  if (!pl.ok) return 0;
+  return size_t(bwd_blocks(rows, pl.rpb)) * size_t(cols);
+}
+
+}  // namespace xt
+
+// ==================================================================================== C ABI
+using namespace xt;
+
+extern "C" {
+
+int xt_norm_bwd_workspace_size(int64_t rows, int64_t cols, size_t* bytes) {
+  XT_REQUIRE(rows >= 0 && cols > 0 && bytes, "xt_norm_bwd_workspace_size: bad arguments");
+  // the scalar path (vector width 1) has the most row groups per block: take the max
+  size_t f = norm_ws_floats(rows, cols, 1);
+  const size_t f4 = norm_ws_floats(rows, cols, 4), f8 = norm_ws_floats(rows, cols, 8);
+  if (f4 > f) f = f4;
+  if (f8 > f) f = f8;
+  *bytes = 2 * f * sizeof(float);
+  return XT_OK;
+}
+
+int xt_rms_norm_fwd(const void* x, const void* gamma, void* y, float* inv_rms, int64_t rows, int64_t cols,
+                    float eps, int dt, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_rms_norm_fwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_rms_norm_fwd: bad sizes");
+  XT_REQUIRE(rows == 0 || (x && gamma && y && inv_rms), "xt_rms_norm_fwd: NULL pointer");
+  if (rows == 0) return XT_OK;
+  const bool vec = rows_vec_ok(cols, dt, {x, gamma, y});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_fwd: row too long (%lld)", (long long)cols);
+  cudaStream_t s = as_stream(stream);
+  const int grid = row_grid(rows, pl.rpb);
+  XT_ROW_DISPATCH(dt, vec, (rms_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+                               static_cast<const T*>(x), static_cast<const T*>(gamma), static_cast<T*>(y), inv_rms,
+                               rows, cols, eps, pl.tpr)));
+  return check_launch("xt_rms_norm_fwd");
+}
+
+int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float* inv_rms, void* dx, void* dgamma,
+                    int64_t rows, int64_t cols, int dt, int dt_param, void* ws, int acc_dx, int acc_param,
+                    void* stream) {
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_param), "xt_rms_norm_bwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_rms_norm_bwd: bad sizes");
+  XT_REQUIRE(rows == 0 || (d && x && gamma && inv_rms), "xt_rms_norm_bwd: NULL input");
+  XT_REQUIRE(!dgamma || ws, "xt_rms_norm_bwd: dgamma needs a workspace");
+  cudaStream_t s = as_stream(stream);
+  if (rows == 0) {
+    if (dgamma && !acc_param)
+      if (cudaMemsetAsync(dgamma, 0, size_t(cols) * dtype_size(dt_param), s) != cudaSuccess)
+        return check_launch("xt_rms_norm_bwd");
+    return XT_OK;
+  }
+  const bool vec = rows_vec_ok(cols, dt, {d, x, gamma, dx});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1, kBwdMaxTpr);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd: row too long (%lld)", (long long)cols);
+  const int nb = bwd_blocks(rows, pl.rpb);
+  float* part = dgamma ? static_cast<float*>(ws) : nullptr;
+  const size_t smem = (32 + size_t(cols)) * sizeof(float);
+  if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd: row too long");
+  XT_ROW_DISPATCH(dt, vec, {
+    auto k = pl.threads <= 256 ? rms_bwd_kernel<T, VW, 256> : rms_bwd_kernel<T, VW, 512>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
+                                   inv_rms, static_cast<T*>(dx), part, rows, cols, pl.tpr, acc_dx);
+  });
+  XT_TRY(check_launch("xt_rms_norm_bwd"));
+  if (dgamma) return finalize(part, nb, cols, dgamma, dt_param, acc_param, s);
+  return XT_OK;
+}
+
+int xt_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean, float* rstd,
+                     int64_t rows, int64_t cols, float eps, int dt, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_layernorm_fwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_layernorm_fwd: bad sizes");
+  XT_REQUIRE(rows == 0 || (x && gamma && beta && y && mean && rstd), "xt_layernorm_fwd: NULL pointer");
+  if (rows == 0) return XT_OK;
+  const bool vec = rows_vec_ok(cols, dt, {x, gamma, beta, y});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_fwd: row too long");
+  cudaStream_t s = as_stream(stream);
+  const int grid = row_grid(rows, pl.rpb);
+  XT_ROW_DISPATCH(dt, vec, (ln_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+                               static_cast<const T*>(x), static_cast<const T*>(gamma), static_cast<const T*>(beta),
+                               static_cast<T*>(y), mean, rstd, rows, cols, eps, pl.tpr)));
+  return check_launch("xt_layernorm_fwd");
+}
+
+int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,
+                     void* dgamma, void* dbeta, int64_t rows, int64_t cols, int dt, int dt_param, void* ws,
+                     int acc_dx, int acc_param, void* stream) {
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_param), "xt_layernorm_bwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_layernorm_bwd: bad sizes");
+  XT_REQUIRE(rows == 0 || (d && x && gamma && mean && rstd), "xt_layernorm_bwd: NULL input");
+  XT_REQUIRE(!(dgamma || dbeta) || ws, "xt_layernorm_bwd: parameter grads need a workspace");
+  cudaStream_t s = as_stream(stream);
+  if (rows == 0) {
+    for (void* p : {dgamma, dbeta})
+      if (p && !acc_param && cudaMemsetAsync(p, 0, size_t(cols) * dtype_size(dt_param), s) != cudaSuccess)
+        return check_launch("xt_layernorm_bwd");
+    return XT_OK;
+  }
+  const bool vec = rows_vec_ok(cols, dt, {d, x, gamma, dx});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1, kBwdMaxTpr);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
+  const int nb = bwd_blocks(rows, pl.rpb);
+  float* part_g = dgamma ? static_cast<float*>(ws) : nullptr;
+  float* part_b = dbeta ? static_cast<float*>(ws) + size_t(nb) * size_t(cols) : nullptr;
+  const size_t smem = (32 + size_t(cols)) * sizeof(float);
+  if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
+  XT_ROW_DISPATCH(dt, vec, {
+    auto k = pl.threads <= 256 ? ln_bwd_kernel<T, VW, 256> : ln_bwd_kernel<T, VW, 512>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
+                                   mean, rstd, static_cast<T*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx);
+  });
+  XT_TRY(check_launch("xt_layernorm_bwd"));
+  if (dgamma) XT_TRY(finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s));
+  if (dbeta) XT_TRY(finalize(part_b, nb, cols, dbeta, dt_param, acc_param, s));
+  return XT_OK;
+}
+
+int xt_colsum_workspace_size(int64_t rows, int64_t cols, size_t* bytes) {
+  XT_REQUIRE(rows >= 0 && cols >= 0 && bytes, "xt_colsum_workspace_size: bad arguments");
+  *bytes = size_t(colsum_chunks(rows)) * size_t(cols) * sizeof(float);
+  return XT_OK;
+}
+
+int xt_add_bias_bwd(const void* d, void* dx, void* dbias, int64_t rows, int64_t cols, int dt, int dt_bias, void* ws,
+                    int acc_dx, int acc_dbias, void* stream) {
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_bias), "xt_add_bias_bwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_add_bias_bwd: bad sizes");
+  XT_REQUIRE(rows == 0 || d, "xt_add_bias_bwd: d is NULL");
+  XT_REQUIRE(dbias && ws, "xt_add_bias_bwd: dbias and ws are required");
+  cudaStream_t s = as_stream(stream);
+  if (rows == 0) {
+    if (!acc_dbias && cudaMemsetAsync(dbias, 0, size_t(cols) * dtype_size(dt_bias), s) != cudaSuccess)
+      return check_launch("xt_add_bias_bwd");
+    return XT_OK;
+  }
+  const int nch = colsum_chunks(rows);
+  float* part = static_cast<float*>(ws);
+  dim3 grid(unsigned(ceil_div(cols, 256) < 65535 ? ceil_div(cols, 256) : 65535), unsigned(nch));
+  if (nch > 65535) return fail(XT_ERR_UNSUPPORTED, "xt_add_bias_bwd: too many rows");
+  if (dt == XT_F32)
+    colsum_stage1<float><<<grid, 256, 0, s>>>(static_cast<const float*>(d), static_cast<float*>(dx), acc_dx, part, rows, cols);
+  else
+    colsum_stage1<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(d), static_cast<bf16*>(dx), acc_dx, part, rows, cols);
+  XT_TRY(check_launch("xt_add_bias_bwd"));
+  return finalize(part, nch, cols, dbias, dt_bias, acc_dbias, s);
+}
+
+int xt_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int causal, int64_t q_len, int dt,
+                   void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_softmax_fwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0 && causal >= 0 && causal <= 2, "xt_softmax_fwd: bad arguments");
+  XT_REQUIRE(!causal || q_len > 0, "xt_softmax_fwd: causal needs q_len > 0");
+  XT_REQUIRE(rows == 0 || (x && y), "xt_softmax_fwd: NULL pointer");
+  if (rows == 0) return XT_OK;
+  const bool vec = rows_vec_ok(cols, dt, {x, y});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_softmax_fwd: row too long");
+  cudaStream_t s = as_stream(stream);
+  const int grid = row_grid(rows, pl.rpb);
+  XT_ROW_DISPATCH(dt, vec, (softmax_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+                               static_cast<const T*>(x), static_cast<T*>(y), rows, cols, causal, q_len, pl.tpr)));
+  return check_launch("xt_softmax_fwd");
+}
+
+int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t cols, int causal, int64_t q_len,
+                   int dt, int acc, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_softmax_bwd: bad dtype");
+  XT_REQUIRE(rows >= 0 && cols > 0 && causal >= 0 && causal <= 2, "xt_softmax_bwd: bad arguments");
+  XT_REQUIRE(!causal || q_len > 0, "xt_softmax_bwd: causal needs q_len > 0");
+  XT_REQUIRE(rows == 0 || (d && y && dx), "xt_softmax_bwd: NULL pointer");
+  if (rows == 0) return XT_OK;
+  const bool vec = rows_vec_ok(cols, dt, {d, y, dx});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_softmax_bwd: row too long");
+  cudaStream_t s = as_stream(stream);
+  const int grid = row_grid(rows, pl.rpb);
+  XT_ROW_DISPATCH(dt, vec, (softmax_bwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+                               static_cast<const T*>(d), static_cast<const T*>(y), static_cast<T*>(dx), rows, cols,
+                               causal, q_len, pl.tpr, acc)));
+  return check_launch("xt_softmax_bwd");
+}
+
+int xt_cross_entropy_workspace_size(int64_t rows, size_t* bytes) {
+  XT_REQUIRE(rows >= 0 && bytes, "xt_cross_entropy_workspace_size: bad arguments");
+  *bytes = size_t(rows > 0 ? rows : 1) * sizeof(float);
+  return XT_OK;
+}
+
+int xt_cross_entropy_fwd(const void* logits, const int32_t* targets, float* lse, float* loss, int64_t rows, int64_t V,
+                         int dt, void* ws, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_cross_entropy_fwd: bad dtype");
+  XT_REQUIRE(rows > 0 && V > 0, "xt_cross_entropy_fwd: bad sizes");
+  XT_REQUIRE(logits && targets && lse && loss && ws, "xt_cross_entropy_fwd: NULL pointer");
+  cudaStream_t s = as_stream(stream);
+  const bool vec = rows_vec_ok(V, dt, {logits});
+  const int vw = vec ? (dt == XT_BF16 ? 8 : 4) : 1;
+  // streaming: threads per row sized so each thread handles ~8 vectors
+  int tpr = next_pow2(ceil_div(ceil_div(V, vw), 8));
+  if (tpr < 32) tpr = 32;
+  if (tpr > 512) tpr = 512;
+  const int threads = tpr < 256 ? 256 : tpr;
+  const int rpb = threads / tpr;
+  const int grid = row_grid(rows, rpb);
+  float* nll = static_cast<float*>(ws);
+  uint32_t* flag = errflag();
+  XT_ROW_DISPATCH(dt, vec, (ce_fwd_kernel<T, VW><<<grid, threads, 0, s>>>(static_cast<const T*>(logits), targets,
+                                                                         lse, nll, rows, V, tpr, flag)));
+  XT_TRY(check_launch("xt_cross_entropy_fwd"));
+  ce_loss_kernel<<<1, 1024, 0, s>>>(nll, rows, loss);
+  return check_launch("xt_cross_entropy_fwd loss");
+}
+
+int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float* lse, const float* upstream,
+                         void* dlogits, int64_t rows, int64_t V, int dt, int dt_grad, int acc, void* stream) {
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_grad), "xt_cross_entropy_bwd: bad dtype");
+  XT_REQUIRE(rows > 0 && V > 0, "xt_cross_entropy_bwd: bad sizes");
+  XT_REQUIRE(logits && targets && lse && upstream && dlogits, "xt_cross_entropy_bwd: NULL pointer");
+  XT_REQUIRE(!(logits == dlogits && dt != dt_grad), "xt_cross_entropy_bwd: in-place needs equal dtypes");
+  cudaStream_t s = as_stream(stream);
+  uint32_t* flag = errflag();
+  const bool vec = V % 8 == 0 && aligned16(logits) && aligned16(dlogits);
+  const int64_t work = rows * V / (vec ? 8 : 1);
+  int64_t grid = ceil_div(work, 256);
+  if (grid > int64_t(num_sms()) * 16) grid = int64_t(num_sms()) * 16;
+  const int g = int(grid < 1 ? 1 : grid);
+#define XT_CE_BWD(TI, TG)                                                                                  \
+  do {                                                                                                     \
+    if (vec) ce_bwd_kernel<TI, TG, 8><<<g, 256, 0, s>>>(static_cast<const TI*>(logits), targets, lse, upstream, \
+                                                        static_cast<TG*>(dlogits), rows, V, acc, flag);    \
+    else ce_bwd_kernel<TI, TG, 1><<<g, 256, 0, s>>>(static_cast<const TI*>(logits), targets, lse, upstream,     \
+                                                    static_cast<TG*>(dlogits), rows, V, acc, flag);        \
+  } while (0)
+  if (dt == XT_F32 && dt_grad == XT_F32) XT_CE_BWD(float, float);
+  else if (dt == XT_BF16 && dt_grad == XT_BF16) XT_CE_BWD(bf16, bf16);
+  else if (dt == XT_BF16 && dt_grad == XT_F32) XT_CE_BWD(bf16, float);
+  else XT_CE_BWD(float, bf16);
+#undef XT_CE_BWD
+  return check_launch("xt_cross_entropy_bwd");
+}
+
+int xt_rope_table(float* table, int S, int hd, double base, int pos_offset, void* stream) {
+  XT_REQUIRE(table && S > 0 && hd > 0 && hd % 2 == 0 && base > 0, "xt_rope_table: bad arguments");
+  const int n = S * (hd / 2);
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(table, S, hd, base, pos_offset);
+  return check_launch("xt_rope_table");
+}
+
+static int rope_run(bool bwd, const void* x, void* y, const float* table, int B, int S, int H, int hd, int64_t ld,
+                    int dt, int acc, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "rope: bad dtype");
+  XT_REQUIRE(B >= 0 && S > 0 && H > 0 && hd > 0 && hd % 2 == 0 && ld >= int64_t(H) * hd, "rope: bad sizes");
+  XT_REQUIRE(B == 0 || (x && y && table), "rope: NULL pointer");
+  if (B == 0) return XT_OK;
+  cudaStream_t s = as_stream(stream);
+  const int vw = dt == XT_BF16 ? 8 : 4;
+  const size_t e = dtype_size(dt);
+  const bool vec = (hd / 2) % vw == 0 && (ld * e) % 16 == 0 && aligned16(x) && aligned16(y);
+  const int64_t total = int64_t(B) * S * H * (hd / 2) / (vec ? vw : 1);
+  int64_t grid = ceil_div(total, 256);
+  if (grid > int64_t(num_sms()) * 16) grid = int64_t(num_sms()) * 16;
+  XT_ROW_DISPATCH(dt, vec, {
+    if (bwd)
+      rope_kernel<T, true, VW><<<int(grid), 256, 0, s>>>(static_cast<const T*>(x), static_cast<T*>(y), table, B, S, H,
+                                                         hd, ld, acc);
+    else
+      rope_kernel<T, false, VW><<<int(grid), 256, 0, s>>>(static_cast<const T*>(x), static_cast<T*>(y), table, B, S,
+                                                          H, hd, ld, acc);
+  });
+  return check_launch("rope");
+}
+
+int xt_rope_fwd(const void* x, void* y, const float* table, int B, int S, int H, int hd, int64_t ld, int dt,
+                void* stream) {
+  return rope_run(false, x, y, table, B, S, H, hd, ld, dt, 0, stream);
+}
+
+int xt_rope_bwd(const void* d, void* dx, const float* table, int B, int S, int H, int hd, int64_t ld, int dt, int acc,
+                void* stream) {
+  XT_REQUIRE(!(acc && d == dx), "xt_rope_bwd: accumulate cannot be in place");
+  return rope_run(true, d, dx, table, B, S, H, hd, ld, dt, acc, stream);
+}
+
+int xt_embedding_workspace_size(int64_t T, size_t* bytes) {
+  XT_REQUIRE(T >= 0 && bytes, "xt_embedding_workspace_size: bad arguments");
+  *bytes = size_t(T > 0 ? T : 1) * sizeof(uint64_t);
+  return XT_OK;
+}
+
+int xt_embedding_fwd(const int32_t* ids, const void* E, const void* P, void* h, int64_t T_, int S, int64_t d,
+                     int64_t V, int dt, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_embedding_fwd: bad dtype");
+  XT_REQUIRE(T_ >= 0 && d > 0 && V > 0 && (!P || S > 0), "xt_embedding_fwd: bad sizes");
+  XT_REQUIRE(T_ == 0 || (ids && E && h), "xt_embedding_fwd: NULL pointer");
+  if (T_ == 0) return XT_OK;
+  cudaStream_t s = as_stream(stream);
+  const bool vec = rows_vec_ok(d, dt, {E, P, h});
+  const int64_t work = T_ * d / (vec ? (dt == XT_BF16 ? 8 : 4) : 1);
+  int64_t grid = ceil_div(work, 256);
+  if (grid > int64_t(num_sms()) * 16) grid = int64_t(num_sms()) * 16;
+  uint32_t* flag = errflag();
+  XT_ROW_DISPATCH(dt, vec, (embed_fwd_kernel<T, VW><<<int(grid), 256, 0, s>>>(
+                               ids, static_cast<const T*>(E), static_cast<const T*>(P), static_cast<T*>(h), T_, S, d,
+                               V, flag)));
+  return check_launch("xt_embedding_fwd");
+}
+
+int xt_embedding_bwd(const int32_t* ids, const void* dh, void* dE, void* dP, int64_t T, int S, int64_t d, int64_t V,
+                     int dt_dh, int dt_grad, void* ws, int acc, void* stream) {
+  XT_REQUIRE(valid_dtype(dt_dh) && valid_dtype(dt_grad), "xt_embedding_bwd: bad dtype");
+  XT_REQUIRE(T >= 0 && d > 0 && V > 0 && (!dP || (S > 0 && T % S == 0)), "xt_embedding_bwd: bad sizes");
+  XT_REQUIRE(T <= kSortMax, "xt_embedding_bwd: T > %d is not supported", kSortMax);
+  XT_REQUIRE(dE && (T == 0 || (ids && dh && ws)), "xt_embedding_bwd: NULL pointer");
+  XT_REQUIRE(V < (int64_t(1) << 31), "xt_embedding_bwd: V too large");
+  cudaStream_t s = as_stream(stream);
+  if (!acc) {
+    if (cudaMemsetAsync(dE, 0, size_t(V) * size_t(d) * dtype_size(dt_grad), s) != cudaSuccess)
+      return check_launch("xt_embedding_bwd zero");
+  }
+  if (T == 0) return XT_OK;
+  uint64_t* sorted = static_cast<uint64_t*>(ws);
+  int n = 1;
+  while (n < T) n <<= 1;
+  const size_t smem = size_t(n) * sizeof(uint64_t);
+  cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  embed_sort_kernel<<<1, 1024, smem, s>>>(ids, T, V, sorted, errflag());
+  XT_TRY(check_launch("xt_embedding_bwd sort"));
+#define XT_EMB(TH, TG)                                                                                      \
+  do {                                                                                                      \
+    embed_scatter_kernel<TH, TG><<<unsigned(T), 256, 0, s>>>(sorted, static_cast<const TH*>(dh),            \
+                                                             static_cast<TG*>(dE), T, d, V);                \
+    if (dP) {                                                                                               \
+      int64_t gp = ceil_div(int64_t(S) * d, 256);                                                           \
+      embed_pos_kernel<TH, TG><<<unsigned(gp), 256, 0, s>>>(static_cast<const TH*>(dh), static_cast<TG*>(dP), \
+                                                            T, S, d, acc);                                  \
+    }                                                                                                       \
+  } while (0)
+  if (dt_dh == XT_F32 && dt_grad == XT_F32) XT_EMB(float, float);
+  else if (dt_dh == XT_BF16 && dt_grad == XT_BF16) XT_EMB(bf16, bf16);
+  else if (dt_dh == XT_BF16 && dt_grad == XT_F32) XT_EMB(bf16, float);
+  else XT_EMB(float, bf16);
+#undef XT_EMB
+  return check_launch("xt_embedding_bwd");
+}
+
+}  // extern "C"

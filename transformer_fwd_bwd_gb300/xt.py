@@ -1,0 +1,403 @@
+"""ctypes binding of libxt (include/xt.h): the same entry points, taking torch tensors.
+
+Argument marshalling only — every computation runs in libxt's CUDA kernels.  Tensors must
+be CUDA tensors; sizes are taken from them where the C call needs them.  A non-zero status
+raises XtError with libxt's message.  There is no fallback: without libxt.so importing the
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libxt.so")
+
+XT_OK, XT_ERR_INVALID_ARG, XT_ERR_UNSUPPORTED, XT_ERR_ALIGNMENT, XT_ERR_CUDA, XT_ERR_TIMEOUT = range(6)
+XT_F32, XT_BF16 = 0, 1
+XT_DEVERR_INDEX, XT_DEVERR_TIMEOUT = 1, 2
+XT_NORM_RMS, XT_NORM_LN = 0, 1
+XT_MLP_SWIGLU, XT_MLP_GELU = 0, 1
+
+
+class XtError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"libxt status {code}: {msg}")
+        self.code = code
+
+
+class MatmulDesc(C.Structure):
+    _fields_ = [("M", C.c_int32), ("N", C.c_int32), ("K", C.c_int32),
+                ("trans_a", C.c_int32), ("trans_b", C.c_int32),
+                ("batch_outer", C.c_int32), ("batch_inner", C.c_int32),
+                ("dtype_ab", C.c_int32), ("dtype_c", C.c_int32),
+                ("accumulate", C.c_int32), ("causal", C.c_int32), ("alpha", C.c_float),
+                ("lda", C.c_int64), ("ldb", C.c_int64), ("ldc", C.c_int64),
+                ("stride_a_outer", C.c_int64), ("stride_a_inner", C.c_int64),
+                ("stride_b_outer", C.c_int64), ("stride_b_inner", C.c_int64),
+                ("stride_c_outer", C.c_int64), ("stride_c_inner", C.c_int64)]
+
+
+class BlockConfig(C.Structure):
+    _fields_ = [("B", C.c_int32), ("S", C.c_int32), ("d", C.c_int32), ("H", C.c_int32),
+                ("hd", C.c_int32), ("F", C.c_int32), ("V", C.c_int32), ("n_layers", C.c_int32),
+                ("norm", C.c_int32), ("mlp", C.c_int32), ("rope", C.c_int32),
+                ("learned_pos", C.c_int32), ("causal", C.c_int32), ("training", C.c_int32),
+                ("dtype", C.c_int32), ("grad_dtype", C.c_int32), ("eps", C.c_float),
+                ("p", C.c_float), ("rope_base", C.c_double), ("base_seed", C.c_uint64)]
+
+
+_VP = C.c_void_p
+_PP = C.POINTER(C.c_void_p)
+
+
+class BlockParams(C.Structure):
+    _fields_ = [("E", _VP), ("P", _VP), ("g1", _PP), ("b1", _PP), ("Wqkv", _PP), ("Wo", _PP),
+                ("g2", _PP), ("b2", _PP), ("W_up", _PP), ("W_down", _PP), ("gf", _VP), ("bf", _VP),
+                ("dE", _VP), ("dP", _VP), ("dg1", _PP), ("db1", _PP), ("dWqkv", _PP), ("dWo", _PP),
+                ("dg2", _PP), ("db2", _PP), ("dW_up", _PP), ("dW_down", _PP), ("dgf", _VP), ("dbf", _VP)]
+
+
+_I, _I64, _F, _D, _U64, _SZP = C.c_int, C.c_int64, C.c_float, C.c_double, C.c_uint64, C.POINTER(C.c_size_t)
+
+# name → argtypes (restype is int for all but the two string getters)
+_SIGS = {
+    "xt_get_device_errors": [C.POINTER(C.c_uint32), _VP],
+    "xt_clear_device_errors": [_VP],
+    "xt_accumulate": [_VP, _I, _VP, _I, _I64, _VP],
+    "xt_add_fwd": [_VP, _VP, _VP, _I64, _I, _VP],
+    "xt_add_bwd": [_VP, _VP, _VP, _I64, _I, _I, _I, _VP],
+    "xt_mul_fwd": [_VP, _VP, _VP, _I64, _I, _VP],
+    "xt_mul_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I, _I, _I, _VP],
+    "xt_scale_fwd": [_VP, _VP, _I64, _F, _I, _VP],
+    "xt_scale_bwd": [_VP, _VP, _I64, _F, _I, _I, _VP],
+    "xt_sum_workspace_size": [_I64, _SZP],
+    "xt_sum_fwd": [_VP, _I64, _I, _VP, _VP, _VP],
+    "xt_sum_bwd": [_VP, _VP, _I64, _I, _I, _VP],
+    "xt_colsum_workspace_size": [_I64, _I64, _SZP],
+    "xt_add_bias_fwd": [_VP, _VP, _VP, _I64, _I64, _I, _VP],
+    "xt_add_bias_bwd": [_VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _I, _I, _VP],
+    "xt_silu_fwd": [_VP, _VP, _I64, _I, _VP],
+    "xt_silu_bwd": [_VP, _VP, _VP, _I64, _I, _I, _VP],
+    "xt_swiglu_fwd": [_VP, _VP, _I64, _VP, _I64, _I64, _I64, _I, _VP],
+    "xt_swiglu_bwd": [_VP, _I64, _VP, _VP, _I64, _VP, _VP, _I64, _I64, _I64, _I, _I, _VP],
+    "xt_gelu_fwd": [_VP, _VP, _I64, _I, _VP],
+    "xt_gelu_bwd": [_VP, _VP, _VP, _I64, _I, _I, _VP],
+    "xt_norm_bwd_workspace_size": [_I64, _I64, _SZP],
+    "xt_rms_norm_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _F, _I, _VP],
+    "xt_rms_norm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _I, _I, _VP],
+    "xt_layernorm_fwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _F, _I, _VP],
+    "xt_layernorm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _I, _I, _VP],
+    "xt_rope_table": [_VP, _I, _I, _D, _I, _VP],
+    "xt_rope_fwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _VP],
+    "xt_rope_bwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _I, _VP],
+    "xt_softmax_fwd": [_VP, _VP, _I64, _I64, _I, _I64, _I, _VP],
+    "xt_softmax_bwd": [_VP, _VP, _VP, _I64, _I64, _I, _I64, _I, _I, _VP],
+    "xt_cross_entropy_workspace_size": [_I64, _SZP],
+    "xt_cross_entropy_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _I, _VP, _VP],
+    "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
+    "xt_dropout_fwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _VP],
+    "xt_dropout_bwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _I, _VP],
+    "xt_dropout_mask": [_VP, _I64, _F, _U64, _VP],
+    "xt_dropout_add_fwd": [_VP, _VP, _VP, _I64, _F, _U64, _I, _I, _VP],
+    "xt_embedding_workspace_size": [_I64, _SZP],
+    "xt_embedding_fwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _VP],
+    "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
+    "xt_matmul_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP],
+    "xt_matmul_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP],
+}
+
+_lib = None
+
+
+def lib():
+    """Loads libxt.so (built in-tree by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build() first")
+        L = C.CDLL(LIB_PATH)
+        L.xt_last_error.restype = C.c_char_p
+        L.xt_last_error.argtypes = []
+        L.xt_version.restype = C.c_char_p
+        L.xt_version.argtypes = []
+        for name, args in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return ["xt_last_error", "xt_version", *_SIGS.keys()]
+
+
+def _check(code):
+    if code != XT_OK:
+        raise XtError(code, lib().xt_last_error().decode(errors="replace"))
+
+
+def call(name, *args):
+    """Calls a libxt entry point with already-marshalled arguments; raises on failure."""
+    _check(getattr(lib(), name)(*args))
+
+
+# ------------------------------------------------------------------------------ marshalling
+
+def dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return XT_F32
+    if t.dtype == torch.bfloat16:
+        return XT_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("libxt takes CUDA tensors")
+    return t.data_ptr()
+
+
+def stream(s=None):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    return s.cuda_stream if hasattr(s, "cuda_stream") else s
+
+
+def ws_bytes(name, *args) -> int:
+    out = C.c_size_t(0)
+    call(name, *args, C.byref(out))
+    return int(out.value)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def device_errors(s=None) -> int:
+    out = C.c_uint32(0)
+    code = lib().xt_get_device_errors(C.byref(out), stream(s))
+    if code not in (XT_OK, XT_ERR_TIMEOUT):
+        _check(code)
+    return int(out.value)
+
+
+def clear_device_errors(s=None):
+    call("xt_clear_device_errors", stream(s))
+
+
+def version() -> str:
+    return lib().xt_version().decode()
+
+
+# ------------------------------------------------------------------------------ op wrappers
+# Same names as the C entry points; tensors in, results written into caller tensors.
+
+def xt_accumulate(dst, src, s=None):
+    call("xt_accumulate", ptr(dst), dt(dst), ptr(src), dt(src), src.numel(), stream(s))
+
+
+def xt_add_fwd(a, b, y, s=None):
+    call("xt_add_fwd", ptr(a), ptr(b), ptr(y), a.numel(), dt(a), stream(s))
+
+
+def xt_add_bwd(d, da, db, acc_a=0, acc_b=0, s=None):
+    call("xt_add_bwd", ptr(d), ptr(da), ptr(db), d.numel(), dt(d), acc_a, acc_b, stream(s))
+
+
+def xt_mul_fwd(a, b, y, s=None):
+    call("xt_mul_fwd", ptr(a), ptr(b), ptr(y), a.numel(), dt(a), stream(s))
+
+
+def xt_mul_bwd(d, a, b, da, db, acc_a=0, acc_b=0, s=None):
+    call("xt_mul_bwd", ptr(d), ptr(a), ptr(b), ptr(da), ptr(db), d.numel(), dt(d), acc_a, acc_b, stream(s))
+
+
+def xt_scale_fwd(x, y, alpha, s=None):
+    call("xt_scale_fwd", ptr(x), ptr(y), x.numel(), float(alpha), dt(x), stream(s))
+
+
+def xt_scale_bwd(d, dx, alpha, acc=0, s=None):
+    call("xt_scale_bwd", ptr(d), ptr(dx), d.numel(), float(alpha), dt(d), acc, stream(s))
+
+
+def xt_sum_fwd(x, out, ws=None, s=None):
+    if ws is None:
+        ws = workspace(ws_bytes("xt_sum_workspace_size", x.numel()), x.device)
+    call("xt_sum_fwd", ptr(x), x.numel(), dt(x), ptr(out), ptr(ws), stream(s))
+
+
+def xt_sum_bwd(upstream, dx, acc=0, s=None):
+    call("xt_sum_bwd", ptr(upstream), ptr(dx), dx.numel(), dt(dx), acc, stream(s))
+
+
+def xt_add_bias_fwd(x, bias, y, s=None):
+    rows, cols = x.shape
+    call("xt_add_bias_fwd", ptr(x), ptr(bias), ptr(y), rows, cols, dt(x), stream(s))
+
+
+def xt_add_bias_bwd(d, dx, dbias, acc_dx=0, acc_dbias=0, ws=None, s=None):
+    rows, cols = d.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_colsum_workspace_size", rows, cols), d.device)
+    call("xt_add_bias_bwd", ptr(d), ptr(dx), ptr(dbias), rows, cols, dt(d), dt(dbias), ptr(ws), acc_dx,
+         acc_dbias, stream(s))
+
+
+def xt_silu_fwd(x, y, s=None):
+    call("xt_silu_fwd", ptr(x), ptr(y), x.numel(), dt(x), stream(s))
+
+
+def xt_silu_bwd(d, x, dx, acc=0, s=None):
+    call("xt_silu_bwd", ptr(d), ptr(x), ptr(dx), d.numel(), dt(d), acc, stream(s))
+
+
+def xt_gelu_fwd(x, y, s=None):
+    call("xt_gelu_fwd", ptr(x), ptr(y), x.numel(), dt(x), stream(s))
+
+
+def xt_gelu_bwd(d, x, dx, acc=0, s=None):
+    call("xt_gelu_bwd", ptr(d), ptr(x), ptr(dx), d.numel(), dt(d), acc, stream(s))
+
+
+def xt_swiglu_fwd(g, u, y, s=None):
+    rows, cols = g.shape
+    call("xt_swiglu_fwd", ptr(g), ptr(u), g.stride(0), ptr(y), y.stride(0), rows, cols, dt(g), stream(s))
+
+
+def xt_swiglu_bwd(d, g, u, dg, du, acc=0, s=None):
+    rows, cols = g.shape
+    assert u.stride(0) == g.stride(0) and du.stride(0) == dg.stride(0)
+    call("xt_swiglu_bwd", ptr(d), d.stride(0), ptr(g), ptr(u), g.stride(0), ptr(dg), ptr(du), dg.stride(0), rows,
+         cols, dt(g), acc, stream(s))
+
+
+def xt_rms_norm_fwd(x, gamma, y, inv_rms, eps, s=None):
+    rows, cols = x.shape
+    call("xt_rms_norm_fwd", ptr(x), ptr(gamma), ptr(y), ptr(inv_rms), rows, cols, float(eps), dt(x), stream(s))
+
+
+def xt_rms_norm_bwd(d, x, gamma, inv_rms, dx, dgamma, acc_dx=0, acc_param=0, ws=None, s=None):
+    rows, cols = x.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_norm_bwd_workspace_size", rows, cols), x.device)
+    call("xt_rms_norm_bwd", ptr(d), ptr(x), ptr(gamma), ptr(inv_rms), ptr(dx), ptr(dgamma), rows, cols, dt(x),
+         dt(dgamma) if dgamma is not None else dt(x), ptr(ws), acc_dx, acc_param, stream(s))
+
+
+def xt_layernorm_fwd(x, gamma, beta, y, mean, rstd, eps, s=None):
+    rows, cols = x.shape
+    call("xt_layernorm_fwd", ptr(x), ptr(gamma), ptr(beta), ptr(y), ptr(mean), ptr(rstd), rows, cols, float(eps),
+         dt(x), stream(s))
+
+
+def xt_layernorm_bwd(d, x, gamma, mean, rstd, dx, dgamma, dbeta, acc_dx=0, acc_param=0, ws=None, s=None):
+    rows, cols = x.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_norm_bwd_workspace_size", rows, cols), x.device)
+    pdt = dt(dgamma) if dgamma is not None else (dt(dbeta) if dbeta is not None else dt(x))
+    call("xt_layernorm_bwd", ptr(d), ptr(x), ptr(gamma), ptr(mean), ptr(rstd), ptr(dx), ptr(dgamma), ptr(dbeta),
+         rows, cols, dt(x), pdt, ptr(ws), acc_dx, acc_param, stream(s))
+
+
+def xt_rope_table(table, S, hd, base, pos_offset=0, s=None):
+    call("xt_rope_table", ptr(table), S, hd, float(base), pos_offset, stream(s))
+
+
+def xt_rope_fwd(x, y, table, B, S, H, hd, ld, s=None):
+    call("xt_rope_fwd", ptr(x), ptr(y), ptr(table), B, S, H, hd, ld, dt(x), stream(s))
+
+
+def xt_rope_bwd(d, dx, table, B, S, H, hd, ld, acc=0, s=None):
+    call("xt_rope_bwd", ptr(d), ptr(dx), ptr(table), B, S, H, hd, ld, dt(d), acc, stream(s))
+
+
+def xt_softmax_fwd(x, y, causal=0, q_len=0, s=None):
+    cols = x.shape[-1]
+    rows = x.numel() // cols
+    call("xt_softmax_fwd", ptr(x), ptr(y), rows, cols, causal, q_len, dt(x), stream(s))
+
+
+def xt_softmax_bwd(d, y, dx, causal=0, q_len=0, acc=0, s=None):
+    cols = y.shape[-1]
+    rows = y.numel() // cols
+    call("xt_softmax_bwd", ptr(d), ptr(y), ptr(dx), rows, cols, causal, q_len, dt(y), acc, stream(s))
+
+
+def xt_cross_entropy_fwd(logits, targets, lse, loss, ws=None, s=None):
+    rows, V = logits.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_cross_entropy_workspace_size", rows), logits.device)
+    call("xt_cross_entropy_fwd", ptr(logits), ptr(targets), ptr(lse), ptr(loss), rows, V, dt(logits), ptr(ws),
+         stream(s))
+
+
+def xt_cross_entropy_bwd(logits, targets, lse, upstream, dlogits, acc=0, s=None):
+    rows, V = logits.shape
+    call("xt_cross_entropy_bwd", ptr(logits), ptr(targets), ptr(lse), ptr(upstream), ptr(dlogits), rows, V,
+         dt(logits), dt(dlogits), acc, stream(s))
+
+
+def xt_dropout_fwd(x, y, p, seed, training=1, s=None):
+    call("xt_dropout_fwd", ptr(x), ptr(y), x.numel(), float(p), int(seed) & (2**64 - 1), int(training), dt(x),
+         stream(s))
+
+
+def xt_dropout_bwd(d, dx, p, seed, training=1, acc=0, s=None):
+    call("xt_dropout_bwd", ptr(d), ptr(dx), d.numel(), float(p), int(seed) & (2**64 - 1), int(training), dt(d),
+         acc, stream(s))
+
+
+def xt_dropout_mask(mask, p, seed, s=None):
+    call("xt_dropout_mask", ptr(mask), mask.numel(), float(p), int(seed) & (2**64 - 1), stream(s))
+
+
+def xt_dropout_add_fwd(h, a, out, p, seed, training=1, s=None):
+    call("xt_dropout_add_fwd", ptr(h), ptr(a), ptr(out), h.numel(), float(p), int(seed) & (2**64 - 1),
+         int(training), dt(h), stream(s))
+
+
+def xt_embedding_fwd(ids, E, P, h, S, s=None):
+    V, d = E.shape
+    call("xt_embedding_fwd", ptr(ids), ptr(E), ptr(P), ptr(h), ids.numel(), S, d, V, dt(E), stream(s))
+
+
+def xt_embedding_bwd(ids, dh, dE, dP, S, acc=0, ws=None, s=None):
+    V, d = dE.shape
+    T = ids.numel()
+    if ws is None:
+        ws = workspace(ws_bytes("xt_embedding_workspace_size", T), dh.device)
+    call("xt_embedding_bwd", ptr(ids), ptr(dh), ptr(dE), ptr(dP), T, S, d, V, dt(dh), dt(dE), ptr(ws), acc,
+         stream(s))
+
+
+def matmul_desc(M, N, K, *, trans_a=0, trans_b=0, lda=None, ldb=None, ldc=None, batch_outer=1, batch_inner=1,
+                dtype_ab=XT_BF16, dtype_c=XT_F32, accumulate=0, causal=0, alpha=1.0, strides=(0, 0, 0, 0, 0, 0)):
+    d = MatmulDesc()
+    d.M, d.N, d.K = M, N, K
+    d.trans_a, d.trans_b = trans_a, trans_b
+    d.lda = lda if lda is not None else (M if trans_a else K)
+    d.ldb = ldb if ldb is not None else (K if trans_b else N)
+    d.ldc = ldc if ldc is not None else N
+    d.batch_outer, d.batch_inner = batch_outer, batch_inner
+    d.dtype_ab, d.dtype_c = dtype_ab, dtype_c
+    d.accumulate, d.causal, d.alpha = accumulate, causal, alpha
+    (d.stride_a_outer, d.stride_a_inner, d.stride_b_outer, d.stride_b_inner,
+     d.stride_c_outer, d.stride_c_inner) = strides
+    return d
+
+
+def xt_matmul_fwd(desc, A, B, Cm, s=None):
+    call("xt_matmul_fwd", C.byref(desc), ptr(A), ptr(B), ptr(Cm), stream(s))
+
+
+def xt_matmul_bwd(desc, A, B, dC, dA, dB, acc_a=0, acc_b=0, s=None):
+    call("xt_matmul_bwd", C.byref(desc), ptr(A), ptr(B), ptr(dC), ptr(dA), ptr(dB),
+         dt(dA) if dA is not None else XT_F32, dt(dB) if dB is not None else XT_F32, acc_a, acc_b, stream(s))
