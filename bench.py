@@ -1,0 +1,351 @@
+#!/usr/bin/env python
+"""Benchmark of the block-stack hot path on GB300: forward + backward tokens/s.
+
+One step = zero the gradient buffers, xt_block_fwd, xt_block_bwd on one batch of synthetic
+tokens (every op of the stack: embedding, norms, QKV / attention / projection / MLP GEMMs,
+RoPE when configured, causal softmax, dropout-residual adds, tied logits, cross-entropy and
+all backward kernels).  Default workload: the 12-layer GPT-style stack (B 8, S 1024, d 768,
+12 heads × 64, LayerNorm, exact-GELU MLP 3072, learned positions, tied 50304-vocab output,
+bf16 storage with fp32 accumulation, fp32 parameter gradients).
+
+Prints one JSON line.  --impl reference times the CPU oracle (float64 NumPy) on a bounded
+sample of the same workload instead.  Under torchrun each rank runs its own replica on its
+own GPU and its own batch (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block fwd+bwd tokens/s on 1 GB300; per-kernel HBM GB/s and GEMM TFLOP/s vs peak"
+
+WORKLOAD_TEXT = {
+    "gpt12": "12-layer pre-norm GPT stack: B8 S1024 d768 H12x64, LayerNorm, exact-GELU MLP 3072, learned "
+             "positions, tied 50304-vocab logits + mean CE, causal composed attention, bf16 storage, fp32 "
+             "accumulate / statistics / parameter grads",
+    "block256": "1 pre-norm block: B4 S256 d256 H4x64, RMSNorm, RoPE, SwiGLU 688, tied 4096-vocab logits + mean CE, "
+                "causal composed attention, residual dropout p=0.1, fp32 storage, tf32 tensor-core GEMMs",
+    "tiny": "1 pre-norm block: B1 S16 d32 H2x16, RMSNorm, RoPE, SwiGLU 64, tied 64-vocab logits, fp32",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample-seqs", type=int, default=1, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample(workload: str, seqs: int, reps: int = 1):
+    """Times the oracle's forward + backward on `seqs` sequences of the workload (float64
+    NumPy, all host cores).  Returns (tokens/s, seconds per rep, tokens)."""
+    import synth
+    from oracle import block as OB
+    cfg = dict(synth.BLOCK_CONFIGS[workload])
+    params = synth.block_params(cfg)
+    ids, tgt = synth.block_tokens(cfg)
+    seqs = min(seqs, cfg["B"])
+    sub = dict(cfg, B=seqs)
+    n = seqs * cfg["S"]
+    times = []
+    for r in range(reps):
+        t0 = time.perf_counter()
+        OB.forward_backward(sub, params, ids[:n], tgt[:n], synth.BASE_SEED_DROPOUT + r, training=True)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return n / t, t, n
+
+
+def cpu_baseline(workload: str, seqs: int):
+    """Runs the oracle sample in a fresh process (no CUDA state shared) and parses its line."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
+           "--sample-seqs", str(seqs)]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"failed: {r.stderr.strip()[-200:]}"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "of measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "of fallback"
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r, t, n = oracle_sample(args.workload, args.sample_seqs)
+        if i >= args.warmup:
+            rates.append((r, t))
+    secs = [t for _, t in rates]
+    import synth
+    cfg = synth.BLOCK_CONFIGS[args.workload]
+    n = min(args.sample_seqs, cfg["B"]) * cfg["S"]
+    value = n / statistics.mean(secs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": cfg["B"], "seq_len": cfg["S"],
+                   "parallelism": "cpu"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{n} tokens ({min(args.sample_seqs, cfg['B'])} of {cfg['B']} sequences), "
+                                   f"all {cfg['n_layers']} layers, float64 NumPy, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ our arm
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import synth
+    from transformer_fwd_bwd_gb300 import xt
+    from transformer_fwd_bwd_gb300.block import NativeBlock
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = dict(synth.BLOCK_CONFIGS[args.workload])
+    T = cfg["B"] * cfg["S"]
+    nb = NativeBlock(cfg, device=dev, training=True, base_seed=synth.BASE_SEED_DROPOUT)
+    nb.load(synth.block_params(cfg))
+    ids_h, tgt_h = synth.block_tokens(cfg, seed=synth.SEED_TOKENS + rank)
+    ids = torch.tensor(ids_h, device=dev)
+    tgt = torch.tensor(tgt_h, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        nb.zero_grads(stream)
+        nb.forward(ids, tgt, stream)
+        nb.backward(ids, tgt, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert xt.device_errors() == 0, "device error flag set during warm-up"
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---------------- timed region (device-resident inputs) ----------------
+    per_step_gemms = 400 * cfg["n_layers"] // 12 + 64
+    xt.profile_gemm(per_step_gemms * args.steps + 64)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = xt.launch_count()
+    with ClockSampler(local_rank) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = xt.launch_count() - launches0
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    flops, gms = xt.profile_gemm_read()
+    xt.profile_gemm(0)
+    assert xt.device_errors() == 0, "device error flag set during the timed region"
+    loss = float(nb.loss.item())
+
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * T / (ms_max / 1000.0)
+
+    # ---------------- end to end: host buffers, copies inside the timed region ----------------
+    ids_pin = torch.tensor(ids_h).pin_memory()
+    tgt_pin = torch.tensor(tgt_h).pin_memory()
+    loss_pin = torch.empty(1, dtype=torch.float32).pin_memory()
+    ids_d = torch.empty_like(ids)
+    tgt_d = torch.empty_like(tgt)
+    e2e_steps = max(3, args.steps // 2)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        ids_d.copy_(ids_pin, non_blocking=True)
+        tgt_d.copy_(tgt_pin, non_blocking=True)
+        nb.zero_grads(stream)
+        nb.forward(ids_d, tgt_d, stream)
+        nb.backward(ids_d, tgt_d, stream)
+        loss_pin.copy_(nb.loss, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        _ = float(loss_pin[0])
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        return
+    peaks, peak_src = measured_peaks()
+    gemm_ms_step = float(np.sum(gms)) / args.steps
+    tflops = float(np.sum(flops)) / (float(np.sum(gms)) * 1e-3) / 1e12 if len(gms) else None
+    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    if cfg["dtype"] == "f32":
+        peak = peak * 1.1 / 2.25   # tf32 dense: the bf16 measurement × the nominal tf32/bf16 ratio
+    roofline = {
+        "kernel": "gemm_kernel (tcgen05.mma + TMA, all GEMM launches of the step)",
+        "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+        "frac": (tflops / peak) if tflops else None, "peak_source": f"{peak_src} "
+        f"({'bf16 sustained' if cfg['dtype'] == 'bf16' else 'bf16 sustained x 1.1/2.25 for tf32'})",
+        "traffic": None, "launches_per_step": len(gms) / args.steps,
+        "share_of_step": gemm_ms_step / ms, "gemm_tflop_per_step": float(np.sum(flops)) / args.steps / 1e12,
+    }
+    cpu = cpu_baseline(args.workload, args.sample_seqs) if world == 1 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic (seeded tokens, N(0,0.02) weights)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "model": args.workload, "global_batch": world * cfg["B"],
+                   "seq_len": cfg["S"], "parallelism": f"replicas x{world} (data parallel, no collective)",
+                   "l2": "inputs larger than L2 (weights 85M params + GBs of saved activations per step)",
+                   "loss": loss},
+        "e2e": {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(2 * T * 4),
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.oracle_sample:
+        r, t, n = oracle_sample(args.workload, args.sample_seqs)
+        print(json.dumps({"value": r, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                          "cpu": cpu_model(),
+                          "sample": f"{n} tokens ({args.sample_seqs} sequence(s)) of the same workload, all layers, "
+                                    f"float64 NumPy forward + backward, {t:.2f} s"}))
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        else:
+            dist.init_process_group("gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -70,6 +70,18 @@ const char* xt_version(void);
 int xt_get_device_errors(uint32_t* out, void* stream);
 int xt_clear_device_errors(void* stream);
 
+/* Number of CUDA kernels libxt has launched in this process (host-side counter). */
+uint64_t xt_launch_count(void);
+
+/* GEMM timing for measurement: with capacity > 0, the next `capacity` GEMM launches are
+ * bracketed by CUDA events recorded on their own stream, each tagged with its algorithmic
+ * FLOPs (2·M·N·K per batch; for the causal modes only the unmasked half).  Events are
+ * created by this call, not during the launches; capacity 0 disables.  xt_profile_gemm_read
+ * waits for the recorded events and copies up to max_records (flops, milliseconds) pairs
+ * into host arrays; *n receives the number recorded. */
+int xt_profile_gemm(int capacity);
+int xt_profile_gemm_read(double* flops, float* ms, int max_records, int* n);
+
 /* ---------------------------------------------------------------------------------
  * Gradient accumulation ([AE] § 梯度累加, push_grad/accumulate): dst[i] += src[i].
  * dst and src may have different dtypes (e.g. bf16 src into an f32 dst).
@@ -130,25 +142,27 @@ int xt_gelu_bwd(const void* d, const void* x, void* dx, int64_t n, int dt, int a
 /* ---------------------------------------------------------------------------------
  * RMSNorm ([AE] § RMSNorm): ir = 1/√(mean_c x² + eps), y = x·ir·γ, inv_rms[r] = ir saved.
  * Backward, g = d∘γ: dx = ir·g − x·ir³/n·Σ_c g·x; dγ[c] = Σ_r d·x·ir.
- * gamma has dtype dt; dgamma has dtype dt_param.  dx or dgamma may be NULL.
+ * d, x, gamma have dtype dt; dx has dtype dt_dx (dt, or XT_F32 with bf16 inputs: a float32
+ * residual-gradient buffer); dgamma has dtype dt_param.  dx or dgamma may be NULL.
  * ------------------------------------------------------------------------------- */
 int xt_norm_bwd_workspace_size(int64_t rows, int64_t cols, size_t* bytes);
 int xt_rms_norm_fwd(const void* x, const void* gamma, void* y, float* inv_rms, int64_t rows,
                     int64_t cols, float eps, int dt, void* stream);
 int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float* inv_rms,
-                    void* dx, void* dgamma, int64_t rows, int64_t cols, int dt, int dt_param,
-                    void* ws, int acc_dx, int acc_param, void* stream);
+                    void* dx, void* dgamma, int64_t rows, int64_t cols, int dt, int dt_dx,
+                    int dt_param, void* ws, int acc_dx, int acc_param, void* stream);
 
 /* LayerNorm (standard definition; [BP] § kernel-pair table k_layernorm_fwd/bwd and
  * § Sparade tensorer: mean and variance saved — saved here as mean and rstd):
  * μ = mean x, var = mean (x−μ)², rstd = 1/√(var+eps), x̂ = (x−μ)·rstd, y = x̂·γ + β.
- * Backward, g = d∘γ: dx = rstd·(g − mean g − x̂·mean(g∘x̂)); dγ = Σ_r d∘x̂; dβ = Σ_r d. */
+ * Backward, g = d∘γ: dx = rstd·(g − mean g − x̂·mean(g∘x̂)); dγ = Σ_r d∘x̂; dβ = Σ_r d.
+ * Dtypes as for xt_rms_norm_bwd. */
 int xt_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
                      float* rstd, int64_t rows, int64_t cols, float eps, int dt, void* stream);
 int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const float* mean,
                      const float* rstd, void* dx, void* dgamma, void* dbeta, int64_t rows,
-                     int64_t cols, int dt, int dt_param, void* ws, int acc_dx, int acc_param,
-                     void* stream);
+                     int64_t cols, int dt, int dt_dx, int dt_param, void* ws, int acc_dx,
+                     int acc_param, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * RoPE ([AE] op table row rope and § RoPE 反向推导): for each pair (i, i+h), h = hd/2,
@@ -203,6 +217,9 @@ int xt_dropout_fwd(const void* x, void* y, int64_t n, float p, uint64_t seed, in
                    int dt, void* stream);
 int xt_dropout_bwd(const void* d, void* dx, int64_t n, float p, uint64_t seed, int training,
                    int dt, int acc, void* stream);
+/* Same, with d of dtype dt_d (e.g. a float32 residual gradient) and dx of dtype dt_dx. */
+int xt_dropout_bwd_ex(const void* d, int dt_d, void* dx, int dt_dx, int64_t n, float p,
+                      uint64_t seed, int training, int acc, void* stream);
 int xt_dropout_mask(uint8_t* mask, int64_t n, float p, uint64_t seed, void* stream);
 int xt_dropout_add_fwd(const void* h, const void* a, void* out, int64_t n, float p,
                        uint64_t seed, int training, int dt, void* stream);
@@ -247,14 +264,19 @@ typedef struct xt_matmul_desc {
   int64_t stride_c_outer, stride_c_inner;
 } xt_matmul_desc;
 
-int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C,
-                  void* stream);
+/* Scratch bytes the call needs: nonzero only for XT_F32 operands read MN-major (trans_a = 1
+ * or trans_b = 0), which are first copied, transposed, into K-major scratch because the
+ * tf32 MMA is fed K-major operands only.  ws may be NULL when the size is 0. */
+int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes);
+int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* ws,
+                  size_t ws_bytes, void* stream);
 /* Backward of C = alpha·op(A)@op(B) given dC (layout of C, dtype dtype_ab):
  * dA = alpha·dC@op(B)ᵀ into A's layout, dB = alpha·op(A)ᵀ@dC into B's layout; dA/dB have
  * dtype dt_grad_a / dt_grad_b; either may be NULL.  causal must be 0. */
+int xt_matmul_bwd_workspace_size(const xt_matmul_desc* desc, size_t* bytes);
 int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* dC,
                   void* dA, void* dB, int dt_grad_a, int dt_grad_b, int acc_a, int acc_b,
-                  void* stream);
+                  void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Native block stack ([BP] § Framåtgåendet; [DO] § dropout 接在哪（wiring）):

@@ -13,7 +13,7 @@ HEADER = os.path.join(ROOT, "include", "xt.h")
 
 def header_functions():
     src = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(xt_\w+)\s*\(", src, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*|uint64_t)\s+(xt_\w+)\s*\(", src, re.M)))
 
 
 @pytest.fixture(scope="module")
@@ -44,18 +44,23 @@ def test_binding_declares_every_symbol(xt):
 
 def test_host_validation(xt):
     L = xt.lib()
-    assert L.xt_matmul_fwd(None, None, None, None, None) == xt.XT_ERR_INVALID_ARG
+    assert L.xt_matmul_fwd(None, None, None, None, None, 0, None) == xt.XT_ERR_INVALID_ARG
     assert b"desc is NULL" in L.xt_last_error()
     assert L.xt_dropout_fwd(None, None, 10, C.c_float(1.5), 1, 1, 0, None) == xt.XT_ERR_INVALID_ARG
     assert L.xt_rope_table(None, 4, 7, C.c_double(1e4), 0, None) == xt.XT_ERR_INVALID_ARG
     assert L.xt_softmax_fwd(None, None, 4, 8, 5, 0, 0, None) == xt.XT_ERR_INVALID_ARG
     assert L.xt_rms_norm_fwd(None, None, None, None, -1, 8, C.c_float(1e-5), 0, None) == xt.XT_ERR_INVALID_ARG
     assert L.xt_accumulate(None, 7, None, 0, 4, None) == xt.XT_ERR_INVALID_ARG
-    d = xt.matmul_desc(64, 64, 60, lda=60, ldb=64)
-    assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None) == xt.XT_ERR_ALIGNMENT
-    d = xt.matmul_desc(64, 64, 64, lda=8)
-    assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None) == xt.XT_ERR_INVALID_ARG
     sz = C.c_size_t(0)
+    d = xt.matmul_desc(64, 64, 60, lda=60, ldb=64)
+    assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None, 0, None) == xt.XT_ERR_ALIGNMENT
+    d = xt.matmul_desc(64, 64, 64, lda=8)
+    assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None, 0, None) == xt.XT_ERR_INVALID_ARG
+    # fp32 operands read MN-major need tf32 staging scratch; bf16 ones do not
+    d = xt.matmul_desc(256, 128, 64, trans_a=1, dtype_ab=xt.XT_F32)
+    assert L.xt_matmul_workspace_size(C.byref(d), C.byref(sz)) == 0 and sz.value >= 256 * 64 * 4 + 128 * 64 * 4
+    d = xt.matmul_desc(256, 128, 64, trans_a=1, dtype_ab=xt.XT_BF16)
+    assert L.xt_matmul_workspace_size(C.byref(d), C.byref(sz)) == 0 and sz.value == 0
     assert L.xt_embedding_workspace_size(1000, C.byref(sz)) == 0 and sz.value == 8000
     assert L.xt_sum_workspace_size(-1, C.byref(sz)) == xt.XT_ERR_INVALID_ARG
     assert xt.version().startswith("xt")

@@ -1,0 +1,112 @@
+"""GPU parity of the native block stack (xt_block_fwd / xt_block_bwd) against the oracle:
+the loss and every leaf gradient, normalised error ‖g − r‖/‖r‖ ≤ 2e-2 per leaf, for the three
+block configurations (tiny fp32, 4×256 fp32 with dropout, 12-layer bf16 GPT stack) and small
+variants; plus the dropout gates, determinism and += accumulation."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import block as OB
+from tests.gpu_util import norm_err
+
+pytestmark = pytest.mark.gpu
+
+xt = pytest.importorskip("transformer_fwd_bwd_gb300.xt")
+from transformer_fwd_bwd_gb300.block import NativeBlock  # noqa: E402
+
+SEED = synth.BASE_SEED_DROPOUT
+
+
+def run_native(cfg, params, ids, tgt, training=True, base_seed=SEED, steps=1):
+    nb = NativeBlock(cfg, training=training, base_seed=base_seed)
+    nb.load(params)
+    nb.zero_grads()
+    I = torch.tensor(ids, device="cuda")
+    Tg = torch.tensor(tgt, device="cuda")
+    for _ in range(steps):
+        loss = nb.step(I, Tg)
+    torch.cuda.synchronize()
+    assert xt.device_errors() == 0
+    return float(loss.item()), nb.grads_named(), nb
+
+
+def compare(cfg, training=True, base_seed=SEED, tol=2e-2, params=None, report=None):
+    params = params if params is not None else synth.block_params(cfg)
+    ids, tgt = synth.block_tokens(cfg)
+    loss, grads, _ = run_native(cfg, params, ids, tgt, training, base_seed)
+    rloss, rgrads = OB.forward_backward(cfg, params, ids, tgt, base_seed, training)
+    errs = {k: norm_err(grads[k], rgrads[k]) for k in rgrads}
+    worst = max(errs, key=errs.get)
+    if report is not None:
+        report.update(errs)
+    assert abs(loss - rloss) <= 1e-3 * abs(rloss), f"loss {loss} vs oracle {rloss}"
+    assert errs[worst] <= tol, f"{worst}: normalised grad error {errs[worst]:.3e}"
+    return errs
+
+
+def variant(name, **over):
+    cfg = dict(synth.BLOCK_CONFIGS[name])
+    cfg.update(over)
+    return cfg
+
+
+def test_block_tiny():
+    """Tiny configuration: 1 block, fp32, RMSNorm + RoPE + SwiGLU, p = 0."""
+    compare(synth.BLOCK_CONFIGS["tiny"])
+
+
+def test_block_tiny_dropout():
+    compare(variant("tiny", p=0.2), training=True)
+
+
+def test_block_tiny_ln_gelu_pos_fp32():
+    """The 12-layer stack's topology (LayerNorm, GELU, learned positions) at tiny size, fp32."""
+    compare(variant("tiny", norm="ln", mlp="gelu", rope=False, learned_pos=True, n_layers=2),
+            params=synth.block_params(variant("tiny", norm="ln", mlp="gelu", rope=False, learned_pos=True,
+                                              n_layers=2), gain_jitter=0.1))
+
+
+def test_block_small_bf16():
+    cfg = variant("gpt12", B=2, S=256, d=128, H=2, hd=64, F=512, V=1000, n_layers=2)
+    compare(cfg, params=synth.block_params(cfg, gain_jitter=0.1))
+
+
+def test_block_256():
+    """Configuration 4×256, d 256, 4 heads, SwiGLU 688, vocab 4096, fp32, dropout 0.1."""
+    compare(synth.BLOCK_CONFIGS["block256"], training=True)
+
+
+def test_block_p0_bit_identity_and_eval():
+    """[DO] gates: p = 0 in training is bit-identical to no dropout; eval is the identity."""
+    cfg = synth.BLOCK_CONFIGS["block256"]
+    params = synth.block_params(cfg)
+    ids, tgt = synth.block_tokens(cfg)
+    l0, g0, _ = run_native(dict(cfg, p=0.0), params, ids, tgt, training=True)
+    l1, g1, _ = run_native(dict(cfg, p=0.1), params, ids, tgt, training=False)
+    assert l0 == l1
+    for k in g0:
+        assert np.array_equal(g0[k], g1[k]), k
+    l2, _, _ = run_native(dict(cfg, p=0.1), params, ids, tgt, training=True)
+    assert l2 != l0
+
+
+def test_block_deterministic_and_accumulates():
+    cfg = synth.BLOCK_CONFIGS["block256"]
+    params = synth.block_params(cfg)
+    ids, tgt = synth.block_tokens(cfg)
+    la, ga, _ = run_native(cfg, params, ids, tgt)
+    lb, gb, _ = run_native(cfg, params, ids, tgt)
+    assert la == lb
+    for k in ga:
+        assert np.array_equal(ga[k], gb[k]), k
+    _, g2, _ = run_native(cfg, params, ids, tgt, steps=2)   # backward adds: two steps = 2×
+    for k in ga:
+        assert norm_err(g2[k], 2 * ga[k]) <= 1e-6, k
+
+
+def test_block_gpt12_full():
+    """12-layer GPT-style stack at full size (B 8, S 1024, d 768, 12 heads, GELU 3072, vocab
+    50304, bf16) — the workload the benchmark times — against the float64 oracle."""
+    errs = compare(synth.BLOCK_CONFIGS["gpt12"], training=True, report={})
+    assert max(errs.values()) <= 2e-2

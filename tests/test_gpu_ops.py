@@ -6,11 +6,10 @@ Column reductions (dγ, dβ, dbias, full sums) are compared with a bound proport
 the sum of the magnitudes of their terms (the condition of a sum): |g − r| ≤ 1e-5·Σ|terms|
 (+ 1 bf16 ulp for bf16 outputs).
 """
-import math
-
 import numpy as np
 import pytest
 import torch
+from scipy.special import erf
 
 import synth
 from oracle import dropout as OD
@@ -52,28 +51,33 @@ def test_elementwise(dtype, n):
     d = inputs((n,), 3, dtype)
     A, B, D = dev(a, dtype), dev(b, dtype), dev(d, dtype)
     y = empty((n,), dtype)
-    xt.xt_add_fwd(A, B, y); sync(); check(host(y), a + b, dtype, "add")
+    xt.xt_add_fwd(A, B, y); sync(); check(host(y), a + b, dtype, "add", mag=np.abs(a) + np.abs(b))
     xt.xt_mul_fwd(A, B, y); sync(); check(host(y), a * b, dtype, "mul")
     xt.xt_scale_fwd(A, y, 0.37); sync(); check(host(y), a * np.float32(0.37), dtype, "scale")
     xt.xt_silu_fwd(A, y); sync(); check(host(y), O.silu_fwd(a), dtype, "silu")
-    xt.xt_silu_bwd(D, A, y); sync(); check(host(y), O.silu_bwd(d, a), dtype, "silu_bwd")
+    sg = O.sigmoid(a)
+    xt.xt_silu_bwd(D, A, y); sync()
+    check(host(y), O.silu_bwd(d, a), dtype, "silu_bwd", mag=np.abs(d) * (sg + np.abs(a) * sg * (1 - sg)))
     xt.xt_gelu_fwd(A, y); sync(); check(host(y), O.gelu_fwd(a), dtype, "gelu")
-    xt.xt_gelu_bwd(D, A, y); sync(); check(host(y), O.gelu_bwd(d, a), dtype, "gelu_bwd")
+    Phi, phi = 0.5 * (1 + erf(a / np.sqrt(2))), np.exp(-a * a / 2) / np.sqrt(2 * np.pi)
+    xt.xt_gelu_bwd(D, A, y); sync()
+    check(host(y), O.gelu_bwd(d, a), dtype, "gelu_bwd", mag=np.abs(d) * (Phi + np.abs(a) * phi))
     da, db = empty((n,), dtype), empty((n,), dtype)
     xt.xt_mul_bwd(D, A, B, da, db); sync()
     ra, rb = O.mul_bwd(d, a, b)
     check(host(da), ra, dtype, "mul_bwd a"); check(host(db), rb, dtype, "mul_bwd b")
     # mul(x, x): both grads pushed into one buffer (accumulate on the second)
     xt.xt_mul_bwd(D, A, A, da, da, 0, 1); sync()
-    check(host(da), 2 * d * a, dtype, "mul(x,x) bwd")
+    check(host(da), 2 * d * a, dtype, "mul(x,x) bwd")  # second push adds an equal value: exact
     # add backward copies / accumulates
     xt.xt_add_bwd(D, da, db, 0, 1); sync()
     check(host(da), d, dtype, "add_bwd copy")
-    check(host(db), synth.to_storage(rb, dtype) + d, dtype, "add_bwd acc")
+    rb_s = synth.to_storage(rb, dtype)
+    check(host(db), rb_s + d, dtype, "add_bwd acc", mag=np.abs(rb_s) + np.abs(d))
     # scale backward with accumulate
     z = dev(np.ones(n), dtype)
     xt.xt_scale_bwd(D, z, 2.0, acc=1); sync()
-    check(host(z), 1 + 2 * d, dtype, "scale_bwd acc")
+    check(host(z), 1 + 2 * d, dtype, "scale_bwd acc", mag=1 + 2 * np.abs(d))
 
 
 def test_accumulate_mixed_dtypes():
@@ -82,10 +86,11 @@ def test_accumulate_mixed_dtypes():
     src = inputs((n,), 5, "bf16")
     dst = dev(base, "f32")
     xt.xt_accumulate(dst, dev(src, "bf16")); sync()
-    check(host(dst), base + src, "f32", "f32 += bf16")
+    check(host(dst), base + src, "f32", "f32 += bf16", mag=np.abs(base) + np.abs(src))
     dstb = dev(synth.round_bf16(base), "bf16")
     xt.xt_accumulate(dstb, dev(src, "bf16")); sync()
-    check(host(dstb), synth.round_bf16(base) + src, "bf16", "bf16 += bf16")
+    bb = synth.round_bf16(base)
+    check(host(dstb), bb + src, "bf16", "bf16 += bf16", mag=np.abs(bb) + np.abs(src))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -121,13 +126,15 @@ def test_rms_norm(dtype, rows, cols):
     dx, dg = O.rms_norm_bwd(d, x, gamma, np.float32(ir).astype(np.float64))
     DX, DG = empty((rows, cols), dtype), empty((cols,), "f32")
     xt.xt_rms_norm_bwd(Dd, X, G, IRo, DX, DG); sync()
-    check(host(DX), dx, dtype, "rms dx")
+    irr = np.float32(ir).astype(np.float64)
+    mag_dx = np.abs(irr[:, None] * d * gamma) + np.abs(x * (irr ** 3 / cols * np.sum(d * gamma * x, 1))[:, None])
+    check(host(DX), dx, dtype, "rms dx", mag=mag_dx)
     check_sum(host(DG), dg, np.abs(d * x * ir[:, None]).sum(0), "f32", "rms dgamma")
     # accumulate paths: dx += , dγ +=
     DX2 = dev(np.ones((rows, cols)), dtype)
     DG2 = dev(np.ones(cols), "f32")
     xt.xt_rms_norm_bwd(Dd, X, G, IRo, DX2, DG2, acc_dx=1, acc_param=1); sync()
-    check(host(DX2), (1 + host(DX)) if dtype == "bf16" else 1 + dx, dtype, "rms dx acc")
+    check(host(DX2), 1 + dx, dtype, "rms dx acc", mag=1 + mag_dx)
     check_sum(host(DG2), 1 + dg, 1 + np.abs(d * x * ir[:, None]).sum(0), "f32", "rms dgamma acc")
 
 
@@ -143,7 +150,8 @@ def test_layernorm(dtype, rows, cols):
     X = dev(x, dtype)
     Y, MU, RS = empty((rows, cols), dtype), empty((rows,), "f32"), empty((rows,), "f32")
     xt.xt_layernorm_fwd(X, dev(gamma, dtype), dev(beta, dtype), Y, MU, RS, eps); sync()
-    check(host(Y), y, dtype, "ln y")
+    xhat = (x - mu[:, None]) * rstd[:, None]
+    check(host(Y), y, dtype, "ln y", mag=np.abs(xhat * gamma) + np.abs(beta))
     assert np.max(np.abs(host(MU) - mu)) <= 1e-5 * np.max(np.abs(x))
     check(host(RS), rstd, "f32", "ln rstd")
     mu32, rs32 = np.float32(mu).astype(np.float64), np.float32(rstd).astype(np.float64)
@@ -277,13 +285,18 @@ def test_rope(dtype, B, S, H, hd):
     out = Buf.clone()
     xt.xt_rope_fwd(Buf, out, table, B, S, H, hd, ld); sync()
     want = O.rope_fwd(q, pos, 10000.0).transpose(0, 2, 1, 3).reshape(B * S, d_model)
+    h = hd // 2
+    th = O.rope_angles(pos, hd, 10000.0)
+    qa = np.abs(q)
+    mag = (np.concatenate([qa[..., :h] * np.abs(np.cos(th)) + qa[..., h:] * np.abs(np.sin(th))] * 2, axis=-1)
+           .transpose(0, 2, 1, 3).reshape(B * S, d_model))
     g = host(out)
-    check(g[:, :d_model], want, dtype, "rope fwd")
+    check(g[:, :d_model], want, dtype, "rope fwd", mag=mag)
     assert np.array_equal(g[:, d_model:], host(Buf)[:, d_model:]), "rope touched other columns"
     # in place, backward
     xt.xt_rope_bwd(Buf, Buf, table, B, S, H, hd, ld); sync()
     wantb = O.rope_bwd(q, pos, 10000.0).transpose(0, 2, 1, 3).reshape(B * S, d_model)
-    check(host(Buf)[:, :d_model], wantb, dtype, "rope bwd")
+    check(host(Buf)[:, :d_model], wantb, dtype, "rope bwd", mag=mag)
 
 
 # ----------------------------------------------------------------------------- dropout
@@ -385,7 +398,8 @@ def test_swiglu(dtype, rows, F):
     DGU = empty((rows, 2 * F), dtype)
     xt.xt_swiglu_bwd(dev(d, dtype), GU[:, :F], GU[:, F:], DGU[:, :F], DGU[:, F:]); sync()
     gd = host(DGU)
-    check(gd[:, :F], dg, dtype, "swiglu dg")
+    sg = O.sigmoid(g)
+    check(gd[:, :F], dg, dtype, "swiglu dg", mag=np.abs(d * u) * (sg + np.abs(g) * sg * (1 - sg)))
     check(gd[:, F:], du, dtype, "swiglu du")
 
 

@@ -1,5 +1,8 @@
-// Status reporting, the device error flag and device facts.
+// Status reporting, the device error flag, device facts, the launch counter and the
+// optional per-GEMM event timing.
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -11,6 +14,18 @@ __device__ uint32_t g_errflag;
 uint32_t* g_flag_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::mutex g_mu;
+std::atomic<uint64_t> g_launches{0};
+
+// GEMM timing: pairs of events recorded around each GEMM launch while enabled.
+struct GemmRecord {
+  double flops;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::vector<cudaEvent_t> g_ev_pool;
+std::vector<GemmRecord> g_records;
+size_t g_ev_next = 0;
+bool g_prof_on = false;
 }  // namespace
 
 namespace xt {
@@ -24,6 +39,7 @@ int fail(int code, const char* fmt, ...) {
 }
 
 int check_launch(const char* what) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(XT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return XT_OK;
@@ -59,9 +75,57 @@ int num_sms() {
   return g_sms[dev];
 }
 
+bool gemm_profile_begin(cudaStream_t s, double flops, void** token) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on || g_ev_next + 2 > g_ev_pool.size()) return false;
+  GemmRecord r{flops, g_ev_pool[g_ev_next], g_ev_pool[g_ev_next + 1]};
+  g_ev_next += 2;
+  cudaEventRecord(r.start, s);
+  g_records.push_back(r);
+  *token = reinterpret_cast<void*>(g_records.size());
+  return true;
+}
+
+void gemm_profile_end(cudaStream_t s, void* token) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  const size_t i = reinterpret_cast<size_t>(token);
+  if (i >= 1 && i <= g_records.size()) cudaEventRecord(g_records[i - 1].stop, s);
+}
+
 }  // namespace xt
 
 extern "C" {
+
+uint64_t xt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int xt_profile_gemm(int capacity) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_records.clear();
+  g_ev_next = 0;
+  g_prof_on = capacity > 0;
+  while (g_ev_pool.size() < size_t(2 * capacity)) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return xt::check_launch("xt_profile_gemm");
+    g_ev_pool.push_back(e);
+  }
+  return XT_OK;
+}
+
+int xt_profile_gemm_read(double* flops, float* ms, int max_records, int* n) {
+  XT_REQUIRE(n != nullptr, "xt_profile_gemm_read: n is NULL");
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  const int cnt = int(g_records.size());
+  *n = cnt;
+  for (int i = 0; i < cnt && i < max_records; ++i) {
+    if (cudaEventSynchronize(g_records[i].stop) != cudaSuccess) return xt::check_launch("xt_profile_gemm_read");
+    float t = 0.f;
+    cudaEventElapsedTime(&t, g_records[i].start, g_records[i].stop);
+    if (flops) flops[i] = g_records[i].flops;
+    if (ms) ms[i] = t;
+  }
+  return XT_OK;
+}
+
 
 const char* xt_last_error(void) { return g_msg; }
 

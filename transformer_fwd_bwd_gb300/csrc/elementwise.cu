@@ -52,7 +52,8 @@ __device__ __forceinline__ bool dropout_keep(uint64_t seed, uint64_t i, float p)
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
-__device__ __forceinline__ float gelu_cdf(float x) { return 0.5f * (1.f + erff(x * 0.70710678118654752f)); }
+// Φ(x) = ½·erfc(−x/√2): no cancellation for x ≪ 0 (unlike ½(1 + erf(x/√2))).
+__device__ __forceinline__ float gelu_cdf(float x) { return 0.5f * erfcf(-x * 0.70710678118654752f); }
 __device__ __forceinline__ float gelu_pdf(float x) { return 0.39894228040143268f * expf(-0.5f * x * x); }
 
 template <EwOp OP>
@@ -419,6 +420,7 @@ int xt_sum_fwd(const void* x, int64_t n, int dt, float* out, void* ws, void* str
     sum_stage1<float><<<nb, kSumThreads, 0, s>>>(static_cast<const float*>(x), n, part);
   else
     sum_stage1<bf16><<<nb, kSumThreads, 0, s>>>(static_cast<const bf16*>(x), n, part);
+  XT_TRY(check_launch("xt_sum_fwd"));
   sum_stage2<<<1, 1024, 0, s>>>(part, nb, out);
   return check_launch("xt_sum_fwd");
 }
@@ -503,6 +505,23 @@ int xt_dropout_bwd(const void* d, void* dx, int64_t n, float p, uint64_t seed, i
   }
   g.p = p; g.dscale = dropout_scale(p); g.seed = seed;
   return ew_dispatch<EW_DROPOUT>(dt, dt, g, stream, "xt_dropout_bwd");
+}
+
+int xt_dropout_bwd_ex(const void* d, int dt_d, void* dx, int dt_dx, int64_t n, float p, uint64_t seed,
+                      int training, int acc, void* stream) {
+  XT_CHECK_N(n);
+  XT_CHECK_DT(dt_d);
+  XT_CHECK_DT(dt_dx);
+  XT_TRY(check_dropout(p));
+  XT_REQUIRE(n == 0 || (d && dx), "xt_dropout_bwd_ex: NULL pointer");
+  EwArgs g = ew_args(d, nullptr, nullptr, dx, nullptr, n);
+  g.acc0 = acc;
+  if (p == 0.f || !training) {
+    g.alpha = 1.f;
+    return ew_dispatch<EW_SCALE>(dt_d, dt_dx, g, stream, "xt_dropout_bwd_ex");
+  }
+  g.p = p; g.dscale = dropout_scale(p); g.seed = seed;
+  return ew_dispatch<EW_DROPOUT>(dt_d, dt_dx, g, stream, "xt_dropout_bwd_ex");
 }
 
 int xt_dropout_add_fwd(const void* h, const void* a, void* out, int64_t n, float p, uint64_t seed,

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "internal.cuh"
 
 namespace xt {
 namespace gemm {
@@ -115,14 +116,91 @@ int run(const Problem& pb, cudaStream_t s) {
   int grid = int(tiles < num_sms() ? tiles : num_sms());
   if (grid < 1) grid = 1;
   const bool amn = pb.A.mn_major, bmn = pb.B.mn_major;
-  if (tf32) return launch_tf32(bn, amn, bmn, ta, tb, p, grid, s);
-  return launch_bf16(bn, amn, bmn, ta, tb, p, grid, s);
+  // algorithmic FLOPs: the unmasked work only for the causal modes
+  const double batches = double(p.batches);
+  double flops = 2.0 * double(pb.M) * double(pb.N) * double(pb.K) * batches;
+  if (pb.causal == 1) flops = 2.0 * double(pb.K) * double(pb.M) * double(pb.M + 1) / 2.0 * batches;
+  if (pb.causal >= 2) flops = 2.0 * double(pb.N) * double(pb.M) * double(pb.M + 1) / 2.0 * batches;
+  void* tok = nullptr;
+  const bool prof = gemm_profile_begin(s, flops, &tok);
+  const int st = tf32 ? launch_tf32(bn, amn, bmn, ta, tb, p, grid, s) : launch_bf16(bn, amn, bmn, ta, tb, p, grid, s);
+  if (prof) gemm_profile_end(s, tok);
+  return st;
 }
 
 }  // namespace gemm
 
+// ------------------------------------------------------------------------------ tf32 staging
+// The tf32 MMA is fed K-major operands only: an fp32 operand stored MN-major (MN
+// contiguous) is first copied, transposed, into K-major scratch (rows of round_up(K, 4)
+// floats) by a tiled shared-memory transpose.  bf16 operands are read MN-major directly.
+
+static int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+static size_t stage_bytes(const gemm::Operand& o) {
+  if (!o.mn_major) return 0;
+  return align256(size_t(o.batch_inner) * size_t(o.batch_outer) * size_t(o.mn) * size_t(round_up(o.K, 4)) * 4);
+}
+
+__global__ void transpose_to_kmajor(const float* __restrict__ src, int64_t ld, int64_t s_inner, int64_t s_outer,
+                                    int bi, int64_t mn, int64_t K, float* __restrict__ dst, int64_t ldk) {
+  __shared__ float tile[32][33];
+  const int z = blockIdx.z;
+  const int zo = z / bi, zi = z - zo * bi;
+  const float* S = src + int64_t(zo) * s_outer + int64_t(zi) * s_inner;
+  float* D = dst + int64_t(z) * mn * ldk;
+  const int64_t i0 = int64_t(blockIdx.x) * 32, k0 = int64_t(blockIdx.y) * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int64_t k = k0 + r, i = i0 + threadIdx.x;
+    tile[r][threadIdx.x] = (k < K && i < mn) ? S[k * ld + i] : 0.f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int64_t i = i0 + r, k = k0 + threadIdx.x;
+    if (i < mn && k < ldk) D[i * ldk + k] = tile[threadIdx.x][r];
+  }
+}
+
+// Rewrites `o` (fp32, MN-major) to point at a K-major copy carved from ws.
+static int stage_operand(gemm::Operand& o, char*& ws, size_t& left, cudaStream_t s) {
+  const size_t need = stage_bytes(o);
+  if (need > left) return fail(XT_ERR_INVALID_ARG, "matmul: workspace too small (tf32 staging)");
+  const int64_t ldk = round_up(o.K, 4);
+  const int batches = o.batch_inner * o.batch_outer;
+  if (batches > 65535) return fail(XT_ERR_UNSUPPORTED, "matmul: too many batches for tf32 staging");
+  dim3 grid(unsigned(ceil_div(o.mn, 32)), unsigned(ceil_div(ldk, 32)), unsigned(batches));
+  transpose_to_kmajor<<<grid, dim3(32, 8), 0, s>>>(static_cast<const float*>(o.ptr), o.ld, o.s_inner, o.s_outer,
+                                                    o.batch_inner, o.mn, o.K, reinterpret_cast<float*>(ws), ldk);
+  XT_TRY(check_launch("matmul tf32 staging"));
+  o.ptr = ws;
+  o.mn_major = false;
+  o.ld = ldk;
+  o.s_inner = o.mn * ldk;
+  o.s_outer = int64_t(o.batch_inner) * o.mn * ldk;
+  ws += need;
+  left -= need;
+  return XT_OK;
+}
+
+static gemm::Operand operand_a(const xt_matmul_desc* d, const void* A) {
+  return gemm::Operand{A, d->trans_a == 1, d->M, d->K, d->lda, d->stride_a_inner, d->stride_a_outer,
+                       d->batch_inner, d->batch_outer};
+}
+// op(B) is K×N; the kernel's B operand is N rows by K: K-major iff B is stored [N, K].
+static gemm::Operand operand_b(const xt_matmul_desc* d, const void* B) {
+  return gemm::Operand{B, d->trans_b == 0, d->N, d->K, d->ldb, d->stride_b_inner, d->stride_b_outer,
+                       d->batch_inner, d->batch_outer};
+}
+
+static size_t matmul_ws(const xt_matmul_desc* d) {
+  if (d->dtype_ab != XT_F32 || d->M == 0 || d->N == 0 || d->K == 0) return 0;
+  return stage_bytes(operand_a(d, nullptr)) + stage_bytes(operand_b(d, nullptr));
+}
+
 // Validates and runs C[M,N] (+)= alpha · op(A) @ op(B) for one matmul descriptor.
-static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, void* C, cudaStream_t s) {
+static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, void* C, void* ws, size_t ws_bytes,
+                      cudaStream_t s) {
   XT_REQUIRE(d != nullptr, "matmul: desc is NULL");
   XT_REQUIRE(d->M >= 0 && d->N >= 0 && d->K >= 0, "matmul: negative size");
   XT_REQUIRE(d->batch_outer >= 1 && d->batch_inner >= 1, "matmul: batch counts must be >= 1");
@@ -164,11 +242,15 @@ static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, voi
   pb.K = d->K;
   pb.batch_inner = d->batch_inner;
   pb.batch_outer = d->batch_outer;
-  pb.A = gemm::Operand{A, d->trans_a == 1, d->M, d->K, d->lda, d->stride_a_inner, d->stride_a_outer,
-                       d->batch_inner, d->batch_outer};
-  // op(B) is K×N; the kernel's B operand is N rows by K: K-major iff B is stored [N, K].
-  pb.B = gemm::Operand{B, d->trans_b == 0, d->N, d->K, d->ldb, d->stride_b_inner, d->stride_b_outer,
-                       d->batch_inner, d->batch_outer};
+  pb.A = operand_a(d, A);
+  pb.B = operand_b(d, B);
+  if (pb.tf32 && (pb.A.mn_major || pb.B.mn_major)) {
+    XT_REQUIRE(ws != nullptr || matmul_ws(d) == 0, "matmul: fp32 operands read MN-major need a workspace");
+    char* w = static_cast<char*>(ws);
+    size_t left = ws_bytes;
+    if (pb.A.mn_major) XT_TRY(stage_operand(pb.A, w, left, s));
+    if (pb.B.mn_major) XT_TRY(stage_operand(pb.B, w, left, s));
+  }
   pb.C = C;
   pb.ldc = d->ldc;
   pb.sc_inner = d->stride_c_inner;
@@ -186,20 +268,29 @@ using namespace xt;
 
 extern "C" {
 
-int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* stream) {
-  return matmul_run(desc, A, B, C, as_stream(stream));
+int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes) {
+  XT_REQUIRE(desc && bytes, "xt_matmul_workspace_size: NULL pointer");
+  *bytes = matmul_ws(desc);
+  return XT_OK;
 }
 
-int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* dC, void* dA, void* dB,
-                  int dt_grad_a, int dt_grad_b, int acc_a, int acc_b, void* stream) {
-  XT_REQUIRE(desc != nullptr, "xt_matmul_bwd: desc is NULL");
-  XT_REQUIRE(desc->causal == 0, "xt_matmul_bwd: causal must be 0");
-  XT_REQUIRE(!dA || valid_dtype(dt_grad_a), "xt_matmul_bwd: bad dt_grad_a");
-  XT_REQUIRE(!dB || valid_dtype(dt_grad_b), "xt_matmul_bwd: bad dt_grad_b");
-  const xt_matmul_desc& f = *desc;
-  cudaStream_t s = as_stream(stream);
-  if (dA) {
-    xt_matmul_desc g{};
+int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* ws, size_t ws_bytes,
+                  void* stream) {
+  return matmul_run(desc, A, B, C, ws, ws_bytes, as_stream(stream));
+}
+
+}  // extern "C"
+
+// The two GEMMs of the matmul backward, as descriptors over (dC, A, B).
+struct BwdPlan {
+  xt_matmul_desc ga, gb;
+  int a_first_is_dc, b_first_is_dc;  // operand order of each GEMM
+};
+
+static BwdPlan bwd_plan(const xt_matmul_desc& f, int dt_grad_a, int dt_grad_b, int acc_a, int acc_b) {
+  BwdPlan pl{};
+  {
+    xt_matmul_desc& g = pl.ga;
     g.batch_outer = f.batch_outer;
     g.batch_inner = f.batch_inner;
     g.dtype_ab = f.dtype_ab;
@@ -211,17 +302,17 @@ int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, cons
       g.trans_a = 0; g.lda = f.ldc; g.stride_a_inner = f.stride_c_inner; g.stride_a_outer = f.stride_c_outer;
       g.trans_b = f.trans_b ? 0 : 1; g.ldb = f.ldb; g.stride_b_inner = f.stride_b_inner; g.stride_b_outer = f.stride_b_outer;
       g.ldc = f.lda; g.stride_c_inner = f.stride_a_inner; g.stride_c_outer = f.stride_a_outer;
-      XT_TRY(matmul_run(&g, dC, B, dA, s));
+      pl.a_first_is_dc = 1;
     } else {  // A stored [K,M]: dA = op(B) @ dCᵀ
       g.M = f.K; g.N = f.M; g.K = f.N;
       g.trans_a = f.trans_b; g.lda = f.ldb; g.stride_a_inner = f.stride_b_inner; g.stride_a_outer = f.stride_b_outer;
       g.trans_b = 1; g.ldb = f.ldc; g.stride_b_inner = f.stride_c_inner; g.stride_b_outer = f.stride_c_outer;
       g.ldc = f.lda; g.stride_c_inner = f.stride_a_inner; g.stride_c_outer = f.stride_a_outer;
-      XT_TRY(matmul_run(&g, B, dC, dA, s));
+      pl.a_first_is_dc = 0;
     }
   }
-  if (dB) {
-    xt_matmul_desc g{};
+  {
+    xt_matmul_desc& g = pl.gb;
     g.batch_outer = f.batch_outer;
     g.batch_inner = f.batch_inner;
     g.dtype_ab = f.dtype_ab;
@@ -233,16 +324,54 @@ int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, cons
       g.trans_a = f.trans_a ? 0 : 1; g.lda = f.lda; g.stride_a_inner = f.stride_a_inner; g.stride_a_outer = f.stride_a_outer;
       g.trans_b = 0; g.ldb = f.ldc; g.stride_b_inner = f.stride_c_inner; g.stride_b_outer = f.stride_c_outer;
       g.ldc = f.ldb; g.stride_c_inner = f.stride_b_inner; g.stride_c_outer = f.stride_b_outer;
-      XT_TRY(matmul_run(&g, A, dC, dB, s));
+      pl.b_first_is_dc = 0;
     } else {  // B stored [N,K]: dB = dCᵀ @ op(A)
       g.M = f.N; g.N = f.K; g.K = f.M;
       g.trans_a = 1; g.lda = f.ldc; g.stride_a_inner = f.stride_c_inner; g.stride_a_outer = f.stride_c_outer;
       g.trans_b = f.trans_a; g.ldb = f.lda; g.stride_b_inner = f.stride_a_inner; g.stride_b_outer = f.stride_a_outer;
       g.ldc = f.ldb; g.stride_c_inner = f.stride_b_inner; g.stride_c_outer = f.stride_b_outer;
-      XT_TRY(matmul_run(&g, dC, A, dB, s));
+      pl.b_first_is_dc = 1;
     }
+  }
+  return pl;
+}
+
+extern "C" {
+
+int xt_matmul_bwd_workspace_size(const xt_matmul_desc* desc, size_t* bytes) {
+  XT_REQUIRE(desc && bytes, "xt_matmul_bwd_workspace_size: NULL pointer");
+  const BwdPlan pl = bwd_plan(*desc, XT_F32, XT_F32, 0, 0);
+  const size_t a = matmul_ws(&pl.ga), b = matmul_ws(&pl.gb);
+  *bytes = a > b ? a : b;
+  return XT_OK;
+}
+
+int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* dC, void* dA, void* dB,
+                  int dt_grad_a, int dt_grad_b, int acc_a, int acc_b, void* ws, size_t ws_bytes, void* stream) {
+  XT_REQUIRE(desc != nullptr, "xt_matmul_bwd: desc is NULL");
+  XT_REQUIRE(desc->causal == 0, "xt_matmul_bwd: causal must be 0");
+  XT_REQUIRE(!dA || valid_dtype(dt_grad_a), "xt_matmul_bwd: bad dt_grad_a");
+  XT_REQUIRE(!dB || valid_dtype(dt_grad_b), "xt_matmul_bwd: bad dt_grad_b");
+  cudaStream_t s = as_stream(stream);
+  const BwdPlan pl = bwd_plan(*desc, dt_grad_a, dt_grad_b, acc_a, acc_b);
+  // the two GEMMs run in stream order, so they can share one workspace
+  if (dA) {
+    if (pl.a_first_is_dc) XT_TRY(matmul_run(&pl.ga, dC, B, dA, ws, ws_bytes, s));
+    else XT_TRY(matmul_run(&pl.ga, B, dC, dA, ws, ws_bytes, s));
+  }
+  if (dB) {
+    if (pl.b_first_is_dc) XT_TRY(matmul_run(&pl.gb, dC, A, dB, ws, ws_bytes, s));
+    else XT_TRY(matmul_run(&pl.gb, A, dC, dB, ws, ws_bytes, s));
   }
   return XT_OK;
 }
 
 }  // extern "C"
+
+namespace xt {
+int matmul(const xt_matmul_desc& d, const void* A, const void* B, void* C, void* ws, size_t ws_bytes,
+           cudaStream_t s) {
+  return matmul_run(&d, A, B, C, ws, ws_bytes, s);
+}
+size_t matmul_workspace(const xt_matmul_desc& d) { return matmul_ws(&d); }
+}  // namespace xt

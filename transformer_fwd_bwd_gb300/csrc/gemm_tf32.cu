@@ -4,13 +4,13 @@
 namespace xt {
 namespace gemm {
 
+// tf32 operands are always K-major here: MN-major fp32 operands are staged K-major by the
+// host side first (the tf32 MMA is fed K-major operands only).
 template <int BN>
 static int pick_major(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid,
                       cudaStream_t s) {
-  if (!a_mn && !b_mn) return launch_one<true, BN, false, false>(ta, tb, p, grid, s);
-  if (!a_mn && b_mn) return launch_one<true, BN, false, true>(ta, tb, p, grid, s);
-  if (a_mn && !b_mn) return launch_one<true, BN, true, false>(ta, tb, p, grid, s);
-  return launch_one<true, BN, true, true>(ta, tb, p, grid, s);
+  if (a_mn || b_mn) return fail(XT_ERR_UNSUPPORTED, "gemm: tf32 operands must be K-major");
+  return launch_one<true, BN, false, false>(ta, tb, p, grid, s);
 }
 
 int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,

@@ -155,10 +155,10 @@ __device__ __forceinline__ void fold_partials(const float (&p)[NV][VW], float* a
   for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) part[int64_t(blockIdx.x) * cols + c] = acc[c];
 }
 
-template <typename T, int VW, int MAXT>
+template <typename T, typename TD, int VW, int MAXT>
 __global__ void __launch_bounds__(MAXT) rms_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
                                                       const T* __restrict__ gamma, const float* __restrict__ inv_rms,
-                                                      T* dx, float* __restrict__ part, int64_t rows, int64_t cols,
+                                                      TD* dx, float* __restrict__ part, int64_t rows, int64_t cols,
                                                       int tpr, int acc_dx) {
   extern __shared__ float smem[];
   float* red = smem;          // 32
@@ -206,14 +206,14 @@ __global__ void __launch_bounds__(MAXT) rms_bwd_kernel(const T* __restrict__ d, 
           pg[k][e] += dv * xv * ir;
         }
         if (dx) {
-          T* p = dx + r * cols + j * VW;
+          TD* p = dx + r * cols + j * VW;
           if (acc_dx) {
             float old[VW];
-            load_vec<T, VW>(p, old);
+            load_vec<TD, VW>(p, old);
 #pragma unroll
             for (int e = 0; e < VW; ++e) o[e] += old[e];
           }
-          store_vec<T, VW>(p, o);
+          store_vec<TD, VW>(p, o);
         }
       }
     }
@@ -273,10 +273,10 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
   }
 }
 
-template <typename T, int VW, int MAXT>
+template <typename T, typename TD, int VW, int MAXT>
 __global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
                                                      const T* __restrict__ gamma, const float* __restrict__ mean,
-                                                     const float* __restrict__ rstd, T* dx, float* __restrict__ part_g,
+                                                     const float* __restrict__ rstd, TD* dx, float* __restrict__ part_g,
                                                      float* __restrict__ part_b, int64_t rows, int64_t cols,
                                                      int tpr, int acc_dx) {
   extern __shared__ float smem[];
@@ -331,14 +331,14 @@ __global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, c
           pb[k][e] += dv;
         }
         if (dx) {
-          T* p = dx + r * cols + j * VW;
+          TD* p = dx + r * cols + j * VW;
           if (acc_dx) {
             float old[VW];
-            load_vec<T, VW>(p, old);
+            load_vec<TD, VW>(p, old);
 #pragma unroll
             for (int e = 0; e < VW; ++e) o[e] += old[e];
           }
-          store_vec<T, VW>(p, o);
+          store_vec<TD, VW>(p, o);
         }
       }
     }
@@ -779,6 +779,24 @@ __global__ void __launch_bounds__(256) embed_pos_kernel(const TH* __restrict__ d
 
 constexpr int kBwdMaxTpr = 512;  // backward row kernels hold two rows + partials in registers
 
+// (T, TD) pairs for the norm backward: dx in the activation dtype, or fp32 from bf16.
+#define XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, ...)                              \
+  do {                                                                         \
+    if ((dt) == XT_F32) {                                                      \
+      using T = float; using TD = float;                                       \
+      if (vec) { constexpr int VW = 4; __VA_ARGS__; }                          \
+      else { constexpr int VW = 1; __VA_ARGS__; }                              \
+    } else if ((dt_dx) == XT_BF16) {                                           \
+      using T = bf16; using TD = bf16;                                         \
+      if (vec) { constexpr int VW = 8; __VA_ARGS__; }                          \
+      else { constexpr int VW = 1; __VA_ARGS__; }                              \
+    } else {                                                                   \
+      using T = bf16; using TD = float;                                        \
+      if (vec) { constexpr int VW = 8; __VA_ARGS__; }                          \
+      else { constexpr int VW = 1; __VA_ARGS__; }                              \
+    }                                                                          \
+  } while (0)
+
 static size_t norm_ws_floats(int64_t rows, int64_t cols, int vw) {
   RowPlan pl = plan_rows(cols, vw, kBwdMaxTpr);
   if (!pl.ok) return 0;
@@ -821,9 +839,10 @@ int xt_rms_norm_fwd(const void* x, const void* gamma, void* y, float* inv_rms, i
 }
 
 int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float* inv_rms, void* dx, void* dgamma,
-                    int64_t rows, int64_t cols, int dt, int dt_param, void* ws, int acc_dx, int acc_param,
+                    int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws, int acc_dx, int acc_param,
                     void* stream) {
-  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_param), "xt_rms_norm_bwd: bad dtype");
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_dx) && valid_dtype(dt_param), "xt_rms_norm_bwd: bad dtype");
+  XT_REQUIRE(dt_dx == dt || (dt == XT_BF16 && dt_dx == XT_F32), "xt_rms_norm_bwd: dx dtype must be dt or f32");
   XT_REQUIRE(rows >= 0 && cols > 0, "xt_rms_norm_bwd: bad sizes");
   XT_REQUIRE(rows == 0 || (d && x && gamma && inv_rms), "xt_rms_norm_bwd: NULL input");
   XT_REQUIRE(!dgamma || ws, "xt_rms_norm_bwd: dgamma needs a workspace");
@@ -841,11 +860,11 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
   float* part = dgamma ? static_cast<float*>(ws) : nullptr;
   const size_t smem = (32 + size_t(cols)) * sizeof(float);
   if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd: row too long");
-  XT_ROW_DISPATCH(dt, vec, {
-    auto k = pl.threads <= 256 ? rms_bwd_kernel<T, VW, 256> : rms_bwd_kernel<T, VW, 512>;
+  XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
+    auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
-                                   inv_rms, static_cast<T*>(dx), part, rows, cols, pl.tpr, acc_dx);
+                                   inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_rms_norm_bwd"));
   if (dgamma) return finalize(part, nb, cols, dgamma, dt_param, acc_param, s);
@@ -870,9 +889,10 @@ int xt_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y
 }
 
 int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,
-                     void* dgamma, void* dbeta, int64_t rows, int64_t cols, int dt, int dt_param, void* ws,
+                     void* dgamma, void* dbeta, int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws,
                      int acc_dx, int acc_param, void* stream) {
-  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_param), "xt_layernorm_bwd: bad dtype");
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_dx) && valid_dtype(dt_param), "xt_layernorm_bwd: bad dtype");
+  XT_REQUIRE(dt_dx == dt || (dt == XT_BF16 && dt_dx == XT_F32), "xt_layernorm_bwd: dx dtype must be dt or f32");
   XT_REQUIRE(rows >= 0 && cols > 0, "xt_layernorm_bwd: bad sizes");
   XT_REQUIRE(rows == 0 || (d && x && gamma && mean && rstd), "xt_layernorm_bwd: NULL input");
   XT_REQUIRE(!(dgamma || dbeta) || ws, "xt_layernorm_bwd: parameter grads need a workspace");
@@ -891,11 +911,11 @@ int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const floa
   float* part_b = dbeta ? static_cast<float*>(ws) + size_t(nb) * size_t(cols) : nullptr;
   const size_t smem = (32 + size_t(cols)) * sizeof(float);
   if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
-  XT_ROW_DISPATCH(dt, vec, {
-    auto k = pl.threads <= 256 ? ln_bwd_kernel<T, VW, 256> : ln_bwd_kernel<T, VW, 512>;
+  XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
+    auto k = pl.threads <= 256 ? ln_bwd_kernel<T, TD, VW, 256> : ln_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
-                                   mean, rstd, static_cast<T*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx);
+                                   mean, rstd, static_cast<TD*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_layernorm_bwd"));
   if (dgamma) XT_TRY(finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s));
@@ -1116,6 +1136,7 @@ int xt_embedding_bwd(const int32_t* ids, const void* dh, void* dE, void* dP, int
   do {                                                                                                      \
     embed_scatter_kernel<TH, TG><<<unsigned(T), 256, 0, s>>>(sorted, static_cast<const TH*>(dh),            \
                                                              static_cast<TG*>(dE), T, d, V);                \
+    XT_TRY(check_launch("xt_embedding_bwd scatter"));                                                       \
     if (dP) {                                                                                               \
       int64_t gp = ceil_div(int64_t(S) * d, 256);                                                           \
       embed_pos_kernel<TH, TG><<<unsigned(gp), 256, 0, s>>>(static_cast<const TH*>(dh), static_cast<TG*>(dP), \

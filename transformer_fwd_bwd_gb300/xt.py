@@ -66,6 +66,8 @@ _I, _I64, _F, _D, _U64, _SZP = C.c_int, C.c_int64, C.c_float, C.c_double, C.c_ui
 _SIGS = {
     "xt_get_device_errors": [C.POINTER(C.c_uint32), _VP],
     "xt_clear_device_errors": [_VP],
+    "xt_profile_gemm": [_I],
+    "xt_profile_gemm_read": [C.POINTER(C.c_double), C.POINTER(C.c_float), _I, C.POINTER(C.c_int)],
     "xt_accumulate": [_VP, _I, _VP, _I, _I64, _VP],
     "xt_add_fwd": [_VP, _VP, _VP, _I64, _I, _VP],
     "xt_add_bwd": [_VP, _VP, _VP, _I64, _I, _I, _I, _VP],
@@ -87,9 +89,9 @@ _SIGS = {
     "xt_gelu_bwd": [_VP, _VP, _VP, _I64, _I, _I, _VP],
     "xt_norm_bwd_workspace_size": [_I64, _I64, _SZP],
     "xt_rms_norm_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _F, _I, _VP],
-    "xt_rms_norm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _I, _I, _VP],
+    "xt_rms_norm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP, _I, _I, _VP],
     "xt_layernorm_fwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _F, _I, _VP],
-    "xt_layernorm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _I, _I, _VP],
+    "xt_layernorm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP, _I, _I, _VP],
     "xt_rope_table": [_VP, _I, _I, _D, _I, _VP],
     "xt_rope_fwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _VP],
     "xt_rope_bwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _I, _VP],
@@ -100,13 +102,20 @@ _SIGS = {
     "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
     "xt_dropout_fwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _VP],
     "xt_dropout_bwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _I, _VP],
+    "xt_dropout_bwd_ex": [_VP, _I, _VP, _I, _I64, _F, _U64, _I, _I, _VP],
     "xt_dropout_mask": [_VP, _I64, _F, _U64, _VP],
     "xt_dropout_add_fwd": [_VP, _VP, _VP, _I64, _F, _U64, _I, _I, _VP],
     "xt_embedding_workspace_size": [_I64, _SZP],
     "xt_embedding_fwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _VP],
     "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
-    "xt_matmul_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP],
-    "xt_matmul_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP],
+    "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
+    "xt_matmul_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, C.c_size_t, _VP],
+    "xt_matmul_bwd_workspace_size": [C.POINTER(MatmulDesc), _SZP],
+    "xt_matmul_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, C.c_size_t, _VP],
+    "xt_block_workspace_size": [C.POINTER(BlockConfig), _SZP],
+    "xt_block_fwd": [C.POINTER(BlockConfig), C.POINTER(BlockParams), _VP, _VP, _VP, _VP, _VP],
+    "xt_block_bwd": [C.POINTER(BlockConfig), C.POINTER(BlockParams), _VP, _VP, _VP, _VP],
+    "xt_block_zero_grads": [C.POINTER(BlockConfig), C.POINTER(BlockParams), _VP],
 }
 
 _lib = None
@@ -123,6 +132,8 @@ def lib():
         L.xt_last_error.argtypes = []
         L.xt_version.restype = C.c_char_p
         L.xt_version.argtypes = []
+        L.xt_launch_count.restype = C.c_uint64
+        L.xt_launch_count.argtypes = []
         for name, args in _SIGS.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -132,7 +143,26 @@ def lib():
 
 
 def exported_symbols():
-    return ["xt_last_error", "xt_version", *_SIGS.keys()]
+    return ["xt_last_error", "xt_version", "xt_launch_count", *_SIGS.keys()]
+
+
+def launch_count() -> int:
+    return int(lib().xt_launch_count())
+
+
+def profile_gemm(capacity: int):
+    call("xt_profile_gemm", int(capacity))
+
+
+def profile_gemm_read(max_records: int = 1 << 16):
+    """Returns (flops, ms) numpy arrays of the GEMM launches recorded since profile_gemm()."""
+    import numpy as np
+    fl = (C.c_double * max_records)()
+    ms = (C.c_float * max_records)()
+    n = C.c_int(0)
+    call("xt_profile_gemm_read", fl, ms, max_records, C.byref(n))
+    k = min(n.value, max_records)
+    return np.array(fl[:k]), np.array(ms[:k], dtype=np.float64)
 
 
 def _check(code):
@@ -289,7 +319,8 @@ def xt_rms_norm_bwd(d, x, gamma, inv_rms, dx, dgamma, acc_dx=0, acc_param=0, ws=
     if ws is None:
         ws = workspace(ws_bytes("xt_norm_bwd_workspace_size", rows, cols), x.device)
     call("xt_rms_norm_bwd", ptr(d), ptr(x), ptr(gamma), ptr(inv_rms), ptr(dx), ptr(dgamma), rows, cols, dt(x),
-         dt(dgamma) if dgamma is not None else dt(x), ptr(ws), acc_dx, acc_param, stream(s))
+         dt(dx) if dx is not None else dt(x), dt(dgamma) if dgamma is not None else dt(x), ptr(ws), acc_dx,
+         acc_param, stream(s))
 
 
 def xt_layernorm_fwd(x, gamma, beta, y, mean, rstd, eps, s=None):
@@ -304,7 +335,7 @@ def xt_layernorm_bwd(d, x, gamma, mean, rstd, dx, dgamma, dbeta, acc_dx=0, acc_p
         ws = workspace(ws_bytes("xt_norm_bwd_workspace_size", rows, cols), x.device)
     pdt = dt(dgamma) if dgamma is not None else (dt(dbeta) if dbeta is not None else dt(x))
     call("xt_layernorm_bwd", ptr(d), ptr(x), ptr(gamma), ptr(mean), ptr(rstd), ptr(dx), ptr(dgamma), ptr(dbeta),
-         rows, cols, dt(x), pdt, ptr(ws), acc_dx, acc_param, stream(s))
+         rows, cols, dt(x), dt(dx) if dx is not None else dt(x), pdt, ptr(ws), acc_dx, acc_param, stream(s))
 
 
 def xt_rope_table(table, S, hd, base, pos_offset=0, s=None):
@@ -355,6 +386,11 @@ def xt_dropout_bwd(d, dx, p, seed, training=1, acc=0, s=None):
          acc, stream(s))
 
 
+def xt_dropout_bwd_ex(d, dx, p, seed, training=1, acc=0, s=None):
+    call("xt_dropout_bwd_ex", ptr(d), dt(d), ptr(dx), dt(dx), d.numel(), float(p), int(seed) & (2**64 - 1),
+         int(training), acc, stream(s))
+
+
 def xt_dropout_mask(mask, p, seed, s=None):
     call("xt_dropout_mask", ptr(mask), mask.numel(), float(p), int(seed) & (2**64 - 1), stream(s))
 
@@ -394,10 +430,18 @@ def matmul_desc(M, N, K, *, trans_a=0, trans_b=0, lda=None, ldb=None, ldc=None, 
     return d
 
 
-def xt_matmul_fwd(desc, A, B, Cm, s=None):
-    call("xt_matmul_fwd", C.byref(desc), ptr(A), ptr(B), ptr(Cm), stream(s))
+def xt_matmul_fwd(desc, A, B, Cm, ws=None, s=None):
+    n = ws_bytes("xt_matmul_workspace_size", C.byref(desc))
+    if n and ws is None:
+        ws = workspace(n, Cm.device)
+    call("xt_matmul_fwd", C.byref(desc), ptr(A), ptr(B), ptr(Cm), ptr(ws), ws.numel() if ws is not None else 0,
+         stream(s))
 
 
-def xt_matmul_bwd(desc, A, B, dC, dA, dB, acc_a=0, acc_b=0, s=None):
+def xt_matmul_bwd(desc, A, B, dC, dA, dB, acc_a=0, acc_b=0, ws=None, s=None):
+    n = ws_bytes("xt_matmul_bwd_workspace_size", C.byref(desc))
+    if n and ws is None:
+        ws = workspace(n, dC.device)
     call("xt_matmul_bwd", C.byref(desc), ptr(A), ptr(B), ptr(dC), ptr(dA), ptr(dB),
-         dt(dA) if dA is not None else XT_F32, dt(dB) if dB is not None else XT_F32, acc_a, acc_b, stream(s))
+         dt(dA) if dA is not None else XT_F32, dt(dB) if dB is not None else XT_F32, acc_a, acc_b, ptr(ws),
+         ws.numel() if ws is not None else 0, stream(s))
