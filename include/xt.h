@@ -87,6 +87,8 @@ int xt_profile_gemm_read(double* flops, float* ms, int max_records, int* n);
  * dst and src may have different dtypes (e.g. bf16 src into an f32 dst).
  * ------------------------------------------------------------------------------- */
 int xt_accumulate(void* dst, int dt_dst, const void* src, int dt_src, int64_t n, void* stream);
+/* dst[i] = src[i] converted between dtypes (bf16 results round to nearest even). */
+int xt_convert(void* dst, int dt_dst, const void* src, int dt_src, int64_t n, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Elementwise ops, [AE] op table rows add / mul / scale.  n elements, one dtype.

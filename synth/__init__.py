@@ -51,7 +51,7 @@ def from_bf16_bits(bits) -> np.ndarray:
 def to_storage(a, dtype: str) -> np.ndarray:
     """Round to the storage type ('f32' or 'bf16'); the result is float64 holding exact values."""
     if dtype == "f32":
-        return np.asarray(a, dtype=np.float32).astype(np.float64)
+        return np.ascontiguousarray(np.asarray(a, dtype=np.float32), dtype=np.float64)
     if dtype == "bf16":
         return round_bf16(a)
     raise ValueError(dtype)
@@ -60,6 +60,18 @@ def to_storage(a, dtype: str) -> np.ndarray:
 def normal(shape, seed: int, std: float = 1.0, mean: float = 0.0, dtype: str = "f32") -> np.ndarray:
     g = rng(seed)
     return to_storage(g.normal(mean, std, size=shape), dtype)
+
+
+def normal_bf16_bits(shape, seed: int, std: float = 1.0, chunk_rows: int = 512) -> np.ndarray:
+    """N(0, std) draws (float32) rounded to bfloat16, returned as uint16 bit patterns; drawn
+    in row chunks so host memory stays bounded for multi-GB tensors."""
+    g = rng(seed)
+    out = np.empty(shape, dtype=np.uint16)
+    for r0 in range(0, shape[0], chunk_rows):
+        n = min(chunk_rows, shape[0] - r0)
+        blk = g.standard_normal((n,) + tuple(shape[1:]), dtype=np.float32) * np.float32(std)
+        out[r0:r0 + n] = bf16_bits(blk)
+    return out
 
 
 def uniform_ids(n: int, vocab: int, seed: int) -> np.ndarray:

@@ -18,7 +18,7 @@ DEV = "cuda"
 
 
 def dev(a, dtype="f32"):
-    t = torch.tensor(np.asarray(a, dtype=np.float32))
+    t = torch.tensor(np.ascontiguousarray(a, dtype=np.float32)).contiguous()
     if dtype == "bf16":
         t = t.to(torch.bfloat16)
     return t.to(DEV)

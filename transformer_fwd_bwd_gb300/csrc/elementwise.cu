@@ -349,6 +349,16 @@ int xt_accumulate(void* dst, int dt_dst, const void* src, int dt_src, int64_t n,
                              "xt_accumulate");
 }
 
+int xt_convert(void* dst, int dt_dst, const void* src, int dt_src, int64_t n, void* stream) {
+  XT_CHECK_N(n);
+  XT_CHECK_DT(dt_dst);
+  XT_CHECK_DT(dt_src);
+  XT_REQUIRE(n == 0 || (dst && src), "xt_convert: NULL pointer");
+  EwArgs g = ew_args(src, nullptr, nullptr, dst, nullptr, n);
+  g.alpha = 1.f;
+  return ew_dispatch<EW_SCALE>(dt_src, dt_dst, g, stream, "xt_convert");
+}
+
 int xt_add_fwd(const void* a, const void* b, void* y, int64_t n, int dt, void* stream) {
   XT_CHECK_N(n);
   XT_CHECK_DT(dt);

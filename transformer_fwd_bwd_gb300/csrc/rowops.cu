@@ -350,21 +350,35 @@ __global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, c
 
 // ============================================================================== column sums
 
-// part[nb][cols] → out[cols] (dtype TO), summing partial rows in order.
+// part[nb][cols] → out[cols] (dtype TO).  Block (32, 32): threadIdx.x picks a column of a
+// 32-column slab, threadIdx.y a slice of partial rows (y, y+32, ...); the 32 slice sums are
+// then added in a fixed tree order, so the result does not depend on timing.
 template <typename TO>
-__global__ void colsum_finalize(const float* __restrict__ part, int nb, int64_t cols, TO* out, int acc) {
-  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < cols; c += int64_t(gridDim.x) * blockDim.x) {
-    float s = 0.f;
-    for (int b = 0; b < nb; ++b) s += part[int64_t(b) * cols + c];
-    if (acc) s += to_f(out[c]);
-    out[c] = from_f<TO>(s);
+__global__ void __launch_bounds__(1024) colsum_finalize(const float* __restrict__ part, int nb, int64_t cols, TO* out,
+                                                       int acc) {
+  __shared__ float red[32][33];
+  const int64_t c = int64_t(blockIdx.x) * 32 + threadIdx.x;
+  float s = 0.f;
+  if (c < cols)
+    for (int b = threadIdx.y; b < nb; b += 32) s += part[int64_t(b) * cols + c];
+  red[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 16; w > 0; w >>= 1) {
+    if (threadIdx.y < w) red[threadIdx.y][threadIdx.x] += red[threadIdx.y + w][threadIdx.x];
+    __syncthreads();
+  }
+  if (threadIdx.y == 0 && c < cols) {
+    float r = red[0][threadIdx.x];
+    if (acc) r += to_f(out[c]);
+    out[c] = from_f<TO>(r);
   }
 }
 
 static int finalize(const float* part, int nb, int64_t cols, void* out, int dt, int acc, cudaStream_t s) {
-  const int grid = int(ceil_div(cols, 256));
-  if (dt == XT_F32) colsum_finalize<float><<<grid, 256, 0, s>>>(part, nb, cols, static_cast<float*>(out), acc);
-  else colsum_finalize<bf16><<<grid, 256, 0, s>>>(part, nb, cols, static_cast<bf16*>(out), acc);
+  const unsigned grid = unsigned(ceil_div(cols, 32));
+  const dim3 block(32, 32);
+  if (dt == XT_F32) colsum_finalize<float><<<grid, block, 0, s>>>(part, nb, cols, static_cast<float*>(out), acc);
+  else colsum_finalize<bf16><<<grid, block, 0, s>>>(part, nb, cols, static_cast<bf16*>(out), acc);
   return check_launch("column-sum finalize");
 }
 

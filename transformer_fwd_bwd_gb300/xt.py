@@ -69,6 +69,7 @@ _SIGS = {
     "xt_profile_gemm": [_I],
     "xt_profile_gemm_read": [C.POINTER(C.c_double), C.POINTER(C.c_float), _I, C.POINTER(C.c_int)],
     "xt_accumulate": [_VP, _I, _VP, _I, _I64, _VP],
+    "xt_convert": [_VP, _I, _VP, _I, _I64, _VP],
     "xt_add_fwd": [_VP, _VP, _VP, _I64, _I, _VP],
     "xt_add_bwd": [_VP, _VP, _VP, _I64, _I, _I, _I, _VP],
     "xt_mul_fwd": [_VP, _VP, _VP, _I64, _I, _VP],
@@ -185,13 +186,18 @@ def dt(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def ptr(t):
+def ptr(t, contiguous=True):
+    """Device address of `t`.  Entry points that take their sizes from a tensor read it as
+    dense row-major, so such tensors must be contiguous; strided views (matmul operands,
+    swiglu column blocks) pass contiguous=False and describe their layout explicitly."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
     if not t.is_cuda:
         raise ValueError("libxt takes CUDA tensors")
+    if contiguous and not t.is_contiguous():
+        raise ValueError("libxt reads this tensor as dense row-major: pass a contiguous tensor")
     return t.data_ptr()
 
 
@@ -232,6 +238,10 @@ def version() -> str:
 
 def xt_accumulate(dst, src, s=None):
     call("xt_accumulate", ptr(dst), dt(dst), ptr(src), dt(src), src.numel(), stream(s))
+
+
+def xt_convert(dst, src, s=None):
+    call("xt_convert", ptr(dst), dt(dst), ptr(src), dt(src), src.numel(), stream(s))
 
 
 def xt_add_fwd(a, b, y, s=None):
@@ -299,14 +309,19 @@ def xt_gelu_bwd(d, x, dx, acc=0, s=None):
 
 def xt_swiglu_fwd(g, u, y, s=None):
     rows, cols = g.shape
-    call("xt_swiglu_fwd", ptr(g), ptr(u), g.stride(0), ptr(y), y.stride(0), rows, cols, dt(g), stream(s))
+    for t in (g, u, y):
+        assert t.stride(1) == 1, "swiglu operands need unit column stride"
+    call("xt_swiglu_fwd", ptr(g, False), ptr(u, False), g.stride(0), ptr(y, False), y.stride(0), rows, cols, dt(g),
+         stream(s))
 
 
 def xt_swiglu_bwd(d, g, u, dg, du, acc=0, s=None):
     rows, cols = g.shape
     assert u.stride(0) == g.stride(0) and du.stride(0) == dg.stride(0)
-    call("xt_swiglu_bwd", ptr(d), d.stride(0), ptr(g), ptr(u), g.stride(0), ptr(dg), ptr(du), dg.stride(0), rows,
-         cols, dt(g), acc, stream(s))
+    for t in (d, g, u, dg, du):
+        assert t.stride(1) == 1, "swiglu operands need unit column stride"
+    call("xt_swiglu_bwd", ptr(d, False), d.stride(0), ptr(g, False), ptr(u, False), g.stride(0), ptr(dg, False),
+         ptr(du, False), dg.stride(0), rows, cols, dt(g), acc, stream(s))
 
 
 def xt_rms_norm_fwd(x, gamma, y, inv_rms, eps, s=None):
@@ -343,11 +358,11 @@ def xt_rope_table(table, S, hd, base, pos_offset=0, s=None):
 
 
 def xt_rope_fwd(x, y, table, B, S, H, hd, ld, s=None):
-    call("xt_rope_fwd", ptr(x), ptr(y), ptr(table), B, S, H, hd, ld, dt(x), stream(s))
+    call("xt_rope_fwd", ptr(x, False), ptr(y, False), ptr(table), B, S, H, hd, ld, dt(x), stream(s))
 
 
 def xt_rope_bwd(d, dx, table, B, S, H, hd, ld, acc=0, s=None):
-    call("xt_rope_bwd", ptr(d), ptr(dx), ptr(table), B, S, H, hd, ld, dt(d), acc, stream(s))
+    call("xt_rope_bwd", ptr(d, False), ptr(dx, False), ptr(table), B, S, H, hd, ld, dt(d), acc, stream(s))
 
 
 def xt_softmax_fwd(x, y, causal=0, q_len=0, s=None):
@@ -434,14 +449,15 @@ def xt_matmul_fwd(desc, A, B, Cm, ws=None, s=None):
     n = ws_bytes("xt_matmul_workspace_size", C.byref(desc))
     if n and ws is None:
         ws = workspace(n, Cm.device)
-    call("xt_matmul_fwd", C.byref(desc), ptr(A), ptr(B), ptr(Cm), ptr(ws), ws.numel() if ws is not None else 0,
-         stream(s))
+    call("xt_matmul_fwd", C.byref(desc), ptr(A, False), ptr(B, False), ptr(Cm, False), ptr(ws),
+         ws.numel() if ws is not None else 0, stream(s))
 
 
 def xt_matmul_bwd(desc, A, B, dC, dA, dB, acc_a=0, acc_b=0, ws=None, s=None):
     n = ws_bytes("xt_matmul_bwd_workspace_size", C.byref(desc))
     if n and ws is None:
         ws = workspace(n, dC.device)
-    call("xt_matmul_bwd", C.byref(desc), ptr(A), ptr(B), ptr(dC), ptr(dA), ptr(dB),
+    call("xt_matmul_bwd", C.byref(desc), ptr(A, False), ptr(B, False), ptr(dC, False), ptr(dA, False),
+         ptr(dB, False),
          dt(dA) if dA is not None else XT_F32, dt(dB) if dB is not None else XT_F32, acc_a, acc_b, ptr(ws),
          ws.numel() if ws is not None else 0, stream(s))
