@@ -77,10 +77,11 @@ uint64_t xt_launch_count(void);
  * bracketed by CUDA events recorded on their own stream, each tagged with its algorithmic
  * FLOPs (2·M·N·K per batch; for the causal modes only the unmasked half).  Events are
  * created by this call, not during the launches; capacity 0 disables.  xt_profile_gemm_read
- * waits for the recorded events and copies up to max_records (flops, milliseconds) pairs
- * into host arrays; *n receives the number recorded. */
+ * waits for the recorded events and copies up to max_records records into host arrays:
+ * flops, milliseconds, and (if shapes != NULL) 8 ints per record: M, N, K, batches, tile
+ * width BN, A MN-major, B MN-major, causal mode.  *n receives the number recorded. */
 int xt_profile_gemm(int capacity);
-int xt_profile_gemm_read(double* flops, float* ms, int max_records, int* n);
+int xt_profile_gemm_read(double* flops, float* ms, int* shapes, int max_records, int* n);
 
 /* ---------------------------------------------------------------------------------
  * Gradient accumulation ([AE] § 梯度累加, push_grad/accumulate): dst[i] += src[i].

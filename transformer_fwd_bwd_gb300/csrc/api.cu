@@ -20,6 +20,7 @@ std::atomic<uint64_t> g_launches{0};
 struct GemmRecord {
   double flops;
   cudaEvent_t start, stop;
+  int shape[8];
 };
 std::mutex g_prof_mu;
 std::vector<cudaEvent_t> g_ev_pool;
@@ -75,10 +76,11 @@ int num_sms() {
   return g_sms[dev];
 }
 
-bool gemm_profile_begin(cudaStream_t s, double flops, void** token) {
+bool gemm_profile_begin(cudaStream_t s, double flops, const int* shape, void** token) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (!g_prof_on || g_ev_next + 2 > g_ev_pool.size()) return false;
-  GemmRecord r{flops, g_ev_pool[g_ev_next], g_ev_pool[g_ev_next + 1]};
+  GemmRecord r{flops, g_ev_pool[g_ev_next], g_ev_pool[g_ev_next + 1], {}};
+  for (int i = 0; i < 8; ++i) r.shape[i] = shape[i];
   g_ev_next += 2;
   cudaEventRecord(r.start, s);
   g_records.push_back(r);
@@ -111,7 +113,7 @@ int xt_profile_gemm(int capacity) {
   return XT_OK;
 }
 
-int xt_profile_gemm_read(double* flops, float* ms, int max_records, int* n) {
+int xt_profile_gemm_read(double* flops, float* ms, int* shapes, int max_records, int* n) {
   XT_REQUIRE(n != nullptr, "xt_profile_gemm_read: n is NULL");
   std::lock_guard<std::mutex> lk(g_prof_mu);
   const int cnt = int(g_records.size());
@@ -122,6 +124,8 @@ int xt_profile_gemm_read(double* flops, float* ms, int max_records, int* n) {
     cudaEventElapsedTime(&t, g_records[i].start, g_records[i].stop);
     if (flops) flops[i] = g_records[i].flops;
     if (ms) ms[i] = t;
+    if (shapes)
+      for (int j = 0; j < 8; ++j) shapes[8 * i + j] = g_records[i].shape[j];
   }
   return XT_OK;
 }

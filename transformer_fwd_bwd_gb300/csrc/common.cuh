@@ -24,7 +24,7 @@ uint32_t* errflag();
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
 // GEMM timing hooks (active only between xt_profile_gemm(capacity > 0) and (0)).
-bool gemm_profile_begin(cudaStream_t s, double flops, void** token);
+bool gemm_profile_begin(cudaStream_t s, double flops, const int* shape, void** token);
 void gemm_profile_end(cudaStream_t s, void* token);
 
 #define XT_REQUIRE(cond, ...)                                      \

@@ -122,7 +122,8 @@ int run(const Problem& pb, cudaStream_t s) {
   if (pb.causal == 1) flops = 2.0 * double(pb.K) * double(pb.M) * double(pb.M + 1) / 2.0 * batches;
   if (pb.causal >= 2) flops = 2.0 * double(pb.N) * double(pb.M) * double(pb.M + 1) / 2.0 * batches;
   void* tok = nullptr;
-  const bool prof = gemm_profile_begin(s, flops, &tok);
+  const int shape[8] = {p.M, p.N, p.K, p.batches, bn, int(amn), int(bmn), p.causal};
+  const bool prof = gemm_profile_begin(s, flops, shape, &tok);
   const int st = tf32 ? launch_tf32(bn, amn, bmn, ta, tb, p, grid, s) : launch_bf16(bn, amn, bmn, ta, tb, p, grid, s);
   if (prof) gemm_profile_end(s, tok);
   return st;

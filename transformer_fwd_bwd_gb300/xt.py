@@ -67,7 +67,8 @@ _SIGS = {
     "xt_get_device_errors": [C.POINTER(C.c_uint32), _VP],
     "xt_clear_device_errors": [_VP],
     "xt_profile_gemm": [_I],
-    "xt_profile_gemm_read": [C.POINTER(C.c_double), C.POINTER(C.c_float), _I, C.POINTER(C.c_int)],
+    "xt_profile_gemm_read": [C.POINTER(C.c_double), C.POINTER(C.c_float), C.POINTER(C.c_int), _I,
+                             C.POINTER(C.c_int)],
     "xt_accumulate": [_VP, _I, _VP, _I, _I64, _VP],
     "xt_convert": [_VP, _I, _VP, _I, _I64, _VP],
     "xt_add_fwd": [_VP, _VP, _VP, _I64, _I, _VP],
@@ -155,15 +156,20 @@ def profile_gemm(capacity: int):
     call("xt_profile_gemm", int(capacity))
 
 
-def profile_gemm_read(max_records: int = 1 << 16):
-    """Returns (flops, ms) numpy arrays of the GEMM launches recorded since profile_gemm()."""
+def profile_gemm_read(max_records: int = 1 << 16, shapes: bool = False):
+    """Returns (flops, ms) numpy arrays of the GEMM launches recorded since profile_gemm(),
+    plus an [n, 8] int array (M, N, K, batches, BN, A MN-major, B MN-major, causal) if shapes."""
     import numpy as np
     fl = (C.c_double * max_records)()
     ms = (C.c_float * max_records)()
+    sh = (C.c_int * (8 * max_records))()
     n = C.c_int(0)
-    call("xt_profile_gemm_read", fl, ms, max_records, C.byref(n))
+    call("xt_profile_gemm_read", fl, ms, sh, max_records, C.byref(n))
     k = min(n.value, max_records)
-    return np.array(fl[:k]), np.array(ms[:k], dtype=np.float64)
+    out = (np.array(fl[:k]), np.array(ms[:k], dtype=np.float64))
+    if shapes:
+        out = out + (np.array(sh[:8 * k], dtype=np.int64).reshape(k, 8),)
+    return out
 
 
 def _check(code):
