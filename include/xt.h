@@ -155,6 +155,26 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
                     void* dx, void* dgamma, int64_t rows, int64_t cols, int dt, int dt_dx,
                     int dt_param, void* ws, int acc_dx, int acc_param, void* stream);
 
+/* Allocation-free variant of xt_rms_norm_bwd (the pages have no counterpart: it exists for
+ * callers, not for the method).  Some callers cannot allocate device memory where they run
+ * the backward: for example a plug-in inside a host framework that owns all device memory
+ * through its own pool and hands out no scratch, or a latency-critical loop in which
+ * cudaMalloc (which can synchronise the device) is not allowed.  They still pass d, x, gamma,
+ * inv_rms, dx and dgamma as for xt_rms_norm_bwd; the dγ partial sums go to a fixed scratch
+ * array inside libxt instead of a ws buffer.  Results equal xt_rms_norm_bwd's up to the
+ * summation order of dγ (at most 128 partial rows here).
+ *   - Limit: cols ≤ 8192 (else XT_ERR_UNSUPPORTED); the scratch is 128 × 8192 floats (4 MiB),
+ *     held by every GPU that loads libxt until the process exits.
+ *   - The first call on each device looks the scratch's device address up with that device
+ *     current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.  Nothing in the
+ *     scratch needs to start at zero: each call overwrites every partial row it reads.
+ *   - All calls share the one array: calls that overlap on the GPU (several streams or host
+ *     threads) race on it and must be serialised by the caller. */
+int xt_rms_norm_bwd_noalloc(const void* d, const void* x, const void* gamma, const float* inv_rms,
+                            void* dx, void* dgamma, int64_t rows, int64_t cols, int dt, int dt_dx,
+                            int dt_param, int acc_dx, int acc_param, void* stream);
+
 /* LayerNorm (standard definition; [BP] § kernel-pair table k_layernorm_fwd/bwd and
  * § Sparade tensorer: mean and variance saved — saved here as mean and rstd):
  * μ = mean x, var = mean (x−μ)², rstd = 1/√(var+eps), x̂ = (x−μ)·rstd, y = x̂·γ + β.

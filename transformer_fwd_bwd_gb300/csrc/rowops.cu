@@ -6,6 +6,8 @@
 // vectors, so one global read feeds the reductions and the outputs.  Several row groups
 // share a block when rows are short.  Column reductions (dγ, dβ, dbias) are deterministic:
 // per-block partial rows in the workspace, then one ordered pass.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace xt {
@@ -881,6 +883,77 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
                                    inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_rms_norm_bwd"));
+  if (dgamma) return finalize(part, nb, cols, dgamma, dt_param, acc_param, s);
+  return XT_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free RMSNorm backward.  Its per-block dγ partial rows live in this file-scope
+// device array instead of caller workspace; every GPU that loads libxt holds the 4 MiB until
+// the process exits.  Host code may not hand the array's name to a kernel (on the host it is
+// only a stand-in for the symbol): the device address is looked up per device with
+// cudaGetSymbolAddress, once, and cached.
+namespace {
+constexpr int kNoAllocMaxBlocks = 128;
+constexpr int64_t kNoAllocMaxCols = 8192;
+__device__ __align__(256) float g_rms_bwd_scratch[kNoAllocMaxBlocks * kNoAllocMaxCols];
+constexpr int kNoAllocDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocDevices] = {};
+
+int noalloc_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocDevices)
+    return fail(XT_ERR_CUDA, "xt_rms_norm_bwd_noalloc: no usable current device");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_rms_bwd_scratch);
+    if (e != cudaSuccess)
+      return fail(XT_ERR_CUDA, "xt_rms_norm_bwd_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return XT_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int xt_rms_norm_bwd_noalloc(const void* d, const void* x, const void* gamma, const float* inv_rms, void* dx,
+                            void* dgamma, int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, int acc_dx,
+                            int acc_param, void* stream) {
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_dx) && valid_dtype(dt_param), "xt_rms_norm_bwd_noalloc: bad dtype");
+  XT_REQUIRE(dt_dx == dt || (dt == XT_BF16 && dt_dx == XT_F32), "xt_rms_norm_bwd_noalloc: dx dtype must be dt or f32");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_rms_norm_bwd_noalloc: bad sizes");
+  XT_REQUIRE(rows == 0 || (d && x && gamma && inv_rms), "xt_rms_norm_bwd_noalloc: NULL input");
+  if (cols > kNoAllocMaxCols)
+    return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd_noalloc: cols = %lld exceeds the fixed scratch limit of %lld",
+                (long long)cols, (long long)kNoAllocMaxCols);
+  cudaStream_t s = as_stream(stream);
+  if (rows == 0) {
+    if (dgamma && !acc_param)
+      if (cudaMemsetAsync(dgamma, 0, size_t(cols) * dtype_size(dt_param), s) != cudaSuccess)
+        return check_launch("xt_rms_norm_bwd_noalloc");
+    return XT_OK;
+  }
+  float* part = nullptr;
+  if (dgamma) XT_TRY(noalloc_scratch(&part));
+  const bool vec = rows_vec_ok(cols, dt, {d, x, gamma, dx});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1, kBwdMaxTpr);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd_noalloc: row too long (%lld)", (long long)cols);
+  int nb = bwd_blocks(rows, pl.rpb);
+  if (nb > kNoAllocMaxBlocks) nb = kNoAllocMaxBlocks;   // each block loops over its share of rows
+  const size_t smem = (32 + size_t(cols)) * sizeof(float);
+  XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
+    auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
+                                   inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
+  });
+  XT_TRY(check_launch("xt_rms_norm_bwd_noalloc"));
   if (dgamma) return finalize(part, nb, cols, dgamma, dt_param, acc_param, s);
   return XT_OK;
 }

@@ -92,6 +92,7 @@ _SIGS = {
     "xt_norm_bwd_workspace_size": [_I64, _I64, _SZP],
     "xt_rms_norm_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _F, _I, _VP],
     "xt_rms_norm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP, _I, _I, _VP],
+    "xt_rms_norm_bwd_noalloc": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _I, _I, _VP],
     "xt_layernorm_fwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _F, _I, _VP],
     "xt_layernorm_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP, _I, _I, _VP],
     "xt_rope_table": [_VP, _I, _I, _D, _I, _VP],
@@ -342,6 +343,14 @@ def xt_rms_norm_bwd(d, x, gamma, inv_rms, dx, dgamma, acc_dx=0, acc_param=0, ws=
     call("xt_rms_norm_bwd", ptr(d), ptr(x), ptr(gamma), ptr(inv_rms), ptr(dx), ptr(dgamma), rows, cols, dt(x),
          dt(dx) if dx is not None else dt(x), dt(dgamma) if dgamma is not None else dt(x), ptr(ws), acc_dx,
          acc_param, stream(s))
+
+
+def xt_rms_norm_bwd_noalloc(d, x, gamma, inv_rms, dx, dgamma, acc_dx=0, acc_param=0, s=None):
+    """Same result as xt_rms_norm_bwd without a workspace argument (scratch is fixed in libxt)."""
+    rows, cols = x.shape
+    call("xt_rms_norm_bwd_noalloc", ptr(d), ptr(x), ptr(gamma), ptr(inv_rms), ptr(dx), ptr(dgamma), rows, cols,
+         dt(x), dt(dx) if dx is not None else dt(x), dt(dgamma) if dgamma is not None else dt(x), acc_dx, acc_param,
+         stream(s))
 
 
 def xt_layernorm_fwd(x, gamma, beta, y, mean, rstd, eps, s=None):
