@@ -175,3 +175,27 @@ def test_matmul_alignment_rejected():
     with pytest.raises(xt.XtError) as ei:
         xt.xt_matmul_fwd(d, A, A, C)
     assert ei.value.code == xt.XT_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("ab", ["bf16", "f32"])
+@pytest.mark.parametrize("c", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(768, 768, 8192), (768, 3072, 8192), (200, 136, 4096)])
+def test_matmul_split_k(ab, c, M, N, K):
+    """Weight-gradient shapes (small M·N, long K) take the deterministic K split: partial
+    tiles in workspace slices, then a fixed-order reduction into C (with += here)."""
+    A = synth.normal((K, M), 56, dtype=ab)   # stored [K, M]: dW = xᵀ dy layout
+    B = synth.normal((K, N), 57, dtype=ab)
+    C0 = synth.normal((M, N), 58, dtype=c)
+    d = xt.matmul_desc(M, N, K, trans_a=1, dtype_ab=xt.XT_BF16 if ab == "bf16" else xt.XT_F32,
+                       dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, accumulate=1, alpha=0.5)
+    outs = []
+    for _ in range(2):
+        Cd = dev(C0, c)
+        xt.xt_matmul_fwd(d, dev(A, ab), dev(B, ab), Cd)
+        sync()
+        outs.append(host(Cd))
+    want = C0 + 0.5 * (A.T @ B)
+    tol = bound(ab, c) if c == "f32" else 8e-3
+    assert norm_err(outs[0], want) <= tol
+    assert np.array_equal(outs[0], outs[1]), "K split is not deterministic"
+    assert xt.device_errors() == 0

@@ -2,6 +2,7 @@
 // matmul C ABI ([AE] op table row matmul: C = A@B; dA = d@Bᵀ, dB = Aᵀ@d).
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "gemm.cuh"
@@ -62,69 +63,159 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn) {
   return XT_OK;
 }
 
-// Tile width: fewest "wave-weighted" columns, with the lower per-FLOP efficiency of narrow
-// tiles (shared-memory operand bandwidth) taken into account.
-static int choose_bn(bool tf32, int64_t M, int64_t N, int64_t batches, int causal) {
+// Tile width and K split from a per-tile time model: rounds of persistent CTAs × the time of
+// one tile at the SM's share of the tensor peak, scaled by the measured relative efficiency of
+// the tile width (narrow tiles move more operand bytes per FLOP), plus for a K split the
+// fixed-order reduction of the partial slices.  The split is used for single-batch,
+// non-causal problems whose tile count leaves SMs idle (the M = d weight gradients).
+static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 128 ? 0.55 : 0.35; }
+
+Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split) {
   const int cands_bf16[3] = {64, 128, 256};
   const int cands_tf32[2] = {64, 128};
   const int* c = tf32 ? cands_tf32 : cands_bf16;
   const int nc = tf32 ? 2 : 3;
   const int sms = num_sms();
-  int best = c[0];
-  double best_cost = 1e300;
+  const int bk = tf32 ? 32 : 64;
+  const double per_sm = tf32 ? 5.6e12 : 11.2e12;
+  Choice best{c[0], 1};
+  double best_t = 1e300;
   for (int i = 0; i < nc; ++i) {
     const int bn = c[i];
     if (i > 0 && c[i - 1] >= N) break;  // wider tiles only add padding
     int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn) * batches;
     if (causal == 1) tiles = (tiles + 1) / 2;
-    const double waves = double(ceil_div(tiles, sms));
-    const double eff = bn >= 256 ? 1.0 : bn >= 128 ? 0.9 : 0.7;
-    const double cost = waves * double(bn) / eff;
-    if (cost < best_cost * 0.999) {
-      best_cost = cost;
-      best = bn;
+    for (int s = 1; s <= 8; s *= 2) {
+      if (s > 1 && (!allow_split || batches != 1 || causal != 0 || N % 4 != 0)) break;
+      if (s > 1 && ceil_div(K, bk) < 4 * s) break;
+      const double rounds = double(ceil_div(tiles * s, sms));
+      const double t_tile = 2.0 * BM * bn * (double(K) / s) / (per_sm * tile_eff(bn)) + 1.5e-6;
+      double t = rounds * t_tile;
+      if (s > 1) t += double(s + 1) * double(M) * double(N) * 4.0 / 5e12 + 4e-6;
+      if (t < best_t * 0.999) {
+        best_t = t;
+        best = Choice{bn, s};
+      }
     }
   }
   return best;
 }
 
+size_t split_bytes(const Choice& c, int64_t M, int64_t N) {
+  if (c.splits <= 1) return 0;
+  return (size_t(c.splits) * size_t(M) * size_t(N) * 4 + 255) & ~size_t(255);
+}
+
+// C (+)= Σ_s part[s] in split order (deterministic); part is [splits][M][N] float32.
+template <typename TC>
+__global__ void splitk_reduce(const float* __restrict__ part, int splits, int64_t M, int64_t N, TC* C, int64_t ldc,
+                              int acc) {
+  const int64_t n4 = N / 4, total = M * n4, slice = M * N;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t m = i / n4, c = (i - m * n4) * 4;
+    float4 a = *reinterpret_cast<const float4*>(part + m * N + c);
+    for (int k = 1; k < splits; ++k) {
+      const float4 b = *reinterpret_cast<const float4*>(part + k * slice + m * N + c);
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    TC* out = C + m * ldc + c;
+    float v[4] = {a.x, a.y, a.z, a.w};
+    if (acc)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] += to_f(out[e]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) out[e] = from_f<TC>(v[e]);
+  }
+}
+
+// An output as the epilogue's TMA stores see it: boxes of 32 rows × 128 bytes, 128-byte swizzle.
+static int make_output_map(CUtensorMap* tm, void* base, bool bf16, int64_t M, int64_t N, int64_t ldc, int bi, int bo,
+                           int64_t s_inner, int64_t s_outer) {
+  auto enc = encode_fn();
+  if (!enc) return fail(XT_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const int64_t e = bf16 ? 2 : 4;
+  const int64_t row_bytes = ldc * e;
+  cuuint64_t dims[4] = {cuuint64_t(N), cuuint64_t(M), cuuint64_t(bi), cuuint64_t(bo)};
+  cuuint64_t strides[3] = {cuuint64_t(row_bytes), cuuint64_t(bi > 1 ? s_inner * e : row_bytes),
+                           cuuint64_t(bo > 1 ? s_outer * e : row_bytes)};
+  cuuint32_t box[4] = {uint32_t(128 / e), 32, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(XT_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", int(r));
+  return XT_OK;
+}
+
 int run(const Problem& pb, cudaStream_t s) {
   const bool tf32 = pb.tf32;
-  const int bn = choose_bn(tf32, pb.M, pb.N, int64_t(pb.batch_outer) * pb.batch_inner, pb.causal);
-  CUtensorMap ta, tb;
+  const int64_t batches = int64_t(pb.batch_outer) * pb.batch_inner;
+  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, true);
+  if (ch.splits > 1 && (pb.split_ws == nullptr || split_bytes(ch, pb.M, pb.N) > pb.split_ws_bytes))
+    ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false);
+  const int bn = ch.bn;
+  const bool split = ch.splits > 1;
+  CUtensorMap ta, tb, tc;
   XT_TRY(make_operand_map(&ta, pb.A, tf32, BM));
   XT_TRY(make_operand_map(&tb, pb.B, tf32, bn));
+  // TMA epilogue for every output except a bf16 C that is accumulated into (TMA reduce-add is
+  // used for float32 only; bf16 accumulation keeps the direct read-modify-write stores).  A K
+  // split stores float32 partial tiles into [splits][M][N] slices instead.
+  const bool tma_store = split || !(pb.c_bf16 && pb.accumulate);
+  memset(&tc, 0, sizeof(tc));
+  if (split)
+    XT_TRY(make_output_map(&tc, pb.split_ws, false, pb.M, pb.N, pb.N, ch.splits, 1, pb.M * pb.N, 0));
+  else if (tma_store)
+    XT_TRY(make_output_map(&tc, pb.C, pb.c_bf16, pb.M, pb.N, pb.ldc, pb.batch_inner, pb.batch_outer, pb.sc_inner,
+                           pb.sc_outer));
   Params p{};
   p.M = int(pb.M);
   p.N = int(pb.N);
   p.K = int(pb.K);
   p.num_m = int(ceil_div(pb.M, BM));
   p.num_n = int(ceil_div(pb.N, bn));
-  p.batch_inner = pb.batch_inner;
-  p.batches = pb.batch_inner * pb.batch_outer;
+  p.batch_inner = split ? ch.splits : pb.batch_inner;
+  p.batches = split ? ch.splits : pb.batch_inner * pb.batch_outer;
+  p.splitk = ch.splits;
+  p.kb_per_split = int(ceil_div(ceil_div(pb.K, tf32 ? 32 : 64), ch.splits));
   p.causal = pb.causal;
-  p.accumulate = pb.accumulate;
-  p.c_bf16 = pb.c_bf16;
+  p.accumulate = split ? 0 : pb.accumulate;
+  p.c_bf16 = split ? 0 : pb.c_bf16;
+  p.tma_store = tma_store ? 1 : 0;
   p.alpha = pb.alpha;
   p.C = pb.C;
   p.ldc = pb.ldc;
   p.sc_inner = pb.sc_inner;
   p.sc_outer = pb.sc_outer;
   p.flag = errflag();
-  const int64_t tiles = int64_t(p.num_m) * p.num_n * p.batches;
+  const int64_t tiles = int64_t(p.num_m) * p.num_n * p.batches;  // a K split counts its slices
   if (tiles > int64_t(1) << 30) return fail(XT_ERR_UNSUPPORTED, "matmul: too many tiles");
   int grid = int(tiles < num_sms() ? tiles : num_sms());
   if (grid < 1) grid = 1;
   const bool amn = pb.A.mn_major, bmn = pb.B.mn_major;
   // algorithmic FLOPs: the unmasked work only for the causal modes
-  const double batches = double(p.batches);
-  double flops = 2.0 * double(pb.M) * double(pb.N) * double(pb.K) * batches;
-  if (pb.causal == 1) flops = 2.0 * double(pb.K) * double(pb.M) * double(pb.M + 1) / 2.0 * batches;
-  if (pb.causal >= 2) flops = 2.0 * double(pb.N) * double(pb.M) * double(pb.M + 1) / 2.0 * batches;
+  const double nb = double(batches);  // problem batches (a K split does not add work)
+  double flops = 2.0 * double(pb.M) * double(pb.N) * double(pb.K) * nb;
+  if (pb.causal == 1) flops = 2.0 * double(pb.K) * double(pb.M) * double(pb.M + 1) / 2.0 * nb;
+  if (pb.causal >= 2) flops = 2.0 * double(pb.N) * double(pb.M) * double(pb.M + 1) / 2.0 * nb;
   void* tok = nullptr;
-  const int shape[8] = {p.M, p.N, p.K, p.batches, bn, int(amn), int(bmn), p.causal};
+  const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, bn, int(amn), int(bmn),
+                        split ? 10 * ch.splits : p.causal};
   const bool prof = gemm_profile_begin(s, flops, shape, &tok);
-  const int st = tf32 ? launch_tf32(bn, amn, bmn, ta, tb, p, grid, s) : launch_bf16(bn, amn, bmn, ta, tb, p, grid, s);
+  int st = tf32 ? launch_tf32(bn, amn, bmn, ta, tb, tc, p, grid, s) : launch_bf16(bn, amn, bmn, ta, tb, tc, p, grid, s);
+  if (st == XT_OK && split) {
+    const int64_t work = pb.M * (pb.N / 4);
+    int64_t g = ceil_div(work, 256);
+    if (g > int64_t(num_sms()) * 8) g = int64_t(num_sms()) * 8;
+    const float* part = static_cast<const float*>(pb.split_ws);
+    if (pb.c_bf16)
+      splitk_reduce<bf16><<<int(g), 256, 0, s>>>(part, ch.splits, pb.M, pb.N, static_cast<bf16*>(pb.C), pb.ldc,
+                                                 pb.accumulate);
+    else
+      splitk_reduce<float><<<int(g), 256, 0, s>>>(part, ch.splits, pb.M, pb.N, static_cast<float*>(pb.C), pb.ldc,
+                                                  pb.accumulate);
+    st = check_launch("gemm K-split reduce");
+  }
   if (prof) gemm_profile_end(s, tok);
   return st;
 }
@@ -195,8 +286,12 @@ static gemm::Operand operand_b(const xt_matmul_desc* d, const void* B) {
 }
 
 static size_t matmul_ws(const xt_matmul_desc* d) {
-  if (d->dtype_ab != XT_F32 || d->M == 0 || d->N == 0 || d->K == 0) return 0;
-  return stage_bytes(operand_a(d, nullptr)) + stage_bytes(operand_b(d, nullptr));
+  if (d->M == 0 || d->N == 0 || d->K == 0) return 0;
+  size_t b = 0;
+  if (d->dtype_ab == XT_F32) b += stage_bytes(operand_a(d, nullptr)) + stage_bytes(operand_b(d, nullptr));
+  const gemm::Choice ch = gemm::choose(d->dtype_ab == XT_F32, d->M, d->N, d->K,
+                                       int64_t(d->batch_outer) * d->batch_inner, d->causal, true);
+  return b + gemm::split_bytes(ch, d->M, d->N);
 }
 
 // Validates and runs C[M,N] (+)= alpha · op(A) @ op(B) for one matmul descriptor.
@@ -245,13 +340,15 @@ static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, voi
   pb.batch_outer = d->batch_outer;
   pb.A = operand_a(d, A);
   pb.B = operand_b(d, B);
+  char* w = static_cast<char*>(ws);
+  size_t left = ws ? ws_bytes : 0;
   if (pb.tf32 && (pb.A.mn_major || pb.B.mn_major)) {
-    XT_REQUIRE(ws != nullptr || matmul_ws(d) == 0, "matmul: fp32 operands read MN-major need a workspace");
-    char* w = static_cast<char*>(ws);
-    size_t left = ws_bytes;
+    XT_REQUIRE(ws != nullptr, "matmul: fp32 operands read MN-major need a workspace");
     if (pb.A.mn_major) XT_TRY(stage_operand(pb.A, w, left, s));
     if (pb.B.mn_major) XT_TRY(stage_operand(pb.B, w, left, s));
   }
+  pb.split_ws = left ? w : nullptr;  // what remains holds K-split partials, if used
+  pb.split_ws_bytes = left;
   pb.C = C;
   pb.ldc = d->ldc;
   pb.sc_inner = d->stride_c_inner;

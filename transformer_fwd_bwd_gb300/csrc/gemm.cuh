@@ -30,17 +30,28 @@ struct Problem {
   float alpha;
   int accumulate;
   int causal;
+  void* split_ws;  // room for K-split partial tiles (may be null)
+  size_t split_ws_bytes;
 };
+
+// Tile width and K split chosen for a problem (see choose()).
+struct Choice {
+  int bn;
+  int splits;
+};
+Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split);
+size_t split_bytes(const Choice& c, int64_t M, int64_t N);
 
 int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn);
 int run(const Problem& pb, cudaStream_t s);
-int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
-                int grid, cudaStream_t s);
-int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
-                int grid, cudaStream_t s);
+int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const Params& p, int grid, cudaStream_t s);
+int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const Params& p, int grid, cudaStream_t s);
 
 template <bool TF32, int BN, bool A_MN, bool B_MN>
-int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, int grid, cudaStream_t s) {
+int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const Params& p, int grid,
+               cudaStream_t s) {
   auto k = gemm_kernel<TF32, BN, A_MN, B_MN>;
   constexpr int smem = Cfg<TF32, BN>::SMEM;
   static bool attr_set = false;  // per instantiation; idempotent if raced
@@ -49,7 +60,7 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, in
       return check_launch("gemm: shared memory attribute");
     attr_set = true;
   }
-  k<<<grid, kThreads, smem, s>>>(ta, tb, p);
+  k<<<grid, kThreads, smem, s>>>(ta, tb, tc, p);
   return check_launch("gemm kernel");
 }
 

@@ -5,7 +5,9 @@
 // Roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 allocates TMEM and its
 // lane 0 issues the MMAs; warps 2..5 drain the accumulator (tcgen05.ld) and store C.
 // TMEM holds two accumulators of BN fp32 columns so the epilogue of tile i overlaps the
-// MMAs of tile i+1.
+// MMAs of tile i+1.  Each epilogue warp stages its 32 rows × 128 bytes of C in a
+// double-buffered, 128-byte-swizzled shared-memory tile and writes it with a TMA bulk tensor
+// store (for accumulation into fp32 C: a TMA reduce-add, performed in L2 without reading C).
 //
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // XT_DEVERR_TIMEOUT in the device flag, every role stops issuing work, the producer waits
@@ -27,9 +29,12 @@ struct Params {
   int M, N, K;
   int num_m, num_n;
   int batch_inner, batches;  // batches = outer × inner
+  int splitk;                // > 1: batch_inner is the K split; partial tiles go to C slices
+  int kb_per_split;
   int causal;
   int accumulate;
   int c_bf16;
+  int tma_store;  // 1: epilogue writes through TMA (C described by tmC); 0: direct stores
   float alpha;
   void* C;
   int64_t ldc, sc_inner, sc_outer;
@@ -87,6 +92,30 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// Shared → global tensor store / reduce-add of one box; completion tracked by bulk groups.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* tm, uint32_t src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most one committed bulk group is still reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -174,12 +203,14 @@ struct Cfg {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
+  static constexpr int STAGING_BYTES = 4 * 2 * 4096;  // 4 epilogue warps × 2 buffers × 32 rows × 128 B
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
 };
 
 struct TileInfo {
   int m0, n0, zi, zo, kb_begin, kb_end;
+  int ozi, ozo;  // batch coordinates of the operands (0 for a K split)
   bool skip;
 };
 
@@ -203,6 +234,15 @@ __device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
   } else if (p.causal == 3) {
     ti.kb_begin = ti.m0 / BK;
   }
+  ti.ozi = ti.zi;
+  ti.ozo = ti.zo;
+  if (p.splitk > 1) {  // K split: zi selects the range of K blocks and the output slice
+    ti.kb_begin = ti.zi * p.kb_per_split;
+    const int e = ti.kb_begin + p.kb_per_split;
+    if (e < ti.kb_end) ti.kb_end = e;
+    ti.ozi = 0;
+    ti.ozo = 0;
+  }
   ti.skip = false;
   (void)nb;
   return ti;
@@ -210,7 +250,8 @@ __device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
 
 template <bool TF32, int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const Params p) {
   using C_ = Cfg<TF32, BN>;
   constexpr int BK = C_::BK, ATOM = C_::ATOM, UK = C_::UK, STAGES = C_::STAGES;
   constexpr uint32_t IDESC = instr_desc<TF32, BN, A_MN, B_MN>();
@@ -218,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C_::STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * C_::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C_::STAGING_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -242,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (p.tma_store) prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TCOLS);
@@ -286,16 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_s = a_s + C_::A_BYTES;
           const int k0 = kb * BK;
           if constexpr (!A_MN) {
-            tma_load_4d(a_s, &tmA, fb, k0, ti.m0, ti.zi, ti.zo);
+            tma_load_4d(a_s, &tmA, fb, k0, ti.m0, ti.ozi, ti.ozo);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / ATOM; ++j) tma_load_4d(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.zi, ti.zo);
+            for (int j = 0; j < BM / ATOM; ++j)
+              tma_load_4d(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.ozi, ti.ozo);
           }
           if constexpr (!B_MN) {
-            tma_load_4d(b_s, &tmB, fb, k0, ti.n0, ti.zi, ti.zo);
+            tma_load_4d(b_s, &tmB, fb, k0, ti.n0, ti.ozi, ti.ozo);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / ATOM; ++j) tma_load_4d(b_s + j * (BK * 128), &tmB, fb, ti.n0 + j * ATOM, k0, ti.zi, ti.zo);
+            for (int j = 0; j < BN / ATOM; ++j)
+              tma_load_4d(b_s + j * (BK * 128), &tmB, fb, ti.n0 + j * ATOM, k0, ti.ozi, ti.ozo);
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -350,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
     int ab = 0;
     uint32_t aphase = 0;
+    uint32_t chunk = 0;  // staged stores issued by this warp (selects the staging buffer)
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const TileInfo ti = info(t);
@@ -363,6 +409,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+      }
+      if (p.tma_store) {
+        // ---- staged TMA stores: chunk = 32 rows × 128 bytes (32 fp32 or 64 bf16 columns)
+        const int cw = p.c_bf16 ? 64 : 32;
+        const int y = ti.m0 + q * 32;
+        const bool rows_in = y < p.M;
+#pragma unroll 1
+        for (int c = 0; c < BN / cw; ++c) {
+          const int x = ti.n0 + c * cw;
+          const bool write = rows_in && x < p.N && !(empty_k && p.accumulate);
+          const uint32_t buf = smem_u32(staging) + uint32_t((q * 2 + (chunk & 1)) * 4096);
+          if (lane == 0) bulk_wait_read_1();  // the store issued from this buffer two chunks ago has read it
+          __syncwarp();
+          uint32_t r[64];
+          if (!empty_k) {
+            tmem_ld32(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN + c * cw), *reinterpret_cast<uint32_t(*)[32]>(r));
+            if (p.c_bf16)
+              tmem_ld32(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN + c * cw + 32),
+                        *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) r[j] = 0u;
+          }
+          if (write) {
+            const uint32_t row_addr = buf + uint32_t(lane) * 128;
+            if (!p.c_bf16) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4),
+                             __float_as_uint(__uint_as_float(r[4 * j]) * p.alpha),
+                             __float_as_uint(__uint_as_float(r[4 * j + 1]) * p.alpha),
+                             __float_as_uint(__uint_as_float(r[4 * j + 2]) * p.alpha),
+                             __float_as_uint(__uint_as_float(r[4 * j + 3]) * p.alpha));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * e]) * p.alpha,
+                                                           __uint_as_float(r[8 * j + 2 * e + 1]) * p.alpha);
+                  w[e] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+              }
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (write && lane == 0) {
+            if (p.accumulate) tma_reduce_add_4d(&tmC, buf, x, y, ti.zi, ti.zo);
+            else tma_store_4d(&tmC, buf, x, y, ti.zi, ti.zo);
+            bulk_commit();
+          }
+          ++chunk;
+        }
+        if (!empty_k) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+          if (++ab == 2) { ab = 0; aphase ^= 1; }
+        }
+        continue;
       }
       const int64_t cbase = int64_t(ti.zo) * p.sc_outer + int64_t(ti.zi) * p.sc_inner + int64_t(row) * p.ldc;
 #pragma unroll 1
@@ -431,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ab == 2) { ab = 0; aphase ^= 1; }
       }
     }
+    if (p.tma_store && lane == 0) bulk_wait_all();  // staging smem must outlive the stores
   }
 
   __syncthreads();

@@ -13,6 +13,7 @@
 namespace xt {
 
 constexpr int NV = 4;  // vectors per thread in row-resident kernels
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Packed storage of one vector (VW elements) of T.
 template <typename T, int VW> struct Raw;
@@ -93,7 +94,7 @@ static int row_grid(int64_t rows, int rpb, int cap_per_sm = 32) {
 // Fixed number of blocks of the column-reducing backward kernels (one partial row each).
 static int bwd_blocks(int64_t rows, int rpb) {
   int64_t g = ceil_div(rows, rpb);
-  const int64_t cap = int64_t(num_sms()) * 2;
+  const int64_t cap = int64_t(num_sms()) * 4;
   if (g > cap) g = cap;
   return int(g < 1 ? 1 : g);
 }
@@ -136,46 +137,63 @@ __global__ void __launch_bounds__(1024) rms_fwd_kernel(const T* __restrict__ x, 
   }
 }
 
-// Sequentially folds each row group's per-column partials into smem `acc` (cols floats) and
-// writes the block's partial row to part[blockIdx.x].  Deterministic.
+// Column partials of the backward kernels live in shared memory, one slice of `cols` floats
+// per row group; each (group, column) is owned by exactly one thread, so no atomics are
+// needed and the order of additions is fixed.  slice_add adds one vector's contribution.
 template <int VW>
-__device__ __forceinline__ void fold_partials(const float (&p)[NV][VW], float* acc, float* part, int tpr,
-                                              int64_t nvec, int64_t cols) {
-  const int rpb = blockDim.x / tpr, grp = threadIdx.x / tpr, l = threadIdx.x % tpr;
-  for (int g = 0; g < rpb; ++g) {
-    if (grp == g) {
+__device__ __forceinline__ void slice_add(float* p, const float (&v)[VW]) {
+  if constexpr (VW % 4 == 0) {
 #pragma unroll
-      for (int k = 0; k < NV; ++k) {
-        const int64_t j = l + int64_t(k) * tpr;
-        if (j < nvec)
-#pragma unroll
-          for (int e = 0; e < VW; ++e) acc[j * VW + e] = (g == 0 ? 0.f : acc[j * VW + e]) + p[k][e];
-      }
+    for (int e = 0; e < VW; e += 4) {
+      float4 q = *reinterpret_cast<float4*>(p + e);
+      q.x += v[e]; q.y += v[e + 1]; q.z += v[e + 2]; q.w += v[e + 3];
+      *reinterpret_cast<float4*>(p + e) = q;
     }
-    __syncthreads();
+  } else {
+#pragma unroll
+    for (int e = 0; e < VW; ++e) p[e] += v[e];
   }
-  for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) part[int64_t(blockIdx.x) * cols + c] = acc[c];
+}
+
+// Zeroes this thread's columns of its group's slice.
+template <int VW>
+__device__ __forceinline__ void slice_zero(float* slice, int l, int tpr, int64_t nvec) {
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t j = l + int64_t(k) * tpr;
+    if (j < nvec)
+#pragma unroll
+      for (int e = 0; e < VW; ++e) slice[j * VW + e] = 0.f;
+  }
+}
+
+// part[blockIdx.x][c] = Σ over the block's row groups (in group order) of slice[g][c].
+__device__ __forceinline__ void slices_fold(const float* slices, int rpb, float* part, int64_t cols) {
+  __syncthreads();
+  for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) {
+    float a = 0.f;
+    for (int g = 0; g < rpb; ++g) a += slices[int64_t(g) * cols + c];
+    part[int64_t(blockIdx.x) * cols + c] = a;
+  }
 }
 
 template <typename T, typename TD, int VW, int MAXT>
-__global__ void __launch_bounds__(MAXT) rms_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
+__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) rms_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
                                                       const T* __restrict__ gamma, const float* __restrict__ inv_rms,
                                                       TD* dx, float* __restrict__ part, int64_t rows, int64_t cols,
                                                       int tpr, int acc_dx) {
   extern __shared__ float smem[];
-  float* red = smem;          // 32
-  float* colacc = smem + 32;  // cols
+  float* red = smem;  // 32
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  float* pg = smem + 32 + int64_t(threadIdx.x / tpr) * cols;  // this row group's dγ slice
   const int64_t nvec = cols / VW;
-  float pg[NV][VW];
   Raw<T, VW> gm[NV];  // this thread's columns of γ, the same for every row
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int64_t j = l + int64_t(k) * tpr;
     if (j < nvec) gm[k].load(gamma + j * VW); else gm[k].zero();
-#pragma unroll
-    for (int e = 0; e < VW; ++e) pg[k][e] = 0.f;
   }
+  if (part) slice_zero<VW>(pg, l, tpr, nvec);
   for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
     const int64_t r = r0 + threadIdx.x / tpr;
     const bool act = r < rows;
@@ -200,13 +218,14 @@ __global__ void __launch_bounds__(MAXT) rms_bwd_kernel(const T* __restrict__ d, 
     for (int k = 0; k < NV; ++k) {
       const int64_t j = l + int64_t(k) * tpr;
       if (act && j < nvec) {
-        float o[VW];
+        float o[VW], pgv[VW];
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const float xv = vx[k].get(e), dv = vd[k].get(e);
           o[e] = ir * dv * gm[k].get(e) - xv * c2;
-          pg[k][e] += dv * xv * ir;
+          pgv[e] = dv * xv * ir;
         }
+        if (part) slice_add<VW>(pg + j * VW, pgv);
         if (dx) {
           TD* p = dx + r * cols + j * VW;
           if (acc_dx) {
@@ -220,7 +239,7 @@ __global__ void __launch_bounds__(MAXT) rms_bwd_kernel(const T* __restrict__ d, 
       }
     }
   }
-  if (part) fold_partials<VW>(pg, colacc, part, tpr, nvec, cols);
+  if (part) slices_fold(smem + 32, rpb, part, cols);
 }
 
 // ============================================================================== LayerNorm
@@ -276,25 +295,25 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
 }
 
 template <typename T, typename TD, int VW, int MAXT>
-__global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
+__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
                                                      const T* __restrict__ gamma, const float* __restrict__ mean,
                                                      const float* __restrict__ rstd, TD* dx, float* __restrict__ part_g,
                                                      float* __restrict__ part_b, int64_t rows, int64_t cols,
                                                      int tpr, int acc_dx) {
   extern __shared__ float smem[];
   float* red = smem;
-  float* colacc = smem + 32;
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  float* pg = smem + 32 + int64_t(threadIdx.x / tpr) * cols;             // dγ slice of this row group
+  float* pb = smem + 32 + int64_t(rpb + threadIdx.x / tpr) * cols;       // dβ slice
   const int64_t nvec = cols / VW;
-  float pg[NV][VW], pb[NV][VW];
   Raw<T, VW> gm[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int64_t j = l + int64_t(k) * tpr;
     if (j < nvec) gm[k].load(gamma + j * VW); else gm[k].zero();
-#pragma unroll
-    for (int e = 0; e < VW; ++e) { pg[k][e] = 0.f; pb[k][e] = 0.f; }
   }
+  if (part_g) slice_zero<VW>(pg, l, tpr, nvec);
+  if (part_b) slice_zero<VW>(pb, l, tpr, nvec);
   const float inv_n = 1.f / float(cols);
   for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
     const int64_t r = r0 + threadIdx.x / tpr;
@@ -324,14 +343,16 @@ __global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, c
     for (int k = 0; k < NV; ++k) {
       const int64_t j = l + int64_t(k) * tpr;
       if (act && j < nvec) {
-        float o[VW];
+        float o[VW], pgv[VW], pbv[VW];
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const float xh = (vx[k].get(e) - mu) * rs, dv = vd[k].get(e);
           o[e] = rs * (dv * gm[k].get(e) - mg - xh * mgx);
-          pg[k][e] += dv * xh;
-          pb[k][e] += dv;
+          pgv[e] = dv * xh;
+          pbv[e] = dv;
         }
+        if (part_g) slice_add<VW>(pg + j * VW, pgv);
+        if (part_b) slice_add<VW>(pb + j * VW, pbv);
         if (dx) {
           TD* p = dx + r * cols + j * VW;
           if (acc_dx) {
@@ -345,9 +366,8 @@ __global__ void __launch_bounds__(MAXT) ln_bwd_kernel(const T* __restrict__ d, c
       }
     }
   }
-  if (part_g) fold_partials<VW>(pg, colacc, part_g, tpr, nvec, cols);
-  __syncthreads();
-  if (part_b) fold_partials<VW>(pb, colacc, part_b, tpr, nvec, cols);
+  if (part_g) slices_fold(smem + 32, rpb, part_g, cols);
+  if (part_b) slices_fold(smem + 32 + int64_t(rpb) * cols, rpb, part_b, cols);
 }
 
 // ============================================================================== column sums
@@ -439,6 +459,8 @@ __global__ void __launch_bounds__(1024) softmax_fwd_kernel(const T* __restrict__
         if (act && j < nvec && j * VW + e < vis) m = fmaxf(m, v[k].get(e));
     }
     m = group_reduce<true>(m, tpr, red);
+    // exp(x − m) = 2^((x − m)·log2 e): one exp2 per element
+    const float ml = m * kLog2e;
     float ex[NV][VW];
     float s = 0.f;
 #pragma unroll
@@ -446,7 +468,7 @@ __global__ void __launch_bounds__(1024) softmax_fwd_kernel(const T* __restrict__
       const int64_t j = l + int64_t(k) * tpr;
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        ex[k][e] = (act && j < nvec && j * VW + e < vis) ? expf(v[k].get(e) - m) : 0.f;
+        ex[k][e] = (act && j < nvec && j * VW + e < vis) ? exp2f(fmaf(v[k].get(e), kLog2e, -ml)) : 0.f;
         s += ex[k][e];
       }
     }
@@ -537,9 +559,10 @@ __global__ void __launch_bounds__(1024) ce_fwd_kernel(const T* __restrict__ x, c
         float vm = v[0];
 #pragma unroll
         for (int e = 1; e < VW; ++e) vm = fmaxf(vm, v[e]);
+        const float vml = vm * kLog2e;
         float vs = 0.f;
 #pragma unroll
-        for (int e = 0; e < VW; ++e) vs += expf(v[e] - vm);
+        for (int e = 0; e < VW; ++e) vs += exp2f(fmaf(v[e], kLog2e, -vml));
         lse_merge(m, s, vm, vs);
       }
     }
@@ -586,35 +609,38 @@ __global__ void ce_loss_kernel(const float* __restrict__ nll, int64_t rows, floa
   }
 }
 
-// dx = (upstream / rows)·(exp(x − lse) − onehot(t))
+// dx = (upstream / rows)·(exp(x − lse) − onehot(t)).  Blocks walk rows; threads walk a
+// row's vectors (no per-element index division).
 template <typename T, typename TG, int VW>
 __global__ void __launch_bounds__(256) ce_bwd_kernel(const T* x, const int32_t* __restrict__ tgt,
                                                     const float* __restrict__ lse, const float* __restrict__ upstream,
                                                     TG* dx, int64_t rows, int64_t V, int acc, uint32_t* flag) {
   const float sc = *upstream / float(rows);
   const int64_t nvec = V / VW;
-  const int64_t total = rows * nvec;
-  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = v / nvec, c = (v - r * nvec) * VW;
-    const float L = lse[r];
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float Ll = lse[r] * kLog2e;
     const int32_t t = tgt[r];
     const bool bad = t < 0 || int64_t(t) >= V;
-    float xv[VW], o[VW];
-    load_vec<T, VW>(x + r * V + c, xv);
+    if (bad && threadIdx.x == 0) flag_error(flag, XT_DEVERR_INDEX);
+    const T* xr = x + r * V;
+    TG* dr = dx + r * V;
+    for (int64_t j = threadIdx.x; j < nvec; j += blockDim.x) {
+      const int64_t c = j * VW;
+      float xv[VW], o[VW];
+      load_vec<T, VW>(xr + c, xv);
 #pragma unroll
-    for (int e = 0; e < VW; ++e) {
-      const float p = expf(xv[e] - L);
-      o[e] = bad ? __int_as_float(0x7fc00000) : sc * (p - (c + e == t ? 1.f : 0.f));
-    }
-    if (bad && c == 0) flag_error(flag, XT_DEVERR_INDEX);
-    TG* p = dx + r * V + c;
-    if (acc) {
-      float old[VW];
-      load_vec<TG, VW>(p, old);
+      for (int e = 0; e < VW; ++e) {
+        const float p = exp2f(fmaf(xv[e], kLog2e, -Ll));
+        o[e] = bad ? __int_as_float(0x7fc00000) : sc * (p - (c + e == t ? 1.f : 0.f));
+      }
+      if (acc) {
+        float old[VW];
+        load_vec<TG, VW>(dr + c, old);
 #pragma unroll
-      for (int e = 0; e < VW; ++e) o[e] += old[e];
+        for (int e = 0; e < VW; ++e) o[e] += old[e];
+      }
+      store_vec<TG, VW>(dr + c, o);
     }
-    store_vec<TG, VW>(p, o);
   }
 }
 
@@ -874,7 +900,7 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd: row too long (%lld)", (long long)cols);
   const int nb = bwd_blocks(rows, pl.rpb);
   float* part = dgamma ? static_cast<float*>(ws) : nullptr;
-  const size_t smem = (32 + size_t(cols)) * sizeof(float);
+  const size_t smem = (32 + size_t(pl.rpb) * size_t(cols)) * sizeof(float);
   if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd: row too long");
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
     auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
@@ -946,7 +972,7 @@ int xt_rms_norm_bwd_noalloc(const void* d, const void* x, const void* gamma, con
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_bwd_noalloc: row too long (%lld)", (long long)cols);
   int nb = bwd_blocks(rows, pl.rpb);
   if (nb > kNoAllocMaxBlocks) nb = kNoAllocMaxBlocks;   // each block loops over its share of rows
-  const size_t smem = (32 + size_t(cols)) * sizeof(float);
+  const size_t smem = (32 + size_t(pl.rpb) * size_t(cols)) * sizeof(float);
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
     auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
@@ -996,7 +1022,7 @@ int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const floa
   const int nb = bwd_blocks(rows, pl.rpb);
   float* part_g = dgamma ? static_cast<float*>(ws) : nullptr;
   float* part_b = dbeta ? static_cast<float*>(ws) + size_t(nb) * size_t(cols) : nullptr;
-  const size_t smem = (32 + size_t(cols)) * sizeof(float);
+  const size_t smem = (32 + 2 * size_t(pl.rpb) * size_t(cols)) * sizeof(float);
   if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
     auto k = pl.threads <= 256 ? ln_bwd_kernel<T, TD, VW, 256> : ln_bwd_kernel<T, TD, VW, 512>;
@@ -1114,8 +1140,7 @@ int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float
   cudaStream_t s = as_stream(stream);
   uint32_t* flag = errflag();
   const bool vec = V % 8 == 0 && aligned16(logits) && aligned16(dlogits);
-  const int64_t work = rows * V / (vec ? 8 : 1);
-  int64_t grid = ceil_div(work, 256);
+  int64_t grid = rows;
   if (grid > int64_t(num_sms()) * 16) grid = int64_t(num_sms()) * 16;
   const int g = int(grid < 1 ? 1 : grid);
 #define XT_CE_BWD(TI, TG)                                                                                  \
