@@ -41,7 +41,7 @@ WORKLOAD_TEXT = {
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=120)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
@@ -53,17 +53,25 @@ def parse_args(argv=None):
 # ------------------------------------------------------------------------------ CPU oracle
 
 
-def oracle_sample(workload: str, seqs: int, reps: int = 1):
+def oracle_sample(workload: str, seqs: int, reps: int = 1, prefix: int = 0):
     """Times the oracle's forward + backward on `seqs` sequences of the workload (float64
-    NumPy, all host cores).  Returns (tokens/s, seconds per rep, tokens)."""
+    NumPy, all host cores), or, with `prefix` > 0, on the first `prefix` positions of one
+    sequence (the same stack on a shorter causal sequence).  Returns (tokens/s, seconds per
+    rep, tokens)."""
     import synth
     from oracle import block as OB
     cfg = dict(synth.BLOCK_CONFIGS[workload])
     params = synth.block_params(cfg)
     ids, tgt = synth.block_tokens(cfg)
-    seqs = min(seqs, cfg["B"])
-    sub = dict(cfg, B=seqs)
-    n = seqs * cfg["S"]
+    if prefix and prefix < cfg["S"]:
+        sub = dict(cfg, B=1, S=prefix)
+        if "P" in params:
+            params = dict(params, P=params["P"][:prefix])
+        n = prefix
+    else:
+        seqs = min(seqs, cfg["B"])
+        sub = dict(cfg, B=seqs)
+        n = seqs * cfg["S"]
     times = []
     for r in range(reps):
         t0 = time.perf_counter()
@@ -93,6 +101,17 @@ def cpu_model():
     except Exception:
         pass
     return None
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of `x` over the ranks of the default process group (x itself with none)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -165,18 +184,27 @@ def measured_peaks():
 # ------------------------------------------------------------------------------ reference arm
 
 
+REF_BUDGET_S = 150.0
+
+
 def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores.  One untimed full-sequence sample sizes the
+    per-step sample: a causal prefix of one sequence (a multiple of 128 positions, at least 128)
+    chosen so that the warm-up and timed steps together take about REF_BUDGET_S seconds."""
     if rank != 0:
         return
+    import synth
+    cfg = synth.BLOCK_CONFIGS[args.workload]
+    S = cfg["S"]
+    _, t_full, _ = oracle_sample(args.workload, 1)
+    per_step = REF_BUDGET_S / max(1, args.warmup + args.steps)
+    prefix = int(min(S, max(128, 128 * int(S * per_step / t_full / 128))))
     rates = []
     for i in range(args.warmup + args.steps):
-        r, t, n = oracle_sample(args.workload, args.sample_seqs)
+        r, t, n = oracle_sample(args.workload, 1, prefix=prefix)
         if i >= args.warmup:
             rates.append((r, t))
     secs = [t for _, t in rates]
-    import synth
-    cfg = synth.BLOCK_CONFIGS[args.workload]
-    n = min(args.sample_seqs, cfg["B"]) * cfg["S"]
     value = n / statistics.mean(secs)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -185,8 +213,8 @@ def run_reference(args, rank, world):
         "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": cfg["B"], "seq_len": cfg["S"],
                    "parallelism": "cpu"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{n} tokens ({min(args.sample_seqs, cfg['B'])} of {cfg['B']} sequences), "
-                                   f"all {cfg['n_layers']} layers, float64 NumPy, per step"},
+                                  "sample": f"per step: the first {n} positions of one sequence (of {cfg['B']} x {S}), "
+                                   f"all {cfg['n_layers']} layers, float64 NumPy forward + backward"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -221,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
         nb.forward(ids, tgt, stream)
         nb.backward(ids, tgt, stream)
 
-    for _ in range(args.warmup):
+    for _ in range(max(1, args.warmup)):   # eager warm-up: kernel attributes and tensor maps are set up here
         step()
     torch.cuda.synchronize(dev)
     assert xt.device_errors() == 0, "device error flag set during warm-up"
@@ -230,63 +258,70 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
 
-    # ---------------- timed region (device-resident inputs) ----------------
+    # ---------------- one step captured as a CUDA graph ----------------
+    # The step is enqueued once into a graph and replayed: the same kernels, without the host
+    # launch gaps between them.  GEMM timing events are captured as graph nodes (re-recorded
+    # on every replay; read after the timed region, they give the last timed step's launches).
     per_step_gemms = 400 * cfg["n_layers"] // 12 + 64
-    xt.profile_gemm(per_step_gemms * args.steps + 64)
+    xt.profile_gemm(per_step_gemms)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    launches0 = xt.launch_count()
+    with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+        cs = torch.cuda.current_stream(dev)
+        nb.zero_grads(cs)
+        nb.forward(ids, tgt, cs)
+        nb.backward(ids, tgt, cs)
+    kernels_per_step = xt.launch_count() - launches0
+    torch.cuda.synchronize(dev)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    assert xt.device_errors() == 0, "device error flag set during graph warm-up"
+
+    # ---------------- timed region (device-resident inputs) ----------------
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
-    launches0 = xt.launch_count()
     with ClockSampler(local_rank) as clocks:
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            graph.replay()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-    launches = xt.launch_count() - launches0
+    launches = kernels_per_step * args.steps
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
-    flops, gms = xt.profile_gemm_read()
-    xt.profile_gemm(0)
+    flops, gms = xt.profile_gemm_read()   # the last timed step's GEMM launches
     assert xt.device_errors() == 0, "device error flag set during the timed region"
     loss = float(nb.loss.item())
 
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
     value = world * T / (ms_max / 1000.0)
 
     # ---------------- end to end: host buffers, copies inside the timed region ----------------
     ids_pin = torch.tensor(ids_h).pin_memory()
     tgt_pin = torch.tensor(tgt_h).pin_memory()
     loss_pin = torch.empty(1, dtype=torch.float32).pin_memory()
-    ids_d = torch.empty_like(ids)
-    tgt_d = torch.empty_like(tgt)
     e2e_steps = max(3, args.steps // 2)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        ids_d.copy_(ids_pin, non_blocking=True)
-        tgt_d.copy_(tgt_pin, non_blocking=True)
-        nb.zero_grads(stream)
-        nb.forward(ids_d, tgt_d, stream)
-        nb.backward(ids_d, tgt_d, stream)
+        ids.copy_(ids_pin, non_blocking=True)      # the graph reads ids / tgt in place
+        tgt.copy_(tgt_pin, non_blocking=True)
+        graph.replay()
         loss_pin.copy_(nb.loss, non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()
         _ = float(loss_pin[0])
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
 
+    xt.profile_gemm(0)
     if rank != 0:
         return
     peaks, peak_src = measured_peaks()
-    gemm_ms_step = float(np.sum(gms)) / args.steps
+    gemm_ms_step = float(np.sum(gms))
     tflops = float(np.sum(flops)) / (float(np.sum(gms)) * 1e-3) / 1e12 if len(gms) else None
     peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
     if cfg["dtype"] == "f32":
@@ -296,8 +331,8 @@ def run_ours(args, rank, world, local_rank):
         "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
         "frac": (tflops / peak) if tflops else None, "peak_source": f"{peak_src} "
         f"({'bf16 sustained' if cfg['dtype'] == 'bf16' else 'bf16 sustained x 1.1/2.25 for tf32'})",
-        "traffic": None, "launches_per_step": len(gms) / args.steps,
-        "share_of_step": gemm_ms_step / ms, "gemm_tflop_per_step": float(np.sum(flops)) / args.steps / 1e12,
+        "traffic": None, "launches_per_step": len(gms),
+        "share_of_step": gemm_ms_step / ms, "gemm_tflop_per_step": float(np.sum(flops)) / 1e12,
     }
     cpu = cpu_baseline(args.workload, args.sample_seqs) if world == 1 else None
     line = {

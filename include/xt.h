@@ -76,7 +76,13 @@ uint64_t xt_launch_count(void);
 /* GEMM timing for measurement: with capacity > 0, the next `capacity` GEMM launches are
  * bracketed by CUDA events recorded on their own stream, each tagged with its algorithmic
  * FLOPs (2·M·N·K per batch; for the causal modes only the unmasked half).  Events are
- * created by this call, not during the launches; capacity 0 disables.  xt_profile_gemm_read
+ * created by this call, not during the launches; capacity 0 disables.  Launches enqueued while
+ * their stream is being captured into a CUDA graph record their events as graph nodes, so
+ * every replay re-records them (the read then returns the latest replay's timings).  The pool's
+ * events live as long as the library; a later xt_profile_gemm call hands them to new records,
+ * so a graph captured with profiling on should not be replayed while other launches are being
+ * profiled.
+ * xt_profile_gemm_read
  * waits for the recorded events and copies up to max_records records into host arrays:
  * flops, milliseconds, and (if shapes != NULL) 8 ints per record: M, N, K, batches, tile
  * width BN, A MN-major, B MN-major, causal mode.  *n receives the number recorded. */

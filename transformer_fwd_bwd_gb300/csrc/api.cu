@@ -76,13 +76,23 @@ int num_sms() {
   return g_sms[dev];
 }
 
+// Inside a stream capture the event becomes an event-record node of the graph, so each
+// replay records it; outside, a plain record.
+static void record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 bool gemm_profile_begin(cudaStream_t s, double flops, const int* shape, void** token) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (!g_prof_on || g_ev_next + 2 > g_ev_pool.size()) return false;
   GemmRecord r{flops, g_ev_pool[g_ev_next], g_ev_pool[g_ev_next + 1], {}};
   for (int i = 0; i < 8; ++i) r.shape[i] = shape[i];
   g_ev_next += 2;
-  cudaEventRecord(r.start, s);
+  record_event(r.start, s);
   g_records.push_back(r);
   *token = reinterpret_cast<void*>(g_records.size());
   return true;
@@ -91,7 +101,7 @@ bool gemm_profile_begin(cudaStream_t s, double flops, const int* shape, void** t
 void gemm_profile_end(cudaStream_t s, void* token) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   const size_t i = reinterpret_cast<size_t>(token);
-  if (i >= 1 && i <= g_records.size()) cudaEventRecord(g_records[i - 1].stop, s);
+  if (i >= 1 && i <= g_records.size()) record_event(g_records[i - 1].stop, s);
 }
 
 }  // namespace xt

@@ -22,6 +22,7 @@ template <typename T> struct Raw<T, 1> {
   __device__ __forceinline__ void load(const T* p) { v = to_f(*p); }
   __device__ __forceinline__ float get(int) const { return v; }
   __device__ __forceinline__ void zero() { v = 0.f; }
+  __device__ __forceinline__ void keep_first(int n) { if (n < 1) v = 0.f; }
 };
 template <> struct Raw<float, 4> {
   float4 q;
@@ -30,6 +31,13 @@ template <> struct Raw<float, 4> {
     return e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
   }
   __device__ __forceinline__ void zero() { q = make_float4(0.f, 0.f, 0.f, 0.f); }
+  // zero elements n.. (n in 0..VW)
+  __device__ __forceinline__ void keep_first(int n) {
+    if (n < 4) q.w = 0.f;
+    if (n < 3) q.z = 0.f;
+    if (n < 2) q.y = 0.f;
+    if (n < 1) q.x = 0.f;
+  }
 };
 template <> struct Raw<bf16, 8> {
   uint4 q;
@@ -39,6 +47,16 @@ template <> struct Raw<bf16, 8> {
     return (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
   }
   __device__ __forceinline__ void zero() { q = make_uint4(0, 0, 0, 0); }
+  // zero elements n.. (n in 0..VW); element e is the low half of word e/2 when e is even
+  __device__ __forceinline__ void keep_first(int n) {
+    q.x &= word_keep(n, 0);
+    q.y &= word_keep(n, 1);
+    q.z &= word_keep(n, 2);
+    q.w &= word_keep(n, 3);
+  }
+  static __device__ __forceinline__ uint32_t word_keep(int n, int i) {
+    return n >= 2 * i + 2 ? 0xFFFFFFFFu : n == 2 * i + 1 ? 0x0000FFFFu : 0u;
+  }
 };
 
 template <typename T, int VW>
@@ -428,110 +446,139 @@ __global__ void colsum_stage1(const T* __restrict__ d, T* dx, int acc_dx, float*
 
 // ============================================================================== softmax
 
-// causal extent of row with query index s: columns read / written
-__device__ __forceinline__ int64_t causal_visible(int64_t s, int64_t cols) { return s + 1 < cols ? s + 1 : cols; }
-__device__ __forceinline__ int64_t causal_extent(int causal, int64_t s, int64_t cols) {
-  if (causal == 2) {
-    const int64_t e = (s / 128 + 1) * 128;
-    return e < cols ? e : cols;
-  }
-  return cols;
+// Causal rows: the row with query index q reads columns [0, vis) with vis = min(q + 1, cols)
+// and writes [0, ext): ext = cols, or, in mode 2, the end of q's 128-wide key block (the extent
+// the probability-times-value product reads), columns in [vis, ext) written as zeros.
+// Column arithmetic is 32-bit (a row holds at most 32768 elements); the visibility test is
+// one integer per 16-byte vector, and only the vector that straddles `vis` is masked per element.
+__device__ __forceinline__ int row_query(int64_t r, int64_t q_len, bool small) {
+  return small ? int(uint32_t(r) % uint32_t(q_len)) : int(r % q_len);
+}
+__device__ __forceinline__ int causal_vis(int causal, int q, int cols) {
+  return causal ? (q + 1 < cols ? q + 1 : cols) : cols;
+}
+__device__ __forceinline__ int causal_ext(int causal, int q, int cols) {
+  if (causal != 2) return cols;
+  const int e = ((q >> 7) + 1) << 7;
+  return e < cols ? e : cols;
 }
 
 template <typename T, int VW>
 __global__ void __launch_bounds__(1024) softmax_fwd_kernel(const T* __restrict__ x, T* __restrict__ y, int64_t rows,
-                                                          int64_t cols, int causal, int64_t q_len, int tpr) {
+                                                          int cols, int causal, int64_t q_len, int tpr) {
   __shared__ float red[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
-  const int64_t nvec = cols / VW;
+  const bool small = rows <= INT32_MAX && q_len <= INT32_MAX;
   for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
     const int64_t r = r0 + threadIdx.x / tpr;
     const bool act = r < rows;
-    const int64_t vis = causal ? causal_visible(r % q_len, cols) : cols;
-    Raw<T, VW> v[NV];
+    const int q = act ? row_query(r, q_len, small) : 0;
+    const int vis = act ? causal_vis(causal, q, cols) : 0;
+    const T* xr = x + (act ? r : 0) * int64_t(cols);
+    float f[NV][VW];
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      const int64_t j = l + int64_t(k) * tpr;
-      if (act && j < nvec && j * VW < vis) v[k].load(x + r * cols + j * VW); else v[k].zero();
+      const int c0 = (l + k * tpr) * VW;
+      const int lim = vis - c0;   // visible elements of this vector (<= 0: none, >= VW: all)
+      if (lim >= VW) {
+        Raw<T, VW> v;
+        v.load(xr + c0);
 #pragma unroll
-      for (int e = 0; e < VW; ++e)
-        if (act && j < nvec && j * VW + e < vis) m = fmaxf(m, v[k].get(e));
+        for (int e = 0; e < VW; ++e) f[k][e] = v.get(e);
+      } else if (lim > 0) {
+        Raw<T, VW> v;
+        v.load(xr + c0);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) f[k][e] = e < lim ? v.get(e) : -INFINITY;
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) f[k][e] = -INFINITY;
+      }
+#pragma unroll
+      for (int e = 0; e < VW; ++e) m = fmaxf(m, f[k][e]);
     }
     m = group_reduce<true>(m, tpr, red);
-    // exp(x − m) = 2^((x − m)·log2 e): one exp2 per element
-    const float ml = m * kLog2e;
-    float ex[NV][VW];
+    // exp(x − m) = 2^(x·log2 e − m·log2 e): one fma and one exp2 per element; masked
+    // elements hold −inf and give exactly 0
+    const float ml = act ? m * kLog2e : 0.f;
     float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const int64_t j = l + int64_t(k) * tpr;
+    for (int k = 0; k < NV; ++k)
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        ex[k][e] = (act && j < nvec && j * VW + e < vis) ? exp2f(fmaf(v[k].get(e), kLog2e, -ml)) : 0.f;
-        s += ex[k][e];
+        f[k][e] = exp2f(fmaf(f[k][e], kLog2e, -ml));
+        s += f[k][e];
       }
-    }
     s = group_reduce<false>(s, tpr, red);
+    if (!act) continue;
     const float inv = 1.f / s;
-    const int64_t ext = causal ? causal_extent(causal, r % q_len, cols) : cols;
+    const int ext = causal_ext(causal, q, cols);
+    T* yr = y + r * int64_t(cols);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      const int64_t j = l + int64_t(k) * tpr;
-      if (act && j < nvec && j * VW < ext) {
+      const int c0 = (l + k * tpr) * VW;
+      if (c0 < ext) {
         float o[VW];
 #pragma unroll
-        for (int e = 0; e < VW; ++e) o[e] = ex[k][e] * inv;
-        store_vec<T, VW>(y + r * cols + j * VW, o);
+        for (int e = 0; e < VW; ++e) o[e] = f[k][e] * inv;
+        store_vec<T, VW>(yr + c0, o);
       }
     }
   }
 }
 
-template <typename T, int VW>
-__global__ void __launch_bounds__(1024) softmax_bwd_kernel(const T* __restrict__ d, const T* __restrict__ y, T* dx,
-                                                          int64_t rows, int64_t cols, int causal, int64_t q_len,
-                                                          int tpr, int acc) {
+// MAXT: the launch's block size bound; 256-thread launches get registers for two packed
+// row shares without spilling.
+template <typename T, int VW, int MAXT>
+__global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) softmax_bwd_kernel(
+    const T* __restrict__ d, const T* __restrict__ y, T* dx, int64_t rows, int cols, int causal, int64_t q_len,
+    int tpr, int acc) {
   __shared__ float red[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
-  const int64_t nvec = cols / VW;
+  const bool small = rows <= INT32_MAX && q_len <= INT32_MAX;
   for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
     const int64_t r = r0 + threadIdx.x / tpr;
     const bool act = r < rows;
-    const int64_t vis = causal ? causal_visible(r % q_len, cols) : cols;
+    const int q = act ? row_query(r, q_len, small) : 0;
+    const int vis = act ? causal_vis(causal, q, cols) : 0;
+    const int64_t base = (act ? r : 0) * int64_t(cols);
+    // packed vectors stay in registers; elements at or past `vis` are zeroed in place, so
+    // they add nothing to Σ d·y and come out as y·(d − s) = 0
     Raw<T, VW> vd[NV], vy[NV];
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      const int64_t j = l + int64_t(k) * tpr;
-      if (act && j < nvec && j * VW < vis) {
-        vd[k].load(d + r * cols + j * VW);
-        vy[k].load(y + r * cols + j * VW);
+      const int c0 = (l + k * tpr) * VW;
+      const int lim = vis - c0;
+      if (lim > 0) {
+        vd[k].load(d + base + c0);
+        vy[k].load(y + base + c0);
+        if (lim < VW) { vd[k].keep_first(lim); vy[k].keep_first(lim); }
       } else {
         vd[k].zero(); vy[k].zero();
       }
 #pragma unroll
-      for (int e = 0; e < VW; ++e)
-        if (j * VW + e < vis) s += vd[k].get(e) * vy[k].get(e);
+      for (int e = 0; e < VW; ++e) s = fmaf(vd[k].get(e), vy[k].get(e), s);
     }
     s = group_reduce<false>(s, tpr, red);
-    const int64_t ext = causal ? causal_extent(causal, r % q_len, cols) : cols;
+    if (!act) continue;
+    const int ext = causal_ext(causal, q, cols);
+    T* p = dx + base;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      const int64_t j = l + int64_t(k) * tpr;
-      if (act && j < nvec && j * VW < ext) {
+      const int c0 = (l + k * tpr) * VW;
+      if (c0 < ext) {
         float o[VW];
 #pragma unroll
-        for (int e = 0; e < VW; ++e)
-          o[e] = (j * VW + e < vis) ? vy[k].get(e) * (vd[k].get(e) - s) : 0.f;
-        T* p = dx + r * cols + j * VW;
+        for (int e = 0; e < VW; ++e) o[e] = fmaf(vy[k].get(e), vd[k].get(e) - s, 0.f);
         if (acc) {
           float old[VW];
-          load_vec<T, VW>(p, old);
+          load_vec<T, VW>(p + c0, old);
 #pragma unroll
           for (int e = 0; e < VW; ++e) o[e] += old[e];
         }
-        store_vec<T, VW>(p, o);
+        store_vec<T, VW>(p + c0, o);
       }
     }
   }
@@ -1079,7 +1126,7 @@ int xt_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int causa
   cudaStream_t s = as_stream(stream);
   const int grid = row_grid(rows, pl.rpb);
   XT_ROW_DISPATCH(dt, vec, (softmax_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
-                               static_cast<const T*>(x), static_cast<T*>(y), rows, cols, causal, q_len, pl.tpr)));
+                               static_cast<const T*>(x), static_cast<T*>(y), rows, int(cols), causal, q_len, pl.tpr)));
   return check_launch("xt_softmax_fwd");
 }
 
@@ -1095,9 +1142,11 @@ int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_softmax_bwd: row too long");
   cudaStream_t s = as_stream(stream);
   const int grid = row_grid(rows, pl.rpb);
-  XT_ROW_DISPATCH(dt, vec, (softmax_bwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
-                               static_cast<const T*>(d), static_cast<const T*>(y), static_cast<T*>(dx), rows, cols,
-                               causal, q_len, pl.tpr, acc)));
+  const bool narrow = pl.threads <= 256;
+  XT_ROW_DISPATCH(dt, vec, ((narrow ? softmax_bwd_kernel<T, VW, 256> : softmax_bwd_kernel<T, VW, 1024>)
+                            <<<grid, pl.threads, 0, s>>>(static_cast<const T*>(d), static_cast<const T*>(y),
+                                                         static_cast<T*>(dx), rows, int(cols), causal, q_len,
+                                                         pl.tpr, acc)));
   return check_launch("xt_softmax_bwd");
 }
 
