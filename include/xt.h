@@ -221,6 +221,33 @@ int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t
                    int64_t q_len, int dt, int acc, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Fused attention ([AE] § Attention 用组合: per (batch, head) scores = Q Kᵀ·(1/√hd),
+ * P = softmax(scores), O = P V; backward dV = Pᵀ dO, dP = dO Vᵀ, dS = softmax_bwd(dP, P),
+ * dQ = dS K·(1/√hd), dK = dSᵀ Q·(1/√hd)), computed tile by tile on the tensor cores without
+ * writing P: the same values as the composition up to rounding (P is rounded to bf16 before
+ * it multiplies V, as in the composed bf16 path).
+ *
+ * Layout: token t = b·S + s is row t of each matrix; head h of q, k, v occupies columns
+ * [h·hd, h·hd + hd) of its row, rows ld_qkv elements apart (q, k, v may be column blocks of
+ * one [T, 3·H·hd] buffer); o and d_o likewise with ld_o; dq, dk, dv with ld_dqkv.
+ * causal: 1 masks key c from query s when c > s (the masked probabilities are 0); 0 none.
+ * lse (float32 [B][H][S], written by the forward, read by the backward) is the natural-log
+ * normaliser log Σ_c exp(scores[s, c]) over the visible keys.
+ * dq, dk, dv are overwritten.  The backward's workspace (xt_attention_bwd_workspace_size)
+ * holds D = Σ_c dO∘O per (b, h, s).
+ * Supported: dt = XT_BF16, hd = 64, row strides multiples of 8 elements, all pointers
+ * 16-byte aligned (else XT_ERR_UNSUPPORTED / XT_ERR_ALIGNMENT).  Device-side waits are
+ * bounded; on expiry XT_DEVERR_TIMEOUT is set in the device error flag.
+ * ------------------------------------------------------------------------------- */
+int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, int64_t ld_o,
+                     float* lse, int B, int S, int H, int hd, int causal, int dt, void* stream);
+int xt_attention_bwd_workspace_size(int B, int S, int H, size_t* bytes);
+int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o,
+                     const void* d_o, int64_t ld_o, const float* lse, void* dq, void* dk, void* dv,
+                     int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S, int H, int hd, int causal,
+                     int dt, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Cross-entropy, mean over rows ([AE] op table row cross_entropy, § Cross-entropy 反向推导):
  * loss = (1/R) Σ_r (lse_r − x[r, t_r]);  dx = upstream·(softmax(x_r) − onehot(t_r))/R.
  * lse (float32 [rows]) is saved by the forward; `loss` and `upstream` are device float32

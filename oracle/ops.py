@@ -352,6 +352,19 @@ def attention_fwd(q, k, v, causal=True):
     return np.einsum("bhst,bhtd->bhsd", P, v), P
 
 
+def attention_lse(q, k, causal=True):
+    """Per (batch, head, query s): the natural-log normaliser of the attention softmax,
+    lse[s] = log Σ_c exp(scores[s, c]) over the visible keys c, scores = (Q Kᵀ)/√hd — the
+    quantity the safe softmax divides by, so that P = exp(scores − lse).  [B, H, S]."""
+    q, k = f64(q), f64(k)
+    hd = q.shape[-1]
+    scores = np.einsum("bhsd,bhtd->bhst", q, k) * (1.0 / math.sqrt(hd))
+    if causal:
+        scores = np.where(causal_mask(scores.shape[-2], scores.shape[-1]), scores, -np.inf)
+    m = np.max(scores, axis=-1, keepdims=True)
+    return (m + np.log(np.sum(np.exp(scores - m), axis=-1, keepdims=True)))[..., 0]
+
+
 def attention_bwd(dO, q, k, v, P):
     """Backward of the composition matmul → scale → softmax → matmul, step by step."""
     dO, q, k, v, P = f64(dO), f64(q), f64(k), f64(v), f64(P)

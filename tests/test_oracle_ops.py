@@ -297,3 +297,25 @@ def test_attention_composed():
     O1, _ = O.attention_fwd(q[:, :, :1], k[:, :, :1], v[:, :, :1])
     assert np.allclose(O1, v[:, :, :1])
     assert np.allclose(O_[:, :, 0], v[:, :, 0])
+
+
+def test_attention_lse():
+    """The softmax normaliser: closed forms (zero queries ⇒ log of the visible-key count;
+    causal row 0 ⇒ its single score) and brute force by loops with the library logsumexp."""
+    r = rng(15)
+    B, H, S, hd = 2, 2, 6, 4
+    q, k = r.normal(size=(B, H, S, hd)), r.normal(size=(B, H, S, hd))
+    lse = O.attention_lse(q, k, causal=True)
+    assert np.allclose(O.attention_lse(np.zeros_like(q), k, causal=True), np.log(np.arange(1, S + 1)), rtol=1e-14)
+    assert np.allclose(O.attention_lse(np.zeros_like(q), k, causal=False), np.log(S), rtol=1e-14)
+    assert np.allclose(lse[:, :, 0], np.sum(q[:, :, 0] * k[:, :, 0], axis=-1) / 2.0, rtol=1e-14)
+    for b in range(B):
+        for h in range(H):
+            for s_ in range(S):
+                sc = [sum(q[b, h, s_, i] * k[b, h, c, i] for i in range(hd)) / math.sqrt(hd) for c in range(s_ + 1)]
+                assert abs(lse[b, h, s_] - logsumexp(sc)) <= 1e-13 * max(1.0, abs(lse[b, h, s_]))
+    # P = exp(scores − lse) is the oracle's own softmax
+    _, P = O.attention_fwd(q, k, k, causal=True)
+    sc = np.einsum("bhsd,bhtd->bhst", q, k) / math.sqrt(hd)
+    vis = np.tril(np.ones((S, S), dtype=bool))
+    assert np.allclose(np.where(vis, np.exp(sc - lse[..., None]), 0.0), P, rtol=1e-12, atol=1e-15)

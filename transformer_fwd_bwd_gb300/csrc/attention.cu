@@ -1,0 +1,1157 @@
+// Fused attention for sm_103a: per (batch, head), scores = Q Kᵀ·α, P = softmax(scores) under
+// the causal mask, O = P V ([AE] § Attention 用组合 gives the composition; this computes the
+// same result tile by tile, so the S × S probabilities never reach global memory).
+//
+// Forward (one CTA per SM, persistent over 128-query tiles, heaviest first):
+//   warp 0      TMA producer: Q tile once per work item, K and V tiles through 3-slot rings;
+//   warp 1      TMEM owner and MMA issuer: S_j = Q K_jᵀ into one of two TMEM score buffers
+//               (so S_{j+1} is computed while the softmax warps read S_j), then O += P_j V_j
+//               into a TMEM accumulator;
+//   warps 2..5  one query row per thread (TMEM lane): load the score row, mask, running max,
+//               exp2, running sum, write P_j as bf16 into shared memory in the 128-byte-swizzled
+//               K-major layout the MMA reads; rescale O in TMEM when the running max grows by
+//               more than 2^8 (otherwise the stale max is kept: O and the sum share it, so O / l
+//               is exact either way); at the end O / l goes out through a TMA store and the row's
+//               natural-log normaliser lse = log Σ exp(scores) is saved for the backward.
+//
+// Backward (deterministic, no atomics): D = rowsum(dO ∘ O); then one kernel per 128-key tile
+// that recomputes Pᵀ = exp(K Qᵀ·α − lse) and dPᵀ = V dOᵀ and accumulates dV = Pᵀ dO and
+// dK = α·dSᵀ Q over the query tiles, and one kernel per 128-query tile that recomputes P and dP
+// and accumulates dQ = α·dS K over the key tiles, with dS = P ∘ (dP − D).
+//
+// Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records XT_DEVERR_TIMEOUT,
+// all roles stop, the producer waits (bounded) for its copies in flight and TMEM is freed.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+
+#include "gemm.cuh"
+
+namespace xt {
+namespace attn {
+
+using namespace gemm;
+
+constexpr int HD = 64;                     // head dimension the kernels are built for
+constexpr int BT = 128;                    // query / key tile
+constexpr int kThreads = 192;
+constexpr int TILE = BT * 128;             // one 128-row × 64-element bf16 tile: 16 KB
+constexpr int PT = 2 * TILE;               // 128 × 128 bf16 operand: two 64-wide K chunks
+constexpr int RING = 3;                    // K / V slots
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.f;            // log2 growth of the running max that forces a rescale
+
+struct FwdParams {
+  int B, H, S, nq, items, causal;
+  float sc;     // α·log2 e
+  float* lse;   // [B, H, S], natural log
+  uint32_t* flag;
+};
+
+// Work item i → (b, h, query tile); with a causal mask, the longest rows come first.
+struct Item {
+  int b, h, qt, nkv;
+};
+__device__ __forceinline__ Item decode(int i, int B, int H, int nq, int causal) {
+  const int bh_n = B * H;
+  Item it;
+  const int t = i / bh_n, bh = i - t * bh_n;
+  it.qt = causal ? nq - 1 - t : t;
+  it.b = bh / H;
+  it.h = bh - it.b * H;
+  it.nkv = causal ? it.qt + 1 : nq;
+  return it;
+}
+
+// Row r (0..127) of a 128-row operand in the 128-byte-swizzled K-major layout: 16-byte unit u of
+// the 64-element chunk c sits at chunk base + r·128 + ((u ^ (r & 7)) << 4).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c, int u) {
+  return base + uint32_t(c) * TILE + uint32_t(r) * 128 + (uint32_t(u ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Bounded wait taken by a whole warp (the decision is warp-uniform).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+// ------------------------------------------------------------------------------ forward
+
+struct FwdSmem {
+  static constexpr int Q = 0;
+  static constexpr int K = Q + TILE;
+  static constexpr int V = K + RING * TILE;
+  static constexpr int P = V + RING * TILE;
+  static constexpr int STAGE = P + 2 * PT;           // O staging: 4 warps × 32 rows × 128 B
+  static constexpr int BARS = STAGE + 4 * 4096;
+  static constexpr int BYTES = 1024 + BARS + 256;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const FwdParams p) {
+  constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_PV = instr_desc_bf16(128, HD, false, true);
+  constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), O [256,320)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FwdSmem::BARS);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + RING;
+  uint64_t* v_full = k_empty + RING;
+  uint64_t* v_empty = v_full + RING;
+  uint64_t* s_full = v_empty + RING;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* p_free = p_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_free + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(q_empty), 1);
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&s_full[b]), 1);
+      mbar_init(smem_u32(&s_free[b]), 4);
+      mbar_init(smem_u32(&p_full[b]), 4);
+      mbar_init(smem_u32(&p_free[b]), 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tO = tbase + 256;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_error(p.flag, XT_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- TMA producer
+      int ks = 0, vs = 0, nk = 0, nv = 0, nqi = 0;
+      uint32_t kph = 0, vph = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+        const Item it = decode(i, p.B, p.H, p.nq, p.causal);
+        if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1)) { ok = false; break; }
+        mbar_expect_tx(smem_u32(q_full), TILE);
+        tma_load_4d(sb + FwdSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
+        ++nqi;
+        for (int j = 0; j < it.nkv; ++j) {
+          if (*abort_flag) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&k_empty[ks]), kph ^ 1)) { ok = false; break; }
+          mbar_expect_tx(smem_u32(&k_full[ks]), TILE);
+          tma_load_4d(sb + FwdSmem::K + ks * TILE, &tmK, smem_u32(&k_full[ks]), 0, it.h, j * BT, it.b);
+          ++nk;
+          if (++ks == RING) { ks = 0; kph ^= 1; }
+          if (!mbar_wait(smem_u32(&v_empty[vs]), vph ^ 1)) { ok = false; break; }
+          mbar_expect_tx(smem_u32(&v_full[vs]), TILE);
+          tma_load_4d(sb + FwdSmem::V + vs * TILE, &tmV, smem_u32(&v_full[vs]), 0, it.h, j * BT, it.b);
+          ++nv;
+          if (++vs == RING) { vs = 0; vph ^= 1; }
+        }
+      }
+      if (!ok) give_up();
+      // bounded wait for the fills that may still be in flight
+      bool drained = true;
+      if (nqi > 0) drained &= mbar_wait(smem_u32(q_full), (nqi - 1) & 1);
+      for (int n = 0; n < (nk < RING ? nk : RING); ++n) {
+        if (--ks < 0) { ks = RING - 1; kph ^= 1; }
+        drained &= mbar_wait(smem_u32(&k_full[ks]), kph);
+      }
+      for (int n = 0; n < (nv < RING ? nv : RING); ++n) {
+        if (--vs < 0) { vs = RING - 1; vph ^= 1; }
+        drained &= mbar_wait(smem_u32(&v_full[vs]), vph);
+      }
+      if (!drained) give_up();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      int ks = 0, vs = 0, nqi = 0;
+      uint32_t kph = 0, vph = 0;
+      uint32_t g = 0;  // score tiles issued so far (selects the S / P buffer and its phase)
+      bool ok = true;
+      auto issue_pv = [&](uint32_t gg, bool first) -> bool {
+        const int b = int(gg & 1);
+        const uint32_t u = gg >> 1;
+        if (!mbar_wait(smem_u32(&p_full[b]), u & 1)) return false;
+        if (!mbar_wait(smem_u32(&v_full[vs]), vph)) return false;
+        tc_fence_after();
+        const uint32_t ps = sb + FwdSmem::P + b * PT;
+        const uint32_t vsm = sb + FwdSmem::V + vs * TILE;
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk) {
+          const uint64_t ad = smem_desc(ps + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc(vsm + kk * 16 * 128, TILE, 1024);
+          tc_mma<false>(tO, ad, bd, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&v_empty[vs]));
+        tc_commit(smem_u32(&p_free[b]));
+        if (++vs == RING) { vs = 0; vph ^= 1; }
+        return true;
+      };
+      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+        const Item it = decode(i, p.B, p.H, p.nq, p.causal);
+        if (!mbar_wait(smem_u32(q_full), nqi & 1)) { ok = false; break; }
+        ++nqi;
+        tc_fence_after();
+        for (int j = 0; j < it.nkv; ++j, ++g) {
+          const int b = int(g & 1);
+          const uint32_t u = g >> 1;
+          if (*abort_flag || !mbar_wait(smem_u32(&k_full[ks]), kph) ||
+              !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ksm = sb + FwdSmem::K + ks * TILE;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            tc_mma<false>(tbase + uint32_t(b * 128), smem_desc(sb + FwdSmem::Q + kk * 32, 16, 1024),
+                          smem_desc(ksm + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          tc_commit(smem_u32(&k_empty[ks]));
+          tc_commit(smem_u32(&s_full[b]));
+          if (j == it.nkv - 1) tc_commit(smem_u32(q_empty));
+          if (++ks == RING) { ks = 0; kph ^= 1; }
+          if (j >= 1 && !issue_pv(g - 1, j == 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!issue_pv(g - 1, it.nkv == 1)) { ok = false; break; }
+      }
+      if (!ok) give_up();
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax / epilogue
+    const int qw = warp & 3;            // TMEM lanes [32 qw, 32 qw + 32)
+    const int rr = qw * 32 + lane;      // row within the query tile
+    const uint32_t lane_off = uint32_t(qw * 32) << 16;
+    const uint32_t stage = sb + FwdSmem::STAGE + uint32_t(qw) * 4096;
+    uint32_t g = 0;
+    for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const Item it = decode(i, p.B, p.H, p.nq, p.causal);
+      const int row = it.qt * BT + rr;
+      float m = -INFINITY;  // running max of the raw scores (Q·K, before α)
+      float l = 0.f;        // running Σ 2^((s − m)·sc)
+      bool ok = true;
+      for (int j = 0; j < it.nkv; ++j, ++g) {
+        const int b = int(g & 1);
+        const uint32_t u = g >> 1;
+        if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
+        // keys at or past `lim` (relative to this tile) are masked
+        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT;
+        if (lim < BT) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) r[c] = __float_as_uint(-INFINITY);
+        }
+        float mt = __uint_as_float(r[0]);
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mt = fmaxf(mt, __uint_as_float(r[c]));
+        const float m_new = fmaxf(m, mt);
+        const bool need = m_new > m && (m == -INFINITY || (m_new - m) * p.sc > kRescale);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O holds Σ 2^((s − m)·sc)·v with the old m: bring it to m_new once PV_{j−1} is done
+          const uint32_t pg = g - 1;
+          if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const float a = need ? exp2f((m - m_new) * p.sc) : 1.f;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + uint32_t(c * 32), o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+            tmem_st32(tO + lane_off + uint32_t(c * 32), o);
+          }
+          tmem_st_wait();
+        }
+        if (need) {
+          l = (m == -INFINITY) ? 0.f : l * exp2f((m - m_new) * p.sc);
+          m = m_new;
+        }
+        const float ms = (m == -INFINITY) ? 0.f : m * p.sc;
+        if (!warp_wait(smem_u32(&p_free[b]), (u & 1) ^ 1)) { ok = false; break; }
+        const uint32_t ps = sb + FwdSmem::P + b * PT;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int un = 0; un < 8; ++un) {
+            float e[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              e[t] = exp2f(fmaf(__uint_as_float(r[c * 64 + un * 8 + t]), p.sc, -ms));
+              l += e[t];
+            }
+            st_shared_v4(swz(ps, rr, c, un), pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
+                         pack_bf16(e[6], e[7]));
+          }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full[b]));
+      }
+      if (!ok) {
+        if (lane == 0) give_up();
+        break;
+      }
+      // ---- epilogue: O / l after the last PV
+      const uint32_t pg = g - 1;
+      if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      tc_fence_after();
+      uint32_t o[64];
+      tmem_ld32(tO + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o));
+      tmem_ld32(tO + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      const float inv = 1.f / l;
+      if (lane == 0) bulk_wait_read_0();  // the previous item's store has read the staging tile
+      __syncwarp();
+#pragma unroll
+      for (int un = 0; un < 8; ++un)
+        st_shared_v4(stage + uint32_t(lane) * 128 + (uint32_t(un ^ (lane & 7)) << 4),
+                     pack_bf16(__uint_as_float(o[8 * un]) * inv, __uint_as_float(o[8 * un + 1]) * inv),
+                     pack_bf16(__uint_as_float(o[8 * un + 2]) * inv, __uint_as_float(o[8 * un + 3]) * inv),
+                     pack_bf16(__uint_as_float(o[8 * un + 4]) * inv, __uint_as_float(o[8 * un + 5]) * inv),
+                     pack_bf16(__uint_as_float(o[8 * un + 6]) * inv, __uint_as_float(o[8 * un + 7]) * inv));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_4d(&tmO, stage, 0, it.h, it.qt * BT + qw * 32, it.b);
+        bulk_commit();
+      }
+      if (row < p.S)
+        p.lse[(int64_t(it.b) * p.H + it.h) * p.S + row] = (m * p.sc + log2f(l)) * kLn2;
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TCOLS);
+  }
+}
+
+// ------------------------------------------------------------------------------ backward
+
+struct BwdParams {
+  int B, H, S, nq, items, causal;
+  float sc;          // α·log2 e
+  float alpha;       // α = 1/√hd
+  const float* lse;  // [B, H, S] natural log, from the forward
+  const float* D;    // [B, H, S] rowsum(dO ∘ O)
+  uint32_t* flag;
+};
+
+// D[b, h, s] = Σ_c dO[t, h·hd + c]·O[t, h·hd + c], t = b·S + s: 8 threads per (t, h), four
+// (t, h) rows per warp; the loop runs warp-uniformly so the shuffles see every lane.
+__global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dO, int64_t ld_o, int B,
+                                  int S, int H, float* __restrict__ D) {
+  const int64_t n = int64_t(B) * S * H;
+  const int lane = threadIdx.x & 31, sub = lane & 7;
+  const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp0 * 4; base < n; base += nwarps * 4) {
+    const int64_t r = base + (lane >> 3);
+    const bool act = r < n;
+    float acc = 0.f;
+    int64_t t = 0;
+    int h = 0;
+    if (act) {
+      t = r / H;
+      h = int(r - t * H);
+      const int64_t off = t * ld_o + int64_t(h) * HD + sub * 8;
+      float a[8], b[8];
+      Vec<bf16>::load(o + off, a);
+      Vec<bf16>::load(dO + off, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (act && sub == 0) {
+      const int64_t bb = t / S, ss = t - bb * S;
+      D[(bb * H + h) * S + ss] = acc;
+    }
+  }
+}
+
+// Work item of the key-tile kernel: (b, h, key tile kt); query tiles kt.. (causal) or all.
+__device__ __forceinline__ Item decode_kv(int i, int B, int H, int nq, int causal) {
+  const int bh_n = B * H;
+  Item it;
+  const int t = i / bh_n, bh = i - t * bh_n;
+  it.qt = t;  // the key tile
+  it.b = bh / H;
+  it.h = bh - it.b * H;
+  it.nkv = causal ? nq - t : nq;  // number of query tiles
+  return it;
+}
+
+// Staged TMA store of one warp's 32 rows × 64 bf16 (values × scale) from TMEM columns [col, col + 64).
+__device__ __forceinline__ void store_rows(uint32_t taddr, float scale, uint32_t stage, int lane,
+                                           const CUtensorMap* tm, int h, int y, int b) {
+  uint32_t o[64];
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(o));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+  tmem_ld_wait();
+#pragma unroll
+  for (int un = 0; un < 8; ++un)
+    st_shared_v4(stage + uint32_t(lane) * 128 + (uint32_t(un ^ (lane & 7)) << 4),
+                 pack_bf16(__uint_as_float(o[8 * un]) * scale, __uint_as_float(o[8 * un + 1]) * scale),
+                 pack_bf16(__uint_as_float(o[8 * un + 2]) * scale, __uint_as_float(o[8 * un + 3]) * scale),
+                 pack_bf16(__uint_as_float(o[8 * un + 4]) * scale, __uint_as_float(o[8 * un + 5]) * scale),
+                 pack_bf16(__uint_as_float(o[8 * un + 6]) * scale, __uint_as_float(o[8 * un + 7]) * scale));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_4d(tm, stage, 0, h, y, b);
+    bulk_commit();
+  }
+}
+
+struct KvSmem {
+  static constexpr int K = 0;
+  static constexpr int V = K + TILE;
+  static constexpr int QD = V + TILE;            // 2 slots × (Q tile, dO tile)
+  static constexpr int P = QD + 2 * 2 * TILE;    // Pᵀ  [keys × queries]
+  static constexpr int DS = P + PT;              // dSᵀ [keys × queries]
+  static constexpr int STAGE = DS + PT;          // 4 warps × (dV, dK) × 4 KB
+  static constexpr int VEC = STAGE + 8 * 4096;   // 2 slots × (lse·log2 e, D) × 128 floats
+  static constexpr int BARS = VEC + 2 * 2 * 512;
+  static constexpr int BYTES = 1024 + BARS + 256;
+};
+
+// dK, dV for one 128-key tile per work item: thread = key row; Sᵀ = K Qᵀ and dPᵀ = V dOᵀ per
+// query tile, Pᵀ = 2^(Sᵀ·sc − lse2[q]) (0 where q < key or q ≥ S), dSᵀ = Pᵀ ∘ (dPᵀ − D[q]);
+// dV += Pᵀ dO and dK += dSᵀ Q accumulate in TMEM; dK is scaled by α on the way out.
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
+                       const BwdParams p) {
+  constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_O = instr_desc_bf16(128, HD, false, true);
+  constexpr uint32_t TCOLS = 512;  // Sᵀ0 [0,128), Sᵀ1 [128,256), dPᵀ [256,384), dV [384,448), dK [448,512)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + KvSmem::BARS);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* qd_full = bars + 2;     // [2]
+  uint64_t* qd_empty = bars + 4;    // [2]
+  uint64_t* s_full = bars + 6;      // [2]
+  uint64_t* s_free = bars + 8;      // [2]
+  uint64_t* dp_full = bars + 10;
+  uint64_t* dp_free = bars + 11;
+  uint64_t* p_full = bars + 12;
+  uint64_t* p_free = bars + 13;
+  uint64_t* ds_full = bars + 14;
+  uint64_t* ds_free = bars + 15;
+  uint64_t* vec_full = bars + 16;   // [2] the query tile's lse / D rows are in shared memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* vec = reinterpret_cast<float*>(smem + KvSmem::VEC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(kv_full), 1);
+    mbar_init(smem_u32(kv_empty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&qd_full[b]), 1);
+      mbar_init(smem_u32(&qd_empty[b]), 1);
+      mbar_init(smem_u32(&s_full[b]), 1);
+      mbar_init(smem_u32(&s_free[b]), 4);
+    }
+    mbar_init(smem_u32(dp_full), 1);
+    mbar_init(smem_u32(dp_free), 4);
+    mbar_init(smem_u32(p_full), 4);
+    mbar_init(smem_u32(p_free), 1);
+    mbar_init(smem_u32(ds_full), 4);
+    mbar_init(smem_u32(ds_free), 1);
+    mbar_init(smem_u32(&vec_full[0]), 128);
+    mbar_init(smem_u32(&vec_full[1]), 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tDP = tbase + 256, tDV = tbase + 384, tDK = tbase + 448;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_error(p.flag, XT_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- TMA producer
+      int slot = 0, nkv = 0, nqd = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+        const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
+        if (!mbar_wait(smem_u32(kv_empty), (nkv & 1) ^ 1)) { ok = false; break; }
+        mbar_expect_tx(smem_u32(kv_full), 2 * TILE);
+        tma_load_4d(sb + KvSmem::K, &tmK, smem_u32(kv_full), 0, it.h, it.qt * BT, it.b);
+        tma_load_4d(sb + KvSmem::V, &tmV, smem_u32(kv_full), 0, it.h, it.qt * BT, it.b);
+        ++nkv;
+        const int q_first = p.causal ? it.qt : 0;
+        for (int j = 0; j < it.nkv; ++j) {
+          if (*abort_flag || !mbar_wait(smem_u32(&qd_empty[slot]), ph ^ 1)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&qd_full[slot]);
+          mbar_expect_tx(fb, 2 * TILE);
+          const uint32_t dst = sb + KvSmem::QD + slot * 2 * TILE;
+          tma_load_4d(dst, &tmQ, fb, 0, it.h, (q_first + j) * BT, it.b);
+          tma_load_4d(dst + TILE, &tmDO, fb, 0, it.h, (q_first + j) * BT, it.b);
+          ++nqd;
+          if (++slot == 2) { slot = 0; ph ^= 1; }
+        }
+      }
+      if (!ok) give_up();
+      bool drained = true;
+      if (nkv > 0) drained &= mbar_wait(smem_u32(kv_full), (nkv - 1) & 1);
+      for (int n = 0; n < (nqd < 2 ? nqd : 2); ++n) {
+        if (--slot < 0) { slot = 1; ph ^= 1; }
+        drained &= mbar_wait(smem_u32(&qd_full[slot]), ph);
+      }
+      if (!drained) give_up();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      int nkv = 0;
+      uint32_t g = 0;  // query tiles processed so far (ring slot, buffers and phases)
+      bool ok = true;
+      auto slot_addr = [&](uint32_t gg) { return sb + KvSmem::QD + uint32_t(gg & 1) * 2 * TILE; };
+      auto issue_s = [&](uint32_t gg) -> bool {  // Sᵀ = K Qᵀ into buffer gg & 1
+        const int b = int(gg & 1);
+        const uint32_t u = gg >> 1;
+        if (!mbar_wait(smem_u32(&qd_full[b]), u & 1) || !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma<false>(tbase + uint32_t(b * 128), smem_desc(sb + KvSmem::K + kk * 32, 16, 1024),
+                        smem_desc(slot_addr(gg) + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(smem_u32(&s_full[b]));
+        return true;
+      };
+      auto issue_dp = [&](uint32_t gg) -> bool {  // dPᵀ = V dOᵀ
+        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma<false>(tDP, smem_desc(sb + KvSmem::V + kk * 32, 16, 1024),
+                        smem_desc(slot_addr(gg) + TILE + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(smem_u32(dp_full));
+        return true;
+      };
+      auto issue_dvdk = [&](uint32_t gg, bool first) -> bool {
+        if (!mbar_wait(smem_u32(p_full), gg & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)  // dV += Pᵀ dO (dO tile read MN-major)
+          tc_mma<false>(tDV, smem_desc(sb + KvSmem::P + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
+                        smem_desc(slot_addr(gg) + TILE + kk * 2048, TILE, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(p_free));
+        if (!mbar_wait(smem_u32(ds_full), gg & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)  // dK += dSᵀ Q (Q tile read MN-major)
+          tc_mma<false>(tDK, smem_desc(sb + KvSmem::DS + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
+                        smem_desc(slot_addr(gg) + kk * 2048, TILE, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(ds_free));
+        tc_commit(smem_u32(&qd_empty[gg & 1]));
+        return true;
+      };
+      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+        const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
+        if (!mbar_wait(smem_u32(kv_full), nkv & 1)) { ok = false; break; }
+        ++nkv;
+        tc_fence_after();
+        const uint32_t g0 = g;
+        if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
+        for (int j = 0; j < it.nkv; ++j) {
+          const uint32_t gg = g0 + uint32_t(j);
+          if (*abort_flag) { ok = false; break; }
+          if (j + 1 < it.nkv && !issue_s(gg + 1)) { ok = false; break; }
+          if (!issue_dvdk(gg, j == 0)) { ok = false; break; }
+          if (j + 1 < it.nkv && !issue_dp(gg + 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(kv_empty));
+        g = g0 + uint32_t(it.nkv);
+      }
+      if (!ok) give_up();
+    }
+  } else {
+    // ---------------------------------------------------------------- Pᵀ / dSᵀ rows, epilogue
+    const int qw = warp & 3;
+    const int rr = qw * 32 + lane;  // key row within the tile
+    const uint32_t lane_off = uint32_t(qw * 32) << 16;
+    const uint32_t stage = sb + KvSmem::STAGE + uint32_t(qw) * 8192;
+    uint32_t g = 0;
+    for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
+      const int q_first = p.causal ? it.qt : 0;
+      const int64_t bh = int64_t(it.b) * p.H + it.h;
+      bool ok = true;
+      for (int j = 0; j < it.nkv; ++j, ++g) {
+        const int b = int(g & 1);
+        const uint32_t u = g >> 1;
+        const int q0 = (q_first + j) * BT;
+        // this query tile's lse·log2 e and D, shared by the four warps through slot g & 1 (a
+        // thread refills a slot only after every thread has arrived for the tile in between,
+        // i.e. has finished reading it)
+        float* lv = vec + b * 256;
+        {
+          const int q = q0 + rr;
+          lv[rr] = q < p.S ? p.lse[bh * p.S + q] * kLog2e : INFINITY;
+          lv[128 + rr] = q < p.S ? p.D[bh * p.S + q] : 0.f;
+        }
+        mbar_arrive(smem_u32(&vec_full[b]));
+        if (!warp_wait(smem_u32(&vec_full[b]), u & 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
+        // Pᵀ[key rr][query c]; the diagonal tile hides queries before this key
+        const int first = (p.causal && q_first + j == it.qt) ? rr : 0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float e = exp2f(fmaf(__uint_as_float(r[c]), p.sc, -lv[c]));
+          r[c] = __float_as_uint(c < first ? 0.f : e);
+        }
+        if (!warp_wait(smem_u32(p_free), (g & 1) ^ 1)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int un = 0; un < 8; ++un) {
+            const int c0 = c * 64 + un * 8;
+            st_shared_v4(swz(sb + KvSmem::P, rr, c, un),
+                         pack_bf16(__uint_as_float(r[c0]), __uint_as_float(r[c0 + 1])),
+                         pack_bf16(__uint_as_float(r[c0 + 2]), __uint_as_float(r[c0 + 3])),
+                         pack_bf16(__uint_as_float(r[c0 + 4]), __uint_as_float(r[c0 + 5])),
+                         pack_bf16(__uint_as_float(r[c0 + 6]), __uint_as_float(r[c0 + 7])));
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(p_full));
+        // dSᵀ = Pᵀ ∘ (dPᵀ − D), 32 query columns at a time
+        if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(ds_free), (g & 1) ^ 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t d[32];
+          tmem_ld32(tDP + lane_off + uint32_t(c * 32), d);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(dp_free));
+          }
+#pragma unroll
+          for (int un = 0; un < 4; ++un) {
+            float ds[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int cc = c * 32 + un * 8 + t;
+              ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - lv[128 + cc]);
+            }
+            st_shared_v4(swz(sb + KvSmem::DS, rr, c >> 1, (c & 1) * 4 + un), pack_bf16(ds[0], ds[1]),
+                         pack_bf16(ds[2], ds[3]), pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(ds_full));
+      }
+      if (!ok) {
+        if (lane == 0) give_up();
+        break;
+      }
+      // ---- epilogue: dV, α·dK once the last tile's MMAs are done
+      if (!warp_wait(smem_u32(ds_free), (g - 1) & 1)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) bulk_wait_read_0();
+      __syncwarp();
+      const int y = it.qt * BT + qw * 32;
+      store_rows(tDV + lane_off, 1.f, stage, lane, &tmDV, it.h, y, it.b);
+      store_rows(tDK + lane_off, p.alpha, stage + 4096, lane, &tmDK, it.h, y, it.b);
+      tc_fence_before();
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TCOLS);
+  }
+}
+
+struct QSmem {
+  static constexpr int Q = 0;
+  static constexpr int DO = Q + TILE;
+  static constexpr int KV = DO + TILE;           // RING slots × (K tile, V tile)
+  static constexpr int DS = KV + RING * 2 * TILE;
+  static constexpr int STAGE = DS + 2 * PT;      // 4 warps × 4 KB
+  static constexpr int BARS = STAGE + 4 * 4096;
+  static constexpr int BYTES = 1024 + BARS + 256;
+};
+
+// dQ for one 128-query tile per work item: thread = query row; S = Q Kᵀ and dP = dO Vᵀ per key
+// tile, P = 2^(S·sc − lse2) (0 where key > query or key ≥ S), dS = P ∘ (dP − D);
+// dQ += dS K accumulates in TMEM and is scaled by α on the way out.
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                      const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+  constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_O = instr_desc_bf16(128, HD, false, true);
+  constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), dP [256,384), dQ [384,448)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QSmem::BARS);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;            // [RING]
+  uint64_t* kv_empty = kv_full + RING;     // [RING]
+  uint64_t* s_full = kv_empty + RING;      // [2]
+  uint64_t* s_free = s_full + 2;           // [2]
+  uint64_t* dp_full = s_free + 2;
+  uint64_t* dp_free = dp_full + 1;
+  uint64_t* ds_full = dp_free + 1;         // [2]
+  uint64_t* ds_free = ds_full + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ds_free + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(q_empty), 1);
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(smem_u32(&kv_full[s]), 1);
+      mbar_init(smem_u32(&kv_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&s_full[b]), 1);
+      mbar_init(smem_u32(&s_free[b]), 4);
+      mbar_init(smem_u32(&ds_full[b]), 4);
+      mbar_init(smem_u32(&ds_free[b]), 1);
+    }
+    mbar_init(smem_u32(dp_full), 1);
+    mbar_init(smem_u32(dp_free), 4);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tDP = tbase + 256, tDQ = tbase + 384;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_error(p.flag, XT_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- TMA producer
+      int ks = 0, nk = 0, nqi = 0;
+      uint32_t kph = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+        const Item it = decode(i, p.B, p.H, p.nq, p.causal);
+        if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1)) { ok = false; break; }
+        mbar_expect_tx(smem_u32(q_full), 2 * TILE);
+        tma_load_4d(sb + QSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
+        tma_load_4d(sb + QSmem::DO, &tmDO, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
+        ++nqi;
+        for (int j = 0; j < it.nkv; ++j) {
+          if (*abort_flag || !mbar_wait(smem_u32(&kv_empty[ks]), kph ^ 1)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&kv_full[ks]);
+          mbar_expect_tx(fb, 2 * TILE);
+          const uint32_t dst = sb + QSmem::KV + ks * 2 * TILE;
+          tma_load_4d(dst, &tmK, fb, 0, it.h, j * BT, it.b);
+          tma_load_4d(dst + TILE, &tmV, fb, 0, it.h, j * BT, it.b);
+          ++nk;
+          if (++ks == RING) { ks = 0; kph ^= 1; }
+        }
+      }
+      if (!ok) give_up();
+      bool drained = true;
+      if (nqi > 0) drained &= mbar_wait(smem_u32(q_full), (nqi - 1) & 1);
+      for (int n = 0; n < (nk < RING ? nk : RING); ++n) {
+        if (--ks < 0) { ks = RING - 1; kph ^= 1; }
+        drained &= mbar_wait(smem_u32(&kv_full[ks]), kph);
+      }
+      if (!drained) give_up();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer
+      int nqi = 0;
+      uint32_t g = 0;  // key tiles processed so far
+      bool ok = true;
+      auto kv_addr = [&](uint32_t gg) { return sb + QSmem::KV + uint32_t(gg % RING) * 2 * TILE; };
+      auto issue_s = [&](uint32_t gg) -> bool {
+        const int b = int(gg & 1);
+        const uint32_t u = gg >> 1;
+        if (!mbar_wait(smem_u32(&kv_full[gg % RING]), (gg / RING) & 1) ||
+            !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma<false>(tbase + uint32_t(b * 128), smem_desc(sb + QSmem::Q + kk * 32, 16, 1024),
+                        smem_desc(kv_addr(gg) + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(smem_u32(&s_full[b]));
+        return true;
+      };
+      auto issue_dp = [&](uint32_t gg) -> bool {
+        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma<false>(tDP, smem_desc(sb + QSmem::DO + kk * 32, 16, 1024),
+                        smem_desc(kv_addr(gg) + TILE + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(smem_u32(dp_full));
+        return true;
+      };
+      auto issue_dq = [&](uint32_t gg, bool first) -> bool {
+        const int b = int(gg & 1);
+        if (!mbar_wait(smem_u32(&ds_full[b]), (gg >> 1) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K (K tile read MN-major)
+          tc_mma<false>(tDQ, smem_desc(sb + QSmem::DS + b * PT + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
+                        smem_desc(kv_addr(gg) + kk * 2048, TILE, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&ds_free[b]));
+        tc_commit(smem_u32(&kv_empty[gg % RING]));
+        return true;
+      };
+      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+        const Item it = decode(i, p.B, p.H, p.nq, p.causal);
+        if (!mbar_wait(smem_u32(q_full), nqi & 1)) { ok = false; break; }
+        ++nqi;
+        tc_fence_after();
+        const uint32_t g0 = g;
+        if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
+        for (int j = 0; j < it.nkv; ++j) {
+          const uint32_t gg = g0 + uint32_t(j);
+          if (*abort_flag) { ok = false; break; }
+          if (j + 1 < it.nkv && !issue_s(gg + 1)) { ok = false; break; }
+          if (!issue_dq(gg, j == 0)) { ok = false; break; }
+          if (j + 1 < it.nkv && !issue_dp(gg + 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(q_empty));
+        g = g0 + uint32_t(it.nkv);
+      }
+      if (!ok) give_up();
+    }
+  } else {
+    // ---------------------------------------------------------------- P / dS rows, epilogue
+    const int qw = warp & 3;
+    const int rr = qw * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = uint32_t(qw * 32) << 16;
+    const uint32_t stage = sb + QSmem::STAGE + uint32_t(qw) * 4096;
+    uint32_t g = 0;
+    for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const Item it = decode(i, p.B, p.H, p.nq, p.causal);
+      const int row = it.qt * BT + rr;
+      const int64_t bh = int64_t(it.b) * p.H + it.h;
+      const float lse2 = row < p.S ? p.lse[bh * p.S + row] * kLog2e : INFINITY;
+      const float Dr = row < p.S ? p.D[bh * p.S + row] : 0.f;
+      bool ok = true;
+      for (int j = 0; j < it.nkv; ++j, ++g) {
+        const int b = int(g & 1);
+        const uint32_t u = g >> 1;
+        if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
+        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float e = exp2f(fmaf(__uint_as_float(r[c]), p.sc, -lse2));
+          r[c] = __float_as_uint(c < lim ? e : 0.f);
+        }
+        if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(&ds_free[b]), (u & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dsb = sb + QSmem::DS + b * PT;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t d[32];
+          tmem_ld32(tDP + lane_off + uint32_t(c * 32), d);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(dp_free));
+          }
+#pragma unroll
+          for (int un = 0; un < 4; ++un) {
+            float ds[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int cc = c * 32 + un * 8 + t;
+              ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - Dr);
+            }
+            st_shared_v4(swz(dsb, rr, c >> 1, (c & 1) * 4 + un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
+                         pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ds_full[b]));
+      }
+      if (!ok) {
+        if (lane == 0) give_up();
+        break;
+      }
+      const uint32_t pg = g - 1;
+      if (!warp_wait(smem_u32(&ds_free[pg & 1]), (pg >> 1) & 1)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) bulk_wait_read_0();
+      __syncwarp();
+      store_rows(tDQ + lane_off, p.alpha, stage, lane, &tmDQ, it.h, it.qt * BT + qw * 32, it.b);
+      tc_fence_before();
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TCOLS);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+
+// [B, S, H, hd] view of a row-major [B·S, ld] matrix whose head h occupies columns h·hd..:
+// dims (innermost first) hd, H, S, B; box 64 × 1 × rows × 1, 128-byte swizzle.
+static int head_map(CUtensorMap* tm, const void* base, int64_t ld, int B, int S, int H, int rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(XT_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[4] = {cuuint64_t(HD), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
+  cuuint64_t strides[3] = {cuuint64_t(HD * 2), cuuint64_t(ld * 2), cuuint64_t(int64_t(S) * ld * 2)};
+  cuuint32_t box[4] = {HD, 1, cuuint32_t(rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(XT_ERR_CUDA, "attention: cuTensorMapEncodeTiled failed (%d)", int(r));
+  return XT_OK;
+}
+
+static int check_common(const char* fn, int B, int S, int H, int hd, int causal, int dt, int64_t ld_in,
+                        int64_t ld_out, std::initializer_list<const void*> ptrs) {
+  XT_REQUIRE(B >= 0 && S >= 0 && H >= 0, "%s: negative size", fn);
+  XT_REQUIRE(causal == 0 || causal == 1, "%s: causal must be 0 or 1", fn);
+  if (dt != XT_BF16) return fail(XT_ERR_UNSUPPORTED, "%s: only bf16 is supported", fn);
+  if (hd != HD) return fail(XT_ERR_UNSUPPORTED, "%s: head_dim must be %d", fn, HD);
+  XT_REQUIRE(ld_in >= int64_t(H) * hd && ld_out >= int64_t(H) * hd, "%s: row stride smaller than H·hd", fn);
+  if ((ld_in % 8) || (ld_out % 8)) return fail(XT_ERR_ALIGNMENT, "%s: row strides must be multiples of 8", fn);
+  for (const void* q : ptrs) {
+    if (B * S * H == 0) break;
+    XT_REQUIRE(q != nullptr, "%s: NULL pointer", fn);
+    if (!aligned16(q)) return fail(XT_ERR_ALIGNMENT, "%s: pointers must be 16-byte aligned", fn);
+  }
+  return XT_OK;
+}
+
+// Raises a kernel's dynamic shared-memory limit once (`done` is the call site's flag).
+static int set_smem(const void* k, int bytes, bool& done, const char* what) {
+  if (done) return XT_OK;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail(XT_ERR_CUDA, "%s: shared memory attribute: %s", what, cudaGetErrorString(e));
+  done = true;
+  return XT_OK;
+}
+
+}  // namespace attn
+}  // namespace xt
+
+using namespace xt;
+using namespace xt::attn;
+
+extern "C" {
+
+int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, int64_t ld_o, float* lse,
+                     int B, int S, int H, int hd, int causal, int dt, void* stream) {
+  XT_TRY(check_common("xt_attention_fwd", B, S, H, hd, causal, dt, ld_qkv, ld_o, {q, k, v, o, lse}));
+  if (int64_t(B) * S * H == 0) return XT_OK;
+  CUtensorMap tq, tk, tv, to;
+  XT_TRY(head_map(&tq, q, ld_qkv, B, S, H, BT));
+  XT_TRY(head_map(&tk, k, ld_qkv, B, S, H, BT));
+  XT_TRY(head_map(&tv, v, ld_qkv, B, S, H, BT));
+  XT_TRY(head_map(&to, o, ld_o, B, S, H, 32));
+  FwdParams p{};
+  p.B = B;
+  p.H = H;
+  p.S = S;
+  p.nq = int(ceil_div(S, BT));
+  p.items = B * H * p.nq;
+  p.causal = causal;
+  p.sc = float(1.0 / std::sqrt(double(hd)) * 1.4426950408889634);
+  p.lse = lse;
+  p.flag = errflag();
+  static bool smem_set = false;
+  XT_TRY(set_smem(reinterpret_cast<const void*>(attn_fwd_kernel), FwdSmem::BYTES, smem_set, "xt_attention_fwd"));
+  const int grid = p.items < num_sms() ? p.items : num_sms();
+  attn_fwd_kernel<<<grid, attn::kThreads, FwdSmem::BYTES, as_stream(stream)>>>(tq, tk, tv, to, p);
+  return check_launch("xt_attention_fwd");
+}
+
+int xt_attention_bwd_workspace_size(int B, int S, int H, size_t* bytes) {
+  XT_REQUIRE(B >= 0 && S >= 0 && H >= 0 && bytes, "xt_attention_bwd_workspace_size: bad arguments");
+  *bytes = (size_t(B) * size_t(S) * size_t(H) * 4 + 255) & ~size_t(255);
+  return XT_OK;
+}
+
+int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o, const void* d_o,
+                     int64_t ld_o, const float* lse, void* dq, void* dk, void* dv, int64_t ld_dqkv, void* ws,
+                     size_t ws_bytes, int B, int S, int H, int hd, int causal, int dt, void* stream) {
+  XT_TRY(check_common("xt_attention_bwd", B, S, H, hd, causal, dt, ld_qkv, ld_o,
+                      {q, k, v, o, d_o, lse, dq, dk, dv, ws}));
+  XT_REQUIRE(ld_dqkv >= int64_t(H) * hd, "xt_attention_bwd: ld_dqkv smaller than H·hd");
+  if (ld_dqkv % 8) return fail(XT_ERR_ALIGNMENT, "xt_attention_bwd: ld_dqkv must be a multiple of 8");
+  if (int64_t(B) * S * H == 0) return XT_OK;
+  size_t need = 0;
+  xt_attention_bwd_workspace_size(B, S, H, &need);
+  XT_REQUIRE(ws_bytes >= need, "xt_attention_bwd: workspace too small (%zu < %zu)", ws_bytes, need);
+  cudaStream_t s = as_stream(stream);
+  float* D = static_cast<float*>(ws);
+  {
+    const int64_t threads = int64_t(B) * S * H * 8;
+    int64_t blocks = ceil_div(threads, 256);
+    const int64_t cap = int64_t(num_sms()) * 8;
+    if (blocks > cap) blocks = cap;
+    attn_delta_kernel<<<int(blocks), 256, 0, s>>>(static_cast<const bf16*>(o), static_cast<const bf16*>(d_o), ld_o,
+                                                   B, S, H, D);
+    XT_TRY(check_launch("xt_attention_bwd (delta)"));
+  }
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  XT_TRY(head_map(&tq, q, ld_qkv, B, S, H, BT));
+  XT_TRY(head_map(&tk, k, ld_qkv, B, S, H, BT));
+  XT_TRY(head_map(&tv, v, ld_qkv, B, S, H, BT));
+  XT_TRY(head_map(&tdo, d_o, ld_o, B, S, H, BT));
+  XT_TRY(head_map(&tdq, dq, ld_dqkv, B, S, H, 32));
+  XT_TRY(head_map(&tdk, dk, ld_dqkv, B, S, H, 32));
+  XT_TRY(head_map(&tdv, dv, ld_dqkv, B, S, H, 32));
+  BwdParams p{};
+  p.B = B;
+  p.H = H;
+  p.S = S;
+  p.nq = int(ceil_div(S, BT));
+  p.items = B * H * p.nq;
+  p.causal = causal;
+  p.alpha = float(1.0 / std::sqrt(double(hd)));
+  p.sc = float(1.0 / std::sqrt(double(hd)) * 1.4426950408889634);
+  p.lse = lse;
+  p.D = D;
+  p.flag = errflag();
+  const int grid = p.items < num_sms() ? p.items : num_sms();
+  static bool kv_set = false, q_set = false;
+  XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel), KvSmem::BYTES, kv_set, "xt_attention_bwd"));
+  XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_q_kernel), QSmem::BYTES, q_set, "xt_attention_bwd"));
+  attn_bwd_kv_kernel<<<grid, attn::kThreads, KvSmem::BYTES, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  XT_TRY(check_launch("xt_attention_bwd (dK, dV)"));
+  attn_bwd_q_kernel<<<grid, attn::kThreads, QSmem::BYTES, s>>>(tq, tk, tv, tdo, tdq, p);
+  return check_launch("xt_attention_bwd (dQ)");
+}
+
+}  // extern "C"

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "gemm_kernel.cuh"
@@ -43,6 +44,8 @@ Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int c
 size_t split_bytes(const Choice& c, int64_t M, int64_t N);
 
 int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn);
+// The driver's cuTensorMapEncodeTiled (null when the driver does not provide it).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 int run(const Problem& pb, cudaStream_t s);
 int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const Params& p, int grid, cudaStream_t s);

@@ -100,6 +100,10 @@ _SIGS = {
     "xt_rope_bwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _I, _VP],
     "xt_softmax_fwd": [_VP, _VP, _I64, _I64, _I, _I64, _I, _VP],
     "xt_softmax_bwd": [_VP, _VP, _VP, _I64, _I64, _I, _I64, _I, _I, _VP],
+    "xt_attention_fwd": [_VP, _VP, _VP, _I64, _VP, _I64, _VP, _I, _I, _I, _I, _I, _I, _VP],
+    "xt_attention_bwd_workspace_size": [_I, _I, _I, _SZP],
+    "xt_attention_bwd": [_VP, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _VP, _VP, _VP, _I64, _VP, C.c_size_t,
+                         _I, _I, _I, _I, _I, _I, _VP],
     "xt_cross_entropy_workspace_size": [_I64, _SZP],
     "xt_cross_entropy_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _I, _VP, _VP],
     "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
@@ -384,6 +388,22 @@ def xt_softmax_fwd(x, y, causal=0, q_len=0, s=None):
     cols = x.shape[-1]
     rows = x.numel() // cols
     call("xt_softmax_fwd", ptr(x), ptr(y), rows, cols, causal, q_len, dt(x), stream(s))
+
+
+def xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, causal=1, s=None):
+    """q, k, v: [B·S, ld] views (head h at columns h·hd); o: [B·S, ld_o]; lse: float32 [B, H, S]."""
+    call("xt_attention_fwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False), o.stride(0),
+         ptr(lse), B, S, H, hd, causal, dt(q), stream(s))
+
+
+def xt_attention_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, S, H, hd, causal=1, ws=None, s=None):
+    n = C.c_size_t(0)
+    call("xt_attention_bwd_workspace_size", B, S, H, C.byref(n))
+    if ws is None:
+        ws = torch.empty(max(1, n.value), dtype=torch.uint8, device=q.device)
+    call("xt_attention_bwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False),
+         ptr(d_o, False), o.stride(0), ptr(lse), ptr(dq, False), ptr(dk, False), ptr(dv, False), dq.stride(0),
+         ptr(ws), ws.numel(), B, S, H, hd, causal, dt(q), stream(s))
 
 
 def xt_softmax_bwd(d, y, dx, causal=0, q_len=0, acc=0, s=None):
