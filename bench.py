@@ -2,9 +2,9 @@
 """Benchmark of the block-stack hot path on GB300: forward + backward tokens/s.
 
 One step = zero the gradient buffers, xt_block_fwd, xt_block_bwd on one batch of synthetic
-tokens (every op of the stack: embedding, norms, QKV / attention / projection / MLP GEMMs,
-RoPE when configured, causal softmax, dropout-residual adds, tied logits, cross-entropy and
-all backward kernels).  Default workload: the 12-layer GPT-style stack (B 8, S 1024, d 768,
+tokens (every op of the stack: embedding, norms, QKV / projection / MLP GEMMs, the fused causal
+attention, RoPE when configured, dropout-residual adds, tied logits, cross-entropy and all
+backward kernels).  Default workload: the 12-layer GPT-style stack (B 8, S 1024, d 768,
 12 heads × 64, LayerNorm, exact-GELU MLP 3072, learned positions, tied 50304-vocab output,
 bf16 storage with fp32 accumulation, fp32 parameter gradients).
 
@@ -30,8 +30,8 @@ METRIC = "block fwd+bwd tokens/s on 1 GB300; per-kernel HBM GB/s and GEMM TFLOP/
 
 WORKLOAD_TEXT = {
     "gpt12": "12-layer pre-norm GPT stack: B8 S1024 d768 H12x64, LayerNorm, exact-GELU MLP 3072, learned "
-             "positions, tied 50304-vocab logits + mean CE, causal composed attention, bf16 storage, fp32 "
-             "accumulate / statistics / parameter grads",
+             "positions, tied 50304-vocab logits + mean CE, causal fused attention (tcgen05, probabilities never "
+             "stored), bf16 storage, fp32 accumulate / statistics / parameter grads",
     "block256": "1 pre-norm block: B4 S256 d256 H4x64, RMSNorm, RoPE, SwiGLU 688, tied 4096-vocab logits + mean CE, "
                 "causal composed attention, residual dropout p=0.1, fp32 storage, tf32 tensor-core GEMMs",
     "tiny": "1 pre-norm block: B1 S16 d32 H2x16, RMSNorm, RoPE, SwiGLU 64, tied 64-vocab logits, fp32",

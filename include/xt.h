@@ -234,18 +234,22 @@ int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t
  * lse (float32 [B][H][S], written by the forward, read by the backward) is the natural-log
  * normaliser log Σ_c exp(scores[s, c]) over the visible keys.
  * dq, dk, dv are overwritten.  The backward's workspace (xt_attention_bwd_workspace_size)
- * holds D = Σ_c dO∘O per (b, h, s).
+ * holds D = Σ_c dO∘O per (b, h, s).  o32 (optional, may be NULL; float32, head h at columns
+ * h·hd of rows ld_o32 apart, 16-byte aligned rows) receives O before its bf16 rounding; passed
+ * to the backward it is the O that D is formed from, which keeps the rows of dS summing to ~0
+ * (with the bf16 O they carry its 2⁻⁹ rounding as a bias).
  * Supported: dt = XT_BF16, hd = 64, row strides multiples of 8 elements, all pointers
  * 16-byte aligned (else XT_ERR_UNSUPPORTED / XT_ERR_ALIGNMENT).  Device-side waits are
  * bounded; on expiry XT_DEVERR_TIMEOUT is set in the device error flag.
  * ------------------------------------------------------------------------------- */
 int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, int64_t ld_o,
-                     float* lse, int B, int S, int H, int hd, int causal, int dt, void* stream);
+                     float* lse, float* o32, int64_t ld_o32, int B, int S, int H, int hd, int causal, int dt,
+                     void* stream);
 int xt_attention_bwd_workspace_size(int B, int S, int H, size_t* bytes);
 int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o,
-                     const void* d_o, int64_t ld_o, const float* lse, void* dq, void* dk, void* dv,
-                     int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S, int H, int hd, int causal,
-                     int dt, void* stream);
+                     const void* d_o, int64_t ld_o, const float* lse, const float* o32, int64_t ld_o32,
+                     void* dq, void* dk, void* dv, int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S,
+                     int H, int hd, int causal, int dt, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Cross-entropy, mean over rows ([AE] op table row cross_entropy, § Cross-entropy 反向推导):
@@ -350,6 +354,11 @@ int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, cons
  * ------------------------------------------------------------------------------- */
 enum { XT_NORM_RMS = 0, XT_NORM_LN = 1 };
 enum { XT_MLP_SWIGLU = 0, XT_MLP_GELU = 1 };
+/* Attention path: AUTO runs the fused kernels (xt_attention_*) when dtype is XT_BF16, hd is
+ * 64 and d is a multiple of 8, else the composition of causal-tile GEMMs around the row
+ * softmax (which also saves P [B, H, S, S]); COMPOSED forces the latter; FUSED requires the
+ * former (XT_ERR_UNSUPPORTED otherwise). */
+enum { XT_ATTN_AUTO = 0, XT_ATTN_COMPOSED = 1, XT_ATTN_FUSED = 2 };
 
 typedef struct xt_block_config {
   int32_t B, S, d, H, hd, F, V, n_layers;
@@ -365,6 +374,7 @@ typedef struct xt_block_config {
   float p;            /* residual dropout probability */
   double rope_base;
   uint64_t base_seed;
+  int32_t attention;  /* XT_ATTN_AUTO, XT_ATTN_COMPOSED or XT_ATTN_FUSED */
 } xt_block_config;
 
 /* Per-layer parameter (and gradient) pointers; arrays of n_layers device pointers,

@@ -35,18 +35,22 @@ def make(B, S, H, seed, std=1.0):
     return qkv, dO
 
 
-def run(B, S, H, causal, qkv, dO):
+def run(B, S, H, causal, qkv, dO, with_o32=True):
+    """Forward then backward; with_o32 keeps the float32 O the backward's D is formed from."""
     d = H * HD
     Q = bf16_dev(qkv)
     o = torch.empty(B * S, d, dtype=torch.bfloat16, device="cuda")
+    o32 = torch.empty(B * S, d, dtype=torch.float32, device="cuda") if with_o32 else None
     lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
-    xt.xt_attention_fwd(Q[:, :d], Q[:, d:2 * d], Q[:, 2 * d:], o, lse, B, S, H, HD, causal)
+    xt.xt_attention_fwd(Q[:, :d], Q[:, d:2 * d], Q[:, 2 * d:], o, lse, B, S, H, HD, causal, o32=o32)
     dqkv = torch.empty(B * S, 3 * d, dtype=torch.bfloat16, device="cuda")
     dOd = bf16_dev(dO)
     xt.xt_attention_bwd(Q[:, :d], Q[:, d:2 * d], Q[:, 2 * d:], o, dOd, lse, dqkv[:, :d], dqkv[:, d:2 * d],
-                        dqkv[:, 2 * d:], B, S, H, HD, causal)
+                        dqkv[:, 2 * d:], B, S, H, HD, causal, o32=o32)
     torch.cuda.synchronize()
     assert xt.device_errors() == 0
+    if with_o32:   # the float32 O rounds to the bf16 O
+        assert torch.equal(o32.to(torch.bfloat16), o)
     return host(o), host(lse), host(dqkv)
 
 
@@ -78,9 +82,9 @@ def grad_err(g, r, mag=None):
     return float(np.linalg.norm(np.asarray(g) - r) / max(den, 1e-300))
 
 
-def check(B, S, H, causal, seed, std=1.0):
+def check(B, S, H, causal, seed, std=1.0, with_o32=True):
     qkv, dO = make(B, S, H, seed, std)
-    o, lse, dqkv = run(B, S, H, causal, qkv, dO)
+    o, lse, dqkv = run(B, S, H, causal, qkv, dO, with_o32)
     d = H * HD
     Ov, rl, dQ, dK, dV, mag = oracle(B, S, H, causal, qkv, dO)
     errs = {"O": norm_err(heads(o, B, S, H), Ov)}
@@ -96,6 +100,11 @@ def check(B, S, H, causal, seed, std=1.0):
                                           (2, 300, 2, 1), (1, 129, 1, 0), (3, 64, 2, 1)])
 def test_attention_parity(B, S, H, causal):
     check(B, S, H, causal, seed=300 + S + H)
+
+
+def test_attention_without_float32_o():
+    """The backward also accepts the bf16 O alone (D from the rounded O)."""
+    check(2, 200, 3, 1, seed=305, with_o32=False)
 
 
 def test_attention_large_scores():

@@ -72,6 +72,31 @@ def test_block_small_bf16():
     compare(cfg, params=synth.block_params(cfg, gain_jitter=0.1))
 
 
+def test_block_small_bf16_composed():
+    """The same stack through the composed attention (causal-tile GEMMs around the softmax)."""
+    cfg = variant("gpt12", B=2, S=256, d=128, H=2, hd=64, F=512, V=1000, n_layers=2, attention="composed")
+    compare(cfg, params=synth.block_params(cfg, gain_jitter=0.1))
+
+
+def test_block_bf16_rope_swiglu_dropout_fused():
+    """RMSNorm + RoPE + SwiGLU + residual dropout 0.1 in bf16 through the fused attention;
+    bit-identical on a second run."""
+    cfg = variant("block256", dtype="bf16", attention="fused")
+    compare(cfg, training=True)
+    params = synth.block_params(cfg)
+    ids, tgt = synth.block_tokens(cfg)
+    la, ga, _ = run_native(cfg, params, ids, tgt)
+    lb, gb, _ = run_native(cfg, params, ids, tgt)
+    assert la == lb
+    for k in ga:
+        assert np.array_equal(ga[k], gb[k]), k
+
+
+def test_block_fused_attention_needs_bf16():
+    with pytest.raises(xt.XtError):
+        NativeBlock(variant("block256", attention="fused"))
+
+
 def test_block_256():
     """Configuration 4×256, d 256, 4 heads, SwiGLU 688, vocab 4096, fp32, dropout 0.1."""
     compare(synth.BLOCK_CONFIGS["block256"], training=True)
@@ -112,11 +137,12 @@ def test_block_gpt12_full():
     assert max(errs.values()) <= 2e-2
 
 
-def test_block_graph_replay_matches_eager():
+@pytest.mark.parametrize("cfg", [synth.BLOCK_CONFIGS["block256"], variant("block256", dtype="bf16")],
+                         ids=["fp32-composed", "bf16-fused"])
+def test_block_graph_replay_matches_eager(cfg):
     """One step (zero grads, forward, backward) captured into a CUDA graph and replayed gives the
     eager step's loss and gradients bit for bit (dropout included: the masks are counter-based);
     GEMM timing events enqueued during the capture are re-recorded by every replay."""
-    cfg = synth.BLOCK_CONFIGS["block256"]
     params = synth.block_params(cfg)
     ids, tgt = synth.block_tokens(cfg)
     la, ga, _ = run_native(cfg, params, ids, tgt)

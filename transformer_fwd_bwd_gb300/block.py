@@ -32,6 +32,8 @@ def config_struct(cfg: dict, training: bool = True, base_seed: int = 0, grad_dty
     c.p = cfg["p"]
     c.rope_base = cfg["rope_base"]
     c.base_seed = base_seed & (2**64 - 1)
+    c.attention = {"auto": xt.XT_ATTN_AUTO, "composed": xt.XT_ATTN_COMPOSED,
+                   "fused": xt.XT_ATTN_FUSED}[cfg.get("attention", "auto")]
     return c
 
 

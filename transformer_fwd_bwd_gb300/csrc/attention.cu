@@ -46,6 +46,8 @@ struct FwdParams {
   int B, H, S, nq, items, causal;
   float sc;     // α·log2 e
   float* lse;   // [B, H, S], natural log
+  float* o32;   // optional float32 copy of O (row t, head h at column h·hd), row stride ld32
+  int64_t ld32;
   uint32_t* flag;
 };
 
@@ -361,8 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_4d(&tmO, stage, 0, it.h, it.qt * BT + qw * 32, it.b);
         bulk_commit();
       }
-      if (row < p.S)
+      if (row < p.S) {
         p.lse[(int64_t(it.b) * p.H + it.h) * p.S + row] = (m * p.sc + log2f(l)) * kLn2;
+        if (p.o32) {
+          float4* dst = reinterpret_cast<float4*>(p.o32 + (int64_t(it.b) * p.S + row) * p.ld32 + int64_t(it.h) * HD);
+#pragma unroll
+          for (int j = 0; j < HD / 4; ++j)
+            dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                 __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        }
+      }
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -386,9 +396,13 @@ struct BwdParams {
 };
 
 // D[b, h, s] = Σ_c dO[t, h·hd + c]·O[t, h·hd + c], t = b·S + s: 8 threads per (t, h), four
-// (t, h) rows per warp; the loop runs warp-uniformly so the shuffles see every lane.
-__global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ dO, int64_t ld_o, int B,
-                                  int S, int H, float* __restrict__ D) {
+// (t, h) rows per warp; the loop runs warp-uniformly so the shuffles see every lane.  O is the
+// forward's float32 copy when there is one: D then agrees with Σ_c P·dP of the recomputed P and
+// dP to float32 rounding, so the rows of dS = P∘(dP − D) sum to ~0 as they must; the bf16 O
+// would leave a bias of its rounding (2⁻⁹ relative) in every row of dS.
+template <typename TO>
+__global__ void attn_delta_kernel(const TO* __restrict__ o, int64_t ld_oo, const bf16* __restrict__ dO, int64_t ld_o,
+                                  int B, int S, int H, float* __restrict__ D) {
   const int64_t n = int64_t(B) * S * H;
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -402,10 +416,9 @@ __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __rest
     if (act) {
       t = r / H;
       h = int(r - t * H);
-      const int64_t off = t * ld_o + int64_t(h) * HD + sub * 8;
       float a[8], b[8];
-      Vec<bf16>::load(o + off, a);
-      Vec<bf16>::load(dO + off, b);
+      Acc<TO, 8>::load(o + t * ld_oo + int64_t(h) * HD + sub * 8, a);
+      Vec<bf16>::load(dO + t * ld_o + int64_t(h) * HD + sub * 8, b);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
     }
@@ -1071,8 +1084,12 @@ using namespace xt::attn;
 extern "C" {
 
 int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, int64_t ld_o, float* lse,
-                     int B, int S, int H, int hd, int causal, int dt, void* stream) {
+                     float* o32, int64_t ld_o32, int B, int S, int H, int hd, int causal, int dt, void* stream) {
   XT_TRY(check_common("xt_attention_fwd", B, S, H, hd, causal, dt, ld_qkv, ld_o, {q, k, v, o, lse}));
+  if (o32) {
+    XT_REQUIRE(ld_o32 >= int64_t(H) * hd, "xt_attention_fwd: ld_o32 smaller than H·hd");
+    if (!aligned16(o32) || ld_o32 % 4) return fail(XT_ERR_ALIGNMENT, "xt_attention_fwd: o32 must be 16-byte aligned rows");
+  }
   if (int64_t(B) * S * H == 0) return XT_OK;
   CUtensorMap tq, tk, tv, to;
   XT_TRY(head_map(&tq, q, ld_qkv, B, S, H, BT));
@@ -1088,6 +1105,8 @@ int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   p.causal = causal;
   p.sc = float(1.0 / std::sqrt(double(hd)) * 1.4426950408889634);
   p.lse = lse;
+  p.o32 = o32;
+  p.ld32 = ld_o32;
   p.flag = errflag();
   static bool smem_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_fwd_kernel), FwdSmem::BYTES, smem_set, "xt_attention_fwd"));
@@ -1103,8 +1122,9 @@ int xt_attention_bwd_workspace_size(int B, int S, int H, size_t* bytes) {
 }
 
 int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o, const void* d_o,
-                     int64_t ld_o, const float* lse, void* dq, void* dk, void* dv, int64_t ld_dqkv, void* ws,
-                     size_t ws_bytes, int B, int S, int H, int hd, int causal, int dt, void* stream) {
+                     int64_t ld_o, const float* lse, const float* o32, int64_t ld_o32, void* dq, void* dk, void* dv,
+                     int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S, int H, int hd, int causal, int dt,
+                     void* stream) {
   XT_TRY(check_common("xt_attention_bwd", B, S, H, hd, causal, dt, ld_qkv, ld_o,
                       {q, k, v, o, d_o, lse, dq, dk, dv, ws}));
   XT_REQUIRE(ld_dqkv >= int64_t(H) * hd, "xt_attention_bwd: ld_dqkv smaller than H·hd");
@@ -1120,8 +1140,14 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
     int64_t blocks = ceil_div(threads, 256);
     const int64_t cap = int64_t(num_sms()) * 8;
     if (blocks > cap) blocks = cap;
-    attn_delta_kernel<<<int(blocks), 256, 0, s>>>(static_cast<const bf16*>(o), static_cast<const bf16*>(d_o), ld_o,
-                                                   B, S, H, D);
+    if (o32) {
+      XT_REQUIRE(ld_o32 >= int64_t(H) * hd, "xt_attention_bwd: ld_o32 smaller than H·hd");
+      if (!aligned16(o32) || ld_o32 % 4) return fail(XT_ERR_ALIGNMENT, "xt_attention_bwd: o32 must be 16-byte aligned rows");
+      attn_delta_kernel<float><<<int(blocks), 256, 0, s>>>(o32, ld_o32, static_cast<const bf16*>(d_o), ld_o, B, S, H, D);
+    } else {
+      attn_delta_kernel<bf16><<<int(blocks), 256, 0, s>>>(static_cast<const bf16*>(o), ld_o,
+                                                          static_cast<const bf16*>(d_o), ld_o, B, S, H, D);
+    }
     XT_TRY(check_launch("xt_attention_bwd (delta)"));
   }
   CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;

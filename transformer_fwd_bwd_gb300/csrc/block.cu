@@ -5,13 +5,15 @@
 // logits = norm(h) @ embedᵀ; loss = cross_entropy(logits, targets).
 // [DO] § dropout 接在哪（wiring）: residual dropout at the attention and FFN outputs with the
 // per-site seeds base ⊕ layer ⊕ {0xA77, 0xF70}.
-// [AE] § Attention 用组合: attention = matmul(softmax(scale(matmul(Q, Kᵀ))), V), here as
-// causal-tile GEMMs around an in-place softmax; its backward follows the same composition.
+// [AE] § Attention 用组合: attention = matmul(softmax(scale(matmul(Q, Kᵀ))), V), either as the
+// fused tile-by-tile kernels (bf16, head_dim 64) or as causal-tile GEMMs around an in-place
+// softmax; the backward follows the same composition.
 // [BP] § Ackumulation över mikrobatcher: the backward adds into every gradient buffer.
 //
 // The residual-stream gradient is kept in float32 whatever the activation dtype (it sums the
 // fan-out of every residual add and norm); everything else is stored in the activation dtype
 // with float32 statistics.
+#include <algorithm>
 #include <vector>
 
 #include "internal.cuh"
@@ -37,7 +39,10 @@ struct Dims {
   int64_t B, S, d, H, hd, F, V, L, T, UP, e;
   int dt, gdt;
   bool rms, swiglu;
+  bool fused;  // attention through xt_attention_fwd / xt_attention_bwd
 };
+
+bool fused_supported(const xt_block_config& c) { return c.dtype == XT_BF16 && c.hd == 64 && c.d % 8 == 0; }
 
 Dims dims_of(const xt_block_config& c) {
   Dims m{};
@@ -49,6 +54,7 @@ Dims dims_of(const xt_block_config& c) {
   m.dt = c.dtype;
   m.gdt = c.grad_dtype;
   m.e = int64_t(dtype_size(c.dtype));
+  m.fused = c.attention == XT_ATTN_FUSED || (c.attention == XT_ATTN_AUTO && fused_supported(c));
   return m;
 }
 
@@ -160,26 +166,28 @@ size_t max_matmul_ws(const Dims& m) {
       lin_fwd(m, m.d, 3 * m.d), lin_fwd(m, m.d, m.d), lin_fwd(m, m.d, m.UP), lin_fwd(m, m.F, m.d),
       lin_dw(m, m.d, 3 * m.d), lin_dw(m, m.d, m.d), lin_dw(m, m.d, m.UP), lin_dw(m, m.F, m.d),
       lin_dx(m, m.d, 3 * m.d), lin_dx(m, m.d, m.d), lin_dx(m, m.d, m.UP), lin_dx(m, m.F, m.d),
-      att_scores(m), att_pv(m), att_dp(m), att_dv(m), att_dq(m), att_dk(m),
       logits_fwd(m), logits_de(m), logits_dhf(m)};
+  const xt_matmul_desc composed[] = {att_scores(m), att_pv(m), att_dp(m), att_dv(m), att_dq(m), att_dk(m)};
   size_t mx = 0;
-  for (const auto& g : all) {
-    const size_t b = matmul_workspace(g);
-    if (b > mx) mx = b;
-  }
+  for (const auto& g : all) mx = std::max(mx, matmul_workspace(g));
+  if (!m.fused)
+    for (const auto& g : composed) mx = std::max(mx, matmul_workspace(g));
   return mx;
 }
 
 // ------------------------------------------------------------------------------ buffers
 
 struct Bufs {
+  // P[l]: the layer's probabilities [B, H, S, S] (composed attention) or its softmax
+  // normaliser lse, float32 [B, H, S] (fused attention)
   std::vector<void*> h_in, x1, qkv, P, o, h_mid, x2, up, mact;
+  std::vector<float*> o32;  // fused attention: float32 copy of o (the backward's D is formed from it)
   std::vector<float*> st1, st2;
   void *h_final, *hf, *logits, *tmp;
   float *stf, *lse, *rope, *dh, *one;
   void *gA, *gB, *dm, *dgu, *dP, *dqkv;
   void *ws_norm, *ws_ce, *ws_emb, *ws_mm;
-  size_t ws_mm_bytes;
+  size_t ws_mm_bytes, dP_bytes = 0;
   size_t total;
 };
 
@@ -189,14 +197,15 @@ int carve(const Dims& m, void* base, Bufs& b) {
   const size_t act = size_t(T * d * e);
   b.h_in.resize(m.L); b.x1.resize(m.L); b.qkv.resize(m.L); b.P.resize(m.L); b.o.resize(m.L);
   b.h_mid.resize(m.L); b.x2.resize(m.L); b.up.resize(m.L); b.mact.resize(m.L);
-  b.st1.resize(m.L); b.st2.resize(m.L);
+  b.st1.resize(m.L); b.st2.resize(m.L); b.o32.assign(m.L, nullptr);
   for (int64_t l = 0; l < m.L; ++l) {
     b.h_in[l] = a.take(act);
     b.x1[l] = a.take(act);
     b.st1[l] = static_cast<float*>(a.take(size_t(2 * T) * 4));
     b.qkv[l] = a.take(size_t(T * 3 * d * e));
-    b.P[l] = a.take(size_t(m.B * m.H * m.S * m.S * e));
+    b.P[l] = a.take(m.fused ? size_t(m.B * m.H * m.S) * 4 : size_t(m.B * m.H * m.S * m.S * e));
     b.o[l] = a.take(act);
+    if (m.fused) b.o32[l] = static_cast<float*>(a.take(size_t(T * d) * 4));
     b.h_mid[l] = a.take(act);
     b.x2[l] = a.take(act);
     b.st2[l] = static_cast<float*>(a.take(size_t(2 * T) * 4));
@@ -216,7 +225,14 @@ int carve(const Dims& m, void* base, Bufs& b) {
   b.gB = a.take(act);
   b.dm = a.take(size_t(T * m.F * e));
   b.dgu = a.take(size_t(T * m.UP * e));
-  b.dP = a.take(size_t(m.B * m.H * m.S * m.S * e));
+  if (m.fused) {  // the attention backward's D = Σ dO∘O per row
+    size_t ab = 0;
+    XT_TRY(xt_attention_bwd_workspace_size(int(m.B), int(m.S), int(m.H), &ab));
+    b.dP = a.take(ab);
+    b.dP_bytes = ab;
+  } else {
+    b.dP = a.take(size_t(m.B * m.H * m.S * m.S * e));
+  }
   b.dqkv = a.take(size_t(T * 3 * d * e));
   size_t nb = 0, cb = 0, eb = 0;
   XT_TRY(xt_norm_bwd_workspace_size(T, d, &nb));
@@ -243,6 +259,9 @@ int validate(const xt_block_config* c) {
   XT_REQUIRE(valid_dtype(c->dtype) && valid_dtype(c->grad_dtype), "block: bad dtype");
   XT_REQUIRE(c->p >= 0.f && c->p < 1.f, "block: dropout p must be in [0, 1)");
   XT_REQUIRE(int64_t(c->B) * c->S <= 16384, "block: B·S above 16384 tokens is not supported");
+  XT_REQUIRE(c->attention >= XT_ATTN_AUTO && c->attention <= XT_ATTN_FUSED, "block: bad attention mode");
+  if (c->attention == XT_ATTN_FUSED && !fused_supported(*c))
+    return fail(XT_ERR_UNSUPPORTED, "block: fused attention needs bf16, head_dim 64 and d a multiple of 8");
   return XT_OK;
 }
 
@@ -318,9 +337,15 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
     XT_TRY(matmul(lin_fwd(m, d, 3 * d), b.x1[l], prm->Wqkv[l], b.qkv[l], b.ws_mm, b.ws_mm_bytes, s));
     if (c.rope)  // q and k blocks are 2H consecutive heads of each qkv row
       XT_TRY(xt_rope_fwd(b.qkv[l], b.qkv[l], b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, stream));
-    XT_TRY(matmul(att_scores(m), b.qkv[l], off(b.qkv[l], d, e), b.P[l], b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(xt_softmax_fwd(b.P[l], b.P[l], m.B * m.H * m.S, m.S, 2, m.S, m.dt, stream));
-    XT_TRY(matmul(att_pv(m), b.P[l], off(b.qkv[l], 2 * d, e), b.o[l], b.ws_mm, b.ws_mm_bytes, s));
+    if (m.fused) {
+      XT_TRY(xt_attention_fwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], d,
+                              static_cast<float*>(b.P[l]), b.o32[l], d, int(m.B), int(m.S), int(m.H), int(m.hd), 1,
+                              m.dt, stream));
+    } else {
+      XT_TRY(matmul(att_scores(m), b.qkv[l], off(b.qkv[l], d, e), b.P[l], b.ws_mm, b.ws_mm_bytes, s));
+      XT_TRY(xt_softmax_fwd(b.P[l], b.P[l], m.B * m.H * m.S, m.S, 2, m.S, m.dt, stream));
+      XT_TRY(matmul(att_pv(m), b.P[l], off(b.qkv[l], 2 * d, e), b.o[l], b.ws_mm, b.ws_mm_bytes, s));
+    }
     XT_TRY(matmul(lin_fwd(m, d, d), b.o[l], prm->Wo[l], b.tmp, b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(xt_dropout_add_fwd(b.h_in[l], b.tmp, b.h_mid[l], T * d, c.p, site_seed(c, l, kSiteAttn), drop, m.dt, stream));
     // MLP sub-block
@@ -376,11 +401,18 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
     XT_TRY(xt_dropout_bwd_ex(b.dh, XT_F32, b.gA, m.dt, T * d, c.p, site_seed(c, l, kSiteAttn), drop, 0, stream));
     XT_TRY(matmul(lin_dw(m, d, d), b.o[l], b.gA, prm->dWo[l], b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(matmul(lin_dx(m, d, d), b.gA, prm->Wo[l], b.gB, b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(matmul(att_dp(m), b.gB, off(b.qkv[l], 2 * d, e), b.dP, b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(xt_softmax_bwd(b.dP, b.P[l], b.dP, m.B * m.H * m.S, m.S, 2, m.S, m.dt, 0, stream));
-    XT_TRY(matmul(att_dv(m), b.P[l], b.gB, off(b.dqkv, 2 * d, e), b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(matmul(att_dq(m), b.dP, off(b.qkv[l], d, e), b.dqkv, b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(matmul(att_dk(m), b.dP, b.qkv[l], off(b.dqkv, d, e), b.ws_mm, b.ws_mm_bytes, s));
+    if (m.fused) {
+      XT_TRY(xt_attention_bwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.gB, d,
+                              static_cast<const float*>(b.P[l]), b.o32[l], d, b.dqkv, off(b.dqkv, d, e),
+                              off(b.dqkv, 2 * d, e),
+                              3 * d, b.dP, b.dP_bytes, int(m.B), int(m.S), int(m.H), int(m.hd), 1, m.dt, stream));
+    } else {
+      XT_TRY(matmul(att_dp(m), b.gB, off(b.qkv[l], 2 * d, e), b.dP, b.ws_mm, b.ws_mm_bytes, s));
+      XT_TRY(xt_softmax_bwd(b.dP, b.P[l], b.dP, m.B * m.H * m.S, m.S, 2, m.S, m.dt, 0, stream));
+      XT_TRY(matmul(att_dv(m), b.P[l], b.gB, off(b.dqkv, 2 * d, e), b.ws_mm, b.ws_mm_bytes, s));
+      XT_TRY(matmul(att_dq(m), b.dP, off(b.qkv[l], d, e), b.dqkv, b.ws_mm, b.ws_mm_bytes, s));
+      XT_TRY(matmul(att_dk(m), b.dP, b.qkv[l], off(b.dqkv, d, e), b.ws_mm, b.ws_mm_bytes, s));
+    }
     if (c.rope)
       XT_TRY(xt_rope_bwd(b.dqkv, b.dqkv, b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, 0, stream));
     XT_TRY(matmul(lin_dw(m, d, 3 * d), b.x1[l], b.dqkv, prm->dWqkv[l], b.ws_mm, b.ws_mm_bytes, s));

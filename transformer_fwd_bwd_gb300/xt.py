@@ -20,6 +20,7 @@ XT_F32, XT_BF16 = 0, 1
 XT_DEVERR_INDEX, XT_DEVERR_TIMEOUT = 1, 2
 XT_NORM_RMS, XT_NORM_LN = 0, 1
 XT_MLP_SWIGLU, XT_MLP_GELU = 0, 1
+XT_ATTN_AUTO, XT_ATTN_COMPOSED, XT_ATTN_FUSED = 0, 1, 2
 
 
 class XtError(RuntimeError):
@@ -46,7 +47,8 @@ class BlockConfig(C.Structure):
                 ("norm", C.c_int32), ("mlp", C.c_int32), ("rope", C.c_int32),
                 ("learned_pos", C.c_int32), ("causal", C.c_int32), ("training", C.c_int32),
                 ("dtype", C.c_int32), ("grad_dtype", C.c_int32), ("eps", C.c_float),
-                ("p", C.c_float), ("rope_base", C.c_double), ("base_seed", C.c_uint64)]
+                ("p", C.c_float), ("rope_base", C.c_double), ("base_seed", C.c_uint64),
+                ("attention", C.c_int32)]
 
 
 _VP = C.c_void_p
@@ -100,10 +102,10 @@ _SIGS = {
     "xt_rope_bwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _I, _VP],
     "xt_softmax_fwd": [_VP, _VP, _I64, _I64, _I, _I64, _I, _VP],
     "xt_softmax_bwd": [_VP, _VP, _VP, _I64, _I64, _I, _I64, _I, _I, _VP],
-    "xt_attention_fwd": [_VP, _VP, _VP, _I64, _VP, _I64, _VP, _I, _I, _I, _I, _I, _I, _VP],
+    "xt_attention_fwd": [_VP, _VP, _VP, _I64, _VP, _I64, _VP, _VP, _I64, _I, _I, _I, _I, _I, _I, _VP],
     "xt_attention_bwd_workspace_size": [_I, _I, _I, _SZP],
-    "xt_attention_bwd": [_VP, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _VP, _VP, _VP, _I64, _VP, C.c_size_t,
-                         _I, _I, _I, _I, _I, _I, _VP],
+    "xt_attention_bwd": [_VP, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _VP,
+                         C.c_size_t, _I, _I, _I, _I, _I, _I, _VP],
     "xt_cross_entropy_workspace_size": [_I64, _SZP],
     "xt_cross_entropy_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _I, _VP, _VP],
     "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
@@ -390,20 +392,22 @@ def xt_softmax_fwd(x, y, causal=0, q_len=0, s=None):
     call("xt_softmax_fwd", ptr(x), ptr(y), rows, cols, causal, q_len, dt(x), stream(s))
 
 
-def xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, causal=1, s=None):
-    """q, k, v: [B·S, ld] views (head h at columns h·hd); o: [B·S, ld_o]; lse: float32 [B, H, S]."""
+def xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, causal=1, o32=None, s=None):
+    """q, k, v: [B·S, ld] views (head h at columns h·hd); o: [B·S, ld_o]; lse: float32 [B, H, S];
+    o32: optional float32 [B·S, ld] copy of O before rounding."""
     call("xt_attention_fwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False), o.stride(0),
-         ptr(lse), B, S, H, hd, causal, dt(q), stream(s))
+         ptr(lse), ptr(o32, False), o32.stride(0) if o32 is not None else 0, B, S, H, hd, causal, dt(q), stream(s))
 
 
-def xt_attention_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, S, H, hd, causal=1, ws=None, s=None):
+def xt_attention_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, S, H, hd, causal=1, o32=None, ws=None, s=None):
     n = C.c_size_t(0)
     call("xt_attention_bwd_workspace_size", B, S, H, C.byref(n))
     if ws is None:
         ws = torch.empty(max(1, n.value), dtype=torch.uint8, device=q.device)
     call("xt_attention_bwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False),
-         ptr(d_o, False), o.stride(0), ptr(lse), ptr(dq, False), ptr(dk, False), ptr(dv, False), dq.stride(0),
-         ptr(ws), ws.numel(), B, S, H, hd, causal, dt(q), stream(s))
+         ptr(d_o, False), o.stride(0), ptr(lse), ptr(o32, False), o32.stride(0) if o32 is not None else 0,
+         ptr(dq, False), ptr(dk, False), ptr(dv, False), dq.stride(0), ptr(ws), ws.numel(), B, S, H, hd, causal,
+         dt(q), stream(s))
 
 
 def xt_softmax_bwd(d, y, dx, causal=0, q_len=0, acc=0, s=None):
