@@ -45,6 +45,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
+    ap.add_argument("--kernel", choices=["attention", "gemm"], default=None,
+                    help="time one kernel family at the workload's sizes instead of the step (for profiling)")
+    ap.add_argument("--shape", default="8192,3072,768,0,1",
+                    help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-seqs", type=int, default=1, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -353,8 +357,71 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel(args):
+    """One kernel family alone on seeded N(0, 1) inputs: 3 untimed launches, then 20 timed with
+    CUDA events; prints one JSON line (µs per launch and algorithmic TFLOP/s)."""
+    import torch
+
+    import __graft_entry__
+    import synth
+    from transformer_fwd_bwd_gb300 import xt
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(synth.SEED_SWEEP)
+
+    clocks = []
+
+    def timed(fn, n=200):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as cs:
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+        clocks.append(cs.summary())
+        assert xt.device_errors() == 0, "device error flag set"
+        return e0.elapsed_time(e1) / n * 1e3
+
+    if args.kernel == "attention":
+        cfg = synth.BLOCK_CONFIGS[args.workload]
+        B, S, H, hd = cfg["B"], cfg["S"], cfg["H"], cfg["hd"]
+        d = H * hd
+        qkv = torch.randn(B * S, 3 * d, generator=g).to(torch.bfloat16).to(dev)
+        dO = torch.randn(B * S, d, generator=g).to(torch.bfloat16).to(dev)
+        o = torch.empty(B * S, d, dtype=torch.bfloat16, device=dev)
+        o_lo = torch.empty(B * S, d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+        dqkv = torch.empty_like(qkv)
+        ws = torch.empty(B * H * S * 4 + 256, dtype=torch.uint8, device=dev)
+        q, k, v = qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:]
+        fwd_us = timed(lambda: xt.xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, 1, o_lo=o_lo))
+        bwd_us = timed(lambda: xt.xt_attention_bwd(q, k, v, o, dO, lse, dqkv[:, :d], dqkv[:, d:2 * d],
+                                                   dqkv[:, 2 * d:], B, S, H, hd, 1, o_lo=o_lo, ws=ws))
+        fl = 2 * 2 * S * S * hd / 2 * B * H   # QKᵀ and PV over the causal half
+        print(json.dumps({"kernel": "attention", "workload": f"B{B} S{S} H{H}x{hd} causal bf16",
+                          "fwd_us": fwd_us, "bwd_us": bwd_us, "fwd_tflops": fl / fwd_us / 1e6,
+                          "bwd_tflops": 2 * fl / bwd_us / 1e6, "clocks": clocks}))
+    else:
+        M, N, K, ta, tb = (int(x) for x in args.shape.split(","))
+        A = (torch.randn(K, M, generator=g) if ta else torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)
+        Bm = (torch.randn(N, K, generator=g) if tb else torch.randn(K, N, generator=g)).to(torch.bfloat16).to(dev)
+        C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        desc = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16)
+        us = timed(lambda: xt.xt_matmul_fwd(desc, A, Bm, C))
+        print(json.dumps({"kernel": "gemm", "shape": [M, N, K, ta, tb], "us": us, "tflops": 2 * M * N * K / us / 1e6,
+                          "clocks": clocks}))
+
+
 def main():
     args = parse_args()
+    if args.kernel:
+        run_kernel(args)
+        return
     if args.oracle_sample:
         r, t, n = oracle_sample(args.workload, args.sample_seqs)
         print(json.dumps({"value": r, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",

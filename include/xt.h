@@ -234,22 +234,21 @@ int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t
  * lse (float32 [B][H][S], written by the forward, read by the backward) is the natural-log
  * normaliser log Σ_c exp(scores[s, c]) over the visible keys.
  * dq, dk, dv are overwritten.  The backward's workspace (xt_attention_bwd_workspace_size)
- * holds D = Σ_c dO∘O per (b, h, s).  o32 (optional, may be NULL; float32, head h at columns
- * h·hd of rows ld_o32 apart, 16-byte aligned rows) receives O before its bf16 rounding; passed
- * to the backward it is the O that D is formed from, which keeps the rows of dS summing to ~0
- * (with the bf16 O they carry its 2⁻⁹ rounding as a bias).
+ * holds D = Σ_c dO∘O per (b, h, s).  o_lo (optional, may be NULL; bf16, the layout and row
+ * stride of o) receives O − bf16(O) rounded to bf16, so o + o_lo holds O to ~2⁻¹⁶ relative;
+ * passed to the backward it is part of the O that D is formed from, which keeps the rows of
+ * dS summing to ~0 (with the bf16 O alone they carry its 2⁻⁹ rounding as a bias).
  * Supported: dt = XT_BF16, hd = 64, row strides multiples of 8 elements, all pointers
  * 16-byte aligned (else XT_ERR_UNSUPPORTED / XT_ERR_ALIGNMENT).  Device-side waits are
  * bounded; on expiry XT_DEVERR_TIMEOUT is set in the device error flag.
  * ------------------------------------------------------------------------------- */
-int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, int64_t ld_o,
-                     float* lse, float* o32, int64_t ld_o32, int B, int S, int H, int hd, int causal, int dt,
-                     void* stream);
+int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, void* o_lo,
+                     int64_t ld_o, float* lse, int B, int S, int H, int hd, int causal, int dt, void* stream);
 int xt_attention_bwd_workspace_size(int B, int S, int H, size_t* bytes);
 int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o,
-                     const void* d_o, int64_t ld_o, const float* lse, const float* o32, int64_t ld_o32,
-                     void* dq, void* dk, void* dv, int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S,
-                     int H, int hd, int causal, int dt, void* stream);
+                     const void* o_lo, const void* d_o, int64_t ld_o, const float* lse, void* dq, void* dk,
+                     void* dv, int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S, int H, int hd,
+                     int causal, int dt, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Cross-entropy, mean over rows ([AE] op table row cross_entropy, § Cross-entropy 反向推导):

@@ -46,8 +46,7 @@ struct FwdParams {
   int B, H, S, nq, items, causal;
   float sc;     // α·log2 e
   float* lse;   // [B, H, S], natural log
-  float* o32;   // optional float32 copy of O (row t, head h at column h·hd), row stride ld32
-  int64_t ld32;
+  int o_lo;     // 1: also store O − bf16(O) rounded to bf16 (through tmOlo)
   uint32_t* flag;
 };
 
@@ -66,6 +65,14 @@ __device__ __forceinline__ Item decode(int i, int B, int H, int nq, int causal) 
   return it;
 }
 
+// Work item of round r for this CTA: rounds alternate direction over the CTAs (a boustrophedon),
+// so with items ordered longest first the CTAs' totals even out (95 % balance for the causal
+// 1024-token case against 84 % for plain round-robin).
+__device__ __forceinline__ int snake_item(int r) {
+  const int G = int(gridDim.x), c = int(blockIdx.x);
+  return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
 // Row r (0..127) of a 128-row operand in the 128-byte-swizzled K-major layout: 16-byte unit u of
 // the 64-element chunk c sits at chunk base + r·128 + ((u ^ (r & 7)) << 4).
 __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c, int u) {
@@ -74,6 +81,15 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c, int u) {
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Pins the computation of r[] before the next volatile asm (an mbarrier wait): the compiler may
+// otherwise sink pure register arithmetic past the wait, serialising it behind the tensor core
+// instead of overlapping the two.  Emits no instruction.
+template <int N>
+__device__ __forceinline__ void keep_before(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 // Bounded wait taken by a whole warp (the decision is warp-uniform).
@@ -88,15 +104,15 @@ struct FwdSmem {
   static constexpr int K = Q + TILE;
   static constexpr int V = K + RING * TILE;
   static constexpr int P = V + RING * TILE;
-  static constexpr int STAGE = P + 2 * PT;           // O staging: 4 warps × 32 rows × 128 B
-  static constexpr int BARS = STAGE + 4 * 4096;
+  static constexpr int STAGE = P + 2 * PT;           // O and O_lo staging: 4 warps × 2 × 32 rows × 128 B
+  static constexpr int BARS = STAGE + 8 * 4096;
   static constexpr int BYTES = 1024 + BARS + 256;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tmOlo, const FwdParams p) {
   constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_PV = instr_desc_bf16(128, HD, false, true);
   constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), O [256,320)
@@ -163,12 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ks = 0, vs = 0, nk = 0, nv = 0, nqi = 0;
       uint32_t kph = 0, vph = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+      #pragma unroll 1
+      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
+        const int i = snake_item(r);
+        if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full), TILE);
         tma_load_4d(sb + FwdSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         ++nqi;
+        #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           if (*abort_flag) { ok = false; break; }
           if (!mbar_wait(smem_u32(&k_empty[ks]), kph ^ 1)) { ok = false; break; }
@@ -223,11 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++vs == RING) { vs = 0; vph ^= 1; }
         return true;
       };
-      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+      #pragma unroll 1
+      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
+        const int i = snake_item(r);
+        if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_full), nqi & 1)) { ok = false; break; }
         ++nqi;
         tc_fence_after();
+        #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j, ++g) {
           const int b = int(g & 1);
           const uint32_t u = g >> 1;
@@ -255,15 +279,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qw = warp & 3;            // TMEM lanes [32 qw, 32 qw + 32)
     const int rr = qw * 32 + lane;      // row within the query tile
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
-    const uint32_t stage = sb + FwdSmem::STAGE + uint32_t(qw) * 4096;
+    const uint32_t stage = sb + FwdSmem::STAGE + uint32_t(qw) * 8192;
     uint32_t g = 0;
-    for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+    #pragma unroll 1
+    for (int r = 0; r * int(gridDim.x) < p.items; ++r) {
+      const int i = snake_item(r);
+      if (i >= p.items) continue;
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Item it = decode(i, p.B, p.H, p.nq, p.causal);
       const int row = it.qt * BT + rr;
       float m = -INFINITY;  // running max of the raw scores (Q·K, before α)
       float l = 0.f;        // running Σ 2^((s − m)·sc)
       bool ok = true;
+      #pragma unroll 1
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int b = int(g & 1);
         const uint32_t u = g >> 1;
@@ -284,9 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= lim) r[c] = __float_as_uint(-INFINITY);
         }
-        float mt = __uint_as_float(r[0]);
+        float mx[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mt = fmaxf(mt, __uint_as_float(r[c]));
+        for (int t = 0; t < 8; ++t) mx[t] = __uint_as_float(r[t]);
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(r[c]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m && (m == -INFINITY || (m_new - m) * p.sc > kRescale);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -313,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ms = (m == -INFINITY) ? 0.f : m * p.sc;
         if (!warp_wait(smem_u32(&p_free[b]), (u & 1) ^ 1)) { ok = false; break; }
         const uint32_t ps = sb + FwdSmem::P + b * PT;
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -321,11 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               e[t] = exp2f(fmaf(__uint_as_float(r[c * 64 + un * 8 + t]), p.sc, -ms));
-              l += e[t];
+              ls[t] += e[t];
             }
             st_shared_v4(swz(ps, rr, c, un), pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
                          pack_bf16(e[6], e[7]));
           }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -348,31 +382,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       const float inv = 1.f / l;
-      if (lane == 0) bulk_wait_read_0();  // the previous item's store has read the staging tile
+      if (lane == 0) bulk_wait_read_0();  // the previous item's stores have read the staging tiles
       __syncwarp();
+      // O rounded to bf16, and (optionally) the rounding residual O − bf16(O) rounded to bf16:
+      // the pair holds O to ~2⁻¹⁶ relative for the backward's D = Σ dO∘O
 #pragma unroll
-      for (int un = 0; un < 8; ++un)
-        st_shared_v4(stage + uint32_t(lane) * 128 + (uint32_t(un ^ (lane & 7)) << 4),
-                     pack_bf16(__uint_as_float(o[8 * un]) * inv, __uint_as_float(o[8 * un + 1]) * inv),
-                     pack_bf16(__uint_as_float(o[8 * un + 2]) * inv, __uint_as_float(o[8 * un + 3]) * inv),
-                     pack_bf16(__uint_as_float(o[8 * un + 4]) * inv, __uint_as_float(o[8 * un + 5]) * inv),
-                     pack_bf16(__uint_as_float(o[8 * un + 6]) * inv, __uint_as_float(o[8 * un + 7]) * inv));
+      for (int un = 0; un < 8; ++un) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = __uint_as_float(o[8 * un + 2 * e]) * inv, b = __uint_as_float(o[8 * un + 2 * e + 1]) * inv;
+          hi[e] = pack_bf16(a, b);
+          const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&hi[e]);
+          lo[e] = pack_bf16(a - __low2float(h), b - __high2float(h));
+        }
+        const uint32_t off = uint32_t(lane) * 128 + (uint32_t(un ^ (lane & 7)) << 4);
+        st_shared_v4(stage + off, hi[0], hi[1], hi[2], hi[3]);
+        if (p.o_lo) st_shared_v4(stage + 4096 + off, lo[0], lo[1], lo[2], lo[3]);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         tma_store_4d(&tmO, stage, 0, it.h, it.qt * BT + qw * 32, it.b);
+        if (p.o_lo) tma_store_4d(&tmOlo, stage + 4096, 0, it.h, it.qt * BT + qw * 32, it.b);
         bulk_commit();
       }
-      if (row < p.S) {
-        p.lse[(int64_t(it.b) * p.H + it.h) * p.S + row] = (m * p.sc + log2f(l)) * kLn2;
-        if (p.o32) {
-          float4* dst = reinterpret_cast<float4*>(p.o32 + (int64_t(it.b) * p.S + row) * p.ld32 + int64_t(it.h) * HD);
-#pragma unroll
-          for (int j = 0; j < HD / 4; ++j)
-            dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                 __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
-        }
-      }
+      if (row < p.S) p.lse[(int64_t(it.b) * p.H + it.h) * p.S + row] = (m * p.sc + log2f(l)) * kLn2;
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -396,13 +431,13 @@ struct BwdParams {
 };
 
 // D[b, h, s] = Σ_c dO[t, h·hd + c]·O[t, h·hd + c], t = b·S + s: 8 threads per (t, h), four
-// (t, h) rows per warp; the loop runs warp-uniformly so the shuffles see every lane.  O is the
-// forward's float32 copy when there is one: D then agrees with Σ_c P·dP of the recomputed P and
-// dP to float32 rounding, so the rows of dS = P∘(dP − D) sum to ~0 as they must; the bf16 O
-// would leave a bias of its rounding (2⁻⁹ relative) in every row of dS.
-template <typename TO>
-__global__ void attn_delta_kernel(const TO* __restrict__ o, int64_t ld_oo, const bf16* __restrict__ dO, int64_t ld_o,
-                                  int B, int S, int H, float* __restrict__ D) {
+// (t, h) rows per warp; the loop runs warp-uniformly so the shuffles see every lane.  With the
+// forward's residual O_lo, O = O_hi + O_lo to ~2⁻¹⁶ and D agrees with Σ_c P·dP of the recomputed
+// P and dP, so the rows of dS = P∘(dP − D) sum to ~0 as they must; the bf16 O alone would leave
+// a bias of its rounding (2⁻⁹ relative) in every row of dS.
+__global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ o_lo,
+                                  const bf16* __restrict__ dO, int64_t ld_o, int B, int S, int H,
+                                  float* __restrict__ D) {
   const int64_t n = int64_t(B) * S * H;
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -416,9 +451,16 @@ __global__ void attn_delta_kernel(const TO* __restrict__ o, int64_t ld_oo, const
     if (act) {
       t = r / H;
       h = int(r - t * H);
+      const int64_t off = t * ld_o + int64_t(h) * HD + sub * 8;
       float a[8], b[8];
-      Acc<TO, 8>::load(o + t * ld_oo + int64_t(h) * HD + sub * 8, a);
-      Vec<bf16>::load(dO + t * ld_o + int64_t(h) * HD + sub * 8, b);
+      Vec<bf16>::load(o + off, a);
+      Vec<bf16>::load(dO + off, b);
+      if (o_lo) {
+        float c[8];
+        Vec<bf16>::load(o_lo + off, c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] += c[e];
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc = fmaf(a[e], b[e], acc);
     }
@@ -558,7 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot = 0, nkv = 0, nqd = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+      #pragma unroll 1
+      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
+        const int i = snake_item(r);
+        if (i >= p.items) continue;
         const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(kv_empty), (nkv & 1) ^ 1)) { ok = false; break; }
         mbar_expect_tx(smem_u32(kv_full), 2 * TILE);
@@ -566,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sb + KvSmem::V, &tmV, smem_u32(kv_full), 0, it.h, it.qt * BT, it.b);
         ++nkv;
         const int q_first = p.causal ? it.qt : 0;
+        #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           if (*abort_flag || !mbar_wait(smem_u32(&qd_empty[slot]), ph ^ 1)) { ok = false; break; }
           const uint32_t fb = smem_u32(&qd_full[slot]);
@@ -633,13 +679,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(smem_u32(&qd_empty[gg & 1]));
         return true;
       };
-      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+      #pragma unroll 1
+      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
+        const int i = snake_item(r);
+        if (i >= p.items) continue;
         const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(kv_full), nkv & 1)) { ok = false; break; }
         ++nkv;
         tc_fence_after();
         const uint32_t g0 = g;
         if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
+        #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           const uint32_t gg = g0 + uint32_t(j);
           if (*abort_flag) { ok = false; break; }
@@ -660,12 +710,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
     const uint32_t stage = sb + KvSmem::STAGE + uint32_t(qw) * 8192;
     uint32_t g = 0;
-    for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+    #pragma unroll 1
+    for (int r = 0; r * int(gridDim.x) < p.items; ++r) {
+      const int i = snake_item(r);
+      if (i >= p.items) continue;
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
       const int q_first = p.causal ? it.qt : 0;
       const int64_t bh = int64_t(it.b) * p.H + it.h;
       bool ok = true;
+      #pragma unroll 1
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int b = int(g & 1);
         const uint32_t u = g >> 1;
@@ -698,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float e = exp2f(fmaf(__uint_as_float(r[c]), p.sc, -lv[c]));
           r[c] = __float_as_uint(c < first ? 0.f : e);
         }
+        keep_before(r);
         if (!warp_wait(smem_u32(p_free), (g & 1) ^ 1)) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -852,13 +907,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ks = 0, nk = 0, nqi = 0;
       uint32_t kph = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+      #pragma unroll 1
+      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
+        const int i = snake_item(r);
+        if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full), 2 * TILE);
         tma_load_4d(sb + QSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         tma_load_4d(sb + QSmem::DO, &tmDO, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         ++nqi;
+        #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           if (*abort_flag || !mbar_wait(smem_u32(&kv_empty[ks]), kph ^ 1)) { ok = false; break; }
           const uint32_t fb = smem_u32(&kv_full[ks]);
@@ -921,13 +980,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(smem_u32(&kv_empty[gg % RING]));
         return true;
       };
-      for (int i = blockIdx.x; i < p.items && ok && !*abort_flag; i += gridDim.x) {
+      #pragma unroll 1
+      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
+        const int i = snake_item(r);
+        if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_full), nqi & 1)) { ok = false; break; }
         ++nqi;
         tc_fence_after();
         const uint32_t g0 = g;
         if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
+        #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           const uint32_t gg = g0 + uint32_t(j);
           if (*abort_flag) { ok = false; break; }
@@ -948,7 +1011,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
     const uint32_t stage = sb + QSmem::STAGE + uint32_t(qw) * 4096;
     uint32_t g = 0;
-    for (int i = blockIdx.x; i < p.items; i += gridDim.x) {
+    #pragma unroll 1
+    for (int r = 0; r * int(gridDim.x) < p.items; ++r) {
+      const int i = snake_item(r);
+      if (i >= p.items) continue;
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Item it = decode(i, p.B, p.H, p.nq, p.causal);
       const int row = it.qt * BT + rr;
@@ -956,6 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse2 = row < p.S ? p.lse[bh * p.S + row] * kLog2e : INFINITY;
       const float Dr = row < p.S ? p.D[bh * p.S + row] : 0.f;
       bool ok = true;
+      #pragma unroll 1
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int b = int(g & 1);
         const uint32_t u = g >> 1;
@@ -975,6 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float e = exp2f(fmaf(__uint_as_float(r[c]), p.sc, -lse2));
           r[c] = __float_as_uint(c < lim ? e : 0.f);
         }
+        keep_before(r);
         if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(&ds_free[b]), (u & 1) ^ 1)) {
           ok = false;
           break;
@@ -1083,19 +1151,17 @@ using namespace xt::attn;
 
 extern "C" {
 
-int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, int64_t ld_o, float* lse,
-                     float* o32, int64_t ld_o32, int B, int S, int H, int hd, int causal, int dt, void* stream) {
+int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv, void* o, void* o_lo, int64_t ld_o,
+                     float* lse, int B, int S, int H, int hd, int causal, int dt, void* stream) {
   XT_TRY(check_common("xt_attention_fwd", B, S, H, hd, causal, dt, ld_qkv, ld_o, {q, k, v, o, lse}));
-  if (o32) {
-    XT_REQUIRE(ld_o32 >= int64_t(H) * hd, "xt_attention_fwd: ld_o32 smaller than H·hd");
-    if (!aligned16(o32) || ld_o32 % 4) return fail(XT_ERR_ALIGNMENT, "xt_attention_fwd: o32 must be 16-byte aligned rows");
-  }
+  if (o_lo && !aligned16(o_lo)) return fail(XT_ERR_ALIGNMENT, "xt_attention_fwd: o_lo must be 16-byte aligned");
   if (int64_t(B) * S * H == 0) return XT_OK;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv, to, tolo;
   XT_TRY(head_map(&tq, q, ld_qkv, B, S, H, BT));
   XT_TRY(head_map(&tk, k, ld_qkv, B, S, H, BT));
   XT_TRY(head_map(&tv, v, ld_qkv, B, S, H, BT));
   XT_TRY(head_map(&to, o, ld_o, B, S, H, 32));
+  XT_TRY(head_map(&tolo, o_lo ? o_lo : o, ld_o, B, S, H, 32));
   FwdParams p{};
   p.B = B;
   p.H = H;
@@ -1105,13 +1171,12 @@ int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   p.causal = causal;
   p.sc = float(1.0 / std::sqrt(double(hd)) * 1.4426950408889634);
   p.lse = lse;
-  p.o32 = o32;
-  p.ld32 = ld_o32;
+  p.o_lo = o_lo != nullptr;
   p.flag = errflag();
   static bool smem_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_fwd_kernel), FwdSmem::BYTES, smem_set, "xt_attention_fwd"));
   const int grid = p.items < num_sms() ? p.items : num_sms();
-  attn_fwd_kernel<<<grid, attn::kThreads, FwdSmem::BYTES, as_stream(stream)>>>(tq, tk, tv, to, p);
+  attn_fwd_kernel<<<grid, attn::kThreads, FwdSmem::BYTES, as_stream(stream)>>>(tq, tk, tv, to, tolo, p);
   return check_launch("xt_attention_fwd");
 }
 
@@ -1121,10 +1186,9 @@ int xt_attention_bwd_workspace_size(int B, int S, int H, size_t* bytes) {
   return XT_OK;
 }
 
-int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o, const void* d_o,
-                     int64_t ld_o, const float* lse, const float* o32, int64_t ld_o32, void* dq, void* dk, void* dv,
-                     int64_t ld_dqkv, void* ws, size_t ws_bytes, int B, int S, int H, int hd, int causal, int dt,
-                     void* stream) {
+int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv, const void* o, const void* o_lo,
+                     const void* d_o, int64_t ld_o, const float* lse, void* dq, void* dk, void* dv, int64_t ld_dqkv,
+                     void* ws, size_t ws_bytes, int B, int S, int H, int hd, int causal, int dt, void* stream) {
   XT_TRY(check_common("xt_attention_bwd", B, S, H, hd, causal, dt, ld_qkv, ld_o,
                       {q, k, v, o, d_o, lse, dq, dk, dv, ws}));
   XT_REQUIRE(ld_dqkv >= int64_t(H) * hd, "xt_attention_bwd: ld_dqkv smaller than H·hd");
@@ -1140,14 +1204,9 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
     int64_t blocks = ceil_div(threads, 256);
     const int64_t cap = int64_t(num_sms()) * 8;
     if (blocks > cap) blocks = cap;
-    if (o32) {
-      XT_REQUIRE(ld_o32 >= int64_t(H) * hd, "xt_attention_bwd: ld_o32 smaller than H·hd");
-      if (!aligned16(o32) || ld_o32 % 4) return fail(XT_ERR_ALIGNMENT, "xt_attention_bwd: o32 must be 16-byte aligned rows");
-      attn_delta_kernel<float><<<int(blocks), 256, 0, s>>>(o32, ld_o32, static_cast<const bf16*>(d_o), ld_o, B, S, H, D);
-    } else {
-      attn_delta_kernel<bf16><<<int(blocks), 256, 0, s>>>(static_cast<const bf16*>(o), ld_o,
-                                                          static_cast<const bf16*>(d_o), ld_o, B, S, H, D);
-    }
+    if (o_lo && !aligned16(o_lo)) return fail(XT_ERR_ALIGNMENT, "xt_attention_bwd: o_lo must be 16-byte aligned");
+    attn_delta_kernel<<<int(blocks), 256, 0, s>>>(static_cast<const bf16*>(o), static_cast<const bf16*>(o_lo),
+                                                   static_cast<const bf16*>(d_o), ld_o, B, S, H, D);
     XT_TRY(check_launch("xt_attention_bwd (delta)"));
   }
   CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;

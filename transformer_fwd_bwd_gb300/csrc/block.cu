@@ -181,7 +181,7 @@ struct Bufs {
   // P[l]: the layer's probabilities [B, H, S, S] (composed attention) or its softmax
   // normaliser lse, float32 [B, H, S] (fused attention)
   std::vector<void*> h_in, x1, qkv, P, o, h_mid, x2, up, mact;
-  std::vector<float*> o32;  // fused attention: float32 copy of o (the backward's D is formed from it)
+  std::vector<void*> o_lo;  // fused attention: o's bf16 rounding residual (the backward's D uses o + o_lo)
   std::vector<float*> st1, st2;
   void *h_final, *hf, *logits, *tmp;
   float *stf, *lse, *rope, *dh, *one;
@@ -197,7 +197,7 @@ int carve(const Dims& m, void* base, Bufs& b) {
   const size_t act = size_t(T * d * e);
   b.h_in.resize(m.L); b.x1.resize(m.L); b.qkv.resize(m.L); b.P.resize(m.L); b.o.resize(m.L);
   b.h_mid.resize(m.L); b.x2.resize(m.L); b.up.resize(m.L); b.mact.resize(m.L);
-  b.st1.resize(m.L); b.st2.resize(m.L); b.o32.assign(m.L, nullptr);
+  b.st1.resize(m.L); b.st2.resize(m.L); b.o_lo.assign(m.L, nullptr);
   for (int64_t l = 0; l < m.L; ++l) {
     b.h_in[l] = a.take(act);
     b.x1[l] = a.take(act);
@@ -205,7 +205,7 @@ int carve(const Dims& m, void* base, Bufs& b) {
     b.qkv[l] = a.take(size_t(T * 3 * d * e));
     b.P[l] = a.take(m.fused ? size_t(m.B * m.H * m.S) * 4 : size_t(m.B * m.H * m.S * m.S * e));
     b.o[l] = a.take(act);
-    if (m.fused) b.o32[l] = static_cast<float*>(a.take(size_t(T * d) * 4));
+    if (m.fused) b.o_lo[l] = a.take(act);
     b.h_mid[l] = a.take(act);
     b.x2[l] = a.take(act);
     b.st2[l] = static_cast<float*>(a.take(size_t(2 * T) * 4));
@@ -338,9 +338,8 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
     if (c.rope)  // q and k blocks are 2H consecutive heads of each qkv row
       XT_TRY(xt_rope_fwd(b.qkv[l], b.qkv[l], b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, stream));
     if (m.fused) {
-      XT_TRY(xt_attention_fwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], d,
-                              static_cast<float*>(b.P[l]), b.o32[l], d, int(m.B), int(m.S), int(m.H), int(m.hd), 1,
-                              m.dt, stream));
+      XT_TRY(xt_attention_fwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.o_lo[l], d,
+                              static_cast<float*>(b.P[l]), int(m.B), int(m.S), int(m.H), int(m.hd), 1, m.dt, stream));
     } else {
       XT_TRY(matmul(att_scores(m), b.qkv[l], off(b.qkv[l], d, e), b.P[l], b.ws_mm, b.ws_mm_bytes, s));
       XT_TRY(xt_softmax_fwd(b.P[l], b.P[l], m.B * m.H * m.S, m.S, 2, m.S, m.dt, stream));
@@ -402,9 +401,8 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
     XT_TRY(matmul(lin_dw(m, d, d), b.o[l], b.gA, prm->dWo[l], b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(matmul(lin_dx(m, d, d), b.gA, prm->Wo[l], b.gB, b.ws_mm, b.ws_mm_bytes, s));
     if (m.fused) {
-      XT_TRY(xt_attention_bwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.gB, d,
-                              static_cast<const float*>(b.P[l]), b.o32[l], d, b.dqkv, off(b.dqkv, d, e),
-                              off(b.dqkv, 2 * d, e),
+      XT_TRY(xt_attention_bwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.o_lo[l], b.gB,
+                              d, static_cast<const float*>(b.P[l]), b.dqkv, off(b.dqkv, d, e), off(b.dqkv, 2 * d, e),
                               3 * d, b.dP, b.dP_bytes, int(m.B), int(m.S), int(m.H), int(m.hd), 1, m.dt, stream));
     } else {
       XT_TRY(matmul(att_dp(m), b.gB, off(b.qkv[l], 2 * d, e), b.dP, b.ws_mm, b.ws_mm_bytes, s));

@@ -102,10 +102,10 @@ _SIGS = {
     "xt_rope_bwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _I, _VP],
     "xt_softmax_fwd": [_VP, _VP, _I64, _I64, _I, _I64, _I, _VP],
     "xt_softmax_bwd": [_VP, _VP, _VP, _I64, _I64, _I, _I64, _I, _I, _VP],
-    "xt_attention_fwd": [_VP, _VP, _VP, _I64, _VP, _I64, _VP, _VP, _I64, _I, _I, _I, _I, _I, _I, _VP],
+    "xt_attention_fwd": [_VP, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _I, _I, _I, _I, _I, _I, _VP],
     "xt_attention_bwd_workspace_size": [_I, _I, _I, _SZP],
-    "xt_attention_bwd": [_VP, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _VP,
-                         C.c_size_t, _I, _I, _I, _I, _I, _I, _VP],
+    "xt_attention_bwd": [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _VP, _VP, _I64, _VP, C.c_size_t,
+                         _I, _I, _I, _I, _I, _I, _VP],
     "xt_cross_entropy_workspace_size": [_I64, _SZP],
     "xt_cross_entropy_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _I, _VP, _VP],
     "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
@@ -392,22 +392,25 @@ def xt_softmax_fwd(x, y, causal=0, q_len=0, s=None):
     call("xt_softmax_fwd", ptr(x), ptr(y), rows, cols, causal, q_len, dt(x), stream(s))
 
 
-def xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, causal=1, o32=None, s=None):
-    """q, k, v: [B·S, ld] views (head h at columns h·hd); o: [B·S, ld_o]; lse: float32 [B, H, S];
-    o32: optional float32 [B·S, ld] copy of O before rounding."""
-    call("xt_attention_fwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False), o.stride(0),
-         ptr(lse), ptr(o32, False), o32.stride(0) if o32 is not None else 0, B, S, H, hd, causal, dt(q), stream(s))
+def xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, causal=1, o_lo=None, s=None):
+    """q, k, v: [B·S, ld] views (head h at columns h·hd); o (and the optional rounding residual
+    o_lo, same layout): [B·S, ld_o] bf16; lse: float32 [B, H, S]."""
+    if o_lo is not None and o_lo.stride(0) != o.stride(0):
+        raise ValueError("o_lo must have o's row stride")
+    call("xt_attention_fwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False),
+         ptr(o_lo, False), o.stride(0), ptr(lse), B, S, H, hd, causal, dt(q), stream(s))
 
 
-def xt_attention_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, S, H, hd, causal=1, o32=None, ws=None, s=None):
+def xt_attention_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, S, H, hd, causal=1, o_lo=None, ws=None, s=None):
+    if d_o.stride(0) != o.stride(0) or (o_lo is not None and o_lo.stride(0) != o.stride(0)):
+        raise ValueError("o, o_lo and d_o must share a row stride")
     n = C.c_size_t(0)
     call("xt_attention_bwd_workspace_size", B, S, H, C.byref(n))
     if ws is None:
         ws = torch.empty(max(1, n.value), dtype=torch.uint8, device=q.device)
     call("xt_attention_bwd", ptr(q, False), ptr(k, False), ptr(v, False), q.stride(0), ptr(o, False),
-         ptr(d_o, False), o.stride(0), ptr(lse), ptr(o32, False), o32.stride(0) if o32 is not None else 0,
-         ptr(dq, False), ptr(dk, False), ptr(dv, False), dq.stride(0), ptr(ws), ws.numel(), B, S, H, hd, causal,
-         dt(q), stream(s))
+         ptr(o_lo, False), ptr(d_o, False), o.stride(0), ptr(lse), ptr(dq, False), ptr(dk, False), ptr(dv, False),
+         dq.stride(0), ptr(ws), ws.numel(), B, S, H, hd, causal, dt(q), stream(s))
 
 
 def xt_softmax_bwd(d, y, dx, causal=0, q_len=0, acc=0, s=None):
