@@ -45,7 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
-    ap.add_argument("--kernel", choices=["attention", "gemm"], default=None,
+    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu"], default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
     ap.add_argument("--shape", default="8192,3072,768,0,1",
                     help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
@@ -406,6 +406,36 @@ def run_kernel(args):
         print(json.dumps({"kernel": "attention", "workload": f"B{B} S{S} H{H}x{hd} causal bf16",
                           "fwd_us": fwd_us, "bwd_us": bwd_us, "fwd_tflops": fl / fwd_us / 1e6,
                           "bwd_tflops": 2 * fl / bwd_us / 1e6, "clocks": clocks}))
+    elif args.kernel == "layernorm":
+        # as the stack launches it: bf16 rows, float32 residual gradient accumulated, float32 dγ / dβ
+        cfg = synth.BLOCK_CONFIGS[args.workload]
+        R, Cn = cfg["B"] * cfg["S"], cfg["d"]
+        x = torch.randn(R, Cn, generator=g).to(torch.bfloat16).to(dev)
+        dy = torch.randn(R, Cn, generator=g).to(torch.bfloat16).to(dev)
+        gam = torch.ones(Cn, dtype=torch.bfloat16, device=dev)
+        bet = torch.zeros(Cn, dtype=torch.bfloat16, device=dev)
+        y = torch.empty_like(x)
+        mean = torch.empty(R, dtype=torch.float32, device=dev)
+        rstd = torch.empty(R, dtype=torch.float32, device=dev)
+        dh = torch.zeros(R, Cn, dtype=torch.float32, device=dev)
+        dg = torch.zeros(Cn, dtype=torch.float32, device=dev)
+        db = torch.zeros(Cn, dtype=torch.float32, device=dev)
+        fwd_us = timed(lambda: xt.xt_layernorm_fwd(x, gam, bet, y, mean, rstd, cfg["eps"]))
+        bwd_us = timed(lambda: xt.xt_layernorm_bwd(dy, x, gam, mean, rstd, dh, dg, db, acc_dx=1, acc_param=1))
+        fb, bb = 2 * R * Cn * 2 + 8 * R, R * Cn * (2 + 2 + 4 + 4) + 8 * R   # fwd: x, y; bwd: d, x, dh read + write
+        print(json.dumps({"kernel": "layernorm", "rows": R, "cols": Cn, "fwd_us": fwd_us, "bwd_us": bwd_us,
+                          "fwd_gbs": fb / fwd_us / 1e3, "bwd_gbs": bb / bwd_us / 1e3, "clocks": clocks}))
+    elif args.kernel == "gelu":
+        cfg = synth.BLOCK_CONFIGS[args.workload]
+        n = cfg["B"] * cfg["S"] * cfg["F"]
+        a = torch.randn(n, generator=g).to(torch.bfloat16).to(dev)
+        d = torch.randn(n, generator=g).to(torch.bfloat16).to(dev)
+        y = torch.empty_like(a)
+        dx = torch.empty_like(a)
+        fwd_us = timed(lambda: xt.xt_gelu_fwd(a, y))
+        bwd_us = timed(lambda: xt.xt_gelu_bwd(d, a, dx))
+        print(json.dumps({"kernel": "gelu", "n": n, "fwd_us": fwd_us, "bwd_us": bwd_us,
+                          "fwd_gbs": 4 * n / fwd_us / 1e3, "bwd_gbs": 6 * n / bwd_us / 1e3, "clocks": clocks}))
     else:
         M, N, K, ta, tb = (int(x) for x in args.shape.split(","))
         A = (torch.randn(K, M, generator=g) if ta else torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)

@@ -312,7 +312,16 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
   }
 }
 
-template <typename T, typename TD, int VW, int MAXT>
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// LayerNorm backward, one row group per row: NVT vectors per thread.  The row's old residual
+// gradient (acc_dx) is prefetched into L1 with d and x, so the accumulate after the two row
+// reductions does not start a second trip to L2.  dγ and dβ partials stay in registers for the
+// thread's fixed columns across all of its rows; the row groups' partials meet in shared memory
+// once, at the end, and are folded in group order.
+template <typename T, typename TD, int VW, int NVT, int MAXT>
 __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
                                                      const T* __restrict__ gamma, const float* __restrict__ mean,
                                                      const float* __restrict__ rstd, TD* dx, float* __restrict__ part_g,
@@ -320,37 +329,35 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
                                                      int tpr, int acc_dx) {
   extern __shared__ float smem[];
   float* red = smem;
-  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
-  float* pg = smem + 32 + int64_t(threadIdx.x / tpr) * cols;             // dγ slice of this row group
-  float* pb = smem + 32 + int64_t(rpb + threadIdx.x / tpr) * cols;       // dβ slice
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr, grp = threadIdx.x / tpr;
   const int64_t nvec = cols / VW;
-  Raw<T, VW> gm[NV];
+  float ag[NVT][VW], ab[NVT][VW];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int64_t j = l + int64_t(k) * tpr;
-    if (j < nvec) gm[k].load(gamma + j * VW); else gm[k].zero();
-  }
-  if (part_g) slice_zero<VW>(pg, l, tpr, nvec);
-  if (part_b) slice_zero<VW>(pb, l, tpr, nvec);
+  for (int k = 0; k < NVT; ++k)
+#pragma unroll
+    for (int e = 0; e < VW; ++e) ag[k][e] = ab[k][e] = 0.f;
   const float inv_n = 1.f / float(cols);
   for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
-    const int64_t r = r0 + threadIdx.x / tpr;
+    const int64_t r = r0 + grp;
     const bool act = r < rows;
     const float mu = act ? mean[r] : 0.f, rs = act ? rstd[r] : 0.f;
-    Raw<T, VW> vd[NV], vx[NV];
+    Raw<T, VW> vd[NVT], vx[NVT];
     float sg = 0.f, sgx = 0.f;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
+    for (int k = 0; k < NVT; ++k) {
       const int64_t j = l + int64_t(k) * tpr;
+      Raw<T, VW> gm;  // γ is re-read from L1 rather than held in registers
       if (act && j < nvec) {
         vd[k].load(d + r * cols + j * VW);
         vx[k].load(x + r * cols + j * VW);
+        gm.load(gamma + j * VW);
+        if (dx && acc_dx) prefetch_l1(dx + r * cols + j * VW);
       } else {
-        vd[k].zero(); vx[k].zero();
+        vd[k].zero(); vx[k].zero(); gm.zero();
       }
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        const float g = vd[k].get(e) * gm[k].get(e);
+        const float g = vd[k].get(e) * gm.get(e);
         sg += g;
         sgx += g * (vx[k].get(e) - mu) * rs;
       }
@@ -358,19 +365,19 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
     const float mg = group_reduce<false>(sg, tpr, red) * inv_n;
     const float mgx = group_reduce<false>(sgx, tpr, red) * inv_n;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
+    for (int k = 0; k < NVT; ++k) {
       const int64_t j = l + int64_t(k) * tpr;
       if (act && j < nvec) {
-        float o[VW], pgv[VW], pbv[VW];
+        Raw<T, VW> gm;
+        gm.load(gamma + j * VW);
+        float o[VW];
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const float xh = (vx[k].get(e) - mu) * rs, dv = vd[k].get(e);
-          o[e] = rs * (dv * gm[k].get(e) - mg - xh * mgx);
-          pgv[e] = dv * xh;
-          pbv[e] = dv;
+          o[e] = rs * (dv * gm.get(e) - mg - xh * mgx);
+          ag[k][e] = fmaf(dv, xh, ag[k][e]);
+          ab[k][e] += dv;
         }
-        if (part_g) slice_add<VW>(pg + j * VW, pgv);
-        if (part_b) slice_add<VW>(pb + j * VW, pbv);
         if (dx) {
           TD* p = dx + r * cols + j * VW;
           if (acc_dx) {
@@ -384,6 +391,21 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
       }
     }
   }
+  if (part_g || part_b) {
+    __syncthreads();  // the reductions' scratch and the slices share shared memory
+    float* sgp = smem + 32 + int64_t(grp) * cols;
+    float* sbp = smem + 32 + int64_t(rpb + grp) * cols;
+#pragma unroll
+    for (int k = 0; k < NVT; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (j < nvec)
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          sgp[j * VW + e] = ag[k][e];
+          sbp[j * VW + e] = ab[k][e];
+        }
+    }
+  }
   if (part_g) slices_fold(smem + 32, rpb, part_g, cols);
   if (part_b) slices_fold(smem + 32 + int64_t(rpb) * cols, rpb, part_b, cols);
 }
@@ -391,17 +413,35 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
 // ============================================================================== column sums
 
 // part[nb][cols] → out[cols] (dtype TO).  Block (32, 32): threadIdx.x picks a column of a
-// 32-column slab, threadIdx.y a slice of partial rows (y, y+32, ...); the 32 slice sums are
-// then added in a fixed tree order, so the result does not depend on timing.
+// 32-column slab, threadIdx.y a slice of partial rows (y, y+32, ...), summed as four running sums
+// over b ≡ 0, 1, 2, 3 (mod 4) of the slice so the loads overlap; the sums, then the 32 slice sums,
+// are added in a fixed order, so the result does not depend on timing.  blockIdx.y selects one of
+// two (part, out) jobs, so two column sums of a kernel finalize in one launch.
+struct ColsumJob {
+  const float* part;
+  void* out;
+};
 template <typename TO>
-__global__ void __launch_bounds__(1024) colsum_finalize(const float* __restrict__ part, int nb, int64_t cols, TO* out,
-                                                       int acc) {
+__global__ void __launch_bounds__(1024) colsum_finalize(ColsumJob j0, ColsumJob j1, int nb, int64_t cols, int acc) {
   __shared__ float red[32][33];
+  const ColsumJob jb = blockIdx.y ? j1 : j0;
+  const float* part = jb.part;
+  TO* out = static_cast<TO*>(jb.out);
   const int64_t c = int64_t(blockIdx.x) * 32 + threadIdx.x;
-  float s = 0.f;
-  if (c < cols)
-    for (int b = threadIdx.y; b < nb; b += 32) s += part[int64_t(b) * cols + c];
-  red[threadIdx.y][threadIdx.x] = s;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  if (c < cols) {
+    int b = threadIdx.y;
+    for (; b + 96 < nb; b += 128) {
+      s0 += part[int64_t(b) * cols + c];
+      s1 += part[int64_t(b + 32) * cols + c];
+      s2 += part[int64_t(b + 64) * cols + c];
+      s3 += part[int64_t(b + 96) * cols + c];
+    }
+    if (b < nb) s0 += part[int64_t(b) * cols + c];
+    if (b + 32 < nb) s1 += part[int64_t(b + 32) * cols + c];
+    if (b + 64 < nb) s2 += part[int64_t(b + 64) * cols + c];
+  }
+  red[threadIdx.y][threadIdx.x] = (s0 + s1) + (s2 + s3);
   __syncthreads();
   for (int w = 16; w > 0; w >>= 1) {
     if (threadIdx.y < w) red[threadIdx.y][threadIdx.x] += red[threadIdx.y + w][threadIdx.x];
@@ -414,11 +454,14 @@ __global__ void __launch_bounds__(1024) colsum_finalize(const float* __restrict_
   }
 }
 
-static int finalize(const float* part, int nb, int64_t cols, void* out, int dt, int acc, cudaStream_t s) {
-  const unsigned grid = unsigned(ceil_div(cols, 32));
+// Finalizes one or two column sums (out1 may be null) of `nb` partial rows each.
+static int finalize(const float* part, int nb, int64_t cols, void* out, int dt, int acc, cudaStream_t s,
+                    const float* part1 = nullptr, void* out1 = nullptr) {
+  const dim3 grid(unsigned(ceil_div(cols, 32)), out1 ? 2u : 1u);
   const dim3 block(32, 32);
-  if (dt == XT_F32) colsum_finalize<float><<<grid, block, 0, s>>>(part, nb, cols, static_cast<float*>(out), acc);
-  else colsum_finalize<bf16><<<grid, block, 0, s>>>(part, nb, cols, static_cast<bf16*>(out), acc);
+  const ColsumJob j0{part, out}, j1{part1, out1};
+  if (dt == XT_F32) colsum_finalize<float><<<grid, block, 0, s>>>(j0, j1, nb, cols, acc);
+  else colsum_finalize<bf16><<<grid, block, 0, s>>>(j0, j1, nb, cols, acc);
   return check_launch("column-sum finalize");
 }
 
@@ -1066,20 +1109,33 @@ int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const floa
   const bool vec = rows_vec_ok(cols, dt, {d, x, gamma, dx});
   RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1, kBwdMaxTpr);
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
-  const int nb = bwd_blocks(rows, pl.rpb);
+  // two blocks per SM are resident (128 registers × 256 threads), and the partials live in
+  // registers across rows: more blocks would only add partial rows to fold
+  int nb = bwd_blocks(rows, pl.rpb);
+  if (nb > 2 * num_sms()) nb = 2 * num_sms();
   float* part_g = dgamma ? static_cast<float*>(ws) : nullptr;
   float* part_b = dbeta ? static_cast<float*>(ws) + size_t(nb) * size_t(cols) : nullptr;
   const size_t smem = (32 + 2 * size_t(pl.rpb) * size_t(cols)) * sizeof(float);
   if (smem > 200 * 1024) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
+  const int64_t nvt = ceil_div(ceil_div(cols, pl.vw), pl.tpr);  // vectors per thread (1..NV)
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
-    auto k = pl.threads <= 256 ? ln_bwd_kernel<T, TD, VW, 256> : ln_bwd_kernel<T, TD, VW, 512>;
+    void (*k)(const T*, const T*, const T*, const float*, const float*, TD*, float*, float*, int64_t, int64_t, int,
+              int) = nullptr;
+    const bool narrow = pl.threads <= 256;
+    switch (nvt) {
+      case 1: k = narrow ? ln_bwd_kernel<T, TD, VW, 1, 256> : ln_bwd_kernel<T, TD, VW, 1, 512>; break;
+      case 2: k = narrow ? ln_bwd_kernel<T, TD, VW, 2, 256> : ln_bwd_kernel<T, TD, VW, 2, 512>; break;
+      case 3: k = narrow ? ln_bwd_kernel<T, TD, VW, 3, 256> : ln_bwd_kernel<T, TD, VW, 3, 512>; break;
+      default: k = narrow ? ln_bwd_kernel<T, TD, VW, 4, 256> : ln_bwd_kernel<T, TD, VW, 4, 512>; break;
+    }
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
                                    mean, rstd, static_cast<TD*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_layernorm_bwd"));
-  if (dgamma) XT_TRY(finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s));
-  if (dbeta) XT_TRY(finalize(part_b, nb, cols, dbeta, dt_param, acc_param, s));
+  if (dgamma && dbeta) return finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s, part_b, dbeta);
+  if (dgamma) return finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s);
+  if (dbeta) return finalize(part_b, nb, cols, dbeta, dt_param, acc_param, s);
   return XT_OK;
 }
 
