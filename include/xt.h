@@ -332,6 +332,20 @@ int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void
 /* Backward of C = alpha·op(A)@op(B) given dC (layout of C, dtype dtype_ab):
  * dA = alpha·dC@op(B)ᵀ into A's layout, dB = alpha·op(A)ᵀ@dC into B's layout; dA/dB have
  * dtype dt_grad_a / dt_grad_b; either may be NULL.  causal must be 0. */
+/* The GELU of the MLP ([BP] § Framåtgåendet: the up projection followed by exact GELU) fused
+ * into the GEMM epilogue, gelu(a) = a·Φ(a):
+ *   xt_matmul_gelu_fwd: C = alpha·op(A)@op(B) (the pre-activation, rounded to bf16) and
+ *                       Y = gelu(C) evaluated on that rounded value;
+ *   xt_matmul_gelu_bwd: C = (alpha·op(A)@op(B)) ∘ gelu'(X) with gelu'(a) = Φ(a) + a·φ(a),
+ *                       X the saved pre-activation (the GELU backward applied to the product).
+ * Y and X are bf16 with C's layout (ldc).  Restrictions (else XT_ERR_UNSUPPORTED /
+ * XT_ERR_INVALID_ARG): dtype_ab = dtype_c = XT_BF16, one batch, accumulate = 0, causal = 0,
+ * N a multiple of 64; Y / X 16-byte aligned.  Workspace as xt_matmul_workspace_size. */
+int xt_matmul_gelu_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* Y,
+                       void* ws, size_t ws_bytes, void* stream);
+int xt_matmul_gelu_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* X, void* C,
+                       void* ws, size_t ws_bytes, void* stream);
+
 int xt_matmul_bwd_workspace_size(const xt_matmul_desc* desc, size_t* bytes);
 int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* dC,
                   void* dA, void* dB, int dt_grad_a, int dt_grad_b, int acc_a, int acc_b,

@@ -12,7 +12,7 @@ import torch
 
 import synth
 from oracle import ops as O
-from tests.gpu_util import dev, host, norm_err, sync
+from tests.gpu_util import check, dev, host, norm_err, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -199,3 +199,51 @@ def test_matmul_split_k(ab, c, M, N, K):
     assert norm_err(outs[0], want) <= tol
     assert np.array_equal(outs[0], outs[1]), "K split is not deterministic"
     assert xt.device_errors() == 0
+
+
+GELU_CASES = [(200, 320, 72), (1000, 768, 328), (256, 3072, 768), (128, 64, 64)]
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", GELU_CASES)
+def test_matmul_gelu_fwd(ta, tb, M, N, K):
+    """[BP] MLP up projection + exact GELU from one GEMM: C = α·op(A)@op(B) in bf16, and
+    Y = gelu(C) of that rounded C to one bf16 ulp; end to end Y against the oracle's
+    gelu(matmul) within the bf16 GEMM bound."""
+    A, B = stored(M, N, K, ta, tb, "bf16", 45)
+    want_c = O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5
+    Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16, alpha=0.5)
+    xt.xt_matmul_gelu_fwd(d, dev(A, "bf16"), dev(B, "bf16"), Cm, Y); sync()
+    assert xt.device_errors() == 0
+    c = host(Cm)
+    assert norm_err(c, want_c) <= 4e-3
+    check(host(Y), O.gelu_fwd(c), "bf16", "gelu of the stored pre-activation")
+    assert norm_err(host(Y), O.gelu_fwd(want_c)) <= 4e-3
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", GELU_CASES)
+def test_matmul_gelu_bwd(ta, tb, M, N, K):
+    """GELU backward fused after the product: C = (α·op(A)@op(B)) ∘ gelu'(X)."""
+    A, B = stored(M, N, K, ta, tb, "bf16", 46)
+    X = synth.normal((M, N), 47, dtype="bf16")
+    want = O.gelu_bwd(O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5, X)
+    Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16, alpha=0.5)
+    xt.xt_matmul_gelu_bwd(d, dev(A, "bf16"), dev(B, "bf16"), dev(X, "bf16"), Cm); sync()
+    assert xt.device_errors() == 0
+    assert norm_err(host(Cm), want) <= 4e-3
+
+
+def test_matmul_gelu_rejects():
+    A = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(64, 96, dtype=torch.bfloat16, device="cuda")
+    Cm = torch.zeros(128, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(xt.XtError):   # N not a multiple of 64
+        xt.xt_matmul_gelu_fwd(xt.matmul_desc(128, 96, 64, dtype_c=xt.XT_BF16), A, B, Cm, Cm)
+    C32 = torch.zeros(128, 128, dtype=torch.float32, device="cuda")
+    B2 = torch.zeros(64, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(xt.XtError):   # float32 output
+        xt.xt_matmul_gelu_fwd(xt.matmul_desc(128, 128, 64, dtype_c=xt.XT_F32), A, B2, C32, C32)

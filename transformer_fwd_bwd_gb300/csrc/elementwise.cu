@@ -52,47 +52,6 @@ __device__ __forceinline__ bool dropout_keep(uint64_t seed, uint64_t i, float p)
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
-// Φ(x) = ½·erfc(−x/√2) (no cancellation for x ≪ 0, unlike ½(1 + erf(x/√2))), with erfc from the
-// Chebyshev-fitted form of Press, Teukolsky, Vetterling & Flannery, Numerical Recipes (§6.2,
-// erfcc): for z ≥ 0, erfc(z) = t·exp(−z² + P(t)), t = 1/(1 + z/2), P a degree-9 polynomial in t;
-// fractional error below 1.2e-7 for every z, and erfc(−z) = 2 − erfc(z).  One reciprocal, one
-// exponential and nine FMAs.  The backward also needs φ(x) = exp(−x²/2)/√(2π) = exp(−z²)/√(2π),
-// so both come out of one evaluation.
-struct Gauss {
-  float cdf, pdf;
-};
-// t and P(t) of the erfc form for z = |x|/√2.
-__device__ __forceinline__ float erfc_poly(float z, float& t) {
-  t = __fdividef(1.f, fmaf(0.5f, z, 1.f));
-  float q = 0.17087277f;
-  q = fmaf(q, t, -0.82215223f);
-  q = fmaf(q, t, 1.48851587f);
-  q = fmaf(q, t, -1.13520398f);
-  q = fmaf(q, t, 0.27886807f);
-  q = fmaf(q, t, -0.18628806f);
-  q = fmaf(q, t, 0.09678418f);
-  q = fmaf(q, t, 0.37409196f);
-  q = fmaf(q, t, 1.00002368f);
-  return fmaf(q, t, -1.26551223f);
-}
-// Φ alone: one reciprocal and one exponential.
-__device__ __forceinline__ float gelu_cdf(float x) {
-  const float z = fabsf(x) * 0.70710678118654752f;
-  float t;
-  const float q = erfc_poly(z, t);
-  const float half_erfc = 0.5f * t * __expf(fmaf(-z, z, q));  // ½·erfc(|x|/√2) = Φ(−|x|)
-  return x <= 0.f ? half_erfc : 1.f - half_erfc;
-}
-// Φ and φ: φ needs exp(−x²/2) on its own, so one more exponential.
-__device__ __forceinline__ Gauss gauss(float x) {
-  const float z = fabsf(x) * 0.70710678118654752f;
-  float t;
-  const float q = erfc_poly(z, t);
-  const float e = __expf(-z * z);                    // exp(−x²/2)
-  const float half_erfc = 0.5f * t * e * __expf(q);  // ½·erfc(|x|/√2) = Φ(−|x|)
-  return Gauss{x <= 0.f ? half_erfc : 1.f - half_erfc, 0.39894228040143268f * e};
-}
-
 template <EwOp OP>
 __device__ __forceinline__ void ew_apply(float a, float b, float c, uint64_t i, const EwArgs& g,
                                          float& r0, float& r1) {

@@ -150,12 +150,15 @@ static int make_output_map(CUtensorMap* tm, void* base, bool bf16, int64_t M, in
 int run(const Problem& pb, cudaStream_t s) {
   const bool tf32 = pb.tf32;
   const int64_t batches = int64_t(pb.batch_outer) * pb.batch_inner;
-  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, true);
+  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, pb.act == 0);
   if (ch.splits > 1 && (pb.split_ws == nullptr || split_bytes(ch, pb.M, pb.N) > pb.split_ws_bytes))
     ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false);
+  if (pb.act) ch = Choice{256, 1};  // the GELU epilogues are built for BN 256 only
   const int bn = ch.bn;
   const bool split = ch.splits > 1;
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tb, tc, tc2;
+  memset(&tc2, 0, sizeof(tc2));
+  if (pb.act == 1) XT_TRY(make_output_map(&tc2, pb.C2, true, pb.M, pb.N, pb.ldc, 1, 1, 0, 0));
   XT_TRY(make_operand_map(&ta, pb.A, tf32, BM));
   XT_TRY(make_operand_map(&tb, pb.B, tf32, bn));
   // TMA epilogue for every output except a bf16 C that is accumulated into (TMA reduce-add is
@@ -187,6 +190,9 @@ int run(const Problem& pb, cudaStream_t s) {
   p.ldc = pb.ldc;
   p.sc_inner = pb.sc_inner;
   p.sc_outer = pb.sc_outer;
+  p.act = pb.act;
+  p.aux = static_cast<const bf16*>(pb.aux);
+  p.ld_aux = pb.ldc;
   p.flag = errflag();
   const int64_t tiles = int64_t(p.num_m) * p.num_n * p.batches;  // a K split counts its slices
   if (tiles > int64_t(1) << 30) return fail(XT_ERR_UNSUPPORTED, "matmul: too many tiles");
@@ -202,7 +208,9 @@ int run(const Problem& pb, cudaStream_t s) {
   const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, bn, int(amn), int(bmn),
                         split ? 10 * ch.splits : p.causal};
   const bool prof = gemm_profile_begin(s, flops, shape, &tok);
-  int st = tf32 ? launch_tf32(bn, amn, bmn, ta, tb, tc, p, grid, s) : launch_bf16(bn, amn, bmn, ta, tb, tc, p, grid, s);
+  int st = tf32      ? launch_tf32(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
+           : pb.act ? launch_bf16_act(pb.act, amn, bmn, ta, tb, tc, tc2, p, grid, s)
+                    : launch_bf16(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s);
   if (st == XT_OK && split) {
     const int64_t work = pb.M * (pb.N / 4);
     int64_t g = ceil_div(work, 256);
@@ -296,8 +304,18 @@ static size_t matmul_ws(const xt_matmul_desc* d) {
 
 // Validates and runs C[M,N] (+)= alpha · op(A) @ op(B) for one matmul descriptor.
 static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, void* C, void* ws, size_t ws_bytes,
-                      cudaStream_t s) {
+                      cudaStream_t s, int act = 0, void* C2 = nullptr, const void* aux = nullptr) {
   XT_REQUIRE(d != nullptr, "matmul: desc is NULL");
+  if (act) {
+    XT_REQUIRE(d->dtype_ab == XT_BF16 && d->dtype_c == XT_BF16, "matmul gelu: bf16 operands and output only");
+    XT_REQUIRE(!d->accumulate && !d->causal && d->batch_outer == 1 && d->batch_inner == 1,
+               "matmul gelu: one batch, no accumulate, no causal mode");
+    if (d->N % 64) return fail(XT_ERR_UNSUPPORTED, "matmul gelu: N must be a multiple of 64");
+    const void* extra = act == 1 ? C2 : aux;
+    XT_REQUIRE(d->M == 0 || d->N == 0 || extra != nullptr, "matmul gelu: %s is NULL", act == 1 ? "Y" : "X");
+    if (extra && !aligned16(extra)) return fail(XT_ERR_ALIGNMENT, "matmul gelu: Y / X must be 16-byte aligned");
+    XT_REQUIRE(d->K > 0 || d->M == 0 || d->N == 0, "matmul gelu: K must be positive");
+  }
   XT_REQUIRE(d->M >= 0 && d->N >= 0 && d->K >= 0, "matmul: negative size");
   XT_REQUIRE(d->batch_outer >= 1 && d->batch_inner >= 1, "matmul: batch counts must be >= 1");
   XT_REQUIRE(valid_dtype(d->dtype_ab) && valid_dtype(d->dtype_c), "matmul: bad dtype");
@@ -357,6 +375,9 @@ static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, voi
   pb.alpha = d->alpha;
   pb.accumulate = d->accumulate;
   pb.causal = d->causal;
+  pb.act = act;
+  pb.C2 = C2;
+  pb.aux = aux;
   return gemm::run(pb, s);
 }
 
@@ -375,6 +396,16 @@ int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes) {
 int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* ws, size_t ws_bytes,
                   void* stream) {
   return matmul_run(desc, A, B, C, ws, ws_bytes, as_stream(stream));
+}
+
+int xt_matmul_gelu_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* Y, void* ws,
+                       size_t ws_bytes, void* stream) {
+  return matmul_run(desc, A, B, C, ws, ws_bytes, as_stream(stream), 1, Y, nullptr);
+}
+
+int xt_matmul_gelu_bwd(const xt_matmul_desc* desc, const void* A, const void* B, const void* X, void* C, void* ws,
+                       size_t ws_bytes, void* stream) {
+  return matmul_run(desc, A, B, C, ws, ws_bytes, as_stream(stream), 2, nullptr, X);
 }
 
 }  // extern "C"
@@ -472,4 +503,5 @@ int matmul(const xt_matmul_desc& d, const void* A, const void* B, void* C, void*
   return matmul_run(&d, A, B, C, ws, ws_bytes, s);
 }
 size_t matmul_workspace(const xt_matmul_desc& d) { return matmul_ws(&d); }
+
 }  // namespace xt

@@ -33,6 +33,9 @@ struct Problem {
   int causal;
   void* split_ws;  // room for K-split partial tiles (may be null)
   size_t split_ws_bytes;
+  int act;         // GELU epilogue (see Params::act); 0 none
+  void* C2;        // act 1: gelu(C), C's layout
+  const void* aux; // act 2: the pre-activation, C's layout
 };
 
 // Tile width and K split chosen for a problem (see choose()).
@@ -48,14 +51,17 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn);
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 int run(const Problem& pb, cudaStream_t s);
 int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                const Params& p, int grid, cudaStream_t s);
+                const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                const Params& p, int grid, cudaStream_t s);
+                const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
+// bf16, BN 256, with the GELU epilogue `act` (1 or 2).
+int launch_bf16_act(int act, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                    const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 
-template <bool TF32, int BN, bool A_MN, bool B_MN>
-int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const Params& p, int grid,
-               cudaStream_t s) {
-  auto k = gemm_kernel<TF32, BN, A_MN, B_MN>;
+template <bool TF32, int BN, bool A_MN, bool B_MN, int ACT = 0>
+int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
+               const Params& p, int grid, cudaStream_t s) {
+  auto k = gemm_kernel<TF32, BN, A_MN, B_MN, ACT>;
   constexpr int smem = Cfg<TF32, BN>::SMEM;
   static bool attr_set = false;  // per instantiation; idempotent if raced
   if (!attr_set) {
@@ -63,7 +69,7 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
       return check_launch("gemm: shared memory attribute");
     attr_set = true;
   }
-  k<<<grid, kThreads, smem, s>>>(ta, tb, tc, p);
+  k<<<grid, kThreads, smem, s>>>(ta, tb, tc, tc2, p);
   return check_launch("gemm kernel");
 }
 

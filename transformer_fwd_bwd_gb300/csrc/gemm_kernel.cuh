@@ -38,6 +38,11 @@ struct Params {
   float alpha;
   void* C;
   int64_t ldc, sc_inner, sc_outer;
+  // GELU epilogue (bf16 C, TMA stores, one batch): 1 = also store gelu(C) through tmC2;
+  // 2 = C = (alpha·A@B) ∘ gelu'(aux), aux bf16 [M, N] with row stride ld_aux
+  int act;
+  const bf16* aux;
+  int64_t ld_aux;
   uint32_t* flag;
 };
 
@@ -269,10 +274,12 @@ __device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
   return ti;
 }
 
-template <bool TF32, int BN, bool A_MN, bool B_MN>
+// ACT: the epilogue's GELU mode (Params::act), a template parameter so the plain GEMMs carry
+// none of its code.
+template <bool TF32, int BN, bool A_MN, bool B_MN, int ACT = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const Params p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, const Params p) {
   using C_ = Cfg<TF32, BN>;
   constexpr int BK = C_::BK, ATOM = C_::ATOM, UK = C_::UK, STAGES = C_::STAGES;
   constexpr uint32_t IDESC = instr_desc<TF32, BN, A_MN, B_MN>();
@@ -306,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (p.tma_store) prefetch_tmap(&tmC);
+    if (ACT == 1) prefetch_tmap(&tmC2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TCOLS);
@@ -440,8 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / cw; ++c) {
           const int x = ti.n0 + c * cw;
           const bool write = rows_in && x < p.N && !(empty_k && p.accumulate);
-          const uint32_t buf = smem_u32(staging) + uint32_t((q * 2 + (chunk & 1)) * 4096);
-          if (lane == 0) bulk_wait_read_1();  // the store issued from this buffer two chunks ago has read it
+          // act 1 stores two tiles per chunk (C and gelu(C)) from both buffers; otherwise the
+          // buffers alternate between chunks
+          const uint32_t buf = smem_u32(staging) + uint32_t((q * 2 + (ACT == 1 ? 0 : (chunk & 1))) * 4096);
+          if (lane == 0) {
+            if (ACT == 1) bulk_wait_read_0();
+            else bulk_wait_read_1();  // the store issued from this buffer two chunks ago has read it
+          }
           __syncwarp();
           uint32_t r[64];
           if (!empty_k) {
@@ -464,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              __float_as_uint(__uint_as_float(r[4 * j + 1]) * p.alpha),
                              __float_as_uint(__uint_as_float(r[4 * j + 2]) * p.alpha),
                              __float_as_uint(__uint_as_float(r[4 * j + 3]) * p.alpha));
-            } else {
+            } else if constexpr (ACT == 0) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 uint32_t w[4];
@@ -476,6 +489,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
               }
+            } else if constexpr (ACT == 1) {
+              // the pre-activation a (rounded to bf16, the value the backward reads) and gelu(a),
+              // 16 columns at a time
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                float av[16], gv[16];
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(r[16 * h + 2 * e]) * p.alpha,
+                                                            __uint_as_float(r[16 * h + 2 * e + 1]) * p.alpha);
+                  w[e] = *reinterpret_cast<uint32_t*>(&hh);
+                  av[2 * e] = __low2float(hh);
+                  av[2 * e + 1] = __high2float(hh);
+                }
+                gelu_batch<16, 0>(av, gv);
+                uint32_t gw[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  __nv_bfloat162 gg = __floats2bfloat162_rn(gv[2 * e], gv[2 * e + 1]);
+                  gw[e] = *reinterpret_cast<uint32_t*>(&gg);
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int j = 2 * h + u;
+                  const uint32_t off = uint32_t(lane) * 128 + (uint32_t(j ^ (lane & 7)) << 4);
+                  st_shared_v4(buf + off, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                  st_shared_v4(buf + 4096 + off, gw[4 * u], gw[4 * u + 1], gw[4 * u + 2], gw[4 * u + 3]);
+                }
+              }
+            } else {
+              // dgelu: C ∘ gelu'(a) with a read from aux (this lane's row, 64 columns from x),
+              // 16 columns at a time; rows past M (a ragged last tile) are clipped by the TMA
+              // store: read nothing there
+              const bool row_ok = y + lane < p.M;
+              const uint4* ap = reinterpret_cast<const uint4*>(p.aux + int64_t(row_ok ? y + lane : y) * p.ld_aux + x);
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                float av[16], dv[16];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const uint4 a4 = row_ok ? __ldg(ap + 2 * h + u) : make_uint4(0u, 0u, 0u, 0u);
+                  const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 ah = *reinterpret_cast<const __nv_bfloat162*>(&aw[e]);
+                    av[8 * u + 2 * e] = __low2float(ah);
+                    av[8 * u + 2 * e + 1] = __high2float(ah);
+                  }
+                }
+                gelu_batch<16, 1>(av, dv);
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(r[16 * h + 2 * e]) * p.alpha * dv[2 * e],
+                                                            __uint_as_float(r[16 * h + 2 * e + 1]) * p.alpha * dv[2 * e + 1]);
+                  w[e] = *reinterpret_cast<uint32_t*>(&hh);
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int j = 2 * h + u;
+                  st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                               w[4 * u + 3]);
+                }
+              }
             }
             fence_proxy_async_smem();
           }
@@ -483,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (write && lane == 0) {
             if (p.accumulate) tma_reduce_add_4d(&tmC, buf, x, y, ti.zi, ti.zo);
             else tma_store_4d(&tmC, buf, x, y, ti.zi, ti.zo);
+            if (ACT == 1) tma_store_4d(&tmC2, buf + 4096, x, y, ti.zi, ti.zo);
             bulk_commit();
           }
           ++chunk;

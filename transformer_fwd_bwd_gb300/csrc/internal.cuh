@@ -8,4 +8,5 @@ namespace xt {
 int matmul(const xt_matmul_desc& d, const void* A, const void* B, void* C, void* ws, size_t ws_bytes,
            cudaStream_t s);
 size_t matmul_workspace(const xt_matmul_desc& d);
+
 }  // namespace xt

@@ -119,6 +119,8 @@ _SIGS = {
     "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
     "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
     "xt_matmul_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, C.c_size_t, _VP],
+    "xt_matmul_gelu_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, C.c_size_t, _VP],
+    "xt_matmul_gelu_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_bwd_workspace_size": [C.POINTER(MatmulDesc), _SZP],
     "xt_matmul_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, C.c_size_t, _VP],
     "xt_block_workspace_size": [C.POINTER(BlockConfig), _SZP],
@@ -492,6 +494,24 @@ def xt_matmul_fwd(desc, A, B, Cm, ws=None, s=None):
     if n and ws is None:
         ws = workspace(n, Cm.device)
     call("xt_matmul_fwd", C.byref(desc), ptr(A, False), ptr(B, False), ptr(Cm, False), ptr(ws),
+         ws.numel() if ws is not None else 0, stream(s))
+
+
+def xt_matmul_gelu_fwd(desc, A, B, Cm, Y, ws=None, s=None):
+    """Cm = alpha·op(A)@op(B) (bf16) and Y = gelu(Cm), from one GEMM."""
+    n = ws_bytes("xt_matmul_workspace_size", C.byref(desc))
+    if n and ws is None:
+        ws = workspace(n, Cm.device)
+    call("xt_matmul_gelu_fwd", C.byref(desc), ptr(A, False), ptr(B, False), ptr(Cm, False), ptr(Y, False), ptr(ws),
+         ws.numel() if ws is not None else 0, stream(s))
+
+
+def xt_matmul_gelu_bwd(desc, A, B, X, Cm, ws=None, s=None):
+    """Cm = (alpha·op(A)@op(B)) ∘ gelu'(X), X the saved pre-activation (Cm's layout)."""
+    n = ws_bytes("xt_matmul_workspace_size", C.byref(desc))
+    if n and ws is None:
+        ws = workspace(n, Cm.device)
+    call("xt_matmul_gelu_bwd", C.byref(desc), ptr(A, False), ptr(B, False), ptr(X, False), ptr(Cm, False), ptr(ws),
          ws.numel() if ws is not None else 0, stream(s))
 
 
