@@ -92,6 +92,14 @@ __device__ __forceinline__ void keep_before(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2⁻²², −inf → +0,
+// results below 2⁻¹²⁶ flushed to 0); the probabilities it feeds are rounded to bf16.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Bounded wait taken by a whole warp (the decision is warp-uniform).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float e[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-              e[t] = exp2f(fmaf(__uint_as_float(r[c * 64 + un * 8 + t]), p.sc, -ms));
+              e[t] = ex2(fmaf(__uint_as_float(r[c * 64 + un * 8 + t]), p.sc, -ms));
               ls[t] += e[t];
             }
             st_shared_v4(swz(ps, rr, c, un), pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
@@ -749,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int first = (p.causal && q_first + j == it.qt) ? rr : 0;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
-          const float e = exp2f(fmaf(__uint_as_float(r[c]), p.sc, -lv[c]));
+          const float e = ex2(fmaf(__uint_as_float(r[c]), p.sc, -lv[c]));
           r[c] = __float_as_uint(c < first ? 0.f : e);
         }
         keep_before(r);
@@ -1039,7 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
-          const float e = exp2f(fmaf(__uint_as_float(r[c]), p.sc, -lse2));
+          const float e = ex2(fmaf(__uint_as_float(r[c]), p.sc, -lse2));
           r[c] = __float_as_uint(c < lim ? e : 0.f);
         }
         keep_before(r);
