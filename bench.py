@@ -45,7 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
-    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu"], default=None,
+    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy"], default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
     ap.add_argument("--shape", default="8192,3072,768,0,1",
                     help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
@@ -436,6 +436,21 @@ def run_kernel(args):
         bwd_us = timed(lambda: xt.xt_gelu_bwd(d, a, dx))
         print(json.dumps({"kernel": "gelu", "n": n, "fwd_us": fwd_us, "bwd_us": bwd_us,
                           "fwd_gbs": 4 * n / fwd_us / 1e3, "bwd_gbs": 6 * n / bwd_us / 1e3, "clocks": clocks}))
+    elif args.kernel == "cross_entropy":
+        # the tied-logit loss as the stack runs it: bf16 logits [B·S, V], backward in place
+        cfg = synth.BLOCK_CONFIGS[args.workload]
+        R, V = cfg["B"] * cfg["S"], cfg["V"]
+        x = (torch.randn(R, V, generator=g) * 2.0).to(torch.bfloat16).to(dev)
+        tg = torch.randint(0, V, (R,), generator=g, dtype=torch.int32).to(dev)
+        lse = torch.empty(R, dtype=torch.float32, device=dev)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        one = torch.ones(1, dtype=torch.float32, device=dev)
+        dx = torch.empty_like(x)
+        fwd_us = timed(lambda: xt.xt_cross_entropy_fwd(x, tg, lse, loss))
+        bwd_us = timed(lambda: xt.xt_cross_entropy_bwd(x, tg, lse, one, dx))
+        print(json.dumps({"kernel": "cross_entropy", "rows": R, "V": V, "fwd_us": fwd_us, "bwd_us": bwd_us,
+                          "fwd_gbs": 2 * R * V / fwd_us / 1e3, "bwd_gbs": 4 * R * V / bwd_us / 1e3,
+                          "clocks": clocks}))
     else:
         M, N, K, ta, tb = (int(x) for x in args.shape.split(","))
         A = (torch.randn(K, M, generator=g) if ta else torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)

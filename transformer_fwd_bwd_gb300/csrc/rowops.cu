@@ -15,6 +15,13 @@ namespace xt {
 constexpr int NV = 4;  // vectors per thread in row-resident kernels
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2⁻²², −inf → +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Packed storage of one vector (VW elements) of T.
 template <typename T, int VW> struct Raw;
 template <typename T> struct Raw<T, 1> {
@@ -640,20 +647,37 @@ __global__ void __launch_bounds__(1024) ce_fwd_kernel(const T* __restrict__ x, c
   for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
     const int64_t r = r0 + threadIdx.x / tpr;
     const bool act = r < rows;
+    // per thread: running max m and s = Σ exp(x − m); s is rescaled only when a vector raises
+    // the max, so each logit costs one hardware exp2 (ex2.approx, relative error ~2⁻²²)
+    // four vectors per step, all four loads issued before any is used
     float m = -INFINITY, s = 0.f;
     if (act) {
       const T* row = x + r * V;
-      for (int64_t j = l; j < nvec; j += tpr) {
-        float v[VW];
-        load_vec<T, VW>(row + j * VW, v);
-        float vm = v[0];
+      for (int64_t j0 = l; j0 < nvec; j0 += 4 * int64_t(tpr)) {
+        float v[4][VW];
 #pragma unroll
-        for (int e = 1; e < VW; ++e) vm = fmaxf(vm, v[e]);
-        const float vml = vm * kLog2e;
-        float vs = 0.f;
+        for (int u = 0; u < 4; ++u) {
+          const int64_t j = j0 + int64_t(u) * tpr;
+          if (j < nvec) load_vec<T, VW>(row + j * VW, v[u]);
+          else
 #pragma unroll
-        for (int e = 0; e < VW; ++e) vs += exp2f(fmaf(v[e], kLog2e, -vml));
-        lse_merge(m, s, vm, vs);
+            for (int e = 0; e < VW; ++e) v[u][e] = -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float vm = v[u][0];
+#pragma unroll
+          for (int e = 1; e < VW; ++e) vm = fmaxf(vm, v[u][e]);
+          if (vm > m) {
+            s = (m == -INFINITY) ? 0.f : s * fast_exp2((m - vm) * kLog2e);
+            m = vm;
+          }
+          const float ml = m * kLog2e;
+          float vs = 0.f;
+#pragma unroll
+          for (int e = 0; e < VW; ++e) vs += fast_exp2(fmaf(v[u][e], kLog2e, -ml));
+          s += vs;
+        }
       }
     }
     // row-group merge of (m, s): warp shuffle, then shared memory across warps
@@ -720,7 +744,7 @@ __global__ void __launch_bounds__(256) ce_bwd_kernel(const T* x, const int32_t* 
       load_vec<T, VW>(xr + c, xv);
 #pragma unroll
       for (int e = 0; e < VW; ++e) {
-        const float p = exp2f(fmaf(xv[e], kLog2e, -Ll));
+        const float p = fast_exp2(fmaf(xv[e], kLog2e, -Ll));
         o[e] = bad ? __int_as_float(0x7fc00000) : sc * (p - (c + e == t ? 1.f : 0.f));
       }
       if (acc) {
