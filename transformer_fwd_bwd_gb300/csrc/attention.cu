@@ -35,6 +35,10 @@ using namespace gemm;
 constexpr int HD = 64;                     // head dimension the kernels are built for
 constexpr int BT = 128;                    // query / key tile
 constexpr int kThreads = 192;
+// Backward kernels: warp 0 TMA, warp 1 MMA, warps 2..9 rows — two warps per TMEM lane quadrant,
+// each owning 64 of a tile's 128 columns (the backward's P and dS are elementwise, so the halves
+// never need each other's values).
+constexpr int kThreadsBwd = 320;
 constexpr int TILE = BT * 128;             // one 128-row × 64-element bf16 tile: 16 KB
 constexpr int PT = 2 * TILE;               // 128 × 128 bf16 operand: two 64-wide K chunks
 constexpr int RING = 3;                    // K / V slots
@@ -531,7 +535,7 @@ struct KvSmem {
 // dK, dV for one 128-key tile per work item: thread = key row; Sᵀ = K Qᵀ and dPᵀ = V dOᵀ per
 // query tile, Pᵀ = 2^(Sᵀ·sc − lse2[q]) (0 where q < key or q ≥ S), dSᵀ = Pᵀ ∘ (dPᵀ − D[q]);
 // dV += Pᵀ dO and dK += dSᵀ Q accumulate in TMEM; dK is scaled by α on the way out.
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsBwd, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
@@ -568,16 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&qd_full[b]), 1);
       mbar_init(smem_u32(&qd_empty[b]), 1);
       mbar_init(smem_u32(&s_full[b]), 1);
-      mbar_init(smem_u32(&s_free[b]), 4);
+      mbar_init(smem_u32(&s_free[b]), 8);
     }
     mbar_init(smem_u32(dp_full), 1);
-    mbar_init(smem_u32(dp_free), 4);
-    mbar_init(smem_u32(p_full), 4);
+    mbar_init(smem_u32(dp_free), 8);
+    mbar_init(smem_u32(p_full), 8);
     mbar_init(smem_u32(p_free), 1);
-    mbar_init(smem_u32(ds_full), 4);
+    mbar_init(smem_u32(ds_full), 8);
     mbar_init(smem_u32(ds_free), 1);
-    mbar_init(smem_u32(&vec_full[0]), 128);
-    mbar_init(smem_u32(&vec_full[1]), 128);
+    mbar_init(smem_u32(&vec_full[0]), 256);
+    mbar_init(smem_u32(&vec_full[1]), 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -714,7 +718,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- Pᵀ / dSᵀ rows, epilogue
     const int qw = warp & 3;
-    const int rr = qw * 32 + lane;  // key row within the tile
+    const int half = (warp - 2) >> 2;  // this warp's 64 query columns: [64·half, 64·half + 64)
+    const int col0 = 64 * half;
+    const int rr = qw * 32 + lane;     // key row within the tile
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
     const uint32_t stage = sb + KvSmem::STAGE + uint32_t(qw) * 8192;
     uint32_t g = 0;
@@ -738,41 +744,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* lv = vec + b * 256;
         {
           const int q = q0 + rr;
-          lv[rr] = q < p.S ? p.lse[bh * p.S + q] * kLog2e : INFINITY;
-          lv[128 + rr] = q < p.S ? p.D[bh * p.S + q] : 0.f;
+          if (half == 0) lv[rr] = q < p.S ? p.lse[bh * p.S + q] * kLog2e : INFINITY;
+          else lv[128 + rr] = q < p.S ? p.D[bh * p.S + q] : 0.f;
         }
         mbar_arrive(smem_u32(&vec_full[b]));
         if (!warp_wait(smem_u32(&vec_full[b]), u & 1)) { ok = false; break; }
         if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t r[128];
+        uint32_t r[64];  // this warp's 64 columns of the row
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        for (int c = 0; c < 2; ++c)
+          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + col0 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
-        // Pᵀ[key rr][query c]; the diagonal tile hides queries before this key
-        const int first = (p.causal && q_first + j == it.qt) ? rr : 0;
+        // Pᵀ[key rr][query col0 + c]; the diagonal tile hides queries before this key
+        const int first = ((p.causal && q_first + j == it.qt) ? rr : 0) - col0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float e = ex2(fmaf(__uint_as_float(r[c]), p.sc, -lv[c]));
+        for (int c = 0; c < 64; ++c) {
+          const float e = ex2(fmaf(__uint_as_float(r[c]), p.sc, -lv[col0 + c]));
           r[c] = __float_as_uint(c < first ? 0.f : e);
         }
         keep_before(r);
         if (!warp_wait(smem_u32(p_free), (g & 1) ^ 1)) { ok = false; break; }
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int un = 0; un < 8; ++un) {
-            const int c0 = c * 64 + un * 8;
-            st_shared_v4(swz(sb + KvSmem::P, rr, c, un),
-                         pack_bf16(__uint_as_float(r[c0]), __uint_as_float(r[c0 + 1])),
-                         pack_bf16(__uint_as_float(r[c0 + 2]), __uint_as_float(r[c0 + 3])),
-                         pack_bf16(__uint_as_float(r[c0 + 4]), __uint_as_float(r[c0 + 5])),
-                         pack_bf16(__uint_as_float(r[c0 + 6]), __uint_as_float(r[c0 + 7])));
-          }
+        for (int un = 0; un < 8; ++un) {
+          const int c0 = un * 8;
+          st_shared_v4(swz(sb + KvSmem::P, rr, half, un),
+                       pack_bf16(__uint_as_float(r[c0]), __uint_as_float(r[c0 + 1])),
+                       pack_bf16(__uint_as_float(r[c0 + 2]), __uint_as_float(r[c0 + 3])),
+                       pack_bf16(__uint_as_float(r[c0 + 4]), __uint_as_float(r[c0 + 5])),
+                       pack_bf16(__uint_as_float(r[c0 + 6]), __uint_as_float(r[c0 + 7])));
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(p_full));
@@ -780,11 +784,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(ds_free), (g & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t d[32];
-          tmem_ld32(tDP + lane_off + uint32_t(c * 32), d);
+          tmem_ld32(tDP + lane_off + uint32_t(col0 + c * 32), d);
           tmem_ld_wait();
-          if (c == 3) {
+          if (c == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(dp_free));
@@ -795,9 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const int cc = c * 32 + un * 8 + t;
-              ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - lv[128 + cc]);
+              ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - lv[128 + col0 + cc]);
             }
-            st_shared_v4(swz(sb + KvSmem::DS, rr, c >> 1, (c & 1) * 4 + un), pack_bf16(ds[0], ds[1]),
+            st_shared_v4(swz(sb + KvSmem::DS, rr, half, c * 4 + un), pack_bf16(ds[0], ds[1]),
                          pack_bf16(ds[2], ds[3]), pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
           }
         }
@@ -809,7 +813,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) give_up();
         break;
       }
-      // ---- epilogue: dV, α·dK once the last tile's MMAs are done
+      // ---- epilogue: dV, α·dK once the last tile's MMAs are done (one warp per quadrant; the
+      // other half's next arrival on p_full comes after this, so the next item's first dV / dK
+      // MMAs cannot overwrite the accumulators before they are read)
+      if (half != 0) continue;
       if (!warp_wait(smem_u32(ds_free), (g - 1) & 1)) {
         if (lane == 0) give_up();
         break;
@@ -845,7 +852,7 @@ struct QSmem {
 // dQ for one 128-query tile per work item: thread = query row; S = Q Kᵀ and dP = dO Vᵀ per key
 // tile, P = 2^(S·sc − lse2) (0 where key > query or key ≥ S), dS = P ∘ (dP − D);
 // dQ += dS K accumulates in TMEM and is scaled by α on the way out.
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsBwd, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -879,12 +886,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&s_full[b]), 1);
-      mbar_init(smem_u32(&s_free[b]), 4);
-      mbar_init(smem_u32(&ds_full[b]), 4);
+      mbar_init(smem_u32(&s_free[b]), 8);
+      mbar_init(smem_u32(&ds_full[b]), 8);
       mbar_init(smem_u32(&ds_free[b]), 1);
     }
     mbar_init(smem_u32(dp_full), 1);
-    mbar_init(smem_u32(dp_free), 4);
+    mbar_init(smem_u32(dp_free), 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -1015,7 +1022,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- P / dS rows, epilogue
     const int qw = warp & 3;
-    const int rr = qw * 32 + lane;  // query row within the tile
+    const int half = (warp - 2) >> 2;  // this warp's 64 key columns: [64·half, 64·half + 64)
+    const int col0 = 64 * half;
+    const int rr = qw * 32 + lane;     // query row within the tile
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
     const uint32_t stage = sb + QSmem::STAGE + uint32_t(qw) * 4096;
     uint32_t g = 0;
@@ -1036,17 +1045,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t u = g >> 1;
         if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
         tc_fence_after();
-        uint32_t r[128];
+        uint32_t r[64];  // this warp's 64 columns of the row
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        for (int c = 0; c < 2; ++c)
+          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + col0 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
-        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT;
+        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT - col0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const float e = ex2(fmaf(__uint_as_float(r[c]), p.sc, -lse2));
           r[c] = __float_as_uint(c < lim ? e : 0.f);
         }
@@ -1058,11 +1067,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t dsb = sb + QSmem::DS + b * PT;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t d[32];
-          tmem_ld32(tDP + lane_off + uint32_t(c * 32), d);
+          tmem_ld32(tDP + lane_off + uint32_t(col0 + c * 32), d);
           tmem_ld_wait();
-          if (c == 3) {
+          if (c == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(dp_free));
@@ -1075,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int cc = c * 32 + un * 8 + t;
               ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - Dr);
             }
-            st_shared_v4(swz(dsb, rr, c >> 1, (c & 1) * 4 + un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
+            st_shared_v4(swz(dsb, rr, half, c * 4 + un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
                          pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
           }
         }
@@ -1087,6 +1096,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) give_up();
         break;
       }
+      // ---- epilogue: α·dQ (one warp per quadrant; the other half's next arrival on ds_full
+      // comes after this, so the next item's first dQ MMA cannot overwrite it before it is read)
+      if (half != 0) continue;
       const uint32_t pg = g - 1;
       if (!warp_wait(smem_u32(&ds_free[pg & 1]), (pg >> 1) & 1)) {
         if (lane == 0) give_up();
@@ -1241,9 +1253,9 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   static bool kv_set = false, q_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel), KvSmem::BYTES, kv_set, "xt_attention_bwd"));
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_q_kernel), QSmem::BYTES, q_set, "xt_attention_bwd"));
-  attn_bwd_kv_kernel<<<grid, attn::kThreads, KvSmem::BYTES, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  attn_bwd_kv_kernel<<<grid, kThreadsBwd, KvSmem::BYTES, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
   XT_TRY(check_launch("xt_attention_bwd (dK, dV)"));
-  attn_bwd_q_kernel<<<grid, attn::kThreads, QSmem::BYTES, s>>>(tq, tk, tv, tdo, tdq, p);
+  attn_bwd_q_kernel<<<grid, kThreadsBwd, QSmem::BYTES, s>>>(tq, tk, tv, tdo, tdq, p);
   return check_launch("xt_attention_bwd (dQ)");
 }
 
