@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         tc_commit(smem_u32(dp_full));
         return true;
       };
-      auto issue_dvdk = [&](uint32_t gg, bool first) -> bool {
+      auto issue_dv = [&](uint32_t gg, bool first) -> bool {
         if (!mbar_wait(smem_u32(p_full), gg & 1)) return false;
         tc_fence_after();
 #pragma unroll
@@ -681,6 +681,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           tc_mma<false>(tDV, smem_desc(sb + KvSmem::P + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
                         smem_desc(slot_addr(gg) + TILE + kk * 2048, TILE, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
         tc_commit(smem_u32(p_free));
+        return true;
+      };
+      auto issue_dk = [&](uint32_t gg, bool first) -> bool {
         if (!mbar_wait(smem_u32(ds_full), gg & 1)) return false;
         tc_fence_after();
 #pragma unroll
@@ -703,11 +706,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
+          // next tile's dPᵀ goes ahead of this tile's dK, so it is computed while the row warps
+          // form dSᵀ (its buffer is free once they have loaded this tile's dPᵀ)
           const uint32_t gg = g0 + uint32_t(j);
           if (*abort_flag) { ok = false; break; }
           if (j + 1 < it.nkv && !issue_s(gg + 1)) { ok = false; break; }
-          if (!issue_dvdk(gg, j == 0)) { ok = false; break; }
+          if (!issue_dv(gg, j == 0)) { ok = false; break; }
           if (j + 1 < it.nkv && !issue_dp(gg + 1)) { ok = false; break; }
+          if (!issue_dk(gg, j == 0)) { ok = false; break; }
         }
         if (!ok) break;
         tc_commit(smem_u32(kv_empty));
@@ -732,21 +738,24 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
       const int q_first = p.causal ? it.qt : 0;
       const int64_t bh = int64_t(it.b) * p.H + it.h;
+      // this thread's entry of a query tile's lse·log2 e (half 0) or D (half 1), read one tile ahead
+      auto vec_entry = [&](int jj) -> float {
+        const int q = (q_first + jj) * BT + rr;
+        if (half == 0) return q < p.S ? p.lse[bh * p.S + q] * kLog2e : INFINITY;
+        return q < p.S ? p.D[bh * p.S + q] : 0.f;
+      };
+      float vnext = vec_entry(0);
       bool ok = true;
       #pragma unroll 1
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int b = int(g & 1);
         const uint32_t u = g >> 1;
-        const int q0 = (q_first + j) * BT;
-        // this query tile's lse·log2 e and D, shared by the four warps through slot g & 1 (a
+        // this query tile's lse·log2 e and D, shared by the row warps through slot g & 1 (a
         // thread refills a slot only after every thread has arrived for the tile in between,
         // i.e. has finished reading it)
         float* lv = vec + b * 256;
-        {
-          const int q = q0 + rr;
-          if (half == 0) lv[rr] = q < p.S ? p.lse[bh * p.S + q] * kLog2e : INFINITY;
-          else lv[128 + rr] = q < p.S ? p.D[bh * p.S + q] : 0.f;
-        }
+        lv[half * 128 + rr] = vnext;
+        if (j + 1 < it.nkv) vnext = vec_entry(j + 1);
         mbar_arrive(smem_u32(&vec_full[b]));
         if (!warp_wait(smem_u32(&vec_full[b]), u & 1)) { ok = false; break; }
         if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
@@ -783,27 +792,23 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         // dSᵀ = Pᵀ ∘ (dPᵀ − D), 32 query columns at a time
         if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(ds_free), (g & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
+        uint32_t d[64];  // both dPᵀ chunks in flight before one wait
+        tmem_ld32(tDP + lane_off + uint32_t(col0), *reinterpret_cast<uint32_t(*)[32]>(d));
+        tmem_ld32(tDP + lane_off + uint32_t(col0 + 32), *reinterpret_cast<uint32_t(*)[32]>(d + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(dp_free));
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t d[32];
-          tmem_ld32(tDP + lane_off + uint32_t(col0 + c * 32), d);
-          tmem_ld_wait();
-          if (c == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(dp_free));
+        for (int un = 0; un < 8; ++un) {
+          float ds[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int cc = un * 8 + t;
+            ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[cc]) - lv[128 + col0 + cc]);
           }
-#pragma unroll
-          for (int un = 0; un < 4; ++un) {
-            float ds[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int cc = c * 32 + un * 8 + t;
-              ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - lv[128 + col0 + cc]);
-            }
-            st_shared_v4(swz(sb + KvSmem::DS, rr, half, c * 4 + un), pack_bf16(ds[0], ds[1]),
-                         pack_bf16(ds[2], ds[3]), pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
-          }
+          st_shared_v4(swz(sb + KvSmem::DS, rr, half, un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
+                       pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -1007,11 +1012,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
+          // next tile's dP goes ahead of this tile's dQ (see the key-tile kernel)
           const uint32_t gg = g0 + uint32_t(j);
           if (*abort_flag) { ok = false; break; }
           if (j + 1 < it.nkv && !issue_s(gg + 1)) { ok = false; break; }
-          if (!issue_dq(gg, j == 0)) { ok = false; break; }
           if (j + 1 < it.nkv && !issue_dp(gg + 1)) { ok = false; break; }
+          if (!issue_dq(gg, j == 0)) { ok = false; break; }
         }
         if (!ok) break;
         tc_commit(smem_u32(q_empty));
@@ -1066,27 +1072,23 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
         tc_fence_after();
         const uint32_t dsb = sb + QSmem::DS + b * PT;
+        uint32_t d[64];  // both dP chunks in flight before one wait
+        tmem_ld32(tDP + lane_off + uint32_t(col0), *reinterpret_cast<uint32_t(*)[32]>(d));
+        tmem_ld32(tDP + lane_off + uint32_t(col0 + 32), *reinterpret_cast<uint32_t(*)[32]>(d + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(dp_free));
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t d[32];
-          tmem_ld32(tDP + lane_off + uint32_t(col0 + c * 32), d);
-          tmem_ld_wait();
-          if (c == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(dp_free));
+        for (int un = 0; un < 8; ++un) {
+          float ds[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int cc = un * 8 + t;
+            ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[cc]) - Dr);
           }
-#pragma unroll
-          for (int un = 0; un < 4; ++un) {
-            float ds[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int cc = c * 32 + un * 8 + t;
-              ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[un * 8 + t]) - Dr);
-            }
-            st_shared_v4(swz(dsb, rr, half, c * 4 + un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
-                         pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
-          }
+          st_shared_v4(swz(dsb, rr, half, un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
+                       pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
         }
         fence_proxy_async_smem();
         __syncwarp();
