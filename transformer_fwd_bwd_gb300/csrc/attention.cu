@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const __grid_constant__ CUtensorMap tmOlo, const FwdParams p) {
+  pdl_begin();
   constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_PV = instr_desc_bf16(128, HD, false, true);
   constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), O [256,320)
@@ -450,6 +451,7 @@ struct BwdParams {
 __global__ void attn_delta_kernel(const bf16* __restrict__ o, const bf16* __restrict__ o_lo,
                                   const bf16* __restrict__ dO, int64_t ld_o, int B, int S, int H,
                                   float* __restrict__ D) {
+  pdl_begin();
   const int64_t n = int64_t(B) * S * H;
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -540,6 +542,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const BwdParams p) {
+  pdl_begin();
   constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_O = instr_desc_bf16(128, HD, false, true);
   constexpr uint32_t TCOLS = 512;  // Sᵀ0 [0,128), Sᵀ1 [128,256), dPᵀ [256,384), dV [384,448), dK [448,512)
@@ -861,6 +864,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+  pdl_begin();
   constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_O = instr_desc_bf16(128, HD, false, true);
   constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), dP [256,384), dQ [384,448)
@@ -1198,7 +1202,7 @@ int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   static bool smem_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_fwd_kernel), FwdSmem::BYTES, smem_set, "xt_attention_fwd"));
   const int grid = p.items < num_sms() ? p.items : num_sms();
-  attn_fwd_kernel<<<grid, attn::kThreads, FwdSmem::BYTES, as_stream(stream)>>>(tq, tk, tv, to, tolo, p);
+  launch(attn_fwd_kernel, grid, attn::kThreads, FwdSmem::BYTES, as_stream(stream), tq, tk, tv, to, tolo, p);
   return check_launch("xt_attention_fwd");
 }
 
@@ -1227,7 +1231,7 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
     const int64_t cap = int64_t(num_sms()) * 8;
     if (blocks > cap) blocks = cap;
     if (o_lo && !aligned16(o_lo)) return fail(XT_ERR_ALIGNMENT, "xt_attention_bwd: o_lo must be 16-byte aligned");
-    attn_delta_kernel<<<int(blocks), 256, 0, s>>>(static_cast<const bf16*>(o), static_cast<const bf16*>(o_lo),
+    launch(attn_delta_kernel, int(blocks), 256, 0, s, static_cast<const bf16*>(o), static_cast<const bf16*>(o_lo),
                                                    static_cast<const bf16*>(d_o), ld_o, B, S, H, D);
     XT_TRY(check_launch("xt_attention_bwd (delta)"));
   }
@@ -1255,9 +1259,9 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   static bool kv_set = false, q_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel), KvSmem::BYTES, kv_set, "xt_attention_bwd"));
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_q_kernel), QSmem::BYTES, q_set, "xt_attention_bwd"));
-  attn_bwd_kv_kernel<<<grid, kThreadsBwd, KvSmem::BYTES, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  launch(attn_bwd_kv_kernel, grid, kThreadsBwd, KvSmem::BYTES, s, tq, tk, tv, tdo, tdk, tdv, p);
   XT_TRY(check_launch("xt_attention_bwd (dK, dV)"));
-  attn_bwd_q_kernel<<<grid, kThreadsBwd, QSmem::BYTES, s>>>(tq, tk, tv, tdo, tdq, p);
+  launch(attn_bwd_q_kernel, grid, kThreadsBwd, QSmem::BYTES, s, tq, tk, tv, tdo, tdq, p);
   return check_launch("xt_attention_bwd (dQ)");
 }
 

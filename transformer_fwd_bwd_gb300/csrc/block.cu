@@ -280,7 +280,8 @@ int check_params(const xt_block_config& c, const xt_block_params* p, bool grads)
   return XT_OK;
 }
 
-__global__ void set_scalar(float* p, float v) { *p = v; }
+__global__ void set_scalar(float* p, float v) {
+  pdl_begin(); *p = v; }
 
 uint64_t site_seed(const xt_block_config& c, int64_t l, uint64_t site) { return c.base_seed ^ uint64_t(l) ^ site; }
 
@@ -376,7 +377,7 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   const int64_t T = m.T, d = m.d, e = m.e;
   const bool drop = c.training && c.p > 0.f;
   // loss → logits (in place: dlogits overwrite the logits) → tied embedding and final norm
-  set_scalar<<<1, 1, 0, s>>>(b.one, 1.f);
+  launch(set_scalar, 1, 1, 0, s, b.one, 1.f);
   XT_TRY(check_launch("xt_block_bwd"));
   XT_TRY(xt_cross_entropy_bwd(b.logits, targets, b.lse, b.one, b.logits, T, m.V, m.dt, m.dt, 0, stream));
   XT_TRY(matmul(logits_de(m), b.logits, b.hf, prm->dE, b.ws_mm, b.ws_mm_bytes, s));

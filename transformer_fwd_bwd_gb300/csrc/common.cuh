@@ -7,6 +7,7 @@
 
 #include <cstdarg>
 #include <cstdint>
+#include <utility>
 #include <cstdio>
 
 #include "../../include/xt.h"
@@ -37,6 +38,22 @@ void gemm_profile_end(cudaStream_t s, void* token);
     int _st = (expr);             \
     if (_st != XT_OK) return _st; \
   } while (0)
+
+// Launches `kernel` on `s` with programmatic stream serialization allowed (see pdl_begin).
+template <typename... KArgs, typename... Args>
+inline void launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline bool valid_dtype(int dt) { return dt == XT_F32 || dt == XT_BF16; }
 inline size_t dtype_size(int dt) { return dt == XT_BF16 ? 2 : 4; }
@@ -244,6 +261,16 @@ __device__ __forceinline__ void gelu_batch(const float (&x)[N], float (&out)[N])
       out[i] = fmaf(x[i], 0.39894228040143268f * e, cdf);
     }
   }
+}
+
+// Programmatic dependent launch.  Every kernel is launched with programmatic stream
+// serialization (launch() below), so it can be resident while its predecessor on the stream
+// drains; pdl_begin() is each kernel's first statement: it waits until the predecessor has
+// completed and its writes are visible (immediate when there is none), then lets the successor
+// be scheduled.  Nothing a kernel does precedes the wait.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void flag_error(uint32_t* flag, uint32_t bit) {

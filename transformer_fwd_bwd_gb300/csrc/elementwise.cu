@@ -96,6 +96,7 @@ template <EwOp OP> struct EwIO {
 
 template <EwOp OP, typename TI, typename TO, bool VEC>
 __global__ void __launch_bounds__(256) ew_kernel(EwArgs g) {
+  pdl_begin();
   using IO = EwIO<OP>;
   const TI* a = static_cast<const TI*>(g.a);
   const TI* b = static_cast<const TI*>(g.b);
@@ -168,9 +169,9 @@ static int ew_run(const EwArgs& g, cudaStream_t s, const char* name) {
   const bool vec = aligned16(g.a) && aligned16(g.b) && aligned16(g.c) && aligned16(g.o0) &&
                    aligned16(g.o1);
   if (vec)
-    ew_kernel<OP, TI, TO, true><<<grid_for(g.n / 8 + 1), 256, 0, s>>>(g);
+    launch(ew_kernel<OP, TI, TO, true>, grid_for(g.n / 8 + 1), 256, 0, s, g);
   else
-    ew_kernel<OP, TI, TO, false><<<grid_for(g.n), 256, 0, s>>>(g);
+    launch(ew_kernel<OP, TI, TO, false>, grid_for(g.n), 256, 0, s, g);
   return check_launch(name);
 }
 
@@ -202,6 +203,7 @@ static int sum_blocks(int64_t n) {
 
 template <typename T>
 __global__ void __launch_bounds__(kSumThreads) sum_stage1(const T* x, int64_t n, float* part) {
+  pdl_begin();
   __shared__ float red[kSumThreads / 32];
   float acc = 0.f;
   for (int64_t i = int64_t(blockIdx.x) * kSumThreads + threadIdx.x; i < n;
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(kSumThreads) sum_stage1(const T* x, int64_t n,
 }
 
 __global__ void sum_stage2(const float* part, int nb, float* out) {
+  pdl_begin();
   __shared__ float red[32];
   float acc = 0.f;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) acc += part[i];
@@ -237,6 +240,7 @@ __global__ void sum_stage2(const float* part, int nb, float* out) {
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const T* g, const T* u, int64_t ld_in, T* y,
                                                          int64_t ld_out, int64_t rows, int64_t cols) {
+  pdl_begin();
   const int64_t W = VEC ? 8 : 1;
   const int64_t per_row = cols / W;
   const int64_t total = rows * per_row;
@@ -263,6 +267,7 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const T* d, int64_t ld_d, const T* g, const T* u,
                                                          int64_t ld_in, T* dg, T* du, int64_t ld_grad,
                                                          int64_t rows, int64_t cols, int acc) {
+  pdl_begin();
   const int64_t W = VEC ? 8 : 1;
   const int64_t per_row = cols / W;
   const int64_t total = rows * per_row;
@@ -308,6 +313,7 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const T* d, int64_t ld_
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(256) add_bias_kernel(const T* x, const T* bias, T* y, int64_t rows,
                                                        int64_t cols) {
+  pdl_begin();
   const int64_t W = VEC ? 8 : 1;
   const int64_t per_row = cols / W;
   const int64_t total = rows * per_row;
@@ -424,11 +430,11 @@ int xt_sum_fwd(const void* x, int64_t n, int dt, float* out, void* ws, void* str
   const int nb = sum_blocks(n);
   float* part = static_cast<float*>(ws);
   if (dt == XT_F32)
-    sum_stage1<float><<<nb, kSumThreads, 0, s>>>(static_cast<const float*>(x), n, part);
+    launch(sum_stage1<float>, nb, kSumThreads, 0, s, static_cast<const float*>(x), n, part);
   else
-    sum_stage1<bf16><<<nb, kSumThreads, 0, s>>>(static_cast<const bf16*>(x), n, part);
+    launch(sum_stage1<bf16>, nb, kSumThreads, 0, s, static_cast<const bf16*>(x), n, part);
   XT_TRY(check_launch("xt_sum_fwd"));
-  sum_stage2<<<1, 1024, 0, s>>>(part, nb, out);
+  launch(sum_stage2, 1, 1024, 0, s, part, nb, out);
   return check_launch("xt_sum_fwd");
 }
 
@@ -547,6 +553,7 @@ int xt_dropout_add_fwd(const void* h, const void* a, void* out, int64_t n, float
 
 namespace xt {
 __global__ void dropout_mask_kernel(uint8_t* mask, int64_t n, float p, uint64_t seed) {
+  pdl_begin();
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
     mask[i] = dropout_keep(seed, uint64_t(i), p) ? 1 : 0;
 }
@@ -559,7 +566,7 @@ int xt_dropout_mask(uint8_t* mask, int64_t n, float p, uint64_t seed, void* stre
   XT_TRY(check_dropout(p));
   XT_REQUIRE(n == 0 || mask, "xt_dropout_mask: NULL pointer");
   if (n == 0) return XT_OK;
-  dropout_mask_kernel<<<grid_for(n), 256, 0, as_stream(stream)>>>(mask, n, p, seed);
+  launch(dropout_mask_kernel, grid_for(n), 256, 0, as_stream(stream), mask, n, p, seed);
   return check_launch("xt_dropout_mask");
 }
 
@@ -576,12 +583,12 @@ int xt_swiglu_fwd(const void* g, const void* u, int64_t ld_in, void* y, int64_t 
   const int grid = grid_for(rows * cols / (vec ? 8 : 1));
   if (dt == XT_F32) {
     auto G = static_cast<const float*>(g); auto U = static_cast<const float*>(u); auto Y = static_cast<float*>(y);
-    if (vec) swiglu_fwd_kernel<float, true><<<grid, 256, 0, s>>>(G, U, ld_in, Y, ld_out, rows, cols);
-    else swiglu_fwd_kernel<float, false><<<grid, 256, 0, s>>>(G, U, ld_in, Y, ld_out, rows, cols);
+    if (vec) launch(swiglu_fwd_kernel<float, true>, grid, 256, 0, s, G, U, ld_in, Y, ld_out, rows, cols);
+    else launch(swiglu_fwd_kernel<float, false>, grid, 256, 0, s, G, U, ld_in, Y, ld_out, rows, cols);
   } else {
     auto G = static_cast<const bf16*>(g); auto U = static_cast<const bf16*>(u); auto Y = static_cast<bf16*>(y);
-    if (vec) swiglu_fwd_kernel<bf16, true><<<grid, 256, 0, s>>>(G, U, ld_in, Y, ld_out, rows, cols);
-    else swiglu_fwd_kernel<bf16, false><<<grid, 256, 0, s>>>(G, U, ld_in, Y, ld_out, rows, cols);
+    if (vec) launch(swiglu_fwd_kernel<bf16, true>, grid, 256, 0, s, G, U, ld_in, Y, ld_out, rows, cols);
+    else launch(swiglu_fwd_kernel<bf16, false>, grid, 256, 0, s, G, U, ld_in, Y, ld_out, rows, cols);
   }
   return check_launch("xt_swiglu_fwd");
 }
@@ -603,14 +610,14 @@ int xt_swiglu_bwd(const void* d, int64_t ld_d, const void* g, const void* u, int
     auto D = static_cast<const float*>(d); auto G = static_cast<const float*>(g);
     auto U = static_cast<const float*>(u);
     auto DG = static_cast<float*>(dg); auto DU = static_cast<float*>(du);
-    if (vec) swiglu_bwd_kernel<float, true><<<grid, 256, 0, s>>>(D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
-    else swiglu_bwd_kernel<float, false><<<grid, 256, 0, s>>>(D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
+    if (vec) launch(swiglu_bwd_kernel<float, true>, grid, 256, 0, s, D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
+    else launch(swiglu_bwd_kernel<float, false>, grid, 256, 0, s, D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
   } else {
     auto D = static_cast<const bf16*>(d); auto G = static_cast<const bf16*>(g);
     auto U = static_cast<const bf16*>(u);
     auto DG = static_cast<bf16*>(dg); auto DU = static_cast<bf16*>(du);
-    if (vec) swiglu_bwd_kernel<bf16, true><<<grid, 256, 0, s>>>(D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
-    else swiglu_bwd_kernel<bf16, false><<<grid, 256, 0, s>>>(D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
+    if (vec) launch(swiglu_bwd_kernel<bf16, true>, grid, 256, 0, s, D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
+    else launch(swiglu_bwd_kernel<bf16, false>, grid, 256, 0, s, D, ld_d, G, U, ld_in, DG, DU, ld_grad, rows, cols, acc);
   }
   return check_launch("xt_swiglu_bwd");
 }
@@ -626,12 +633,12 @@ int xt_add_bias_fwd(const void* x, const void* bias, void* y, int64_t rows, int6
   const int grid = grid_for(rows * cols / (vec ? 8 : 1));
   if (dt == XT_F32) {
     auto X = static_cast<const float*>(x); auto Bb = static_cast<const float*>(bias); auto Y = static_cast<float*>(y);
-    if (vec) add_bias_kernel<float, true><<<grid, 256, 0, s>>>(X, Bb, Y, rows, cols);
-    else add_bias_kernel<float, false><<<grid, 256, 0, s>>>(X, Bb, Y, rows, cols);
+    if (vec) launch(add_bias_kernel<float, true>, grid, 256, 0, s, X, Bb, Y, rows, cols);
+    else launch(add_bias_kernel<float, false>, grid, 256, 0, s, X, Bb, Y, rows, cols);
   } else {
     auto X = static_cast<const bf16*>(x); auto Bb = static_cast<const bf16*>(bias); auto Y = static_cast<bf16*>(y);
-    if (vec) add_bias_kernel<bf16, true><<<grid, 256, 0, s>>>(X, Bb, Y, rows, cols);
-    else add_bias_kernel<bf16, false><<<grid, 256, 0, s>>>(X, Bb, Y, rows, cols);
+    if (vec) launch(add_bias_kernel<bf16, true>, grid, 256, 0, s, X, Bb, Y, rows, cols);
+    else launch(add_bias_kernel<bf16, false>, grid, 256, 0, s, X, Bb, Y, rows, cols);
   }
   return check_launch("xt_add_bias_fwd");
 }

@@ -110,6 +110,7 @@ size_t split_bytes(const Choice& c, int64_t M, int64_t N) {
 template <typename TC>
 __global__ void splitk_reduce(const float* __restrict__ part, int splits, int64_t M, int64_t N, TC* C, int64_t ldc,
                               int acc) {
+  pdl_begin();
   const int64_t n4 = N / 4, total = M * n4, slice = M * N;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     const int64_t m = i / n4, c = (i - m * n4) * 4;
@@ -217,10 +218,10 @@ int run(const Problem& pb, cudaStream_t s) {
     if (g > int64_t(num_sms()) * 8) g = int64_t(num_sms()) * 8;
     const float* part = static_cast<const float*>(pb.split_ws);
     if (pb.c_bf16)
-      splitk_reduce<bf16><<<int(g), 256, 0, s>>>(part, ch.splits, pb.M, pb.N, static_cast<bf16*>(pb.C), pb.ldc,
+      launch(splitk_reduce<bf16>, int(g), 256, 0, s, part, ch.splits, pb.M, pb.N, static_cast<bf16*>(pb.C), pb.ldc,
                                                  pb.accumulate);
     else
-      splitk_reduce<float><<<int(g), 256, 0, s>>>(part, ch.splits, pb.M, pb.N, static_cast<float*>(pb.C), pb.ldc,
+      launch(splitk_reduce<float>, int(g), 256, 0, s, part, ch.splits, pb.M, pb.N, static_cast<float*>(pb.C), pb.ldc,
                                                   pb.accumulate);
     st = check_launch("gemm K-split reduce");
   }
@@ -245,6 +246,7 @@ static size_t stage_bytes(const gemm::Operand& o) {
 
 __global__ void transpose_to_kmajor(const float* __restrict__ src, int64_t ld, int64_t s_inner, int64_t s_outer,
                                     int bi, int64_t mn, int64_t K, float* __restrict__ dst, int64_t ldk) {
+  pdl_begin();
   __shared__ float tile[32][33];
   const int z = blockIdx.z;
   const int zo = z / bi, zi = z - zo * bi;
@@ -270,7 +272,7 @@ static int stage_operand(gemm::Operand& o, char*& ws, size_t& left, cudaStream_t
   const int batches = o.batch_inner * o.batch_outer;
   if (batches > 65535) return fail(XT_ERR_UNSUPPORTED, "matmul: too many batches for tf32 staging");
   dim3 grid(unsigned(ceil_div(o.mn, 32)), unsigned(ceil_div(ldk, 32)), unsigned(batches));
-  transpose_to_kmajor<<<grid, dim3(32, 8), 0, s>>>(static_cast<const float*>(o.ptr), o.ld, o.s_inner, o.s_outer,
+  launch(transpose_to_kmajor, grid, dim3(32, 8), 0, s, static_cast<const float*>(o.ptr), o.ld, o.s_inner, o.s_outer,
                                                     o.batch_inner, o.mn, o.K, reinterpret_cast<float*>(ws), ldk);
   XT_TRY(check_launch("matmul tf32 staging"));
   o.ptr = ws;

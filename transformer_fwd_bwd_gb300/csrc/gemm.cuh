@@ -69,7 +69,7 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
       return check_launch("gemm: shared memory attribute");
     attr_set = true;
   }
-  k<<<grid, kThreads, smem, s>>>(ta, tb, tc, tc2, p);
+  launch(k, grid, kThreads, smem, s, ta, tb, tc, tc2, p);
   return check_launch("gemm kernel");
 }
 

@@ -280,6 +280,7 @@ template <bool TF32, int BN, bool A_MN, bool B_MN, int ACT = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, const Params p) {
+  pdl_begin();
   using C_ = Cfg<TF32, BN>;
   constexpr int BK = C_::BK, ATOM = C_::ATOM, UK = C_::UK, STAGES = C_::STAGES;
   constexpr uint32_t IDESC = instr_desc<TF32, BN, A_MN, B_MN>();

@@ -130,6 +130,7 @@ template <typename T, int VW>
 __global__ void __launch_bounds__(1024) rms_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
                                                       T* __restrict__ y, float* __restrict__ inv_rms,
                                                       int64_t rows, int64_t cols, float eps, int tpr) {
+  pdl_begin();
   __shared__ float red[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
   const int64_t nvec = cols / VW;
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) rms_bwd_kernel(cons
                                                       const T* __restrict__ gamma, const float* __restrict__ inv_rms,
                                                       TD* dx, float* __restrict__ part, int64_t rows, int64_t cols,
                                                       int tpr, int acc_dx) {
+  pdl_begin();
   extern __shared__ float smem[];
   float* red = smem;  // 32
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
                                                      const T* __restrict__ beta, T* __restrict__ y,
                                                      float* __restrict__ mean_out, float* __restrict__ rstd_out,
                                                      int64_t rows, int64_t cols, float eps, int tpr) {
+  pdl_begin();
   __shared__ float red[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
   const int64_t nvec = cols / VW;
@@ -334,6 +337,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
                                                      const float* __restrict__ rstd, TD* dx, float* __restrict__ part_g,
                                                      float* __restrict__ part_b, int64_t rows, int64_t cols,
                                                      int tpr, int acc_dx) {
+  pdl_begin();
   extern __shared__ float smem[];
   float* red = smem;
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr, grp = threadIdx.x / tpr;
@@ -430,6 +434,7 @@ struct ColsumJob {
 };
 template <typename TO>
 __global__ void __launch_bounds__(1024) colsum_finalize(ColsumJob j0, ColsumJob j1, int nb, int64_t cols, int acc) {
+  pdl_begin();
   __shared__ float red[32][33];
   const ColsumJob jb = blockIdx.y ? j1 : j0;
   const float* part = jb.part;
@@ -467,8 +472,8 @@ static int finalize(const float* part, int nb, int64_t cols, void* out, int dt, 
   const dim3 grid(unsigned(ceil_div(cols, 32)), out1 ? 2u : 1u);
   const dim3 block(32, 32);
   const ColsumJob j0{part, out}, j1{part1, out1};
-  if (dt == XT_F32) colsum_finalize<float><<<grid, block, 0, s>>>(j0, j1, nb, cols, acc);
-  else colsum_finalize<bf16><<<grid, block, 0, s>>>(j0, j1, nb, cols, acc);
+  if (dt == XT_F32) launch(colsum_finalize<float>, grid, block, 0, s, j0, j1, nb, cols, acc);
+  else launch(colsum_finalize<bf16>, grid, block, 0, s, j0, j1, nb, cols, acc);
   return check_launch("column-sum finalize");
 }
 
@@ -480,6 +485,7 @@ static int colsum_chunks(int64_t rows) { return int(ceil_div(rows, kColChunkRows
 template <typename T>
 __global__ void colsum_stage1(const T* __restrict__ d, T* dx, int acc_dx, float* __restrict__ part, int64_t rows,
                               int64_t cols) {
+  pdl_begin();
   const int64_t chunk = blockIdx.y;
   const int64_t r_begin = chunk * kColChunkRows;
   const int64_t r_end = r_begin + kColChunkRows < rows ? r_begin + kColChunkRows : rows;
@@ -516,6 +522,7 @@ __device__ __forceinline__ int causal_ext(int causal, int q, int cols) {
 template <typename T, int VW>
 __global__ void __launch_bounds__(1024) softmax_fwd_kernel(const T* __restrict__ x, T* __restrict__ y, int64_t rows,
                                                           int cols, int causal, int64_t q_len, int tpr) {
+  pdl_begin();
   __shared__ float red[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
   const bool small = rows <= INT32_MAX && q_len <= INT32_MAX;
@@ -584,6 +591,7 @@ template <typename T, int VW, int MAXT>
 __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) softmax_bwd_kernel(
     const T* __restrict__ d, const T* __restrict__ y, T* dx, int64_t rows, int cols, int causal, int64_t q_len,
     int tpr, int acc) {
+  pdl_begin();
   __shared__ float red[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
   const bool small = rows <= INT32_MAX && q_len <= INT32_MAX;
@@ -641,6 +649,7 @@ template <typename T, int VW>
 __global__ void __launch_bounds__(1024) ce_fwd_kernel(const T* __restrict__ x, const int32_t* __restrict__ tgt,
                                                      float* __restrict__ lse, float* __restrict__ nll, int64_t rows,
                                                      int64_t V, int tpr, uint32_t* flag) {
+  pdl_begin();
   __shared__ float red_m[32], red_s[32];
   const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
   const int64_t nvec = V / VW;
@@ -710,6 +719,7 @@ __global__ void __launch_bounds__(1024) ce_fwd_kernel(const T* __restrict__ x, c
 
 // loss = Σ nll / rows in a fixed order (one block).
 __global__ void ce_loss_kernel(const float* __restrict__ nll, int64_t rows, float* loss) {
+  pdl_begin();
   __shared__ float red[32];
   float acc = 0.f;
   for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) acc += nll[i];
@@ -729,6 +739,7 @@ template <typename T, typename TG, int VW>
 __global__ void __launch_bounds__(256) ce_bwd_kernel(const T* x, const int32_t* __restrict__ tgt,
                                                     const float* __restrict__ lse, const float* __restrict__ upstream,
                                                     TG* dx, int64_t rows, int64_t V, int acc, uint32_t* flag) {
+  pdl_begin();
   const float sc = *upstream / float(rows);
   const int64_t nvec = V / VW;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -761,6 +772,7 @@ __global__ void __launch_bounds__(256) ce_bwd_kernel(const T* x, const int32_t* 
 // ============================================================================== RoPE
 
 __global__ void rope_table_kernel(float* table, int S, int hd, double base, int pos_offset) {
+  pdl_begin();
   const int h = hd / 2;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < S * h; idx += gridDim.x * blockDim.x) {
     const int s = idx / h, i = idx - s * h;
@@ -777,6 +789,7 @@ __global__ void rope_table_kernel(float* table, int S, int hd, double base, int 
 template <typename T, bool BWD, int VW>
 __global__ void __launch_bounds__(256) rope_kernel(const T* x, T* y, const float* __restrict__ table, int B, int S,
                                                   int H, int hd, int64_t ld, int acc) {
+  pdl_begin();
   const int h = hd / 2;
   const int per_head = h / VW;
   const int64_t total = int64_t(B) * S * H * per_head;
@@ -825,6 +838,7 @@ template <typename T, int VW>
 __global__ void __launch_bounds__(256) embed_fwd_kernel(const int32_t* __restrict__ ids, const T* __restrict__ E,
                                                        const T* __restrict__ P, T* __restrict__ h, int64_t T_,
                                                        int S, int64_t d, int64_t V, uint32_t* flag) {
+  pdl_begin();
   const int64_t per = d / VW;
   const int64_t total = T_ * per;
   for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
@@ -854,6 +868,7 @@ constexpr int kSortMax = 16384;
 // [0, V) get the key (V << 32 | t) so they sort last and are skipped.
 __global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restrict__ ids, int64_t T_, int64_t V,
                                                          uint64_t* __restrict__ sorted, uint32_t* flag) {
+  pdl_begin();
   extern __shared__ uint64_t keys[];
   int n = 1;
   while (n < T_) n <<= 1;
@@ -889,6 +904,7 @@ __global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restr
 template <typename TH, typename TG>
 __global__ void __launch_bounds__(256) embed_scatter_kernel(const uint64_t* __restrict__ sorted, const TH* __restrict__ dh,
                                                            TG* dE, int64_t T_, int64_t d, int64_t V) {
+  pdl_begin();
   const int64_t i = blockIdx.x;
   const uint64_t key = sorted[i];
   const int64_t id = int64_t(key >> 32);
@@ -908,6 +924,7 @@ __global__ void __launch_bounds__(256) embed_scatter_kernel(const uint64_t* __re
 template <typename TH, typename TG>
 __global__ void __launch_bounds__(256) embed_pos_kernel(const TH* __restrict__ dh, TG* dP, int64_t T_, int S, int64_t d,
                                                        int acc) {
+  pdl_begin();
   const int64_t nb = T_ / S;
   for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < int64_t(S) * d; v += int64_t(gridDim.x) * blockDim.x) {
     const int64_t s = v / d, c = v - s * d;
@@ -988,7 +1005,7 @@ int xt_rms_norm_fwd(const void* x, const void* gamma, void* y, float* inv_rms, i
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_rms_norm_fwd: row too long (%lld)", (long long)cols);
   cudaStream_t s = as_stream(stream);
   const int grid = row_grid(rows, pl.rpb);
-  XT_ROW_DISPATCH(dt, vec, (rms_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+  XT_ROW_DISPATCH(dt, vec, (launch(rms_fwd_kernel<T, VW>, grid, pl.threads, 0, s, 
                                static_cast<const T*>(x), static_cast<const T*>(gamma), static_cast<T*>(y), inv_rms,
                                rows, cols, eps, pl.tpr)));
   return check_launch("xt_rms_norm_fwd");
@@ -1019,7 +1036,7 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
     auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
+    launch(k, nb, pl.threads, smem, s, static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
                                    inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_rms_norm_bwd"));
@@ -1090,7 +1107,7 @@ int xt_rms_norm_bwd_noalloc(const void* d, const void* x, const void* gamma, con
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
     auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
+    launch(k, nb, pl.threads, smem, s, static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
                                    inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_rms_norm_bwd_noalloc"));
@@ -1109,7 +1126,7 @@ int xt_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_fwd: row too long");
   cudaStream_t s = as_stream(stream);
   const int grid = row_grid(rows, pl.rpb);
-  XT_ROW_DISPATCH(dt, vec, (ln_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+  XT_ROW_DISPATCH(dt, vec, (launch(ln_fwd_kernel<T, VW>, grid, pl.threads, 0, s, 
                                static_cast<const T*>(x), static_cast<const T*>(gamma), static_cast<const T*>(beta),
                                static_cast<T*>(y), mean, rstd, rows, cols, eps, pl.tpr)));
   return check_launch("xt_layernorm_fwd");
@@ -1153,7 +1170,7 @@ int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const floa
       default: k = narrow ? ln_bwd_kernel<T, TD, VW, 4, 256> : ln_bwd_kernel<T, TD, VW, 4, 512>; break;
     }
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    k<<<nb, pl.threads, smem, s>>>(static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
+    launch(k, nb, pl.threads, smem, s, static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
                                    mean, rstd, static_cast<TD*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx);
   });
   XT_TRY(check_launch("xt_layernorm_bwd"));
@@ -1186,9 +1203,9 @@ int xt_add_bias_bwd(const void* d, void* dx, void* dbias, int64_t rows, int64_t 
   dim3 grid(unsigned(ceil_div(cols, 256) < 65535 ? ceil_div(cols, 256) : 65535), unsigned(nch));
   if (nch > 65535) return fail(XT_ERR_UNSUPPORTED, "xt_add_bias_bwd: too many rows");
   if (dt == XT_F32)
-    colsum_stage1<float><<<grid, 256, 0, s>>>(static_cast<const float*>(d), static_cast<float*>(dx), acc_dx, part, rows, cols);
+    launch(colsum_stage1<float>, grid, 256, 0, s, static_cast<const float*>(d), static_cast<float*>(dx), acc_dx, part, rows, cols);
   else
-    colsum_stage1<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(d), static_cast<bf16*>(dx), acc_dx, part, rows, cols);
+    launch(colsum_stage1<bf16>, grid, 256, 0, s, static_cast<const bf16*>(d), static_cast<bf16*>(dx), acc_dx, part, rows, cols);
   XT_TRY(check_launch("xt_add_bias_bwd"));
   return finalize(part, nch, cols, dbias, dt_bias, acc_dbias, s);
 }
@@ -1205,7 +1222,7 @@ int xt_softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int causa
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_softmax_fwd: row too long");
   cudaStream_t s = as_stream(stream);
   const int grid = row_grid(rows, pl.rpb);
-  XT_ROW_DISPATCH(dt, vec, (softmax_fwd_kernel<T, VW><<<grid, pl.threads, 0, s>>>(
+  XT_ROW_DISPATCH(dt, vec, (launch(softmax_fwd_kernel<T, VW>, grid, pl.threads, 0, s, 
                                static_cast<const T*>(x), static_cast<T*>(y), rows, int(cols), causal, q_len, pl.tpr)));
   return check_launch("xt_softmax_fwd");
 }
@@ -1223,10 +1240,9 @@ int xt_softmax_bwd(const void* d, const void* y, void* dx, int64_t rows, int64_t
   cudaStream_t s = as_stream(stream);
   const int grid = row_grid(rows, pl.rpb);
   const bool narrow = pl.threads <= 256;
-  XT_ROW_DISPATCH(dt, vec, ((narrow ? softmax_bwd_kernel<T, VW, 256> : softmax_bwd_kernel<T, VW, 1024>)
-                            <<<grid, pl.threads, 0, s>>>(static_cast<const T*>(d), static_cast<const T*>(y),
-                                                         static_cast<T*>(dx), rows, int(cols), causal, q_len,
-                                                         pl.tpr, acc)));
+  XT_ROW_DISPATCH(dt, vec, (launch(narrow ? softmax_bwd_kernel<T, VW, 256> : softmax_bwd_kernel<T, VW, 1024>, grid,
+                                   pl.threads, 0, s, static_cast<const T*>(d), static_cast<const T*>(y),
+                                   static_cast<T*>(dx), rows, int(cols), causal, q_len, pl.tpr, acc)));
   return check_launch("xt_softmax_bwd");
 }
 
@@ -1253,10 +1269,10 @@ int xt_cross_entropy_fwd(const void* logits, const int32_t* targets, float* lse,
   const int grid = row_grid(rows, rpb);
   float* nll = static_cast<float*>(ws);
   uint32_t* flag = errflag();
-  XT_ROW_DISPATCH(dt, vec, (ce_fwd_kernel<T, VW><<<grid, threads, 0, s>>>(static_cast<const T*>(logits), targets,
+  XT_ROW_DISPATCH(dt, vec, (launch(ce_fwd_kernel<T, VW>, grid, threads, 0, s, static_cast<const T*>(logits), targets,
                                                                          lse, nll, rows, V, tpr, flag)));
   XT_TRY(check_launch("xt_cross_entropy_fwd"));
-  ce_loss_kernel<<<1, 1024, 0, s>>>(nll, rows, loss);
+  launch(ce_loss_kernel, 1, 1024, 0, s, nll, rows, loss);
   return check_launch("xt_cross_entropy_fwd loss");
 }
 
@@ -1274,9 +1290,9 @@ int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float
   const int g = int(grid < 1 ? 1 : grid);
 #define XT_CE_BWD(TI, TG)                                                                                  \
   do {                                                                                                     \
-    if (vec) ce_bwd_kernel<TI, TG, 8><<<g, 256, 0, s>>>(static_cast<const TI*>(logits), targets, lse, upstream, \
+    if (vec) launch(ce_bwd_kernel<TI, TG, 8>, g, 256, 0, s, static_cast<const TI*>(logits), targets, lse, upstream, \
                                                         static_cast<TG*>(dlogits), rows, V, acc, flag);    \
-    else ce_bwd_kernel<TI, TG, 1><<<g, 256, 0, s>>>(static_cast<const TI*>(logits), targets, lse, upstream,     \
+    else launch(ce_bwd_kernel<TI, TG, 1>, g, 256, 0, s, static_cast<const TI*>(logits), targets, lse, upstream,     \
                                                     static_cast<TG*>(dlogits), rows, V, acc, flag);        \
   } while (0)
   if (dt == XT_F32 && dt_grad == XT_F32) XT_CE_BWD(float, float);
@@ -1290,7 +1306,7 @@ int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float
 int xt_rope_table(float* table, int S, int hd, double base, int pos_offset, void* stream) {
   XT_REQUIRE(table && S > 0 && hd > 0 && hd % 2 == 0 && base > 0, "xt_rope_table: bad arguments");
   const int n = S * (hd / 2);
-  rope_table_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(table, S, hd, base, pos_offset);
+  launch(rope_table_kernel, (n + 255) / 256, 256, 0, as_stream(stream), table, S, hd, base, pos_offset);
   return check_launch("xt_rope_table");
 }
 
@@ -1309,10 +1325,10 @@ static int rope_run(bool bwd, const void* x, void* y, const float* table, int B,
   if (grid > int64_t(num_sms()) * 16) grid = int64_t(num_sms()) * 16;
   XT_ROW_DISPATCH(dt, vec, {
     if (bwd)
-      rope_kernel<T, true, VW><<<int(grid), 256, 0, s>>>(static_cast<const T*>(x), static_cast<T*>(y), table, B, S, H,
+      launch(rope_kernel<T, true, VW>, int(grid), 256, 0, s, static_cast<const T*>(x), static_cast<T*>(y), table, B, S, H,
                                                          hd, ld, acc);
     else
-      rope_kernel<T, false, VW><<<int(grid), 256, 0, s>>>(static_cast<const T*>(x), static_cast<T*>(y), table, B, S,
+      launch(rope_kernel<T, false, VW>, int(grid), 256, 0, s, static_cast<const T*>(x), static_cast<T*>(y), table, B, S,
                                                           H, hd, ld, acc);
   });
   return check_launch("rope");
@@ -1347,7 +1363,7 @@ int xt_embedding_fwd(const int32_t* ids, const void* E, const void* P, void* h, 
   int64_t grid = ceil_div(work, 256);
   if (grid > int64_t(num_sms()) * 16) grid = int64_t(num_sms()) * 16;
   uint32_t* flag = errflag();
-  XT_ROW_DISPATCH(dt, vec, (embed_fwd_kernel<T, VW><<<int(grid), 256, 0, s>>>(
+  XT_ROW_DISPATCH(dt, vec, (launch(embed_fwd_kernel<T, VW>, int(grid), 256, 0, s, 
                                ids, static_cast<const T*>(E), static_cast<const T*>(P), static_cast<T*>(h), T_, S, d,
                                V, flag)));
   return check_launch("xt_embedding_fwd");
@@ -1371,16 +1387,16 @@ int xt_embedding_bwd(const int32_t* ids, const void* dh, void* dE, void* dP, int
   while (n < T) n <<= 1;
   const size_t smem = size_t(n) * sizeof(uint64_t);
   cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  embed_sort_kernel<<<1, 1024, smem, s>>>(ids, T, V, sorted, errflag());
+  launch(embed_sort_kernel, 1, 1024, smem, s, ids, T, V, sorted, errflag());
   XT_TRY(check_launch("xt_embedding_bwd sort"));
 #define XT_EMB(TH, TG)                                                                                      \
   do {                                                                                                      \
-    embed_scatter_kernel<TH, TG><<<unsigned(T), 256, 0, s>>>(sorted, static_cast<const TH*>(dh),            \
+    launch(embed_scatter_kernel<TH, TG>, unsigned(T), 256, 0, s, sorted, static_cast<const TH*>(dh),            \
                                                              static_cast<TG*>(dE), T, d, V);                \
     XT_TRY(check_launch("xt_embedding_bwd scatter"));                                                       \
     if (dP) {                                                                                               \
       int64_t gp = ceil_div(int64_t(S) * d, 256);                                                           \
-      embed_pos_kernel<TH, TG><<<unsigned(gp), 256, 0, s>>>(static_cast<const TH*>(dh), static_cast<TG*>(dP), \
+      launch(embed_pos_kernel<TH, TG>, unsigned(gp), 256, 0, s, static_cast<const TH*>(dh), static_cast<TG*>(dP), \
                                                             T, S, d, acc);                                  \
     }                                                                                                       \
   } while (0)
