@@ -68,13 +68,13 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn) {
 // the tile width (narrow tiles move more operand bytes per FLOP), plus for a K split the
 // fixed-order reduction of the partial slices.  The split is used for single-batch,
 // non-causal problems whose tile count leaves SMs idle (the M = d weight gradients).
-static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 128 ? 0.55 : 0.35; }
+static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 192 ? 0.77 : bn >= 128 ? 0.64 : 0.35; }
 
 Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split) {
-  const int cands_bf16[3] = {64, 128, 256};
+  const int cands_bf16[4] = {64, 128, 192, 256};
   const int cands_tf32[2] = {64, 128};
   const int* c = tf32 ? cands_tf32 : cands_bf16;
-  const int nc = tf32 ? 2 : 3;
+  const int nc = tf32 ? 2 : 4;
   const int sms = num_sms();
   const int bk = tf32 ? 32 : 64;
   const double per_sm = tf32 ? 5.6e12 : 11.2e12;

@@ -18,6 +18,7 @@ int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUten
   switch (bn) {
     case 64: return pick_major<64>(a_mn, b_mn, ta, tb, tc, tc2, p, grid, s);
     case 128: return pick_major<128>(a_mn, b_mn, ta, tb, tc, tc2, p, grid, s);
+    case 192: return pick_major<192>(a_mn, b_mn, ta, tb, tc, tc2, p, grid, s);
     case 256: return pick_major<256>(a_mn, b_mn, ta, tb, tc, tc2, p, grid, s);
     default: return fail(XT_ERR_UNSUPPORTED, "gemm: tile width %d", bn);
   }
