@@ -47,6 +47,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
     ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy"], default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-kernel HBM GB/s of the memory-bound ops (rows 8192 x cols 768..8192, fp32 and bf16) "
+                         "and of the 8192 x 128256 cross-entropy / fan-out case; one JSON line per case")
     ap.add_argument("--shape", default="8192,3072,768,0,1",
                     help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -480,8 +483,118 @@ def run_kernel(args):
                           "clocks": clocks}))
 
 
+def run_sweep(args):
+    """Isolated memory-bound ops, forward and backward, at rows 8192 × cols ∈ {768, 2048, 4096, 8192} in fp32 and
+    bf16 (x and the upstream gradient ~N(0, 1); RoPE with head_dim 128 and position = row mod 1024; dropout at
+    p ∈ {0, 0.1, 0.5}), then cross-entropy and the three-branch fan-out on 8192 × 128256 bf16 logits ~N(0, 2).
+    Each case: 3 untimed launches, 50 timed with CUDA events; GB/s = algorithmic bytes / time, `frac` of the
+    measured HBM copy bandwidth."""
+    import torch
+
+    import __graft_entry__
+    import synth
+    from transformer_fwd_bwd_gb300 import tape as TP
+    from transformer_fwd_bwd_gb300 import xt
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    g = torch.Generator().manual_seed(synth.SEED_SWEEP)
+
+    def timed(fn, n=50):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        assert xt.device_errors() == 0, "device error flag set"
+        return e0.elapsed_time(e1) / n * 1e3
+
+    def report(case, us, nbytes):
+        gbs = nbytes / us / 1e3
+        print(json.dumps({"sweep": case, "us": round(us, 2), "bytes": int(nbytes), "gbs": round(gbs, 1),
+                          "frac": round(gbs / hbm, 3), "peak": f"{hbm:.0f} GB/s {peak_src}"}), flush=True)
+
+    R = synth.SWEEP_ROWS
+    for dtn, tdt in (("f32", torch.float32), ("bf16", torch.bfloat16)):
+        e = 4 if dtn == "f32" else 2
+        for C in synth.SWEEP_COLS:
+            X = R * C * e
+            rn = lambda *shape: torch.randn(*shape, generator=g).to(tdt).to(dev)  # noqa: E731
+            x, d = rn(R, C), rn(R, C)
+            y, dx = torch.empty_like(x), torch.empty_like(x)
+            gam = (1 + 0.1 * torch.randn(C, generator=g)).to(tdt).to(dev)
+            bet = (0.1 * torch.randn(C, generator=g)).to(tdt).to(dev)
+            st1 = torch.empty(R, dtype=torch.float32, device=dev)
+            st2 = torch.empty(R, dtype=torch.float32, device=dev)
+            pg = torch.empty(C, dtype=torch.float32, device=dev)
+            pb = torch.empty(C, dtype=torch.float32, device=dev)
+            nws = xt.workspace(xt.ws_bytes("xt_norm_bwd_workspace_size", R, C), dev)
+            cws = xt.workspace(xt.ws_bytes("xt_colsum_workspace_size", R, C), dev)
+            tag = f"{dtn} {R}x{C}"
+            report(f"rms_norm fwd {tag}", timed(lambda: xt.xt_rms_norm_fwd(x, gam, y, st1, 1e-5)), 2 * X + 4 * R)
+            report(f"rms_norm bwd {tag}", timed(lambda: xt.xt_rms_norm_bwd(d, x, gam, st1, dx, pg, ws=nws)),
+                   3 * X + 4 * R)
+            report(f"layernorm fwd {tag}", timed(lambda: xt.xt_layernorm_fwd(x, gam, bet, y, st1, st2, 1e-5)),
+                   2 * X + 8 * R)
+            report(f"layernorm bwd {tag}",
+                   timed(lambda: xt.xt_layernorm_bwd(d, x, gam, st1, st2, dx, pg, pb, ws=nws)), 3 * X + 8 * R)
+            report(f"softmax fwd {tag}", timed(lambda: xt.xt_softmax_fwd(x, y)), 2 * X)
+            report(f"softmax bwd {tag}", timed(lambda: xt.xt_softmax_bwd(d, y, dx)), 3 * X)
+            report(f"silu fwd {tag}", timed(lambda: xt.xt_silu_fwd(x, y)), 2 * X)
+            report(f"silu bwd {tag}", timed(lambda: xt.xt_silu_bwd(d, x, dx)), 3 * X)
+            u, du = rn(R, C), torch.empty_like(x)
+            report(f"swiglu fwd {tag}", timed(lambda: xt.xt_swiglu_fwd(x, u, y)), 3 * X)
+            report(f"swiglu bwd {tag}", timed(lambda: xt.xt_swiglu_bwd(d, x, u, dx, du)), 5 * X)
+            hd = synth.SWEEP_ROPE_HD
+            S = synth.SWEEP_ROPE_SEQ
+            tab = torch.empty(2 * S * hd // 2, dtype=torch.float32, device=dev)
+            xt.xt_rope_table(tab, S, hd, 10000.0)
+            report(f"rope fwd {tag}", timed(lambda: xt.xt_rope_fwd(x, y, tab, R // S, S, C // hd, hd, C)), 2 * X)
+            report(f"rope bwd {tag}", timed(lambda: xt.xt_rope_bwd(d, dx, tab, R // S, S, C // hd, hd, C)), 2 * X)
+            report(f"add_bias fwd {tag}", timed(lambda: xt.xt_add_bias_fwd(x, bet, y)), 2 * X + C * e)
+            report(f"add_bias bwd (dbias) {tag}", timed(lambda: xt.xt_add_bias_bwd(d, None, pb, ws=cws)), X)
+            for pdrop in synth.SWEEP_DROPOUT_P:
+                report(f"dropout fwd p={pdrop} {tag}",
+                       timed(lambda: xt.xt_dropout_fwd(x, y, pdrop, synth.BASE_SEED_DROPOUT)), 2 * X)
+                report(f"dropout bwd p={pdrop} {tag}",
+                       timed(lambda: xt.xt_dropout_bwd(d, dx, pdrop, synth.BASE_SEED_DROPOUT)), 2 * X)
+            del x, d, y, dx, u, du
+            torch.cuda.empty_cache()
+
+    # cross-entropy on 8192 × 128256 bf16 logits, and the fan-out CE(x) + Σ 0.5·x + Σ x∘x into one fp32 gradient
+    cfg = synth.BIGVOCAB
+    R, V = cfg["rows"], cfg["V"]
+    X = (torch.randn(R, V, generator=g) * cfg["std"]).to(torch.bfloat16).to(dev)
+    tg = torch.randint(0, V, (R,), generator=g, dtype=torch.int32).to(dev)
+    lse = torch.empty(R, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    G = torch.empty(R, V, dtype=torch.float32, device=dev)
+    cws = xt.workspace(xt.ws_bytes("xt_cross_entropy_workspace_size", R), dev)
+    n = R * V
+    report(f"cross_entropy fwd bf16 {R}x{V}", timed(lambda: xt.xt_cross_entropy_fwd(X, tg, lse, loss, ws=cws)), 2 * n)
+    report(f"cross_entropy bwd bf16 -> f32 grad {R}x{V}",
+           timed(lambda: xt.xt_cross_entropy_bwd(X, tg, lse, one, G)), 2 * n + 4 * n)
+
+    def fanout():
+        x = TP.leaf(X, grad_dtype=torch.float32)
+        L = TP.add(TP.add(TP.cross_entropy(x, tg), TP.sum_all(TP.scale(x, 0.5))), TP.sum_all(TP.mul(x, x)))
+        TP.backward(L)
+    report(f"fan-out CE + sum(0.5x) + sum(x*x), tape fwd+bwd, fp32 grad {R}x{V} (vs the fused minimum)",
+           timed(fanout, n=5), 2 * n + 4 * n)
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.kernel:
         run_kernel(args)
         return
