@@ -283,6 +283,30 @@ int xt_dropout_mask(uint8_t* mask, int64_t n, float p, uint64_t seed, void* stre
 int xt_dropout_add_fwd(const void* h, const void* a, void* out, int64_t n, float p,
                        uint64_t seed, int training, int dt, void* stream);
 
+enum { XT_NORM_RMS = 0, XT_NORM_LN = 1 };  /* norm kinds (also the block stack's norm field) */
+
+/* ---------------------------------------------------------------------------------
+ * The residual path's dropout fused with its neighbouring pre-norm ([DO] § dropout 接在哪
+ * (wiring): every residual add of the block is followed by the next sub-block's norm, and
+ * every norm backward by the preceding site's dropout backward).  Same masks, same
+ * arithmetic, same results as the separate calls, one pass over the rows:
+ *   xt_dropout_add_norm_fwd: sum = h + dropout(a) over [rows, cols] (flat index i = r·cols + c,
+ *     as xt_dropout_add_fwd), then y = norm(sum as stored) with its statistics:
+ *     norm = XT_NORM_RMS: stat0 = inv_rms (xt_rms_norm_fwd; beta, stat1 unused);
+ *     norm = XT_NORM_LN:  stat0 = mean, stat1 = rstd (xt_layernorm_fwd).
+ *   xt_norm_bwd_dropout: the norm backward (xt_rms_norm_bwd with stat0 = inv_rms, or
+ *     xt_layernorm_bwd with stat0 = mean, stat1 = rstd; dx required) that also writes
+ *     g = dropout_bwd(dx as stored) (xt_dropout_bwd_ex from dx to g), g of dtype dt.
+ * ------------------------------------------------------------------------------- */
+int xt_dropout_add_norm_fwd(const void* h, const void* a, void* sum, const void* gamma,
+                            const void* beta, void* y, float* stat0, float* stat1, int64_t rows,
+                            int64_t cols, float p, uint64_t seed, int training, int norm, float eps,
+                            int dt, void* stream);
+int xt_norm_bwd_dropout(int norm, const void* d, const void* x, const void* gamma, const float* stat0,
+                        const float* stat1, void* dx, void* dgamma, void* dbeta, void* g, int64_t rows,
+                        int64_t cols, int dt, int dt_dx, int dt_param, void* ws, int acc_dx,
+                        int acc_param, float p, uint64_t seed, int training, void* stream);
+
 /* ---------------------------------------------------------------------------------
  * Embedding ([BP] § kernel-pair table k_embed_fwd/bwd; § Var gradienter lever i minnet):
  * h[t] = E[ids[t]] (+ P[t mod S] when P != NULL).  Backward: dE[v] = Σ_{t: ids[t]=v} dh[t]
@@ -365,7 +389,6 @@ int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, cons
  * call xt_block_zero_grads first for a fresh step.  No host synchronisation; the pair can
  * be captured in a CUDA graph.
  * ------------------------------------------------------------------------------- */
-enum { XT_NORM_RMS = 0, XT_NORM_LN = 1 };
 enum { XT_MLP_SWIGLU = 0, XT_MLP_GELU = 1 };
 /* Attention path: AUTO runs the fused kernels (xt_attention_*) when dtype is XT_BF16, hd is
  * 64 and d is a multiple of 8, else the composition of causal-tile GEMMs around the row

@@ -417,3 +417,56 @@ def test_add_bias(dtype, rows, cols):
     rdx, rdb = O.add_bias_bwd(d)
     check(host(DX), rdx, dtype, "add_bias dx")
     check_sum(host(DB), rdb, np.abs(d).sum(0), "f32", "add_bias dbias")
+
+
+@pytest.mark.parametrize("norm", ["rms", "ln"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p,training", [(0.0, 1), (0.1, 1), (0.1, 0)])
+@pytest.mark.parametrize("rows,cols", [(333, 768), (64, 97), (40, 2048)])
+def test_dropout_add_norm_fused_equals_separate(norm, dtype, p, training, rows, cols):
+    """[DO] § dropout 接在哪 (wiring): the residual add and the next pre-norm in one pass give the
+    separate calls' results bit for bit (same masks, same arithmetic): sum, y and the statistics;
+    and the norm backward fused with the preceding site's dropout backward gives the separate
+    norm backward and xt_dropout_bwd_ex bit for bit (dx, dγ, dβ and the passed-on gradient)."""
+    if dtype == "bf16" and cols % 8:
+        cols += 8 - cols % 8
+    seed = synth.BASE_SEED_DROPOUT + 7
+    kind = xt.XT_NORM_RMS if norm == "rms" else xt.XT_NORM_LN
+    h, a, dy = (dev(synth.normal((rows, cols), 90 + i, dtype=dtype), dtype) for i in range(3))
+    gam = dev(synth.normal((cols,), 93, std=0.1, mean=1.0, dtype=dtype), dtype)
+    bet = dev(synth.normal((cols,), 94, std=0.1, dtype=dtype), dtype)
+    # forward: separate
+    s1, y1 = empty((rows, cols), dtype), empty((rows, cols), dtype)
+    st_a, st_b = empty((rows,)), empty((rows,))
+    xt.xt_dropout_add_fwd(h, a, s1, p, seed, training)
+    if norm == "rms":
+        xt.xt_rms_norm_fwd(s1, gam, y1, st_a, 1e-5)
+    else:
+        xt.xt_layernorm_fwd(s1, gam, bet, y1, st_a, st_b, 1e-5)
+    # forward: fused
+    s2, y2 = empty((rows, cols), dtype), empty((rows, cols), dtype)
+    st_c, st_d = empty((rows,)), empty((rows,))
+    xt.xt_dropout_add_norm_fwd(h, a, s2, gam, bet, y2, st_c, st_d if norm == "ln" else None, p, seed, training, kind,
+                               1e-5)
+    sync()
+    assert torch.equal(s1, s2) and torch.equal(y1, y2) and torch.equal(st_a, st_c)
+    if norm == "ln":
+        assert torch.equal(st_b, st_d)
+    # backward: separate (dx accumulated into a float32 residual gradient, then the dropout backward)
+    dh1 = dev(synth.normal((rows, cols), 95), "f32")
+    dh2 = dh1.clone()
+    dg1, dg2 = empty((cols,)), empty((cols,))
+    db1, db2 = empty((cols,)), empty((cols,))
+    g1, g2 = empty((rows, cols), dtype), empty((rows, cols), dtype)
+    if norm == "rms":
+        xt.xt_rms_norm_bwd(dy, s1, gam, st_a, dh1, dg1, acc_dx=1)
+    else:
+        xt.xt_layernorm_bwd(dy, s1, gam, st_a, st_b, dh1, dg1, db1, acc_dx=1)
+    xt.xt_dropout_bwd_ex(dh1, g1, p, seed, training)
+    xt.xt_norm_bwd_dropout(kind, dy, s1, gam, st_a, st_b if norm == "ln" else None, dh2, dg2,
+                           db2 if norm == "ln" else None, g2, p, seed, training, acc_dx=1)
+    sync()
+    assert xt.device_errors() == 0
+    assert torch.equal(dh1, dh2) and torch.equal(dg1, dg2) and torch.equal(g1, g2)
+    if norm == "ln":
+        assert torch.equal(db1, db2)

@@ -293,6 +293,22 @@ int norm_fwd(const xt_block_config& c, const Dims& m, const void* x, const void*
   return xt_layernorm_fwd(x, g, b, y, st, st + m.T, m.T, m.d, c.eps, m.dt, stream);
 }
 
+// sum = h + dropout(a), y = norm(sum) in one pass (xt_dropout_add_norm_fwd).
+int add_norm_fwd(const xt_block_config& c, const Dims& m, const void* h, const void* a, void* sum, const void* g,
+                 const void* b, void* y, float* st, uint64_t seed, bool drop, void* stream) {
+  return xt_dropout_add_norm_fwd(h, a, sum, g, b, y, st, m.rms ? nullptr : st + m.T, m.T, m.d, c.p, seed, drop,
+                                 m.rms ? XT_NORM_RMS : XT_NORM_LN, c.eps, m.dt, stream);
+}
+
+// The norm backward into dh (float32, += when acc_dx) that also writes g = dropout_bwd(dh) for the
+// residual dropout site before it (xt_norm_bwd_dropout); parameter grads +=.
+int norm_bwd_g(const xt_block_config& c, const Dims& m, const void* dy, const void* x, const void* g, const float* st,
+               float* dh, void* dg, void* db, int acc_dx, void* gout, uint64_t seed, bool drop, const Bufs& b,
+               void* stream) {
+  return xt_norm_bwd_dropout(m.rms ? XT_NORM_RMS : XT_NORM_LN, dy, x, g, st, m.rms ? nullptr : st + m.T, dh, dg, db,
+                             gout, m.T, m.d, m.dt, XT_F32, m.gdt, b.ws_norm, acc_dx, 1, c.p, seed, drop, stream);
+}
+
 // dh (float32) += norm backward of dy; parameter grads += as well.
 int norm_bwd(const Dims& m, const void* dy, const void* x, const void* g, const float* st, float* dh, void* dg,
              void* db, int acc_dx, const Bufs& b, void* stream) {
@@ -332,9 +348,10 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   const bool drop = c.training && c.p > 0.f;
   if (c.rope) XT_TRY(xt_rope_table(b.rope, int(m.S), int(m.hd), c.rope_base, 0, stream));
   XT_TRY(xt_embedding_fwd(ids, prm->E, c.learned_pos ? prm->P : nullptr, b.h_in[0], T, int(m.S), d, m.V, m.dt, stream));
+  // the first pre-norm; every later one is fused with the residual add before it
+  XT_TRY(norm_fwd(c, m, b.h_in[0], prm->g1[0], prm->b1 ? prm->b1[0] : nullptr, b.x1[0], b.st1[0], stream));
   for (int64_t l = 0; l < m.L; ++l) {
     // attention sub-block
-    XT_TRY(norm_fwd(c, m, b.h_in[l], prm->g1[l], prm->b1 ? prm->b1[l] : nullptr, b.x1[l], b.st1[l], stream));
     XT_TRY(matmul(lin_fwd(m, d, 3 * d), b.x1[l], prm->Wqkv[l], b.qkv[l], b.ws_mm, b.ws_mm_bytes, s));
     if (c.rope)  // q and k blocks are 2H consecutive heads of each qkv row
       XT_TRY(xt_rope_fwd(b.qkv[l], b.qkv[l], b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, stream));
@@ -347,19 +364,24 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
       XT_TRY(matmul(att_pv(m), b.P[l], off(b.qkv[l], 2 * d, e), b.o[l], b.ws_mm, b.ws_mm_bytes, s));
     }
     XT_TRY(matmul(lin_fwd(m, d, d), b.o[l], prm->Wo[l], b.tmp, b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(xt_dropout_add_fwd(b.h_in[l], b.tmp, b.h_mid[l], T * d, c.p, site_seed(c, l, kSiteAttn), drop, m.dt, stream));
+    // residual dropout-add, then the MLP sub-block's pre-norm, in one pass
+    XT_TRY(add_norm_fwd(c, m, b.h_in[l], b.tmp, b.h_mid[l], prm->g2[l], prm->b2 ? prm->b2[l] : nullptr, b.x2[l],
+                        b.st2[l], site_seed(c, l, kSiteAttn), drop, stream));
     // MLP sub-block
-    XT_TRY(norm_fwd(c, m, b.h_mid[l], prm->g2[l], prm->b2 ? prm->b2[l] : nullptr, b.x2[l], b.st2[l], stream));
     XT_TRY(matmul(lin_fwd(m, d, m.UP), b.x2[l], prm->W_up[l], b.up[l], b.ws_mm, b.ws_mm_bytes, s));
     if (m.swiglu)
       XT_TRY(xt_swiglu_fwd(b.up[l], off(b.up[l], m.F, e), m.UP, b.mact[l], m.F, T, m.F, m.dt, stream));
     else
       XT_TRY(xt_gelu_fwd(b.up[l], b.mact[l], T * m.F, m.dt, stream));
     XT_TRY(matmul(lin_fwd(m, m.F, d), b.mact[l], prm->W_down[l], b.tmp, b.ws_mm, b.ws_mm_bytes, s));
-    void* h_next = l + 1 < m.L ? b.h_in[l + 1] : b.h_final;
-    XT_TRY(xt_dropout_add_fwd(b.h_mid[l], b.tmp, h_next, T * d, c.p, site_seed(c, l, kSiteFfn), drop, m.dt, stream));
+    // residual dropout-add, then the next layer's first pre-norm (or the final norm)
+    if (l + 1 < m.L)
+      XT_TRY(add_norm_fwd(c, m, b.h_mid[l], b.tmp, b.h_in[l + 1], prm->g1[l + 1], prm->b1 ? prm->b1[l + 1] : nullptr,
+                          b.x1[l + 1], b.st1[l + 1], site_seed(c, l, kSiteFfn), drop, stream));
+    else
+      XT_TRY(add_norm_fwd(c, m, b.h_mid[l], b.tmp, b.h_final, prm->gf, prm->bf, b.hf, b.stf,
+                          site_seed(c, l, kSiteFfn), drop, stream));
   }
-  XT_TRY(norm_fwd(c, m, b.h_final, prm->gf, prm->bf, b.hf, b.stf, stream));
   XT_TRY(matmul(logits_fwd(m), b.hf, prm->E, b.logits, b.ws_mm, b.ws_mm_bytes, s));
   return xt_cross_entropy_fwd(b.logits, targets, b.lse, loss, T, m.V, m.dt, b.ws_ce, stream);
 }
@@ -382,12 +404,14 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   XT_TRY(xt_cross_entropy_bwd(b.logits, targets, b.lse, b.one, b.logits, T, m.V, m.dt, m.dt, 0, stream));
   XT_TRY(matmul(logits_de(m), b.logits, b.hf, prm->dE, b.ws_mm, b.ws_mm_bytes, s));
   XT_TRY(matmul(logits_dhf(m), b.logits, prm->E, b.gA, b.ws_mm, b.ws_mm_bytes, s));
-  XT_TRY(norm_bwd(m, b.gA, b.h_final, prm->gf, b.stf, b.dh, prm->dgf, prm->dbf, 0, b, stream));
+  // Each norm backward also writes the gradient the residual dropout before it passes on: the
+  // MLP sub-block reads its df from gB, the attention sub-block its input gradient from gA.
+  XT_TRY(norm_bwd_g(c, m, b.gA, b.h_final, prm->gf, b.stf, b.dh, prm->dgf, prm->dbf, 0, b.gB,
+                    site_seed(c, m.L - 1, kSiteFfn), drop, b, stream));
   for (int64_t l = m.L - 1; l >= 0; --l) {
-    // MLP sub-block: df = dropout'(dh); dW_down += mᵀ df; dm = df W_downᵀ; activation'; ...
-    XT_TRY(xt_dropout_bwd_ex(b.dh, XT_F32, b.gA, m.dt, T * d, c.p, site_seed(c, l, kSiteFfn), drop, 0, stream));
-    XT_TRY(matmul(lin_dw(m, m.F, d), b.mact[l], b.gA, prm->dW_down[l], b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(matmul(lin_dx(m, m.F, d), b.gA, prm->W_down[l], b.dm, b.ws_mm, b.ws_mm_bytes, s));
+    // MLP sub-block: df = dropout'(dh) (in gB); dW_down += mᵀ df; dm = df W_downᵀ; activation'; ...
+    XT_TRY(matmul(lin_dw(m, m.F, d), b.mact[l], b.gB, prm->dW_down[l], b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(matmul(lin_dx(m, m.F, d), b.gB, prm->W_down[l], b.dm, b.ws_mm, b.ws_mm_bytes, s));
     if (m.swiglu)
       XT_TRY(xt_swiglu_bwd(b.dm, m.F, b.up[l], off(b.up[l], m.F, e), m.UP, b.dgu, off(b.dgu, m.F, e), m.UP, T, m.F,
                            m.dt, 0, stream));
@@ -395,10 +419,9 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
       XT_TRY(xt_gelu_bwd(b.dm, b.up[l], b.dgu, T * m.F, m.dt, 0, stream));
     XT_TRY(matmul(lin_dw(m, d, m.UP), b.x2[l], b.dgu, prm->dW_up[l], b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(matmul(lin_dx(m, d, m.UP), b.dgu, prm->W_up[l], b.gB, b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(norm_bwd(m, b.gB, b.h_mid[l], prm->g2[l], b.st2[l], b.dh, prm->dg2[l], prm->db2 ? prm->db2[l] : nullptr, 1,
-                    b, stream));
-    // attention sub-block
-    XT_TRY(xt_dropout_bwd_ex(b.dh, XT_F32, b.gA, m.dt, T * d, c.p, site_seed(c, l, kSiteAttn), drop, 0, stream));
+    XT_TRY(norm_bwd_g(c, m, b.gB, b.h_mid[l], prm->g2[l], b.st2[l], b.dh, prm->dg2[l],
+                      prm->db2 ? prm->db2[l] : nullptr, 1, b.gA, site_seed(c, l, kSiteAttn), drop, b, stream));
+    // attention sub-block (its input gradient dropout'(dh) is in gA)
     XT_TRY(matmul(lin_dw(m, d, d), b.o[l], b.gA, prm->dWo[l], b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(matmul(lin_dx(m, d, d), b.gA, prm->Wo[l], b.gB, b.ws_mm, b.ws_mm_bytes, s));
     if (m.fused) {
@@ -416,8 +439,12 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
       XT_TRY(xt_rope_bwd(b.dqkv, b.dqkv, b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, 0, stream));
     XT_TRY(matmul(lin_dw(m, d, 3 * d), b.x1[l], b.dqkv, prm->dWqkv[l], b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(matmul(lin_dx(m, d, 3 * d), b.dqkv, prm->Wqkv[l], b.gA, b.ws_mm, b.ws_mm_bytes, s));
-    XT_TRY(norm_bwd(m, b.gA, b.h_in[l], prm->g1[l], b.st1[l], b.dh, prm->dg1[l], prm->db1 ? prm->db1[l] : nullptr, 1,
-                    b, stream));
+    if (l > 0)
+      XT_TRY(norm_bwd_g(c, m, b.gA, b.h_in[l], prm->g1[l], b.st1[l], b.dh, prm->dg1[l],
+                        prm->db1 ? prm->db1[l] : nullptr, 1, b.gB, site_seed(c, l - 1, kSiteFfn), drop, b, stream));
+    else
+      XT_TRY(norm_bwd(m, b.gA, b.h_in[l], prm->g1[l], b.st1[l], b.dh, prm->dg1[l], prm->db1 ? prm->db1[l] : nullptr,
+                      1, b, stream));
   }
   return xt_embedding_bwd(ids, b.dh, prm->dE, c.learned_pos ? prm->dP : nullptr, T, int(m.S), d, m.V, XT_F32, m.gdt,
                           b.ws_emb, 1, stream);

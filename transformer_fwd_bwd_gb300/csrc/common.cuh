@@ -186,6 +186,18 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = mm;
 }
 
+// [DO] § RNG：counter-based.  splitmix64 (Steele, Lea & Flood) from state `key`; the keep
+// decision uses the top 24 bits only.  The final `z ^ (z >> 31)` step of the mixer leaves
+// bits 63..40 unchanged (z >> 31 has its top 31 bits clear), so it is omitted.
+__device__ __forceinline__ bool dropout_keep(uint64_t seed, uint64_t i, float p) {
+  uint64_t z = seed ^ (i * 0x9E3779B97F4A7C15ull);
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  const float u = static_cast<float>(static_cast<uint32_t>(z >> 40)) * 0x1.0p-24f;
+  return u >= p;
+}
+
 // Φ(x) = ½·erfc(−x/√2) (no cancellation for x ≪ 0, unlike ½(1 + erf(x/√2))), with erfc from the
 // Chebyshev-fitted form of Press, Teukolsky, Vetterling & Flannery, Numerical Recipes (§6.2,
 // erfcc): for z ≥ 0, erfc(z) = t·exp(−z² + P(t)), t = 1/(1 + z/2), P a degree-9 polynomial in t;

@@ -203,11 +203,29 @@ __device__ __forceinline__ void slices_fold(const float* slices, int rpb, float*
   }
 }
 
+// Optional second output of the norm backward kernels: the gradient the preceding residual
+// dropout passes on, g = keep(seed, i) ? dh·dscale : 0 (dh itself when drop is 0), written in
+// the activation dtype from the final residual gradient dh the kernel stores (i the flat index).
+struct GradOut {
+  void* g;
+  float p, dscale;
+  uint64_t seed;
+  int drop;
+};
+template <typename T, int VW>
+__device__ __forceinline__ void grad_out_store(const GradOut& go, int64_t off, const float (&dh)[VW]) {
+  float v[VW];
+#pragma unroll
+  for (int e = 0; e < VW; ++e)
+    v[e] = go.drop ? (dropout_keep(go.seed, uint64_t(off + e), go.p) ? dh[e] * go.dscale : 0.f) : dh[e];
+  store_vec<T, VW>(static_cast<T*>(go.g) + off, v);
+}
+
 template <typename T, typename TD, int VW, int MAXT>
 __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) rms_bwd_kernel(const T* __restrict__ d, const T* __restrict__ x,
                                                       const T* __restrict__ gamma, const float* __restrict__ inv_rms,
                                                       TD* dx, float* __restrict__ part, int64_t rows, int64_t cols,
-                                                      int tpr, int acc_dx) {
+                                                      int tpr, int acc_dx, GradOut go) {
   pdl_begin();
   extern __shared__ float smem[];
   float* red = smem;  // 32
@@ -262,6 +280,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) rms_bwd_kernel(cons
             for (int e = 0; e < VW; ++e) o[e] += old[e];
           }
           store_vec<TD, VW>(p, o);
+          if (go.g) grad_out_store<T, VW>(go, r * cols + j * VW, o);
         }
       }
     }
@@ -336,7 +355,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
                                                      const T* __restrict__ gamma, const float* __restrict__ mean,
                                                      const float* __restrict__ rstd, TD* dx, float* __restrict__ part_g,
                                                      float* __restrict__ part_b, int64_t rows, int64_t cols,
-                                                     int tpr, int acc_dx) {
+                                                     int tpr, int acc_dx, GradOut go) {
   pdl_begin();
   extern __shared__ float smem[];
   float* red = smem;
@@ -398,6 +417,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
             for (int e = 0; e < VW; ++e) o[e] += old[e];
           }
           store_vec<TD, VW>(p, o);
+          if (go.g) grad_out_store<T, VW>(go, r * cols + j * VW, o);
         }
       }
     }
@@ -419,6 +439,99 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
   }
   if (part_g) slices_fold(smem + 32, rpb, part_g, cols);
   if (part_b) slices_fold(smem + 32 + int64_t(rpb) * cols, rpb, part_b, cols);
+}
+
+// Residual dropout-add fused with the next pre-norm: s = h + (keep(seed, i) ? a·dscale : 0) (plain h + a
+// when drop is 0) is stored in T, and the norm of the stored s follows in the same pass, with the
+// expressions and accumulation order of rms_fwd_kernel / ln_fwd_kernel, so y and the statistics are
+// those of the two separate kernels.
+template <typename T, int VW, bool LN>
+__global__ void __launch_bounds__(1024) add_norm_fwd_kernel(const T* __restrict__ h, const T* __restrict__ a,
+                                                            T* __restrict__ sum, const T* __restrict__ gamma,
+                                                            const T* __restrict__ beta, T* __restrict__ y,
+                                                            float* __restrict__ st0, float* __restrict__ st1,
+                                                            int64_t rows, int64_t cols, float eps, int tpr, int drop,
+                                                            float p, float dscale, uint64_t seed) {
+  pdl_begin();
+  __shared__ float red[32];
+  const int rpb = blockDim.x / tpr, l = threadIdx.x % tpr;
+  const int64_t nvec = cols / VW;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+    const int64_t r = r0 + threadIdx.x / tpr;
+    const bool act = r < rows;
+    float f[NV][VW];
+    float s1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t j = l + int64_t(k) * tpr;
+      if (act && j < nvec) {
+        Raw<T, VW> hv, av;
+        hv.load(h + r * cols + j * VW);
+        av.load(a + r * cols + j * VW);
+        float o[VW];
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          const float ae = av.get(e);
+          o[e] = hv.get(e) + (drop ? (dropout_keep(seed, uint64_t(r * cols + j * VW + e), p) ? ae * dscale : 0.f) : ae);
+        }
+        store_vec<T, VW>(sum + r * cols + j * VW, o);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) f[k][e] = to_f(from_f<T>(o[e]));  // the stored value
+      } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) f[k][e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        if constexpr (LN) s1 += f[k][e];
+        else s1 += f[k][e] * f[k][e];
+      }
+    }
+    if constexpr (LN) {
+      const float mu = group_reduce<false>(s1, tpr, red) / float(cols);
+      float q = 0.f;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int64_t j = l + int64_t(k) * tpr;
+        if (j < nvec)
+#pragma unroll
+          for (int e = 0; e < VW; ++e) {
+            const float c = f[k][e] - mu;
+            q += c * c;
+          }
+      }
+      const float var = group_reduce<false>(q, tpr, red) / float(cols);
+      const float rs = 1.f / sqrtf(var + eps);
+      if (act && l == 0) { st0[r] = mu; st1[r] = rs; }
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int64_t j = l + int64_t(k) * tpr;
+        if (act && j < nvec) {
+          float gm[VW], bt[VW], o[VW];
+          load_vec<T, VW>(gamma + j * VW, gm);
+          load_vec<T, VW>(beta + j * VW, bt);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) o[e] = (f[k][e] - mu) * rs * gm[e] + bt[e];
+          store_vec<T, VW>(y + r * cols + j * VW, o);
+        }
+      }
+    } else {
+      const float ss = group_reduce<false>(s1, tpr, red);
+      const float ir = 1.f / sqrtf(ss / float(cols) + eps);
+      if (act && l == 0) st0[r] = ir;
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int64_t j = l + int64_t(k) * tpr;
+        if (act && j < nvec) {
+          float gm[VW], o[VW];
+          load_vec<T, VW>(gamma + j * VW, gm);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) o[e] = f[k][e] * ir * gm[e];
+          store_vec<T, VW>(y + r * cols + j * VW, o);
+        }
+      }
+    }
+  }
 }
 
 // ============================================================================== column sums
@@ -1011,9 +1124,9 @@ int xt_rms_norm_fwd(const void* x, const void* gamma, void* y, float* inv_rms, i
   return check_launch("xt_rms_norm_fwd");
 }
 
-int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float* inv_rms, void* dx, void* dgamma,
-                    int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws, int acc_dx, int acc_param,
-                    void* stream) {
+static int rms_bwd_impl(const void* d, const void* x, const void* gamma, const float* inv_rms, void* dx, void* dgamma,
+                        int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws, int acc_dx, int acc_param,
+                        void* stream, GradOut go) {
   XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_dx) && valid_dtype(dt_param), "xt_rms_norm_bwd: bad dtype");
   XT_REQUIRE(dt_dx == dt || (dt == XT_BF16 && dt_dx == XT_F32), "xt_rms_norm_bwd: dx dtype must be dt or f32");
   XT_REQUIRE(rows >= 0 && cols > 0, "xt_rms_norm_bwd: bad sizes");
@@ -1037,11 +1150,18 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
     auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     launch(k, nb, pl.threads, smem, s, static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
-                                   inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
+                                   inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx, go);
   });
   XT_TRY(check_launch("xt_rms_norm_bwd"));
   if (dgamma) return finalize(part, nb, cols, dgamma, dt_param, acc_param, s);
   return XT_OK;
+}
+
+int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float* inv_rms, void* dx, void* dgamma,
+                    int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws, int acc_dx, int acc_param,
+                    void* stream) {
+  return rms_bwd_impl(d, x, gamma, inv_rms, dx, dgamma, rows, cols, dt, dt_dx, dt_param, ws, acc_dx, acc_param, stream,
+                      GradOut{});
 }
 
 }  // extern "C"
@@ -1108,7 +1228,7 @@ int xt_rms_norm_bwd_noalloc(const void* d, const void* x, const void* gamma, con
     auto k = pl.threads <= 256 ? rms_bwd_kernel<T, TD, VW, 256> : rms_bwd_kernel<T, TD, VW, 512>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     launch(k, nb, pl.threads, smem, s, static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
-                                   inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx);
+                                   inv_rms, static_cast<TD*>(dx), part, rows, cols, pl.tpr, acc_dx, GradOut{});
   });
   XT_TRY(check_launch("xt_rms_norm_bwd_noalloc"));
   if (dgamma) return finalize(part, nb, cols, dgamma, dt_param, acc_param, s);
@@ -1132,9 +1252,9 @@ int xt_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y
   return check_launch("xt_layernorm_fwd");
 }
 
-int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,
-                     void* dgamma, void* dbeta, int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws,
-                     int acc_dx, int acc_param, void* stream) {
+static int ln_bwd_impl(const void* d, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,
+                       void* dgamma, void* dbeta, int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws,
+                       int acc_dx, int acc_param, void* stream, GradOut go) {
   XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_dx) && valid_dtype(dt_param), "xt_layernorm_bwd: bad dtype");
   XT_REQUIRE(dt_dx == dt || (dt == XT_BF16 && dt_dx == XT_F32), "xt_layernorm_bwd: dx dtype must be dt or f32");
   XT_REQUIRE(rows >= 0 && cols > 0, "xt_layernorm_bwd: bad sizes");
@@ -1161,7 +1281,7 @@ int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const floa
   const int64_t nvt = ceil_div(ceil_div(cols, pl.vw), pl.tpr);  // vectors per thread (1..NV)
   XT_NORM_BWD_DISPATCH(dt, dt_dx, vec, {
     void (*k)(const T*, const T*, const T*, const float*, const float*, TD*, float*, float*, int64_t, int64_t, int,
-              int) = nullptr;
+              int, GradOut) = nullptr;
     const bool narrow = pl.threads <= 256;
     switch (nvt) {
       case 1: k = narrow ? ln_bwd_kernel<T, TD, VW, 1, 256> : ln_bwd_kernel<T, TD, VW, 1, 512>; break;
@@ -1171,13 +1291,66 @@ int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const floa
     }
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     launch(k, nb, pl.threads, smem, s, static_cast<const T*>(d), static_cast<const T*>(x), static_cast<const T*>(gamma),
-                                   mean, rstd, static_cast<TD*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx);
+                                   mean, rstd, static_cast<TD*>(dx), part_g, part_b, rows, cols, pl.tpr, acc_dx, go);
   });
   XT_TRY(check_launch("xt_layernorm_bwd"));
   if (dgamma && dbeta) return finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s, part_b, dbeta);
   if (dgamma) return finalize(part_g, nb, cols, dgamma, dt_param, acc_param, s);
   if (dbeta) return finalize(part_b, nb, cols, dbeta, dt_param, acc_param, s);
   return XT_OK;
+}
+
+int xt_layernorm_bwd(const void* d, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,
+                     void* dgamma, void* dbeta, int64_t rows, int64_t cols, int dt, int dt_dx, int dt_param, void* ws,
+                     int acc_dx, int acc_param, void* stream) {
+  return ln_bwd_impl(d, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, cols, dt, dt_dx, dt_param, ws, acc_dx, acc_param,
+                     stream, GradOut{});
+}
+
+int xt_dropout_add_norm_fwd(const void* h, const void* a, void* sum, const void* gamma, const void* beta, void* y,
+                            float* stat0, float* stat1, int64_t rows, int64_t cols, float p, uint64_t seed,
+                            int training, int norm, float eps, int dt, void* stream) {
+  XT_REQUIRE(valid_dtype(dt), "xt_dropout_add_norm_fwd: bad dtype");
+  XT_REQUIRE(norm == XT_NORM_RMS || norm == XT_NORM_LN, "xt_dropout_add_norm_fwd: bad norm");
+  XT_REQUIRE(rows >= 0 && cols > 0, "xt_dropout_add_norm_fwd: bad sizes");
+  XT_REQUIRE(p >= 0.f && p < 1.f, "xt_dropout_add_norm_fwd: p must be in [0, 1)");
+  XT_REQUIRE(rows == 0 || (h && a && sum && gamma && y && stat0 && (norm == XT_NORM_RMS || (beta && stat1))),
+             "xt_dropout_add_norm_fwd: NULL pointer");
+  if (rows == 0) return XT_OK;
+  const bool vec = rows_vec_ok(cols, dt, {h, a, sum, gamma, beta, y});
+  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1);
+  if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_dropout_add_norm_fwd: row too long");
+  cudaStream_t s = as_stream(stream);
+  const int grid = row_grid(rows, pl.rpb);
+  const int drop = (training && p > 0.f) ? 1 : 0;
+  const float dscale = float(1.0 / (1.0 - double(p)));
+  if (norm == XT_NORM_LN)
+    XT_ROW_DISPATCH(dt, vec, (launch(add_norm_fwd_kernel<T, VW, true>, grid, pl.threads, 0, s, static_cast<const T*>(h),
+                                     static_cast<const T*>(a), static_cast<T*>(sum), static_cast<const T*>(gamma),
+                                     static_cast<const T*>(beta), static_cast<T*>(y), stat0, stat1, rows, cols, eps,
+                                     pl.tpr, drop, p, dscale, seed)));
+  else
+    XT_ROW_DISPATCH(dt, vec, (launch(add_norm_fwd_kernel<T, VW, false>, grid, pl.threads, 0, s, static_cast<const T*>(h),
+                                     static_cast<const T*>(a), static_cast<T*>(sum), static_cast<const T*>(gamma),
+                                     static_cast<const T*>(beta), static_cast<T*>(y), stat0, stat1, rows, cols, eps,
+                                     pl.tpr, drop, p, dscale, seed)));
+  return check_launch("xt_dropout_add_norm_fwd");
+}
+
+int xt_norm_bwd_dropout(int norm, const void* d, const void* x, const void* gamma, const float* stat0,
+                        const float* stat1, void* dx, void* dgamma, void* dbeta, void* g, int64_t rows, int64_t cols,
+                        int dt, int dt_dx, int dt_param, void* ws, int acc_dx, int acc_param, float p, uint64_t seed,
+                        int training, void* stream) {
+  XT_REQUIRE(norm == XT_NORM_RMS || norm == XT_NORM_LN, "xt_norm_bwd_dropout: bad norm");
+  XT_REQUIRE(dx && g, "xt_norm_bwd_dropout: dx and g are required");
+  XT_REQUIRE(p >= 0.f && p < 1.f, "xt_norm_bwd_dropout: p must be in [0, 1)");
+  if (!aligned16(g)) return fail(XT_ERR_ALIGNMENT, "xt_norm_bwd_dropout: g must be 16-byte aligned");
+  GradOut go{g, p, float(1.0 / (1.0 - double(p))), seed, (training && p > 0.f) ? 1 : 0};
+  if (norm == XT_NORM_RMS)
+    return rms_bwd_impl(d, x, gamma, stat0, dx, dgamma, rows, cols, dt, dt_dx, dt_param, ws, acc_dx, acc_param,
+                        stream, go);
+  return ln_bwd_impl(d, x, gamma, stat0, stat1, dx, dgamma, dbeta, rows, cols, dt, dt_dx, dt_param, ws, acc_dx,
+                     acc_param, stream, go);
 }
 
 int xt_colsum_workspace_size(int64_t rows, int64_t cols, size_t* bytes) {

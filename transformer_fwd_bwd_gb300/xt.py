@@ -101,6 +101,9 @@ _SIGS = {
     "xt_rope_fwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _VP],
     "xt_rope_bwd": [_VP, _VP, _VP, _I, _I, _I, _I, _I64, _I, _I, _VP],
     "xt_softmax_fwd": [_VP, _VP, _I64, _I64, _I, _I64, _I, _VP],
+    "xt_dropout_add_norm_fwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _F, _U64, _I, _I, _F, _I, _VP],
+    "xt_norm_bwd_dropout": [_I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP, _I, _I, _F,
+                            _U64, _I, _VP],
     "xt_softmax_bwd": [_VP, _VP, _VP, _I64, _I64, _I, _I64, _I, _I, _VP],
     "xt_attention_fwd": [_VP, _VP, _VP, _I64, _VP, _VP, _I64, _VP, _I, _I, _I, _I, _I, _I, _VP],
     "xt_attention_bwd_workspace_size": [_I, _I, _I, _SZP],
@@ -374,6 +377,23 @@ def xt_layernorm_bwd(d, x, gamma, mean, rstd, dx, dgamma, dbeta, acc_dx=0, acc_p
     pdt = dt(dgamma) if dgamma is not None else (dt(dbeta) if dbeta is not None else dt(x))
     call("xt_layernorm_bwd", ptr(d), ptr(x), ptr(gamma), ptr(mean), ptr(rstd), ptr(dx), ptr(dgamma), ptr(dbeta),
          rows, cols, dt(x), dt(dx) if dx is not None else dt(x), pdt, ptr(ws), acc_dx, acc_param, stream(s))
+
+
+def xt_dropout_add_norm_fwd(h, a, sum_out, gamma, beta, y, stat0, stat1, p, seed, training, norm, eps, s=None):
+    rows, cols = h.shape
+    call("xt_dropout_add_norm_fwd", ptr(h), ptr(a), ptr(sum_out), ptr(gamma), ptr(beta), ptr(y), ptr(stat0),
+         ptr(stat1), rows, cols, float(p), int(seed) & (2**64 - 1), int(training), norm, float(eps), dt(h), stream(s))
+
+
+def xt_norm_bwd_dropout(norm, d, x, gamma, stat0, stat1, dx, dgamma, dbeta, g, p, seed, training, acc_dx=0,
+                        acc_param=0, ws=None, s=None):
+    rows, cols = x.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_norm_bwd_workspace_size", rows, cols), x.device)
+    pdt = dt(dgamma) if dgamma is not None else (dt(dbeta) if dbeta is not None else dt(x))
+    call("xt_norm_bwd_dropout", norm, ptr(d), ptr(x), ptr(gamma), ptr(stat0), ptr(stat1), ptr(dx), ptr(dgamma),
+         ptr(dbeta), ptr(g), rows, cols, dt(x), dt(dx), pdt, ptr(ws), acc_dx, acc_param, float(p),
+         int(seed) & (2**64 - 1), int(training), stream(s))
 
 
 def xt_rope_table(table, S, hd, base, pos_offset=0, s=None):
