@@ -315,7 +315,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------- GEMM roofline pass: the same step with the GEMM events ----------------
     ms_prof, clocks_prof = timed_replays(graph_prof, args.steps)
-    flops, gms = xt.profile_gemm_read()   # the last replay's GEMM launches
+    flops, gms, gshapes = xt.profile_gemm_read(shapes=True)   # the last replay's GEMM launches
     xt.profile_gemm(0)
     assert xt.device_errors() == 0, "device error flag set during the profiled pass"
 
@@ -358,6 +358,7 @@ def run_ours(args, rank, world, local_rank):
                         f"launch (events captured into the graph); that pass ran {ms_prof:.3f} ms/step, the "
                         f"event-free timed pass that gives `value` {ms:.3f} ms/step"),
         "clocks_profiled_pass": clocks_prof.summary(),
+        "by_shape": gemm_by_shape(flops, gms, gshapes),
     }
     cpu = cpu_baseline(args.workload, args.sample_seqs) if world == 1 else None
     line = {
@@ -376,6 +377,27 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def gemm_by_shape(flops, gms, shapes, top=12):
+    """The GEMM launches of one step grouped by (M, N, K, batches, BN, A MN-major, B MN-major, causal
+    mode, 10 x K splits, 1000 for stream-K over every SM, 1000 + s for s lockstep K slices): launches per step, summed event time (a K split's
+    reduce included) and TFLOP/s of each group, largest time first."""
+    groups = {}
+    for f, t, sh in zip(flops, gms, shapes):
+        g = groups.setdefault(tuple(int(x) for x in sh), [0, 0.0, 0.0])
+        g[0] += 1
+        g[1] += float(t)
+        g[2] += float(f)
+    rows = sorted(groups.items(), key=lambda kv: -kv[1][1])[:top]
+    def sched(c):
+        if c >= 1000:
+            return "stream_k" if c == 1000 else f"stream_k_slices_{c - 1000}"
+        return f"k_split_{c // 10}" if c >= 10 else "tiles"
+    return [{"mnk": list(k[:3]), "batches": 1 if 10 <= k[7] < 1000 else k[3], "bn": k[4], "a_mn": k[5],
+             "b_mn": k[6], "causal": 0 if k[7] >= 10 else k[7], "schedule": sched(k[7]),
+             "launches": n, "ms": round(t, 4), "tflops": round(f / (t * 1e-3) / 1e12, 1) if t > 0 else None}
+            for k, (n, t, f) in rows]
 
 
 def run_kernel(args):
@@ -478,7 +500,8 @@ def run_kernel(args):
         Bm = (torch.randn(N, K, generator=g) if tb else torch.randn(K, N, generator=g)).to(torch.bfloat16).to(dev)
         C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         desc = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16)
-        us = timed(lambda: xt.xt_matmul_fwd(desc, A, Bm, C))
+        mws = xt.matmul_workspace(desc, dev)
+        us = timed(lambda: xt.xt_matmul_fwd(desc, A, Bm, C, ws=mws))
         print(json.dumps({"kernel": "gemm", "shape": [M, N, K, ta, tb], "us": us, "tflops": 2 * M * N * K / us / 1e6,
                           "clocks": clocks}))
 

@@ -18,7 +18,8 @@
  *   - Pointers: DEVICE pointers owned by the caller, unless a comment says "host".
  *     The library never allocates or frees memory.  Scratch space ("ws") is caller
  *     memory of at least the size the matching *_workspace_size() reports; its contents
- *     on entry do not matter.
+ *     on entry do not matter, except for the matmul and block workspaces, whose first
+ *     4096 bytes must be zero before their first use (every call leaves them zero).
  *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).  Every call
  *     only enqueues work on it and returns; nothing synchronises, except
  *     xt_get_device_errors().
@@ -347,10 +348,28 @@ typedef struct xt_matmul_desc {
   int64_t stride_c_outer, stride_c_inner;
 } xt_matmul_desc;
 
-/* Scratch bytes the call needs: nonzero only for XT_F32 operands read MN-major (trans_a = 1
- * or trans_b = 0), which are first copied, transposed, into K-major scratch because the
- * tf32 MMA is fed K-major operands only.  ws may be NULL when the size is 0. */
+/* Scratch bytes the call needs, laid out as
+ *   [4096 bytes of stream-K flag words][tf32 staging][partial tiles]:
+ *   - flag words: zero before the workspace's first use (e.g. cudaMemset once when it is
+ *     allocated); each call leaves them zero.  A stream-K launch's CTAs signal through them
+ *     that a partial tile is ready, so two matmul calls must not share a workspace while
+ *     both can run (on two streams);
+ *   - staging: XT_F32 operands read MN-major (trans_a = 1 or trans_b = 0) are first copied,
+ *     transposed, into K-major scratch because the tf32 MMA is fed K-major operands only;
+ *   - partial tiles: fp32 partial accumulators of a K split or of the stream-K schedule.
+ * The schedule is chosen per problem from a per-tile time model: whole output tiles over
+ * persistent CTAs, or (with a workspace, non-causal) a K split reduced in a fixed order by a
+ * second kernel, or stream-K: every SM's CTA an equal share of the tiles' k-block
+ * iterations, or tiles × s CTAs each computing one K slice of one tile; a tile shared by
+ * several CTAs is summed, in CTA order, by the CTA holding its first k-blocks.  All are
+ * deterministic.  ws = NULL (or fewer bytes than reported) restricts the choice
+ * to whole tiles, and is an error for the tf32 staging case. */
 int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes);
+/* Schedule override for every later matmul call of the process (tests, tuning): 0 the
+ * time model's choice (default), 1 whole tiles only, 2 a K split wherever one is allowed,
+ * 3 stream-K over every SM wherever allowed, 4 stream-K in lockstep K slices (tiles × s
+ * CTAs, each one K slice of one tile) wherever allowed.  XT_ERR_INVALID_ARG otherwise. */
+int xt_gemm_set_schedule(int mode);
 int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* ws,
                   size_t ws_bytes, void* stream);
 /* Backward of C = alpha·op(A)@op(B) given dC (layout of C, dtype dtype_ab):
@@ -432,6 +451,8 @@ typedef struct xt_block_params {
   void* dgf; void* dbf;
 } xt_block_params;
 
+/* The workspace holds the saved activations and every scratch buffer of the step; its first
+ * 4096 bytes (the matmul scratch's stream-K flag words) must be zero before its first use. */
 int xt_block_workspace_size(const xt_block_config* cfg, size_t* bytes);
 int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const int32_t* ids,
                  const int32_t* targets, float* loss, void* ws, void* stream);

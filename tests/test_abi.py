@@ -56,11 +56,16 @@ def test_host_validation(xt):
     assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None, 0, None) == xt.XT_ERR_ALIGNMENT
     d = xt.matmul_desc(64, 64, 64, lda=8)
     assert L.xt_matmul_fwd(C.byref(d), 16, 16, 16, None, 0, None) == xt.XT_ERR_INVALID_ARG
-    # fp32 operands read MN-major need tf32 staging scratch; bf16 ones do not
+    # every matmul workspace starts with 4096 bytes of stream-K flag words; fp32 operands read
+    # MN-major add tf32 staging scratch; a short-K bf16 problem (no split, no stream-K) nothing
     d = xt.matmul_desc(256, 128, 64, trans_a=1, dtype_ab=xt.XT_F32)
-    assert L.xt_matmul_workspace_size(C.byref(d), C.byref(sz)) == 0 and sz.value >= 256 * 64 * 4 + 128 * 64 * 4
+    assert L.xt_matmul_workspace_size(C.byref(d), C.byref(sz)) == 0
+    assert sz.value >= 4096 + 256 * 64 * 4 + 128 * 64 * 4
     d = xt.matmul_desc(256, 128, 64, trans_a=1, dtype_ab=xt.XT_BF16)
+    assert L.xt_matmul_workspace_size(C.byref(d), C.byref(sz)) == 0 and sz.value == 4096
+    d = xt.matmul_desc(0, 128, 64)
     assert L.xt_matmul_workspace_size(C.byref(d), C.byref(sz)) == 0 and sz.value == 0
+    assert L.xt_gemm_set_schedule(5) == xt.XT_ERR_INVALID_ARG and L.xt_gemm_set_schedule(0) == 0
     assert L.xt_embedding_workspace_size(1000, C.byref(sz)) == 0 and sz.value == 8000
     assert L.xt_sum_workspace_size(-1, C.byref(sz)) == xt.XT_ERR_INVALID_ARG
     assert xt.version().startswith("xt")

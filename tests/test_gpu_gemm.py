@@ -177,12 +177,33 @@ def test_matmul_alignment_rejected():
     assert ei.value.code == xt.XT_ERR_ALIGNMENT
 
 
+@pytest.fixture
+def schedule():
+    """Sets the GEMM schedule override for one test and restores the model's choice after."""
+    yield xt.gemm_set_schedule
+    xt.gemm_set_schedule(0)
+
+
+def schedules_of(fn):
+    """Runs fn with GEMM profiling on; the schedule code of each GEMM launch it made
+    (causal mode, 10 × K splits, or 1000 for stream-K)."""
+    xt.profile_gemm(64)
+    try:
+        fn()
+        sync()
+        _, _, sh = xt.profile_gemm_read(shapes=True)
+    finally:
+        xt.profile_gemm(0)
+    return [int(x) for x in sh[:, 7]]
+
+
 @pytest.mark.parametrize("ab", ["bf16", "f32"])
 @pytest.mark.parametrize("c", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", [(768, 768, 8192), (768, 3072, 8192), (200, 136, 4096)])
-def test_matmul_split_k(ab, c, M, N, K):
-    """Weight-gradient shapes (small M·N, long K) take the deterministic K split: partial
+def test_matmul_split_k(ab, c, M, N, K, schedule):
+    """Weight-gradient shapes (small M·N, long K) under the deterministic K split: partial
     tiles in workspace slices, then a fixed-order reduction into C (with += here)."""
+    schedule(2)
     A = synth.normal((K, M), 56, dtype=ab)   # stored [K, M]: dW = xᵀ dy layout
     B = synth.normal((K, N), 57, dtype=ab)
     C0 = synth.normal((M, N), 58, dtype=c)
@@ -199,6 +220,84 @@ def test_matmul_split_k(ab, c, M, N, K):
     assert norm_err(outs[0], want) <= tol
     assert np.array_equal(outs[0], outs[1]), "K split is not deterministic"
     assert xt.device_errors() == 0
+
+
+# (M, N, K, trans_a): the weight-gradient layout; ragged M, N and K; one output tile over
+# 160 (bf16) k-blocks, so every CTA holds a piece of it and the tile's first CTA adds 151
+# partials; a tile count that is not a multiple of the SMs with short K.
+SK_CASES = [(768, 768, 8192, 1), (200, 136, 4096, 1), (128, 256, 10240, 0), (1000, 776, 328, 0)]
+
+
+@pytest.mark.parametrize("form", [3, 4])
+@pytest.mark.parametrize("ab", ["bf16", "f32"])
+@pytest.mark.parametrize("c", ["f32", "bf16"])
+@pytest.mark.parametrize("acc", [0, 1])
+@pytest.mark.parametrize("M,N,K,ta", SK_CASES)
+def test_matmul_stream_k(form, ab, c, acc, M, N, K, ta, schedule):
+    """Stream-K schedules (3: equal shares of k-block iterations over every SM; 4: tiles × s
+    CTAs, one K slice each): partial tiles pass through workspace slots and flags and are
+    summed in CTA order by each tile's first CTA.  Same bound as the whole-tile schedule,
+    bit-identical on a rerun."""
+    schedule(form)
+    A = synth.normal((K, M) if ta else (M, K), 60, dtype=ab)
+    B = synth.normal((K, N), 61, dtype=ab)
+    C0 = synth.normal((M, N), 62, dtype=c)
+    d = xt.matmul_desc(M, N, K, trans_a=ta, dtype_ab=xt.XT_BF16 if ab == "bf16" else xt.XT_F32,
+                       dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, accumulate=acc, alpha=0.5)
+    Ad, Bd = dev(A, ab), dev(B, ab)
+    ws = xt.matmul_workspace(d)
+    outs = []
+    for _ in range(2):
+        Cd = dev(C0, c)
+        codes = schedules_of(lambda: xt.xt_matmul_fwd(d, Ad, Bd, Cd, ws=ws))
+        assert len(codes) == 1 and (codes[0] == 1000 if form == 3 else codes[0] > 1000), codes
+        outs.append(host(Cd))
+    want = (C0 if acc else 0) + 0.5 * (op(A, ta) @ B)
+    tol = bound(ab, c) if (c == "f32" or not acc) else 8e-3
+    assert norm_err(outs[0], want) <= tol
+    assert np.array_equal(outs[0], outs[1]), "stream-K is not deterministic"
+    assert xt.device_errors() == 0
+    # the flag words are left zero for the next call
+    assert int(ws[:4096].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("form", [3, 4])
+def test_matmul_stream_k_batched(form, schedule):
+    """Stream-K over batched tiles (outer 2 × inner 3 batches with element strides)."""
+    schedule(form)
+    Bo, Bi, M, N, K = 2, 3, 200, 96, 2048
+    A = synth.normal((Bo, Bi, M, K), 63, dtype="bf16")
+    B = synth.normal((Bo, Bi, K, N), 64, dtype="bf16")
+    Cd = torch.empty((Bo, Bi, M, N), dtype=torch.float32, device="cuda")
+    d = xt.matmul_desc(M, N, K, batch_outer=Bo, batch_inner=Bi,
+                       strides=(Bi * M * K, M * K, Bi * K * N, K * N, Bi * M * N, M * N))
+    codes = schedules_of(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), Cd))
+    assert len(codes) == 1 and (codes[0] == 1000 if form == 3 else codes[0] > 1000), codes
+    assert norm_err(host(Cd), A @ B) <= 1e-5
+    assert xt.device_errors() == 0
+
+
+@pytest.mark.parametrize("M,N,K,tb", [(8192, 768, 3072, 0), (3072, 768, 8192, 0), (8192, 768, 2304, 1)])
+def test_matmul_model_schedule_full_size(M, N, K, tb):
+    """The 12-layer stack's shapes under the time model's own choice (a stream-K form for
+    these), checked on sampled rows against the oracle product of those rows."""
+    A = synth.normal((M, K), 65, std=0.5, dtype="bf16")
+    B = synth.normal((N, K) if tb else (K, N), 66, std=0.02, dtype="bf16")
+    Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    d = xt.matmul_desc(M, N, K, trans_b=tb, dtype_c=xt.XT_BF16)
+    Ad, Bd = dev(A, "bf16"), dev(B, "bf16")
+    codes = schedules_of(lambda: xt.xt_matmul_fwd(d, Ad, Bd, Cm))
+    assert len(codes) == 1 and codes[0] >= 1000, codes
+    rows = np.random.default_rng(1).choice(M, 24, replace=False)
+    rows = np.concatenate([rows, [0, 127, 128, M - 1]])
+    want = A[rows] @ op(B, tb)
+    assert norm_err(host(Cm[torch.tensor(rows, device="cuda")]), want) <= 4e-3
+    assert xt.device_errors() == 0
+
+
+def test_gemm_set_schedule_rejects():
+    with pytest.raises(xt.XtError):
+        xt.gemm_set_schedule(5)
 
 
 GELU_CASES = [(200, 320, 72), (1000, 768, 328), (256, 3072, 768), (128, 64, 64)]

@@ -70,7 +70,8 @@ class NativeBlock:
         self.params = self._params_struct()
         nbytes = C.c_size_t(0)
         xt.call("xt_block_workspace_size", C.byref(self.c), C.byref(nbytes))
-        self.ws = torch.empty(int(nbytes.value), dtype=torch.uint8, device=self.device)
+        # zero-filled: the matmul scratch inside it starts with stream-K flag words
+        self.ws = torch.zeros(int(nbytes.value), dtype=torch.uint8, device=self.device)
         self.loss = torch.zeros(1, dtype=torch.float32, device=self.device)
 
     # -------------------------------------------------------------------------- structs

@@ -195,6 +195,9 @@ int carve(const Dims& m, void* base, Bufs& b) {
   Arena a{static_cast<char*>(base)};
   const int64_t T = m.T, d = m.d, e = m.e;
   const size_t act = size_t(T * d * e);
+  // the matmul scratch first: its leading stream-K flag words are the workspace's first bytes
+  b.ws_mm_bytes = max_matmul_ws(m);
+  b.ws_mm = a.take(b.ws_mm_bytes);
   b.h_in.resize(m.L); b.x1.resize(m.L); b.qkv.resize(m.L); b.P.resize(m.L); b.o.resize(m.L);
   b.h_mid.resize(m.L); b.x2.resize(m.L); b.up.resize(m.L); b.mact.resize(m.L);
   b.st1.resize(m.L); b.st2.resize(m.L); b.o_lo.assign(m.L, nullptr);
@@ -241,8 +244,6 @@ int carve(const Dims& m, void* base, Bufs& b) {
   b.ws_norm = a.take(nb);
   b.ws_ce = a.take(cb);
   b.ws_emb = a.take(eb);
-  b.ws_mm_bytes = max_matmul_ws(m);
-  b.ws_mm = a.take(b.ws_mm_bytes);
   b.total = a.off + 256;
   return XT_OK;
 }

@@ -2,6 +2,7 @@
 // matmul C ABI ([AE] op table row matmul: C = A@B; dA = d@Bᵀ, dB = Aᵀ@d).
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -63,14 +64,31 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn) {
   return XT_OK;
 }
 
-// Tile width and K split from a per-tile time model: rounds of persistent CTAs × the time of
-// one tile at the SM's share of the tensor peak, scaled by the measured relative efficiency of
-// the tile width (narrow tiles move more operand bytes per FLOP), plus for a K split the
-// fixed-order reduction of the partial slices.  The split is used for single-batch,
-// non-causal problems whose tile count leaves SMs idle (the M = d weight gradients).
+// Tile width, K split and schedule from a per-tile time model: rounds of persistent CTAs × the
+// time of one tile at the SM's share of the tensor peak, scaled by the measured relative
+// efficiency of the tile width (narrow tiles move more operand bytes per FLOP), plus for a K
+// split the fixed-order reduction of the partial slices by a second kernel.  Two stream-K
+// forms (in-kernel fixup, one partial tile written and read per shared tile piece):
+//   - over every SM: each CTA an equal share of the k-block iterations, so no SM idles in a
+//     last round; the CTAs sit at staggered K offsets, so only when the operands stay
+//     resident in L2 (≤ 80 MB);
+//   - lockstep K slices: tiles × s CTAs (≤ the SMs), each one K slice of one tile, every CTA
+//     at the same K offsets as the others of its slice (operand tiles shared through L2 as
+//     by whole tiles).
+// Splits and stream-K need a workspace and a non-causal problem; the K split one batch.
 static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 192 ? 0.77 : bn >= 128 ? 0.64 : 0.35; }
 
+// Schedule override (xt_gemm_set_schedule): 0 the model's choice, 1 whole tiles only, 2 a K
+// split where one is allowed, 3 stream-K over every SM where allowed, 4 stream-K in lockstep
+// K slices where allowed.
+static int g_schedule = 0;
+
+// Fixup time of a stream-K tile shared by `parts` CTAs: one latency plus one pass per partial.
+static double sk_fixup_time(int64_t parts) { return 0.7e-6 + 0.8e-6 * double(parts - 1); }
+
 Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split) {
+  const int mode = allow_split ? g_schedule : 1;
+  if (mode == 1) allow_split = false;
   const int cands_bf16[4] = {64, 128, 192, 256};
   const int cands_tf32[2] = {64, 128};
   const int* c = tf32 ? cands_tf32 : cands_bf16;
@@ -78,30 +96,58 @@ Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int c
   const int sms = num_sms();
   const int bk = tf32 ? 32 : 64;
   const double per_sm = tf32 ? 5.6e12 : 11.2e12;
-  Choice best{c[0], 1};
+  const double e = tf32 ? 4.0 : 2.0;
+  Choice best{c[0], 1, 0, 0};
   double best_t = 1e300;
+  const int64_t kbt = ceil_div(K, bk);
+  const bool sk_ok = allow_split && causal == 0 && sms <= kSkMaxCtas;
+  // forced modes: the forced kind of candidate first, whole tiles when it is not allowed
+  auto weigh = [&](double t, int kind) {  // kind 1 tiles, 2 K split, 3 stream-K all SMs, 4 lockstep
+    if (mode >= 2) t *= (kind == mode) ? 1e-6 : (kind == 1 ? 1.0 : 1e6);
+    return t;
+  };
+  auto offer = [&](double t, Choice ch) {
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = ch;
+    }
+  };
   for (int i = 0; i < nc; ++i) {
     const int bn = c[i];
     if (i > 0 && c[i - 1] >= N) break;  // wider tiles only add padding
     int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn) * batches;
     if (causal == 1) tiles = (tiles + 1) / 2;
+    const double t_kb = 2.0 * BM * bn * bk / (per_sm * tile_eff(bn));
     for (int s = 1; s <= 8; s *= 2) {
       if (s > 1 && (!allow_split || batches != 1 || causal != 0 || N % 4 != 0)) break;
-      if (s > 1 && ceil_div(K, bk) < 4 * s) break;
+      if (s > 1 && kbt < 4 * s) break;
       const double rounds = double(ceil_div(tiles * s, sms));
       const double t_tile = 2.0 * BM * bn * (double(K) / s) / (per_sm * tile_eff(bn)) + 1.5e-6;
       double t = rounds * t_tile;
       if (s > 1) t += double(s + 1) * double(M) * double(N) * 4.0 / 5e12 + 4e-6;
-      if (t < best_t * 0.999) {
-        best_t = t;
-        best = Choice{bn, s};
-      }
+      offer(weigh(t, s > 1 ? 2 : 1), Choice{bn, s, 0, 0});
+    }
+    if (!sk_ok) continue;
+    const int64_t iters = tiles * kbt;
+    const double operands = double(M + N) * double(batches) * double(K) * e;
+    if (iters >= sms && tiles % sms != 0 && (operands <= 80e6 || mode == 3)) {
+      const double share = double(iters) / sms;
+      const int64_t parts = int64_t(std::ceil(double(kbt) / share)) + 1;
+      // + 6.5 µs: the measured cost per launch beyond the model (staggered tiles, partial
+      // stores, the exposed fixup), fitted on 8192-row shapes with K 768 to 3072
+      const double t = std::ceil(share) * t_kb + (double(tiles) / sms + 1.0) * 1.5e-6 + sk_fixup_time(parts) + 6.5e-6;
+      offer(weigh(t, 3), Choice{bn, 1, 1, sms});
+    }
+    for (int64_t sl = 2; sl <= 8 && tiles * sl <= sms && kbt >= 2 * sl; ++sl) {
+      const double t = double(ceil_div(kbt, sl)) * t_kb + 1.5e-6 + sk_fixup_time(sl);
+      offer(weigh(t, 4), Choice{bn, 1, 2, int(tiles * sl)});
     }
   }
   return best;
 }
 
 size_t split_bytes(const Choice& c, int64_t M, int64_t N) {
+  if (c.sk) return size_t(c.grid) * BM * size_t(c.bn) * 4;
   if (c.splits <= 1) return 0;
   return (size_t(c.splits) * size_t(M) * size_t(N) * 4 + 255) & ~size_t(255);
 }
@@ -152,9 +198,10 @@ int run(const Problem& pb, cudaStream_t s) {
   const bool tf32 = pb.tf32;
   const int64_t batches = int64_t(pb.batch_outer) * pb.batch_inner;
   Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, pb.act == 0);
-  if (ch.splits > 1 && (pb.split_ws == nullptr || split_bytes(ch, pb.M, pb.N) > pb.split_ws_bytes))
+  if ((ch.splits > 1 || ch.sk) && (pb.split_ws == nullptr || split_bytes(ch, pb.M, pb.N) > pb.split_ws_bytes ||
+                                   (ch.sk && pb.sk_flags == nullptr)))
     ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false);
-  if (pb.act) ch = Choice{256, 1};  // the GELU epilogues are built for BN 256 only
+  if (pb.act) ch = Choice{256, 1, 0, 0};  // the GELU epilogues are built for BN 256 only
   const int bn = ch.bn;
   const bool split = ch.splits > 1;
   CUtensorMap ta, tb, tc, tc2;
@@ -199,6 +246,14 @@ int run(const Problem& pb, cudaStream_t s) {
   if (tiles > int64_t(1) << 30) return fail(XT_ERR_UNSUPPORTED, "matmul: too many tiles");
   int grid = int(tiles < num_sms() ? tiles : num_sms());
   if (grid < 1) grid = 1;
+  if (ch.sk) {
+    p.sk = 1;
+    p.kb_tile = int(ceil_div(pb.K, tf32 ? 32 : 64));
+    p.sk_iters = tiles * p.kb_tile;
+    p.sk_part = static_cast<float*>(pb.split_ws);
+    p.sk_flag = pb.sk_flags;
+    grid = ch.grid;  // ≤ the SMs and ≤ the iterations: every CTA resident, every share non-empty
+  }
   const bool amn = pb.A.mn_major, bmn = pb.B.mn_major;
   // algorithmic FLOPs: the unmasked work only for the causal modes
   const double nb = double(batches);  // problem batches (a K split does not add work)
@@ -206,7 +261,10 @@ int run(const Problem& pb, cudaStream_t s) {
   if (pb.causal == 1) flops = 2.0 * double(pb.K) * double(pb.M) * double(pb.M + 1) / 2.0 * nb;
   if (pb.causal >= 2) flops = 2.0 * double(pb.N) * double(pb.M) * double(pb.M + 1) / 2.0 * nb;
   void* tok = nullptr;
+  // record: causal mode, or 10 × K splits, or 1000 for stream-K over every SM, 1000 + slices
+  // for stream-K in lockstep K slices
   const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, bn, int(amn), int(bmn),
+                        ch.sk == 1 ? 1000 : ch.sk == 2 ? 1000 + int(ch.grid / tiles) :
                         split ? 10 * ch.splits : p.causal};
   const bool prof = gemm_profile_begin(s, flops, shape, &tok);
   int st = tf32      ? launch_tf32(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
@@ -295,9 +353,11 @@ static gemm::Operand operand_b(const xt_matmul_desc* d, const void* B) {
                        d->batch_inner, d->batch_outer};
 }
 
+// Workspace: the stream-K flag words (zero between calls), then fp32 staging copies, then
+// K-split or stream-K partial tiles.
 static size_t matmul_ws(const xt_matmul_desc* d) {
   if (d->M == 0 || d->N == 0 || d->K == 0) return 0;
-  size_t b = 0;
+  size_t b = gemm::kSkFlagBytes;
   if (d->dtype_ab == XT_F32) b += stage_bytes(operand_a(d, nullptr)) + stage_bytes(operand_b(d, nullptr));
   const gemm::Choice ch = gemm::choose(d->dtype_ab == XT_F32, d->M, d->N, d->K,
                                        int64_t(d->batch_outer) * d->batch_inner, d->causal, true);
@@ -362,6 +422,14 @@ static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, voi
   pb.B = operand_b(d, B);
   char* w = static_cast<char*>(ws);
   size_t left = ws ? ws_bytes : 0;
+  pb.sk_flags = nullptr;
+  if (left >= gemm::kSkFlagBytes) {
+    pb.sk_flags = reinterpret_cast<uint32_t*>(w);
+    w += gemm::kSkFlagBytes;
+    left -= gemm::kSkFlagBytes;
+  } else {
+    left = 0;  // too small to hold the flags: no workspace is used
+  }
   if (pb.tf32 && (pb.A.mn_major || pb.B.mn_major)) {
     XT_REQUIRE(ws != nullptr, "matmul: fp32 operands read MN-major need a workspace");
     if (pb.A.mn_major) XT_TRY(stage_operand(pb.A, w, left, s));
@@ -388,6 +456,12 @@ static int matmul_run(const xt_matmul_desc* d, const void* A, const void* B, voi
 using namespace xt;
 
 extern "C" {
+
+int xt_gemm_set_schedule(int mode) {
+  XT_REQUIRE(mode >= 0 && mode <= 4, "xt_gemm_set_schedule: mode must be 0..4");
+  gemm::g_schedule = mode;
+  return XT_OK;
+}
 
 int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes) {
   XT_REQUIRE(desc && bytes, "xt_matmul_workspace_size: NULL pointer");

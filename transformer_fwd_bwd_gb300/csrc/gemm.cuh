@@ -31,20 +31,27 @@ struct Problem {
   float alpha;
   int accumulate;
   int causal;
-  void* split_ws;  // room for K-split partial tiles (may be null)
+  void* split_ws;  // room for K-split or stream-K partial tiles (may be null)
   size_t split_ws_bytes;
+  uint32_t* sk_flags;  // kSkFlagBytes of stream-K flag words, zero between calls (null: no stream-K)
   int act;         // GELU epilogue (see Params::act); 0 none
   void* C2;        // act 1: gelu(C), C's layout
   const void* aux; // act 2: the pre-activation, C's layout
 };
 
-// Tile width and K split chosen for a problem (see choose()).
+// Tile width, K split and schedule chosen for a problem (see choose()).
 struct Choice {
   int bn;
   int splits;
+  int sk;    // stream-K schedule: 1 over every SM, 2 in lockstep K slices
+  int grid;  // stream-K CTAs: the SMs, or tiles × K slices (lockstep)
 };
 Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split);
 size_t split_bytes(const Choice& c, int64_t M, int64_t N);
+
+// Stream-K flag words at the head of every matmul workspace: 4 per CTA for up to kSkMaxCtas CTAs.
+constexpr int kSkMaxCtas = 256;
+constexpr size_t kSkFlagBytes = size_t(kSkMaxCtas) * 4 * sizeof(uint32_t);
 
 int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn);
 // The driver's cuTensorMapEncodeTiled (null when the driver does not provide it).

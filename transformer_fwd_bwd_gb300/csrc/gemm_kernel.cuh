@@ -44,6 +44,19 @@ struct Params {
   const bf16* aux;
   int64_t ld_aux;
   uint32_t* flag;
+  // Stream-K schedule (sk = 1): CTA c computes the k-block iterations [⌊c·I/G⌋, ⌊(c+1)·I/G⌋) of
+  // the tiles × kb_tile iteration space (I = sk_iters ≥ G = gridDim.x ≤ the SMs), so every CTA
+  // does the same amount of MMA work whatever the tile count (G = the SMs), or every CTA one
+  // K slice of one tile with all CTAs at the same K offsets (G = tiles × slices).  A CTA whose share starts inside a tile
+  // writes that piece's raw fp32 accumulator to slot c of sk_part ([G][BM·BN] floats) and sets
+  // sk_flag[4c + q] = tile + 1 for each TMEM lane quadrant q; the CTA that computes the tile's
+  // first k-blocks (the last piece of its own share) waits for those flags, adds the slots in
+  // CTA order (a fixed order: deterministic), clears the flags and stores C.
+  int sk;
+  int kb_tile;
+  int64_t sk_iters;
+  float* sk_part;
+  uint32_t* sk_flag;
 };
 
 // ------------------------------------------------------------------------------ PTX wrappers
@@ -119,6 +132,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
@@ -274,6 +296,80 @@ __device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
   return ti;
 }
 
+// The pieces (tile, k-block range) a CTA computes, in order: whole tiles blockIdx.x + i·gridDim.x,
+// or under stream-K the parts of the tiles its contiguous share of iterations covers.
+struct Cursor {
+  int64_t it, end;
+};
+__device__ __forceinline__ Cursor cursor_begin(const Params& p) {
+  Cursor c;
+  if (p.sk) {
+    c.it = int64_t(blockIdx.x) * p.sk_iters / gridDim.x;
+    c.end = int64_t(blockIdx.x + 1) * p.sk_iters / gridDim.x;
+  } else {
+    c.it = blockIdx.x;
+    c.end = 0;
+  }
+  return c;
+}
+// Next piece, false when none is left; kb0 = kb1 = -1 for a whole tile of the plain schedule.
+__device__ __forceinline__ bool cursor_next(Cursor& c, const Params& p, int total, int& t, int& kb0, int& kb1) {
+  if (!p.sk) {
+    if (c.it >= total) return false;
+    t = int(c.it);
+    c.it += gridDim.x;
+    kb0 = kb1 = -1;
+    return true;
+  }
+  if (c.it >= c.end) return false;
+  t = int(c.it / p.kb_tile);
+  kb0 = int(c.it - int64_t(t) * p.kb_tile);
+  const int64_t room = c.end - c.it;
+  kb1 = room < int64_t(p.kb_tile - kb0) ? kb0 + int(room) : p.kb_tile;
+  c.it += kb1 - kb0;
+  return true;
+}
+// Stream-K: the CTA whose share holds iteration x, i.e. the largest c with ⌊c·I/G⌋ ≤ x.
+__device__ __forceinline__ int sk_cta_of(int64_t x, const Params& p) {
+  return int(((x + 1) * int64_t(gridDim.x) - 1) / p.sk_iters);
+}
+
+// Stream-K fixup of a tile's accumulator in TMEM (columns tacc .. tacc + BN of this warp's
+// lanes): adds the partial accumulators of CTAs first..last, in CTA order, 32 columns at a
+// time (tcgen05.ld, add, tcgen05.st), with the loads of the group two ahead in flight.  Slot
+// layout: float4 (g·8 + j)·BM + row holds columns 32·g + 4·j .. +4 of the row, so a warp's
+// loads and stores each cover 512 contiguous bytes.
+template <int BN>
+__device__ __forceinline__ void sk_fixup(uint32_t tacc, const Params& p, int first, int last, int row) {
+  constexpr int NG = BN / 32;
+  for (int cc = first; cc <= last; ++cc) {
+    const float4* src = reinterpret_cast<const float4*>(p.sk_part) + size_t(cc) * (BM * BN / 4) + row;
+    float4 v[2][8];
+#pragma unroll
+    for (int g = 0; g < 2 && g < NG; ++g)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[g][j] = __ldcg(src + size_t(g * 8 + j) * BM);
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      uint32_t a[32];
+      tmem_ld32(tacc + uint32_t(g * 32), a);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        a[4 * j] = __float_as_uint(__uint_as_float(a[4 * j]) + v[g & 1][j].x);
+        a[4 * j + 1] = __float_as_uint(__uint_as_float(a[4 * j + 1]) + v[g & 1][j].y);
+        a[4 * j + 2] = __float_as_uint(__uint_as_float(a[4 * j + 2]) + v[g & 1][j].z);
+        a[4 * j + 3] = __float_as_uint(__uint_as_float(a[4 * j + 3]) + v[g & 1][j].w);
+      }
+      if (g + 2 < NG)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[g & 1][j] = __ldcg(src + size_t((g + 2) * 8 + j) * BM);
+      tmem_st32(tacc + uint32_t(g * 32), a);
+    }
+    tmem_st_wait();
+  }
+}
+
 // ACT: the epilogue's GELU mode (Params::act), a template parameter so the plain GEMMs carry
 // none of its code.
 template <bool TF32, int BN, bool A_MN, bool B_MN, int ACT = 0>
@@ -327,12 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int total = p.num_m * p.num_n * p.batches;
 
-  auto info = [&](int t) {
+  auto info = [&](int t, int kb0, int kb1) {
     TileInfo ti = tile_info<BK>(t, p);
     const int per = p.num_m * p.num_n;
     const int r = t - (t / per) * per;
     ti.n0 = (r / p.num_m) * BN;
     if (p.causal == 1 && ti.n0 >= ti.m0 + BM) ti.skip = true;
+    if (kb0 >= 0) {  // a stream-K piece
+      ti.kb_begin = kb0;
+      ti.kb_end = kb1;
+    }
     return ti;
   };
 
@@ -347,8 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = info(t);
+      Cursor cur = cursor_begin(p);
+      int t, kb0, kb1;
+      while (!*abort_flag && cursor_next(cur, p, total, t, kb0, kb1)) {
+        const TileInfo ti = info(t, kb0, kb1);
         if (ti.skip) continue;
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
           if (*abort_flag) break;
@@ -391,8 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int ab = 0;
       uint32_t aphase = 0;
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const TileInfo ti = info(t);
+      Cursor cur = cursor_begin(p);
+      int t, kb0, kb1;
+      while (!*abort_flag && cursor_next(cur, p, total, t, kb0, kb1)) {
+        const TileInfo ti = info(t, kb0, kb1);
         if (ti.skip || ti.kb_end <= ti.kb_begin) continue;
         if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1)) { give_up(); break; }
         tc_fence_after();
@@ -426,12 +530,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aphase = 0;
     uint32_t chunk = 0;  // staged stores issued by this warp (selects the staging buffer)
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    Cursor cur = cursor_begin(p);
+    int t, kb0, kb1;
+    while (cursor_next(cur, p, total, t, kb0, kb1)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const TileInfo ti = info(t);
+      const TileInfo ti = info(t, kb0, kb1);
       if (ti.skip) continue;
       const int row = ti.m0 + q * 32 + lane;
       const bool empty_k = ti.kb_end <= ti.kb_begin;
+      // stream-K piece kind: 1 = a later part of the tile (partial to its slot), 2 = the tile's
+      // first k-blocks with later parts in CTAs blockIdx.x + 1 .. sk_last (adds their partials)
+      const int kind = kb0 > 0 ? 1 : (kb0 == 0 && kb1 < p.kb_tile) ? 2 : 0;
       if (!empty_k) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[ab]), aphase));
         if (!ok) {
@@ -439,6 +548,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+      }
+      if (kind == 1) {
+        float4* slot = reinterpret_cast<float4*>(p.sk_part) + size_t(blockIdx.x) * (BM * BN / 4);
+        const int rowt = q * 32 + lane;
+#pragma unroll 1
+        for (int g = 0; g < BN / 32; ++g) {
+          uint32_t r[32];
+          tmem_ld32(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN + g * 32), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            slot[size_t(g * 8 + j) * BM + rowt] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+        if (++ab == 2) { ab = 0; aphase ^= 1; }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, uint32_t(t + 1));
+        continue;
+      }
+      int sk_last = 0;
+      if (kind == 2) {
+        sk_last = sk_cta_of(int64_t(t) * p.kb_tile + p.kb_tile - 1, p);
+        bool ok = true;
+        for (int cc = blockIdx.x + 1; cc <= sk_last && ok; ++cc) {
+          const uint32_t* f = p.sk_flag + cc * 4 + q;
+          if (ld_acquire_gpu(f) != uint32_t(t + 1)) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(f) != uint32_t(t + 1))
+              if (globaltimer() - t0 > kTimeoutNs) { ok = false; break; }
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) give_up();
+          break;
+        }
+        // the flags are this launch's alone until it completes: clear them for the next one
+        if (lane == 0)
+          for (int cc = blockIdx.x + 1; cc <= sk_last; ++cc) p.sk_flag[cc * 4 + q] = 0u;
+        // the later parts' sums join this piece's accumulator in TMEM; the store paths below
+        // then read the tile's full sum
+        sk_fixup<BN>(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN), p, blockIdx.x + 1, sk_last, q * 32 + lane);
       }
       if (p.tma_store) {
         // ---- staged TMA stores: chunk = 32 rows × 128 bytes (32 fp32 or 64 bf16 columns)

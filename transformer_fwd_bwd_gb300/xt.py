@@ -121,6 +121,7 @@ _SIGS = {
     "xt_embedding_fwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _VP],
     "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
     "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
+    "xt_gemm_set_schedule": [_I],
     "xt_matmul_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_gelu_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_gelu_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, C.c_size_t, _VP],
@@ -232,7 +233,14 @@ def ws_bytes(name, *args) -> int:
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    """Zero-filled scratch (the matmul workspace's flag words must start at zero)."""
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def gemm_set_schedule(mode: int):
+    """0 model's choice, 1 whole tiles, 2 K split, 3 stream-K over every SM, 4 stream-K in
+    lockstep K slices (2-4 where allowed)."""
+    call("xt_gemm_set_schedule", int(mode))
 
 
 def device_errors(s=None) -> int:
@@ -507,6 +515,12 @@ def matmul_desc(M, N, K, *, trans_a=0, trans_b=0, lda=None, ldb=None, ldc=None, 
     (d.stride_a_outer, d.stride_a_inner, d.stride_b_outer, d.stride_b_inner,
      d.stride_c_outer, d.stride_c_inner) = strides
     return d
+
+
+def matmul_workspace(desc, device="cuda"):
+    """A zero-filled workspace of the size xt_matmul_workspace_size reports (None if 0)."""
+    n = ws_bytes("xt_matmul_workspace_size", C.byref(desc))
+    return workspace(n, device) if n else None
 
 
 def xt_matmul_fwd(desc, A, B, Cm, ws=None, s=None):
