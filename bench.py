@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
+    ap.add_argument("--recompute", action="store_true",
+                    help="activation recompute: keep each layer's input only, redo its forward in the backward")
     ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy"], default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
     ap.add_argument("--sweep", action="store_true",
@@ -242,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
     __graft_entry__.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cfg = dict(synth.BLOCK_CONFIGS[args.workload])
+    cfg = dict(synth.BLOCK_CONFIGS[args.workload], recompute=int(args.recompute))
     T = cfg["B"] * cfg["S"]
     nb = NativeBlock(cfg, device=dev, training=True, base_seed=synth.BASE_SEED_DROPOUT)
     nb.load(synth.block_params(cfg))
@@ -367,6 +369,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic (seeded tokens, N(0,0.02) weights)",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "model": args.workload, "global_batch": world * cfg["B"],
                    "seq_len": cfg["S"], "parallelism": f"replicas x{world} (data parallel, no collective)",
+                   "activation_recompute": bool(args.recompute), "workspace_gb": round(nb.ws.numel() / 1e9, 3),
                    "l2": "inputs larger than L2 (weights 85M params + GBs of saved activations per step)",
                    "loss": loss},
         "e2e": {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(2 * T * 4),
@@ -440,7 +443,8 @@ def run_kernel(args):
         o_lo = torch.empty(B * S, d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
         dqkv = torch.empty_like(qkv)
-        ws = torch.empty(B * H * S * 4 + 256, dtype=torch.uint8, device=dev)
+        nws = xt.ws_bytes("xt_attention_bwd_workspace_size", B, S, H)
+        ws = torch.empty(max(1, nws), dtype=torch.uint8, device=dev)
         q, k, v = qkv[:, :d], qkv[:, d:2 * d], qkv[:, 2 * d:]
         fwd_us = timed(lambda: xt.xt_attention_fwd(q, k, v, o, lse, B, S, H, hd, 1, o_lo=o_lo))
         bwd_us = timed(lambda: xt.xt_attention_bwd(q, k, v, o, dO, lse, dqkv[:, :d], dqkv[:, d:2 * d],

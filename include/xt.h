@@ -430,6 +430,11 @@ typedef struct xt_block_config {
   double rope_base;
   uint64_t base_seed;
   int32_t attention;  /* XT_ATTN_AUTO, XT_ATTN_COMPOSED or XT_ATTN_FUSED */
+  int32_t recompute;  /* 1: activation recompute — the workspace keeps each layer's input only
+                         and the backward recomputes the layer's forward (norm, projections,
+                         attention, activation) from it before its backward; the recomputed
+                         values are the forward's bit for bit (same kernels, same inputs,
+                         counter-based dropout), so are the gradients; 0: keep everything */
 } xt_block_config;
 
 /* Per-layer parameter (and gradient) pointers; arrays of n_layers device pointers,

@@ -69,3 +69,22 @@ def test_host_validation(xt):
     assert L.xt_embedding_workspace_size(1000, C.byref(sz)) == 0 and sz.value == 8000
     assert L.xt_sum_workspace_size(-1, C.byref(sz)) == xt.XT_ERR_INVALID_ARG
     assert xt.version().startswith("xt")
+
+
+def test_block_recompute_workspace_and_validation(xt):
+    """The recompute option keeps one layer's activations instead of every layer's: the block
+    workspace shrinks by about (n_layers − 1) layers' worth; modes other than 0/1 are rejected."""
+    import synth
+    from transformer_fwd_bwd_gb300.block import config_struct
+    L = xt.lib()
+    cfg = dict(synth.BLOCK_CONFIGS["gpt12"])
+    sizes = {}
+    for rc in (0, 1):
+        c = config_struct(dict(cfg, recompute=rc))
+        n = C.c_size_t(0)
+        assert L.xt_block_workspace_size(C.byref(c), C.byref(n)) == 0
+        sizes[rc] = n.value
+    assert sizes[1] < sizes[0] * 0.7, sizes
+    c = config_struct(dict(cfg, recompute=2))
+    n = C.c_size_t(0)
+    assert L.xt_block_workspace_size(C.byref(c), C.byref(n)) == xt.XT_ERR_INVALID_ARG

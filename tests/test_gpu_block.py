@@ -175,3 +175,21 @@ def test_block_graph_replay_matches_eager(cfg):
             assert np.array_equal(ga[k], gb[k]), k
     del g
     xt.profile_gemm(0)
+
+
+@pytest.mark.parametrize("cfg", [variant("block256", n_layers=2), variant("block256", dtype="bf16", n_layers=2),
+                                 variant("gpt12", B=2, S=256, d=128, H=2, hd=64, F=512, V=1000, n_layers=3)],
+                         ids=["fp32-composed-rope-swiglu-dropout", "bf16-fused", "bf16-ln-gelu-3layers"])
+def test_block_recompute_bit_identical(cfg):
+    """Activation recompute (keep each layer's input, redo the layer's forward in the backward;
+    [DO] § RNG：counter-based … 与重计算兼容 requires the recomputed dropout masks to be the
+    forward's): the workspace shrinks and the loss and every gradient are bit-identical to the
+    run that keeps all activations (same kernels on the same inputs, masks from their counters)."""
+    params = synth.block_params(cfg)
+    ids, tgt = synth.block_tokens(cfg)
+    l0, g0, nb0 = run_native(cfg, params, ids, tgt)
+    l1, g1, nb1 = run_native(dict(cfg, recompute=1), params, ids, tgt)
+    assert nb1.ws.numel() <= nb0.ws.numel() and (cfg["n_layers"] == 1 or nb1.ws.numel() < nb0.ws.numel())
+    assert l0 == l1
+    for k in g0:
+        assert np.array_equal(g0[k], g1[k]), k

@@ -34,6 +34,7 @@ def config_struct(cfg: dict, training: bool = True, base_seed: int = 0, grad_dty
     c.base_seed = base_seed & (2**64 - 1)
     c.attention = {"auto": xt.XT_ATTN_AUTO, "composed": xt.XT_ATTN_COMPOSED,
                    "fused": xt.XT_ATTN_FUSED}[cfg.get("attention", "auto")]
+    c.recompute = int(cfg.get("recompute", 0))
     return c
 
 

@@ -39,7 +39,8 @@ struct Dims {
   int64_t B, S, d, H, hd, F, V, L, T, UP, e;
   int dt, gdt;
   bool rms, swiglu;
-  bool fused;  // attention through xt_attention_fwd / xt_attention_bwd
+  bool fused;      // attention through xt_attention_fwd / xt_attention_bwd
+  bool recompute;  // layer activations recomputed in the backward from the layer input
 };
 
 bool fused_supported(const xt_block_config& c) { return c.dtype == XT_BF16 && c.hd == 64 && c.d % 8 == 0; }
@@ -55,6 +56,7 @@ Dims dims_of(const xt_block_config& c) {
   m.gdt = c.grad_dtype;
   m.e = int64_t(dtype_size(c.dtype));
   m.fused = c.attention == XT_ATTN_FUSED || (c.attention == XT_ATTN_AUTO && fused_supported(c));
+  m.recompute = c.recompute != 0;
   return m;
 }
 
@@ -201,8 +203,16 @@ int carve(const Dims& m, void* base, Bufs& b) {
   b.h_in.resize(m.L); b.x1.resize(m.L); b.qkv.resize(m.L); b.P.resize(m.L); b.o.resize(m.L);
   b.h_mid.resize(m.L); b.x2.resize(m.L); b.up.resize(m.L); b.mact.resize(m.L);
   b.st1.resize(m.L); b.st2.resize(m.L); b.o_lo.assign(m.L, nullptr);
+  // With recompute every layer but its input shares one set of activation buffers: the forward
+  // overwrites them layer by layer and the backward refills them for the layer it is at.
   for (int64_t l = 0; l < m.L; ++l) {
     b.h_in[l] = a.take(act);
+    if (m.recompute && l > 0) {
+      b.x1[l] = b.x1[0]; b.st1[l] = b.st1[0]; b.qkv[l] = b.qkv[0]; b.P[l] = b.P[0]; b.o[l] = b.o[0];
+      b.o_lo[l] = b.o_lo[0]; b.h_mid[l] = b.h_mid[0]; b.x2[l] = b.x2[0]; b.st2[l] = b.st2[0];
+      b.up[l] = b.up[0]; b.mact[l] = b.mact[0];
+      continue;
+    }
     b.x1[l] = a.take(act);
     b.st1[l] = static_cast<float*>(a.take(size_t(2 * T) * 4));
     b.qkv[l] = a.take(size_t(T * 3 * d * e));
@@ -261,6 +271,7 @@ int validate(const xt_block_config* c) {
   XT_REQUIRE(c->p >= 0.f && c->p < 1.f, "block: dropout p must be in [0, 1)");
   XT_REQUIRE(int64_t(c->B) * c->S <= 16384, "block: B·S above 16384 tokens is not supported");
   XT_REQUIRE(c->attention >= XT_ATTN_AUTO && c->attention <= XT_ATTN_FUSED, "block: bad attention mode");
+  XT_REQUIRE(c->recompute == 0 || c->recompute == 1, "block: recompute must be 0 or 1");
   if (c->attention == XT_ATTN_FUSED && !fused_supported(*c))
     return fail(XT_ERR_UNSUPPORTED, "block: fused attention needs bf16, head_dim 64 and d a multiple of 8");
   return XT_OK;
@@ -319,6 +330,42 @@ int norm_bwd(const Dims& m, const void* dy, const void* x, const void* g, const 
                           stream);
 }
 
+// Layer l's forward from its input up to the MLP activation (x1 … mact), into the layer's
+// buffers.  The forward forms x1 = norm1(h_in) in the previous layer's fused add + norm (or, for
+// layer 0, before the loop); the recompute (with_norm1) forms it here with the plain norm,
+// which gives the same bits (the fused pass normalises the stored sum).
+int layer_front(const xt_block_config& c, const Dims& m, const xt_block_params* prm, const Bufs& b, int64_t l,
+                bool with_norm1, void* stream) {
+  cudaStream_t s = as_stream(stream);
+  const int64_t T = m.T, d = m.d, e = m.e;
+  const bool drop = c.training && c.p > 0.f;
+  if (with_norm1)
+    XT_TRY(norm_fwd(c, m, b.h_in[l], prm->g1[l], prm->b1 ? prm->b1[l] : nullptr, b.x1[l], b.st1[l], stream));
+  // attention sub-block
+  XT_TRY(matmul(lin_fwd(m, d, 3 * d), b.x1[l], prm->Wqkv[l], b.qkv[l], b.ws_mm, b.ws_mm_bytes, s));
+  if (c.rope)  // q and k blocks are 2H consecutive heads of each qkv row
+    XT_TRY(xt_rope_fwd(b.qkv[l], b.qkv[l], b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, stream));
+  if (m.fused) {
+    XT_TRY(xt_attention_fwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.o_lo[l], d,
+                            static_cast<float*>(b.P[l]), int(m.B), int(m.S), int(m.H), int(m.hd), 1, m.dt, stream));
+  } else {
+    XT_TRY(matmul(att_scores(m), b.qkv[l], off(b.qkv[l], d, e), b.P[l], b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(xt_softmax_fwd(b.P[l], b.P[l], m.B * m.H * m.S, m.S, 2, m.S, m.dt, stream));
+    XT_TRY(matmul(att_pv(m), b.P[l], off(b.qkv[l], 2 * d, e), b.o[l], b.ws_mm, b.ws_mm_bytes, s));
+  }
+  XT_TRY(matmul(lin_fwd(m, d, d), b.o[l], prm->Wo[l], b.tmp, b.ws_mm, b.ws_mm_bytes, s));
+  // residual dropout-add, then the MLP sub-block's pre-norm, in one pass
+  XT_TRY(add_norm_fwd(c, m, b.h_in[l], b.tmp, b.h_mid[l], prm->g2[l], prm->b2 ? prm->b2[l] : nullptr, b.x2[l],
+                      b.st2[l], site_seed(c, l, kSiteAttn), drop, stream));
+  // MLP sub-block
+  XT_TRY(matmul(lin_fwd(m, d, m.UP), b.x2[l], prm->W_up[l], b.up[l], b.ws_mm, b.ws_mm_bytes, s));
+  if (m.swiglu)
+    XT_TRY(xt_swiglu_fwd(b.up[l], off(b.up[l], m.F, e), m.UP, b.mact[l], m.F, T, m.F, m.dt, stream));
+  else
+    XT_TRY(xt_gelu_fwd(b.up[l], b.mact[l], T * m.F, m.dt, stream));
+  return XT_OK;
+}
+
 }  // namespace
 }  // namespace xt
 
@@ -345,35 +392,14 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   Bufs b;
   XT_TRY(carve(m, ws, b));
   cudaStream_t s = as_stream(stream);
-  const int64_t T = m.T, d = m.d, e = m.e;
+  const int64_t T = m.T, d = m.d;
   const bool drop = c.training && c.p > 0.f;
   if (c.rope) XT_TRY(xt_rope_table(b.rope, int(m.S), int(m.hd), c.rope_base, 0, stream));
   XT_TRY(xt_embedding_fwd(ids, prm->E, c.learned_pos ? prm->P : nullptr, b.h_in[0], T, int(m.S), d, m.V, m.dt, stream));
   // the first pre-norm; every later one is fused with the residual add before it
   XT_TRY(norm_fwd(c, m, b.h_in[0], prm->g1[0], prm->b1 ? prm->b1[0] : nullptr, b.x1[0], b.st1[0], stream));
   for (int64_t l = 0; l < m.L; ++l) {
-    // attention sub-block
-    XT_TRY(matmul(lin_fwd(m, d, 3 * d), b.x1[l], prm->Wqkv[l], b.qkv[l], b.ws_mm, b.ws_mm_bytes, s));
-    if (c.rope)  // q and k blocks are 2H consecutive heads of each qkv row
-      XT_TRY(xt_rope_fwd(b.qkv[l], b.qkv[l], b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, stream));
-    if (m.fused) {
-      XT_TRY(xt_attention_fwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.o_lo[l], d,
-                              static_cast<float*>(b.P[l]), int(m.B), int(m.S), int(m.H), int(m.hd), 1, m.dt, stream));
-    } else {
-      XT_TRY(matmul(att_scores(m), b.qkv[l], off(b.qkv[l], d, e), b.P[l], b.ws_mm, b.ws_mm_bytes, s));
-      XT_TRY(xt_softmax_fwd(b.P[l], b.P[l], m.B * m.H * m.S, m.S, 2, m.S, m.dt, stream));
-      XT_TRY(matmul(att_pv(m), b.P[l], off(b.qkv[l], 2 * d, e), b.o[l], b.ws_mm, b.ws_mm_bytes, s));
-    }
-    XT_TRY(matmul(lin_fwd(m, d, d), b.o[l], prm->Wo[l], b.tmp, b.ws_mm, b.ws_mm_bytes, s));
-    // residual dropout-add, then the MLP sub-block's pre-norm, in one pass
-    XT_TRY(add_norm_fwd(c, m, b.h_in[l], b.tmp, b.h_mid[l], prm->g2[l], prm->b2 ? prm->b2[l] : nullptr, b.x2[l],
-                        b.st2[l], site_seed(c, l, kSiteAttn), drop, stream));
-    // MLP sub-block
-    XT_TRY(matmul(lin_fwd(m, d, m.UP), b.x2[l], prm->W_up[l], b.up[l], b.ws_mm, b.ws_mm_bytes, s));
-    if (m.swiglu)
-      XT_TRY(xt_swiglu_fwd(b.up[l], off(b.up[l], m.F, e), m.UP, b.mact[l], m.F, T, m.F, m.dt, stream));
-    else
-      XT_TRY(xt_gelu_fwd(b.up[l], b.mact[l], T * m.F, m.dt, stream));
+    XT_TRY(layer_front(c, m, prm, b, l, false, stream));
     XT_TRY(matmul(lin_fwd(m, m.F, d), b.mact[l], prm->W_down[l], b.tmp, b.ws_mm, b.ws_mm_bytes, s));
     // residual dropout-add, then the next layer's first pre-norm (or the final norm)
     if (l + 1 < m.L)
@@ -410,6 +436,9 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   XT_TRY(norm_bwd_g(c, m, b.gA, b.h_final, prm->gf, b.stf, b.dh, prm->dgf, prm->dbf, 0, b.gB,
                     site_seed(c, m.L - 1, kSiteFfn), drop, b, stream));
   for (int64_t l = m.L - 1; l >= 0; --l) {
+    // activation recompute: the layer's forward again from its saved input (the gradients in
+    // gA / gB and dh are untouched by it)
+    if (m.recompute) XT_TRY(layer_front(c, m, prm, b, l, true, stream));
     // MLP sub-block: df = dropout'(dh) (in gB); dW_down += mᵀ df; dm = df W_downᵀ; activation'; ...
     XT_TRY(matmul(lin_dw(m, m.F, d), b.mact[l], b.gB, prm->dW_down[l], b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(matmul(lin_dx(m, m.F, d), b.gB, prm->W_down[l], b.dm, b.ws_mm, b.ws_mm_bytes, s));

@@ -48,7 +48,7 @@ class BlockConfig(C.Structure):
                 ("learned_pos", C.c_int32), ("causal", C.c_int32), ("training", C.c_int32),
                 ("dtype", C.c_int32), ("grad_dtype", C.c_int32), ("eps", C.c_float),
                 ("p", C.c_float), ("rope_base", C.c_double), ("base_seed", C.c_uint64),
-                ("attention", C.c_int32)]
+                ("attention", C.c_int32), ("recompute", C.c_int32)]
 
 
 _VP = C.c_void_p
