@@ -7,9 +7,11 @@ import pytest
 
 import oracle.dropout as D
 import oracle.ops as O
+import oracle.optim as OP
 from tests import test_oracle_block as TB
 from tests import test_oracle_engine as TE
 from tests import test_oracle_ops as TO
+from tests import test_oracle_optim as TOP
 
 
 def _rms_bwd_dropped_term(d, x, gamma, ir):
@@ -80,6 +82,26 @@ def _swiglu_bwd_swapped(d, g, u):
     return du, dg
 
 
+def _adamw_no_bias_correction(p, g, m, v, step, lr, beta1, beta2, eps, weight_decay):
+    m = beta1 * np.asarray(m, float) + (1 - beta1) * g
+    v = beta2 * np.asarray(v, float) + (1 - beta2) * g * g
+    return p * (1 - lr * weight_decay) - lr * m / (np.sqrt(v) + eps), m, v
+
+
+def _adamw_coupled_decay(p, g, m, v, step, lr, beta1, beta2, eps, weight_decay):
+    # weight decay folded into the gradient (Adam with an L2 term) instead of decoupled
+    return _adamw_coupled_decay.__wrapped__(p, np.asarray(g) + weight_decay * np.asarray(p), m, v, step, lr,
+                                            beta1, beta2, eps, 0.0)
+
+
+def _clip_always(norm, max_norm):
+    return 1.0 if max_norm <= 0 else max_norm / (norm + 1e-6)
+
+
+def _norm_unscaled(grads, scale=1.0):
+    return math.sqrt(sum(float(np.sum(np.asarray(g, float) ** 2)) for g in grads))
+
+
 MUTANTS = [
     ("rms_norm_bwd", _rms_bwd_dropped_term, O, TO.test_rms_norm),
     ("rms_norm_bwd", _rms_bwd_wrong_power, O, TO.test_rms_norm),
@@ -95,6 +117,11 @@ MUTANTS = [
     ("swiglu_bwd", _swiglu_bwd_swapped, O, TO.test_swiglu_equals_composition),
     ("rms_norm_bwd", _rms_bwd_dropped_term, O, lambda: TB.test_block_fd_all_leaves("rms_swiglu")),
     ("layernorm_bwd", _ln_bwd_no_mean, O, lambda: TB.test_block_fd_all_leaves("ln_gelu_pos")),
+    ("adamw_tensor", _adamw_no_bias_correction, OP, TOP.test_adamw_matches_torch_over_steps),
+    ("adamw_tensor", _adamw_no_bias_correction, OP, TOP.test_first_step_closed_form),
+    ("adamw_tensor", _adamw_coupled_decay, OP, TOP.test_adamw_matches_torch_over_steps),
+    ("clip_coefficient", _clip_always, OP, lambda: TOP.test_clip_matches_torch(1e3)),
+    ("global_grad_norm", _norm_unscaled, OP, lambda: TOP.test_microbatch_average_identity(2)),
 ]
 
 
