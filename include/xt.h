@@ -395,6 +395,36 @@ int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, cons
                   void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Optimizer step after the backward ([BP] § Ackumulation över mikrobatcher: gradients of
+ * every microbatch are summed into the buffers, then scaled by 1/n_microbatches before one
+ * optimizer step; [BP] § Parningsdisciplinen: gradient clipping as a partial and a final
+ * gradient-norm reduction and a gradient scale; [BP] § Optimiser-tillståndet: AdamW with a
+ * first moment m and a second moment v per weight).  Over n tensors i, all float32:
+ *   s    = grad_scale (e.g. 1 / n_microbatches),  norm = ‖s·g‖₂ over every element of every
+ *          tensor,  c = min(1, max_grad_norm / (norm + 1e-6))  (c = 1 when max_grad_norm ≤ 0),
+ *   g'   = s·c·g,   m ← β₁ m + (1−β₁) g',   v ← β₂ v + (1−β₂) g'²,
+ *   θ    ← θ (1 − lr·λ) − lr · (m / (1−β₁ᵗ)) / (√(v / (1−β₂ᵗ)) + ε)   (t = step ≥ 1).
+ * param, m, v are updated in place; grad is read only.  shadow (NULL, or per tensor NULL or
+ * a device pointer) receives the updated θ converted to shadow_dtype (XT_BF16 / XT_F32): the
+ * working copy a bf16 model computes with while param holds the float32 master weights.
+ * param, grad, m, v, shadow and numel are HOST arrays of n entries (device pointers, sizes).
+ * norm_out (device float, may be NULL) receives norm.  The workspace
+ * (xt_adamw_workspace_size) holds one partial sum per 4096-element tile and is needed when
+ * clipping or norm_out is requested.  Deterministic: fixed-order sums, no atomics.
+ * ------------------------------------------------------------------------------- */
+typedef struct xt_adamw_config {
+  float lr, beta1, beta2, eps, weight_decay;
+  float max_grad_norm; /* ≤ 0: no clipping */
+  float grad_scale;    /* applied to every gradient before the norm (1 / n_microbatches) */
+  int32_t step;        /* t ≥ 1, for the bias corrections */
+} xt_adamw_config;
+
+int xt_adamw_workspace_size(int n, const int64_t* numel, size_t* bytes);
+int xt_adamw_step(const xt_adamw_config* cfg, int n, float* const* param, const float* const* grad, float* const* m,
+                  float* const* v, void* const* shadow, int shadow_dtype, const int64_t* numel, float* norm_out,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Native block stack ([BP] § Framåtgåendet; [DO] § dropout 接在哪（wiring）):
  *   h = E[ids] (+ P);  per layer l:  h += dropout(attn(norm1 h), seed ⊕ l ⊕ 0xA77),
  *                                    h += dropout(mlp(norm2 h),  seed ⊕ l ⊕ 0xF70);

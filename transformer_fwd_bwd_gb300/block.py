@@ -167,3 +167,50 @@ class NativeBlock:
         self.forward(ids, targets, stream)
         self.backward(ids, targets, stream)
         return self.loss
+
+    # -------------------------------------------------------------------------- optimizer
+
+    def init_optimizer(self, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_grad_norm=1.0):
+        """AdamW state ([BP] § Optimiser-tillståndet): float32 master weights (the parameters
+        themselves when they are float32; for bf16 parameters a float32 copy, the bf16 tensors
+        then being the working copy every step rewrites), first and second moments at zero."""
+        if self.gdt != torch.float32:
+            raise ValueError("the optimizer reads float32 gradients (grad_dtype='f32')")
+        self.hyper = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay,
+                          max_grad_norm=max_grad_norm)
+        self._names = list(self.p)
+        self.master = {k: (v if v.dtype == torch.float32 else v.float().contiguous()) for k, v in self.p.items()}
+        self.m = {k: torch.zeros(v.shape, dtype=torch.float32, device=self.device) for k, v in self.p.items()}
+        self.v = {k: torch.zeros(v.shape, dtype=torch.float32, device=self.device) for k, v in self.p.items()}
+        self.opt_step = 0
+        self.grad_norm = torch.zeros(1, dtype=torch.float32, device=self.device)
+        self._opt_ws = xt.adamw_workspace([self.p[k].numel() for k in self._names], self.device)
+
+    def optimizer_step(self, n_microbatches=1, stream=None):
+        """Clipped AdamW over every parameter with the gradients scaled by 1 / n_microbatches
+        (the buffers hold the sum over the microbatches); the gradient norm before clipping
+        lands in self.grad_norm."""
+        self.opt_step += 1
+        h = self.hyper
+        cfg = xt.adamw_config(h["lr"], h["beta1"], h["beta2"], h["eps"], h["weight_decay"], h["max_grad_norm"],
+                              1.0 / n_microbatches, self.opt_step)
+        names = self._names
+        shadows = None
+        if self.dt != torch.float32:
+            shadows = [self.p[k] for k in names]
+        xt.xt_adamw_step(cfg, [self.master[k] for k in names], [self.g[k] for k in names],
+                         [self.m[k] for k in names], [self.v[k] for k in names], shadows=shadows,
+                         norm_out=self.grad_norm, ws=self._opt_ws, s=stream)
+
+    def train_step(self, microbatches, stream=None):
+        """[BP] § Ackumulation över mikrobatcher: zero the gradients, forward + backward every
+        microbatch (each backward adds into the buffers), one optimizer step on the average.
+        Returns the microbatch losses (device tensors)."""
+        self.zero_grads(stream)
+        losses = []
+        for ids, targets in microbatches:
+            self.forward(ids, targets, stream)
+            losses.append(self.loss.clone())
+            self.backward(ids, targets, stream)
+        self.optimizer_step(len(microbatches), stream)
+        return losses

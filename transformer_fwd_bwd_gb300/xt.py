@@ -41,6 +41,12 @@ class MatmulDesc(C.Structure):
                 ("stride_c_outer", C.c_int64), ("stride_c_inner", C.c_int64)]
 
 
+class AdamWConfig(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("weight_decay", C.c_float), ("max_grad_norm", C.c_float), ("grad_scale", C.c_float),
+                ("step", C.c_int32)]
+
+
 class BlockConfig(C.Structure):
     _fields_ = [("B", C.c_int32), ("S", C.c_int32), ("d", C.c_int32), ("H", C.c_int32),
                 ("hd", C.c_int32), ("F", C.c_int32), ("V", C.c_int32), ("n_layers", C.c_int32),
@@ -122,6 +128,10 @@ _SIGS = {
     "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
     "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
     "xt_gemm_set_schedule": [_I],
+    "xt_adamw_workspace_size": [_I, C.POINTER(C.c_int64), _SZP],
+    "xt_adamw_step": [C.POINTER(AdamWConfig), _I, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                      C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), _I,
+                      C.POINTER(C.c_int64), _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_gelu_fwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_gelu_bwd": [C.POINTER(MatmulDesc), _VP, _VP, _VP, _VP, _VP, C.c_size_t, _VP],
@@ -515,6 +525,50 @@ def matmul_desc(M, N, K, *, trans_a=0, trans_b=0, lda=None, ldb=None, ldc=None, 
     (d.stride_a_outer, d.stride_a_inner, d.stride_b_outer, d.stride_b_inner,
      d.stride_c_outer, d.stride_c_inner) = strides
     return d
+
+
+def adamw_config(lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0, max_grad_norm=0.0, grad_scale=1.0, step=1):
+    return AdamWConfig(lr, beta1, beta2, eps, weight_decay, max_grad_norm, grad_scale, step)
+
+
+def adamw_workspace(numels, device="cuda"):
+    arr = (C.c_int64 * max(1, len(numels)))(*numels)
+    return workspace(ws_bytes("xt_adamw_workspace_size", len(numels), arr), device)
+
+
+def xt_adamw_step(cfg, params, grads, m, v, shadows=None, norm_out=None, ws=None, s=None):
+    """One AdamW step over lists of float32 tensors (params, grads, m, v updated in place
+    except grads); shadows: None or a list (entries may be None) of bf16 / float32 tensors that
+    receive the updated weights; norm_out: a float32 device tensor of one element or None."""
+    n = len(params)
+    if not (len(grads) == len(m) == len(v) == n):
+        raise ValueError("params, grads, m, v must have the same length")
+    for t in list(params) + list(grads) + list(m) + list(v):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("params, grads, m, v must be contiguous float32")
+    numel = [t.numel() for t in params]
+    for lst in (grads, m, v):
+        if [t.numel() for t in lst] != numel:
+            raise ValueError("tensor sizes differ")
+    P = (C.c_void_p * n)(*[t.data_ptr() for t in params])
+    G = (C.c_void_p * n)(*[t.data_ptr() for t in grads])
+    M = (C.c_void_p * n)(*[t.data_ptr() for t in m])
+    V = (C.c_void_p * n)(*[t.data_ptr() for t in v])
+    SH, sdt = None, XT_F32
+    if shadows is not None:
+        dts = {t.dtype for t in shadows if t is not None}
+        if len(dts) > 1:
+            raise ValueError("shadows must share one dtype")
+        sdt = XT_BF16 if dts == {torch.bfloat16} else XT_F32
+        for t, p in zip(shadows, params):
+            if t is not None and (t.numel() != p.numel() or not t.is_contiguous()):
+                raise ValueError("shadow shapes must match params")
+        SH = (C.c_void_p * n)(*[(t.data_ptr() if t is not None else None) for t in shadows])
+    N = (C.c_int64 * n)(*numel)
+    if ws is None and (cfg.max_grad_norm > 0 or norm_out is not None):
+        ws = adamw_workspace(numel, params[0].device)
+    call("xt_adamw_step", C.byref(cfg), n, P, G, M, V, SH, sdt, N, ptr(norm_out), ptr(ws),
+         ws.numel() if ws is not None else 0, stream(s))
 
 
 def matmul_workspace(desc, device="cuda"):
