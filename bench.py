@@ -47,7 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recompute: keep each layer's input only, redo its forward in the backward")
-    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy"], default=None,
+    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy", "adamw"], default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="per-kernel HBM GB/s of the memory-bound ops (rows 8192 x cols 768..8192, fp32 and bf16) "
@@ -483,6 +483,30 @@ def run_kernel(args):
         bwd_us = timed(lambda: xt.xt_gelu_bwd(d, a, dx))
         print(json.dumps({"kernel": "gelu", "n": n, "fwd_us": fwd_us, "bwd_us": bwd_us,
                           "fwd_gbs": 4 * n / fwd_us / 1e3, "bwd_gbs": 6 * n / bwd_us / 1e3, "clocks": clocks}))
+    elif args.kernel == "adamw":
+        # the optimizer step over the stack's parameter tensors (float32 masters, bf16 copies)
+        cfg = synth.BLOCK_CONFIGS[args.workload]
+        d, F, V, S, L = cfg["d"], cfg["F"], cfg["V"], cfg["S"], cfg["n_layers"]
+        up = 2 * F if cfg["mlp"] == "swiglu" else F
+        shapes = [(V, d), (d,), (d,)] + ([(S, d)] if cfg["learned_pos"] else [])
+        for _ in range(L):
+            shapes += [(d,), (d,), (d,), (d,), (d, 3 * d), (d, d), (d, up), (F, d)]
+        mk = lambda sh: (torch.randn(*sh, generator=g) * 0.02).to(dev)  # noqa: E731
+        P = [mk(sh) for sh in shapes]
+        G = [mk(sh) for sh in shapes]
+        M = [torch.zeros_like(x) for x in P]
+        Vv = [torch.zeros_like(x) for x in P]
+        SH = [torch.empty(x.shape, dtype=torch.bfloat16, device=dev) for x in P]
+        nrm = torch.zeros(1, dtype=torch.float32, device=dev)
+        ows = xt.adamw_workspace([x.numel() for x in P], dev)
+        acfg = xt.adamw_config(1e-4, weight_decay=0.1, max_grad_norm=1.0, grad_scale=0.5, step=1)
+        us = timed(lambda: xt.xt_adamw_step(acfg, P, G, M, Vv, shadows=SH, norm_out=nrm, ws=ows))
+        n = sum(x.numel() for x in P)
+        nbytes = n * (4 + 16 + 12 + 2)   # norm pass reads g; update reads θ, g, m, v, writes θ, m, v, bf16 θ
+        peak = measured_peaks()[0].get("hbm_gbs", 6780.0)
+        print(json.dumps({"kernel": "adamw", "tensors": len(P), "params": n, "us": us,
+                          "gbs": nbytes / us / 1e3, "frac_of_measured_hbm": nbytes / us / 1e3 / peak,
+                          "clocks": clocks}))
     elif args.kernel == "cross_entropy":
         # the tied-logit loss as the stack runs it: bf16 logits [B·S, V], backward in place
         cfg = synth.BLOCK_CONFIGS[args.workload]
