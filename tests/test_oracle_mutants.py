@@ -6,11 +6,13 @@ import numpy as np
 import pytest
 
 import oracle.dropout as D
+import oracle.fp8 as F8
 import oracle.ops as O
 import oracle.optim as OP
 from tests import test_oracle_block as TB
 from tests import test_oracle_engine as TE
 from tests import test_oracle_ops as TO
+from tests import test_oracle_fp8 as TF8
 from tests import test_oracle_optim as TOP
 
 
@@ -102,6 +104,25 @@ def _norm_unscaled(grads, scale=1.0):
     return math.sqrt(sum(float(np.sum(np.asarray(g, float) ** 2)) for g in grads))
 
 
+def _fp8_ties_away(x):
+    # nearest code with ties away from zero instead of to the even code
+    x = np.asarray(x, float)
+    out = _fp8_ties_away.__wrapped__(x)
+    pos = F8.DECODE[:0x7F]
+    for i, v in enumerate(x.ravel()):
+        a = min(abs(v), F8.MAX)
+        lo = int(np.searchsorted(pos, a, side="right")) - 1
+        if lo < 0x7E and a - pos[lo] == pos[lo + 1] - a:
+            out.ravel()[i] = (0x80 if v < 0 else 0) | (lo + 1)
+    return out
+
+
+def _fp8_no_saturation(x):
+    out = _fp8_no_saturation.__wrapped__(x)
+    out[np.abs(np.asarray(x, float)) > F8.MAX] = 0x7F
+    return out
+
+
 MUTANTS = [
     ("rms_norm_bwd", _rms_bwd_dropped_term, O, TO.test_rms_norm),
     ("rms_norm_bwd", _rms_bwd_wrong_power, O, TO.test_rms_norm),
@@ -122,6 +143,9 @@ MUTANTS = [
     ("adamw_tensor", _adamw_coupled_decay, OP, TOP.test_adamw_matches_torch_over_steps),
     ("clip_coefficient", _clip_always, OP, lambda: TOP.test_clip_matches_torch(1e3)),
     ("global_grad_norm", _norm_unscaled, OP, lambda: TOP.test_microbatch_average_identity(2)),
+    ("encode", _fp8_ties_away, F8, TF8.test_encode_matches_torch_in_range_and_on_ties),
+    ("encode", _fp8_ties_away, F8, TF8.test_printed_constants_and_saturation),
+    ("encode", _fp8_no_saturation, F8, TF8.test_printed_constants_and_saturation),
 ]
 
 
