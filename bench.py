@@ -47,7 +47,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recompute: keep each layer's input only, redo its forward in the backward")
-    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy", "adamw"], default=None,
+    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy", "adamw", "fp8gemm"],
+                    default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="per-kernel HBM GB/s of the memory-bound ops (rows 8192 x cols 768..8192, fp32 and bf16) "
@@ -507,6 +508,26 @@ def run_kernel(args):
         print(json.dumps({"kernel": "adamw", "tensors": len(P), "params": n, "us": us,
                           "gbs": nbytes / us / 1e3, "frac_of_measured_hbm": nbytes / us / 1e3 / peak,
                           "clocks": clocks}))
+    elif args.kernel == "fp8gemm":
+        # e4m3 GEMM (A [M, K], B [N, K], K contiguous) after per-tensor quantization, bf16 out
+        M, N, K, _, _ = (int(x) for x in args.shape.split(","))
+        A = torch.randn(M, K, generator=g).to(dev)
+        Bm = torch.randn(N, K, generator=g).to(dev)
+        Aq = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        Bq = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        da = torch.empty(1, dtype=torch.float32, device=dev)
+        db = torch.empty(1, dtype=torch.float32, device=dev)
+        xt.xt_quantize_fp8(A, Aq, da)
+        xt.xt_quantize_fp8(Bm, Bq, db)
+        C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        us = timed(lambda: xt.xt_matmul_fp8_fwd(Aq, Bq, C, scale_a=da, scale_b=db))
+        qus = timed(lambda: xt.xt_quantize_fp8(A, Aq, da))
+        peaks, src = measured_peaks()
+        peak = 2.0 * peaks.get("bf16_tflops", 1900.0)   # the bf16 burst measurement × the nominal fp8/bf16 ratio
+        tf = 2 * M * N * K / us / 1e6
+        print(json.dumps({"kernel": "fp8gemm", "shape": [M, N, K], "us": us, "tflops": tf, "peak_tflops": peak,
+                          "frac": tf / peak, "peak_source": f"{src} bf16 burst x 4.5/2.25",
+                          "quantize_us": qus, "quantize_gbs": M * K * (4 + 1) / qus / 1e3, "clocks": clocks}))
     elif args.kernel == "cross_entropy":
         # the tied-logit loss as the stack runs it: bf16 logits [B·S, V], backward in place
         cfg = synth.BLOCK_CONFIGS[args.workload]

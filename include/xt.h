@@ -395,6 +395,28 @@ int xt_matmul_bwd(const xt_matmul_desc* desc, const void* A, const void* B, cons
                   void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * FP8 E4M3 ([BP] § Vad generiska ramverk kostar, item 4: an FP8 E4M3 tensor-core path in the
+ * mixed-precision pipeline; the pages give no format details, so the OCP E4M3 format is used:
+ * bias 7, 3 mantissa bits, subnormals m·2⁻⁹, largest finite 448, no infinities).
+ *   xt_quantize_fp8: per-tensor quantization of n elements of x (XT_F32 / XT_BF16):
+ *     scale = 448 / max|x| (one float32 division; 1 when all are 0), out[i] = e4m3(x[i]·scale)
+ *     rounded to nearest even and saturated to ±448; *dequant (device float) = max|x| / 448
+ *     (1 when all are 0), the factor a code is multiplied by to stand for x.  The workspace
+ *     (xt_quantize_fp8_workspace_size) holds per-block maxima.  Deterministic.
+ *   xt_matmul_fp8_fwd: C [M, N] (+)= alpha · (*scale_a) · (*scale_b) · A Bᵀ on the tensor cores
+ *     (tcgen05 kind::f8f6f4, float32 accumulation): A [M, K] and B [N, K] e4m3 codes with K
+ *     contiguous (rows lda / ldb bytes apart, multiples of 16), C float32 or bf16 (ldc
+ *     elements); scale_a / scale_b are device floats (may be NULL: 1), e.g. the dequant factors
+ *     of xt_quantize_fp8.  A, B, C 16-byte aligned (else XT_ERR_ALIGNMENT).
+ * ------------------------------------------------------------------------------- */
+int xt_quantize_fp8_workspace_size(int64_t n, size_t* bytes);
+int xt_quantize_fp8(const void* x, int64_t n, int dt, uint8_t* out, float* dequant, void* ws, size_t ws_bytes,
+                    void* stream);
+int xt_matmul_fp8_fwd(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda, const uint8_t* B, int64_t ldb,
+                      void* C, int64_t ldc, int dt_c, float alpha, const float* scale_a, const float* scale_b,
+                      int accumulate, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Optimizer step after the backward ([BP] § Ackumulation över mikrobatcher: gradients of
  * every microbatch are summed into the buffers, then scaled by 1/n_microbatches before one
  * optimizer step; [BP] § Parningsdisciplinen: gradient clipping as a partial and a final

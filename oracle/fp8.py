@@ -64,11 +64,11 @@ def decode(codes) -> np.ndarray:
 
 
 def quantize(x):
-    """Per-tensor quantization: (codes, scale) with scale = 448 / amax (1 when amax = 0) and
-    the codes of float32(x)·float32(scale) formed in float32."""
+    """Per-tensor quantization: (codes, scale) with scale = 448 / amax as one float32
+    division (1 when amax = 0) and the codes of float32(x)·scale formed in float32."""
     x32 = np.asarray(x, dtype=np.float32)
     amax = float(np.max(np.abs(x32))) if x32.size else 0.0
-    scale = np.float32(MAX / amax) if amax > 0 else np.float32(1.0)
+    scale = np.float32(MAX) / np.float32(amax) if amax > 0 else np.float32(1.0)   # one float32 division
     return encode((x32 * scale).astype(np.float32)), float(scale)
 
 

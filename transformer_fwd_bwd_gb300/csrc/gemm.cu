@@ -28,10 +28,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Operand as the kernel sees it: `mn` rows (M or N) by K, either K contiguous (K-major) or
 // MN contiguous (MN-major), with two batch levels.
-int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn) {
+int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn) {
   auto enc = encode_fn();
   if (!enc) return fail(XT_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const int64_t e = tf32 ? 4 : 2;
+  const int64_t e = kind == kTf32 ? 4 : kind == kFp8 ? 1 : 2;
   const uint32_t atom = uint32_t(128 / e);
   cuuint64_t dims[4];
   cuuint64_t strides[3];
@@ -56,8 +56,10 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn) {
   strides[0] = cuuint64_t(row_bytes);
   strides[1] = cuuint64_t(o.batch_inner > 1 ? o.s_inner * e : row_bytes);
   strides[2] = cuuint64_t(o.batch_outer > 1 ? o.s_outer * e : row_bytes);
-  CUresult r = enc(tm, tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                   const_cast<void*>(o.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const CUtensorMapDataType dt = kind == kTf32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : kind == kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(tm, dt, 4, const_cast<void*>(o.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(XT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
@@ -86,17 +88,20 @@ static int g_schedule = 0;
 // Fixup time of a stream-K tile shared by `parts` CTAs: one latency plus one pass per partial.
 static double sk_fixup_time(int64_t parts) { return 0.7e-6 + 0.8e-6 * double(parts - 1); }
 
-Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split) {
+Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split,
+              bool fp8) {
+  if (fp8) allow_split = false;  // fp8: whole tiles only
   const int mode = allow_split ? g_schedule : 1;
   if (mode == 1) allow_split = false;
   const int cands_bf16[4] = {64, 128, 192, 256};
   const int cands_tf32[2] = {64, 128};
-  const int* c = tf32 ? cands_tf32 : cands_bf16;
-  const int nc = tf32 ? 2 : 4;
+  const int cands_fp8[2] = {128, 256};
+  const int* c = fp8 ? cands_fp8 : tf32 ? cands_tf32 : cands_bf16;
+  const int nc = fp8 || tf32 ? 2 : 4;
   const int sms = num_sms();
-  const int bk = tf32 ? 32 : 64;
-  const double per_sm = tf32 ? 5.6e12 : 11.2e12;
-  const double e = tf32 ? 4.0 : 2.0;
+  const int bk = fp8 ? 128 : tf32 ? 32 : 64;
+  const double per_sm = fp8 ? 22.4e12 : tf32 ? 5.6e12 : 11.2e12;
+  const double e = fp8 ? 1.0 : tf32 ? 4.0 : 2.0;
   Choice best{c[0], 1, 0, 0};
   double best_t = 1e300;
   const int64_t kbt = ceil_div(K, bk);
@@ -197,18 +202,19 @@ static int make_output_map(CUtensorMap* tm, void* base, bool bf16, int64_t M, in
 int run(const Problem& pb, cudaStream_t s) {
   const bool tf32 = pb.tf32;
   const int64_t batches = int64_t(pb.batch_outer) * pb.batch_inner;
-  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, pb.act == 0);
+  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, pb.act == 0, pb.fp8);
   if ((ch.splits > 1 || ch.sk) && (pb.split_ws == nullptr || split_bytes(ch, pb.M, pb.N) > pb.split_ws_bytes ||
                                    (ch.sk && pb.sk_flags == nullptr)))
-    ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false);
+    ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false, pb.fp8);
   if (pb.act) ch = Choice{256, 1, 0, 0};  // the GELU epilogues are built for BN 256 only
   const int bn = ch.bn;
   const bool split = ch.splits > 1;
   CUtensorMap ta, tb, tc, tc2;
   memset(&tc2, 0, sizeof(tc2));
   if (pb.act == 1) XT_TRY(make_output_map(&tc2, pb.C2, true, pb.M, pb.N, pb.ldc, 1, 1, 0, 0));
-  XT_TRY(make_operand_map(&ta, pb.A, tf32, BM));
-  XT_TRY(make_operand_map(&tb, pb.B, tf32, bn));
+  const int kind = pb.fp8 ? kFp8 : tf32 ? kTf32 : kBf16;
+  XT_TRY(make_operand_map(&ta, pb.A, kind, BM));
+  XT_TRY(make_operand_map(&tb, pb.B, kind, bn));
   // TMA epilogue for every output except a bf16 C that is accumulated into (TMA reduce-add is
   // used for float32 only; bf16 accumulation keeps the direct read-modify-write stores).  A K
   // split stores float32 partial tiles into [splits][M][N] slices instead.
@@ -228,7 +234,8 @@ int run(const Problem& pb, cudaStream_t s) {
   p.batch_inner = split ? ch.splits : pb.batch_inner;
   p.batches = split ? ch.splits : pb.batch_inner * pb.batch_outer;
   p.splitk = ch.splits;
-  p.kb_per_split = int(ceil_div(ceil_div(pb.K, tf32 ? 32 : 64), ch.splits));
+  const int bk = pb.fp8 ? 128 : tf32 ? 32 : 64;
+  p.kb_per_split = int(ceil_div(ceil_div(pb.K, bk), ch.splits));
   p.causal = pb.causal;
   p.accumulate = split ? 0 : pb.accumulate;
   p.c_bf16 = split ? 0 : pb.c_bf16;
@@ -242,13 +249,15 @@ int run(const Problem& pb, cudaStream_t s) {
   p.aux = static_cast<const bf16*>(pb.aux);
   p.ld_aux = pb.ldc;
   p.flag = errflag();
+  p.scale_a = pb.scale_a;
+  p.scale_b = pb.scale_b;
   const int64_t tiles = int64_t(p.num_m) * p.num_n * p.batches;  // a K split counts its slices
   if (tiles > int64_t(1) << 30) return fail(XT_ERR_UNSUPPORTED, "matmul: too many tiles");
   int grid = int(tiles < num_sms() ? tiles : num_sms());
   if (grid < 1) grid = 1;
   if (ch.sk) {
     p.sk = 1;
-    p.kb_tile = int(ceil_div(pb.K, tf32 ? 32 : 64));
+    p.kb_tile = int(ceil_div(pb.K, bk));
     p.sk_iters = tiles * p.kb_tile;
     p.sk_part = static_cast<float*>(pb.split_ws);
     p.sk_flag = pb.sk_flags;
@@ -267,7 +276,8 @@ int run(const Problem& pb, cudaStream_t s) {
                         ch.sk == 1 ? 1000 : ch.sk == 2 ? 1000 + int(ch.grid / tiles) :
                         split ? 10 * ch.splits : p.causal};
   const bool prof = gemm_profile_begin(s, flops, shape, &tok);
-  int st = tf32      ? launch_tf32(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
+  int st = pb.fp8    ? launch_fp8(bn, ta, tb, tc, tc2, p, grid, s)
+           : tf32    ? launch_tf32(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
            : pb.act ? launch_bf16_act(pb.act, amn, bmn, ta, tb, tc, tc2, p, grid, s)
                     : launch_bf16(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s);
   if (st == XT_OK && split) {

@@ -22,6 +22,9 @@ struct Operand {
 
 struct Problem {
   bool tf32;
+  bool fp8;              // e4m3 operands (K-major), kind::f8f6f4
+  const float* scale_a;  // device per-tensor factors multiplying alpha (may be null)
+  const float* scale_b;
   int64_t M, N, K;
   int batch_inner, batch_outer;
   Operand A, B;
@@ -46,14 +49,16 @@ struct Choice {
   int sk;    // stream-K schedule: 1 over every SM, 2 in lockstep K slices
   int grid;  // stream-K CTAs: the SMs, or tiles × K slices (lockstep)
 };
-Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split);
+Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split,
+              bool fp8 = false);
 size_t split_bytes(const Choice& c, int64_t M, int64_t N);
 
 // Stream-K flag words at the head of every matmul workspace: 4 per CTA for up to kSkMaxCtas CTAs.
 constexpr int kSkMaxCtas = 256;
 constexpr size_t kSkFlagBytes = size_t(kSkMaxCtas) * 4 * sizeof(uint32_t);
 
-int make_operand_map(CUtensorMap* tm, const Operand& o, bool tf32, int box_mn);
+// kind: kBf16, kTf32 or kFp8 (element size 2, 4, 1)
+int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn);
 // The driver's cuTensorMapEncodeTiled (null when the driver does not provide it).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 int run(const Problem& pb, cudaStream_t s);
@@ -61,15 +66,18 @@ int launch_bf16(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUten
                 const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 int launch_tf32(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
+// fp8 e4m3, K-major operands, BN 128 or 256.
+int launch_fp8(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
+               const Params& p, int grid, cudaStream_t s);
 // bf16, BN 256, with the GELU epilogue `act` (1 or 2).
 int launch_bf16_act(int act, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                     const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 
-template <bool TF32, int BN, bool A_MN, bool B_MN, int ACT = 0>
+template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0>
 int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                const Params& p, int grid, cudaStream_t s) {
-  auto k = gemm_kernel<TF32, BN, A_MN, B_MN, ACT>;
-  constexpr int smem = Cfg<TF32, BN>::SMEM;
+  auto k = gemm_kernel<KIND, BN, A_MN, B_MN, ACT>;
+  constexpr int smem = Cfg<KIND, BN>::SMEM;
   static bool attr_set = false;  // per instantiation; idempotent if raced
   if (!attr_set) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

@@ -22,6 +22,9 @@ namespace xt {
 namespace gemm {
 
 constexpr int BM = 128;
+// Operand kinds (the KIND template parameter): bf16 (tcgen05 kind::f16), tf32 (kind::tf32) and
+// fp8 e4m3 (kind::f8f6f4).  One MMA instruction consumes 32 bytes of K of each operand row.
+constexpr int kBf16 = 0, kTf32 = 1, kFp8 = 2;
 constexpr int kThreads = 192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
@@ -57,6 +60,10 @@ struct Params {
   int64_t sk_iters;
   float* sk_part;
   uint32_t* sk_flag;
+  // per-tensor factors (device floats, may be null) multiplying alpha: the dequantization
+  // factors of fp8 operands
+  const float* scale_a;
+  const float* scale_b;
 };
 
 // ------------------------------------------------------------------------------ PTX wrappers
@@ -168,10 +175,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-template <bool TF32>
+template <int KIND>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accum) {
-  if constexpr (TF32) {
+  if constexpr (KIND == kFp8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+  } else if constexpr (KIND == kTf32) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -222,12 +235,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
-// Instruction descriptor for kind::f16 / kind::tf32: fp32 accumulator, A/B types (bf16 = 1,
-// tf32 = 2), operand majorness (1 = MN-major), N >> 3, M >> 4.
-template <bool TF32, int N, bool A_MN, bool B_MN>
+// Instruction descriptor for kind::f16 / kind::tf32 / kind::f8f6f4: fp32 accumulator, A/B
+// types (bf16 = 1, tf32 = 2, e4m3 = 0), operand majorness (1 = MN-major), N >> 3, M >> 4.
+template <int KIND, int N, bool A_MN, bool B_MN>
 __host__ __device__ constexpr uint32_t instr_desc() {
-  return (1u << 4) | ((TF32 ? 2u : 1u) << 7) | ((TF32 ? 2u : 1u) << 10) | ((A_MN ? 1u : 0u) << 15) |
-         ((B_MN ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+  constexpr uint32_t t = KIND == kTf32 ? 2u : KIND == kFp8 ? 0u : 1u;
+  return (1u << 4) | (t << 7) | (t << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(BM >> 4) << 24);
 }
 
 // bf16 × bf16 → fp32 instruction descriptor for an M × N tile.
@@ -241,12 +255,12 @@ constexpr uint32_t tmem_cols() {
   return 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
 }
 
-template <bool TF32, int BN>
+template <int KIND, int BN>
 struct Cfg {
-  static constexpr int E = TF32 ? 4 : 2;
+  static constexpr int E = KIND == kTf32 ? 4 : KIND == kFp8 ? 1 : 2;
   static constexpr int BK = 128 / E;         // K elements per stage (one 128-byte row)
   static constexpr int ATOM = 128 / E;       // MN elements per 128-byte swizzle row
-  static constexpr int UK = TF32 ? 8 : 16;   // K per MMA instruction
+  static constexpr int UK = 32 / E;          // K per MMA instruction (32 bytes)
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -372,14 +386,14 @@ __device__ __forceinline__ void sk_fixup(uint32_t tacc, const Params& p, int fir
 
 // ACT: the epilogue's GELU mode (Params::act), a template parameter so the plain GEMMs carry
 // none of its code.
-template <bool TF32, int BN, bool A_MN, bool B_MN, int ACT = 0>
+template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, const Params p) {
   pdl_begin();
-  using C_ = Cfg<TF32, BN>;
+  using C_ = Cfg<KIND, BN>;
   constexpr int BK = C_::BK, ATOM = C_::ATOM, UK = C_::UK, STAGES = C_::STAGES;
-  constexpr uint32_t IDESC = instr_desc<TF32, BN, A_MN, B_MN>();
+  constexpr uint32_t IDESC = instr_desc<KIND, BN, A_MN, B_MN>();
   constexpr uint32_t TCOLS = tmem_cols<BN>();
 
   extern __shared__ uint8_t smem_raw[];
@@ -513,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc(a_s + kk * UK * C_::E, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(b_s + kk * UK * 128, BK * 128, 1024)
                                      : smem_desc(b_s + kk * UK * C_::E, 16, 1024);
-            tc_mma<TF32>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
+            tc_mma<KIND>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&empty[stage]));  // frees the smem slot once these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -527,6 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------------- epilogue
     // Every decision below is warp-uniform: tcgen05.ld is a .sync.aligned instruction.
     const int q = warp & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
+    // alpha times the operands' per-tensor factors (exactly alpha when there are none)
+    const float alpha = p.alpha * (p.scale_a ? __ldg(p.scale_a) : 1.f) * (p.scale_b ? __ldg(p.scale_b) : 1.f);
     int ab = 0;
     uint32_t aphase = 0;
     uint32_t chunk = 0;  // staged stores issued by this warp (selects the staging buffer)
@@ -628,18 +644,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j)
                 st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4),
-                             __float_as_uint(__uint_as_float(r[4 * j]) * p.alpha),
-                             __float_as_uint(__uint_as_float(r[4 * j + 1]) * p.alpha),
-                             __float_as_uint(__uint_as_float(r[4 * j + 2]) * p.alpha),
-                             __float_as_uint(__uint_as_float(r[4 * j + 3]) * p.alpha));
+                             __float_as_uint(__uint_as_float(r[4 * j]) * alpha),
+                             __float_as_uint(__uint_as_float(r[4 * j + 1]) * alpha),
+                             __float_as_uint(__uint_as_float(r[4 * j + 2]) * alpha),
+                             __float_as_uint(__uint_as_float(r[4 * j + 3]) * alpha));
             } else if constexpr (ACT == 0) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * e]) * p.alpha,
-                                                           __uint_as_float(r[8 * j + 2 * e + 1]) * p.alpha);
+                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * e]) * alpha,
+                                                           __uint_as_float(r[8 * j + 2 * e + 1]) * alpha);
                   w[e] = *reinterpret_cast<uint32_t*>(&h);
                 }
                 st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
@@ -653,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                  __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(r[16 * h + 2 * e]) * p.alpha,
-                                                            __uint_as_float(r[16 * h + 2 * e + 1]) * p.alpha);
+                  __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(r[16 * h + 2 * e]) * alpha,
+                                                            __uint_as_float(r[16 * h + 2 * e + 1]) * alpha);
                   w[e] = *reinterpret_cast<uint32_t*>(&hh);
                   av[2 * e] = __low2float(hh);
                   av[2 * e + 1] = __high2float(hh);
@@ -698,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                  __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(r[16 * h + 2 * e]) * p.alpha * dv[2 * e],
-                                                            __uint_as_float(r[16 * h + 2 * e + 1]) * p.alpha * dv[2 * e + 1]);
+                  __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(r[16 * h + 2 * e]) * alpha * dv[2 * e],
+                                                            __uint_as_float(r[16 * h + 2 * e + 1]) * alpha * dv[2 * e + 1]);
                   w[e] = *reinterpret_cast<uint32_t*>(&hh);
                 }
 #pragma unroll
@@ -745,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row >= p.M || col0 >= p.N) continue;
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * p.alpha;
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * alpha;
         const bool full_cols = col0 + 32 <= p.N;
         if (!p.c_bf16) {
           float* cp = static_cast<float*>(p.C) + cbase + col0;

@@ -128,6 +128,9 @@ _SIGS = {
     "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
     "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
     "xt_gemm_set_schedule": [_I],
+    "xt_quantize_fp8_workspace_size": [_I64, _SZP],
+    "xt_quantize_fp8": [_VP, _I64, _I, _VP, _VP, _VP, C.c_size_t, _VP],
+    "xt_matmul_fp8_fwd": [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _I, _F, _VP, _VP, _I, _VP],
     "xt_adamw_workspace_size": [_I, C.POINTER(C.c_int64), _SZP],
     "xt_adamw_step": [C.POINTER(AdamWConfig), _I, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                       C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), _I,
@@ -569,6 +572,31 @@ def xt_adamw_step(cfg, params, grads, m, v, shadows=None, norm_out=None, ws=None
         ws = adamw_workspace(numel, params[0].device)
     call("xt_adamw_step", C.byref(cfg), n, P, G, M, V, SH, sdt, N, ptr(norm_out), ptr(ws),
          ws.numel() if ws is not None else 0, stream(s))
+
+
+def xt_quantize_fp8(x, out, dequant, ws=None, s=None):
+    """Per-tensor e4m3 quantization of x (float32 / bf16) into out (uint8, x's element count);
+    dequant: a float32 device tensor of one element receiving max|x| / 448."""
+    if out.dtype != torch.uint8 or out.numel() != x.numel():
+        raise ValueError("out must be uint8 with x's element count")
+    n = x.numel()
+    if ws is None:
+        ws = workspace(ws_bytes("xt_quantize_fp8_workspace_size", n), x.device)
+    call("xt_quantize_fp8", ptr(x), n, dt(x), ptr(out), ptr(dequant), ptr(ws), ws.numel(), stream(s))
+
+
+def xt_matmul_fp8_fwd(A, B, Cm, alpha=1.0, scale_a=None, scale_b=None, accumulate=0, s=None):
+    """C [M, N] (+)= alpha·sa·sb·A Bᵀ with A [M, K] and B [N, K] uint8 e4m3 codes (row strides
+    from the tensors), C float32 or bf16; scale_a / scale_b: float32 device tensors of one
+    element or None."""
+    if A.dtype != torch.uint8 or B.dtype != torch.uint8:
+        raise ValueError("A and B must be uint8 e4m3 codes")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(Cm.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    call("xt_matmul_fp8_fwd", M, N, K, ptr(A, False), A.stride(0), ptr(B, False), B.stride(0), ptr(Cm, False),
+         Cm.stride(0), dt(Cm), float(alpha), ptr(scale_a), ptr(scale_b), int(accumulate), stream(s))
 
 
 def matmul_workspace(desc, device="cuda"):
