@@ -312,7 +312,8 @@ int xt_norm_bwd_dropout(int norm, const void* d, const void* x, const void* gamm
  * Embedding ([BP] § kernel-pair table k_embed_fwd/bwd; § Var gradienter lever i minnet):
  * h[t] = E[ids[t]] (+ P[t mod S] when P != NULL).  Backward: dE[v] = Σ_{t: ids[t]=v} dh[t]
  * summed in ascending t (deterministic), dP[s] = Σ_b dh[b·S+s].  With acc == 0 the rows
- * of dE that no token touches are zeroed.  T ≤ 65536.
+ * of dE that no token touches are zeroed.  T ≤ 16384.  The workspace (kept for the
+ * interface) may be NULL.
  * ------------------------------------------------------------------------------- */
 int xt_embedding_workspace_size(int64_t T, size_t* bytes);
 int xt_embedding_fwd(const int32_t* ids, const void* E, const void* P, void* h, int64_t T, int S,

@@ -976,60 +976,87 @@ __global__ void __launch_bounds__(256) embed_fwd_kernel(const int32_t* __restric
 }
 
 constexpr int kSortMax = 16384;
+constexpr int kEmbThreads = 512;
 
-// One block sorts keys (id << 32 | t) ascending (bitonic, in shared memory); ids outside
-// [0, V) get the key (V << 32 | t) so they sort last and are skipped.
-__global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restrict__ ids, int64_t T_, int64_t V,
-                                                         uint64_t* __restrict__ sorted, uint32_t* flag) {
+// dE[v] (+)= Σ_{t: ids[t] = v} dh[t], the sum formed in float32 in ascending t and then added
+// to dE[v].  Block b owns the ids [b·per, (b+1)·per): it lists, in ascending t, the tokens
+// whose id falls in its range (ballot compaction over all T ids), then warp w takes the ids
+// v0 + w, v0 + w + warps, …: for each it walks the list in order and sums the rows of the
+// tokens with that id, 8 columns per lane per pass (lane-interleaved, coalesced).  Ids outside
+// [0, V) set XT_DEVERR_INDEX (block 0) and are skipped.  No sort and no atomics.
+template <typename TH, typename TG>
+__global__ void __launch_bounds__(kEmbThreads) embed_bwd_kernel(const int32_t* __restrict__ ids,
+                                                                const TH* __restrict__ dh, TG* dE, int T_,
+                                                                int64_t d, int64_t V, int64_t per, uint32_t* flag) {
   pdl_begin();
-  extern __shared__ uint64_t keys[];
-  int n = 1;
-  while (n < T_) n <<= 1;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    if (i < T_) {
-      const int32_t id = ids[i];
-      const bool bad = id < 0 || int64_t(id) >= V;
-      if (bad) flag_error(flag, XT_DEVERR_INDEX);
-      keys[i] = (uint64_t(bad ? uint64_t(V) : uint64_t(id)) << 32) | uint64_t(i);
-    } else {
-      keys[i] = ~uint64_t(0);
-    }
-  }
+  extern __shared__ int emb_list[];   // [T] token indices, then [T] their ids
+  __shared__ int warp_base[kEmbThreads / 32];
+  __shared__ int total;
+  int* lt = emb_list;
+  int* lid = emb_list + T_;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  constexpr int NW = kEmbThreads / 32;
+  const int64_t v0 = int64_t(blockIdx.x) * per;
+  const int64_t v1 = v0 + per < V ? v0 + per : V;
+  if (threadIdx.x == 0) total = 0;
   __syncthreads();
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int p = i ^ j;
-        if (p > i) {
-          const uint64_t a = keys[i], b = keys[p];
-          const bool up = (i & k) == 0;
-          if ((a > b) == up) { keys[i] = b; keys[p] = a; }
+  for (int base = 0; base < T_; base += kEmbThreads) {
+    const int t = base + int(threadIdx.x);
+    bool m = false;
+    int32_t id = 0;
+    if (t < T_) {
+      id = ids[t];
+      const bool bad = id < 0 || int64_t(id) >= V;
+      if (bad && blockIdx.x == 0) flag_error(flag, XT_DEVERR_INDEX);
+      m = !bad && int64_t(id) >= v0 && int64_t(id) < v1;
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    if (lane == 0) warp_base[w] = __popc(bal);
+    __syncthreads();
+    if (threadIdx.x == 0) {  // exclusive prefix over the warps, in warp order
+      int acc = total;
+      for (int i = 0; i < NW; ++i) {
+        const int c = warp_base[i];
+        warp_base[i] = acc;
+        acc += c;
+      }
+      total = acc;
+    }
+    __syncthreads();
+    if (m) {
+      const int pos = warp_base[w] + __popc(bal & ((1u << lane) - 1u));
+      lt[pos] = t;
+      lid[pos] = id;
+    }
+    __syncthreads();
+  }
+  const int count = total;
+  for (int64_t v = v0 + w; v < v1; v += NW) {
+    for (int64_t c0 = 0; c0 < d; c0 += 32 * 8) {
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      bool any = false;
+      for (int k = 0; k < count; ++k) {
+        if (lid[k] != int(v)) continue;
+        any = true;
+        const TH* row = dh + int64_t(lt[k]) * d;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int64_t c = c0 + lane + 32 * e;
+          if (c < d) acc[e] += to_f(row[c]);
         }
       }
-      __syncthreads();
+      if (!any) break;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int64_t c = c0 + lane + 32 * e;
+        if (c < d) {
+          TG* q = dE + v * d + c;
+          *q = from_f<TG>(to_f(*q) + acc[e]);
+        }
+      }
     }
-  }
-  for (int i = threadIdx.x; i < T_; i += blockDim.x) sorted[i] = keys[i];
-}
-
-// Block i: if sorted position i starts a run of equal ids, sums that run's dh rows in
-// ascending t and adds the sum into dE[id].
-template <typename TH, typename TG>
-__global__ void __launch_bounds__(256) embed_scatter_kernel(const uint64_t* __restrict__ sorted, const TH* __restrict__ dh,
-                                                           TG* dE, int64_t T_, int64_t d, int64_t V) {
-  pdl_begin();
-  const int64_t i = blockIdx.x;
-  const uint64_t key = sorted[i];
-  const int64_t id = int64_t(key >> 32);
-  if (id >= V) return;
-  if (i > 0 && int64_t(sorted[i - 1] >> 32) == id) return;
-  int64_t end = i + 1;
-  while (end < T_ && int64_t(sorted[end] >> 32) == id) ++end;
-  for (int64_t c = threadIdx.x; c < d; c += blockDim.x) {
-    float s = 0.f;
-    for (int64_t k = i; k < end; ++k) s += to_f(dh[int64_t(uint32_t(sorted[k])) * d + c]);
-    TG* p = dE + id * d + c;
-    *p = from_f<TG>(to_f(*p) + s);
   }
 }
 
@@ -1520,7 +1547,7 @@ int xt_rope_bwd(const void* d, void* dx, const float* table, int B, int S, int H
 
 int xt_embedding_workspace_size(int64_t T, size_t* bytes) {
   XT_REQUIRE(T >= 0 && bytes, "xt_embedding_workspace_size: bad arguments");
-  *bytes = size_t(T > 0 ? T : 1) * sizeof(uint64_t);
+  *bytes = 16;  // kept for the interface; the backward needs no scratch
   return XT_OK;
 }
 
@@ -1547,7 +1574,7 @@ int xt_embedding_bwd(const int32_t* ids, const void* dh, void* dE, void* dP, int
   XT_REQUIRE(valid_dtype(dt_dh) && valid_dtype(dt_grad), "xt_embedding_bwd: bad dtype");
   XT_REQUIRE(T >= 0 && d > 0 && V > 0 && (!dP || (S > 0 && T % S == 0)), "xt_embedding_bwd: bad sizes");
   XT_REQUIRE(T <= kSortMax, "xt_embedding_bwd: T > %d is not supported", kSortMax);
-  XT_REQUIRE(dE && (T == 0 || (ids && dh && ws)), "xt_embedding_bwd: NULL pointer");
+  XT_REQUIRE(dE && (T == 0 || (ids && dh)), "xt_embedding_bwd: NULL pointer");
   XT_REQUIRE(V < (int64_t(1) << 31), "xt_embedding_bwd: V too large");
   cudaStream_t s = as_stream(stream);
   if (!acc) {
@@ -1555,18 +1582,15 @@ int xt_embedding_bwd(const int32_t* ids, const void* dh, void* dE, void* dP, int
       return check_launch("xt_embedding_bwd zero");
   }
   if (T == 0) return XT_OK;
-  uint64_t* sorted = static_cast<uint64_t*>(ws);
-  int n = 1;
-  while (n < T) n <<= 1;
-  const size_t smem = size_t(n) * sizeof(uint64_t);
-  cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  launch(embed_sort_kernel, 1, 1024, smem, s, ids, T, V, sorted, errflag());
-  XT_TRY(check_launch("xt_embedding_bwd sort"));
+  const int64_t blocks = V < int64_t(num_sms()) * 4 ? V : int64_t(num_sms()) * 4;
+  const int64_t per = ceil_div(V, blocks);
+  const size_t smem = size_t(T) * 2 * sizeof(int);
 #define XT_EMB(TH, TG)                                                                                      \
   do {                                                                                                      \
-    launch(embed_scatter_kernel<TH, TG>, unsigned(T), 256, 0, s, sorted, static_cast<const TH*>(dh),            \
-                                                             static_cast<TG*>(dE), T, d, V);                \
-    XT_TRY(check_launch("xt_embedding_bwd scatter"));                                                       \
+    cudaFuncSetAttribute(embed_bwd_kernel<TH, TG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));  \
+    launch(embed_bwd_kernel<TH, TG>, unsigned(ceil_div(V, per)), kEmbThreads, smem, s, ids,                 \
+           static_cast<const TH*>(dh), static_cast<TG*>(dE), int(T), d, V, per, errflag());                 \
+    XT_TRY(check_launch("xt_embedding_bwd"));                                                               \
     if (dP) {                                                                                               \
       int64_t gp = ceil_div(int64_t(S) * d, 256);                                                           \
       launch(embed_pos_kernel<TH, TG>, unsigned(gp), 256, 0, s, static_cast<const TH*>(dh), static_cast<TG*>(dP), \
