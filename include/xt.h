@@ -258,6 +258,14 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
  * scalars.  dlogits may alias logits (in place) when dt_grad == dt.
  * ------------------------------------------------------------------------------- */
 int xt_cross_entropy_workspace_size(int64_t rows, size_t* bytes);
+/* Forward and backward in one pass over the logits (for the loss at the root of a training
+ * graph): the results of xt_cross_entropy_fwd followed by xt_cross_entropy_bwd with acc = 0
+ * (lse, loss, dlogits; dlogits may be logits), up to float32 summation order.  Each row is
+ * held in shared memory while its lse and gradient are formed, so the logits are read from
+ * HBM once; rows of more than 200 KB, or dt ≠ dt_grad, take the two-kernel path. */
+int xt_cross_entropy_fwd_bwd(const void* logits, const int32_t* targets, float* lse, float* loss,
+                             const float* upstream, void* dlogits, int64_t rows, int64_t V, int dt,
+                             int dt_grad, void* ws, void* stream);
 int xt_cross_entropy_fwd(const void* logits, const int32_t* targets, float* lse, float* loss,
                          int64_t rows, int64_t V, int dt, void* ws, void* stream);
 int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float* lse,

@@ -257,6 +257,27 @@ def test_cross_entropy(dtype, rows, V):
     assert np.max(np.abs(host(DXa) - 1 - dx)) <= 1e-5 * np.max(np.abs(dx)) + 1e-7
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,V", [(3, 64), (37, 1000), (7, 1001), (64, 50304), (5, 128256)])
+def test_cross_entropy_fwd_bwd_fused(dtype, rows, V):
+    """The one-pass forward + backward (the row held in shared memory) against the oracle, in
+    place as the block runs it; rows that are not whole 16-byte vectors or exceed 200 KB
+    (1001; float32 50304; 128256) take the two-kernel path."""
+    x = inputs((rows, V), 21, dtype, std=2.0)
+    t = synth.uniform_ids(rows, V, 22)
+    loss, lse = O.cross_entropy_fwd(x, t)
+    X, Tg = dev(x, dtype), torch.tensor(t, device="cuda")
+    LSE, L = empty((rows,), "f32"), empty((1,), "f32")
+    up = torch.tensor([1.3], device="cuda")
+    xt.xt_cross_entropy_fwd_bwd(X, Tg, LSE, L, up, X); sync()
+    assert xt.device_errors() == 0
+    check(host(LSE), lse, "f32", "lse")
+    assert abs(host(L)[0] - loss) <= 1e-5 * abs(loss)
+    dx = O.cross_entropy_bwd(x, t, np.float32(host(LSE)).astype(np.float64), np.float32(1.3))
+    rel = 1e-5 if dtype == "f32" else 2.0 ** -8
+    assert np.all(np.abs(host(X) - dx) <= rel * np.abs(dx) + 1e-6 * 1.3 / rows), "fused ce dx"
+
+
 def test_cross_entropy_bad_target_sets_flag():
     xt.clear_device_errors()
     x = dev(np.zeros((4, 64)))

@@ -410,7 +410,12 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
                           site_seed(c, l, kSiteFfn), drop, stream));
   }
   XT_TRY(matmul(logits_fwd(m), b.hf, prm->E, b.logits, b.ws_mm, b.ws_mm_bytes, s));
-  return xt_cross_entropy_fwd(b.logits, targets, b.lse, loss, T, m.V, m.dt, b.ws_ce, stream);
+  // The loss is the graph's root and the backward seeds it with 1, so the forward forms the
+  // loss and dlogits in one pass over the logits (dlogits overwrite them in place).
+  launch(set_scalar, 1, 1, 0, s, b.one, 1.f);
+  XT_TRY(check_launch("xt_block_fwd"));
+  return xt_cross_entropy_fwd_bwd(b.logits, targets, b.lse, loss, b.one, b.logits, T, m.V, m.dt, m.dt, b.ws_ce,
+                                  stream);
 }
 
 int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const int32_t* ids, const int32_t* targets,
@@ -425,10 +430,8 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   cudaStream_t s = as_stream(stream);
   const int64_t T = m.T, d = m.d, e = m.e;
   const bool drop = c.training && c.p > 0.f;
-  // loss → logits (in place: dlogits overwrite the logits) → tied embedding and final norm
-  launch(set_scalar, 1, 1, 0, s, b.one, 1.f);
-  XT_TRY(check_launch("xt_block_bwd"));
-  XT_TRY(xt_cross_entropy_bwd(b.logits, targets, b.lse, b.one, b.logits, T, m.V, m.dt, m.dt, 0, stream));
+  // dlogits are in the logits buffer (written by the forward's cross-entropy pass) → tied
+  // embedding and final norm
   XT_TRY(matmul(logits_de(m), b.logits, b.hf, prm->dE, b.ws_mm, b.ws_mm_bytes, s));
   XT_TRY(matmul(logits_dhf(m), b.logits, prm->E, b.gA, b.ws_mm, b.ws_mm_bytes, s));
   // Each norm backward also writes the gradient the residual dropout before it passes on: the

@@ -882,6 +882,90 @@ __global__ void __launch_bounds__(256) ce_bwd_kernel(const T* x, const int32_t* 
   }
 }
 
+// Forward and backward of the mean cross-entropy in one pass over the logits (training, the
+// loss being the graph's root): one block per row at a time holds the row in shared memory
+// (read from HBM once), forms max, Σ exp(x − max) and lse from it, writes lse[r] and
+// nll[r] = lse − x[t], then dx = (upstream / rows)·(exp(x − lse) − onehot(t)) (dx may be x).
+constexpr int kCeFusedThreads = 512;
+
+template <typename T, typename TG>
+__global__ void __launch_bounds__(kCeFusedThreads) ce_fused_kernel(const T* x, const int32_t* __restrict__ tgt,
+                                                                   float* __restrict__ lse, float* __restrict__ nll,
+                                                                   const float* __restrict__ upstream, TG* dx,
+                                                                   int64_t rows, int64_t V, uint32_t* flag) {
+  pdl_begin();
+  extern __shared__ __align__(16) uint8_t ce_row_raw[];
+  T* row_s = reinterpret_cast<T*>(ce_row_raw);
+  __shared__ float red[kCeFusedThreads / 32];
+  constexpr int VW = 16 / sizeof(T);
+  const float sc = *upstream / float(rows);
+  const int64_t nvec = V / VW;  // V % VW == 0 (checked on the host)
+  auto block_reduce = [&](float v, bool is_max) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float w = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, w) : v + w;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int i = 1; i < kCeFusedThreads / 32; ++i) r = is_max ? fmaxf(r, red[i]) : r + red[i];
+    return r;
+  };
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T* xr = x + r * V;
+    // 1. the row into shared memory (16-byte vectors, several in flight), running max
+    float m = -INFINITY;
+    for (int64_t j = threadIdx.x; j < nvec; j += kCeFusedThreads) {
+      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(xr) + j);
+      reinterpret_cast<uint4*>(row_s)[j] = u;
+      float v[VW];
+      load_vec<T, VW>(reinterpret_cast<const T*>(&u), v);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) m = fmaxf(m, v[e]);
+    }
+    m = block_reduce(m, true);
+    // 2. Σ exp(x − max) from shared memory
+    const float ml = m * kLog2e;
+    float s = 0.f;
+    for (int64_t j = threadIdx.x; j < nvec; j += kCeFusedThreads) {
+      float v[VW];
+      load_vec<T, VW>(row_s + j * VW, v);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) s += fast_exp2(fmaf(v[e], kLog2e, -ml));
+    }
+    s = block_reduce(s, false);
+    const float L = m + logf(s);
+    const int32_t t = tgt[r];
+    const bool bad = t < 0 || int64_t(t) >= V;
+    if (threadIdx.x == 0) {
+      lse[r] = L;
+      if (bad) {
+        flag_error(flag, XT_DEVERR_INDEX);
+        nll[r] = __int_as_float(0x7fc00000);
+      } else {
+        nll[r] = L - to_f(row_s[t]);
+      }
+    }
+    // 3. the gradient from shared memory
+    const float Ll = L * kLog2e;
+    TG* dr = dx + r * V;
+    for (int64_t j = threadIdx.x; j < nvec; j += kCeFusedThreads) {
+      const int64_t c = j * VW;
+      float v[VW], o[VW];
+      load_vec<T, VW>(row_s + c, v);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        const float pr = fast_exp2(fmaf(v[e], kLog2e, -Ll));
+        o[e] = bad ? __int_as_float(0x7fc00000) : sc * (pr - (c + e == t ? 1.f : 0.f));
+      }
+      store_vec<TG, VW>(dr + c, o);
+    }
+    __syncthreads();  // the next row overwrites the shared row
+  }
+}
+
 // ============================================================================== RoPE
 
 __global__ void rope_table_kernel(float* table, int S, int hd, double base, int pos_offset) {
@@ -999,13 +1083,24 @@ __global__ void __launch_bounds__(kEmbThreads) embed_bwd_kernel(const int32_t* _
   const int64_t v0 = int64_t(blockIdx.x) * per;
   const int64_t v1 = v0 + per < V ? v0 + per : V;
   if (threadIdx.x == 0) total = 0;
+  // every id this thread inspects is loaded first (one memory latency, not one per round)
+  constexpr int kPer = kSortMax / kEmbThreads;
+  int32_t idv[kPer];
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int t = r * kEmbThreads + int(threadIdx.x);
+    idv[r] = t < T_ ? __ldg(ids + t) : 0;
+  }
   __syncthreads();
-  for (int base = 0; base < T_; base += kEmbThreads) {
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int base = r * kEmbThreads;
+    if (base >= T_) break;
     const int t = base + int(threadIdx.x);
     bool m = false;
     int32_t id = 0;
     if (t < T_) {
-      id = ids[t];
+      id = idv[r];
       const bool bad = id < 0 || int64_t(id) >= V;
       if (bad && blockIdx.x == 0) flag_error(flag, XT_DEVERR_INDEX);
       m = !bad && int64_t(id) >= v0 && int64_t(id) < v1;
@@ -1501,6 +1596,43 @@ int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float
   else XT_CE_BWD(float, bf16);
 #undef XT_CE_BWD
   return check_launch("xt_cross_entropy_bwd");
+}
+
+static bool ce_fused_fits(int64_t V, int dt) {
+  const size_t e = dtype_size(dt);
+  return valid_dtype(dt) && V % int64_t(16 / e) == 0 && size_t(V) * e <= size_t(200) * 1024;
+}
+
+int xt_cross_entropy_fwd_bwd(const void* logits, const int32_t* targets, float* lse, float* loss, const float* upstream,
+                             void* dlogits, int64_t rows, int64_t V, int dt, int dt_grad, void* ws, void* stream) {
+  XT_REQUIRE(valid_dtype(dt) && valid_dtype(dt_grad), "xt_cross_entropy_fwd_bwd: bad dtype");
+  XT_REQUIRE(rows > 0 && V > 0, "xt_cross_entropy_fwd_bwd: bad sizes");
+  XT_REQUIRE(logits && targets && lse && loss && upstream && dlogits && ws, "xt_cross_entropy_fwd_bwd: NULL pointer");
+  XT_REQUIRE(!(logits == dlogits && dt != dt_grad), "xt_cross_entropy_fwd_bwd: in-place needs equal dtypes");
+  cudaStream_t s = as_stream(stream);
+  if (!ce_fused_fits(V, dt) || dt != dt_grad || !aligned16(logits) || !aligned16(dlogits)) {
+    // rows that do not fit the single pass: the forward then the backward
+    XT_TRY(xt_cross_entropy_fwd(logits, targets, lse, loss, rows, V, dt, ws, stream));
+    return xt_cross_entropy_bwd(logits, targets, lse, upstream, dlogits, rows, V, dt, dt_grad, 0, stream);
+  }
+  const size_t smem = size_t(V) * dtype_size(dt);
+  int64_t grid = rows;
+  const int64_t cap = int64_t(num_sms()) * 2;
+  if (grid > cap) grid = cap;
+  float* nll = static_cast<float*>(ws);
+  uint32_t* flag = errflag();
+  if (dt == XT_BF16) {
+    cudaFuncSetAttribute(ce_fused_kernel<bf16, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    launch(ce_fused_kernel<bf16, bf16>, int(grid), kCeFusedThreads, smem, s, static_cast<const bf16*>(logits),
+           targets, lse, nll, upstream, static_cast<bf16*>(dlogits), rows, V, flag);
+  } else {
+    cudaFuncSetAttribute(ce_fused_kernel<float, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    launch(ce_fused_kernel<float, float>, int(grid), kCeFusedThreads, smem, s, static_cast<const float*>(logits),
+           targets, lse, nll, upstream, static_cast<float*>(dlogits), rows, V, flag);
+  }
+  XT_TRY(check_launch("xt_cross_entropy_fwd_bwd"));
+  launch(ce_loss_kernel, 1, 1024, 0, s, static_cast<const float*>(nll), rows, loss);
+  return check_launch("xt_cross_entropy_fwd_bwd loss");
 }
 
 int xt_rope_table(float* table, int S, int hd, double base, int pos_offset, void* stream) {

@@ -117,6 +117,7 @@ _SIGS = {
                          _I, _I, _I, _I, _I, _I, _VP],
     "xt_cross_entropy_workspace_size": [_I64, _SZP],
     "xt_cross_entropy_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _I, _VP, _VP],
+    "xt_cross_entropy_fwd_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _VP],
     "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
     "xt_dropout_fwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _VP],
     "xt_dropout_bwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _I, _VP],
@@ -468,6 +469,15 @@ def xt_cross_entropy_fwd(logits, targets, lse, loss, ws=None, s=None):
         ws = workspace(ws_bytes("xt_cross_entropy_workspace_size", rows), logits.device)
     call("xt_cross_entropy_fwd", ptr(logits), ptr(targets), ptr(lse), ptr(loss), rows, V, dt(logits), ptr(ws),
          stream(s))
+
+
+def xt_cross_entropy_fwd_bwd(logits, targets, lse, loss, upstream, dlogits, ws=None, s=None):
+    """Forward and backward in one pass (dlogits may be logits)."""
+    rows, V = logits.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_cross_entropy_workspace_size", rows), logits.device)
+    call("xt_cross_entropy_fwd_bwd", ptr(logits), ptr(targets), ptr(lse), ptr(loss), ptr(upstream), ptr(dlogits),
+         rows, V, dt(logits), dt(dlogits), ptr(ws), stream(s))
 
 
 def xt_cross_entropy_bwd(logits, targets, lse, upstream, dlogits, acc=0, s=None):
