@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -355,7 +356,8 @@ def run_ours(args, rank, world, local_rank):
         "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
         "frac": (tflops / peak) if tflops else None, "peak_source": f"{peak_src} "
         f"({'bf16 sustained' if cfg['dtype'] == 'bf16' else 'bf16 sustained x 1.1/2.25 for tf32'})",
-        "traffic": None, "launches_per_step": len(gms),
+        "traffic": gemm_traffic_per_launch(args.workload), "traffic_unit": "bytes per GEMM launch (ncu, step mean)",
+        "launches_per_step": len(gms),
         "share_of_step": gemm_ms_step / ms_prof, "gemm_tflop_per_step": float(np.sum(flops)) / 1e12,
         "measured_in": (f"second pass of {args.steps} graph replays with a CUDA event before and after every GEMM "
                         f"launch (events captured into the graph); that pass ran {ms_prof:.3f} ms/step, the "
@@ -381,6 +383,27 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def gemm_traffic_per_launch(workload):
+    """Mean DRAM bytes (read + write) per GEMM launch of the step from the committed ncu capture
+    (profiles/gemm_step_dram_traffic_gpt12.md), or None when the workload differs or the GEMM
+    sources changed since the counters were taken."""
+    import hashlib
+    if workload != "gpt12":
+        return None
+    path = os.path.join(ROOT, "profiles", "gemm_step_dram_traffic_gpt12.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    mb = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
+    mh = re.search(r"gemm_sources_sha256_16: ([0-9a-f]+)", txt)
+    if not (mb and mh):
+        return None
+    csrc = os.path.join(ROOT, "transformer_fwd_bwd_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, "gemm_kernel.cuh"), "rb").read() +
+                       open(os.path.join(csrc, "gemm.cu"), "rb").read()).hexdigest()[:16]
+    return int(mb.group(1)) if h == mh.group(1) else None
 
 
 def gemm_by_shape(flops, gms, shapes, top=12):
