@@ -86,13 +86,14 @@ static int next_pow2(int64_t v) {
   return p;
 }
 
-// Plans a row-resident launch: vector width, threads per row, block size, rows per block.
-static RowPlan plan_rows(int64_t cols, int vw, int max_tpr = 1024) {
+// Plans a row-resident launch: vector width, threads per row, block size, rows per block; nv is
+// the most vectors a thread holds (≤ NV).
+static RowPlan plan_rows(int64_t cols, int vw, int max_tpr = 1024, int nv = NV) {
   RowPlan pl{};
   pl.vw = vw;
   const int64_t nvec = ceil_div(cols, vw);
-  if (nvec > int64_t(NV) * max_tpr) { pl.ok = false; return pl; }
-  int tpr = next_pow2(ceil_div(nvec, NV));
+  if (nvec > int64_t(nv) * max_tpr) { pl.ok = false; return pl; }
+  int tpr = next_pow2(ceil_div(nvec, nv));
   if (tpr < 32) tpr = 32;
   pl.tpr = tpr;
   pl.threads = tpr < 256 ? 256 : tpr;
@@ -344,10 +345,15 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 // LayerNorm backward, one row group per row: NVT vectors per thread.  The row's old residual
 // gradient (acc_dx) is prefetched into L1 with d and x, so the accumulate after the two row
-// reductions does not start a second trip to L2.  dγ and dβ partials stay in registers for the
+// reductions does not start a second trip to L2.  A row of 8 KB or more also has the group's next
+// row prefetched into L2 while it is processed, so that row's loads do not wait on HBM (shorter
+// rows measured slower with it: the prefetches cost more issue slots than the latency they hide).  dγ and dβ partials stay in registers for the
 // thread's fixed columns across all of its rows; the row groups' partials meet in shared memory
 // once, at the end, and are folded in group order.
 template <typename T, typename TD, int VW, int NVT, int MAXT>
@@ -367,9 +373,23 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) ln_bwd_kernel(const
 #pragma unroll
     for (int e = 0; e < VW; ++e) ag[k][e] = ab[k][e] = 0.f;
   const float inv_n = 1.f / float(cols);
-  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += int64_t(gridDim.x) * rpb) {
+  const int64_t step = int64_t(gridDim.x) * rpb;
+  const bool pf = cols * int64_t(sizeof(T)) >= 8192;
+  for (int64_t r0 = int64_t(blockIdx.x) * rpb; r0 < rows; r0 += step) {
     const int64_t r = r0 + grp;
     const bool act = r < rows;
+    if (pf && r + step < rows) {
+      const int64_t rn = r + step;
+#pragma unroll
+      for (int k = 0; k < NVT; ++k) {
+        const int64_t j = l + int64_t(k) * tpr;
+        if (j < nvec) {
+          prefetch_l2(d + rn * cols + j * VW);
+          prefetch_l2(x + rn * cols + j * VW);
+          if (dx && acc_dx) prefetch_l2(dx + rn * cols + j * VW);
+        }
+      }
+    }
     const float mu = act ? mean[r] : 0.f, rs = act ? rstd[r] : 0.f;
     Raw<T, VW> vd[NVT], vx[NVT];
     float sg = 0.f, sgx = 0.f;
@@ -1205,8 +1225,22 @@ constexpr int kBwdMaxTpr = 512;  // backward row kernels hold two rows + partial
     }                                                                          \
   } while (0)
 
-static size_t norm_ws_floats(int64_t rows, int64_t cols, int vw) {
+// LayerNorm backward plan: a bf16 row that the default plan gives four vectors per thread runs
+// with twice the threads and two vectors each instead, since four vectors of bf16 plus both
+// sets of (dγ, dβ) partials do not fit in the 128 registers of two resident blocks, as long as
+// that stays within 256-thread blocks (a 512-thread row, one block per SM, measured slower than
+// the spilling plan).
+static RowPlan ln_bwd_plan(int64_t cols, int vw) {
   RowPlan pl = plan_rows(cols, vw, kBwdMaxTpr);
+  if (pl.ok && vw == 8 && ceil_div(ceil_div(cols, vw), pl.tpr) == NV) {
+    const RowPlan p2 = plan_rows(cols, vw, kBwdMaxTpr, 2);
+    if (p2.ok && p2.threads <= 256) pl = p2;
+  }
+  return pl;
+}
+
+static size_t norm_ws_floats(int64_t rows, int64_t cols, int vw, bool ln = false) {
+  RowPlan pl = ln ? ln_bwd_plan(cols, vw) : plan_rows(cols, vw, kBwdMaxTpr);
   if (!pl.ok) return 0;
   return size_t(bwd_blocks(rows, pl.rpb)) * size_t(cols);
 }
@@ -1222,9 +1256,9 @@ int xt_norm_bwd_workspace_size(int64_t rows, int64_t cols, size_t* bytes) {
   XT_REQUIRE(rows >= 0 && cols > 0 && bytes, "xt_norm_bwd_workspace_size: bad arguments");
   // the scalar path (vector width 1) has the most row groups per block: take the max
   size_t f = norm_ws_floats(rows, cols, 1);
-  const size_t f4 = norm_ws_floats(rows, cols, 4), f8 = norm_ws_floats(rows, cols, 8);
-  if (f4 > f) f = f4;
-  if (f8 > f) f = f8;
+  for (const size_t fv : {norm_ws_floats(rows, cols, 4), norm_ws_floats(rows, cols, 8),
+                          norm_ws_floats(rows, cols, 8, true)})
+    if (fv > f) f = fv;
   *bytes = 2 * f * sizeof(float);
   return XT_OK;
 }
@@ -1390,7 +1424,7 @@ static int ln_bwd_impl(const void* d, const void* x, const void* gamma, const fl
     return XT_OK;
   }
   const bool vec = rows_vec_ok(cols, dt, {d, x, gamma, dx});
-  RowPlan pl = plan_rows(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1, kBwdMaxTpr);
+  RowPlan pl = ln_bwd_plan(cols, vec ? (dt == XT_BF16 ? 8 : 4) : 1);
   if (!pl.ok) return fail(XT_ERR_UNSUPPORTED, "xt_layernorm_bwd: row too long");
   // two blocks per SM are resident (128 registers × 256 threads), and the partials live in
   // registers across rows: more blocks would only add partial rows to fold
