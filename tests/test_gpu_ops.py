@@ -44,6 +44,26 @@ def check_sum(g, r, abs_sum, dtype, what=""):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+def test_gelu_paired_matches_scalar(dtype):
+    """The 16-byte-aligned path evaluates GELU's erfc polynomial two elements per paired FMA; an
+    unaligned view takes the one-element path. Each lane of a paired FMA rounds as the scalar FMA
+    does, so the two must agree bit for bit."""
+    n = 8 * 4101
+    a = inputs((n,), 31, dtype) * 3
+    d = inputs((n,), 32, dtype)
+    A, D = dev(a, dtype), dev(d, dtype)
+    y1, y2 = empty((n,), dtype), empty((n,), dtype)
+    xt.xt_gelu_fwd(A, y1)
+    xt.xt_gelu_fwd(A[1:], y2[1:])
+    sync()
+    assert torch.equal(y1[1:], y2[1:])
+    xt.xt_gelu_bwd(D, A, y1)
+    xt.xt_gelu_bwd(D[1:], A[1:], y2[1:])
+    sync()
+    assert torch.equal(y1[1:], y2[1:])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("n", [1, 37, 4101, 768 * 1024])
 def test_elementwise(dtype, n):
     a = inputs((n,), 1, dtype) * 2

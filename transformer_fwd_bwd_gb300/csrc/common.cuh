@@ -221,6 +221,34 @@ __device__ __forceinline__ float erfc_poly(float z, float& t) {
   q = fmaf(q, t, 1.00002368f);
   return fmaf(q, t, -1.26551223f);
 }
+// Two fp32 lanes in one 64-bit register for the paired FP32 instructions of sm_100+ (PTX
+// fma.rn.f32x2): each lane is rounded as the scalar fma.rn.f32 rounds it, so a pair of Horner
+// chains evaluated this way is bit-identical to two scalar chains, in half the issue slots.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// erfc_poly for two arguments at once (the same operations, the Horner steps paired).
+__device__ __forceinline__ void erfc_poly2(float z0, float z1, float& t0, float& t1, float& q0, float& q1) {
+  t0 = __fdividef(1.f, fmaf(0.5f, z0, 1.f));
+  t1 = __fdividef(1.f, fmaf(0.5f, z1, 1.f));
+  const uint64_t t = f32x2_pack(t0, t1);
+  constexpr float c[9] = {-0.82215223f, 1.48851587f, -1.13520398f, 0.27886807f, -0.18628806f,
+                          0.09678418f,  0.37409196f, 1.00002368f,  -1.26551223f};
+  uint64_t q = f32x2_pack(0.17087277f, 0.17087277f);
+#pragma unroll
+  for (int k = 0; k < 9; ++k) q = f32x2_fma(q, t, f32x2_pack(c[k], c[k]));
+  f32x2_unpack(q, q0, q1);
+}
 // Φ alone: one reciprocal and one exponential.
 __device__ __forceinline__ float gelu_cdf(float x) {
   const float z = fabsf(x) * 0.70710678118654752f;
@@ -237,6 +265,26 @@ __device__ __forceinline__ Gauss gauss(float x) {
   const float e = __expf(-z * z);                    // exp(−x²/2)
   const float half_erfc = 0.5f * t * e * __expf(q);  // ½·erfc(|x|/√2) = Φ(−|x|)
   return Gauss{x <= 0.f ? half_erfc : 1.f - half_erfc, 0.39894228040143268f * e};
+}
+// gelu(x) = x·Φ(x) (MODE 0) or d·gelu′(x) = d·(Φ(x) + x·φ(x)) (MODE 1) for a pair, with the
+// expressions of gelu_cdf / gauss around the paired polynomial.
+template <int MODE>
+__device__ __forceinline__ void gelu_pair(float x0, float x1, float d0, float d1, float& r0, float& r1) {
+  const float z0 = fabsf(x0) * 0.70710678118654752f, z1 = fabsf(x1) * 0.70710678118654752f;
+  float t0, t1, q0, q1;
+  erfc_poly2(z0, z1, t0, t1, q0, q1);
+  if constexpr (MODE == 0) {
+    const float h0 = 0.5f * t0 * __expf(fmaf(-z0, z0, q0));
+    const float h1 = 0.5f * t1 * __expf(fmaf(-z1, z1, q1));
+    r0 = x0 * (x0 <= 0.f ? h0 : 1.f - h0);
+    r1 = x1 * (x1 <= 0.f ? h1 : 1.f - h1);
+  } else {
+    const float e0 = __expf(-z0 * z0), e1 = __expf(-z1 * z1);
+    const float h0 = 0.5f * t0 * e0 * __expf(q0), h1 = 0.5f * t1 * e1 * __expf(q1);
+    const float c0 = x0 <= 0.f ? h0 : 1.f - h0, c1 = x1 <= 0.f ? h1 : 1.f - h1;
+    r0 = d0 * fmaf(x0, 0.39894228040143268f * e0, c0);
+    r1 = d1 * fmaf(x1, 0.39894228040143268f * e1, c1);
+  }
 }
 
 

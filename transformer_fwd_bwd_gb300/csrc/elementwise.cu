@@ -103,8 +103,16 @@ __global__ void __launch_bounds__(256) ew_kernel(EwArgs g) {
       if constexpr (IO::A) V8<TI>::load(a + i0, va);
       if constexpr (IO::B) V8<TI>::load(b + i0, vb);
       if constexpr (IO::C) V8<TI>::load(c + i0, vc);
+      if constexpr (OP == EW_GELU) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ew_apply<OP>(va[j], vb[j], vc[j], uint64_t(i0 + j), g, r0[j], r1[j]);
+        for (int j = 0; j < 8; j += 2) gelu_pair<0>(va[j], va[j + 1], 0.f, 0.f, r0[j], r0[j + 1]);
+      } else if constexpr (OP == EW_GELU_BWD) {
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) gelu_pair<1>(vb[j], vb[j + 1], va[j], va[j + 1], r0[j], r0[j + 1]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ew_apply<OP>(va[j], vb[j], vc[j], uint64_t(i0 + j), g, r0[j], r1[j]);
+      }
       if (o0) {
         if (acc0) {
           float old[8];
