@@ -110,3 +110,125 @@ def test_dropout_sites_use_distinct_masks():
     a = D.keep_mask(n, 0.5, D.site_seed(0x5EED, 0, D.SITE_ATTN))
     f = D.keep_mask(n, 0.5, D.site_seed(0x5EED, 0, D.SITE_FFN))
     assert not np.array_equal(a, f)
+
+
+# ----------------------------------------------------------------------------- structure pins
+#
+# The finite-difference pin above holds for any forward (the tape derives the backward from
+# whatever graph is built), so the stack's structure is pinned separately: closed forms that
+# follow when some weights are zero, written with the separately pinned ops and cumulative
+# sums rather than with the stack's own code, and the causality / per-sequence invariants.
+
+VARIANTS = ["rms_swiglu", "ln_gelu_pos"]
+
+
+def _variant(name, **over):
+    if name == "rms_swiglu":
+        cfg = _tiny(B=2, S=6, n_layers=2)
+    else:
+        cfg = _tiny(B=2, S=6, norm="ln", mlp="gelu", rope=False, learned_pos=True, n_layers=2)
+    cfg.update(over)
+    return cfg
+
+
+def _down(cfg):
+    return "Wd" if cfg["mlp"] == "swiglu" else "W2"
+
+
+def _norm(cfg, x, g, b):
+    if cfg["norm"] == "rms":
+        return O.rms_norm_fwd(x, g, cfg["eps"])[0]
+    return O.layernorm_fwd(x, g, b, cfg["eps"])[0]
+
+
+def _params(cfg, seed=3):
+    """Block weights at N(0, 0.3) (large enough that every path moves the loss), gains jittered."""
+    params = synth.block_params(cfg, gain_jitter=0.1)
+    r = np.random.default_rng(seed)
+    for k, v in params.items():
+        if v.ndim == 2 and k not in ("E", "P"):
+            params[k] = r.normal(0.0, 0.3, size=v.shape)
+    return params
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_block_zero_sublayers_is_residual_identity(variant):
+    """Every W_O and MLP down projection zero: each sub-block adds exactly zero to the residual
+    stream (its dropout, p = 0.3, acts on that zero), so the stack is embed → final norm → tied
+    logits → mean cross-entropy, computed here from those ops alone."""
+    cfg = _variant(variant, p=0.3)
+    params = _params(cfg)
+    for l in range(cfg["n_layers"]):
+        params[f"l{l}.Wo"] = np.zeros_like(params[f"l{l}.Wo"])
+        params[f"l{l}.{_down(cfg)}"] = np.zeros_like(params[f"l{l}.{_down(cfg)}"])
+    ids, tgt = synth.block_tokens(cfg)
+    h0 = O.embedding_fwd(ids, params["E"], params.get("P"), cfg["S"])
+    hf = _norm(cfg, h0, params["gf"], params.get("bf"))
+    want, _ = O.cross_entropy_fwd(hf @ params["E"].T, tgt)
+    got = OB.loss_only(cfg, params, ids, tgt, base_seed=7, training=True)
+    assert got == pytest.approx(want, rel=1e-12)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_block_uniform_attention_closed_form(variant):
+    """W_Q = W_K = 0 makes every visible score 0, so causal attention is the plain mean of the
+    values at positions 0..s (the softmax of a row of zeros is uniform over the visible keys);
+    with the MLP's down projection zero as well, layer 0 outputs
+    h0 + runningmean_s(norm1(h0) W_V) W_O per sequence, written here with cumulative sums."""
+    cfg = _variant(variant, n_layers=1)
+    params = _params(cfg)
+    B, S, d = cfg["B"], cfg["S"], cfg["d"]
+    params["l0.Wq"] = np.zeros((d, d))
+    params["l0.Wk"] = np.zeros((d, d))
+    params[f"l0.{_down(cfg)}"] = np.zeros_like(params[f"l0.{_down(cfg)}"])
+    ids, tgt = synth.block_tokens(cfg)
+    keep = {}
+    OB.model_loss(cfg, params, ids, tgt, keep=keep)
+    h0 = O.embedding_fwd(ids, params["E"], params.get("P"), S)
+    v = (_norm(cfg, h0, params["l0.g1"], params.get("l0.b1")) @ params["l0.Wv"]).reshape(B, S, d)
+    mean = np.cumsum(v, axis=1) / np.arange(1, S + 1)[None, :, None]
+    want = h0 + mean.reshape(B * S, d) @ params["l0.Wo"]
+    assert np.allclose(keep["h1"].value, want, rtol=1e-12, atol=1e-14)
+
+
+def test_block_heads_are_separate():
+    """Query / key weights nonzero only in head 0's columns: head 1 scores zero everywhere, so
+    its output columns are the running mean of its own value columns, while head 0's are not.
+    W_O = I and a zero MLP down projection expose the merged head outputs as h1 − h0."""
+    cfg = _variant("ln_gelu_pos", n_layers=1)
+    params = _params(cfg)
+    d, hd, B, S = cfg["d"], cfg["hd"], cfg["B"], cfg["S"]
+    for w in ("Wq", "Wk"):
+        params[f"l0.{w}"][:, hd:] = 0.0
+    params["l0.Wo"] = np.eye(d)
+    params["l0.W2"] = np.zeros_like(params["l0.W2"])
+    ids, tgt = synth.block_tokens(cfg)
+    keep = {}
+    OB.model_loss(cfg, params, ids, tgt, keep=keep)
+    h0 = O.embedding_fwd(ids, params["E"], params["P"], S)
+    o = (keep["h1"].value - h0).reshape(B, S, d)
+    v = (_norm(cfg, h0, params["l0.g1"], params["l0.b1"]) @ params["l0.Wv"]).reshape(B, S, d)
+    mean = np.cumsum(v, axis=1) / np.arange(1, S + 1)[None, :, None]
+    assert np.allclose(o[..., hd:], mean[..., hd:], rtol=1e-10, atol=1e-12)
+    assert not np.allclose(o[..., :hd], mean[..., :hd], rtol=1e-3, atol=1e-6)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_block_logits_causal_and_per_sequence(variant):
+    """Changing the token at position j of sequence 0 leaves that sequence's logits before j
+    and every logit of sequence 1 unchanged, and changes the logits from j on."""
+    cfg = _variant(variant)
+    params = _params(cfg)
+    B, S, V = cfg["B"], cfg["S"], cfg["V"]
+    ids, tgt = synth.block_tokens(cfg)
+    j = 3
+    ids2 = ids.copy()
+    ids2[j] = (ids2[j] + 1) % V
+    k0, k1 = {}, {}
+    OB.model_loss(cfg, params, ids, tgt, keep=k0)
+    OB.model_loss(cfg, params, ids2, tgt, keep=k1)
+    L0, L1 = k0["logits"].value.reshape(B, S, V), k1["logits"].value.reshape(B, S, V)
+    assert np.allclose(L1[0, :j], L0[0, :j], rtol=1e-13, atol=1e-15)
+    assert np.allclose(L1[1], L0[1], rtol=1e-13, atol=1e-15)
+    for s in range(j, S):
+        assert not np.allclose(L1[0, s], L0[0, s], rtol=1e-6, atol=1e-9)

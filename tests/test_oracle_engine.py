@@ -245,3 +245,13 @@ def test_site_seeds():
     assert D.site_seed(0x5EED, 0, D.SITE_ATTN) == 0x5EED ^ 0xA77
     assert D.site_seed(0x5EED, 3, D.SITE_FFN) == 0x5EED ^ 3 ^ 0xF70
     assert D.site_seed(1, 0, D.SITE_ATTN) != D.site_seed(1, 0, D.SITE_FFN)
+
+
+def test_dropout_keep_boundary():
+    """keep = (u ≥ p): with p equal to one element's u (a multiple of 2⁻²⁴, exact in float32)
+    that element is kept, and with p one float32 step above it, dropped."""
+    seed = 0x5EED ^ 0xF70
+    u = D.uniforms(4096, seed)
+    j = int(np.argmin(np.abs(u - np.float32(0.37))))
+    assert D.keep_mask(4096, float(u[j]), seed)[j]
+    assert not D.keep_mask(4096, float(np.nextafter(u[j], np.float32(1.0))), seed)[j]

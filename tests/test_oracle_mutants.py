@@ -9,6 +9,7 @@ import oracle.dropout as D
 import oracle.fp8 as F8
 import oracle.ops as O
 import oracle.optim as OP
+import oracle.tape as T
 from tests import test_oracle_block as TB
 from tests import test_oracle_engine as TE
 from tests import test_oracle_ops as TO
@@ -123,6 +124,82 @@ def _fp8_no_saturation(x):
     return out
 
 
+def _gelu_tanh(x):
+    # the tanh approximation instead of the erf definition
+    x = np.asarray(x, float)
+    return 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))
+
+
+def _rms_eps_outside(x, gamma, eps):
+    x = np.asarray(x, float)
+    ir = 1.0 / (np.sqrt(np.mean(x * x, axis=-1)) + eps)
+    return x * ir[..., None] * gamma, ir
+
+
+def _ln_unbiased(x, gamma, beta, eps):
+    x = np.asarray(x, float)
+    mu = np.mean(x, axis=-1)
+    xc = x - mu[..., None]
+    rstd = 1.0 / np.sqrt(np.sum(xc * xc, axis=-1) / (x.shape[-1] - 1) + eps)
+    return xc * rstd[..., None] * gamma + beta, mu, rstd
+
+
+def _rope_half_frequency(positions, hd, base):
+    i = np.arange(hd // 2, dtype=np.float64)
+    return np.asarray(positions, float)[..., None] * base ** (-i / hd)
+
+
+def _causal_diagonal_hidden(q_len, k_len):
+    return np.arange(k_len)[None, :] < np.arange(q_len)[:, None]
+
+
+def _ce_sum(x, targets):
+    loss, lse = _ce_sum.__wrapped__(x, targets)
+    return loss * np.asarray(x).shape[0], lse
+
+
+def _embed_no_pos(ids, E, P=None, S=None):
+    return _embed_no_pos.__wrapped__(ids, E)
+
+
+def _attention_scale_hd(q, k, v, causal=True):
+    q, k, v = (np.asarray(a, float) for a in (q, k, v))
+    scores = np.einsum("bhsd,bhtd->bhst", q, k) / q.shape[-1]
+    P = O.softmax_fwd(scores, causal=causal)
+    return np.einsum("bhst,bhtd->bhsd", P, v), P
+
+
+def _dropout_scale_inverse_p(p):
+    return np.float32(1.0 / float(np.float32(p)))
+
+
+def _keep_strict(n, p, seed):
+    return D.uniforms(n, seed) > np.float32(p)
+
+
+def _site_seed_added(base_seed, layer, site):
+    return (int(base_seed) + int(layer) + int(site)) & 0xFFFFFFFFFFFFFFFF
+
+
+# block structure mistakes, planted in the tape ops the stack is built from
+def _residual_dropped(a, b):
+    return b
+
+
+def _post_norm(a, b):
+    s = _post_norm.__wrapped__(a, b)
+    return T.rms_norm(s, T.leaf(np.ones(s.value.shape[-1])), 1e-5)
+
+
+def _attention_not_causal(q, k, v, causal=True):
+    return _attention_not_causal.__wrapped__(q, k, v, causal=False)
+
+
+def _heads_interleaved(x, B, S, H, hd):
+    # columns read as [hd, H] instead of [H, hd]: every "head" mixes all heads' columns
+    return T.Var(np.transpose(x.value.reshape(B, S, hd, H), (0, 3, 1, 2)), [x], lambda g, ps: None)
+
+
 MUTANTS = [
     ("rms_norm_bwd", _rms_bwd_dropped_term, O, TO.test_rms_norm),
     ("rms_norm_bwd", _rms_bwd_wrong_power, O, TO.test_rms_norm),
@@ -146,6 +223,24 @@ MUTANTS = [
     ("encode", _fp8_ties_away, F8, TF8.test_encode_matches_torch_in_range_and_on_ties),
     ("encode", _fp8_ties_away, F8, TF8.test_printed_constants_and_saturation),
     ("encode", _fp8_no_saturation, F8, TF8.test_printed_constants_and_saturation),
+    ("gelu_fwd", _gelu_tanh, O, TO.test_gelu),
+    ("rms_norm_fwd", _rms_eps_outside, O, TO.test_rms_norm),
+    ("layernorm_fwd", _ln_unbiased, O, TO.test_layernorm),
+    ("rope_angles", _rope_half_frequency, O, TO.test_rope_identities),
+    ("causal_mask", _causal_diagonal_hidden, O, TO.test_softmax_causal),
+    ("cross_entropy_fwd", _ce_sum, O, TO.test_cross_entropy),
+    ("embedding_fwd", _embed_no_pos, O, TO.test_embedding),
+    ("attention_fwd", _attention_scale_hd, O, TO.test_attention_composed),
+    ("scale_f32", _dropout_scale_inverse_p, D, TE.test_dropout_expectation_and_identities),
+    ("keep_mask", _keep_strict, D, TE.test_dropout_keep_boundary),
+    ("site_seed", _site_seed_added, D, TE.test_site_seeds),
+    ("add", _residual_dropped, T, lambda: TB.test_block_zero_sublayers_is_residual_identity("rms_swiglu")),
+    ("add", _residual_dropped, T, lambda: TB.test_block_zero_sublayers_is_residual_identity("ln_gelu_pos")),
+    ("add", _post_norm, T, lambda: TB.test_block_uniform_attention_closed_form("rms_swiglu")),
+    ("add", _post_norm, T, lambda: TB.test_block_uniform_attention_closed_form("ln_gelu_pos")),
+    ("attention", _attention_not_causal, T, lambda: TB.test_block_logits_causal_and_per_sequence("rms_swiglu")),
+    ("attention", _attention_not_causal, T, lambda: TB.test_block_uniform_attention_closed_form("ln_gelu_pos")),
+    ("split_heads", _heads_interleaved, T, TB.test_block_heads_are_separate),
 ]
 
 
