@@ -57,7 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--shape", default="8192,3072,768,0,1",
                     help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--sample-seqs", type=int, default=1, help=argparse.SUPPRESS)
+    # two of the 8 sequences: ≈ 11 s of float64 oracle work on 16 Arm cores
+    ap.add_argument("--sample-seqs", type=int, default=2, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -331,16 +332,22 @@ def run_ours(args, rank, world, local_rank):
     tgt_pin = torch.tensor(tgt_h).pin_memory()
     loss_pin = torch.empty(1, dtype=torch.float32).pin_memory()
     e2e_steps = max(3, args.steps // 2)
-    barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+
+    def e2e_step():
         ids.copy_(ids_pin, non_blocking=True)      # the graph reads ids / tgt in place
         tgt.copy_(tgt_pin, non_blocking=True)
         graph.replay()
         loss_pin.copy_(nb.loss, non_blocking=True)
         torch.cuda.current_stream(dev).synchronize()
-        _ = float(loss_pin[0])
+        return float(loss_pin[0])
+
+    for _ in range(3):   # untimed: first use of the pinned buffers and of this copy path
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
 
     if rank != 0:
