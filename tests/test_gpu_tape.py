@@ -71,6 +71,25 @@ def test_composed_attention_tape(dtype):
         assert norm_err(host(got), want) <= 2e-2
 
 
+def test_composed_attention_tape_full_size_sampled_heads():
+    """The composed attention at the 12-layer stack's size (B 8 × H 12 = 96 heads, S 1024, hd 64, bf16:
+    201 MB of probabilities), dQ, dK, dV on sampled heads against the oracle."""
+    BH, S, hd = 96, 1024, 64
+    q0, k0, v0 = (synth.normal((BH, S, hd), 340 + i, dtype="bf16") for i in range(3))
+    W = synth.normal((BH, S, hd), 343, dtype="bf16")
+    q, k, v = (T.leaf(dev(a, "bf16"), grad_dtype=torch.float32) for a in (q0, k0, v0))
+    out = T.attention(q, k, v, causal=True)
+    T.backward(T.sum_all(T.mul(out, T.leaf(dev(W, "bf16")))))
+    torch.cuda.synchronize()
+    for z in (0, 41, 95):
+        sl = slice(z, z + 1)
+        Ov, P = O.attention_fwd(q0[None, sl], k0[None, sl], v0[None, sl], causal=True)
+        dQ, dK, dV = O.attention_bwd(W[None, sl], q0[None, sl], k0[None, sl], v0[None, sl], P)
+        assert norm_err(host(out.value[z]), Ov[0, 0]) <= 2e-2
+        for got, want in ((q.grad[z], dQ[0, 0]), (k.grad[z], dK[0, 0]), (v.grad[z], dV[0, 0])):
+            assert norm_err(host(got), want) <= 2e-2, z
+
+
 def test_large_vocab_fanout():
     """8192 × 128256 bf16 logits ~ N(0, 2): L = CE(x) + Σ(0.5·x) + Σ(x∘x), all three gradient
     contributions summed into one fp32 buffer, checked on sampled rows against the oracle's
@@ -109,3 +128,41 @@ def test_large_vocab_fanout():
     T.backward(T.cross_entropy(x2, Tg))
     torch.cuda.synchronize()
     assert norm_err(host(x2.grad[rows_d]), ce_part) <= 1e-5
+
+
+def _aliasing_graphs():
+    """Graphs whose reverse walk gives an add's parents their first push from the add and a later
+    push from another consumer ([AE] § 梯度累加: first push sets, later pushes add, per Var)."""
+    def scale_then_add(lib, x, y):
+        return lib.add(lib.sum_all(lib.scale(x, 2.0)), lib.sum_all(lib.add(x, y)))
+
+    def residual_chain(lib, x, y):
+        u, v = lib.scale(x, 3.0), lib.silu(y)
+        s = lib.add(u, v)
+        other = lib.add(lib.sum_all(lib.scale(u, 0.5)), lib.sum_all(lib.mul(v, y)))
+        return lib.add(other, lib.sum_all(lib.mul(s, s)))
+
+    return {"scale_then_add": scale_then_add, "residual_chain": residual_chain}
+
+
+@pytest.mark.parametrize("name", ["scale_then_add", "residual_chain"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tape_add_siblings_own_their_grads(name, dtype):
+    """Both parents of an add are pushed into again after the add's backward: every leaf gradient
+    equals the oracle tape's element by element (each Var owns its gradient buffer)."""
+    build = _aliasing_graphs()[name]
+    x0, y0 = (synth.normal((67, 131), 92 + i, dtype=dtype) for i in range(2))
+    x, y = (T.leaf(dev(a, dtype), grad_dtype=torch.float32) for a in (x0, y0))
+    T.backward(build(T, x, y))
+    torch.cuda.synchronize()
+    rx, ry = OT.leaf(x0), OT.leaf(y0)
+    OT.backward(build(OT, rx, ry))
+    for got, want in ((x.grad, rx.grad), (y.grad, ry.grad)):
+        g = host(got)
+        if dtype == "f32":   # float32 element-wise bound, relative to max(|r|, 1)
+            assert np.max(np.abs(g - want) / np.maximum(np.abs(want), 1.0)) <= 1e-5
+        else:                # interior grads are bf16 (a few ulps of 2^-8 each); a shared buffer is O(1) off
+            assert norm_err(g, want) <= 1e-2
+    if name == "scale_then_add":
+        assert np.array_equal(host(x.grad), np.full(x0.shape, 3.0, np.float32))
+        assert np.array_equal(host(y.grad), np.ones(y0.shape, np.float32))

@@ -43,10 +43,15 @@ def leaf(value: torch.Tensor, grad_dtype=None, name=None) -> Var:
     return Var(value, grad_dtype=grad_dtype, name=name)
 
 
-def push(v: Var, g: torch.Tensor):
-    """Adds contribution g to v.grad (first push sets it)."""
+def push(v: Var, g: torch.Tensor, owned: bool = False):
+    """Adds contribution g to v.grad (first push sets it).
+
+    A first push stores g itself only when the caller hands over a buffer nobody else holds
+    (owned=True: a gradient the closure has just written).  Any other g (the node's own grad
+    passed through by add / add_bias, or a buffer also pushed to a sibling) is copied into a
+    buffer of v's own, so a later accumulate into v can never change another Var's grad."""
     if v.grad is None:
-        if g.dtype == v.grad_dtype:
+        if owned and g.dtype == v.grad_dtype:
             v.grad = g
         else:
             v.grad = torch.empty(g.shape, dtype=v.grad_dtype, device=g.device)
@@ -80,7 +85,7 @@ def backward(loss: Var):
     seed = torch.empty(1, dtype=_F32, device=loss.value.device)
     one = torch.ones(1, dtype=_F32, device=loss.value.device)
     xt.xt_convert(seed, one)
-    push(loss, seed if loss.value.dtype == _F32 else _cast(seed, loss.value.dtype))
+    push(loss, seed if loss.value.dtype == _F32 else _cast(seed, loss.value.dtype), owned=True)
     for node in reversed(order):
         if node.backward_fn is not None and node.grad is not None:
             node.backward_fn(node.grad, node.parents)
@@ -124,8 +129,8 @@ def mul(a: Var, b: Var) -> Var:
         g = _as(g, ps[0].value)
         da, db = _empty_like(ps[0].value), _empty_like(ps[1].value)
         xt.xt_mul_bwd(g, ps[0].value, ps[1].value, da, db)
-        push(ps[0], da)
-        push(ps[1], db)
+        push(ps[0], da, owned=True)
+        push(ps[1], db, owned=True)
     return Var(y, [a, b], bw)
 
 
@@ -137,7 +142,7 @@ def scale(x: Var, alpha: float) -> Var:
         g = _as(g, ps[0].value)
         dx = _empty_like(g)
         xt.xt_scale_bwd(g, dx, alpha)
-        push(ps[0], dx)
+        push(ps[0], dx, owned=True)
     return Var(y, [x], bw)
 
 
@@ -148,7 +153,7 @@ def sum_all(x: Var) -> Var:
     def bw(g, ps):
         dx = _empty_like(ps[0].value)
         xt.xt_sum_bwd(_cast(g, _F32), dx)
-        push(ps[0], dx)
+        push(ps[0], dx, owned=True)
     return Var(y, [x], bw)
 
 
@@ -167,8 +172,8 @@ def matmul(a: Var, b: Var, trans_b: bool = False) -> Var:
         g = _as(g, ps[0].value)
         dA, dB = _empty_like(ps[0].value), _empty_like(ps[1].value)
         xt.xt_matmul_bwd(d, ps[0].value, ps[1].value, g, dA, dB)
-        push(ps[0], dA)
-        push(ps[1], dB)
+        push(ps[0], dA, owned=True)
+        push(ps[1], dB, owned=True)
     return Var(y, [a, b], bw)
 
 
@@ -181,7 +186,7 @@ def add_bias(x: Var, b: Var) -> Var:
         db = _empty_like(ps[1].value, _F32)
         xt.xt_add_bias_bwd(g, None, db)
         push(ps[0], g)
-        push(ps[1], _cast(db, ps[1].grad_dtype))
+        push(ps[1], _cast(db, ps[1].grad_dtype), owned=True)
     return Var(y, [x, b], bw)
 
 
@@ -193,7 +198,7 @@ def silu(x: Var) -> Var:
         g = _as(g, ps[0].value)
         dx = _empty_like(g)
         xt.xt_silu_bwd(g, ps[0].value, dx)
-        push(ps[0], dx)
+        push(ps[0], dx, owned=True)
     return Var(y, [x], bw)
 
 
@@ -205,7 +210,7 @@ def gelu(x: Var) -> Var:
         g = _as(g, ps[0].value)
         dx = _empty_like(g)
         xt.xt_gelu_bwd(g, ps[0].value, dx)
-        push(ps[0], dx)
+        push(ps[0], dx, owned=True)
     return Var(y, [x], bw)
 
 
@@ -217,8 +222,8 @@ def swiglu(gate: Var, up: Var) -> Var:
         g = _as(g, ps[0].value)
         dg, du = _empty_like(ps[0].value), _empty_like(ps[1].value)
         xt.xt_swiglu_bwd(g, ps[0].value, ps[1].value, dg, du)
-        push(ps[0], dg)
-        push(ps[1], du)
+        push(ps[0], dg, owned=True)
+        push(ps[1], du, owned=True)
     return Var(y, [gate, up], bw)
 
 
@@ -232,8 +237,8 @@ def rms_norm(x: Var, gamma: Var, eps: float) -> Var:
         g = _as(g, ps[0].value)
         dx, dg = _empty_like(ps[0].value), _empty_like(ps[1].value, _F32)
         xt.xt_rms_norm_bwd(g, ps[0].value, ps[1].value, ir, dx, dg)
-        push(ps[0], dx)
-        push(ps[1], _cast(dg, ps[1].grad_dtype))
+        push(ps[0], dx, owned=True)
+        push(ps[1], _cast(dg, ps[1].grad_dtype), owned=True)
     return Var(y, [x, gamma], bw)
 
 
@@ -249,9 +254,9 @@ def layernorm(x: Var, gamma: Var, beta: Var, eps: float) -> Var:
         dx = _empty_like(ps[0].value)
         dg, db = _empty_like(ps[1].value, _F32), _empty_like(ps[2].value, _F32)
         xt.xt_layernorm_bwd(g, ps[0].value, ps[1].value, mu, rs, dx, dg, db)
-        push(ps[0], dx)
-        push(ps[1], _cast(dg, ps[1].grad_dtype))
-        push(ps[2], _cast(db, ps[2].grad_dtype))
+        push(ps[0], dx, owned=True)
+        push(ps[1], _cast(dg, ps[1].grad_dtype), owned=True)
+        push(ps[2], _cast(db, ps[2].grad_dtype), owned=True)
     return Var(y, [x, gamma, beta], bw)
 
 
@@ -265,7 +270,7 @@ def softmax(x: Var, causal: bool = False) -> Var:
         g = _as(g, y)
         dx = _empty_like(y)
         xt.xt_softmax_bwd(g, y, dx, causal=1 if causal else 0, q_len=ps[0].value.shape[-2] if causal else 0)
-        push(ps[0], dx)
+        push(ps[0], dx, owned=True)
     del S
     return Var(y, [x], bw)
 
@@ -298,7 +303,7 @@ def dropout(x: Var, p: float, seed: int, training: bool = True) -> Var:
         g = _as(g, ps[0].value)
         dx = _empty_like(g)
         xt.xt_dropout_bwd(g, dx, p, seed)
-        push(ps[0], dx)
+        push(ps[0], dx, owned=True)
     return Var(y, [x], bw)
 
 
@@ -327,6 +332,6 @@ def _bmm(a: Var, b: Var, trans_b: bool, alpha: float) -> Var:
         g = _as(g, ps[0].value)
         dA, dB = _empty_like(ps[0].value), _empty_like(ps[1].value)
         xt.xt_matmul_bwd(d, ps[0].value, ps[1].value, g, dA, dB)
-        push(ps[0], dA)
-        push(ps[1], dB)
+        push(ps[0], dA, owned=True)
+        push(ps[1], dB, owned=True)
     return Var(y, [a, b], bw)
