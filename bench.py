@@ -16,7 +16,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import re
 import os
 import statistics
 import subprocess
@@ -39,6 +38,20 @@ WORKLOAD_TEXT = {
 }
 
 
+# The reference arm runs the float64 oracle (composed attention: probabilities formed and kept)
+# on a causal prefix of one sequence; its label says so.
+REFERENCE_TEXT = {
+    "gpt12": "float64 NumPy oracle of the 12-layer pre-norm GPT stack (d768 H12x64, LayerNorm, exact-GELU MLP 3072, "
+             "learned positions, tied 50304-vocab logits + mean CE), composed causal attention "
+             "(softmax(QK^T/sqrt(hd)) kept, then @V), on the first {n} positions of one sequence per step",
+    "block256": "float64 NumPy oracle of 1 pre-norm block (d256 H4x64, RMSNorm, RoPE, SwiGLU 688, tied 4096-vocab "
+                "logits + mean CE, residual dropout p=0.1), composed causal attention, on the first {n} positions "
+                "of one sequence per step",
+    "tiny": "float64 NumPy oracle of 1 pre-norm block (d32 H2x16, RMSNorm, RoPE, SwiGLU 64, tied 64-vocab logits), "
+            "composed causal attention, on the first {n} positions of one sequence per step",
+}
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -56,6 +69,10 @@ def parse_args(argv=None):
                          "and of the 8192 x 128256 cross-entropy / fan-out case; one JSON line per case")
     ap.add_argument("--shape", default="8192,3072,768,0,1",
                     help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
+    ap.add_argument("--pairing", type=int, choices=[0, 1, 2], default=0,
+                    help="--kernel gemm: 0 model's choice, 1 single-CTA kernel only, 2 paired-CTA kernel")
+    ap.add_argument("--schedule", type=int, choices=[0, 1, 2, 3, 4], default=0,
+                    help="--kernel gemm: schedule override (0 model, 1 tiles, 2 K split, 3 stream-K, 4 lockstep)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     # two of the 8 sequences: ≈ 11 s of float64 oracle work on 16 Arm cores
     ap.add_argument("--sample-seqs", type=int, default=2, help=argparse.SUPPRESS)
@@ -222,8 +239,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.mean(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "global_batch": cfg["B"], "seq_len": cfg["S"],
-                   "parallelism": "cpu"},
+        "config": {"workload": REFERENCE_TEXT[args.workload].format(n=n), "global_batch": cfg["B"],
+                   "seq_len": cfg["S"], "parallelism": "cpu"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                   "sample": f"per step: the first {n} positions of one sequence (of {cfg['B']} x {S}), "
                                    f"all {cfg['n_layers']} layers, float64 NumPy forward + backward"},
@@ -274,10 +291,10 @@ def run_ours(args, rank, world, local_rank):
     # The step is enqueued once into a graph and replayed: the same kernels, without host launch
     # gaps, and with every kernel launched as a programmatic dependent of the one before it.
     # Two captures of the same step: `graph` for the throughput (and e2e) measurement, and
-    # `graph_prof` with a CUDA event recorded on the stream around every GEMM launch, for the
-    # GEMM roofline.  An event-record node between two kernels breaks their programmatic edge,
-    # so the profiled graph runs slower; it is timed in a second pass and reported separately.
-    def capture(profile):
+    # `graph_prof` with GEMM timing on, for the GEMM roofline: every CTA of every GEMM launch
+    # stores %globaltimer when it starts work and when it is done (no event or extra node enters
+    # the graph, so the programmatic edges stay); the pass is timed and reported separately.
+    def capture(block, profile):
         xt.profile_gemm(400 * cfg["n_layers"] // 12 + 64 if profile else 0)
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
@@ -285,14 +302,14 @@ def run_ours(args, rank, world, local_rank):
         n0 = xt.launch_count()
         with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
             cs = torch.cuda.current_stream(dev)
-            nb.zero_grads(cs)
-            nb.forward(ids, tgt, cs)
-            nb.backward(ids, tgt, cs)
+            block.zero_grads(cs)
+            block.forward(ids, tgt, cs)
+            block.backward(ids, tgt, cs)
         torch.cuda.synchronize(dev)
         return g, xt.launch_count() - n0
 
-    graph, kernels_per_step = capture(False)  # (profile_gemm(0) clears the records: capture this one first)
-    graph_prof, _ = capture(True)
+    graph, kernels_per_step = capture(nb, False)  # (profile_gemm(0) clears the records: capture this one first)
+    graph_prof, _ = capture(nb, True)
     for g_ in (graph, graph_prof):
         for _ in range(3):
             g_.replay()
@@ -318,11 +335,39 @@ def run_ours(args, rank, world, local_rank):
     assert xt.device_errors() == 0, "device error flag set during the timed region"
     loss = float(nb.loss.item())
 
-    # ---------------- GEMM roofline pass: the same step with the GEMM events ----------------
+    # ---------------- GEMM roofline pass: the same step with the GEMM timestamps ----------------
     ms_prof, clocks_prof = timed_replays(graph_prof, args.steps)
     flops, gms, gshapes = xt.profile_gemm_read(shapes=True)   # the last replay's GEMM launches
     xt.profile_gemm(0)
     assert xt.device_errors() == 0, "device error flag set during the profiled pass"
+    del graph_prof
+
+    # ---------------- the composed attention path of the same workload ----------------
+    # The pages' attention, matmul(softmax(QKᵀ·scale), V) with the probabilities stored, as
+    # separate causal-tile GEMMs around the row softmax (the fused kernel is the default path).
+    composed = None
+    if cfg.get("attention", "auto") != "composed" and cfg["dtype"] == "bf16" and world == 1:
+        nbc = NativeBlock(dict(cfg, attention="composed"), device=dev, training=True,
+                          base_seed=synth.BASE_SEED_DROPOUT)
+        nbc.load(synth.block_params(cfg))
+        for _ in range(max(1, args.warmup)):
+            nbc.zero_grads(stream)
+            nbc.forward(ids, tgt, stream)
+            nbc.backward(ids, tgt, stream)
+        torch.cuda.synchronize(dev)
+        graph_c, kernels_c = capture(nbc, False)
+        for _ in range(3):
+            graph_c.replay()
+        ms_c, clocks_c = timed_replays(graph_c, args.steps)
+        assert xt.device_errors() == 0, "device error flag set during the composed-attention pass"
+        composed = {"value": T / (ms_c / 1000.0), "unit": "tokens/s", "ms_per_step": ms_c,
+                    "loss": float(nbc.loss.item()), "gpu_launches_per_step": int(kernels_c),
+                    "workspace_gb": round(nbc.ws.numel() / 1e9, 3),
+                    "attention": "composed: causal-tile QK^T GEMM, row softmax (probabilities stored, bf16), "
+                                 "P@V GEMM; backward through the same ops",
+                    "clocks": clocks_c.summary()}
+        del graph_c, nbc
+        torch.cuda.synchronize(dev)
 
     ms_max = max_over_ranks(ms, dev)
     value = world * T / (ms_max / 1000.0)
@@ -355,20 +400,29 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_src = measured_peaks()
     gemm_ms_step = float(np.sum(gms))
     tflops = float(np.sum(flops)) / (float(np.sum(gms)) * 1e-3) / 1e12 if len(gms) else None
-    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
     if cfg["dtype"] == "f32":
-        peak = peak * 1.1 / 2.25   # tf32 dense: the bf16 measurement × the nominal tf32/bf16 ratio
+        # tf32 dense peak measured on this GPU (cuBLAS through torch.matmul, fp32 with TF32 on)
+        peak = measure_tf32_peak(dev)
+        peak_sus, src_txt = None, "measured tf32 burst (torch.matmul fp32 8192^3, TF32 allowed, this run)"
+    else:
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        peak_sus = float(peaks.get("bf16_tflops_sustained", 1700.0))
+        src_txt = f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
     roofline = {
         "kernel": "gemm_kernel (tcgen05.mma + TMA, all GEMM launches of the step)",
         "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-        "frac": (tflops / peak) if tflops else None, "peak_source": f"{peak_src} "
-        f"({'bf16 sustained' if cfg['dtype'] == 'bf16' else 'bf16 sustained x 1.1/2.25 for tf32'})",
-        "traffic": gemm_traffic_per_launch(args.workload), "traffic_unit": "bytes per GEMM launch (ncu, step mean)",
+        "frac": (tflops / peak) if tflops else None, "peak_source": src_txt,
+        "frac_of_sustained": (tflops / peak_sus) if (tflops and peak_sus) else None,
+        "peak_sustained": peak_sus,
+        "traffic": None,
+        "traffic_note": "DRAM bytes are not measured in this run (ncu only); see profiles/ for captures",
         "launches_per_step": len(gms),
         "share_of_step": gemm_ms_step / ms_prof, "gemm_tflop_per_step": float(np.sum(flops)) / 1e12,
-        "measured_in": (f"second pass of {args.steps} graph replays with a CUDA event before and after every GEMM "
-                        f"launch (events captured into the graph); that pass ran {ms_prof:.3f} ms/step, the "
-                        f"event-free timed pass that gives `value` {ms:.3f} ms/step"),
+        "measured_in": (f"second pass of {args.steps} replays of the same step graph with GEMM timing on: each CTA "
+                        f"of each GEMM launch stores %globaltimer after its wait for the preceding kernel and when "
+                        f"done; a launch's time is the latest end minus the earliest start (programmatic launch "
+                        f"edges intact); that pass ran {ms_prof:.3f} ms/step, the timed pass that gives `value` "
+                        f"{ms:.3f} ms/step"),
         "clocks_profiled_pass": clocks_prof.summary(),
         "by_shape": gemm_by_shape(flops, gms, gshapes),
     }
@@ -386,37 +440,45 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": 4},
         "gpu_launches": int(launches),
         "roofline": roofline,
+        "composed_attention": composed,
         "cpu_baseline": cpu,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
 
 
-def gemm_traffic_per_launch(workload):
-    """Mean DRAM bytes (read + write) per GEMM launch of the step from the committed ncu capture
-    (profiles/gemm_step_dram_traffic_gpt12.md), or None when the workload differs or the GEMM
-    sources changed since the counters were taken."""
-    import hashlib
-    if workload != "gpt12":
-        return None
-    path = os.path.join(ROOT, "profiles", "gemm_step_dram_traffic_gpt12.md")
-    if not os.path.exists(path):
-        return None
-    txt = open(path).read()
-    mb = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
-    mh = re.search(r"gemm_sources_sha256_16: ([0-9a-f]+)", txt)
-    if not (mb and mh):
-        return None
-    csrc = os.path.join(ROOT, "transformer_fwd_bwd_gb300", "csrc")
-    h = hashlib.sha256(open(os.path.join(csrc, "gemm_kernel.cuh"), "rb").read() +
-                       open(os.path.join(csrc, "gemm.cu"), "rb").read()).hexdigest()[:16]
-    return int(mb.group(1)) if h == mh.group(1) else None
+def measure_tf32_peak(dev):
+    """Dense tf32 tensor throughput of this GPU: cuBLAS (torch.matmul) on 8192³ fp32 operands with
+    TF32 allowed, best of 10 after 3 untimed, CUDA events on the current stream (TFLOP/s)."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 
 
 def gemm_by_shape(flops, gms, shapes, top=12):
-    """The GEMM launches of one step grouped by (M, N, K, batches, BN, A MN-major, B MN-major, causal
-    mode, 10 x K splits, 1000 for stream-K over every SM, 1000 + s for s lockstep K slices): launches per step, summed event time (a K split's
-    reduce included) and TFLOP/s of each group, largest time first."""
+    """The GEMM launches of one step grouped by (M, N, K, batches, BN (1000 + BN for the paired-CTA
+    kernel), A MN-major, B MN-major, causal mode, 10 x K splits, 1000 for stream-K over every SM,
+    1000 + s for s lockstep K slices): launches per step, summed event time (a K split's reduce
+    included) and TFLOP/s of each group, largest time first."""
     groups = {}
     for f, t, sh in zip(flops, gms, shapes):
         g = groups.setdefault(tuple(int(x) for x in sh), [0, 0.0, 0.0])
@@ -428,7 +490,8 @@ def gemm_by_shape(flops, gms, shapes, top=12):
         if c >= 1000:
             return "stream_k" if c == 1000 else f"stream_k_slices_{c - 1000}"
         return f"k_split_{c // 10}" if c >= 10 else "tiles"
-    return [{"mnk": list(k[:3]), "batches": 1 if 10 <= k[7] < 1000 else k[3], "bn": k[4], "a_mn": k[5],
+    return [{"mnk": list(k[:3]), "batches": 1 if 10 <= k[7] < 1000 else k[3], "bn": k[4] % 1000,
+             "paired": k[4] > 1000, "a_mn": k[5],
              "b_mn": k[6], "causal": 0 if k[7] >= 10 else k[7], "schedule": sched(k[7]),
              "launches": n, "ms": round(t, 4), "tflops": round(f / (t * 1e-3) / 1e12, 1) if t > 0 else None}
             for k, (n, t, f) in rows]
@@ -578,10 +641,19 @@ def run_kernel(args):
         A = (torch.randn(K, M, generator=g) if ta else torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)
         Bm = (torch.randn(N, K, generator=g) if tb else torch.randn(K, N, generator=g)).to(torch.bfloat16).to(dev)
         C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        xt.gemm_set_pairing(args.pairing)
+        xt.gemm_set_schedule(args.schedule)
         desc = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16)
         mws = xt.matmul_workspace(desc, dev)
         us = timed(lambda: xt.xt_matmul_fwd(desc, A, Bm, C, ws=mws))
+        xt.profile_gemm(8)
+        xt.xt_matmul_fwd(desc, A, Bm, C, ws=mws)
+        torch.cuda.synchronize(dev)
+        _, _, sh = xt.profile_gemm_read(shapes=True)
+        xt.profile_gemm(0)
+        bn = int(sh[0][4])
         print(json.dumps({"kernel": "gemm", "shape": [M, N, K, ta, tb], "us": us, "tflops": 2 * M * N * K / us / 1e6,
+                          "paired": bn > 1000, "bn": bn % 1000, "schedule_code": int(sh[0][7]),
                           "clocks": clocks}))
 
 

@@ -74,19 +74,36 @@ int xt_clear_device_errors(void* stream);
 /* Number of CUDA kernels libxt has launched in this process (host-side counter). */
 uint64_t xt_launch_count(void);
 
-/* GEMM timing for measurement: with capacity > 0, the next `capacity` GEMM launches are
- * bracketed by CUDA events recorded on their own stream, each tagged with its algorithmic
- * FLOPs (2·M·N·K per batch; for the causal modes only the unmasked half).  Events are
- * created by this call, not during the launches; capacity 0 disables.  Launches enqueued while
- * their stream is being captured into a CUDA graph record their events as graph nodes, so
- * every replay re-records them (the read then returns the latest replay's timings).  The pool's
- * events live as long as the library; a later xt_profile_gemm call hands them to new records,
- * so a graph captured with profiling on should not be replayed while other launches are being
- * profiled.
+/* Limit, in nanoseconds, of the bounded waits inside the tensor-core kernels (the GEMM and the
+ * fused attention) on work from their other roles: TMA copies landing, MMAs completing, an
+ * accumulator being drained, a stream-K partial being published.  A wait that runs out sets
+ * XT_DEVERR_TIMEOUT in the device flag; the kernel then stops issuing work, waits (with the
+ * default limit) for the copies and MMAs it already issued, releases its tensor memory and
+ * returns, so the context stays usable.  Process-wide; read when a launch is enqueued (a
+ * captured graph keeps the value it was captured with).  ns = 0 restores the default of 2 s.
+ * Limits under 1 ms poll without suspending (for tests of the give-up paths).  After a
+ * give-up the outputs are undefined, and a stream-K matmul workspace may hold stale flag
+ * words: zero it before its next use.  Always returns XT_OK. */
+int xt_set_wait_limit_ns(uint64_t ns);
+uint64_t xt_get_wait_limit_ns(void);
+
+/* GEMM timing for measurement: with capacity > 0, the next `capacity` GEMM launches each get
+ * a record tagged with its algorithmic FLOPs (2·M·N·K per batch; for the causal modes only the
+ * unmasked half) and a region of a device buffer in which every CTA of the GEMM kernel (and of
+ * a K split's reduce kernel) writes %globaltimer when it starts work (after its wait for the
+ * preceding kernel) and when it has finished.  No event or extra node enters the stream, so the
+ * launches keep their programmatic dependent-launch overlap.  The buffer (capacity × 32 KB) is
+ * allocated by this call on the current device, not during the launches; capacity 0 disables
+ * recording (the buffer is kept for reuse).  Launches captured into a CUDA graph keep their
+ * region, so every replay rewrites it (the read returns the latest replay's timings); a graph
+ * captured with profiling on should not be replayed after a later xt_profile_gemm call.
  * xt_profile_gemm_read
- * waits for the recorded events and copies up to max_records records into host arrays:
- * flops, milliseconds, and (if shapes != NULL) 8 ints per record: M, N, K, batches, tile
- * width BN, A MN-major, B MN-major, causal mode.  *n receives the number recorded. */
+ * synchronises the device and copies up to max_records records into host arrays: flops,
+ * milliseconds (latest end minus earliest start over the record's CTAs), and (if shapes !=
+ * NULL) 8 ints per record: M, N, K, batches, tile width BN (1000 + BN for the paired-CTA
+ * kernel), A MN-major, B MN-major, schedule code (causal mode, 10 × K splits, 1000 for
+ * stream-K over every unit, 1000 + s for s lockstep K slices).  *n receives the number
+ * recorded. */
 int xt_profile_gemm(int capacity);
 int xt_profile_gemm_read(double* flops, float* ms, int* shapes, int max_records, int* n);
 
@@ -379,6 +396,16 @@ int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes);
  * 3 stream-K over every SM wherever allowed, 4 stream-K in lockstep K slices (tiles × s
  * CTAs, each one K slice of one tile) wherever allowed.  XT_ERR_INVALID_ARG otherwise. */
 int xt_gemm_set_schedule(int mode);
+/* Process-wide override of the paired-CTA GEMM (bf16 operands, no causal mode, no GELU
+ * epilogue): two CTAs of a cluster compute one 256-row tile with the paired tensor-core MMA,
+ * each staging its own 128 rows of A and half of B's rows.  0 = the time model's choice
+ * (default), 1 = never, 2 = wherever allowed.  Either kernel accumulates in fp32 over the
+ * same K order; the choice is deterministic for a given shape.  XT_ERR_INVALID_ARG otherwise. */
+int xt_gemm_set_pairing(int mode);
+/* Process-wide override of the GEMM tile width: 0 = the time model's choice (default), else
+ * BN ∈ {64, 128, 192, 256} wherever it is a candidate for the problem (the model's choice
+ * otherwise).  For measurement and tests.  XT_ERR_INVALID_ARG for other values. */
+int xt_gemm_set_tile(int bn);
 int xt_matmul_fwd(const xt_matmul_desc* desc, const void* A, const void* B, void* C, void* ws,
                   size_t ws_bytes, void* stream);
 /* Backward of C = alpha·op(A)@op(B) given dC (layout of C, dtype dtype_ab):

@@ -279,15 +279,16 @@ def test_matmul_stream_k_batched(form, schedule):
 
 @pytest.mark.parametrize("M,N,K,tb", [(8192, 768, 3072, 0), (3072, 768, 8192, 0), (8192, 768, 2304, 1)])
 def test_matmul_model_schedule_full_size(M, N, K, tb):
-    """The 12-layer stack's shapes under the time model's own choice (a stream-K form for
-    these), checked on sampled rows against the oracle product of those rows."""
+    """The 12-layer stack's shapes under the time model's own choice (whole tiles, a K split or
+    a stream-K form, single or paired CTAs), checked on sampled rows against the oracle product
+    of those rows."""
     A = synth.normal((M, K), 65, std=0.5, dtype="bf16")
     B = synth.normal((N, K) if tb else (K, N), 66, std=0.02, dtype="bf16")
     Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     d = xt.matmul_desc(M, N, K, trans_b=tb, dtype_c=xt.XT_BF16)
     Ad, Bd = dev(A, "bf16"), dev(B, "bf16")
     codes = schedules_of(lambda: xt.xt_matmul_fwd(d, Ad, Bd, Cm))
-    assert len(codes) == 1 and codes[0] >= 1000, codes
+    assert len(codes) == 1, codes
     rows = np.random.default_rng(1).choice(M, 24, replace=False)
     rows = np.concatenate([rows, [0, 127, 128, M - 1]])
     want = A[rows] @ op(B, tb)

@@ -1,5 +1,5 @@
 // Status reporting, the device error flag, device facts, the launch counter and the
-// optional per-GEMM event timing.
+// optional per-GEMM timing.
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -15,17 +15,22 @@ uint32_t* g_flag_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::mutex g_mu;
 std::atomic<uint64_t> g_launches{0};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
-// GEMM timing: pairs of events recorded around each GEMM launch while enabled.
+// GEMM timing: while enabled, each GEMM launch gets a record and a region of a device buffer
+// in which every CTA of the GEMM kernel (and of a K split's reduce kernel) stores %globaltimer
+// when it starts work (after its programmatic-launch wait) and when it has finished.
 struct GemmRecord {
   double flops;
-  cudaEvent_t start, stop;
   int shape[8];
+  int grid, rgrid;  // CTAs of the GEMM kernel and of the reduce kernel (0: none)
 };
 std::mutex g_prof_mu;
-std::vector<cudaEvent_t> g_ev_pool;
+unsigned long long* g_ts_buf = nullptr;  // capacity × kProfSlots × 2 words
+int g_ts_dev = -1;
+size_t g_prof_cap = 0;
 std::vector<GemmRecord> g_records;
-size_t g_ev_next = 0;
 bool g_prof_on = false;
 }  // namespace
 
@@ -64,6 +69,8 @@ uint32_t* errflag() {
   return g_flag_ptr[dev];
 }
 
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 int num_sms() {
   int dev = current_device();
   if (dev < 0) return 1;
@@ -76,32 +83,24 @@ int num_sms() {
   return g_sms[dev];
 }
 
-// Inside a stream capture the event becomes an event-record node of the graph, so each
-// replay records it; outside, a plain record.
-static void record_event(cudaEvent_t e, cudaStream_t s) {
-  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
-    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
-  else
-    cudaEventRecord(e, s);
-}
-
-bool gemm_profile_begin(cudaStream_t s, double flops, const int* shape, void** token) {
+bool gemm_profile_begin(double flops, const int* shape, unsigned long long** ts, void** token) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  if (!g_prof_on || g_ev_next + 2 > g_ev_pool.size()) return false;
-  GemmRecord r{flops, g_ev_pool[g_ev_next], g_ev_pool[g_ev_next + 1], {}};
+  if (!g_prof_on || !g_ts_buf || g_records.size() >= g_prof_cap) return false;
+  GemmRecord r{flops, {}, 0, 0};
   for (int i = 0; i < 8; ++i) r.shape[i] = shape[i];
-  g_ev_next += 2;
-  record_event(r.start, s);
+  *ts = g_ts_buf + g_records.size() * size_t(kProfSlots) * 2;
   g_records.push_back(r);
   *token = reinterpret_cast<void*>(g_records.size());
   return true;
 }
 
-void gemm_profile_end(cudaStream_t s, void* token) {
+void gemm_profile_grids(void* token, int grid, int rgrid) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   const size_t i = reinterpret_cast<size_t>(token);
-  if (i >= 1 && i <= g_records.size()) record_event(g_records[i - 1].stop, s);
+  if (i >= 1 && i <= g_records.size()) {
+    g_records[i - 1].grid = grid;
+    g_records[i - 1].rgrid = rgrid;
+  }
 }
 
 }  // namespace xt
@@ -110,15 +109,34 @@ extern "C" {
 
 uint64_t xt_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int xt_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+  return XT_OK;
+}
+
+uint64_t xt_get_wait_limit_ns(void) { return g_wait_ns.load(std::memory_order_relaxed); }
+
 int xt_profile_gemm(int capacity) {
+  XT_REQUIRE(capacity >= 0, "xt_profile_gemm: negative capacity");
   std::lock_guard<std::mutex> lk(g_prof_mu);
   g_records.clear();
-  g_ev_next = 0;
   g_prof_on = capacity > 0;
-  while (g_ev_pool.size() < size_t(2 * capacity)) {
-    cudaEvent_t e;
-    if (cudaEventCreate(&e) != cudaSuccess) return xt::check_launch("xt_profile_gemm");
-    g_ev_pool.push_back(e);
+  if (!g_prof_on) return XT_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return xt::check_launch("xt_profile_gemm");
+  if (g_ts_buf && (g_ts_dev != dev || g_prof_cap < size_t(capacity))) {
+    cudaFree(g_ts_buf);
+    g_ts_buf = nullptr;
+  }
+  if (!g_ts_buf) {
+    const size_t bytes = size_t(capacity) * xt::kProfSlots * 2 * sizeof(unsigned long long);
+    if (cudaMalloc(&g_ts_buf, bytes) != cudaSuccess) {
+      g_ts_buf = nullptr;
+      g_prof_on = false;
+      return xt::check_launch("xt_profile_gemm");
+    }
+    g_ts_dev = dev;
+    g_prof_cap = size_t(capacity);
   }
   return XT_OK;
 }
@@ -128,18 +146,30 @@ int xt_profile_gemm_read(double* flops, float* ms, int* shapes, int max_records,
   std::lock_guard<std::mutex> lk(g_prof_mu);
   const int cnt = int(g_records.size());
   *n = cnt;
+  if (cnt == 0) return XT_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) return xt::check_launch("xt_profile_gemm_read");
+  std::vector<unsigned long long> ts(size_t(cnt) * xt::kProfSlots * 2);
+  if (cudaMemcpy(ts.data(), g_ts_buf, ts.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return xt::check_launch("xt_profile_gemm_read");
   for (int i = 0; i < cnt && i < max_records; ++i) {
-    if (cudaEventSynchronize(g_records[i].stop) != cudaSuccess) return xt::check_launch("xt_profile_gemm_read");
-    float t = 0.f;
-    cudaEventElapsedTime(&t, g_records[i].start, g_records[i].stop);
-    if (flops) flops[i] = g_records[i].flops;
-    if (ms) ms[i] = t;
+    const GemmRecord& r = g_records[i];
+    const unsigned long long* t = ts.data() + size_t(i) * xt::kProfSlots * 2;
+    unsigned long long t0 = ~0ull, t1 = 0;
+    for (int c = 0; c < r.grid; ++c) {
+      if (t[2 * c] < t0) t0 = t[2 * c];
+      if (t[2 * c + 1] > t1) t1 = t[2 * c + 1];
+    }
+    for (int c = 0; c < r.rgrid; ++c) {
+      const unsigned long long e = t[2 * (xt::kProfGemmSlots + c) + 1];
+      if (e > t1) t1 = e;
+    }
+    if (flops) flops[i] = r.flops;
+    if (ms) ms[i] = t1 > t0 ? float(double(t1 - t0) * 1e-6) : 0.f;
     if (shapes)
-      for (int j = 0; j < 8; ++j) shapes[8 * i + j] = g_records[i].shape[j];
+      for (int j = 0; j < 8; ++j) shapes[8 * i + j] = r.shape[j];
   }
   return XT_OK;
 }
-
 
 const char* xt_last_error(void) { return g_msg; }
 

@@ -52,6 +52,7 @@ struct FwdParams {
   float* lse;   // [B, H, S], natural log
   int o_lo;     // 1: also store O − bf16(O) rounded to bf16 (through tmOlo)
   uint32_t* flag;
+  uint64_t wait_ns;  // limit of the waits on work; draining the CTA's own copies / MMAs keeps the default
 };
 
 // Work item i → (b, h, query tile); with a causal mask, the longest rows come first.
@@ -105,8 +106,8 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Bounded wait taken by a whole warp (the decision is warp-uniform).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
 }
 
 // ------------------------------------------------------------------------------ forward
@@ -143,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* p_free = p_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_free + 2);
+  uint64_t* mma_done = p_free + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&p_full[b]), 4);
       mbar_init(smem_u32(&p_free[b]), 1);
     }
+    mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -197,19 +200,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full), TILE);
         tma_load_4d(sb + FwdSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         ++nqi;
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           if (*abort_flag) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&k_empty[ks]), kph ^ 1)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&k_empty[ks]), kph ^ 1, p.wait_ns)) { ok = false; break; }
           mbar_expect_tx(smem_u32(&k_full[ks]), TILE);
           tma_load_4d(sb + FwdSmem::K + ks * TILE, &tmK, smem_u32(&k_full[ks]), 0, it.h, j * BT, it.b);
           ++nk;
           if (++ks == RING) { ks = 0; kph ^= 1; }
-          if (!mbar_wait(smem_u32(&v_empty[vs]), vph ^ 1)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&v_empty[vs]), vph ^ 1, p.wait_ns)) { ok = false; break; }
           mbar_expect_tx(smem_u32(&v_full[vs]), TILE);
           tma_load_4d(sb + FwdSmem::V + vs * TILE, &tmV, smem_u32(&v_full[vs]), 0, it.h, j * BT, it.b);
           ++nv;
@@ -240,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](uint32_t gg, bool first) -> bool {
         const int b = int(gg & 1);
         const uint32_t u = gg >> 1;
-        if (!mbar_wait(smem_u32(&p_full[b]), u & 1)) return false;
-        if (!mbar_wait(smem_u32(&v_full[vs]), vph)) return false;
+        if (!mbar_wait(smem_u32(&p_full[b]), u & 1, p.wait_ns)) return false;
+        if (!mbar_wait(smem_u32(&v_full[vs]), vph, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t ps = sb + FwdSmem::P + b * PT;
         const uint32_t vsm = sb + FwdSmem::V + vs * TILE;
@@ -261,15 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_full), nqi & 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(q_full), nqi & 1, p.wait_ns)) { ok = false; break; }
         ++nqi;
         tc_fence_after();
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j, ++g) {
           const int b = int(g & 1);
           const uint32_t u = g >> 1;
-          if (*abort_flag || !mbar_wait(smem_u32(&k_full[ks]), kph) ||
-              !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait(smem_u32(&k_full[ks]), kph, p.wait_ns) ||
+              !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t ksm = sb + FwdSmem::K + ks * TILE;
 #pragma unroll
@@ -286,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!issue_pv(g - 1, it.nkv == 1)) { ok = false; break; }
       }
       if (!ok) give_up();
+      // every MMA issued has completed (also after a give-up) before TMEM is released
+      tc_commit(smem_u32(mma_done));
+      if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
     }
   } else {
     // ---------------------------------------------------------------- softmax / epilogue
@@ -308,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int b = int(g & 1);
         const uint32_t u = g >> 1;
-        if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&s_full[b]), u & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         uint32_t r[128];
 #pragma unroll
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O holds Σ 2^((s − m)·sc)·v with the old m: bring it to m_new once PV_{j−1} is done
           const uint32_t pg = g - 1;
-          if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1)) { ok = false; break; }
+          if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const float a = need ? exp2f((m - m_new) * p.sc) : 1.f;
 #pragma unroll
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
         }
         const float ms = (m == -INFINITY) ? 0.f : m * p.sc;
-        if (!warp_wait(smem_u32(&p_free[b]), (u & 1) ^ 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&p_free[b]), (u & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         const uint32_t ps = sb + FwdSmem::P + b * PT;
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
 #pragma unroll
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // ---- epilogue: O / l after the last PV
       const uint32_t pg = g - 1;
-      if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1)) {
+      if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1, p.wait_ns)) {
         if (lane == 0) give_up();
         break;
       }
@@ -441,6 +447,7 @@ struct BwdParams {
   const float* lse;  // [B, H, S] natural log, from the forward
   const float* D;    // [B, H, S] rowsum(dO ∘ O)
   uint32_t* flag;
+  uint64_t wait_ns;  // limit of the waits on work; draining the CTA's own copies / MMAs keeps the default
 };
 
 // D[b, h, s] = Σ_c dO[t, h·hd + c]·O[t, h·hd + c], t = b·S + s: 8 threads per (t, h), four
@@ -563,7 +570,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   uint64_t* ds_full = bars + 14;
   uint64_t* ds_free = bars + 15;
   uint64_t* vec_full = bars + 16;   // [2] the query tile's lse / D rows are in shared memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* mma_done = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* vec = reinterpret_cast<float*>(smem + KvSmem::VEC);
 
@@ -585,6 +593,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_init(smem_u32(ds_free), 1);
     mbar_init(smem_u32(&vec_full[0]), 256);
     mbar_init(smem_u32(&vec_full[1]), 256);
+    mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -620,7 +629,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(kv_empty), (nkv & 1) ^ 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(kv_empty), (nkv & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         mbar_expect_tx(smem_u32(kv_full), 2 * TILE);
         tma_load_4d(sb + KvSmem::K, &tmK, smem_u32(kv_full), 0, it.h, it.qt * BT, it.b);
         tma_load_4d(sb + KvSmem::V, &tmV, smem_u32(kv_full), 0, it.h, it.qt * BT, it.b);
@@ -628,7 +637,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int q_first = p.causal ? it.qt : 0;
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
-          if (*abort_flag || !mbar_wait(smem_u32(&qd_empty[slot]), ph ^ 1)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait(smem_u32(&qd_empty[slot]), ph ^ 1, p.wait_ns)) { ok = false; break; }
           const uint32_t fb = smem_u32(&qd_full[slot]);
           mbar_expect_tx(fb, 2 * TILE);
           const uint32_t dst = sb + KvSmem::QD + slot * 2 * TILE;
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       auto issue_s = [&](uint32_t gg) -> bool {  // Sᵀ = K Qᵀ into buffer gg & 1
         const int b = int(gg & 1);
         const uint32_t u = gg >> 1;
-        if (!mbar_wait(smem_u32(&qd_full[b]), u & 1) || !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1)) return false;
+        if (!mbar_wait(smem_u32(&qd_full[b]), u & 1, p.wait_ns) || !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
@@ -667,7 +676,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dp = [&](uint32_t gg) -> bool {  // dPᵀ = V dOᵀ
-        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1)) return false;
+        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
@@ -677,7 +686,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dv = [&](uint32_t gg, bool first) -> bool {
-        if (!mbar_wait(smem_u32(p_full), gg & 1)) return false;
+        if (!mbar_wait(smem_u32(p_full), gg & 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)  // dV += Pᵀ dO (dO tile read MN-major)
@@ -687,7 +696,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dk = [&](uint32_t gg, bool first) -> bool {
-        if (!mbar_wait(smem_u32(ds_full), gg & 1)) return false;
+        if (!mbar_wait(smem_u32(ds_full), gg & 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)  // dK += dSᵀ Q (Q tile read MN-major)
@@ -702,7 +711,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(kv_full), nkv & 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(kv_full), nkv & 1, p.wait_ns)) { ok = false; break; }
         ++nkv;
         tc_fence_after();
         const uint32_t g0 = g;
@@ -723,6 +732,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         g = g0 + uint32_t(it.nkv);
       }
       if (!ok) give_up();
+      // every MMA issued has completed (also after a give-up) before TMEM is released
+      tc_commit(smem_u32(mma_done));
+      if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
     }
   } else {
     // ---------------------------------------------------------------- Pᵀ / dSᵀ rows, epilogue
@@ -760,8 +772,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         lv[half * 128 + rr] = vnext;
         if (j + 1 < it.nkv) vnext = vec_entry(j + 1);
         mbar_arrive(smem_u32(&vec_full[b]));
-        if (!warp_wait(smem_u32(&vec_full[b]), u & 1)) { ok = false; break; }
-        if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&vec_full[b]), u & 1, p.wait_ns)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&s_full[b]), u & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         uint32_t r[64];  // this warp's 64 columns of the row
 #pragma unroll
@@ -779,7 +791,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           r[c] = __float_as_uint(c < first ? 0.f : e);
         }
         keep_before(r);
-        if (!warp_wait(smem_u32(p_free), (g & 1) ^ 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(p_free), (g & 1) ^ 1, p.wait_ns)) { ok = false; break; }
 #pragma unroll
         for (int un = 0; un < 8; ++un) {
           const int c0 = un * 8;
@@ -793,7 +805,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(p_full));
         // dSᵀ = Pᵀ ∘ (dPᵀ − D), 32 query columns at a time
-        if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(ds_free), (g & 1) ^ 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(dp_full), g & 1, p.wait_ns) || !warp_wait(smem_u32(ds_free), (g & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         uint32_t d[64];  // both dPᵀ chunks in flight before one wait
         tmem_ld32(tDP + lane_off + uint32_t(col0), *reinterpret_cast<uint32_t(*)[32]>(d));
@@ -825,7 +837,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       // other half's next arrival on p_full comes after this, so the next item's first dV / dK
       // MMAs cannot overwrite the accumulators before they are read)
       if (half != 0) continue;
-      if (!warp_wait(smem_u32(ds_free), (g - 1) & 1)) {
+      if (!warp_wait(smem_u32(ds_free), (g - 1) & 1, p.wait_ns)) {
         if (lane == 0) give_up();
         break;
       }
@@ -882,7 +894,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   uint64_t* dp_free = dp_full + 1;
   uint64_t* ds_full = dp_free + 1;         // [2]
   uint64_t* ds_free = ds_full + 2;         // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ds_free + 2);
+  uint64_t* mma_done = ds_free + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -901,6 +914,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     }
     mbar_init(smem_u32(dp_full), 1);
     mbar_init(smem_u32(dp_free), 8);
+    mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -936,14 +950,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full), 2 * TILE);
         tma_load_4d(sb + QSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         tma_load_4d(sb + QSmem::DO, &tmDO, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         ++nqi;
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
-          if (*abort_flag || !mbar_wait(smem_u32(&kv_empty[ks]), kph ^ 1)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait(smem_u32(&kv_empty[ks]), kph ^ 1, p.wait_ns)) { ok = false; break; }
           const uint32_t fb = smem_u32(&kv_full[ks]);
           mbar_expect_tx(fb, 2 * TILE);
           const uint32_t dst = sb + QSmem::KV + ks * 2 * TILE;
@@ -972,8 +986,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       auto issue_s = [&](uint32_t gg) -> bool {
         const int b = int(gg & 1);
         const uint32_t u = gg >> 1;
-        if (!mbar_wait(smem_u32(&kv_full[gg % RING]), (gg / RING) & 1) ||
-            !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1)) return false;
+        if (!mbar_wait(smem_u32(&kv_full[gg % RING]), (gg / RING) & 1, p.wait_ns) ||
+            !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
@@ -983,7 +997,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dp = [&](uint32_t gg) -> bool {
-        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1)) return false;
+        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
@@ -994,7 +1008,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       };
       auto issue_dq = [&](uint32_t gg, bool first) -> bool {
         const int b = int(gg & 1);
-        if (!mbar_wait(smem_u32(&ds_full[b]), (gg >> 1) & 1)) return false;
+        if (!mbar_wait(smem_u32(&ds_full[b]), (gg >> 1) & 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K (K tile read MN-major)
@@ -1009,7 +1023,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_full), nqi & 1)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(q_full), nqi & 1, p.wait_ns)) { ok = false; break; }
         ++nqi;
         tc_fence_after();
         const uint32_t g0 = g;
@@ -1028,6 +1042,9 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         g = g0 + uint32_t(it.nkv);
       }
       if (!ok) give_up();
+      // every MMA issued has completed (also after a give-up) before TMEM is released
+      tc_commit(smem_u32(mma_done));
+      if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
     }
   } else {
     // ---------------------------------------------------------------- P / dS rows, epilogue
@@ -1053,7 +1070,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       for (int j = 0; j < it.nkv; ++j, ++g) {
         const int b = int(g & 1);
         const uint32_t u = g >> 1;
-        if (!warp_wait(smem_u32(&s_full[b]), u & 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&s_full[b]), u & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         uint32_t r[64];  // this warp's 64 columns of the row
 #pragma unroll
@@ -1070,7 +1087,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
           r[c] = __float_as_uint(c < lim ? e : 0.f);
         }
         keep_before(r);
-        if (!warp_wait(smem_u32(dp_full), g & 1) || !warp_wait(smem_u32(&ds_free[b]), (u & 1) ^ 1)) {
+        if (!warp_wait(smem_u32(dp_full), g & 1, p.wait_ns) || !warp_wait(smem_u32(&ds_free[b]), (u & 1) ^ 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1106,7 +1123,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       // comes after this, so the next item's first dQ MMA cannot overwrite it before it is read)
       if (half != 0) continue;
       const uint32_t pg = g - 1;
-      if (!warp_wait(smem_u32(&ds_free[pg & 1]), (pg >> 1) & 1)) {
+      if (!warp_wait(smem_u32(&ds_free[pg & 1]), (pg >> 1) & 1, p.wait_ns)) {
         if (lane == 0) give_up();
         break;
       }
@@ -1199,6 +1216,7 @@ int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   p.lse = lse;
   p.o_lo = o_lo != nullptr;
   p.flag = errflag();
+  p.wait_ns = wait_limit_ns();
   static bool smem_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_fwd_kernel), FwdSmem::BYTES, smem_set, "xt_attention_fwd"));
   const int grid = p.items < num_sms() ? p.items : num_sms();
@@ -1255,6 +1273,7 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   p.lse = lse;
   p.D = D;
   p.flag = errflag();
+  p.wait_ns = wait_limit_ns();
   const int grid = p.items < num_sms() ? p.items : num_sms();
   static bool kv_set = false, q_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel), KvSmem::BYTES, kv_set, "xt_attention_bwd"));

@@ -24,9 +24,16 @@ int check_launch(const char* what);
 uint32_t* errflag();
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
-// GEMM timing hooks (active only between xt_profile_gemm(capacity > 0) and (0)).
-bool gemm_profile_begin(cudaStream_t s, double flops, const int* shape, void** token);
-void gemm_profile_end(cudaStream_t s, void* token);
+// Limit of the kernels' bounded waits on work, in ns (xt_set_wait_limit_ns; default 2 s).
+uint64_t wait_limit_ns();
+// GEMM timing hooks (active only between xt_profile_gemm(capacity > 0) and (0)): a record per
+// GEMM launch and its timestamp region, kProfSlots pairs of words: [0, kProfGemmSlots) for
+// the GEMM kernel's CTAs, the rest for a K split's reduce kernel.  Each CTA writes
+// (start, end) %globaltimer words at 2·cta.
+constexpr int kProfGemmSlots = 256;
+constexpr int kProfSlots = 2048;
+bool gemm_profile_begin(double flops, const int* shape, unsigned long long** ts, void** token);
+void gemm_profile_grids(void* token, int grid, int rgrid);
 
 #define XT_REQUIRE(cond, ...)                                      \
   do {                                                             \
@@ -52,6 +59,27 @@ inline void launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// As launch(), as clusters of `cluster_x` CTAs along x (gridDim.x a multiple of it).
+template <typename... KArgs, typename... Args>
+inline void launch_clustered(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             int cluster_x, Args&&... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = unsigned(cluster_x);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -331,6 +359,18 @@ __device__ __forceinline__ void gelu_batch(const float (&x)[N], float (&out)[N])
 __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Split form of pdl_begin() for kernels whose set-up touches nothing a predecessor writes:
+// the set-up runs before pdl_wait(), overlapping the predecessor's drain when the CTA is
+// already resident.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 __device__ __forceinline__ void flag_error(uint32_t* flag, uint32_t bit) {

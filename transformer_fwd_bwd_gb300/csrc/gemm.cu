@@ -78,74 +78,108 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn) {
 //     at the same K offsets as the others of its slice (operand tiles shared through L2 as
 //     by whole tiles).
 // Splits and stream-K need a workspace and a non-causal problem; the K split one batch.
-static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 192 ? 0.77 : bn >= 128 ? 0.64 : 0.35; }
+//
+// The constants were fitted to CUDA-graph timings of the 12-layer stack's fifteen GEMM shapes
+// under every (kernel, tile width, schedule) combination on a GB300: the model's pick is then
+// within 0.6 µs of the fastest measured one on each shape.
+static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 192 ? 0.95 : bn >= 128 ? 0.64 : 0.35; }
+// The same for the paired kernel's 256-row tiles (relative to the single-CTA BN 256 rate):
+// each CTA stages 128 rows of A and bn / 2 rows of B per k-block, 2/3 of the single kernel's
+// bytes per FLOP at bn 256, with six pipeline stages instead of four.
+static double pair_eff(int bn) { return bn >= 256 ? 1.08 : bn >= 192 ? 0.9 : 0.7; }
 
 // Schedule override (xt_gemm_set_schedule): 0 the model's choice, 1 whole tiles only, 2 a K
 // split where one is allowed, 3 stream-K over every SM where allowed, 4 stream-K in lockstep
 // K slices where allowed.
 static int g_schedule = 0;
+// Paired-kernel override (xt_gemm_set_pairing): 0 the model's choice, 1 never, 2 wherever allowed.
+static int g_pairing = 0;
+// Tile-width override (xt_gemm_set_tile): 0 the model's choice, else that BN wherever it is a
+// candidate.
+static int g_tile = 0;
 
 // Fixup time of a stream-K tile shared by `parts` CTAs: one latency plus one pass per partial.
-static double sk_fixup_time(int64_t parts) { return 0.7e-6 + 0.8e-6 * double(parts - 1); }
+static double sk_fixup_time(int64_t parts) { return 0.7e-6 + 1.2e-6 * double(parts - 1); }
 
 Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split,
-              bool fp8) {
+              bool fp8, bool b_mn) {
+  const bool pair_ok = !tf32 && !fp8 && causal == 0 && g_pairing != 1;
   if (fp8) allow_split = false;  // fp8: whole tiles only
   const int mode = allow_split ? g_schedule : 1;
   if (mode == 1) allow_split = false;
   const int cands_bf16[4] = {64, 128, 192, 256};
   const int cands_tf32[2] = {64, 128};
   const int cands_fp8[2] = {128, 256};
-  const int* c = fp8 ? cands_fp8 : tf32 ? cands_tf32 : cands_bf16;
-  const int nc = fp8 || tf32 ? 2 : 4;
+  // paired tiles stage BN / 2 rows of B per CTA: whole 64-element swizzle atoms when B is read
+  // MN-major (BN 128, 256), any multiple of 16 rows K-major (also BN 192)
+  const int cands_pair[3] = {128, 192, 256};
   const int sms = num_sms();
   const int bk = fp8 ? 128 : tf32 ? 32 : 64;
   const double per_sm = fp8 ? 22.4e12 : tf32 ? 5.6e12 : 11.2e12;
   const double e = fp8 ? 1.0 : tf32 ? 4.0 : 2.0;
-  Choice best{c[0], 1, 0, 0};
+  Choice best{fp8 ? cands_fp8[0] : tf32 ? cands_tf32[0] : cands_bf16[0], 1, 0, 0};
   double best_t = 1e300;
   const int64_t kbt = ceil_div(K, bk);
-  const bool sk_ok = allow_split && causal == 0 && sms <= kSkMaxCtas;
   // forced modes: the forced kind of candidate first, whole tiles when it is not allowed
-  auto weigh = [&](double t, int kind) {  // kind 1 tiles, 2 K split, 3 stream-K all SMs, 4 lockstep
+  auto weigh = [&](double t, int kind, int cg) {  // kind 1 tiles, 2 K split, 3 stream-K all units, 4 lockstep
     if (mode >= 2) t *= (kind == mode) ? 1e-6 : (kind == 1 ? 1.0 : 1e6);
+    if (g_pairing == 2 && cg == 2) t *= 1e-12;
     return t;
   };
+  auto tile_weight = [&](int bn) { return g_tile != 0 && bn != g_tile ? 1e18 : 1.0; };
   auto offer = [&](double t, Choice ch) {
     if (t < best_t * 0.999) {
       best_t = t;
       best = ch;
     }
   };
-  for (int i = 0; i < nc; ++i) {
-    const int bn = c[i];
-    if (i > 0 && c[i - 1] >= N) break;  // wider tiles only add padding
-    int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn) * batches;
-    if (causal == 1) tiles = (tiles + 1) / 2;
-    const double t_kb = 2.0 * BM * bn * bk / (per_sm * tile_eff(bn));
-    for (int s = 1; s <= 8; s *= 2) {
-      if (s > 1 && (!allow_split || batches != 1 || causal != 0 || N % 4 != 0)) break;
-      if (s > 1 && kbt < 4 * s) break;
-      const double rounds = double(ceil_div(tiles * s, sms));
-      const double t_tile = 2.0 * BM * bn * (double(K) / s) / (per_sm * tile_eff(bn)) + 1.5e-6;
-      double t = rounds * t_tile;
-      if (s > 1) t += double(s + 1) * double(M) * double(N) * 4.0 / 5e12 + 4e-6;
-      offer(weigh(t, s > 1 ? 2 : 1), Choice{bn, s, 0, 0});
-    }
-    if (!sk_ok) continue;
-    const int64_t iters = tiles * kbt;
-    const double operands = double(M + N) * double(batches) * double(K) * e;
-    if (iters >= sms && tiles % sms != 0 && (operands <= 80e6 || mode == 3)) {
-      const double share = double(iters) / sms;
-      const int64_t parts = int64_t(std::ceil(double(kbt) / share)) + 1;
-      // + 6.5 µs: the measured cost per launch beyond the model (staggered tiles, partial
-      // stores, the exposed fixup), fitted on 8192-row shapes with K 768 to 3072
-      const double t = std::ceil(share) * t_kb + (double(tiles) / sms + 1.0) * 1.5e-6 + sk_fixup_time(parts) + 6.5e-6;
-      offer(weigh(t, 3), Choice{bn, 1, 1, sms});
-    }
-    for (int64_t sl = 2; sl <= 8 && tiles * sl <= sms && kbt >= 2 * sl; ++sl) {
-      const double t = double(ceil_div(kbt, sl)) * t_kb + 1.5e-6 + sk_fixup_time(sl);
-      offer(weigh(t, 4), Choice{bn, 1, 2, int(tiles * sl)});
+  for (int cg = 1; cg <= 2; ++cg) {
+    // units: CTAs, or CTA pairs that can be resident together (stream-K waits need every unit resident)
+    const int units = cg == 1 ? sms : (pair_ok ? pair_capacity() : 0);
+    if (units < 1) continue;
+    const int bm = BM * cg;
+    const int* c = cg == 2 ? cands_pair : fp8 ? cands_fp8 : tf32 ? cands_tf32 : cands_bf16;
+    const int nc = cg == 2 ? 3 : fp8 || tf32 ? 2 : 4;
+    const double rate = per_sm * cg;  // per unit
+    const bool sk_ok = allow_split && causal == 0 && units * cg <= kSkMaxCtas;
+    for (int i = 0; i < nc; ++i) {
+      const int bn = c[i];
+      if (i > 0 && c[i - 1] >= N) break;  // wider tiles only add padding
+      if (cg == 2 && bn == 192 && b_mn) continue;
+      const double eff = cg == 2 ? pair_eff(bn) : tile_eff(bn);
+      int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn) * batches;
+      if (causal == 1) tiles = (tiles + 1) / 2;
+      const double t_kb = 2.0 * bm * bn * bk / (rate * eff);
+      for (int s = 1; s <= 8; s *= 2) {
+        if (s > 1 && (!allow_split || batches != 1 || causal != 0 || N % 4 != 0)) break;
+        if (s > 1 && kbt < 4 * s) break;
+        const double rounds = double(ceil_div(tiles * s, units));
+        const double t_tile = 2.0 * bm * bn * (double(K) / s) / (rate * eff) + 1.5e-6;
+        double t = rounds * t_tile;
+        if (s > 1) t += double(s + 1) * double(M) * double(N) * 4.0 / 5e12 + 2e-6;
+        Choice ch{bn, s, 0, 0};
+        ch.cg = cg;
+        offer(weigh(t, s > 1 ? 2 : 1, cg) * tile_weight(bn), ch);
+      }
+      if (!sk_ok) continue;
+      const int64_t iters = tiles * kbt;
+      const double operands = double(M + N) * double(batches) * double(K) * e;
+      if (iters >= units && tiles % units != 0 && (operands <= 80e6 || mode == 3)) {
+        const double share = double(iters) / units;
+        const int64_t parts = int64_t(std::ceil(double(kbt) / share)) + 1;
+        // + 3 µs: the measured cost per launch beyond the model (staggered tiles, partial
+        // stores, the exposed fixup)
+        const double t = std::ceil(share) * t_kb + (double(tiles) / units + 1.0) * 1.5e-6 + sk_fixup_time(parts) + 3e-6;
+        Choice ch{bn, 1, 1, units * cg};
+        ch.cg = cg;
+        offer(weigh(t, 3, cg) * tile_weight(bn), ch);
+      }
+      for (int64_t sl = 2; sl <= 8 && tiles * sl <= units && kbt >= 2 * sl; ++sl) {
+        const double t = double(ceil_div(kbt, sl)) * t_kb + 1.5e-6 + sk_fixup_time(sl);
+        Choice ch{bn, 1, 2, int(tiles * sl) * cg};
+        ch.cg = cg;
+        offer(weigh(t, 4, cg) * tile_weight(bn), ch);
+      }
     }
   }
   return best;
@@ -158,10 +192,12 @@ size_t split_bytes(const Choice& c, int64_t M, int64_t N) {
 }
 
 // C (+)= Σ_s part[s] in split order (deterministic); part is [splits][M][N] float32.
+// ts (may be null): this launch's timestamp slots, (start, end) %globaltimer per block.
 template <typename TC>
 __global__ void splitk_reduce(const float* __restrict__ part, int splits, int64_t M, int64_t N, TC* C, int64_t ldc,
-                              int acc) {
+                              int acc, unsigned long long* ts) {
   pdl_begin();
+  if (ts && threadIdx.x == 0) ts[2 * blockIdx.x] = global_ns();
   const int64_t n4 = N / 4, total = M * n4, slice = M * N;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     const int64_t m = i / n4, c = (i - m * n4) * 4;
@@ -177,6 +213,10 @@ __global__ void splitk_reduce(const float* __restrict__ part, int splits, int64_
       for (int e = 0; e < 4; ++e) v[e] += to_f(out[e]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) out[e] = from_f<TC>(v[e]);
+  }
+  if (ts) {
+    __syncthreads();
+    if (threadIdx.x == 0) ts[2 * blockIdx.x + 1] = global_ns();
   }
 }
 
@@ -202,19 +242,20 @@ static int make_output_map(CUtensorMap* tm, void* base, bool bf16, int64_t M, in
 int run(const Problem& pb, cudaStream_t s) {
   const bool tf32 = pb.tf32;
   const int64_t batches = int64_t(pb.batch_outer) * pb.batch_inner;
-  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, pb.act == 0, pb.fp8);
+  Choice ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, pb.act == 0, pb.fp8, pb.B.mn_major);
   if ((ch.splits > 1 || ch.sk) && (pb.split_ws == nullptr || split_bytes(ch, pb.M, pb.N) > pb.split_ws_bytes ||
                                    (ch.sk && pb.sk_flags == nullptr)))
-    ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false, pb.fp8);
+    ch = choose(tf32, pb.M, pb.N, pb.K, batches, pb.causal, false, pb.fp8, pb.B.mn_major);
   if (pb.act) ch = Choice{256, 1, 0, 0};  // the GELU epilogues are built for BN 256 only
   const int bn = ch.bn;
+  const int cg = ch.cg;
   const bool split = ch.splits > 1;
   CUtensorMap ta, tb, tc, tc2;
   memset(&tc2, 0, sizeof(tc2));
   if (pb.act == 1) XT_TRY(make_output_map(&tc2, pb.C2, true, pb.M, pb.N, pb.ldc, 1, 1, 0, 0));
   const int kind = pb.fp8 ? kFp8 : tf32 ? kTf32 : kBf16;
   XT_TRY(make_operand_map(&ta, pb.A, kind, BM));
-  XT_TRY(make_operand_map(&tb, pb.B, kind, bn));
+  XT_TRY(make_operand_map(&tb, pb.B, kind, bn / cg));  // a pair's CTA stages half of B's rows
   // TMA epilogue for every output except a bf16 C that is accumulated into (TMA reduce-add is
   // used for float32 only; bf16 accumulation keeps the direct read-modify-write stores).  A K
   // split stores float32 partial tiles into [splits][M][N] slices instead.
@@ -229,7 +270,7 @@ int run(const Problem& pb, cudaStream_t s) {
   p.M = int(pb.M);
   p.N = int(pb.N);
   p.K = int(pb.K);
-  p.num_m = int(ceil_div(pb.M, BM));
+  p.num_m = int(ceil_div(pb.M, int64_t(BM) * cg));
   p.num_n = int(ceil_div(pb.N, bn));
   p.batch_inner = split ? ch.splits : pb.batch_inner;
   p.batches = split ? ch.splits : pb.batch_inner * pb.batch_outer;
@@ -249,11 +290,19 @@ int run(const Problem& pb, cudaStream_t s) {
   p.aux = static_cast<const bf16*>(pb.aux);
   p.ld_aux = pb.ldc;
   p.flag = errflag();
+  p.wait_ns = wait_limit_ns();
   p.scale_a = pb.scale_a;
   p.scale_b = pb.scale_b;
   const int64_t tiles = int64_t(p.num_m) * p.num_n * p.batches;  // a K split counts its slices
   if (tiles > int64_t(1) << 30) return fail(XT_ERR_UNSUPPORTED, "matmul: too many tiles");
-  int grid = int(tiles < num_sms() ? tiles : num_sms());
+  int grid;
+  if (cg == 2) {
+    const int units = pair_capacity();
+    if (units < 1) return fail(XT_ERR_CUDA, "gemm: no CTA pair can be resident");
+    grid = 2 * int(tiles < units ? tiles : units);
+  } else {
+    grid = int(tiles < num_sms() ? tiles : num_sms());
+  }
   if (grid < 1) grid = 1;
   if (ch.sk) {
     p.sk = 1;
@@ -261,7 +310,7 @@ int run(const Problem& pb, cudaStream_t s) {
     p.sk_iters = tiles * p.kb_tile;
     p.sk_part = static_cast<float*>(pb.split_ws);
     p.sk_flag = pb.sk_flags;
-    grid = ch.grid;  // ≤ the SMs and ≤ the iterations: every CTA resident, every share non-empty
+    grid = ch.grid;  // ≤ the resident units and ≤ the iterations: every unit resident, every share non-empty
   }
   const bool amn = pb.A.mn_major, bmn = pb.B.mn_major;
   // algorithmic FLOPs: the unmasked work only for the causal modes
@@ -272,28 +321,35 @@ int run(const Problem& pb, cudaStream_t s) {
   void* tok = nullptr;
   // record: causal mode, or 10 × K splits, or 1000 for stream-K over every SM, 1000 + slices
   // for stream-K in lockstep K slices
-  const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, bn, int(amn), int(bmn),
-                        ch.sk == 1 ? 1000 : ch.sk == 2 ? 1000 + int(ch.grid / tiles) :
+  // (the tile width of a paired launch is recorded as 1000 + BN)
+  const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, cg == 2 ? 1000 + bn : bn, int(amn), int(bmn),
+                        ch.sk == 1 ? 1000 : ch.sk == 2 ? 1000 + int(ch.grid / cg / tiles) :
                         split ? 10 * ch.splits : p.causal};
-  const bool prof = gemm_profile_begin(s, flops, shape, &tok);
+  unsigned long long* ts = nullptr;
+  const bool prof = gemm_profile_begin(flops, shape, &ts, &tok) && grid <= kProfGemmSlots;
+  p.prof_ts = prof ? ts : nullptr;
+  int rgrid = 0;
   int st = pb.fp8    ? launch_fp8(bn, ta, tb, tc, tc2, p, grid, s)
            : tf32    ? launch_tf32(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
            : pb.act ? launch_bf16_act(pb.act, amn, bmn, ta, tb, tc, tc2, p, grid, s)
+           : cg == 2 ? launch_bf16_pair(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
                     : launch_bf16(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s);
   if (st == XT_OK && split) {
     const int64_t work = pb.M * (pb.N / 4);
     int64_t g = ceil_div(work, 256);
     if (g > int64_t(num_sms()) * 8) g = int64_t(num_sms()) * 8;
     const float* part = static_cast<const float*>(pb.split_ws);
+    unsigned long long* rts = prof && g <= kProfSlots - kProfGemmSlots ? ts + 2 * kProfGemmSlots : nullptr;
+    rgrid = rts ? int(g) : 0;
     if (pb.c_bf16)
       launch(splitk_reduce<bf16>, int(g), 256, 0, s, part, ch.splits, pb.M, pb.N, static_cast<bf16*>(pb.C), pb.ldc,
-                                                 pb.accumulate);
+                                                 pb.accumulate, rts);
     else
       launch(splitk_reduce<float>, int(g), 256, 0, s, part, ch.splits, pb.M, pb.N, static_cast<float*>(pb.C), pb.ldc,
-                                                  pb.accumulate);
+                                                  pb.accumulate, rts);
     st = check_launch("gemm K-split reduce");
   }
-  if (prof) gemm_profile_end(s, tok);
+  if (prof) gemm_profile_grids(tok, grid, rgrid);
   return st;
 }
 
@@ -370,7 +426,8 @@ static size_t matmul_ws(const xt_matmul_desc* d) {
   size_t b = gemm::kSkFlagBytes;
   if (d->dtype_ab == XT_F32) b += stage_bytes(operand_a(d, nullptr)) + stage_bytes(operand_b(d, nullptr));
   const gemm::Choice ch = gemm::choose(d->dtype_ab == XT_F32, d->M, d->N, d->K,
-                                       int64_t(d->batch_outer) * d->batch_inner, d->causal, true);
+                                       int64_t(d->batch_outer) * d->batch_inner, d->causal, true, false,
+                                       d->trans_b == 0);
   return b + gemm::split_bytes(ch, d->M, d->N);
 }
 
@@ -470,6 +527,18 @@ extern "C" {
 int xt_gemm_set_schedule(int mode) {
   XT_REQUIRE(mode >= 0 && mode <= 4, "xt_gemm_set_schedule: mode must be 0..4");
   gemm::g_schedule = mode;
+  return XT_OK;
+}
+
+int xt_gemm_set_tile(int bn) {
+  XT_REQUIRE(bn == 0 || bn == 64 || bn == 128 || bn == 192 || bn == 256, "xt_gemm_set_tile: bn must be 0, 64, 128, 192 or 256");
+  gemm::g_tile = bn;
+  return XT_OK;
+}
+
+int xt_gemm_set_pairing(int mode) {
+  XT_REQUIRE(mode >= 0 && mode <= 2, "xt_gemm_set_pairing: mode must be 0..2");
+  gemm::g_pairing = mode;
   return XT_OK;
 }
 

@@ -46,11 +46,12 @@ struct Problem {
 struct Choice {
   int bn;
   int splits;
-  int sk;    // stream-K schedule: 1 over every SM, 2 in lockstep K slices
-  int grid;  // stream-K CTAs: the SMs, or tiles × K slices (lockstep)
+  int sk;      // stream-K schedule: 1 over every SM (every resident unit), 2 in lockstep K slices
+  int grid;    // stream-K units: the SMs (or pairs), or tiles × K slices (lockstep)
+  int cg = 1;  // 2: the paired-CTA kernel, tiles of 2·BM rows, units are CTA pairs
 };
 Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split,
-              bool fp8 = false);
+              bool fp8, bool b_mn);
 size_t split_bytes(const Choice& c, int64_t M, int64_t N);
 
 // Stream-K flag words at the head of every matmul workspace: 4 per CTA for up to kSkMaxCtas CTAs.
@@ -73,20 +74,34 @@ int launch_fp8(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 int launch_bf16_act(int act, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                     const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 
-template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0>
+template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0, int CG = 1>
 int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                const Params& p, int grid, cudaStream_t s) {
-  auto k = gemm_kernel<KIND, BN, A_MN, B_MN, ACT>;
-  constexpr int smem = Cfg<KIND, BN>::SMEM;
+  auto k = gemm_kernel<KIND, BN, A_MN, B_MN, ACT, CG>;
+  constexpr int smem = Cfg<KIND, BN, CG>::SMEM;
   static bool attr_set = false;  // per instantiation; idempotent if raced
   if (!attr_set) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return check_launch("gemm: shared memory attribute");
+    if (CG == 2 && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+      return check_launch("gemm: cluster attribute");
     attr_set = true;
   }
-  launch(k, grid, kThreads, smem, s, ta, tb, tc, tc2, p);
+  if constexpr (CG == 2) {
+    if (grid % 2) return fail(XT_ERR_INVALID_ARG, "gemm: paired launch needs an even grid");
+    launch_clustered(k, grid, kThreads, smem, s, 2, ta, tb, tc, tc2, p);
+  } else {
+    launch(k, grid, kThreads, smem, s, ta, tb, tc, tc2, p);
+  }
   return check_launch("gemm kernel");
 }
+
+// bf16 paired-CTA GEMM (BN 128, 256, or 192 with B K-major; plain epilogue), launched as
+// clusters of two.
+int launch_bf16_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                     const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
+// CTA pairs of the paired kernel that can be resident at once on the current device (0 if none).
+int pair_capacity();
 
 }  // namespace gemm
 }  // namespace xt

@@ -64,6 +64,11 @@ struct Params {
   // factors of fp8 operands
   const float* scale_a;
   const float* scale_b;
+  // measurement (may be null): (start, end) %globaltimer words per CTA, at 2·blockIdx.x
+  unsigned long long* prof_ts;
+  // limit of the waits on work (xt_set_wait_limit_ns); the waits that drain a CTA's own copies
+  // and MMAs before it exits keep kTimeoutNs
+  uint64_t wait_ns;
 };
 
 // ------------------------------------------------------------------------------ PTX wrappers
@@ -99,13 +104,34 @@ __device__ __forceinline__ uint64_t globaltimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait for the phase of parity `parity`; false when the time limit expired.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of parity `parity`; false when `limit_ns` expired.  Limits of a
+// millisecond or more use the suspending try_wait; a shorter limit (set for tests of the
+// give-up paths) polls with the non-blocking test_wait, so that a wait cannot outlast it by a
+// suspension.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kTimeoutNs) {
+  if (limit_ns >= 1000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
+  }
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kTimeoutNs) return false;
+    if (mbar_test_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 
@@ -175,27 +201,92 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-template <int KIND>
+// One MMA: D (+)= A·Bᵀ over 32 bytes of K.  CG = 2 issues the paired-CTA form: the issuing
+// (even) CTA and its peer each supply 128 rows of A and half of B's rows from the same
+// shared-memory offsets, and each peer's TMEM receives its own 128 rows of D.
+template <int KIND, int CG = 1>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accum) {
-  if constexpr (KIND == kFp8) {
+#define XT_TC_MMA(GROUP, K_)                                                                       \
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                                 \
+               "tcgen05.mma.cta_group::" GROUP ".kind::" K_ " [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem), \
+               "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)                                      \
+               : "memory")
+  if constexpr (CG == 2) {
+    if constexpr (KIND == kFp8) XT_TC_MMA("2", "f8f6f4");
+    else if constexpr (KIND == kTf32) XT_TC_MMA("2", "tf32");
+    else XT_TC_MMA("2", "f16");
+  } else {
+    if constexpr (KIND == kFp8) XT_TC_MMA("1", "f8f6f4");
+    else if constexpr (KIND == kTf32) XT_TC_MMA("1", "tf32");
+    else XT_TC_MMA("1", "f16");
+  }
+#undef XT_TC_MMA
+}
+
+// ------------------------------------------------------------- paired-CTA (cluster of two) forms
+// All tcgen05 instructions of one kernel use the same cta_group; the pair kernel uses these.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Every thread of both CTAs; release / acquire orders shared-memory writes (barrier inits)
+// before the peer's first remote access.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// Tile load whose completion is signalled on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_cg(uint32_t dst_smem, uint32_t ncols) {
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+  else
+    tmem_alloc(dst_smem, ncols);
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_cg() {
+  if constexpr (CG == 2) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else tmem_relinquish();
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) {
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    tmem_dealloc(taddr, ncols);
+}
+// Arrives on `bar` once this thread's earlier tcgen05 operations have completed: CG = 2 on the
+// barrier at that offset in both CTAs of the pair, CG = 1 on this CTA's barrier only.
+template <int CG>
+__device__ __forceinline__ void tc_commit_cg(uint32_t bar) {
+  if constexpr (CG == 2) {
+    const uint16_t mask = 3;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-        : "memory");
-  } else if constexpr (KIND == kTf32) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
         : "memory");
   } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-        : "memory");
+    tc_commit(bar);
   }
 }
 // 32 lanes × 32 consecutive fp32 columns: thread t of the warp receives row (lane base + t).
@@ -237,11 +328,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Instruction descriptor for kind::f16 / kind::tf32 / kind::f8f6f4: fp32 accumulator, A/B
 // types (bf16 = 1, tf32 = 2, e4m3 = 0), operand majorness (1 = MN-major), N >> 3, M >> 4.
-template <int KIND, int N, bool A_MN, bool B_MN>
+template <int KIND, int N, bool A_MN, bool B_MN, int M = BM>
 __host__ __device__ constexpr uint32_t instr_desc() {
   constexpr uint32_t t = KIND == kTf32 ? 2u : KIND == kFp8 ? 0u : 1u;
   return (1u << 4) | (t << 7) | (t << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         (uint32_t(N >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // bf16 × bf16 → fp32 instruction descriptor for an M × N tile.
@@ -255,14 +346,16 @@ constexpr uint32_t tmem_cols() {
   return 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
 }
 
-template <int KIND, int BN>
+// CG = 2: a CTA pair computes a (2·BM) × BN tile; each CTA stages its own BM rows of A and
+// BN / 2 rows of B.
+template <int KIND, int BN, int CG = 1>
 struct Cfg {
   static constexpr int E = KIND == kTf32 ? 4 : KIND == kFp8 ? 1 : 2;
   static constexpr int BK = 128 / E;         // K elements per stage (one 128-byte row)
   static constexpr int ATOM = 128 / E;       // MN elements per 128-byte swizzle row
   static constexpr int UK = 32 / E;          // K per MMA instruction (32 bytes)
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = BN / CG * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
   static constexpr int STAGING_BYTES = 4 * 2 * 4096;  // 4 epilogue warps × 2 buffers × 32 rows × 128 B
@@ -315,23 +408,25 @@ __device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
 struct Cursor {
   int64_t it, end;
 };
-__device__ __forceinline__ Cursor cursor_begin(const Params& p) {
+// `u` of `nu` schedule units: a CTA, or a CTA pair of the paired kernel.
+__device__ __forceinline__ Cursor cursor_begin(const Params& p, int u, int nu) {
   Cursor c;
   if (p.sk) {
-    c.it = int64_t(blockIdx.x) * p.sk_iters / gridDim.x;
-    c.end = int64_t(blockIdx.x + 1) * p.sk_iters / gridDim.x;
+    c.it = int64_t(u) * p.sk_iters / nu;
+    c.end = int64_t(u + 1) * p.sk_iters / nu;
   } else {
-    c.it = blockIdx.x;
+    c.it = u;
     c.end = 0;
   }
   return c;
 }
 // Next piece, false when none is left; kb0 = kb1 = -1 for a whole tile of the plain schedule.
-__device__ __forceinline__ bool cursor_next(Cursor& c, const Params& p, int total, int& t, int& kb0, int& kb1) {
+__device__ __forceinline__ bool cursor_next(Cursor& c, const Params& p, int total, int nu, int& t, int& kb0,
+                                            int& kb1) {
   if (!p.sk) {
     if (c.it >= total) return false;
     t = int(c.it);
-    c.it += gridDim.x;
+    c.it += nu;
     kb0 = kb1 = -1;
     return true;
   }
@@ -343,9 +438,9 @@ __device__ __forceinline__ bool cursor_next(Cursor& c, const Params& p, int tota
   c.it += kb1 - kb0;
   return true;
 }
-// Stream-K: the CTA whose share holds iteration x, i.e. the largest c with ⌊c·I/G⌋ ≤ x.
-__device__ __forceinline__ int sk_cta_of(int64_t x, const Params& p) {
-  return int(((x + 1) * int64_t(gridDim.x) - 1) / p.sk_iters);
+// Stream-K: the unit whose share holds iteration x, i.e. the largest c with ⌊c·I/G⌋ ≤ x.
+__device__ __forceinline__ int sk_cta_of(int64_t x, const Params& p, int nu) {
+  return int(((x + 1) * int64_t(nu) - 1) / p.sk_iters);
 }
 
 // Stream-K fixup of a tile's accumulator in TMEM (columns tacc .. tacc + BN of this warp's
@@ -353,11 +448,12 @@ __device__ __forceinline__ int sk_cta_of(int64_t x, const Params& p) {
 // time (tcgen05.ld, add, tcgen05.st), with the loads of the group two ahead in flight.  Slot
 // layout: float4 (g·8 + j)·BM + row holds columns 32·g + 4·j .. +4 of the row, so a warp's
 // loads and stores each cover 512 contiguous bytes.
-template <int BN>
-__device__ __forceinline__ void sk_fixup(uint32_t tacc, const Params& p, int first, int last, int row) {
+// Slot of unit cc: cc·CG + rank (each CTA of a pair keeps its own rows' partial).
+template <int BN, int CG = 1>
+__device__ __forceinline__ void sk_fixup(uint32_t tacc, const Params& p, int first, int last, int rank, int row) {
   constexpr int NG = BN / 32;
   for (int cc = first; cc <= last; ++cc) {
-    const float4* src = reinterpret_cast<const float4*>(p.sk_part) + size_t(cc) * (BM * BN / 4) + row;
+    const float4* src = reinterpret_cast<const float4*>(p.sk_part) + size_t(cc * CG + rank) * (BM * BN / 4) + row;
     float4 v[2][8];
 #pragma unroll
     for (int g = 0; g < 2 && g < NG; ++g)
@@ -386,15 +482,28 @@ __device__ __forceinline__ void sk_fixup(uint32_t tacc, const Params& p, int fir
 
 // ACT: the epilogue's GELU mode (Params::act), a template parameter so the plain GEMMs carry
 // none of its code.
-template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0>
+//
+// CG = 2 (launched as clusters of two CTAs): each pair computes (2·BM) × BN tiles with the
+// paired MMA.  The even CTA's lane issues every MMA; each CTA's producer loads its own BM rows
+// of A and BN / 2 rows of B into its own shared memory and signals the even CTA's full barrier
+// (which expects both CTAs' bytes); each MMA group's commit arrives on the stage's empty
+// barrier of both CTAs and, per tile, on both CTAs' accumulator-full barriers; both CTAs'
+// epilogues (each draining its own 128 TMEM lanes) arrive on the even CTA's accumulator-empty
+// barrier.  Schedule units (Params::num_m tiles of 2·BM rows, stream-K shares) are pairs.
+template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0, int CG = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, const Params p) {
-  pdl_begin();
-  using C_ = Cfg<KIND, BN>;
+  static_assert(CG == 1 || (CG == 2 && ACT == 0 && BN % 32 == 0), "paired tiles: plain epilogue, BN / 2 whole atoms");
+  // The set-up below (barriers, tensor-map prefetch, TMEM) reads nothing a preceding kernel
+  // writes, so it runs before the programmatic-launch wait.
+  using C_ = Cfg<KIND, BN, CG>;
   constexpr int BK = C_::BK, ATOM = C_::ATOM, UK = C_::UK, STAGES = C_::STAGES;
-  constexpr uint32_t IDESC = instr_desc<KIND, BN, A_MN, B_MN>();
+  constexpr uint32_t IDESC = instr_desc<KIND, BN, A_MN, B_MN, BM * CG>();
   constexpr uint32_t TCOLS = tmem_cols<BN>();
+  constexpr int BNH = BN / CG;  // B rows staged by one CTA
+  const int rank = CG == 2 ? int(cluster_ctarank()) : 0;
+  const int unit = int(blockIdx.x) / CG, units = int(gridDim.x) / CG;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -404,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  uint64_t* mma_done = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -415,8 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 4);
+      mbar_init(smem_u32(&tempty[b]), 4 * CG);
     }
+    mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -427,20 +538,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ACT == 1) prefetch_tmap(&tmC2);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TCOLS);
-    tmem_relinquish();
+    tmem_alloc_cg<CG>(smem_u32(tmem_slot), TCOLS);
+    tmem_relinquish_cg<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) cluster_sync_all();  // the peer's barriers exist before any remote arrive
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  pdl_wait();  // the operands (and C, when accumulating) are the preceding kernels' outputs
+  pdl_trigger();
+  if (p.prof_ts && threadIdx.x == 0) p.prof_ts[2 * blockIdx.x] = global_ns();
 
   const int total = p.num_m * p.num_n * p.batches;
 
+  // ti.m0: this CTA's first row (tile row + rank·BM); ti.n0: the tile's first column.
   auto info = [&](int t, int kb0, int kb1) {
     TileInfo ti = tile_info<BK>(t, p);
     const int per = p.num_m * p.num_n;
     const int r = t - (t / per) * per;
+    if constexpr (CG == 2) ti.m0 = ti.m0 * 2 + rank * BM;
     ti.n0 = (r / p.num_m) * BN;
     if (p.causal == 1 && ti.n0 >= ti.m0 + BM) ti.skip = true;
     if (kb0 >= 0) {  // a stream-K piece
@@ -461,63 +578,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      Cursor cur = cursor_begin(p);
+      Cursor cur = cursor_begin(p, unit, units);
       int t, kb0, kb1;
-      while (!*abort_flag && cursor_next(cur, p, total, t, kb0, kb1)) {
+      // load: one box into this CTA's stage, completing on the stage's full barrier (the even
+      // CTA's for a pair)
+      auto load = [&](uint32_t dst, const CUtensorMap* tm, uint32_t fb, int c0, int c1, int c2, int c3) {
+        if constexpr (CG == 2) tma_load_4d_pair(dst, tm, fb, c0, c1, c2, c3);
+        else tma_load_4d(dst, tm, fb, c0, c1, c2, c3);
+      };
+      while (!*abort_flag && cursor_next(cur, p, total, units, t, kb0, kb1)) {
         const TileInfo ti = info(t, kb0, kb1);
         if (ti.skip) continue;
+        const int nb0 = ti.n0 + rank * BNH;  // this CTA's rows of B
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
           if (*abort_flag) break;
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1)) { give_up(); break; }
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_expect_tx(fb, C_::STAGE_BYTES);
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.wait_ns)) { give_up(); break; }
+          uint32_t fb = smem_u32(&full[stage]);
+          if (rank == 0) mbar_expect_tx(fb, CG * C_::STAGE_BYTES);
+          if constexpr (CG == 2) fb = mapa_shared(fb, 0);
           const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
           const uint32_t b_s = a_s + C_::A_BYTES;
           const int k0 = kb * BK;
           if constexpr (!A_MN) {
-            tma_load_4d(a_s, &tmA, fb, k0, ti.m0, ti.ozi, ti.ozo);
+            load(a_s, &tmA, fb, k0, ti.m0, ti.ozi, ti.ozo);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / ATOM; ++j)
-              tma_load_4d(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.ozi, ti.ozo);
+              load(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.ozi, ti.ozo);
           }
           if constexpr (!B_MN) {
-            tma_load_4d(b_s, &tmB, fb, k0, ti.n0, ti.ozi, ti.ozo);
+            load(b_s, &tmB, fb, k0, nb0, ti.ozi, ti.ozo);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / ATOM; ++j)
-              tma_load_4d(b_s + j * (BK * 128), &tmB, fb, ti.n0 + j * ATOM, k0, ti.ozi, ti.ozo);
+            for (int j = 0; j < BNH / ATOM; ++j)
+              load(b_s + j * (BK * 128), &tmB, fb, nb0 + j * ATOM, k0, ti.ozi, ti.ozo);
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
       // Wait (bounded) for the copies that may still be in flight: the last min(STAGES, issued)
-      // fills, so no TMA write lands in shared memory after the CTA exits.
-      const int pending = issued < STAGES ? issued : STAGES;
+      // fills, so no TMA write lands in shared memory after the CTA exits.  A pair's full
+      // barriers live in the even CTA and count both CTAs' bytes: the even CTA waits for both,
+      // and the cluster barrier before exit keeps the odd CTA resident until then.
+      const int pending = rank != 0 ? 0 : issued < STAGES ? issued : STAGES;
       for (int i = 0; i < pending; ++i) {
         if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
         if (!mbar_wait(smem_u32(&full[stage]), phase)) { give_up(); break; }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ------------------------------------------------------------------ MMA issuer
       int stage = 0;
       uint32_t phase = 0;
       int ab = 0;
       uint32_t aphase = 0;
-      Cursor cur = cursor_begin(p);
+      bool any = false;
+      Cursor cur = cursor_begin(p, unit, units);
       int t, kb0, kb1;
-      while (!*abort_flag && cursor_next(cur, p, total, t, kb0, kb1)) {
-        const TileInfo ti = info(t, kb0, kb1);
-        if (ti.skip || ti.kb_end <= ti.kb_begin) continue;
-        if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1)) { give_up(); break; }
+      // The next piece's coordinates are worked out while the current tile's first MMAs run, so
+      // the tensor pipe does not wait on this thread's index arithmetic between tiles.
+      bool have = cursor_next(cur, p, total, units, t, kb0, kb1);
+      TileInfo ti_next;
+      if (have) ti_next = info(t, kb0, kb1);
+      while (have && !*abort_flag) {
+        const TileInfo ti = ti_next;
+        bool fetched = false;
+        auto fetch = [&]() {
+          have = cursor_next(cur, p, total, units, t, kb0, kb1);
+          if (have) ti_next = info(t, kb0, kb1);
+          fetched = true;
+        };
+        if (ti.skip || ti.kb_end <= ti.kb_begin) {
+          fetch();
+          continue;
+        }
+        if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1, p.wait_ns)) { give_up(); break; }
         tc_fence_after();
         const uint32_t d_tmem = tbase + uint32_t(ab * BN);
         bool ok = true;
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
-          if (*abort_flag || !mbar_wait(smem_u32(&full[stage]), phase)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait(smem_u32(&full[stage]), phase, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
           const uint32_t b_s = a_s + C_::A_BYTES;
@@ -527,14 +669,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc(a_s + kk * UK * C_::E, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(b_s + kk * UK * 128, BK * 128, 1024)
                                      : smem_desc(b_s + kk * UK * C_::E, 16, 1024);
-            tc_mma<KIND>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
+            tc_mma<KIND, CG>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
           }
-          tc_commit(smem_u32(&empty[stage]));  // frees the smem slot once these MMAs finish
+          any = true;
+          tc_commit_cg<CG>(smem_u32(&empty[stage]));  // frees the smem slot(s) once these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (!fetched) fetch();
         }
         if (!ok) { give_up(); break; }
-        tc_commit(smem_u32(&tfull[ab]));  // accumulator ready for the epilogue
+        tc_commit_cg<CG>(smem_u32(&tfull[ab]));  // accumulator ready for the epilogue(s)
         if (++ab == 2) { ab = 0; aphase ^= 1; }
+      }
+      // every MMA issued has completed (also after a give-up) before TMEM is released
+      if (any) {
+        tc_commit_cg<CG>(smem_u32(mma_done));  // (a pair's odd CTA receives an unused arrival)
+        if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
       }
     }
   } else {
@@ -546,19 +695,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aphase = 0;
     uint32_t chunk = 0;  // staged stores issued by this warp (selects the staging buffer)
-    Cursor cur = cursor_begin(p);
+    const int self = unit * CG + rank;  // this CTA's stream-K slot and flags
+    // this warp's share of freeing accumulator ab: a pair's barrier is in the even CTA
+    const uint32_t tempty0 = smem_u32(&tempty[0]);
+    const uint32_t tempty_at = CG == 2 ? mapa_shared(tempty0, 0) : tempty0;
+    auto release_acc = [&](int b) {
+      if (CG == 2 && rank != 0) mbar_arrive_cluster(tempty_at + uint32_t(b * 8));
+      else mbar_arrive(tempty0 + uint32_t(b * 8));
+    };
+    Cursor cur = cursor_begin(p, unit, units);
     int t, kb0, kb1;
-    while (cursor_next(cur, p, total, t, kb0, kb1)) {
+    while (cursor_next(cur, p, total, units, t, kb0, kb1)) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const TileInfo ti = info(t, kb0, kb1);
       if (ti.skip) continue;
       const int row = ti.m0 + q * 32 + lane;
       const bool empty_k = ti.kb_end <= ti.kb_begin;
       // stream-K piece kind: 1 = a later part of the tile (partial to its slot), 2 = the tile's
-      // first k-blocks with later parts in CTAs blockIdx.x + 1 .. sk_last (adds their partials)
+      // first k-blocks with later parts in units unit + 1 .. sk_last (adds their partials)
       const int kind = kb0 > 0 ? 1 : (kb0 == 0 && kb1 < p.kb_tile) ? 2 : 0;
       if (!empty_k) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[ab]), aphase));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[ab]), aphase, p.wait_ns));
         if (!ok) {
           if (lane == 0) give_up();
           break;
@@ -566,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       if (kind == 1) {
-        float4* slot = reinterpret_cast<float4*>(p.sk_part) + size_t(blockIdx.x) * (BM * BN / 4);
+        float4* slot = reinterpret_cast<float4*>(p.sk_part) + size_t(self) * (BM * BN / 4);
         const int rowt = q * 32 + lane;
 #pragma unroll 1
         for (int g = 0; g < BN / 32; ++g) {
@@ -580,23 +737,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+        if (lane == 0) release_acc(ab);
         if (++ab == 2) { ab = 0; aphase ^= 1; }
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(p.sk_flag + blockIdx.x * 4 + q, uint32_t(t + 1));
+        if (lane == 0) st_release_gpu(p.sk_flag + self * 4 + q, uint32_t(t + 1));
         continue;
       }
       int sk_last = 0;
       if (kind == 2) {
-        sk_last = sk_cta_of(int64_t(t) * p.kb_tile + p.kb_tile - 1, p);
+        sk_last = sk_cta_of(int64_t(t) * p.kb_tile + p.kb_tile - 1, p, units);
         bool ok = true;
-        for (int cc = blockIdx.x + 1; cc <= sk_last && ok; ++cc) {
-          const uint32_t* f = p.sk_flag + cc * 4 + q;
+        for (int cc = unit + 1; cc <= sk_last && ok; ++cc) {
+          const uint32_t* f = p.sk_flag + (cc * CG + rank) * 4 + q;
           if (ld_acquire_gpu(f) != uint32_t(t + 1)) {
             const uint64_t t0 = globaltimer();
             while (ld_acquire_gpu(f) != uint32_t(t + 1))
-              if (globaltimer() - t0 > kTimeoutNs) { ok = false; break; }
+              if (globaltimer() - t0 > p.wait_ns) { ok = false; break; }
           }
         }
         if (!__all_sync(0xffffffffu, ok)) {
@@ -605,10 +762,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the flags are this launch's alone until it completes: clear them for the next one
         if (lane == 0)
-          for (int cc = blockIdx.x + 1; cc <= sk_last; ++cc) p.sk_flag[cc * 4 + q] = 0u;
+          for (int cc = unit + 1; cc <= sk_last; ++cc) p.sk_flag[(cc * CG + rank) * 4 + q] = 0u;
         // the later parts' sums join this piece's accumulator in TMEM; the store paths below
         // then read the tile's full sum
-        sk_fixup<BN>(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN), p, blockIdx.x + 1, sk_last, q * 32 + lane);
+        sk_fixup<BN, CG>(tbase + (uint32_t(q * 32) << 16) + uint32_t(ab * BN), p, unit + 1, sk_last, rank,
+                         q * 32 + lane);
       }
       if (p.tma_store) {
         // ---- staged TMA stores: chunk = 32 rows × 128 bytes (32 fp32 or 64 bf16 columns)
@@ -740,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!empty_k) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+          if (lane == 0) release_acc(ab);
           if (++ab == 2) { ab = 0; aphase ^= 1; }
         }
         continue;
@@ -808,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!empty_k) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tempty[ab]));
+        if (lane == 0) release_acc(ab);
         if (++ab == 2) { ab = 0; aphase ^= 1; }
       }
     }
@@ -816,10 +974,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  // a pair: neither CTA releases TMEM or exits while the other may still signal its barriers
+  // or (the even CTA's MMAs) read its shared memory and write its TMEM
+  if constexpr (CG == 2) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, TCOLS);
+    tmem_dealloc_cg<CG>(tbase, TCOLS);
   }
+  if (p.prof_ts && threadIdx.x == 0) p.prof_ts[2 * blockIdx.x + 1] = global_ns();
 }
 
 }  // namespace gemm

@@ -74,6 +74,7 @@ _I, _I64, _F, _D, _U64, _SZP = C.c_int, C.c_int64, C.c_float, C.c_double, C.c_ui
 _SIGS = {
     "xt_get_device_errors": [C.POINTER(C.c_uint32), _VP],
     "xt_clear_device_errors": [_VP],
+    "xt_set_wait_limit_ns": [C.c_uint64],
     "xt_profile_gemm": [_I],
     "xt_profile_gemm_read": [C.POINTER(C.c_double), C.POINTER(C.c_float), C.POINTER(C.c_int), _I,
                              C.POINTER(C.c_int)],
@@ -129,6 +130,8 @@ _SIGS = {
     "xt_embedding_bwd": [_VP, _VP, _VP, _VP, _I64, _I, _I64, _I64, _I, _I, _VP, _I, _VP],
     "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
     "xt_gemm_set_schedule": [_I],
+    "xt_gemm_set_pairing": [_I],
+    "xt_gemm_set_tile": [_I],
     "xt_quantize_fp8_workspace_size": [_I64, _SZP],
     "xt_quantize_fp8": [_VP, _I64, _I, _VP, _VP, _VP, C.c_size_t, _VP],
     "xt_matmul_fp8_fwd": [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _I, _F, _VP, _VP, _I, _VP],
@@ -163,6 +166,8 @@ def lib():
         L.xt_version.argtypes = []
         L.xt_launch_count.restype = C.c_uint64
         L.xt_launch_count.argtypes = []
+        L.xt_get_wait_limit_ns.restype = C.c_uint64
+        L.xt_get_wait_limit_ns.argtypes = []
         for name, args in _SIGS.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -172,11 +177,20 @@ def lib():
 
 
 def exported_symbols():
-    return ["xt_last_error", "xt_version", "xt_launch_count", *_SIGS.keys()]
+    return ["xt_last_error", "xt_version", "xt_launch_count", "xt_get_wait_limit_ns", *_SIGS.keys()]
 
 
 def launch_count() -> int:
     return int(lib().xt_launch_count())
+
+
+def set_wait_limit_ns(ns: int):
+    """Limit of the tensor-core kernels' bounded waits on work (0: the default, 2 s)."""
+    call("xt_set_wait_limit_ns", int(ns))
+
+
+def wait_limit_ns() -> int:
+    return int(lib().xt_get_wait_limit_ns())
 
 
 def profile_gemm(capacity: int):
@@ -255,6 +269,16 @@ def gemm_set_schedule(mode: int):
     """0 model's choice, 1 whole tiles, 2 K split, 3 stream-K over every SM, 4 stream-K in
     lockstep K slices (2-4 where allowed)."""
     call("xt_gemm_set_schedule", int(mode))
+
+
+def gemm_set_pairing(mode: int):
+    """0 model's choice, 1 never the paired-CTA kernel, 2 the paired kernel wherever allowed."""
+    call("xt_gemm_set_pairing", int(mode))
+
+
+def gemm_set_tile(bn: int):
+    """0 model's choice, else the GEMM tile width BN (64, 128, 192, 256) wherever allowed."""
+    call("xt_gemm_set_tile", int(bn))
 
 
 def device_errors(s=None) -> int:
