@@ -762,6 +762,36 @@ def run_sweep(args):
         TP.backward(L)
     report(f"fan-out CE + sum(0.5x) + sum(x*x), tape fwd+bwd, fp32 grad {R}x{V} (vs the fused minimum)",
            timed(fanout, n=5), 2 * n + 4 * n)
+    # one pass: rows split across a cluster of CTAs (forward and backward, the gradient in place)
+    Xc = X.clone()
+    report(f"cross_entropy fwd+bwd one pass (rows split over a cluster), bf16 in place {R}x{V}",
+           timed(lambda: xt.xt_cross_entropy_fwd_bwd(Xc, tg, lse, loss, one, Xc, ws=cws)), 2 * n + 2 * n)
+    del Xc
+    report(f"cross_entropy fwd+bwd one pass (rows split over a cluster), bf16 -> f32 grad {R}x{V}",
+           timed(lambda: xt.xt_cross_entropy_fwd_bwd(X, tg, lse, loss, one, G, ws=cws)), 2 * n + 4 * n)
+    sums = torch.empty(3, dtype=torch.float32, device=dev)
+    fws = xt.workspace(xt.ws_bytes("xt_cross_entropy_fanout_workspace_size", R), dev)
+    # the 12-layer stack's vocabulary: in place (one CTA per row) and into a float32 gradient
+    # (rows split over a cluster)
+    Vs = synth.BLOCK_CONFIGS["gpt12"]["V"]
+    Xs = (torch.randn(R, Vs, generator=g) * cfg["std"]).to(torch.bfloat16).to(dev)
+    tgs = torch.randint(0, Vs, (R,), generator=g, dtype=torch.int32).to(dev)
+    Gs = torch.empty(R, Vs, dtype=torch.float32, device=dev)
+    ns = R * Vs
+    report(f"cross_entropy fwd+bwd one pass, bf16 in place {R}x{Vs}",
+           timed(lambda: xt.xt_cross_entropy_fwd_bwd(Xs, tgs, lse, loss, one, Xs, ws=cws)), 4 * ns)
+    report(f"cross_entropy fwd+bwd one pass (rows split over a cluster), bf16 -> f32 grad {R}x{Vs}",
+           timed(lambda: xt.xt_cross_entropy_fwd_bwd(Xs, tgs, lse, loss, one, Gs, ws=cws)), 6 * ns)
+    del Xs, Gs
+
+    def fanout_fused():
+        x = TP.leaf(X, grad_dtype=torch.float32)
+        TP.backward(TP.cross_entropy_fanout(x, tg, 0.5, 1.0))
+    report(f"fan-out CE + sum(0.5x) + sum(x*x), fused node (one pass), tape fwd+bwd, fp32 grad {R}x{V} "
+           f"(vs the fused minimum)", timed(fanout_fused, n=20), 2 * n + 4 * n)
+    report(f"fan-out fused kernel alone, fp32 grad {R}x{V} (vs the fused minimum)",
+           timed(lambda: xt.xt_cross_entropy_fanout_fwd_bwd(X, tg, 0.5, 1.0, lse, loss, sums, G, ws=fws)),
+           2 * n + 4 * n)
 
 
 def main():

@@ -279,12 +279,35 @@ int xt_cross_entropy_workspace_size(int64_t rows, size_t* bytes);
  * graph): the results of xt_cross_entropy_fwd followed by xt_cross_entropy_bwd with acc = 0
  * (lse, loss, dlogits; dlogits may be logits), up to float32 summation order.  Each row is
  * held in shared memory while its lse and gradient are formed, so the logits are read from
- * HBM once; rows of more than 200 KB, or dt ≠ dt_grad, take the two-kernel path. */
+ * HBM once.  Rows of more than 200 KB (e.g. 128256 bf16 logits) are split across a cluster of
+ * 2, 4 or 8 CTAs, each holding its chunk of the row; the chunks' (max, Σ exp) pairs are
+ * exchanged through distributed shared memory and merged in rank order.  Rows whose length
+ * is not a multiple of 16 bytes, or buffers not 16-byte aligned, take the two-kernel path. */
 int xt_cross_entropy_fwd_bwd(const void* logits, const int32_t* targets, float* lse, float* loss,
                              const float* upstream, void* dlogits, int64_t rows, int64_t V, int dt,
                              int dt_grad, void* ws, void* stream);
 int xt_cross_entropy_fwd(const void* logits, const int32_t* targets, float* lse, float* loss,
                          int64_t rows, int64_t V, int dt, void* ws, void* stream);
+/* The fan-out of [AE] § 梯度累加 fused: one logits tensor x [rows, V] consumed by three ops
+ * whose scalar results are added, L = CE(x) + c_lin·Σx + c_sq·Σ(x∘x), forward and backward in
+ * one pass over x.  The gradient is the sum of the three consumers' contributions times the
+ * upstream gradient u of L (device float32 scalar; NULL means 1, the loss at the root):
+ *   grad (+)= u·((softmax(x_r) − onehot(t_r))/rows + c_lin + 2·c_sq·x)   (float32, [rows, V]),
+ * written once (acc = 1 adds it to grad's contents: later pushes add).  Outputs (device
+ * float32): loss = CE mean, sums[0] = Σx, sums[1] = Σx², sums[2] = L; lse [rows].  Rows are
+ * split across a cluster of CTAs as in xt_cross_entropy_fwd_bwd; V·element size must be a
+ * multiple of 16 bytes and logits / grad 16-byte aligned (XT_ERR_ALIGNMENT).  ws:
+ * xt_cross_entropy_fanout_workspace_size bytes.  A target outside [0, V) sets XT_DEVERR_INDEX
+ * and makes that row's loss term and gradient NaN. */
+int xt_cross_entropy_fanout_workspace_size(int64_t rows, size_t* bytes);
+/* Process-wide override of how the one-pass cross-entropy splits wide rows: clusters of cl ∈
+ * {1, 2, 4, 8} CTAs with nb ∈ {1, 2} chunk buffers each (where the chunks fit), or (0, 0) for
+ * the automatic choice (default).  For measurement and tests; XT_ERR_INVALID_ARG otherwise. */
+int xt_ce_set_split(int cl, int nb);
+int xt_cross_entropy_fanout_fwd_bwd(const void* logits, const int32_t* targets, float c_lin, float c_sq,
+                                    const float* upstream, float* lse, float* loss, float* sums, void* grad,
+                                    int acc, int64_t rows, int64_t V, int dt, void* ws, size_t ws_bytes,
+                                    void* stream);
 int xt_cross_entropy_bwd(const void* logits, const int32_t* targets, const float* lse,
                          const float* upstream, void* dlogits, int64_t rows, int64_t V, int dt,
                          int dt_grad, int acc, void* stream);

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "internal.cuh"
 
 namespace xt {
 
@@ -1644,8 +1645,16 @@ int xt_cross_entropy_fwd_bwd(const void* logits, const int32_t* targets, float* 
   XT_REQUIRE(logits && targets && lse && loss && upstream && dlogits && ws, "xt_cross_entropy_fwd_bwd: NULL pointer");
   XT_REQUIRE(!(logits == dlogits && dt != dt_grad), "xt_cross_entropy_fwd_bwd: in-place needs equal dtypes");
   cudaStream_t s = as_stream(stream);
-  if (!ce_fused_fits(V, dt) || dt != dt_grad || !aligned16(logits) || !aligned16(dlogits)) {
-    // rows that do not fit the single pass: the forward then the backward
+  const bool vec_ok = V % int64_t(16 / dtype_size(dt)) == 0 && aligned16(logits) && aligned16(dlogits);
+  if (vec_ok && (!ce_fused_fits(V, dt) || dt != dt_grad) && ce_split_cluster(V, dt) > 0)
+    // wide rows, or a gradient of another dtype: the chunked one-pass kernel (rows split
+    // across a cluster of CTAs when wide); rows of up to 200 KB written in place keep the
+    // one-CTA-per-row kernel below, which measured faster in place (0.65 against 0.62 of HBM
+    // at 8192 × 50304 bf16)
+    return ce_split_run(logits, targets, lse, loss, nullptr, upstream, dlogits, rows, V, dt, dt_grad, 0, 0.f, 0.f, ws,
+                        s);
+  if (!vec_ok || !ce_fused_fits(V, dt) || dt != dt_grad) {
+    // rows without 16-byte vectors: the forward then the backward
     XT_TRY(xt_cross_entropy_fwd(logits, targets, lse, loss, rows, V, dt, ws, stream));
     return xt_cross_entropy_bwd(logits, targets, lse, upstream, dlogits, rows, V, dt, dt_grad, 0, stream);
   }

@@ -78,6 +78,11 @@ def topo_order(root: Var):
     return order
 
 
+# The seed tensor of the backward pass in progress (the loss's grad, exactly 1): a closure that
+# receives it knows its node is the root with upstream 1.
+_seed = [None]
+
+
 def backward(loss: Var):
     if loss.value.numel() != 1:
         raise ValueError("backward() needs a scalar loss")
@@ -85,10 +90,15 @@ def backward(loss: Var):
     seed = torch.empty(1, dtype=_F32, device=loss.value.device)
     one = torch.ones(1, dtype=_F32, device=loss.value.device)
     xt.xt_convert(seed, one)
-    push(loss, seed if loss.value.dtype == _F32 else _cast(seed, loss.value.dtype), owned=True)
-    for node in reversed(order):
-        if node.backward_fn is not None and node.grad is not None:
-            node.backward_fn(node.grad, node.parents)
+    seed = seed if loss.value.dtype == _F32 else _cast(seed, loss.value.dtype)
+    push(loss, seed, owned=True)
+    _seed[0] = seed
+    try:
+        for node in reversed(order):
+            if node.backward_fn is not None and node.grad is not None:
+                node.backward_fn(node.grad, node.parents)
+    finally:
+        _seed[0] = None
 
 
 def _empty_like(t, dtype=None):
@@ -290,6 +300,47 @@ def cross_entropy(x: Var, targets: torch.Tensor) -> Var:
         else:                # later push: accumulate in place (no intermediate buffer)
             xt.xt_cross_entropy_bwd(p.value, targets, lse, up, p.grad, acc=1)
     return Var(loss, [x], bw)
+
+
+def cross_entropy_fanout(x: Var, targets: torch.Tensor, c_lin: float, c_sq: float) -> Var:
+    """L = cross_entropy(x) + c_lin·Σx + c_sq·Σ(x∘x) as one node: the three consumers of x of
+    [AE] § 梯度累加's fan-out example fused, forward and backward in one pass over x (each row
+    held on chip while its lse and gradient are formed).  The forward already writes
+    dL/dx for upstream 1 into a float32 buffer the node owns; when the node is the backward's
+    root (its upstream is the seed, exactly 1) that buffer is pushed as x's gradient, otherwise
+    the backward runs the pass again scaled by the upstream.  Value: the float32 scalar L, a
+    view of a 3-element tensor (Σx, Σx², L)."""
+    rows, V = x.value.shape
+    dev = x.value.device
+    lse = torch.empty(rows, dtype=_F32, device=dev)
+    loss = torch.empty(1, dtype=_F32, device=dev)
+    sums = torch.empty(3, dtype=_F32, device=dev)
+    gbuf = torch.empty((rows, V), dtype=_F32, device=dev)
+    xt.xt_cross_entropy_fanout_fwd_bwd(x.value, targets, c_lin, c_sq, lse, loss, sums, gbuf)
+    state = {"g": gbuf}
+
+    def bw(g, ps):
+        p = ps[0]
+        buf = state.pop("g")
+        if g is _seed[0]:
+            push(p, buf, owned=True)
+            return
+        del buf
+        up = _cast(g, _F32)
+        if p.grad is None:
+            out = torch.empty(p.value.shape, dtype=_F32, device=dev)
+            xt.xt_cross_entropy_fanout_fwd_bwd(p.value, targets, c_lin, c_sq, lse, loss, sums, out, upstream=up)
+            push(p, out, owned=True)
+        elif p.grad.dtype == _F32:
+            xt.xt_cross_entropy_fanout_fwd_bwd(p.value, targets, c_lin, c_sq, lse, loss, sums, p.grad, upstream=up,
+                                               acc=1)
+        else:
+            out = torch.empty(p.value.shape, dtype=_F32, device=dev)
+            xt.xt_cross_entropy_fanout_fwd_bwd(p.value, targets, c_lin, c_sq, lse, loss, sums, out, upstream=up)
+            push(p, out)
+    node = Var(sums[2:3], [x], bw)
+    node.name = "cross_entropy_fanout"
+    return node
 
 
 def dropout(x: Var, p: float, seed: int, training: bool = True) -> Var:

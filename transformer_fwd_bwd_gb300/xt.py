@@ -120,6 +120,10 @@ _SIGS = {
     "xt_cross_entropy_fwd": [_VP, _VP, _VP, _VP, _I64, _I64, _I, _VP, _VP],
     "xt_cross_entropy_fwd_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _VP, _VP],
     "xt_cross_entropy_bwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I, _I, _I, _VP],
+    "xt_cross_entropy_fanout_workspace_size": [_I64, _SZP],
+    "xt_ce_set_split": [_I, _I],
+    "xt_cross_entropy_fanout_fwd_bwd": [_VP, _VP, _F, _F, _VP, _VP, _VP, _VP, _VP, _I, _I64, _I64, _I, _VP,
+                                        C.c_size_t, _VP],
     "xt_dropout_fwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _VP],
     "xt_dropout_bwd": [_VP, _VP, _I64, _F, _U64, _I, _I, _I, _VP],
     "xt_dropout_bwd_ex": [_VP, _I, _VP, _I, _I64, _F, _U64, _I, _I, _VP],
@@ -274,6 +278,11 @@ def gemm_set_schedule(mode: int):
 def gemm_set_pairing(mode: int):
     """0 model's choice, 1 never the paired-CTA kernel, 2 the paired kernel wherever allowed."""
     call("xt_gemm_set_pairing", int(mode))
+
+
+def ce_set_split(cl: int, nb: int):
+    """Cross-entropy row split: clusters of cl CTAs with nb chunk buffers, (0, 0) automatic."""
+    call("xt_ce_set_split", int(cl), int(nb))
 
 
 def gemm_set_tile(bn: int):
@@ -502,6 +511,17 @@ def xt_cross_entropy_fwd_bwd(logits, targets, lse, loss, upstream, dlogits, ws=N
         ws = workspace(ws_bytes("xt_cross_entropy_workspace_size", rows), logits.device)
     call("xt_cross_entropy_fwd_bwd", ptr(logits), ptr(targets), ptr(lse), ptr(loss), ptr(upstream), ptr(dlogits),
          rows, V, dt(logits), dt(dlogits), ptr(ws), stream(s))
+
+
+def xt_cross_entropy_fanout_fwd_bwd(logits, targets, c_lin, c_sq, lse, loss, sums, grad, upstream=None, acc=0,
+                                    ws=None, s=None):
+    """L = CE(x) + c_lin·Σx + c_sq·Σx∘x forward and backward in one pass; grad (+)= u·dL/dx (float32),
+    u the device scalar `upstream` (None: 1)."""
+    rows, V = logits.shape
+    if ws is None:
+        ws = workspace(ws_bytes("xt_cross_entropy_fanout_workspace_size", rows), logits.device)
+    call("xt_cross_entropy_fanout_fwd_bwd", ptr(logits), ptr(targets), float(c_lin), float(c_sq), ptr(upstream),
+         ptr(lse), ptr(loss), ptr(sums), ptr(grad), int(acc), rows, V, dt(logits), ptr(ws), ws.numel(), stream(s))
 
 
 def xt_cross_entropy_bwd(logits, targets, lse, upstream, dlogits, acc=0, s=None):
