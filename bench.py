@@ -61,7 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gpt12")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recompute: keep each layer's input only, redo its forward in the backward")
-    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy", "adamw", "fp8gemm"],
+    ap.add_argument("--kernel", choices=["attention", "gemm", "layernorm", "gelu", "cross_entropy", "adamw", "fp8gemm",
+                                         "ce_fanout"],
                     default=None,
                     help="time one kernel family at the workload's sizes instead of the step (for profiling)")
     ap.add_argument("--sweep", action="store_true",
@@ -69,11 +70,15 @@ def parse_args(argv=None):
                          "and of the 8192 x 128256 cross-entropy / fan-out case; one JSON line per case")
     ap.add_argument("--shape", default="8192,3072,768,0,1",
                     help="--kernel gemm: M,N,K,trans_a,trans_b (bf16 operands and output)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="--kernel ce_fanout: logits rows (default: the 8192 of the large-vocabulary case)")
     ap.add_argument("--pairing", type=int, choices=[0, 1, 2], default=0,
                     help="--kernel gemm: 0 model's choice, 1 single-CTA kernel only, 2 paired-CTA kernel")
     ap.add_argument("--schedule", type=int, choices=[0, 1, 2, 3, 4], default=0,
                     help="--kernel gemm: schedule override (0 model, 1 tiles, 2 K split, 3 stream-K, 4 lockstep)")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    # profiling runs of the step only: leave out the composed-attention pass and the oracle baseline
+    ap.add_argument("--step-only", action="store_true", help=argparse.SUPPRESS)
     # two of the 8 sequences: ≈ 11 s of float64 oracle work on 16 Arm cores
     ap.add_argument("--sample-seqs", type=int, default=2, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -216,6 +221,82 @@ def measured_peaks():
 REF_BUDGET_S = 150.0
 
 
+def run_reference_sweep(args):
+    """The oracle on the memory-bound op sweep and the large-vocabulary cross-entropy fan-out:
+    each op's forward + backward on a row sample of each shape (float64 NumPy, this process's
+    threads), reported as GB/s of the same algorithmic bytes the GPU sweep counts, scaled from
+    the sample's rows to the shape's.  One JSON line per case."""
+    import numpy as np
+    import synth
+    from oracle import dropout as OD
+    from oracle import ops as O
+    rng = np.random.default_rng(synth.SEED_SWEEP)
+    sample = 64   # rows timed per shape
+
+    def timed(fn, reps=3):
+        best = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    cores = os.environ.get("OPENBLAS_NUM_THREADS") or str(os.cpu_count())
+    for dtn, e in (("f32", 4), ("bf16", 2)):
+        for C in synth.SWEEP_COLS:
+            x = rng.standard_normal((sample, C))
+            d = rng.standard_normal((sample, C))
+            gam = 1.0 + 0.1 * rng.standard_normal(C)
+            bet = 0.1 * rng.standard_normal(C)
+            X = synth.SWEEP_ROWS * C * e
+
+            def rms():
+                y, ir = O.rms_norm_fwd(x, gam, 1e-5)
+                O.rms_norm_bwd(d, x, gam, ir)
+
+            def ln():
+                y, mu, rs = O.layernorm_fwd(x, gam, bet, 1e-5)
+                O.layernorm_bwd(d, x, gam, mu, rs)
+
+            def sm():
+                y = O.softmax_fwd(x)
+                O.softmax_bwd(d, y)
+
+            def silu():
+                O.silu_fwd(x)
+                O.silu_bwd(d, x)
+
+            def swiglu():
+                O.swiglu_fwd(x, d)
+                O.swiglu_bwd(d, x, d)
+
+            def drop():
+                OD.dropout_fwd(x.reshape(-1), 0.1, 0x5EED, dtype=dtn)
+                OD.dropout_bwd(d.reshape(-1), 0.1, 0x5EED, dtype=dtn)
+
+            for name, fn, nbytes in (("rms_norm", rms, 5 * X), ("layernorm", ln, 5 * X), ("softmax", sm, 5 * X),
+                                     ("silu", silu, 5 * X), ("swiglu", swiglu, 8 * X), ("dropout p=0.1", drop, 4 * X)):
+                t = timed(fn) * synth.SWEEP_ROWS / sample
+                print(json.dumps({"impl": "reference", "sweep": f"{name} fwd+bwd {dtn} {synth.SWEEP_ROWS}x{C}",
+                                  "seconds": round(t, 4), "bytes": int(nbytes), "gbs": round(nbytes / t / 1e9, 3),
+                                  "threads": cores, "sample_rows": sample}), flush=True)
+    cfg = synth.BIGVOCAB
+    R, V = cfg["rows"], cfg["V"]
+    rows = 16
+    x = rng.standard_normal((rows, V)) * cfg["std"]
+    t = rng.integers(0, V, size=rows)
+
+    def fan():
+        _, lse = O.cross_entropy_fwd(x, t)
+        ones = np.ones_like(x)
+        O.cross_entropy_bwd(x, t, lse, 1.0) + O.scale_bwd(ones, 0.5) + sum(O.mul_bwd(ones, x, x))
+    tt = timed(fan) * R / rows
+    nbytes = 6 * R * V
+    print(json.dumps({"impl": "reference", "sweep": f"fan-out CE + sum(0.5x) + sum(x*x) fwd+bwd {R}x{V}",
+                      "seconds": round(tt, 3), "bytes": int(nbytes), "gbs": round(nbytes / tt / 1e9, 3),
+                      "threads": cores, "sample_rows": rows}), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle, as it stands, on the host cores.  One untimed full-sequence sample sizes the
     per-step sample: a causal prefix of one sequence (a multiple of 128 positions, at least 128)
@@ -346,7 +427,7 @@ def run_ours(args, rank, world, local_rank):
     # The pages' attention, matmul(softmax(QKᵀ·scale), V) with the probabilities stored, as
     # separate causal-tile GEMMs around the row softmax (the fused kernel is the default path).
     composed = None
-    if cfg.get("attention", "auto") != "composed" and cfg["dtype"] == "bf16" and world == 1:
+    if cfg.get("attention", "auto") != "composed" and cfg["dtype"] == "bf16" and world == 1 and not args.step_only:
         nbc = NativeBlock(dict(cfg, attention="composed"), device=dev, training=True,
                           base_seed=synth.BASE_SEED_DROPOUT)
         nbc.load(synth.block_params(cfg))
@@ -426,7 +507,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks_profiled_pass": clocks_prof.summary(),
         "by_shape": gemm_by_shape(flops, gms, gshapes),
     }
-    cpu = cpu_baseline(args.workload, args.sample_seqs) if world == 1 else None
+    cpu = cpu_baseline(args.workload, args.sample_seqs) if world == 1 and not args.step_only else None
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -621,6 +702,22 @@ def run_kernel(args):
         print(json.dumps({"kernel": "fp8gemm", "shape": [M, N, K], "us": us, "tflops": tf, "peak_tflops": peak,
                           "frac": tf / peak, "peak_source": f"{src} bf16 burst x 4.5/2.25",
                           "quantize_us": qus, "quantize_gbs": M * K * (4 + 1) / qus / 1e3, "clocks": clocks}))
+    elif args.kernel == "ce_fanout":
+        # the fused fan-out L = CE(x) + 0.5·Σx + Σx∘x on 128256-wide bf16 logits ~N(0, 2), float32 gradient
+        cfg = synth.BIGVOCAB
+        R, V = (args.rows or cfg["rows"]), cfg["V"]
+        x = (torch.randn(R, V, generator=g) * cfg["std"]).to(torch.bfloat16).to(dev)
+        tg = torch.randint(0, V, (R,), generator=g, dtype=torch.int32).to(dev)
+        G = torch.empty(R, V, dtype=torch.float32, device=dev)
+        lse = torch.empty(R, dtype=torch.float32, device=dev)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        sums = torch.empty(3, dtype=torch.float32, device=dev)
+        fws = xt.workspace(xt.ws_bytes("xt_cross_entropy_fanout_workspace_size", R), dev)
+        us = timed(lambda: xt.xt_cross_entropy_fanout_fwd_bwd(x, tg, 0.5, 1.0, lse, loss, sums, G, ws=fws), n=20)
+        nbytes = 6 * R * V
+        peak = measured_peaks()[0].get("hbm_gbs", 6780.0)
+        print(json.dumps({"kernel": "ce_fanout", "rows": R, "V": V, "us": us, "gbs": nbytes / us / 1e3,
+                          "frac_of_measured_hbm": nbytes / us / 1e3 / peak, "clocks": clocks}))
     elif args.kernel == "cross_entropy":
         # the tied-logit loss as the stack runs it: bf16 logits [B·S, V], backward in place
         cfg = synth.BLOCK_CONFIGS[args.workload]
@@ -796,6 +893,9 @@ def run_sweep(args):
 
 def main():
     args = parse_args()
+    if args.sweep and args.impl == "reference":
+        run_reference_sweep(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
@@ -804,10 +904,15 @@ def main():
         return
     if args.oracle_sample:
         r, t, n = oracle_sample(args.workload, args.sample_seqs)
+        reps = 1
+        if t < 2.0:   # a small workload: repeat to about 10 s of CPU work, report the median
+            reps = max(1, min(2000, int(10.0 / max(t, 1e-4))))
+            r, t, n = oracle_sample(args.workload, args.sample_seqs, reps=reps)
         print(json.dumps({"value": r, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                           "cpu": cpu_model(),
                           "sample": f"{n} tokens ({args.sample_seqs} sequence(s)) of the same workload, all layers, "
-                                    f"float64 NumPy forward + backward, {t:.2f} s"}))
+                                    f"float64 NumPy forward + backward, {t:.3f} s"
+                                    + (f" (median of {reps} repetitions)" if reps > 1 else "")}))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

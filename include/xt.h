@@ -190,7 +190,12 @@ int xt_rms_norm_bwd(const void* d, const void* x, const void* gamma, const float
  *   - Limit: cols ≤ 8192 (else XT_ERR_UNSUPPORTED); the scratch is 128 × 8192 floats (4 MiB),
  *     held by every GPU that loads libxt until the process exits.
  *   - The first call on each device looks the scratch's device address up with that device
- *     current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     current (cudaGetSymbolAddress); make that first call before any stream capture.  The
+ *     address is kept for the life of the process: after cudaDeviceReset on a device (which
+ *     reloads libxt's device code there, possibly elsewhere) do not call this entry point on
+ *     that device again in the same process.
+ *   - At most 128 blocks walk the rows (the scratch holds one partial row per block), against
+ *     up to 4 per SM for xt_rms_norm_bwd: on long inputs it is correspondingly slower.
  *   - No cudaMalloc, cudaFree or allocating library routine is called.  Nothing in the
  *     scratch needs to start at zero: each call overwrites every partial row it reads.
  *   - All calls share the one array: calls that overlap on the GPU (several streams or host

@@ -8,3 +8,19 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300) and the built libxt.so")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(autouse=True)
+def _output_guards(request):
+    """After every GPU test: the guard bands around the outputs it allocated are intact."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    from tests import gpu_util
+    import torch
+    torch.cuda.synchronize()
+    bad = gpu_util.check_guards()
+    assert not bad, "; ".join(bad[:5])

@@ -1,6 +1,8 @@
 """Helpers for the GPU parity tests: moving synthetic inputs to the device and comparing
 device results with the oracle under the tolerances the tests use.
 
+Output buffers carry guard bands that are checked after every GPU test (see empty()).
+
 Tolerances:
   * fp32 row / elementwise ops: max_i |g − r| / max(|r_i|, m_i, 1e-6·max|r|) ≤ 1e-5, where
     m_i is the magnitude of the terms that the defining formula adds for element i (its
@@ -28,11 +30,42 @@ def host(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+# Guard bands (canaries): every output buffer the tests allocate with empty() is the middle of
+# a larger allocation whose 256 bytes before and after hold a fixed bit pattern; after each GPU
+# test the bands are read back, and a kernel that wrote outside its output fails the test
+# (check_guards, called from conftest.py).  256 bytes keep the output 16-byte aligned.
+GUARD_BYTES = 256
+_PATTERN = {torch.float32: (torch.int32, 0x7FC0DEAD), torch.bfloat16: (torch.int16, 0x7FDE)}
+_guards = []
+
+
 def empty(shape, dtype="f32", fill=None):
     td = torch.bfloat16 if dtype == "bf16" else torch.float32
-    if fill is None:
-        return torch.empty(shape, dtype=td, device=DEV)
-    return torch.full(shape, fill, dtype=td, device=DEV)
+    shape = tuple(shape) if isinstance(shape, (tuple, list)) else (shape,)
+    n = int(np.prod(shape)) if len(shape) else 1
+    g = GUARD_BYTES // torch.tensor([], dtype=td).element_size()
+    buf = torch.empty(n + 2 * g, dtype=td, device=DEV)
+    it, pat = _PATTERN[td]
+    bits = buf.view(it)
+    bits[:g] = pat
+    bits[g + n:] = pat
+    out = buf[g:g + n].view(shape)
+    if fill is not None:
+        out.fill_(fill)
+    _guards.append((buf, g, n, it, pat))
+    return out
+
+
+def check_guards():
+    """Bands around every empty() buffer since the last call that no longer hold the pattern."""
+    bad = []
+    for buf, g, n, it, pat in _guards:
+        bits = buf.view(it)
+        for name, band in (("before", bits[:g]), ("after", bits[g + n:])):
+            if not bool((band == pat).all()):
+                bad.append(f"{tuple(buf.shape)} {buf.dtype} output: guard band {name} overwritten")
+    _guards.clear()
+    return bad
 
 
 def _mag(r, mag):

@@ -10,7 +10,7 @@ import torch
 
 import synth
 from oracle import ops as O
-from tests.gpu_util import host, norm_err
+from tests.gpu_util import empty, host, norm_err
 
 pytestmark = pytest.mark.gpu
 
@@ -39,11 +39,11 @@ def run(B, S, H, causal, qkv, dO, with_lo=True):
     """Forward then backward; with_lo keeps O's bf16 rounding residual for the backward's D."""
     d = H * HD
     Q = bf16_dev(qkv)
-    o = torch.empty(B * S, d, dtype=torch.bfloat16, device="cuda")
-    o_lo = torch.empty(B * S, d, dtype=torch.bfloat16, device="cuda") if with_lo else None
-    lse = torch.empty(B, H, S, dtype=torch.float32, device="cuda")
+    o = empty((B * S, d), "bf16")
+    o_lo = empty((B * S, d), "bf16") if with_lo else None
+    lse = empty((B, H, S))
     xt.xt_attention_fwd(Q[:, :d], Q[:, d:2 * d], Q[:, 2 * d:], o, lse, B, S, H, HD, causal, o_lo=o_lo)
-    dqkv = torch.empty(B * S, 3 * d, dtype=torch.bfloat16, device="cuda")
+    dqkv = empty((B * S, 3 * d), "bf16")
     dOd = bf16_dev(dO)
     xt.xt_attention_bwd(Q[:, :d], Q[:, d:2 * d], Q[:, 2 * d:], o, dOd, lse, dqkv[:, :d], dqkv[:, d:2 * d],
                         dqkv[:, 2 * d:], B, S, H, HD, causal, o_lo=o_lo)

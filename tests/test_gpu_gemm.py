@@ -12,7 +12,7 @@ import torch
 
 import synth
 from oracle import ops as O
-from tests.gpu_util import check, dev, host, norm_err, sync
+from tests.gpu_util import check, dev, empty, host, norm_err, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ CASES = [(128, 64, 64), (200, 96, 72), (256, 256, 128), (1000, 776, 328), (64, 4
 def test_matmul_fwd(ab, c, ta, tb, M, N, K):
     A, B = stored(M, N, K, ta, tb, ab, 40)
     want = O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5
-    C = torch.empty((M, N), dtype=torch.float32 if c == "f32" else torch.bfloat16, device="cuda")
+    C = empty((M, N), c)
     d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_ab=xt.XT_BF16 if ab == "bf16" else xt.XT_F32,
                        dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, alpha=0.5)
     xt.xt_matmul_fwd(d, dev(A, ab), dev(B, ab), C); sync()
@@ -84,7 +84,7 @@ def test_matmul_batched_heads(ab, S, hd):
     dab = xt.XT_BF16 if ab == "bf16" else xt.XT_F32
     e = 2 if ab == "bf16" else 4
     sc = 1.0 / np.sqrt(hd)
-    scores = torch.empty((Bn, H, S, S), dtype=torch.float32, device="cuda")
+    scores = empty((Bn, H, S, S))
     d = xt.matmul_desc(S, S, hd, trans_a=0, trans_b=1, lda=3 * dm, ldb=3 * dm, ldc=S, batch_outer=Bn,
                        batch_inner=H, dtype_ab=dab, dtype_c=xt.XT_F32, alpha=sc,
                        strides=(S * 3 * dm, hd, S * 3 * dm, hd, H * S * S, S * S))
@@ -111,7 +111,7 @@ def test_matmul_causal_modes(S):
     q = synth.normal((S, hd), 46, dtype="bf16")
     k = synth.normal((S, hd), 47, dtype="bf16")
     full = q @ k.T
-    C = torch.full((S, S), float("nan"), dtype=torch.float32, device="cuda")
+    C = empty((S, S), fill=float("nan"))
     d = xt.matmul_desc(S, S, hd, trans_b=1, causal=1)
     xt.xt_matmul_fwd(d, dev(q, "bf16"), dev(k, "bf16"), C); sync()
     g = host(C)
@@ -122,13 +122,13 @@ def test_matmul_causal_modes(S):
     P = np.where(c_idx <= s_idx, synth.normal((S, S), 48, dtype="bf16"), 0.0)
     Pd = dev(np.where(need, P, np.nan), "bf16")   # beyond the extent: never read
     v = synth.normal((S, hd), 49, dtype="bf16")
-    O2 = torch.empty((S, hd), dtype=torch.float32, device="cuda")
+    O2 = empty((S, hd))
     d2 = xt.matmul_desc(S, hd, S, causal=2)
     xt.xt_matmul_fwd(d2, Pd, dev(v, "bf16"), O2); sync()
     assert norm_err(host(O2), P @ v) <= 1e-5
     # mode 3: dV = Pᵀ dO with P stored [S_q, S_k] read transposed
     dO = synth.normal((S, hd), 50, dtype="bf16")
-    dV = torch.empty((S, hd), dtype=torch.float32, device="cuda")
+    dV = empty((S, hd))
     d3 = xt.matmul_desc(S, hd, S, trans_a=1, causal=3)
     xt.xt_matmul_fwd(d3, Pd, dev(dO, "bf16"), dV); sync()
     assert norm_err(host(dV), P.T @ dO) <= 1e-5
@@ -145,7 +145,7 @@ def test_matmul_bwd(ab, ta, tb):
     dA_r, dB_r = op(dA_r, ta) * 2.0, op(dB_r, tb) * 2.0   # back into the stored layouts, alpha = 2
     dab = xt.XT_BF16 if ab == "bf16" else xt.XT_F32
     d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_ab=dab, alpha=2.0)
-    dA = torch.empty(A.shape, dtype=torch.float32, device="cuda")
+    dA = empty(A.shape)
     dB = torch.ones(B.shape, dtype=torch.float32, device="cuda")
     xt.xt_matmul_bwd(d, dev(A, ab), dev(B, ab), dev(dC, ab), dA, dB, 0, 1); sync()
     assert norm_err(host(dA), dA_r) <= bound(ab, "f32")
@@ -158,7 +158,7 @@ def test_matmul_large_sampled():
     for (M, N, K, tb) in [(8192, 2304, 768, 0), (8192, 50304, 768, 1)]:
         A = synth.normal((M, K), 54, dtype="bf16")
         B = synth.normal((N, K) if tb else (K, N), 55, std=0.02, dtype="bf16")
-        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        C = empty((M, N), "bf16")
         d = xt.matmul_desc(M, N, K, trans_b=tb, dtype_c=xt.XT_BF16)
         xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), C); sync()
         rows = np.random.default_rng(0).choice(M, 24, replace=False)
@@ -268,7 +268,7 @@ def test_matmul_stream_k_batched(form, schedule):
     Bo, Bi, M, N, K = 2, 3, 200, 96, 2048
     A = synth.normal((Bo, Bi, M, K), 63, dtype="bf16")
     B = synth.normal((Bo, Bi, K, N), 64, dtype="bf16")
-    Cd = torch.empty((Bo, Bi, M, N), dtype=torch.float32, device="cuda")
+    Cd = empty((Bo, Bi, M, N))
     d = xt.matmul_desc(M, N, K, batch_outer=Bo, batch_inner=Bi,
                        strides=(Bi * M * K, M * K, Bi * K * N, K * N, Bi * M * N, M * N))
     codes = schedules_of(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), Cd))
@@ -284,7 +284,7 @@ def test_matmul_model_schedule_full_size(M, N, K, tb):
     of those rows."""
     A = synth.normal((M, K), 65, std=0.5, dtype="bf16")
     B = synth.normal((N, K) if tb else (K, N), 66, std=0.02, dtype="bf16")
-    Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Cm = empty((M, N), "bf16")
     d = xt.matmul_desc(M, N, K, trans_b=tb, dtype_c=xt.XT_BF16)
     Ad, Bd = dev(A, "bf16"), dev(B, "bf16")
     codes = schedules_of(lambda: xt.xt_matmul_fwd(d, Ad, Bd, Cm))
@@ -313,7 +313,7 @@ def test_matmul_gelu_fwd(ta, tb, M, N, K):
     A, B = stored(M, N, K, ta, tb, "bf16", 45)
     want_c = O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5
     Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Y = empty((M, N), "bf16")
     d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16, alpha=0.5)
     xt.xt_matmul_gelu_fwd(d, dev(A, "bf16"), dev(B, "bf16"), Cm, Y); sync()
     assert xt.device_errors() == 0

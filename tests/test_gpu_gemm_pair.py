@@ -11,7 +11,7 @@ import torch
 
 import synth
 from oracle import ops as O
-from tests.gpu_util import dev, host, norm_err, sync
+from tests.gpu_util import dev, empty, host, norm_err, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +58,7 @@ def test_pair_fwd(c, ta, tb, M, N, K, paired):
     A = synth.normal((K, M) if ta else (M, K), 140, dtype="bf16")
     B = synth.normal((N, K) if tb else (K, N), 141, dtype="bf16")
     want = O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5
-    C = torch.empty((M, N), dtype=torch.float32 if c == "f32" else torch.bfloat16, device="cuda")
+    C = empty((M, N), c)
     d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, alpha=0.5)
     Ad, Bd = dev(A, "bf16"), dev(B, "bf16")
     rec = records(lambda: xt.xt_matmul_fwd(d, Ad, Bd, C))
@@ -128,7 +128,7 @@ def test_pair_full_size_sampled(M, N, K, ta, tb, paired):
     CTAs' halves of a 256-row tile and the last row) against the oracle's product of those rows."""
     A = synth.normal((K, M) if ta else (M, K), 148, std=0.5, dtype="bf16")
     B = synth.normal((N, K) if tb else (K, N), 149, std=0.02, dtype="bf16")
-    Cm = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Cm = empty((M, N), "bf16")
     d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16)
     Ad, Bd = dev(A, "bf16"), dev(B, "bf16")
     rec = records(lambda: xt.xt_matmul_fwd(d, Ad, Bd, Cm))
@@ -152,7 +152,7 @@ def test_pair_matches_single():
     try:
         for mode in (1, 2):
             xt.gemm_set_pairing(mode)
-            C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            C = empty((M, N))
             rec = records(lambda: xt.xt_matmul_fwd(d, Ad, Bd, C))
             assert (rec[0][0] > 1000) == (mode == 2), rec
             outs[mode] = host(C)
@@ -177,7 +177,7 @@ def test_pair_tile_192(ta, M, N, K, paired):
     try:
         A = synth.normal((K, M) if ta else (M, K), 152, dtype="bf16")
         B = synth.normal((N, K), 153, dtype="bf16")   # [N, K]: K-major
-        C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        C = empty((M, N))
         d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=1)
         rec = records(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), C))
         assert rec[0][0] == 1192, rec
