@@ -82,8 +82,31 @@ template <EwOp OP> struct EwIO {
   static constexpr bool TWO_OUT = OP == EW_COPY2 || OP == EW_MUL_BWD;
 };
 
+// Eight elements as loaded: one 16-byte word of bf16, two of fp32; unpacked per element.
+template <typename T> struct Raw8;
+template <> struct Raw8<bf16> {
+  uint4 q;
+  __device__ __forceinline__ void load(const bf16* p) { q = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ float get(int j) const {
+    const uint32_t w = j < 2 ? q.x : j < 4 ? q.y : j < 6 ? q.z : q.w;
+    return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = reinterpret_cast<const float4*>(p)[0];
+    b = reinterpret_cast<const float4*>(p)[1];
+  }
+  __device__ __forceinline__ float get(int j) const {
+    const float4& f = j < 4 ? a : b;
+    const int k = j & 3;
+    return k == 0 ? f.x : k == 1 ? f.y : k == 2 ? f.z : f.w;
+  }
+};
+
 template <EwOp OP, typename TI, typename TO, bool VEC>
-__global__ void __launch_bounds__(256) ew_kernel(EwArgs g) {
+__global__ void __launch_bounds__(256, 4) ew_kernel(EwArgs g) {
   pdl_begin();
   using IO = EwIO<OP>;
   const TI* a = static_cast<const TI*>(g.a);
@@ -97,6 +120,57 @@ __global__ void __launch_bounds__(256) ew_kernel(EwArgs g) {
   int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if constexpr (VEC) {
     const int64_t nv = g.n / 8;
+    // The plain streaming ops take U vectors per thread per step, all loads issued before any is
+    // used, so an SM keeps U times the bytes in flight; GELU and dropout (bound by their
+    // arithmetic: erfc, the per-element hash) keep one, as their registers set their occupancy.
+    constexpr int U = (OP == EW_GELU || OP == EW_GELU_BWD || OP == EW_DROPOUT || OP == EW_DROPOUT_ADD) ? 1
+                      : OP == EW_MUL_BWD ? (sizeof(TI) == 2 ? 2 : 1) : 16 / int(sizeof(TI)) / 2;
+    if constexpr (U > 1) {
+      for (int64_t v0 = t; v0 < nv; v0 += U * stride) {
+        // raw 16-byte words: the loads of all U vectors are in flight before any is unpacked
+        Raw8<TI> ra[U], rb[U], rc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t v = v0 + int64_t(u) * stride;
+          if (v < nv) {
+            if constexpr (IO::A) ra[u].load(a + v * 8);
+            if constexpr (IO::B) rb[u].load(b + v * 8);
+            if constexpr (IO::C) rc[u].load(c + v * 8);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t v = v0 + int64_t(u) * stride;
+          if (v >= nv) break;
+          const int64_t i0 = v * 8;
+          float r0[8], r1[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ew_apply<OP>(IO::A ? ra[u].get(j) : 0.f, IO::B ? rb[u].get(j) : 0.f, IO::C ? rc[u].get(j) : 0.f,
+                         uint64_t(i0 + j), g, r0[j], r1[j]);
+          if (o0) {
+            if (acc0) {
+              float old[8];
+              V8<TO>::load(o0 + i0, old);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) r0[j] += old[j];
+            }
+            V8<TO>::store(o0 + i0, r0);
+          }
+          if constexpr (IO::TWO_OUT) {
+            if (o1) {
+              if (acc1) {
+                float old[8];
+                V8<TO>::load(o1 + i0, old);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) r1[j] += old[j];
+              }
+              V8<TO>::store(o1 + i0, r1);
+            }
+          }
+        }
+      }
+    } else
     for (int64_t v = t; v < nv; v += stride) {
       const int64_t i0 = v * 8;
       float va[8] = {}, vb[8] = {}, vc[8] = {}, r0[8], r1[8];
