@@ -626,8 +626,8 @@ def run_kernel(args):
                                                    dqkv[:, 2 * d:], B, S, H, hd, 1, o_lo=o_lo, ws=ws))
         fl = 2 * 2 * S * S * hd / 2 * B * H   # QKᵀ and PV over the causal half
         print(json.dumps({"kernel": "attention", "workload": f"B{B} S{S} H{H}x{hd} causal bf16",
-                          "fwd_us": fwd_us, "bwd_us": bwd_us, "fwd_tflops": fl / fwd_us / 1e6,
-                          "bwd_tflops": 2 * fl / bwd_us / 1e6, "clocks": clocks}))
+                          "fwd_us": fwd_us, "bwd_us": bwd_us,
+                          "fwd_tflops": fl / fwd_us / 1e6, "bwd_tflops": 2 * fl / bwd_us / 1e6, "clocks": clocks}))
     elif args.kernel == "layernorm":
         # as the stack launches it: bf16 rows, float32 residual gradient accumulated, float32 dγ / dβ
         cfg = synth.BLOCK_CONFIGS[args.workload]
@@ -759,7 +759,7 @@ def run_sweep(args):
     bf16 (x and the upstream gradient ~N(0, 1); RoPE with head_dim 128 and position = row mod 1024; dropout at
     p ∈ {0, 0.1, 0.5}), then cross-entropy and the three-branch fan-out on 8192 × 128256 bf16 logits ~N(0, 2).
     Each case: 3 untimed launches, then 30 launches each timed alone with its own CUDA events after 1 GiB has been
-    written (so no input is left in the 129 MB L2); the median is reported.  GB/s = algorithmic bytes / time,
+    read (so no input, and no dirty line, is left in the 129 MB L2); the median is reported.  GB/s = algorithmic bytes / time,
     `frac` of the measured HBM copy bandwidth."""
     import torch
 
@@ -774,7 +774,8 @@ def run_sweep(args):
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     g = torch.Generator().manual_seed(synth.SEED_SWEEP)
 
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.float32, device=dev)   # 1 GiB
+    flush = torch.zeros(256 * 1024 * 1024, dtype=torch.float32, device=dev)   # 1 GiB
+    flush_acc = torch.zeros((), dtype=torch.float32, device=dev)
 
     def timed(fn, n=30):
         for _ in range(3):
@@ -782,7 +783,9 @@ def run_sweep(args):
         torch.cuda.synchronize(dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         for e0, e1 in evs:
-            flush.zero_()      # L2 flushed; the launch below is enqueued while this write runs
+            # L2 flushed by a 1 GiB read: the lines left behind are clean, so the timed launch pays
+            # for no write-back of the flush itself (a 1 GiB write would leave up to 129 MB dirty)
+            torch.sum(flush, 0, out=flush_acc)
             e0.record()
             fn()
             e1.record()

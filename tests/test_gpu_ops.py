@@ -450,7 +450,7 @@ def test_swiglu(dtype, rows, F):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("rows,cols", [(37, 768), (8192, 2048), (5, 13)])
+@pytest.mark.parametrize("rows,cols", [(37, 768), (8192, 2048), (5, 13), (1000, 520), (130, 1001)])
 def test_add_bias(dtype, rows, cols):
     x = inputs((rows, cols), 30, dtype)
     b = inputs((cols,), 31, dtype, std=0.1)
@@ -463,6 +463,14 @@ def test_add_bias(dtype, rows, cols):
     rdx, rdb = O.add_bias_bwd(d)
     check(host(DX), rdx, dtype, "add_bias dx")
     check_sum(host(DB), rdb, np.abs(d).sum(0), "f32", "add_bias dbias")
+    # accumulate forms: dx += d into a buffer holding x, dbias += Σ into one holding b; dbias alone
+    DXa, DBa = dev(x, dtype), dev(b, "f32")
+    xt.xt_add_bias_bwd(dev(d, dtype), DXa, DBa, acc_dx=1, acc_dbias=1); sync()
+    check(host(DXa), O.add_fwd(x, d), dtype, "add_bias dx accumulated")
+    check_sum(host(DBa), rdb + b, np.abs(d).sum(0) + np.abs(b), "f32", "add_bias dbias accumulated")
+    DB1 = empty((cols,), "f32")
+    xt.xt_add_bias_bwd(dev(d, dtype), None, DB1); sync()
+    assert np.array_equal(host(DB1), host(DB)), "dbias without dx differs"
 
 
 @pytest.mark.parametrize("norm", ["rms", "ln"])

@@ -1246,7 +1246,7 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   {
     const int64_t threads = int64_t(B) * S * H * 8;
     int64_t blocks = ceil_div(threads, 256);
-    const int64_t cap = int64_t(num_sms()) * 8;
+    const int64_t cap = int64_t(num_sms()) * 32;  // one (t, h) row per 8 threads up to 1.2 M rows
     if (blocks > cap) blocks = cap;
     if (o_lo && !aligned16(o_lo)) return fail(XT_ERR_ALIGNMENT, "xt_attention_bwd: o_lo must be 16-byte aligned");
     launch(attn_delta_kernel, int(blocks), 256, 0, s, static_cast<const bf16*>(o), static_cast<const bf16*>(o_lo),

@@ -2,6 +2,8 @@
 // warp / row-group reductions, device facts.
 #pragma once
 
+#include <cmath>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -224,6 +226,27 @@ __device__ __forceinline__ bool dropout_keep(uint64_t seed, uint64_t i, float p)
   z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
   const float u = static_cast<float>(static_cast<uint32_t>(z >> 40)) * 0x1.0p-24f;
   return u >= p;
+}
+
+// The same decision as an integer test: with k = z >> 40 (an integer below 2²⁴, so k·2⁻²⁴ and
+// p·2²⁴ are exact in float), k·2⁻²⁴ ≥ p ⟺ k ≥ ⌈p·2²⁴⌉ ⟺ z ≥ ⌈p·2²⁴⌉·2⁴⁰ — the threshold
+// dropout_threshold(p).  Eight consecutive counters i0 .. i0 + 7 share one multiply: the
+// counter's i·γ is i0·γ + j·γ (mod 2⁶⁴).
+inline uint64_t dropout_threshold(float p) {
+  return static_cast<uint64_t>(std::ceil(static_cast<double>(p) * 16777216.0)) << 40;
+}
+__device__ __forceinline__ uint32_t dropout_keep8(uint64_t seed, uint64_t i0, uint64_t thr) {
+  constexpr uint64_t kG = 0x9E3779B97F4A7C15ull;
+  const uint64_t base = i0 * kG;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint64_t z = (seed ^ (base + uint64_t(j) * kG)) + kG;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    bits |= (z >= thr ? 1u : 0u) << j;
+  }
+  return bits;
 }
 
 // Φ(x) = ½·erfc(−x/√2) (no cancellation for x ≪ 0, unlike ½(1 + erf(x/√2))), with erfc from the

@@ -34,6 +34,7 @@ struct EwArgs {
   float p;
   float dscale;
   uint64_t seed;
+  uint64_t thr;  // dropout_threshold(p)
   int acc0, acc1;
   const float* scalar;
 };
@@ -180,6 +181,13 @@ __global__ void __launch_bounds__(256, 4) ew_kernel(EwArgs g) {
       if constexpr (OP == EW_GELU) {
 #pragma unroll
         for (int j = 0; j < 8; j += 2) gelu_pair<0>(va[j], va[j + 1], 0.f, 0.f, r0[j], r0[j + 1]);
+      } else if constexpr (OP == EW_DROPOUT || OP == EW_DROPOUT_ADD) {
+        const uint32_t keep = dropout_keep8(g.seed, uint64_t(i0), g.thr);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if constexpr (OP == EW_DROPOUT) r0[j] = ((keep >> j) & 1u) ? va[j] * g.dscale : 0.f;
+          else r0[j] = va[j] + (((keep >> j) & 1u) ? vb[j] * g.dscale : 0.f);
+        }
       } else if constexpr (OP == EW_GELU_BWD) {
 #pragma unroll
         for (int j = 0; j < 8; j += 2) gelu_pair<1>(vb[j], vb[j + 1], va[j], va[j + 1], r0[j], r0[j + 1]);
@@ -569,7 +577,7 @@ int xt_dropout_fwd(const void* x, void* y, int64_t n, float p, uint64_t seed, in
     return XT_OK;
   }
   EwArgs g = ew_args(x, nullptr, nullptr, y, nullptr, n);
-  g.p = p; g.dscale = dropout_scale(p); g.seed = seed;
+  g.p = p; g.dscale = dropout_scale(p); g.seed = seed; g.thr = dropout_threshold(p);
   return ew_dispatch<EW_DROPOUT>(dt, dt, g, stream, "xt_dropout_fwd");
 }
 
@@ -586,7 +594,7 @@ int xt_dropout_bwd(const void* d, void* dx, int64_t n, float p, uint64_t seed, i
     g.alpha = 1.f;
     return ew_dispatch<EW_SCALE>(dt, dt, g, stream, "xt_dropout_bwd");
   }
-  g.p = p; g.dscale = dropout_scale(p); g.seed = seed;
+  g.p = p; g.dscale = dropout_scale(p); g.seed = seed; g.thr = dropout_threshold(p);
   return ew_dispatch<EW_DROPOUT>(dt, dt, g, stream, "xt_dropout_bwd");
 }
 
@@ -603,7 +611,7 @@ int xt_dropout_bwd_ex(const void* d, int dt_d, void* dx, int dt_dx, int64_t n, f
     g.alpha = 1.f;
     return ew_dispatch<EW_SCALE>(dt_d, dt_dx, g, stream, "xt_dropout_bwd_ex");
   }
-  g.p = p; g.dscale = dropout_scale(p); g.seed = seed;
+  g.p = p; g.dscale = dropout_scale(p); g.seed = seed; g.thr = dropout_threshold(p);
   return ew_dispatch<EW_DROPOUT>(dt_d, dt_dx, g, stream, "xt_dropout_bwd_ex");
 }
 
@@ -615,7 +623,7 @@ int xt_dropout_add_fwd(const void* h, const void* a, void* out, int64_t n, float
   XT_REQUIRE(n == 0 || (h && a && out), "xt_dropout_add_fwd: NULL pointer");
   EwArgs g = ew_args(h, a, nullptr, out, nullptr, n);
   if (p == 0.f || !training) return ew_dispatch<EW_ADD>(dt, dt, g, stream, "xt_dropout_add_fwd");
-  g.p = p; g.dscale = dropout_scale(p); g.seed = seed;
+  g.p = p; g.dscale = dropout_scale(p); g.seed = seed; g.thr = dropout_threshold(p);
   return ew_dispatch<EW_DROPOUT_ADD>(dt, dt, g, stream, "xt_dropout_add_fwd");
 }
 

@@ -635,26 +635,66 @@ static int finalize(const float* part, int nb, int64_t cols, void* out, int dt, 
   return check_launch("column-sum finalize");
 }
 
-constexpr int kColChunkRows = 16;  // rows per partial in the plain column sum
+constexpr int kColChunkRows = 64;  // rows per partial in the plain column sum
 
 static int colsum_chunks(int64_t rows) { return int(ceil_div(rows, kColChunkRows)); }
 
-// Plain column sum of d [rows, cols] into per-chunk partials (and an optional copy dx = d).
-template <typename T>
-__global__ void colsum_stage1(const T* __restrict__ d, T* dx, int acc_dx, float* __restrict__ part, int64_t rows,
-                              int64_t cols) {
+// Plain column sum of d [rows, cols] into one partial row per 64-row chunk (and an optional copy
+// dx = d, or dx += d).  A block of 8 warps owns a slab of 32 vectors of VW columns (512 bytes of
+// a row per warp access) and one chunk: warp w sums rows w, w + 8, ... of the chunk, four rows in
+// flight per thread, and the eight warp sums are added in warp order, so the partials do not
+// depend on timing.  VW = 1 is the form for ragged or misaligned rows.
+template <typename T, int VW>
+__global__ void __launch_bounds__(256) colsum_stage1(const T* __restrict__ d, T* dx, int acc_dx,
+                                                     float* __restrict__ part, int64_t rows, int64_t cols) {
   pdl_begin();
-  const int64_t chunk = blockIdx.y;
-  const int64_t r_begin = chunk * kColChunkRows;
-  const int64_t r_end = r_begin + kColChunkRows < rows ? r_begin + kColChunkRows : rows;
-  for (int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < cols; c += int64_t(gridDim.x) * blockDim.x) {
-    float s = 0.f;
-    for (int64_t r = r_begin; r < r_end; ++r) {
-      const float v = to_f(d[r * cols + c]);
-      s += v;
-      if (dx) dx[r * cols + c] = from_f<T>(acc_dx ? to_f(dx[r * cols + c]) + v : v);
+  __shared__ float red[8][32 * VW];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c = (int64_t(blockIdx.x) * 32 + lane) * VW;
+  const int64_t r0 = int64_t(blockIdx.y) * kColChunkRows;
+  const int64_t r1 = r0 + kColChunkRows < rows ? r0 + kColChunkRows : rows;
+  float s[VW];
+#pragma unroll
+  for (int e = 0; e < VW; ++e) s[e] = 0.f;
+  if (c < cols) {
+    auto row = [&](int64_t r, const float (&v)[VW]) {
+      if (dx) {
+        if (acc_dx) {
+          float o[VW];
+          load_vec<T, VW>(dx + r * cols + c, o);
+#pragma unroll
+          for (int e = 0; e < VW; ++e) o[e] += v[e];
+          store_vec<T, VW>(dx + r * cols + c, o);
+        } else {
+          store_vec<T, VW>(dx + r * cols + c, v);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < VW; ++e) s[e] += v[e];
+    };
+    int64_t r = r0 + warp;
+    for (; r + 24 < r1; r += 32) {
+      float v[4][VW];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) load_vec<T, VW>(d + (r + 8 * k) * cols + c, v[k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) row(r + 8 * k, v[k]);
     }
-    part[chunk * cols + c] = s;
+    for (; r < r1; r += 8) {
+      float v[VW];
+      load_vec<T, VW>(d + r * cols + c, v);
+      row(r, v);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < VW; ++e) red[warp][lane * VW + e] = s[e];
+  __syncthreads();
+  for (int t = threadIdx.x; t < 32 * VW; t += blockDim.x) {
+    const int64_t cc = int64_t(blockIdx.x) * 32 * VW + t;
+    float a = red[0][t];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) a += red[w][t];
+    if (cc < cols) part[int64_t(blockIdx.y) * cols + cc] = a;
   }
 }
 
@@ -1554,12 +1594,24 @@ int xt_add_bias_bwd(const void* d, void* dx, void* dbias, int64_t rows, int64_t 
   }
   const int nch = colsum_chunks(rows);
   float* part = static_cast<float*>(ws);
-  dim3 grid(unsigned(ceil_div(cols, 256) < 65535 ? ceil_div(cols, 256) : 65535), unsigned(nch));
   if (nch > 65535) return fail(XT_ERR_UNSUPPORTED, "xt_add_bias_bwd: too many rows");
-  if (dt == XT_F32)
-    launch(colsum_stage1<float>, grid, 256, 0, s, static_cast<const float*>(d), static_cast<float*>(dx), acc_dx, part, rows, cols);
-  else
-    launch(colsum_stage1<bf16>, grid, 256, 0, s, static_cast<const bf16*>(d), static_cast<bf16*>(dx), acc_dx, part, rows, cols);
+  const int vw = dt == XT_F32 ? 4 : 8;
+  const bool vec = cols % vw == 0 && aligned16(d) && (!dx || aligned16(dx));
+  const int64_t slab = 32 * (vec ? vw : 1);
+  const int64_t slabs = ceil_div(cols, slab);
+  if (slabs > INT32_MAX) return fail(XT_ERR_UNSUPPORTED, "xt_add_bias_bwd: too many columns");
+  const dim3 grid{unsigned(slabs), unsigned(nch)};
+  if (dt == XT_F32) {
+    auto D = static_cast<const float*>(d);
+    auto DX = static_cast<float*>(dx);
+    if (vec) launch(colsum_stage1<float, 4>, grid, 256, 0, s, D, DX, acc_dx, part, rows, cols);
+    else launch(colsum_stage1<float, 1>, grid, 256, 0, s, D, DX, acc_dx, part, rows, cols);
+  } else {
+    auto D = static_cast<const bf16*>(d);
+    auto DX = static_cast<bf16*>(dx);
+    if (vec) launch(colsum_stage1<bf16, 8>, grid, 256, 0, s, D, DX, acc_dx, part, rows, cols);
+    else launch(colsum_stage1<bf16, 1>, grid, 256, 0, s, D, DX, acc_dx, part, rows, cols);
+  }
   XT_TRY(check_launch("xt_add_bias_bwd"));
   return finalize(part, nch, cols, dbias, dt_bias, acc_dbias, s);
 }
