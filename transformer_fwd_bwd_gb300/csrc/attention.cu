@@ -2,17 +2,19 @@
 // the causal mask, O = P V ([AE] § Attention 用组合 gives the composition; this computes the
 // same result tile by tile, so the S × S probabilities never reach global memory).
 //
-// Forward (one CTA per SM, persistent over 128-query tiles, heaviest first):
-//   warp 0      TMA producer: Q tile once per work item, K and V tiles through 3-slot rings;
-//   warp 1      TMEM owner and MMA issuer: S_j = Q K_jᵀ into one of two TMEM score buffers
-//               (so S_{j+1} is computed while the softmax warps read S_j), then O += P_j V_j
-//               into a TMEM accumulator;
-//   warps 2..5  one query row per thread (TMEM lane): load the score row, mask, running max,
-//               exp2, running sum, write P_j as bf16 into shared memory in the 128-byte-swizzled
-//               K-major layout the MMA reads; rescale O in TMEM when the running max grows by
-//               more than 2^8 (otherwise the stale max is kept: O and the sum share it, so O / l
-//               is exact either way); at the end O / l goes out through a TMA store and the row's
-//               natural-log normaliser lse = log Σ exp(scores) is saved for the backward.
+// Forward (one CTA per SM, persistent, two independent streams of 128-query tiles, heaviest
+// first; each stream has its own warps, buffers and work items, so one stream's MMA round trips
+// overlap the other's softmax):
+//   warps 0 / 2  TMA producer: Q tile once per work item, K and V tiles through 2-slot rings;
+//   warps 1 / 3  MMA issuer (warp 1 also owns TMEM): S_j = Q K_jᵀ into the stream's TMEM score
+//                buffer (issued once the softmax warps have loaded S_{j−1}), then O += P_j V_j
+//                into the stream's TMEM accumulator;
+//   warps 4..7 / 8..11  one query row per thread (TMEM lane): load the score row, mask, running
+//                max, exp2, running sum, write P_j as bf16 into shared memory in the 128-byte-
+//                swizzled K-major layout the MMA reads; rescale O in TMEM when the running max
+//                grows by more than 2^8 (otherwise the stale max is kept: O and the sum share it,
+//                so O / l is exact either way); at the end O / l goes out through a TMA store and
+//                the row's natural-log normaliser lse = log Σ exp(scores) is saved for the backward.
 //
 // Backward (deterministic, no atomics): D = rowsum(dO ∘ O); then one kernel per 128-key tile
 // that recomputes Pᵀ = exp(K Qᵀ·α − lse) and dPᵀ = V dOᵀ and accumulates dV = Pᵀ dO and
@@ -34,14 +36,13 @@ using namespace gemm;
 
 constexpr int HD = 64;                     // head dimension the kernels are built for
 constexpr int BT = 128;                    // query / key tile
-constexpr int kThreads = 192;
 // Backward kernels: warp 0 TMA, warp 1 MMA, warps 2..9 rows — two warps per TMEM lane quadrant,
 // each owning 64 of a tile's 128 columns (the backward's P and dS are elementwise, so the halves
 // never need each other's values).
 constexpr int kThreadsBwd = 320;
 constexpr int TILE = BT * 128;             // one 128-row × 64-element bf16 tile: 16 KB
 constexpr int PT = 2 * TILE;               // 128 × 128 bf16 operand: two 64-wide K chunks
-constexpr int RING = 3;                    // K / V slots
+constexpr int RING = 3;                    // K / V slots of the query-tile backward kernel
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.f;            // log2 growth of the running max that forces a rescale
@@ -112,59 +113,61 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 
 // ------------------------------------------------------------------------------ forward
 
+
+// setmaxnreg: a warp group gives registers back to the pool or takes them from it (all four
+// warps of the group execute it).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// The forward with two independent query-tile streams per CTA: each stream has its own TMA
+// producer (warps 0 / 2), MMA issuer (warps 1 / 3), four softmax warps (4–7 / 8–11), TMEM score
+// buffer and O accumulator, Q tile, two-slot K / V rings and P tile, and its own work items
+// (virtual CTA 2·blockIdx + stream of a grid twice as wide).  A stream's softmax warps wait for
+// their scores while the other stream's compute, so the per-tile MMA round trips of one stream
+// overlap the other's exp and P stores.  With one score buffer per stream, S_{j+1} is computed
+// as soon as the softmax warps have loaded S_j.  The epilogue stages O (and O_lo) in the warp's
+// own rows of the P tile once the last P V is done.
+constexpr int kThreadsFwd = 384;
+constexpr int KV_SLOTS = 2;
+constexpr uint32_t kFwdRegsCtl = 72, kFwdRegsRows = 216;  // 128·72 + 256·216 = 384·168
 struct FwdSmem {
   static constexpr int Q = 0;
   static constexpr int K = Q + TILE;
-  static constexpr int V = K + RING * TILE;
-  static constexpr int P = V + RING * TILE;
-  static constexpr int STAGE = P + 2 * PT;           // O and O_lo staging: 4 warps × 2 × 32 rows × 128 B
-  static constexpr int BARS = STAGE + 8 * 4096;
-  static constexpr int BYTES = 1024 + BARS + 256;
+  static constexpr int V = K + KV_SLOTS * TILE;
+  static constexpr int P = V + KV_SLOTS * TILE;
+  static constexpr int STREAM = P + PT;           // 112 KB per stream
+  static constexpr int BARS = 2 * STREAM;
+  static constexpr int BYTES = 1024 + BARS + 512;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFwd, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const __grid_constant__ CUtensorMap tmOlo, const FwdParams p) {
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const __grid_constant__ CUtensorMap tmOlo, const FwdParams p) {
   pdl_begin();
   constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_PV = instr_desc_bf16(128, HD, false, true);
-  constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), O [256,320)
+  constexpr uint32_t TCOLS = 512;  // stream s: S [256 s, 256 s + 128), O [256 s + 128, 256 s + 192)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
+  // per stream, 16 slots: q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full,
+  // s_free, p_full, p_free, mma_done
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + FwdSmem::BARS);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = k_full + RING;
-  uint64_t* v_full = k_empty + RING;
-  uint64_t* v_empty = v_full + RING;
-  uint64_t* s_full = v_empty + RING;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* p_free = p_full + 2;
-  uint64_t* mma_done = p_free + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(q_full), 1);
-    mbar_init(smem_u32(q_empty), 1);
-    for (int s = 0; s < RING; ++s) {
-      mbar_init(smem_u32(&k_full[s]), 1);
-      mbar_init(smem_u32(&k_empty[s]), 1);
-      mbar_init(smem_u32(&v_full[s]), 1);
-      mbar_init(smem_u32(&v_empty[s]), 1);
+    for (int st = 0; st < 2; ++st) {
+      uint64_t* b = bars + 16 * st;
+      for (int i = 0; i < 15; ++i) mbar_init(smem_u32(&b[i]), (i == 11 || i == 12) ? 4 : 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&s_full[b]), 1);
-      mbar_init(smem_u32(&s_free[b]), 4);
-      mbar_init(smem_u32(&p_full[b]), 4);
-      mbar_init(smem_u32(&p_free[b]), 1);
-    }
-    mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -182,72 +185,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const uint32_t tO = tbase + 256;
 
   auto give_up = [&]() {
     *abort_flag = 1;
     flag_error(p.flag, XT_DEVERR_TIMEOUT);
   };
+  const int VG = 2 * int(gridDim.x);
+  // work item of round r for virtual CTA vc (rounds alternate direction, longest items first)
+  auto vitem = [&](int r, int vc) { return r * VG + ((r & 1) ? VG - 1 - vc : vc); };
 
-  if (warp == 0) {
-    if (lane == 0) {
+  const int wg = warp >> 2;
+  if (wg == 0) {
+    regs_dec<kFwdRegsCtl>();
+    const int st = warp >> 1;
+    const int vc = 2 * int(blockIdx.x) + st;
+    uint64_t* b = bars + 16 * st;
+    uint64_t *q_full = b, *q_empty = b + 1, *k_full = b + 2, *k_empty = b + 4, *v_full = b + 6, *v_empty = b + 8;
+    uint64_t *s_full = b + 10, *s_free = b + 11, *p_full = b + 12, *p_free = b + 13, *mma_done = b + 14;
+    const uint32_t base = sb + uint32_t(st * FwdSmem::STREAM);
+    if ((warp & 1) == 0 && lane == 0) {
       // -------------------------------------------------------------- TMA producer
       int ks = 0, vs = 0, nk = 0, nv = 0, nqi = 0;
       uint32_t kph = 0, vph = 0;
       bool ok = true;
       #pragma unroll 1
-      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
-        const int i = snake_item(r);
+      for (int r = 0; r * VG < p.items && ok && !*abort_flag; ++r) {
+        const int i = vitem(r, vc);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full), TILE);
-        tma_load_4d(sb + FwdSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
+        tma_load_4d(base + FwdSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         ++nqi;
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j) {
           if (*abort_flag) { ok = false; break; }
           if (!mbar_wait(smem_u32(&k_empty[ks]), kph ^ 1, p.wait_ns)) { ok = false; break; }
           mbar_expect_tx(smem_u32(&k_full[ks]), TILE);
-          tma_load_4d(sb + FwdSmem::K + ks * TILE, &tmK, smem_u32(&k_full[ks]), 0, it.h, j * BT, it.b);
+          tma_load_4d(base + FwdSmem::K + ks * TILE, &tmK, smem_u32(&k_full[ks]), 0, it.h, j * BT, it.b);
           ++nk;
-          if (++ks == RING) { ks = 0; kph ^= 1; }
+          if (++ks == KV_SLOTS) { ks = 0; kph ^= 1; }
           if (!mbar_wait(smem_u32(&v_empty[vs]), vph ^ 1, p.wait_ns)) { ok = false; break; }
           mbar_expect_tx(smem_u32(&v_full[vs]), TILE);
-          tma_load_4d(sb + FwdSmem::V + vs * TILE, &tmV, smem_u32(&v_full[vs]), 0, it.h, j * BT, it.b);
+          tma_load_4d(base + FwdSmem::V + vs * TILE, &tmV, smem_u32(&v_full[vs]), 0, it.h, j * BT, it.b);
           ++nv;
-          if (++vs == RING) { vs = 0; vph ^= 1; }
+          if (++vs == KV_SLOTS) { vs = 0; vph ^= 1; }
         }
       }
       if (!ok) give_up();
       // bounded wait for the fills that may still be in flight
       bool drained = true;
       if (nqi > 0) drained &= mbar_wait(smem_u32(q_full), (nqi - 1) & 1);
-      for (int n = 0; n < (nk < RING ? nk : RING); ++n) {
-        if (--ks < 0) { ks = RING - 1; kph ^= 1; }
+      for (int n = 0; n < (nk < KV_SLOTS ? nk : KV_SLOTS); ++n) {
+        if (--ks < 0) { ks = KV_SLOTS - 1; kph ^= 1; }
         drained &= mbar_wait(smem_u32(&k_full[ks]), kph);
       }
-      for (int n = 0; n < (nv < RING ? nv : RING); ++n) {
-        if (--vs < 0) { vs = RING - 1; vph ^= 1; }
+      for (int n = 0; n < (nv < KV_SLOTS ? nv : KV_SLOTS); ++n) {
+        if (--vs < 0) { vs = KV_SLOTS - 1; vph ^= 1; }
         drained &= mbar_wait(smem_u32(&v_full[vs]), vph);
       }
       if (!drained) give_up();
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    } else if ((warp & 1) == 1 && lane == 0) {
       // -------------------------------------------------------------- MMA issuer
+      const uint32_t tS = tbase + uint32_t(256 * st), tO = tS + 128;
       int ks = 0, vs = 0, nqi = 0;
       uint32_t kph = 0, vph = 0;
-      uint32_t g = 0;  // score tiles issued so far (selects the S / P buffer and its phase)
+      uint32_t g = 0;  // score tiles issued so far (phases of the single S and P buffers)
       bool ok = true;
       auto issue_pv = [&](uint32_t gg, bool first) -> bool {
-        const int b = int(gg & 1);
-        const uint32_t u = gg >> 1;
-        if (!mbar_wait(smem_u32(&p_full[b]), u & 1, p.wait_ns)) return false;
+        if (!mbar_wait(smem_u32(p_full), gg & 1, p.wait_ns)) return false;
         if (!mbar_wait(smem_u32(&v_full[vs]), vph, p.wait_ns)) return false;
         tc_fence_after();
-        const uint32_t ps = sb + FwdSmem::P + b * PT;
-        const uint32_t vsm = sb + FwdSmem::V + vs * TILE;
+        const uint32_t ps = base + FwdSmem::P;
+        const uint32_t vsm = base + FwdSmem::V + vs * TILE;
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk) {
           const uint64_t ad = smem_desc(ps + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024);
@@ -255,13 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma<false>(tO, ad, bd, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&v_empty[vs]));
-        tc_commit(smem_u32(&p_free[b]));
-        if (++vs == RING) { vs = 0; vph ^= 1; }
+        tc_commit(smem_u32(p_free));
+        if (++vs == KV_SLOTS) { vs = 0; vph ^= 1; }
         return true;
       };
       #pragma unroll 1
-      for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
-        const int i = snake_item(r);
+      for (int r = 0; r * VG < p.items && ok && !*abort_flag; ++r) {
+        const int i = vitem(r, vc);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_full), nqi & 1, p.wait_ns)) { ok = false; break; }
@@ -269,20 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j, ++g) {
-          const int b = int(g & 1);
-          const uint32_t u = g >> 1;
           if (*abort_flag || !mbar_wait(smem_u32(&k_full[ks]), kph, p.wait_ns) ||
-              !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) { ok = false; break; }
+              !mbar_wait(smem_u32(s_free), (g & 1) ^ 1, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t ksm = sb + FwdSmem::K + ks * TILE;
+          const uint32_t ksm = base + FwdSmem::K + ks * TILE;
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)
-            tc_mma<false>(tbase + uint32_t(b * 128), smem_desc(sb + FwdSmem::Q + kk * 32, 16, 1024),
-                          smem_desc(ksm + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+            tc_mma<false>(tS, smem_desc(base + FwdSmem::Q + kk * 32, 16, 1024), smem_desc(ksm + kk * 32, 16, 1024),
+                          IDESC_S, kk > 0 ? 1u : 0u);
           tc_commit(smem_u32(&k_empty[ks]));
-          tc_commit(smem_u32(&s_full[b]));
+          tc_commit(smem_u32(s_full));
           if (j == it.nkv - 1) tc_commit(smem_u32(q_empty));
-          if (++ks == RING) { ks = 0; kph ^= 1; }
+          if (++ks == KV_SLOTS) { ks = 0; kph ^= 1; }
           if (j >= 1 && !issue_pv(g - 1, j == 1)) { ok = false; break; }
         }
         if (!ok) break;
@@ -294,15 +302,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
     }
   } else {
+    regs_inc<kFwdRegsRows>();
     // ---------------------------------------------------------------- softmax / epilogue
+    const int st = wg - 1;
+    const int vc = 2 * int(blockIdx.x) + st;
+    uint64_t* b = bars + 16 * st;
+    uint64_t *s_full = b + 10, *s_free = b + 11, *p_full = b + 12, *p_free = b + 13;
+    const uint32_t base = sb + uint32_t(st * FwdSmem::STREAM);
+    const uint32_t tS = tbase + uint32_t(256 * st), tO = tS + 128;
     const int qw = warp & 3;            // TMEM lanes [32 qw, 32 qw + 32)
     const int rr = qw * 32 + lane;      // row within the query tile
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
-    const uint32_t stage = sb + FwdSmem::STAGE + uint32_t(qw) * 8192;
+    // O and O_lo are staged in this warp's own rows of the P tile (chunk 0 and chunk 1)
+    const uint32_t stage = base + FwdSmem::P + uint32_t(qw) * 4096;
     uint32_t g = 0;
     #pragma unroll 1
-    for (int r = 0; r * int(gridDim.x) < p.items; ++r) {
-      const int i = snake_item(r);
+    for (int r = 0; r * VG < p.items; ++r) {
+      const int i = vitem(r, vc);
       if (i >= p.items) continue;
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const Item it = decode(i, p.B, p.H, p.nq, p.causal);
@@ -312,18 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       #pragma unroll 1
       for (int j = 0; j < it.nkv; ++j, ++g) {
-        const int b = int(g & 1);
-        const uint32_t u = g >> 1;
-        if (!warp_wait(smem_u32(&s_full[b]), u & 1, p.wait_ns)) { ok = false; break; }
+        if (!warp_wait(smem_u32(s_full), g & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         uint32_t r[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+          tmem_ld32(tS + lane_off + uint32_t(c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
+        if (lane == 0) mbar_arrive(smem_u32(s_free));
         // keys at or past `lim` (relative to this tile) are masked
         const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT;
         if (lim < BT) {
@@ -340,10 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m && (m == -INFINITY || (m_new - m) * p.sc > kRescale);
+        // P V of the previous tile is complete before P is rewritten (and before O is rescaled)
+        if (!warp_wait(smem_u32(p_free), (g & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // O holds Σ 2^((s − m)·sc)·v with the old m: bring it to m_new once PV_{j−1} is done
-          const uint32_t pg = g - 1;
-          if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1, p.wait_ns)) { ok = false; break; }
+          // O holds Σ 2^((s − m)·sc)·v with the old m: bring it to m_new
           tc_fence_after();
           const float a = need ? exp2f((m - m_new) * p.sc) : 1.f;
 #pragma unroll
@@ -362,8 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
         }
         const float ms = (m == -INFINITY) ? 0.f : m * p.sc;
-        if (!warp_wait(smem_u32(&p_free[b]), (u & 1) ^ 1, p.wait_ns)) { ok = false; break; }
-        const uint32_t ps = sb + FwdSmem::P + b * PT;
+        if (j == 0) {  // the previous item's O stores have read this warp's rows of the P tile
+          if (lane == 0) bulk_wait_read_0();
+          __syncwarp();
+        }
+        const uint32_t ps = base + FwdSmem::P;
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -382,15 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&p_full[b]));
+        if (lane == 0) mbar_arrive(smem_u32(p_full));
       }
       if (!ok) {
         if (lane == 0) give_up();
         break;
       }
-      // ---- epilogue: O / l after the last PV
-      const uint32_t pg = g - 1;
-      if (!warp_wait(smem_u32(&p_free[pg & 1]), (pg >> 1) & 1, p.wait_ns)) {
+      // ---- epilogue: O / l after the last P V
+      if (!warp_wait(smem_u32(p_free), (g - 1) & 1, p.wait_ns)) {
         if (lane == 0) give_up();
         break;
       }
@@ -401,29 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       const float inv = 1.f / l;
-      if (lane == 0) bulk_wait_read_0();  // the previous item's stores have read the staging tiles
-      __syncwarp();
-      // O rounded to bf16, and (optionally) the rounding residual O − bf16(O) rounded to bf16:
-      // the pair holds O to ~2⁻¹⁶ relative for the backward's D = Σ dO∘O
+      // O rounded to bf16, and (optionally) the rounding residual O − bf16(O) rounded to bf16
 #pragma unroll
       for (int un = 0; un < 8; ++un) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a = __uint_as_float(o[8 * un + 2 * e]) * inv, b = __uint_as_float(o[8 * un + 2 * e + 1]) * inv;
-          hi[e] = pack_bf16(a, b);
+          const float a = __uint_as_float(o[8 * un + 2 * e]) * inv, bb = __uint_as_float(o[8 * un + 2 * e + 1]) * inv;
+          hi[e] = pack_bf16(a, bb);
           const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&hi[e]);
-          lo[e] = pack_bf16(a - __low2float(h), b - __high2float(h));
+          lo[e] = pack_bf16(a - __low2float(h), bb - __high2float(h));
         }
         const uint32_t off = uint32_t(lane) * 128 + (uint32_t(un ^ (lane & 7)) << 4);
         st_shared_v4(stage + off, hi[0], hi[1], hi[2], hi[3]);
-        if (p.o_lo) st_shared_v4(stage + 4096 + off, lo[0], lo[1], lo[2], lo[3]);
+        if (p.o_lo) st_shared_v4(stage + TILE + off, lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         tma_store_4d(&tmO, stage, 0, it.h, it.qt * BT + qw * 32, it.b);
-        if (p.o_lo) tma_store_4d(&tmOlo, stage + 4096, 0, it.h, it.qt * BT + qw * 32, it.b);
+        if (p.o_lo) tma_store_4d(&tmOlo, stage + TILE, 0, it.h, it.qt * BT + qw * 32, it.b);
         bulk_commit();
       }
       if (row < p.S) p.lse[(int64_t(it.b) * p.H + it.h) * p.S + row] = (m * p.sc + log2f(l)) * kLn2;
@@ -1218,9 +1231,21 @@ int xt_attention_fwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   p.flag = errflag();
   p.wait_ns = wait_limit_ns();
   static bool smem_set = false;
+  static int regs = -1;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_fwd_kernel), FwdSmem::BYTES, smem_set, "xt_attention_fwd"));
-  const int grid = p.items < num_sms() ? p.items : num_sms();
-  launch(attn_fwd_kernel, grid, attn::kThreads, FwdSmem::BYTES, as_stream(stream), tq, tk, tv, to, tolo, p);
+  if (regs < 0) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, attn_fwd_kernel) != cudaSuccess)
+      return fail(XT_ERR_CUDA, "xt_attention_fwd: cudaFuncGetAttributes failed");
+    regs = fa.numRegs;
+  }
+  // the warp groups' register split (kFwdRegsCtl + 2 × kFwdRegsRows per 128 threads) adds up to
+  // the 168 per thread the kernel is launched with; any other count could never be met
+  if (regs != 168)
+    return fail(XT_ERR_UNSUPPORTED, "xt_attention_fwd: forward kernel built with %d registers, not 168", regs);
+  const int pairs = (p.items + 1) / 2;  // two query-tile streams per CTA
+  const int grid = pairs < num_sms() ? pairs : num_sms();
+  launch(attn_fwd_kernel, grid, kThreadsFwd, FwdSmem::BYTES, as_stream(stream), tq, tk, tv, to, tolo, p);
   return check_launch("xt_attention_fwd");
 }
 

@@ -235,16 +235,22 @@ __device__ __forceinline__ bool dropout_keep(uint64_t seed, uint64_t i, float p)
 inline uint64_t dropout_threshold(float p) {
   return static_cast<uint64_t>(std::ceil(static_cast<double>(p) * 16777216.0)) << 40;
 }
+// Only the high word of the last product is formed (the threshold's low 40 bits are zero, so
+// z ≥ thr ⟺ z >> 32 ≥ thr >> 32): hi32(y·C) = umulhi(y_lo, C_lo) + y_lo·C_hi + y_hi·C_lo (mod 2³²).
 __device__ __forceinline__ uint32_t dropout_keep8(uint64_t seed, uint64_t i0, uint64_t thr) {
   constexpr uint64_t kG = 0x9E3779B97F4A7C15ull;
+  constexpr uint32_t kC2lo = 0x133111EBu, kC2hi = 0x94D049BBu;
+  const uint32_t thr_hi = uint32_t(thr >> 32);
   const uint64_t base = i0 * kG;
   uint32_t bits = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint64_t z = (seed ^ (base + uint64_t(j) * kG)) + kG;
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    bits |= (z >= thr ? 1u : 0u) << j;
+    const uint64_t y = z ^ (z >> 27);
+    const uint32_t ylo = uint32_t(y), yhi = uint32_t(y >> 32);
+    const uint32_t hi = __umulhi(ylo, kC2lo) + ylo * kC2hi + yhi * kC2lo;
+    bits |= (hi >= thr_hi ? 1u : 0u) << j;
   }
   return bits;
 }

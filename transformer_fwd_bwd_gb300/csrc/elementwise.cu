@@ -39,7 +39,10 @@ struct EwArgs {
   const float* scalar;
 };
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+// σ(x) = 1/(1 + e^(−x)) with the hardware exponential (ex2.approx of −x·log2 e: relative error
+// ≲ |x|·2⁻²⁴ from rounding the argument, ≈ 5e-6 at the edge of the fp32 range) and the
+// correctly rounded reciprocal, inside the fp32 ops' 1e-5 bound.
+__device__ __forceinline__ float sigmoidf_(float x) { return __frcp_rn(1.f + __expf(-x)); }
 
 template <EwOp OP>
 __device__ __forceinline__ void ew_apply(float a, float b, float c, uint64_t i, const EwArgs& g,
@@ -122,9 +125,10 @@ __global__ void __launch_bounds__(256, 4) ew_kernel(EwArgs g) {
   if constexpr (VEC) {
     const int64_t nv = g.n / 8;
     // The plain streaming ops take U vectors per thread per step, all loads issued before any is
-    // used, so an SM keeps U times the bytes in flight; GELU and dropout (bound by their
-    // arithmetic: erfc, the per-element hash) keep one, as their registers set their occupancy.
-    constexpr int U = (OP == EW_GELU || OP == EW_GELU_BWD || OP == EW_DROPOUT || OP == EW_DROPOUT_ADD) ? 1
+    // used, so an SM keeps U times the bytes in flight; GELU (bound by its erfc arithmetic) and
+    // fp32 dropout keep one, as their registers set their occupancy; bf16 dropout two.
+    constexpr int U = (OP == EW_GELU || OP == EW_GELU_BWD) ? 1
+                      : (OP == EW_DROPOUT || OP == EW_DROPOUT_ADD) ? (sizeof(TI) == 2 ? 2 : 1)
                       : OP == EW_MUL_BWD ? (sizeof(TI) == 2 ? 2 : 1) : 16 / int(sizeof(TI)) / 2;
     if constexpr (U > 1) {
       for (int64_t v0 = t; v0 < nv; v0 += U * stride) {
@@ -145,10 +149,19 @@ __global__ void __launch_bounds__(256, 4) ew_kernel(EwArgs g) {
           if (v >= nv) break;
           const int64_t i0 = v * 8;
           float r0[8], r1[8];
+          if constexpr (OP == EW_DROPOUT || OP == EW_DROPOUT_ADD) {
+            const uint32_t keep = dropout_keep8(g.seed, uint64_t(i0), g.thr);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ew_apply<OP>(IO::A ? ra[u].get(j) : 0.f, IO::B ? rb[u].get(j) : 0.f, IO::C ? rc[u].get(j) : 0.f,
-                         uint64_t(i0 + j), g, r0[j], r1[j]);
+            for (int j = 0; j < 8; ++j) {
+              if constexpr (OP == EW_DROPOUT) r0[j] = ((keep >> j) & 1u) ? ra[u].get(j) * g.dscale : 0.f;
+              else r0[j] = ra[u].get(j) + (((keep >> j) & 1u) ? rb[u].get(j) * g.dscale : 0.f);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              ew_apply<OP>(IO::A ? ra[u].get(j) : 0.f, IO::B ? rb[u].get(j) : 0.f, IO::C ? rc[u].get(j) : 0.f,
+                           uint64_t(i0 + j), g, r0[j], r1[j]);
+          }
           if (o0) {
             if (acc0) {
               float old[8];

@@ -404,23 +404,18 @@ __device__ __forceinline__ TileInfo tile_info(int t, const Params& p) {
 }
 
 // The pieces (tile, k-block range) a CTA computes, in order: whole tiles blockIdx.x + i·gridDim.x,
-// or under stream-K the parts of the tiles its contiguous share of iterations covers.  The
-// causal modes 2 and 3, whose tiles' K ranges grow (mode 2) or shrink (mode 3) with the tile
-// row, take whole tiles longest first — all batches' longest row blocks, then the next — over
-// rounds that alternate direction across the units, which evens out the units' totals.
+// or under stream-K the parts of the tiles its contiguous share of iterations covers.
 struct Cursor {
   int64_t it, end;
-  int u;
 };
 // `u` of `nu` schedule units: a CTA, or a CTA pair of the paired kernel.
 __device__ __forceinline__ Cursor cursor_begin(const Params& p, int u, int nu) {
   Cursor c;
-  c.u = u;
   if (p.sk) {
     c.it = int64_t(u) * p.sk_iters / nu;
     c.end = int64_t(u + 1) * p.sk_iters / nu;
   } else {
-    c.it = p.causal >= 2 ? 0 : u;
+    c.it = u;
     c.end = 0;
   }
   return c;
@@ -429,22 +424,10 @@ __device__ __forceinline__ Cursor cursor_begin(const Params& p, int u, int nu) {
 __device__ __forceinline__ bool cursor_next(Cursor& c, const Params& p, int total, int nu, int& t, int& kb0,
                                             int& kb1) {
   if (!p.sk) {
-    kb0 = kb1 = -1;
-    if (p.causal >= 2) {
-      const int64_t r = c.it;  // round
-      const int64_t x = r * nu + ((r & 1) ? nu - 1 - c.u : c.u);
-      if (x >= total) return false;
-      ++c.it;
-      const int rest = p.num_n * p.batches;  // tiles per row block
-      const int k = int(x / rest), w = int(x - int64_t(k) * rest);
-      const int mb = p.causal == 2 ? p.num_m - 1 - k : k;
-      const int z = w / p.num_n, nb = w - z * p.num_n;
-      t = (z * p.num_n + nb) * p.num_m + mb;
-      return true;
-    }
     if (c.it >= total) return false;
     t = int(c.it);
     c.it += nu;
+    kb0 = kb1 = -1;
     return true;
   }
   if (c.it >= c.end) return false;

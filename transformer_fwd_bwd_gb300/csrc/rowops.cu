@@ -126,6 +126,28 @@ static int bwd_blocks(int64_t rows, int rpb) {
   return int(g < 1 ? 1 : g);
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Rows of 4 KB or more: a row group asks L2 for the row it takes next (its vectors of row rn)
+// while it still waits on this row's loads, so that row's loads are L2 hits.  With one or two
+// row groups per SM, a row's DRAM latency is otherwise paid once per row, unhidden.
+template <typename T, int VW>
+__device__ __forceinline__ void prefetch_next_row(const T* base, int64_t rn, int64_t rows, int64_t cols, int l,
+                                                  int tpr) {
+  if (rn >= rows || cols * int64_t(sizeof(T)) < 4096) return;
+  const int64_t nvec = cols / VW;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t j = l + int64_t(k) * tpr;
+    if (j < nvec) prefetch_l2(base + rn * cols + j * VW);
+  }
+}
+
 // ============================================================================== RMSNorm
 
 template <typename T, int VW>
@@ -145,6 +167,10 @@ __global__ void __launch_bounds__(1024) rms_fwd_kernel(const T* __restrict__ x, 
     for (int k = 0; k < NV; ++k) {
       const int64_t j = l + int64_t(k) * tpr;
       if (act && j < nvec) v[k].load(x + r * cols + j * VW); else v[k].zero();
+    }
+    prefetch_next_row<T, VW>(x, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
 #pragma unroll
       for (int e = 0; e < VW; ++e) ss += v[k].get(e) * v[k].get(e);
     }
@@ -255,6 +281,11 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) rms_bwd_kernel(cons
       } else {
         vd[k].zero(); vx[k].zero();
       }
+    }
+    prefetch_next_row<T, VW>(d, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
+    prefetch_next_row<T, VW>(x, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
 #pragma unroll
       for (int e = 0; e < VW; ++e) s += vd[k].get(e) * gm[k].get(e) * vx[k].get(e);
     }
@@ -310,6 +341,10 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
     for (int k = 0; k < NV; ++k) {
       const int64_t j = l + int64_t(k) * tpr;
       if (act && j < nvec) v[k].load(x + r * cols + j * VW); else v[k].zero();
+    }
+    prefetch_next_row<T, VW>(x, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
 #pragma unroll
       for (int e = 0; e < VW; ++e) s += v[k].get(e);
     }
@@ -341,13 +376,6 @@ __global__ void __launch_bounds__(1024) ln_fwd_kernel(const T* __restrict__ x, c
       }
     }
   }
-}
-
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // LayerNorm backward, one row group per row: NVT vectors per thread.  The next row's d, x and
@@ -753,6 +781,7 @@ __global__ void __launch_bounds__(1024) softmax_fwd_kernel(const T* __restrict__
 #pragma unroll
       for (int e = 0; e < VW; ++e) m = fmaxf(m, f[k][e]);
     }
+    prefetch_next_row<T, VW>(x, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
     m = group_reduce<true>(m, tpr, red);
     // exp(x − m) = 2^(x·log2 e − m·log2 e): one fma and one exp2 per element; masked
     // elements hold −inf and give exactly 0
@@ -817,6 +846,8 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 256 ? 2 : 1) softmax_bwd_kernel(
 #pragma unroll
       for (int e = 0; e < VW; ++e) s = fmaf(vd[k].get(e), vy[k].get(e), s);
     }
+    prefetch_next_row<T, VW>(d, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
+    prefetch_next_row<T, VW>(y, r + int64_t(gridDim.x) * rpb, rows, cols, l, tpr);
     s = group_reduce<false>(s, tpr, red);
     if (!act) continue;
     const int ext = causal_ext(causal, q, cols);
