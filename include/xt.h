@@ -522,7 +522,12 @@ int xt_adamw_step(const xt_adamw_config* cfg, int n, float* const* param, const 
  * xt_block_fwd runs the forward and keeps the saved tensors in ws; xt_block_bwd then adds
  * every parameter gradient into the grad buffers (+=, [BP] § Ackumulation över mikrobatcher);
  * call xt_block_zero_grads first for a fresh step.  No host synchronisation; the pair can
- * be captured in a CUDA graph.
+ * be captured in a CUDA graph.  xt_block_bwd runs the weight-gradient GEMMs on a second
+ * stream of the device (created by the first xt_block_workspace_size call, never destroyed),
+ * forked from and joined back into `stream` with events, so the work it enqueues is complete
+ * when `stream` reaches its end; calls on one device must not be issued concurrently from
+ * several host threads (they share that stream's events).  With recompute = 1 everything
+ * stays on `stream`.
  * ------------------------------------------------------------------------------- */
 enum { XT_MLP_SWIGLU = 0, XT_MLP_GELU = 1 };
 /* Attention path: AUTO runs the fused kernels (xt_attention_*) when dtype is XT_BF16, hd is
@@ -580,6 +585,11 @@ int xt_block_fwd(const xt_block_config* cfg, const xt_block_params* prm, const i
 int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const int32_t* ids,
                  const int32_t* targets, void* ws, void* stream);
 int xt_block_zero_grads(const xt_block_config* cfg, const xt_block_params* prm, void* stream);
+/* Process-wide: 1 (default) the backward's weight-gradient GEMMs run on the second stream; 0 all
+ * on `stream` (for measurement: a GEMM launch timed beside other kernels includes the time it
+ * waits for SMs they hold).  Applies to backward calls enqueued afterwards; XT_ERR_INVALID_ARG
+ * for other values. */
+int xt_block_set_overlap(int on);
 
 #ifdef __cplusplus
 }

@@ -130,6 +130,26 @@ def test_block_deterministic_and_accumulates():
         assert norm_err(g2[k], 2 * ga[k]) <= 1e-6, k
 
 
+@pytest.mark.parametrize("cfg", [variant("gpt12", B=2, S=256, d=128, H=2, hd=64, F=512, V=1000, n_layers=3),
+                                 variant("block256", p=0.1)], ids=["bf16-fused-3layers", "fp32-composed-dropout"])
+def test_block_weight_gradient_stream_matches_one_stream(cfg):
+    """The backward with its weight-gradient GEMMs on the second stream gives the one-stream
+    backward's loss and every gradient bit for bit: the same kernels on the same inputs, so any
+    missing ordering between the streams (a dW reading a buffer the main stream has already
+    overwritten) would show as a difference."""
+    params = synth.block_params(cfg, gain_jitter=0.1)
+    ids, tgt = synth.block_tokens(cfg)
+    xt.block_set_overlap(0)
+    try:
+        l0, g0, _ = run_native(cfg, params, ids, tgt, steps=2)
+    finally:
+        xt.block_set_overlap(1)
+    l1, g1, _ = run_native(cfg, params, ids, tgt, steps=2)
+    assert l0 == l1
+    for k in g0:
+        assert np.array_equal(g0[k], g1[k]), k
+
+
 def test_block_gpt12_full():
     """12-layer GPT-style stack at full size (B 8, S 1024, d 768, 12 heads, GELU 3072, vocab
     50304, bf16) — the workload the benchmark times — against the float64 oracle."""

@@ -13,7 +13,14 @@
 // The residual-stream gradient is kept in float32 whatever the activation dtype (it sums the
 // fan-out of every residual add and norm); everything else is stored in the activation dtype
 // with float32 statistics.
+//
+// The backward puts the weight-gradient GEMMs (dW = Xᵀ·dY, off the path that carries the
+// gradient down the stack) on a second stream of the same device, forked and joined with events
+// around the buffers they read, so they run beside the data-gradient GEMMs, the attention
+// backward and the row kernels instead of between them.
 #include <algorithm>
+#include <map>
+#include <mutex>
 #include <vector>
 
 #include "internal.cuh"
@@ -188,7 +195,7 @@ struct Bufs {
   void *h_final, *hf, *logits, *tmp;
   float *stf, *lse, *rope, *dh, *one;
   void *gA, *gB, *dm, *dgu, *dP, *dqkv;
-  void *ws_norm, *ws_ce, *ws_emb, *ws_mm;
+  void *ws_norm, *ws_ce, *ws_emb, *ws_mm, *ws_mm2;  // ws_mm2: the weight-gradient stream's matmul scratch
   size_t ws_mm_bytes, dP_bytes = 0;
   size_t total;
 };
@@ -200,6 +207,7 @@ int carve(const Dims& m, void* base, Bufs& b) {
   // the matmul scratch first: its leading stream-K flag words are the workspace's first bytes
   b.ws_mm_bytes = max_matmul_ws(m);
   b.ws_mm = a.take(b.ws_mm_bytes);
+  b.ws_mm2 = a.take(b.ws_mm_bytes);  // its flag words are zero on a zeroed workspace, as ws_mm's
   b.h_in.resize(m.L); b.x1.resize(m.L); b.qkv.resize(m.L); b.P.resize(m.L); b.o.resize(m.L);
   b.h_mid.resize(m.L); b.x2.resize(m.L); b.up.resize(m.L); b.mact.resize(m.L);
   b.st1.resize(m.L); b.st2.resize(m.L); b.o_lo.assign(m.L, nullptr);
@@ -299,6 +307,33 @@ uint64_t site_seed(const xt_block_config& c, int64_t l, uint64_t site) { return 
 
 char* off(void* p, int64_t elems, int64_t e) { return static_cast<char*>(p) + elems * e; }
 
+int g_overlap = 1;  // xt_block_set_overlap
+
+// The weight-gradient stream of the current device and its events: [0] fork, [1..4] the last
+// dW_down / dW_up / dWo / dWqkv done, [5] all done.  Created once per device (the first
+// xt_block_workspace_size or xt_block_bwd call), never destroyed.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[6] = {};
+};
+int side_stream(SideStream** out) {
+  static std::mutex mu;
+  static std::map<int, SideStream> per_device;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(XT_ERR_CUDA, "block: cudaGetDevice failed");
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& ss = per_device[dev];
+  if (!ss.s) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(XT_ERR_CUDA, "block: cannot create the weight-gradient stream");
+    for (auto& e : ss.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return fail(XT_ERR_CUDA, "block: cannot create the weight-gradient stream's events");
+  }
+  *out = &ss;
+  return XT_OK;
+}
+
 int norm_fwd(const xt_block_config& c, const Dims& m, const void* x, const void* g, const void* b, void* y, float* st,
              void* stream) {
   if (m.rms) return xt_rms_norm_fwd(x, g, y, st, m.T, m.d, c.eps, m.dt, stream);
@@ -379,6 +414,15 @@ int xt_block_workspace_size(const xt_block_config* cfg, size_t* bytes) {
   Bufs b;
   XT_TRY(carve(dims_of(*cfg), nullptr, b));
   *bytes = b.total;
+  // the weight-gradient stream is created here when a device is present, before any stream
+  // capture the caller may start (xt_block_bwd creates it otherwise)
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0) {
+    SideStream* ss = nullptr;
+    XT_TRY(side_stream(&ss));
+  } else {
+    cudaGetLastError();  // no device: a size query only
+  }
   return XT_OK;
 }
 
@@ -430,9 +474,38 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
   cudaStream_t s = as_stream(stream);
   const int64_t T = m.T, d = m.d, e = m.e;
   const bool drop = c.training && c.p > 0.f;
+  // Weight gradients go to the side stream s2 (with its own matmul scratch) unless activations
+  // are recomputed: then the layers share one set of activation buffers, which the next layer's
+  // recompute overwrites while a dW of this layer could still be reading them.
+  const bool side = !m.recompute && g_overlap;
+  SideStream* ss = nullptr;
+  if (side) XT_TRY(side_stream(&ss));
+  cudaStream_t s2 = side ? ss->s : s;
+  void* ws2 = side ? b.ws_mm2 : b.ws_mm;
+  bool recorded[5] = {false, false, false, false, false};
+  auto cuda_ok = [](cudaError_t e) { return e == cudaSuccess ? XT_OK : fail(XT_ERR_CUDA, "block: %s", cudaGetErrorString(e)); };
+  // s2 waits for what s has enqueued so far (the dW's operands are written)
+  auto fork = [&]() -> int {
+    if (!side) return XT_OK;
+    XT_TRY(cuda_ok(cudaEventRecord(ss->ev[0], s)));
+    return cuda_ok(cudaStreamWaitEvent(s2, ss->ev[0], 0));
+  };
+  auto done = [&](int k) -> int {
+    if (!side) return XT_OK;
+    recorded[k] = true;
+    return cuda_ok(cudaEventRecord(ss->ev[k], s2));
+  };
+  // s waits until dW k (the latest one enqueued) has read its operands, before overwriting them
+  auto join = [&](int k) -> int {
+    if (!side || !recorded[k]) return XT_OK;
+    return cuda_ok(cudaStreamWaitEvent(s, ss->ev[k], 0));
+  };
+  enum { kDown = 1, kUp = 2, kO = 3, kQkv = 4 };
   // dlogits are in the logits buffer (written by the forward's cross-entropy pass) → tied
-  // embedding and final norm
-  XT_TRY(matmul(logits_de(m), b.logits, b.hf, prm->dE, b.ws_mm, b.ws_mm_bytes, s));
+  // embedding and final norm; dE (the embedding's weight gradient) on s2, read again only by
+  // the embedding backward after the final join
+  XT_TRY(fork());
+  XT_TRY(matmul(logits_de(m), b.logits, b.hf, prm->dE, ws2, b.ws_mm_bytes, s2));
   XT_TRY(matmul(logits_dhf(m), b.logits, prm->E, b.gA, b.ws_mm, b.ws_mm_bytes, s));
   // Each norm backward also writes the gradient the residual dropout before it passes on: the
   // MLP sub-block reads its df from gB, the attention sub-block its input gradient from gA.
@@ -443,20 +516,29 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
     // gA / gB and dh are untouched by it)
     if (m.recompute) XT_TRY(layer_front(c, m, prm, b, l, true, stream));
     // MLP sub-block: df = dropout'(dh) (in gB); dW_down += mᵀ df; dm = df W_downᵀ; activation'; ...
-    XT_TRY(matmul(lin_dw(m, m.F, d), b.mact[l], b.gB, prm->dW_down[l], b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(fork());
+    XT_TRY(matmul(lin_dw(m, m.F, d), b.mact[l], b.gB, prm->dW_down[l], ws2, b.ws_mm_bytes, s2));
+    XT_TRY(done(kDown));
     XT_TRY(matmul(lin_dx(m, m.F, d), b.gB, prm->W_down[l], b.dm, b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(join(kUp));  // the layer above's dW_up has read dgu
     if (m.swiglu)
       XT_TRY(xt_swiglu_bwd(b.dm, m.F, b.up[l], off(b.up[l], m.F, e), m.UP, b.dgu, off(b.dgu, m.F, e), m.UP, T, m.F,
                            m.dt, 0, stream));
     else
       XT_TRY(xt_gelu_bwd(b.dm, b.up[l], b.dgu, T * m.F, m.dt, 0, stream));
-    XT_TRY(matmul(lin_dw(m, d, m.UP), b.x2[l], b.dgu, prm->dW_up[l], b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(fork());
+    XT_TRY(matmul(lin_dw(m, d, m.UP), b.x2[l], b.dgu, prm->dW_up[l], ws2, b.ws_mm_bytes, s2));
+    XT_TRY(done(kUp));
+    XT_TRY(join(kDown));  // dW_down has read gB
     XT_TRY(matmul(lin_dx(m, d, m.UP), b.dgu, prm->W_up[l], b.gB, b.ws_mm, b.ws_mm_bytes, s));
     XT_TRY(norm_bwd_g(c, m, b.gB, b.h_mid[l], prm->g2[l], b.st2[l], b.dh, prm->dg2[l],
                       prm->db2 ? prm->db2[l] : nullptr, 1, b.gA, site_seed(c, l, kSiteAttn), drop, b, stream));
     // attention sub-block (its input gradient dropout'(dh) is in gA)
-    XT_TRY(matmul(lin_dw(m, d, d), b.o[l], b.gA, prm->dWo[l], b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(fork());
+    XT_TRY(matmul(lin_dw(m, d, d), b.o[l], b.gA, prm->dWo[l], ws2, b.ws_mm_bytes, s2));
+    XT_TRY(done(kO));
     XT_TRY(matmul(lin_dx(m, d, d), b.gA, prm->Wo[l], b.gB, b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(join(kQkv));  // the layer above's dWqkv has read dqkv
     if (m.fused) {
       XT_TRY(xt_attention_bwd(b.qkv[l], off(b.qkv[l], d, e), off(b.qkv[l], 2 * d, e), 3 * d, b.o[l], b.o_lo[l], b.gB,
                               d, static_cast<const float*>(b.P[l]), b.dqkv, off(b.dqkv, d, e), off(b.dqkv, 2 * d, e),
@@ -470,7 +552,10 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
     }
     if (c.rope)
       XT_TRY(xt_rope_bwd(b.dqkv, b.dqkv, b.rope, int(m.B), int(m.S), int(2 * m.H), int(m.hd), 3 * d, m.dt, 0, stream));
-    XT_TRY(matmul(lin_dw(m, d, 3 * d), b.x1[l], b.dqkv, prm->dWqkv[l], b.ws_mm, b.ws_mm_bytes, s));
+    XT_TRY(fork());
+    XT_TRY(matmul(lin_dw(m, d, 3 * d), b.x1[l], b.dqkv, prm->dWqkv[l], ws2, b.ws_mm_bytes, s2));
+    XT_TRY(done(kQkv));
+    XT_TRY(join(kO));  // dWo has read gA
     XT_TRY(matmul(lin_dx(m, d, 3 * d), b.dqkv, prm->Wqkv[l], b.gA, b.ws_mm, b.ws_mm_bytes, s));
     if (l > 0)
       XT_TRY(norm_bwd_g(c, m, b.gA, b.h_in[l], prm->g1[l], b.st1[l], b.dh, prm->dg1[l],
@@ -479,8 +564,19 @@ int xt_block_bwd(const xt_block_config* cfg, const xt_block_params* prm, const i
       XT_TRY(norm_bwd(m, b.gA, b.h_in[l], prm->g1[l], b.st1[l], b.dh, prm->dg1[l], prm->db1 ? prm->db1[l] : nullptr,
                       1, b, stream));
   }
+  // every weight gradient is in before the embedding backward adds into dE and the call returns
+  if (side) {
+    XT_TRY(cuda_ok(cudaEventRecord(ss->ev[5], s2)));
+    XT_TRY(cuda_ok(cudaStreamWaitEvent(s, ss->ev[5], 0)));
+  }
   return xt_embedding_bwd(ids, b.dh, prm->dE, c.learned_pos ? prm->dP : nullptr, T, int(m.S), d, m.V, XT_F32, m.gdt,
                           b.ws_emb, 1, stream);
+}
+
+int xt_block_set_overlap(int on) {
+  XT_REQUIRE(on == 0 || on == 1, "xt_block_set_overlap: on must be 0 or 1");
+  g_overlap = on;
+  return XT_OK;
 }
 
 int xt_block_zero_grads(const xt_block_config* cfg, const xt_block_params* prm, void* stream) {

@@ -135,6 +135,7 @@ _SIGS = {
     "xt_matmul_workspace_size": [C.POINTER(MatmulDesc), _SZP],
     "xt_gemm_set_schedule": [_I],
     "xt_gemm_set_pairing": [_I],
+    "xt_block_set_overlap": [_I],
     "xt_gemm_set_tile": [_I],
     "xt_quantize_fp8_workspace_size": [_I64, _SZP],
     "xt_quantize_fp8": [_VP, _I64, _I, _VP, _VP, _VP, C.c_size_t, _VP],
@@ -278,6 +279,11 @@ def gemm_set_schedule(mode: int):
 def gemm_set_pairing(mode: int):
     """0 model's choice, 1 never the paired-CTA kernel, 2 the paired kernel wherever allowed."""
     call("xt_gemm_set_pairing", int(mode))
+
+
+def block_set_overlap(on: int):
+    """1 (default): the block backward's weight-gradient GEMMs on a second stream; 0: one stream."""
+    call("xt_block_set_overlap", int(on))
 
 
 def ce_set_split(cl: int, nb: int):
