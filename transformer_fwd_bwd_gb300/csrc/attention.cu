@@ -42,7 +42,6 @@ constexpr int BT = 128;                    // query / key tile
 constexpr int kThreadsBwd = 320;
 constexpr int TILE = BT * 128;             // one 128-row × 64-element bf16 tile: 16 KB
 constexpr int PT = 2 * TILE;               // 128 × 128 bf16 operand: two 64-wide K chunks
-constexpr int RING = 3;                    // K / V slots of the query-tile backward kernel
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.f;            // log2 growth of the running max that forces a rescale
@@ -872,62 +871,68 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   }
 }
 
-struct QSmem {
+// dQ with two streams per CTA: one 128-query tile per work item, its key tiles split between the
+// streams (stream 0 the even ones, stream 1 the odd ones).  Each stream has an MMA issuer (warps
+// 1 / 2), four row warps (4–7 / 8–11: one query row per thread, all 128 key columns), a TMEM
+// buffer that holds S and then dP of its current key tile, a dQ accumulator, and a dS tile in
+// shared memory; the Q / dO tiles and a three-slot K / V ring (tiles in key order, filled by
+// warp 0) are shared.  Per key tile: S = Q Kᵀ; the rows load S and form P = 2^(S·sc − lse2)
+// (masked), in registers; dP = dO Vᵀ into the same buffer; the rows form dS = P ∘ (dP − D), 32
+// columns at a time, into the stream's dS tile; dQ_s += dS K.  One stream's MMA round trips
+// overlap the other's row work.  At the end of an item stream 0's rows add the two accumulators
+// (in stream order, so the sum does not depend on timing), scale by α and store dQ.
+constexpr int kThreadsQ2 = 384;
+constexpr int Q2_RING = 3;
+constexpr uint32_t kQ2RegsCtl = 72, kQ2RegsRows = 216;  // 128·72 + 256·216 = 384·168
+struct Q2Smem {
   static constexpr int Q = 0;
   static constexpr int DO = Q + TILE;
-  static constexpr int KV = DO + TILE;           // RING slots × (K tile, V tile)
-  static constexpr int DS = KV + RING * 2 * TILE;
-  static constexpr int STAGE = DS + 2 * PT;      // 4 warps × 4 KB
-  static constexpr int BARS = STAGE + 4 * 4096;
-  static constexpr int BYTES = 1024 + BARS + 256;
+  static constexpr int KV = DO + TILE;               // Q2_RING slots × (K tile, V tile)
+  static constexpr int DS = KV + Q2_RING * 2 * TILE;  // 2 streams × dS [queries × keys]
+  static constexpr int BARS = DS + 2 * PT;
+  static constexpr int BYTES = 1024 + BARS + 512;
 };
 
-// dQ for one 128-query tile per work item: thread = query row; S = Q Kᵀ and dP = dO Vᵀ per key
-// tile, P = 2^(S·sc − lse2) (0 where key > query or key ≥ S), dS = P ∘ (dP − D);
-// dQ += dS K accumulates in TMEM and is scaled by α on the way out.
-__global__ void __launch_bounds__(kThreadsBwd, 1)
+__global__ void __launch_bounds__(kThreadsQ2, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   pdl_begin();
   constexpr uint32_t IDESC_S = instr_desc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_O = instr_desc_bf16(128, HD, false, true);
-  constexpr uint32_t TCOLS = 512;  // S0 [0,128), S1 [128,256), dP [256,384), dQ [384,448)
+  constexpr uint32_t TCOLS = 512;  // stream s: S / dP [256 s, 256 s + 128), dQ [256 s + 128, 256 s + 192)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QSmem::BARS);
+  // q_full, q_empty, kv_full[3], kv_empty[3], per stream s (8 + 8 s): s_full, s_read, dp_full,
+  // ds_full, ds_free, acc_full, mma_done; acc_free
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Q2Smem::BARS);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;            // [RING]
-  uint64_t* kv_empty = kv_full + RING;     // [RING]
-  uint64_t* s_full = kv_empty + RING;      // [2]
-  uint64_t* s_free = s_full + 2;           // [2]
-  uint64_t* dp_full = s_free + 2;
-  uint64_t* dp_free = dp_full + 1;
-  uint64_t* ds_full = dp_free + 1;         // [2]
-  uint64_t* ds_free = ds_full + 2;         // [2]
-  uint64_t* mma_done = ds_free + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* kv_full = bars + 2;
+  uint64_t* kv_empty = bars + 5;
+  uint64_t* acc_free = bars + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
-    mbar_init(smem_u32(q_empty), 1);
-    for (int s = 0; s < RING; ++s) {
+    mbar_init(smem_u32(q_empty), 2);  // one arrival per stream
+    for (int s = 0; s < Q2_RING; ++s) {
       mbar_init(smem_u32(&kv_full[s]), 1);
       mbar_init(smem_u32(&kv_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&s_full[b]), 1);
-      mbar_init(smem_u32(&s_free[b]), 8);
-      mbar_init(smem_u32(&ds_full[b]), 8);
-      mbar_init(smem_u32(&ds_free[b]), 1);
+    for (int st = 0; st < 2; ++st) {
+      uint64_t* b = bars + 8 + 8 * st;
+      mbar_init(smem_u32(&b[0]), 1);  // s_full
+      mbar_init(smem_u32(&b[1]), 4);  // s_read
+      mbar_init(smem_u32(&b[2]), 1);  // dp_full
+      mbar_init(smem_u32(&b[3]), 4);  // ds_full
+      mbar_init(smem_u32(&b[4]), 1);  // ds_free
+      mbar_init(smem_u32(&b[5]), 1);  // acc_full
+      mbar_init(smem_u32(&b[6]), 1);  // mma_done
     }
-    mbar_init(smem_u32(dp_full), 1);
-    mbar_init(smem_u32(dp_free), 8);
-    mbar_init(smem_u32(mma_done), 1);
+    mbar_init(smem_u32(acc_free), 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -936,6 +941,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    prefetch_tmap(&tmDQ);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TCOLS);
@@ -945,18 +951,18 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const uint32_t tDP = tbase + 256, tDQ = tbase + 384;
 
   auto give_up = [&]() {
     *abort_flag = 1;
     flag_error(p.flag, XT_DEVERR_TIMEOUT);
   };
-
-  if (warp == 0) {
-    if (lane == 0) {
+  const int wg = warp >> 2;
+  if (wg == 0) {
+    regs_dec<kQ2RegsCtl>();
+    if (warp == 0 && lane == 0) {
       // -------------------------------------------------------------- TMA producer
-      int ks = 0, nk = 0, nqi = 0;
-      uint32_t kph = 0;
+      int nqi = 0;
+      uint32_t gt = 0;  // K / V tiles loaded so far
       bool ok = true;
       #pragma unroll 1
       for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
@@ -965,109 +971,110 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
         if (!mbar_wait(smem_u32(q_empty), (nqi & 1) ^ 1, p.wait_ns)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full), 2 * TILE);
-        tma_load_4d(sb + QSmem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
-        tma_load_4d(sb + QSmem::DO, &tmDO, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
+        tma_load_4d(sb + Q2Smem::Q, &tmQ, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
+        tma_load_4d(sb + Q2Smem::DO, &tmDO, smem_u32(q_full), 0, it.h, it.qt * BT, it.b);
         ++nqi;
         #pragma unroll 1
-        for (int j = 0; j < it.nkv; ++j) {
-          if (*abort_flag || !mbar_wait(smem_u32(&kv_empty[ks]), kph ^ 1, p.wait_ns)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&kv_full[ks]);
+        for (int j = 0; j < it.nkv; ++j, ++gt) {
+          const int slot = int(gt % Q2_RING);
+          if (*abort_flag || !mbar_wait(smem_u32(&kv_empty[slot]), ((gt / Q2_RING) & 1) ^ 1, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&kv_full[slot]);
           mbar_expect_tx(fb, 2 * TILE);
-          const uint32_t dst = sb + QSmem::KV + ks * 2 * TILE;
+          const uint32_t dst = sb + Q2Smem::KV + uint32_t(slot) * 2 * TILE;
           tma_load_4d(dst, &tmK, fb, 0, it.h, j * BT, it.b);
           tma_load_4d(dst + TILE, &tmV, fb, 0, it.h, j * BT, it.b);
-          ++nk;
-          if (++ks == RING) { ks = 0; kph ^= 1; }
         }
       }
       if (!ok) give_up();
+      // bounded wait for the fills that may still be in flight
       bool drained = true;
       if (nqi > 0) drained &= mbar_wait(smem_u32(q_full), (nqi - 1) & 1);
-      for (int n = 0; n < (nk < RING ? nk : RING); ++n) {
-        if (--ks < 0) { ks = RING - 1; kph ^= 1; }
-        drained &= mbar_wait(smem_u32(&kv_full[ks]), kph);
+      for (uint32_t n = 0; n < (gt < Q2_RING ? gt : uint32_t(Q2_RING)); ++n) {
+        const uint32_t g = gt - 1 - n;
+        drained &= mbar_wait(smem_u32(&kv_full[g % Q2_RING]), (g / Q2_RING) & 1);
       }
       if (!drained) give_up();
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------------------- MMA issuer
-      int nqi = 0;
-      uint32_t g = 0;  // key tiles processed so far
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+      // -------------------------------------------------------------- MMA issuer, stream warp − 1
+      const int st = warp - 1;
+      uint64_t* b = bars + 8 + 8 * st;
+      const uint32_t tS = tbase + uint32_t(256 * st), tDQ = tS + 128;
+      const uint32_t dsb = sb + Q2Smem::DS + uint32_t(st) * PT;
+      uint32_t t = 0, gt0 = 0;  // this stream's tiles so far; K / V tiles of the items before this one
+      int k = 0;                // items so far
       bool ok = true;
-      auto kv_addr = [&](uint32_t gg) { return sb + QSmem::KV + uint32_t(gg % RING) * 2 * TILE; };
-      auto issue_s = [&](uint32_t gg) -> bool {
-        const int b = int(gg & 1);
-        const uint32_t u = gg >> 1;
-        if (!mbar_wait(smem_u32(&kv_full[gg % RING]), (gg / RING) & 1, p.wait_ns) ||
-            !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          tc_mma<false>(tbase + uint32_t(b * 128), smem_desc(sb + QSmem::Q + kk * 32, 16, 1024),
-                        smem_desc(kv_addr(gg) + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(smem_u32(&s_full[b]));
-        return true;
-      };
-      auto issue_dp = [&](uint32_t gg) -> bool {
-        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1, p.wait_ns)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          tc_mma<false>(tDP, smem_desc(sb + QSmem::DO + kk * 32, 16, 1024),
-                        smem_desc(kv_addr(gg) + TILE + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(smem_u32(dp_full));
-        return true;
-      };
-      auto issue_dq = [&](uint32_t gg, bool first) -> bool {
-        const int b = int(gg & 1);
-        if (!mbar_wait(smem_u32(&ds_full[b]), (gg >> 1) & 1, p.wait_ns)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K (K tile read MN-major)
-          tc_mma<false>(tDQ, smem_desc(sb + QSmem::DS + b * PT + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
-                        smem_desc(kv_addr(gg) + kk * 2048, TILE, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&ds_free[b]));
-        tc_commit(smem_u32(&kv_empty[gg % RING]));
-        return true;
-      };
       #pragma unroll 1
       for (int r = 0; r * int(gridDim.x) < p.items && ok && !*abort_flag; ++r) {
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_full), nqi & 1, p.wait_ns)) { ok = false; break; }
-        ++nqi;
+        if (!mbar_wait(smem_u32(q_full), k & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t g0 = g;
-        if (!issue_s(g0) || !issue_dp(g0)) { ok = false; break; }
+        bool first = true;
         #pragma unroll 1
-        for (int j = 0; j < it.nkv; ++j) {
-          // next tile's dP goes ahead of this tile's dQ (see the key-tile kernel)
-          const uint32_t gg = g0 + uint32_t(j);
-          if (*abort_flag) { ok = false; break; }
-          if (j + 1 < it.nkv && !issue_s(gg + 1)) { ok = false; break; }
-          if (j + 1 < it.nkv && !issue_dp(gg + 1)) { ok = false; break; }
-          if (!issue_dq(gg, j == 0)) { ok = false; break; }
+        for (int j = st; j < it.nkv; j += 2, ++t) {
+          const uint32_t gt = gt0 + uint32_t(j);
+          const int slot = int(gt % Q2_RING);
+          const uint32_t kvs = sb + Q2Smem::KV + uint32_t(slot) * 2 * TILE;
+          if (*abort_flag || !mbar_wait(smem_u32(&kv_full[slot]), (gt / Q2_RING) & 1, p.wait_ns)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)  // S = Q Kᵀ
+            tc_mma<false>(tS, smem_desc(sb + Q2Smem::Q + kk * 32, 16, 1024), smem_desc(kvs + kk * 32, 16, 1024),
+                          IDESC_S, kk > 0 ? 1u : 0u);
+          tc_commit(smem_u32(&b[0]));
+          if (!mbar_wait(smem_u32(&b[1]), t & 1, p.wait_ns)) { ok = false; break; }  // the rows have loaded S
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)  // dP = dO Vᵀ into the same columns
+            tc_mma<false>(tS, smem_desc(sb + Q2Smem::DO + kk * 32, 16, 1024),
+                          smem_desc(kvs + TILE + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          tc_commit(smem_u32(&b[2]));
+          if (!mbar_wait(smem_u32(&b[3]), t & 1, p.wait_ns)) { ok = false; break; }  // dS written, dP read
+          if (first && !mbar_wait(smem_u32(acc_free), (k & 1) ^ 1, p.wait_ns)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BT / 16; ++kk)  // dQ_s += dS K (K tile read MN-major)
+            tc_mma<false>(tDQ, smem_desc(dsb + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
+                          smem_desc(kvs + kk * 2048, TILE, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&b[4]));
+          tc_commit(smem_u32(&kv_empty[slot]));
+          first = false;
         }
         if (!ok) break;
-        tc_commit(smem_u32(q_empty));
-        g = g0 + uint32_t(it.nkv);
+        // this stream is done with the item: its accumulator is final, Q and dO are free to it
+        if (!first) {
+          tc_commit(smem_u32(&b[5]));
+          tc_commit(smem_u32(q_empty));
+        } else {
+          mbar_arrive(smem_u32(&b[5]));
+          mbar_arrive(smem_u32(q_empty));
+        }
+        gt0 += uint32_t(it.nkv);
+        ++k;
       }
       if (!ok) give_up();
       // every MMA issued has completed (also after a give-up) before TMEM is released
-      tc_commit(smem_u32(mma_done));
-      if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
+      tc_commit(smem_u32(&b[6]));
+      if (!mbar_wait(smem_u32(&b[6]), 0)) give_up();
     }
   } else {
+    regs_inc<kQ2RegsRows>();
     // ---------------------------------------------------------------- P / dS rows, epilogue
+    const int st = wg - 1;
+    uint64_t* b = bars + 8 + 8 * st;
+    const uint32_t tS = tbase + uint32_t(256 * st);
+    const uint32_t dsb = sb + Q2Smem::DS + uint32_t(st) * PT;
     const int qw = warp & 3;
-    const int half = (warp - 2) >> 2;  // this warp's 64 key columns: [64·half, 64·half + 64)
-    const int col0 = 64 * half;
-    const int rr = qw * 32 + lane;     // query row within the tile
+    const int rr = qw * 32 + lane;  // query row within the tile
     const uint32_t lane_off = uint32_t(qw * 32) << 16;
-    const uint32_t stage = sb + QSmem::STAGE + uint32_t(qw) * 4096;
-    uint32_t g = 0;
+    // stream 0 stages α·dQ in its warp's own 32 rows of its dS tile (chunk 0)
+    const uint32_t stage = sb + Q2Smem::DS + uint32_t(qw) * 4096;
+    uint32_t t = 0;
+    int k = 0;
     #pragma unroll 1
     for (int r = 0; r * int(gridDim.x) < p.items; ++r) {
       const int i = snake_item(r);
@@ -1080,71 +1087,99 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       const float Dr = row < p.S ? p.D[bh * p.S + row] : 0.f;
       bool ok = true;
       #pragma unroll 1
-      for (int j = 0; j < it.nkv; ++j, ++g) {
-        const int b = int(g & 1);
-        const uint32_t u = g >> 1;
-        if (!warp_wait(smem_u32(&s_full[b]), u & 1, p.wait_ns)) { ok = false; break; }
+      for (int j = st; j < it.nkv; j += 2, ++t) {
+        if (!warp_wait(smem_u32(&b[0]), t & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
-        uint32_t r[64];  // this warp's 64 columns of the row
+        uint32_t pr[128];  // S, then P, of this row's 128 keys
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tmem_ld32(tbase + lane_off + uint32_t(b * 128 + col0 + c * 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tS + lane_off + uint32_t(c * 32), *reinterpret_cast<uint32_t(*)[32]>(pr + 32 * c));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_free[b]));
-        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT - col0;
+        if (lane == 0) mbar_arrive(smem_u32(&b[1]));
+        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BT;  // keys at or past lim are masked
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float e = ex2(fmaf(__uint_as_float(r[c]), p.sc, -lse2));
-          r[c] = __float_as_uint(c < lim ? e : 0.f);
+        for (int c = 0; c < 128; ++c) {
+          const float e = ex2(fmaf(__uint_as_float(pr[c]), p.sc, -lse2));
+          pr[c] = __float_as_uint(c < lim ? e : 0.f);
         }
-        keep_before(r);
-        if (!warp_wait(smem_u32(dp_full), g & 1, p.wait_ns) || !warp_wait(smem_u32(&ds_free[b]), (u & 1) ^ 1, p.wait_ns)) {
+        keep_before(pr);
+        if (!warp_wait(smem_u32(&b[2]), t & 1, p.wait_ns) || !warp_wait(smem_u32(&b[4]), (t & 1) ^ 1, p.wait_ns)) {
           ok = false;
           break;
         }
+        if (st == 0 && j == 0) {  // the previous item's dQ stores have read this warp's rows of the tile
+          if (lane == 0) bulk_wait_read_0();
+          __syncwarp();
+        }
         tc_fence_after();
-        const uint32_t dsb = sb + QSmem::DS + b * PT;
-        uint32_t d[64];  // both dP chunks in flight before one wait
-        tmem_ld32(tDP + lane_off + uint32_t(col0), *reinterpret_cast<uint32_t(*)[32]>(d));
-        tmem_ld32(tDP + lane_off + uint32_t(col0 + 32), *reinterpret_cast<uint32_t(*)[32]>(d + 32));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(dp_free));
 #pragma unroll
-        for (int un = 0; un < 8; ++un) {
-          float ds[8];
+        for (int c4 = 0; c4 < 4; ++c4) {  // dS = P ∘ (dP − D), 32 keys at a time
+          uint32_t d[32];
+          tmem_ld32(tS + lane_off + uint32_t(c4 * 32), d);
+          tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int cc = un * 8 + t;
-            ds[t] = __uint_as_float(r[cc]) * (__uint_as_float(d[cc]) - Dr);
+          for (int u = 0; u < 4; ++u) {
+            float ds[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int cc = c4 * 32 + u * 8 + e;
+              ds[e] = __uint_as_float(pr[cc]) * (__uint_as_float(d[u * 8 + e]) - Dr);
+            }
+            st_shared_v4(swz(dsb, rr, c4 >> 1, (c4 & 1) * 4 + u), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
+                         pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
           }
-          st_shared_v4(swz(dsb, rr, half, un), pack_bf16(ds[0], ds[1]), pack_bf16(ds[2], ds[3]),
-                       pack_bf16(ds[4], ds[5]), pack_bf16(ds[6], ds[7]));
         }
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ds_full[b]));
+        if (lane == 0) mbar_arrive(smem_u32(&b[3]));
       }
       if (!ok) {
         if (lane == 0) give_up();
         break;
       }
-      // ---- epilogue: α·dQ (one warp per quadrant; the other half's next arrival on ds_full
-      // comes after this, so the next item's first dQ MMA cannot overwrite it before it is read)
-      if (half != 0) continue;
-      const uint32_t pg = g - 1;
-      if (!warp_wait(smem_u32(&ds_free[pg & 1]), (pg >> 1) & 1, p.wait_ns)) {
-        if (lane == 0) give_up();
-        break;
+      if (st == 0) {
+        // ---- epilogue: α·(dQ_0 + dQ_1) once both streams are done with the item
+        uint64_t* b1 = bars + 16;
+        if (!warp_wait(smem_u32(&b[5]), k & 1, p.wait_ns) || !warp_wait(smem_u32(&b1[5]), k & 1, p.wait_ns)) {
+          if (lane == 0) give_up();
+          break;
+        }
+        tc_fence_after();
+        uint32_t o[64];
+        tmem_ld32(tbase + 128 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld32(tbase + 160 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+        tmem_ld_wait();
+        if (it.nkv > 1) {  // stream 1 holds the odd key tiles' sum
+          uint32_t o1[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld32(tbase + 256 + 128 + uint32_t(c * 32) + lane_off, o1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[c * 32 + e] = __float_as_uint(__uint_as_float(o[c * 32 + e]) + __uint_as_float(o1[e]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(acc_free));
+#pragma unroll
+        for (int un = 0; un < 8; ++un)
+          st_shared_v4(stage + uint32_t(lane) * 128 + (uint32_t(un ^ (lane & 7)) << 4),
+                       pack_bf16(__uint_as_float(o[8 * un]) * p.alpha, __uint_as_float(o[8 * un + 1]) * p.alpha),
+                       pack_bf16(__uint_as_float(o[8 * un + 2]) * p.alpha, __uint_as_float(o[8 * un + 3]) * p.alpha),
+                       pack_bf16(__uint_as_float(o[8 * un + 4]) * p.alpha, __uint_as_float(o[8 * un + 5]) * p.alpha),
+                       pack_bf16(__uint_as_float(o[8 * un + 6]) * p.alpha, __uint_as_float(o[8 * un + 7]) * p.alpha));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&tmDQ, stage, 0, it.h, it.qt * BT + qw * 32, it.b);
+          bulk_commit();
+        }
       }
-      tc_fence_after();
-      if (lane == 0) bulk_wait_read_0();
-      __syncwarp();
-      store_rows(tDQ + lane_off, p.alpha, stage, lane, &tmDQ, it.h, it.qt * BT + qw * 32, it.b);
-      tc_fence_before();
+      ++k;
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -1302,10 +1337,21 @@ int xt_attention_bwd(const void* q, const void* k, const void* v, int64_t ld_qkv
   const int grid = p.items < num_sms() ? p.items : num_sms();
   static bool kv_set = false, q_set = false;
   XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_kv_kernel), KvSmem::BYTES, kv_set, "xt_attention_bwd"));
-  XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_q_kernel), QSmem::BYTES, q_set, "xt_attention_bwd"));
+  XT_TRY(set_smem(reinterpret_cast<const void*>(attn_bwd_q_kernel), Q2Smem::BYTES, q_set, "xt_attention_bwd"));
+  static int q_regs = -1;
+  if (q_regs < 0) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, attn_bwd_q_kernel) != cudaSuccess)
+      return fail(XT_ERR_CUDA, "xt_attention_bwd: cudaFuncGetAttributes failed");
+    q_regs = fa.numRegs;
+  }
+  // the dQ kernel's register split (kQ2RegsCtl + 2 × kQ2RegsRows per 128 threads) adds up to the
+  // 168 per thread it is launched with
+  if (q_regs != 168)
+    return fail(XT_ERR_UNSUPPORTED, "xt_attention_bwd: dQ kernel built with %d registers, not 168", q_regs);
   launch(attn_bwd_kv_kernel, grid, kThreadsBwd, KvSmem::BYTES, s, tq, tk, tv, tdo, tdk, tdv, p);
   XT_TRY(check_launch("xt_attention_bwd (dK, dV)"));
-  launch(attn_bwd_q_kernel, grid, kThreadsBwd, QSmem::BYTES, s, tq, tk, tv, tdo, tdq, p);
+  launch(attn_bwd_q_kernel, grid, kThreadsQ2, Q2Smem::BYTES, s, tq, tk, tv, tdo, tdq, p);
   return check_launch("xt_attention_bwd (dQ)");
 }
 
