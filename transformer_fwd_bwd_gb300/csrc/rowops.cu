@@ -1042,6 +1042,13 @@ __global__ void __launch_bounds__(kCeFusedThreads) ce_fused_kernel(const T* x, c
       for (int e = 0; e < VW; ++e) m = fmaxf(m, v[e]);
     }
     m = block_reduce(m, true);
+    // the block's next row is asked of L2 now, so its copy into shared memory after this row's
+    // two passes over shared memory and its gradient stores does not wait on DRAM
+    if (r + gridDim.x < rows) {
+      const T* xn = x + (r + gridDim.x) * V;
+      for (int64_t j = int64_t(threadIdx.x) * 8; j < nvec; j += int64_t(kCeFusedThreads) * 8)
+        prefetch_l2(reinterpret_cast<const uint4*>(xn) + j);
+    }
     // 2. Σ exp(x − max) from shared memory
     const float ml = m * kLog2e;
     float s = 0.f;
@@ -1180,7 +1187,8 @@ constexpr int kEmbThreads = 512;
 
 // dE[v] (+)= Σ_{t: ids[t] = v} dh[t], the sum formed in float32 in ascending t and then added
 // to dE[v].  Block b owns the ids [b·per, (b+1)·per): it lists, in ascending t, the tokens
-// whose id falls in its range (ballot compaction over all T ids), then warp w takes the ids
+// whose id falls in its range (each warp compacts a contiguous range of t with ballots, the
+// warps' lists joined in warp order: two block barriers in all), then warp w takes the ids
 // v0 + w, v0 + w + warps, …: for each it walks the list in order and sums the rows of the
 // tokens with that id, 8 columns per lane per pass (lane-interleaved, coalesced).  Ids outside
 // [0, V) set XT_DEVERR_INDEX (block 0) and are skipped.  No sort and no atomics.
@@ -1198,49 +1206,52 @@ __global__ void __launch_bounds__(kEmbThreads) embed_bwd_kernel(const int32_t* _
   constexpr int NW = kEmbThreads / 32;
   const int64_t v0 = int64_t(blockIdx.x) * per;
   const int64_t v1 = v0 + per < V ? v0 + per : V;
-  if (threadIdx.x == 0) total = 0;
-  // every id this thread inspects is loaded first (one memory latency, not one per round)
-  constexpr int kPer = kSortMax / kEmbThreads;
+  // Warp w lists the tokens of its own contiguous range [w·cw, (w + 1)·cw) that fall in this
+  // block's id range: a count pass, one barrier for the warps' offsets (ranges in warp order, so
+  // the list is in ascending t), then a write pass; the ids are loaded once, before either pass.
+  const int cw = ((T_ + NW - 1) / NW + 31) & ~31;
+  const int t_begin = w * cw;
+  constexpr int kPer = kSortMax / kEmbThreads;  // rounds of 32 ids a warp can have
   int32_t idv[kPer];
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
-    const int t = r * kEmbThreads + int(threadIdx.x);
-    idv[r] = t < T_ ? __ldg(ids + t) : 0;
+    const int t = t_begin + r * 32 + lane;
+    idv[r] = (r * 32 < cw && t < T_) ? __ldg(ids + t) : -1;
   }
-  __syncthreads();
+  auto match = [&](int r) {
+    const int32_t id = idv[r];
+    return id >= 0 && int64_t(id) < V && int64_t(id) >= v0 && int64_t(id) < v1;
+  };
+  int cnt = 0;
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
-    const int base = r * kEmbThreads;
-    if (base >= T_) break;
-    const int t = base + int(threadIdx.x);
-    bool m = false;
-    int32_t id = 0;
-    if (t < T_) {
-      id = idv[r];
-      const bool bad = id < 0 || int64_t(id) >= V;
-      if (bad && blockIdx.x == 0) flag_error(flag, XT_DEVERR_INDEX);
-      m = !bad && int64_t(id) >= v0 && int64_t(id) < v1;
-    }
-    const unsigned bal = __ballot_sync(0xffffffffu, m);
-    if (lane == 0) warp_base[w] = __popc(bal);
-    __syncthreads();
-    if (threadIdx.x == 0) {  // exclusive prefix over the warps, in warp order
-      int acc = total;
-      for (int i = 0; i < NW; ++i) {
-        const int c = warp_base[i];
-        warp_base[i] = acc;
-        acc += c;
-      }
-      total = acc;
-    }
-    __syncthreads();
-    if (m) {
-      const int pos = warp_base[w] + __popc(bal & ((1u << lane) - 1u));
-      lt[pos] = t;
-      lid[pos] = id;
-    }
-    __syncthreads();
+    if (r * 32 >= cw) break;
+    const int t = t_begin + r * 32 + lane;
+    if (blockIdx.x == 0 && t < T_ && (idv[r] < 0 || int64_t(idv[r]) >= V)) flag_error(flag, XT_DEVERR_INDEX);
+    cnt += __popc(__ballot_sync(0xffffffffu, match(r)));
   }
+  if (lane == 0) warp_base[w] = cnt;
+  __syncthreads();
+  int pos = 0, all = 0;
+  for (int i = 0; i < NW; ++i) {
+    const int c = warp_base[i];
+    pos += i < w ? c : 0;
+    all += c;
+  }
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    if (r * 32 >= cw) break;
+    const bool m = match(r);
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    if (m) {
+      const int k = pos + __popc(bal & ((1u << lane) - 1u));
+      lt[k] = t_begin + r * 32 + lane;
+      lid[k] = idv[r];
+    }
+    pos += __popc(bal);
+  }
+  if (threadIdx.x == 0) total = all;
+  __syncthreads();
   const int count = total;
   for (int64_t v = v0 + w; v < v1; v += NW) {
     for (int64_t c0 = 0; c0 < d; c0 += 32 * 8) {
