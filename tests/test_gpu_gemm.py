@@ -222,10 +222,10 @@ def test_matmul_split_k(ab, c, M, N, K, schedule):
     assert xt.device_errors() == 0
 
 
-# (M, N, K, trans_a): the weight-gradient layout; ragged M, N and K; one output tile over
-# 160 (bf16) k-blocks, so every CTA holds a piece of it and the tile's first CTA adds 151
-# partials; a tile count that is not a multiple of the SMs with short K.
-SK_CASES = [(768, 768, 8192, 1), (200, 136, 4096, 1), (128, 256, 10240, 0), (1000, 776, 328, 0)]
+# (M, N, K, trans_a): the weight-gradient layout; ragged M, N and K; a few output tiles over
+# a long K, so every CTA holds a piece of one and a tile's first CTA adds many partials; a tile
+# count that is not a multiple of the SMs with short K (enough k-blocks for two-way slices).
+SK_CASES = [(768, 768, 8192, 1), (200, 136, 4096, 1), (128, 256, 10240, 0), (1000, 776, 656, 0)]
 
 
 @pytest.mark.parametrize("form", [3, 4])

@@ -28,7 +28,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Operand as the kernel sees it: `mn` rows (M or N) by K, either K contiguous (K-major) or
 // MN contiguous (MN-major), with two batch levels.
-int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn) {
+int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn, int k_atom_count) {
   auto enc = encode_fn();
   if (!enc) return fail(XT_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const int64_t e = kind == kTf32 ? 4 : kind == kFp8 ? 1 : 2;
@@ -46,7 +46,7 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn) {
     dims[0] = cuuint64_t(o.mn);
     dims[1] = cuuint64_t(o.K);
     box[0] = atom;
-    box[1] = atom;  // BK rows of K
+    box[1] = atom * uint32_t(k_atom_count);  // BK rows of K
   }
   dims[2] = cuuint64_t(o.batch_inner);
   dims[3] = cuuint64_t(o.batch_outer);
@@ -114,12 +114,12 @@ Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int c
   // MN-major (BN 128, 256), any multiple of 16 rows K-major (also BN 192)
   const int cands_pair[3] = {128, 192, 256};
   const int sms = num_sms();
-  const int bk = fp8 ? 128 : tf32 ? 32 : 64;
+  const int bk1 = fp8 ? 128 : tf32 ? 32 : 64;  // K elements per 128-byte atom
   const double per_sm = fp8 ? 22.4e12 : tf32 ? 5.6e12 : 11.2e12;
   const double e = fp8 ? 1.0 : tf32 ? 4.0 : 2.0;
   Choice best{fp8 ? cands_fp8[0] : tf32 ? cands_tf32[0] : cands_bf16[0], 1, 0, 0};
   double best_t = 1e300;
-  const int64_t kbt = ceil_div(K, bk);
+
   // forced modes: the forced kind of candidate first, whole tiles when it is not allowed
   auto weigh = [&](double t, int kind, int cg) {  // kind 1 tiles, 2 K split, 3 stream-K all units, 4 lockstep
     if (mode >= 2) t *= (kind == mode) ? 1e-6 : (kind == 1 ? 1.0 : 1e6);
@@ -138,6 +138,8 @@ Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int c
     const int units = cg == 1 ? sms : (pair_ok ? pair_capacity() : 0);
     if (units < 1) continue;
     const int bm = BM * cg;
+    const int bk = bk1 * k_atoms(cg);  // K per stage of this kernel
+    const int64_t kbt = ceil_div(K, bk);
     const int* c = cg == 2 ? cands_pair : fp8 ? cands_fp8 : tf32 ? cands_tf32 : cands_bf16;
     const int nc = cg == 2 ? 3 : fp8 || tf32 ? 2 : 4;
     const double rate = per_sm * cg;  // per unit
@@ -254,8 +256,8 @@ int run(const Problem& pb, cudaStream_t s) {
   memset(&tc2, 0, sizeof(tc2));
   if (pb.act == 1) XT_TRY(make_output_map(&tc2, pb.C2, true, pb.M, pb.N, pb.ldc, 1, 1, 0, 0));
   const int kind = pb.fp8 ? kFp8 : tf32 ? kTf32 : kBf16;
-  XT_TRY(make_operand_map(&ta, pb.A, kind, BM));
-  XT_TRY(make_operand_map(&tb, pb.B, kind, bn / cg));  // a pair's CTA stages half of B's rows
+  XT_TRY(make_operand_map(&ta, pb.A, kind, BM, k_atoms(cg)));
+  XT_TRY(make_operand_map(&tb, pb.B, kind, bn / cg, k_atoms(cg)));  // a pair's CTA stages half of B's rows
   // TMA epilogue for every output except a bf16 C that is accumulated into (TMA reduce-add is
   // used for float32 only; bf16 accumulation keeps the direct read-modify-write stores).  A K
   // split stores float32 partial tiles into [splits][M][N] slices instead.
@@ -275,7 +277,7 @@ int run(const Problem& pb, cudaStream_t s) {
   p.batch_inner = split ? ch.splits : pb.batch_inner;
   p.batches = split ? ch.splits : pb.batch_inner * pb.batch_outer;
   p.splitk = ch.splits;
-  const int bk = pb.fp8 ? 128 : tf32 ? 32 : 64;
+  const int bk = (pb.fp8 ? 128 : tf32 ? 32 : 64) * k_atoms(cg);
   p.kb_per_split = int(ceil_div(ceil_div(pb.K, bk), ch.splits));
   p.causal = pb.causal;
   p.accumulate = split ? 0 : pb.accumulate;

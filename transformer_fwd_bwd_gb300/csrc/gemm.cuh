@@ -59,7 +59,7 @@ constexpr int kSkMaxCtas = 256;
 constexpr size_t kSkFlagBytes = size_t(kSkMaxCtas) * 4 * sizeof(uint32_t);
 
 // kind: kBf16, kTf32 or kFp8 (element size 2, 4, 1)
-int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn);
+int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn, int k_atom_count);
 // The driver's cuTensorMapEncodeTiled (null when the driver does not provide it).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 int run(const Problem& pb, cudaStream_t s);

@@ -346,16 +346,23 @@ constexpr uint32_t tmem_cols() {
   return 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
 }
 
+// K per stage, in 128-byte swizzle atoms: a K-major operand is staged as that many chunks of
+// [rows × 128 B] (one TMA box each), an MN-major one as [BK rows × 128 B] chunks along MN.  The
+// paired kernel takes two (half the mbarrier round trips per tile, three stages); the single-CTA
+// kernel one (its wide tiles would keep only two stages of two).
+__host__ __device__ constexpr int k_atoms(int cg) { return cg == 2 ? 2 : 1; }
+
 // CG = 2: a CTA pair computes a (2·BM) × BN tile; each CTA stages its own BM rows of A and
 // BN / 2 rows of B.
 template <int KIND, int BN, int CG = 1>
 struct Cfg {
   static constexpr int E = KIND == kTf32 ? 4 : KIND == kFp8 ? 1 : 2;
-  static constexpr int BK = 128 / E;         // K elements per stage (one 128-byte row)
-  static constexpr int ATOM = 128 / E;       // MN elements per 128-byte swizzle row
+  static constexpr int KA = k_atoms(CG);     // 128-byte K atoms per stage
+  static constexpr int BK = KA * 128 / E;    // K elements per stage
+  static constexpr int ATOM = 128 / E;       // MN (or K) elements per 128-byte swizzle row
   static constexpr int UK = 32 / E;          // K per MMA instruction (32 bytes)
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN / CG * 128;
+  static constexpr int A_BYTES = BM * 128 * KA;
+  static constexpr int B_BYTES = BN / CG * 128 * KA;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
   static constexpr int STAGING_BYTES = 4 * 2 * 4096;  // 4 epilogue warps × 2 buffers × 32 rows × 128 B
@@ -600,14 +607,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_s = a_s + C_::A_BYTES;
           const int k0 = kb * BK;
           if constexpr (!A_MN) {
-            load(a_s, &tmA, fb, k0, ti.m0, ti.ozi, ti.ozo);
+#pragma unroll
+            for (int c = 0; c < C_::KA; ++c) load(a_s + c * (BM * 128), &tmA, fb, k0 + c * ATOM, ti.m0, ti.ozi, ti.ozo);
           } else {
 #pragma unroll
             for (int j = 0; j < BM / ATOM; ++j)
               load(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.ozi, ti.ozo);
           }
           if constexpr (!B_MN) {
-            load(b_s, &tmB, fb, k0, nb0, ti.ozi, ti.ozo);
+#pragma unroll
+            for (int c = 0; c < C_::KA; ++c) load(b_s + c * (BNH * 128), &tmB, fb, k0 + c * ATOM, nb0, ti.ozi, ti.ozo);
           } else {
 #pragma unroll
             for (int j = 0; j < BNH / ATOM; ++j)
@@ -665,10 +674,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_s = a_s + C_::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
+            // K-major: K step kk lies in atom kk / (ATOM / UK) at byte (kk % (ATOM / UK))·32
+            constexpr int PA = ATOM / UK;
             const uint64_t ad = A_MN ? smem_desc(a_s + kk * UK * 128, BK * 128, 1024)
-                                     : smem_desc(a_s + kk * UK * C_::E, 16, 1024);
+                                     : smem_desc(a_s + (kk / PA) * (BM * 128) + (kk % PA) * UK * C_::E, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(b_s + kk * UK * 128, BK * 128, 1024)
-                                     : smem_desc(b_s + kk * UK * C_::E, 16, 1024);
+                                     : smem_desc(b_s + (kk / PA) * (BNH * 128) + (kk % PA) * UK * C_::E, 16, 1024);
             tc_mma<KIND, CG>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
           }
           any = true;
