@@ -81,12 +81,14 @@ int make_operand_map(CUtensorMap* tm, const Operand& o, int kind, int box_mn, in
 //
 // The constants were fitted to CUDA-graph timings of the 12-layer stack's fifteen GEMM shapes
 // under every (kernel, tile width, schedule) combination on a GB300: the model's pick is then
-// within 0.6 µs of the fastest measured one on each shape.
+// within 0.6 µs of the fastest measured one on each shape.  The paired kernel's factors were
+// raised once it staged two K atoms per stage (8192 × 2304 × 768 in whole 256-wide tiles and
+// 8192 × 768 × 2304 in whole 192-wide tiles, graph-timed, give ≈ 1.15 and ≈ 1.0).
 static double tile_eff(int bn) { return bn >= 256 ? 1.0 : bn >= 192 ? 0.95 : bn >= 128 ? 0.64 : 0.35; }
 // The same for the paired kernel's 256-row tiles (relative to the single-CTA BN 256 rate):
 // each CTA stages 128 rows of A and bn / 2 rows of B per k-block, 2/3 of the single kernel's
 // bytes per FLOP at bn 256, with six pipeline stages instead of four.
-static double pair_eff(int bn) { return bn >= 256 ? 1.08 : bn >= 192 ? 0.9 : 0.7; }
+static double pair_eff(int bn) { return bn >= 256 ? 1.15 : bn >= 192 ? 1.0 : 0.75; }
 
 // Schedule override (xt_gemm_set_schedule): 0 the model's choice, 1 whole tiles only, 2 a K
 // split where one is allowed, 3 stream-K over every SM where allowed, 4 stream-K in lockstep
