@@ -135,6 +135,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// Bounded wait that polls with the non-blocking test_wait: the waiting thread sees the phase
+// flip on its next poll instead of after a suspended try_wait wakes, for the MMA issuer's waits
+// on landed operand stages (a few per tile, each on the tensor core's critical path).
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c0, int c1,
                                             int c2, int c3) {
   asm volatile(
@@ -668,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tbase + uint32_t(ab * BN);
         bool ok = true;
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
-          if (*abort_flag || !mbar_wait(smem_u32(&full[stage]), phase, p.wait_ns)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait_spin(smem_u32(&full[stage]), phase, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
           const uint32_t b_s = a_s + C_::A_BYTES;
