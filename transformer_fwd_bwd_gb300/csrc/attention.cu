@@ -252,8 +252,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       uint32_t g = 0;  // score tiles issued so far (phases of the single S and P buffers)
       bool ok = true;
       auto issue_pv = [&](uint32_t gg, bool first) -> bool {
-        if (!mbar_wait(smem_u32(p_full), gg & 1, p.wait_ns)) return false;
-        if (!mbar_wait(smem_u32(&v_full[vs]), vph, p.wait_ns)) return false;
+        if (!mbar_wait_spin(smem_u32(p_full), gg & 1, p.wait_ns)) return false;
+        if (!mbar_wait_spin(smem_u32(&v_full[vs]), vph, p.wait_ns)) return false;
         tc_fence_after();
         const uint32_t ps = base + FwdSmem::P;
         const uint32_t vsm = base + FwdSmem::V + vs * TILE;
@@ -273,13 +273,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const int i = vitem(r, vc);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_full), nqi & 1, p.wait_ns)) { ok = false; break; }
+        if (!mbar_wait_spin(smem_u32(q_full), nqi & 1, p.wait_ns)) { ok = false; break; }
         ++nqi;
         tc_fence_after();
         #pragma unroll 1
         for (int j = 0; j < it.nkv; ++j, ++g) {
-          if (*abort_flag || !mbar_wait(smem_u32(&k_full[ks]), kph, p.wait_ns) ||
-              !mbar_wait(smem_u32(s_free), (g & 1) ^ 1, p.wait_ns)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait_spin(smem_u32(&k_full[ks]), kph, p.wait_ns) ||
+              !mbar_wait_spin(smem_u32(s_free), (g & 1) ^ 1, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t ksm = base + FwdSmem::K + ks * TILE;
 #pragma unroll
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       auto issue_s = [&](uint32_t gg) -> bool {  // Sᵀ = K Qᵀ into buffer gg & 1
         const int b = int(gg & 1);
         const uint32_t u = gg >> 1;
-        if (!mbar_wait(smem_u32(&qd_full[b]), u & 1, p.wait_ns) || !mbar_wait(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) return false;
+        if (!mbar_wait_spin(smem_u32(&qd_full[b]), u & 1, p.wait_ns) || !mbar_wait_spin(smem_u32(&s_free[b]), (u & 1) ^ 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dp = [&](uint32_t gg) -> bool {  // dPᵀ = V dOᵀ
-        if (!mbar_wait(smem_u32(dp_free), (gg & 1) ^ 1, p.wait_ns)) return false;
+        if (!mbar_wait_spin(smem_u32(dp_free), (gg & 1) ^ 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dv = [&](uint32_t gg, bool first) -> bool {
-        if (!mbar_wait(smem_u32(p_full), gg & 1, p.wait_ns)) return false;
+        if (!mbar_wait_spin(smem_u32(p_full), gg & 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)  // dV += Pᵀ dO (dO tile read MN-major)
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         return true;
       };
       auto issue_dk = [&](uint32_t gg, bool first) -> bool {
-        if (!mbar_wait(smem_u32(ds_full), gg & 1, p.wait_ns)) return false;
+        if (!mbar_wait_spin(smem_u32(ds_full), gg & 1, p.wait_ns)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BT / 16; ++kk)  // dK += dSᵀ Q (Q tile read MN-major)
@@ -723,7 +723,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode_kv(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(kv_full), nkv & 1, p.wait_ns)) { ok = false; break; }
+        if (!mbar_wait_spin(smem_u32(kv_full), nkv & 1, p.wait_ns)) { ok = false; break; }
         ++nkv;
         tc_fence_after();
         const uint32_t g0 = g;
@@ -1011,7 +1011,7 @@ __global__ void __launch_bounds__(kThreadsQ2, 1)
         const int i = snake_item(r);
         if (i >= p.items) continue;
         const Item it = decode(i, p.B, p.H, p.nq, p.causal);
-        if (!mbar_wait(smem_u32(q_full), k & 1, p.wait_ns)) { ok = false; break; }
+        if (!mbar_wait_spin(smem_u32(q_full), k & 1, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         bool first = true;
         #pragma unroll 1
@@ -1019,22 +1019,22 @@ __global__ void __launch_bounds__(kThreadsQ2, 1)
           const uint32_t gt = gt0 + uint32_t(j);
           const int slot = int(gt % Q2_RING);
           const uint32_t kvs = sb + Q2Smem::KV + uint32_t(slot) * 2 * TILE;
-          if (*abort_flag || !mbar_wait(smem_u32(&kv_full[slot]), (gt / Q2_RING) & 1, p.wait_ns)) { ok = false; break; }
+          if (*abort_flag || !mbar_wait_spin(smem_u32(&kv_full[slot]), (gt / Q2_RING) & 1, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)  // S = Q Kᵀ
             tc_mma<false>(tS, smem_desc(sb + Q2Smem::Q + kk * 32, 16, 1024), smem_desc(kvs + kk * 32, 16, 1024),
                           IDESC_S, kk > 0 ? 1u : 0u);
           tc_commit(smem_u32(&b[0]));
-          if (!mbar_wait(smem_u32(&b[1]), t & 1, p.wait_ns)) { ok = false; break; }  // the rows have loaded S
+          if (!mbar_wait_spin(smem_u32(&b[1]), t & 1, p.wait_ns)) { ok = false; break; }  // the rows have loaded S
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)  // dP = dO Vᵀ into the same columns
             tc_mma<false>(tS, smem_desc(sb + Q2Smem::DO + kk * 32, 16, 1024),
                           smem_desc(kvs + TILE + kk * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
           tc_commit(smem_u32(&b[2]));
-          if (!mbar_wait(smem_u32(&b[3]), t & 1, p.wait_ns)) { ok = false; break; }  // dS written, dP read
-          if (first && !mbar_wait(smem_u32(acc_free), (k & 1) ^ 1, p.wait_ns)) { ok = false; break; }
+          if (!mbar_wait_spin(smem_u32(&b[3]), t & 1, p.wait_ns)) { ok = false; break; }  // dS written, dP read
+          if (first && !mbar_wait_spin(smem_u32(acc_free), (k & 1) ^ 1, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)  // dQ_s += dS K (K tile read MN-major)

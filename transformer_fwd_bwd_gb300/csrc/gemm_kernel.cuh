@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fetch();
           continue;
         }
-        if (!mbar_wait(smem_u32(&tempty[ab]), aphase ^ 1, p.wait_ns)) { give_up(); break; }
+        if (!mbar_wait_spin(smem_u32(&tempty[ab]), aphase ^ 1, p.wait_ns)) { give_up(); break; }
         tc_fence_after();
         const uint32_t d_tmem = tbase + uint32_t(ab * BN);
         bool ok = true;
