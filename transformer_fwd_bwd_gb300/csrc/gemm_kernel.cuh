@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb0 = ti.n0 + rank * BNH;  // this CTA's rows of B
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
           if (*abort_flag) break;
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.wait_ns)) { give_up(); break; }
+          if (!mbar_wait_spin(smem_u32(&empty[stage]), phase ^ 1, p.wait_ns)) { give_up(); break; }
           uint32_t fb = smem_u32(&full[stage]);
           if (rank == 0) mbar_expect_tx(fb, CG * C_::STAGE_BYTES);
           if constexpr (CG == 2) fb = mapa_shared(fb, 0);
