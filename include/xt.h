@@ -426,9 +426,13 @@ int xt_matmul_workspace_size(const xt_matmul_desc* desc, size_t* bytes);
 int xt_gemm_set_schedule(int mode);
 /* Process-wide override of the paired-CTA GEMM (bf16 operands, no causal mode, no GELU
  * epilogue): two CTAs of a cluster compute one 256-row tile with the paired tensor-core MMA,
- * each staging its own 128 rows of A and half of B's rows.  0 = the time model's choice
- * (default), 1 = never, 2 = wherever allowed.  Either kernel accumulates in fp32 over the
- * same K order; the choice is deterministic for a given shape.  XT_ERR_INVALID_ARG otherwise. */
+ * each staging its own 128 rows of A and half of B's rows.  Its multicast form runs clusters
+ * of two such pairs on vertically adjacent 256 × 256 tiles (whole tiles, an even number of
+ * 256-row tiles), each CTA loading half of its B rows for both pairs.  0 = the time model's
+ * choice (default; never the multicast form, which measured slower than the plain pairs on
+ * the 12-layer stack's shapes), 1 = never, 2 = the plain pairs wherever allowed, 3 = the
+ * multicast form wherever allowed (else as 2).  Every kernel accumulates in fp32 over the same K order; the
+ * choice is deterministic for a given shape.  XT_ERR_INVALID_ARG otherwise. */
 int xt_gemm_set_pairing(int mode);
 /* Process-wide override of the GEMM tile width: 0 = the time model's choice (default), else
  * BN ∈ {64, 128, 192, 256} wherever it is a candidate for the problem (the model's choice

@@ -166,7 +166,111 @@ def test_pair_matches_single():
 
 def test_gemm_set_pairing_rejects():
     with pytest.raises(xt.XtError):
-        xt.gemm_set_pairing(3)
+        xt.gemm_set_pairing(4)
+
+
+@pytest.fixture
+def multicast():
+    """Forces the multicast form of the paired kernel for one test; restores the model's choice."""
+    xt.gemm_set_pairing(3)
+    yield
+    xt.gemm_set_pairing(0)
+
+
+# even numbers of 256-row tiles (a cluster's two pairs take vertically adjacent tiles): one
+# tile group, ragged M / N / K (the out-of-range rows of a multicast half arrive zero-filled),
+# several groups per cluster
+MC_CASES = [(512, 256, 128), (384, 264, 72), (1000, 776, 328), (2048, 1536, 520), (4096, 2304, 768)]
+
+
+@pytest.mark.parametrize("c", ["f32", "bf16"])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", MC_CASES)
+def test_pair_multicast_fwd(c, ta, tb, M, N, K, multicast):
+    """Clusters of two pairs sharing B by TMA multicast, every operand majorness, against the
+    oracle with the whole-tile bounds; the launch record shows the multicast form ran."""
+    A = synth.normal((K, M) if ta else (M, K), 160, dtype="bf16")
+    B = synth.normal((N, K) if tb else (K, N), 161, dtype="bf16")
+    want = O.matmul_fwd(op(A, ta), op(B, tb)) * 0.5
+    C = empty((M, N), c)
+    d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, alpha=0.5)
+    rec = records(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), C))
+    assert len(rec) == 1 and rec[0][0] == 2256, rec
+    e = norm_err(host(C), want)
+    assert e <= (1e-5 if c == "f32" else 4e-3), f"normalised error {e:.2e}"
+    assert xt.device_errors() == 0
+
+
+@pytest.mark.parametrize("c", ["f32", "bf16"])
+def test_pair_multicast_accumulate(c, multicast):
+    """C += A@B on the multicast form: fp32 C through the TMA reduce-add, bf16 C direct."""
+    M, N, K = 1024, 520, 200
+    A = synth.normal((M, K), 162, dtype="bf16")
+    B = synth.normal((K, N), 163, dtype="bf16")
+    C0 = synth.normal((M, N), 164, dtype=c)
+    Cd = dev(C0, c)
+    d = xt.matmul_desc(M, N, K, dtype_c=xt.XT_F32 if c == "f32" else xt.XT_BF16, accumulate=1)
+    rec = records(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), Cd))
+    assert rec[0][0] == 2256, rec
+    assert norm_err(host(Cd), C0 + A @ B) <= (1e-5 if c == "f32" else 8e-3)
+    assert xt.device_errors() == 0
+
+
+@pytest.mark.parametrize("tb", [0, 1])
+def test_pair_multicast_matches_pair(tb):
+    """The multicast form runs the same MMAs in the same K order on the same tiles as the plain
+    pairs: bit-identical results, and identical on a rerun."""
+    M, N, K = 2048, 1280, 1000
+    A = synth.normal((M, K), 165, dtype="bf16")
+    B = synth.normal((N, K) if tb else (K, N), 166, dtype="bf16")
+    d = xt.matmul_desc(M, N, K, trans_b=tb)
+    Ad, Bd = dev(A, "bf16"), dev(B, "bf16")
+    outs = []
+    try:
+        xt.gemm_set_tile(256)
+        for mode, code in ((2, 1256), (3, 2256), (3, 2256)):
+            xt.gemm_set_pairing(mode)
+            C = empty((M, N))
+            rec = records(lambda: xt.xt_matmul_fwd(d, Ad, Bd, C))
+            assert rec[0][0] == code, rec
+            outs.append(host(C))
+    finally:
+        xt.gemm_set_pairing(0)
+        xt.gemm_set_tile(0)
+    assert norm_err(outs[0], A @ op(B, tb)) <= 1e-5
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    assert xt.device_errors() == 0
+
+
+def test_pair_multicast_needs_even_tile_rows(multicast):
+    """An odd number of 256-row tiles leaves the second pair of a cluster without a tile: the
+    plain pairs run instead."""
+    M, N, K = 768, 512, 256
+    A = synth.normal((M, K), 167, dtype="bf16")
+    B = synth.normal((K, N), 168, dtype="bf16")
+    C = empty((M, N))
+    d = xt.matmul_desc(M, N, K)
+    rec = records(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), C))
+    assert 1000 < rec[0][0] < 2000, rec
+    assert norm_err(host(C), A @ B) <= 1e-5
+
+
+@pytest.mark.parametrize("M,N,K,ta,tb", [(8192, 3072, 768, 0, 0), (8192, 3072, 768, 0, 1), (8192, 768, 3072, 0, 1),
+                                         (8192, 2304, 768, 0, 0), (8192, 50304, 768, 0, 1)])
+def test_pair_multicast_full_size_sampled(M, N, K, ta, tb, multicast):
+    """The stack's 8192-row GEMM shapes on the multicast form, sampled rows (both pairs' tiles of
+    a group, both CTAs' halves of a tile, the last row) against the oracle's product of those rows."""
+    A = synth.normal((K, M) if ta else (M, K), 169, std=0.5, dtype="bf16")
+    B = synth.normal((N, K) if tb else (K, N), 170, std=0.02, dtype="bf16")
+    Cm = empty((M, N), "bf16")
+    d = xt.matmul_desc(M, N, K, trans_a=ta, trans_b=tb, dtype_c=xt.XT_BF16)
+    rec = records(lambda: xt.xt_matmul_fwd(d, dev(A, "bf16"), dev(B, "bf16"), Cm))
+    assert len(rec) == 1 and rec[0][0] == 2256, rec
+    rows = np.random.default_rng(3).choice(M, 24, replace=False)
+    rows = np.concatenate([rows, [0, 127, 128, 255, 256, 383, 384, 511, M - 1]])
+    want = op(A, ta)[rows] @ op(B, tb)
+    assert norm_err(host(Cm[torch.tensor(rows, device="cuda")]), want) <= 4e-3
+    assert xt.device_errors() == 0
 
 
 @pytest.mark.parametrize("ta", [0, 1])

@@ -94,7 +94,8 @@ static double pair_eff(int bn) { return bn >= 256 ? 1.15 : bn >= 192 ? 1.0 : 0.7
 // split where one is allowed, 3 stream-K over every SM where allowed, 4 stream-K in lockstep
 // K slices where allowed.
 static int g_schedule = 0;
-// Paired-kernel override (xt_gemm_set_pairing): 0 the model's choice, 1 never, 2 wherever allowed.
+// Paired-kernel override (xt_gemm_set_pairing): 0 the model's choice, 1 never, 2 wherever allowed,
+// 3 the multicast form of the paired kernel wherever allowed (else as 2).
 static int g_pairing = 0;
 // Tile-width override (xt_gemm_set_tile): 0 the model's choice, else that BN wherever it is a
 // candidate.
@@ -123,9 +124,10 @@ Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int c
   double best_t = 1e300;
 
   // forced modes: the forced kind of candidate first, whole tiles when it is not allowed
-  auto weigh = [&](double t, int kind, int cg) {  // kind 1 tiles, 2 K split, 3 stream-K all units, 4 lockstep
+  auto weigh = [&](double t, int kind, int cg, int mc = 1) {  // kind 1 tiles, 2 K split, 3 stream-K all units, 4 lockstep
     if (mode >= 2) t *= (kind == mode) ? 1e-6 : (kind == 1 ? 1.0 : 1e6);
-    if (g_pairing == 2 && cg == 2) t *= 1e-12;
+    if (g_pairing >= 2 && cg == 2) t *= 1e-12;
+    if (g_pairing == 3 && mc == 2) t *= 1e-12;
     return t;
   };
   auto tile_weight = [&](int bn) { return g_tile != 0 && bn != g_tile ? 1e18 : 1.0; };
@@ -164,6 +166,23 @@ Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int c
         Choice ch{bn, s, 0, 0};
         ch.cg = cg;
         offer(weigh(t, s > 1 ? 2 : 1, cg) * tile_weight(bn), ch);
+      }
+      // multicast pairs (only when forced: graph-timed against the plain pairs at BN 256 they
+      // were slower on every shape of the 12-layer stack, 38.2 against 29.2 µs at 8192 × 3072 ×
+      // 768 and 504 against 379 µs on the logits): whole 256-wide tiles, an even number of
+      // 256-row tiles (the two pairs of a cluster take vertically adjacent ones), in clusters
+      // that can be resident at once
+      const int64_t num_m = ceil_div(M, bm);
+      if (g_pairing == 3 && cg == 2 && bn == 256 && causal == 0 && num_m % 2 == 0 && (mode == 0 || mode == 1)) {
+        const int mcu = mc_capacity();
+        if (mcu > 0) {
+          const double rounds = double(ceil_div(tiles / 2, mcu));
+          const double t = rounds * (2.0 * bm * bn * double(K) / (rate * eff) + 1.5e-6);
+          Choice ch{bn, 1, 0, 0};
+          ch.cg = 2;
+          ch.mc = 2;
+          offer(weigh(t, 1, cg, 2) * tile_weight(bn), ch);
+        }
       }
       if (!sk_ok) continue;
       const int64_t iters = tiles * kbt;
@@ -259,7 +278,8 @@ int run(const Problem& pb, cudaStream_t s) {
   if (pb.act == 1) XT_TRY(make_output_map(&tc2, pb.C2, true, pb.M, pb.N, pb.ldc, 1, 1, 0, 0));
   const int kind = pb.fp8 ? kFp8 : tf32 ? kTf32 : kBf16;
   XT_TRY(make_operand_map(&ta, pb.A, kind, BM, k_atoms(cg)));
-  XT_TRY(make_operand_map(&tb, pb.B, kind, bn / cg, k_atoms(cg)));  // a pair's CTA stages half of B's rows
+  // a pair's CTA stages half of B's rows; a multicast pair's CTA loads half of those
+  XT_TRY(make_operand_map(&tb, pb.B, kind, bn / cg / ch.mc, k_atoms(cg)));
   // TMA epilogue for every output except a bf16 C that is accumulated into (TMA reduce-add is
   // used for float32 only; bf16 accumulation keeps the direct read-modify-write stores).  A K
   // split stores float32 partial tiles into [splits][M][N] slices instead.
@@ -300,7 +320,13 @@ int run(const Problem& pb, cudaStream_t s) {
   const int64_t tiles = int64_t(p.num_m) * p.num_n * p.batches;  // a K split counts its slices
   if (tiles > int64_t(1) << 30) return fail(XT_ERR_UNSUPPORTED, "matmul: too many tiles");
   int grid;
-  if (cg == 2) {
+  if (ch.mc == 2) {
+    const int units = mc_capacity();
+    if (units < 1) return fail(XT_ERR_CUDA, "gemm: no cluster of two pairs can be resident");
+    if (p.num_m % 2 || p.sk || p.splitk > 1) return fail(XT_ERR_INVALID_ARG, "gemm: bad multicast schedule");
+    const int64_t groups = tiles / 2;
+    grid = 4 * int(groups < units ? groups : units);
+  } else if (cg == 2) {
     const int units = pair_capacity();
     if (units < 1) return fail(XT_ERR_CUDA, "gemm: no CTA pair can be resident");
     grid = 2 * int(tiles < units ? tiles : units);
@@ -325,8 +351,8 @@ int run(const Problem& pb, cudaStream_t s) {
   void* tok = nullptr;
   // record: causal mode, or 10 × K splits, or 1000 for stream-K over every SM, 1000 + slices
   // for stream-K in lockstep K slices
-  // (the tile width of a paired launch is recorded as 1000 + BN)
-  const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, cg == 2 ? 1000 + bn : bn, int(amn), int(bmn),
+  // (the tile width of a paired launch is recorded as 1000 + BN, of a multicast pair as 2000 + BN)
+  const int shape[8] = {p.M, p.N, p.K, split ? ch.splits : p.batches, cg == 2 ? 1000 * ch.mc + bn : bn, int(amn), int(bmn),
                         ch.sk == 1 ? 1000 : ch.sk == 2 ? 1000 + int(ch.grid / cg / tiles) :
                         split ? 10 * ch.splits : p.causal};
   unsigned long long* ts = nullptr;
@@ -336,7 +362,7 @@ int run(const Problem& pb, cudaStream_t s) {
   int st = pb.fp8    ? launch_fp8(bn, ta, tb, tc, tc2, p, grid, s)
            : tf32    ? launch_tf32(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
            : pb.act ? launch_bf16_act(pb.act, amn, bmn, ta, tb, tc, tc2, p, grid, s)
-           : cg == 2 ? launch_bf16_pair(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s)
+           : cg == 2 ? launch_bf16_pair(bn, ch.mc, amn, bmn, ta, tb, tc, tc2, p, grid, s)
                     : launch_bf16(bn, amn, bmn, ta, tb, tc, tc2, p, grid, s);
   if (st == XT_OK && split) {
     const int64_t work = pb.M * (pb.N / 4);
@@ -541,7 +567,7 @@ int xt_gemm_set_tile(int bn) {
 }
 
 int xt_gemm_set_pairing(int mode) {
-  XT_REQUIRE(mode >= 0 && mode <= 2, "xt_gemm_set_pairing: mode must be 0..2");
+  XT_REQUIRE(mode >= 0 && mode <= 3, "xt_gemm_set_pairing: mode must be 0..3");
   gemm::g_pairing = mode;
   return XT_OK;
 }

@@ -49,6 +49,7 @@ struct Choice {
   int sk;      // stream-K schedule: 1 over every SM (every resident unit), 2 in lockstep K slices
   int grid;    // stream-K units: the SMs (or pairs), or tiles × K slices (lockstep)
   int cg = 1;  // 2: the paired-CTA kernel, tiles of 2·BM rows, units are CTA pairs
+  int mc = 1;  // 2 (with cg 2): clusters of two pairs sharing B by multicast, units are clusters
 };
 Choice choose(bool tf32, int64_t M, int64_t N, int64_t K, int64_t batches, int causal, bool allow_split,
               bool fp8, bool b_mn);
@@ -74,10 +75,10 @@ int launch_fp8(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 int launch_bf16_act(int act, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                     const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 
-template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0, int CG = 1>
+template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0, int CG = 1, int MC = 1>
 int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                const Params& p, int grid, cudaStream_t s) {
-  auto k = gemm_kernel<KIND, BN, A_MN, B_MN, ACT, CG>;
+  auto k = gemm_kernel<KIND, BN, A_MN, B_MN, ACT, CG, MC>;
   constexpr int smem = Cfg<KIND, BN, CG>::SMEM;
   static bool attr_set = false;  // per instantiation; idempotent if raced
   if (!attr_set) {
@@ -88,8 +89,8 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
     attr_set = true;
   }
   if constexpr (CG == 2) {
-    if (grid % 2) return fail(XT_ERR_INVALID_ARG, "gemm: paired launch needs an even grid");
-    launch_clustered(k, grid, kThreads, smem, s, 2, ta, tb, tc, tc2, p);
+    if (grid % (CG * MC)) return fail(XT_ERR_INVALID_ARG, "gemm: clustered launch needs whole clusters");
+    launch_clustered(k, grid, kThreads, smem, s, CG * MC, ta, tb, tc, tc2, p);
   } else {
     launch(k, grid, kThreads, smem, s, ta, tb, tc, tc2, p);
   }
@@ -97,11 +98,13 @@ int launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& 
 }
 
 // bf16 paired-CTA GEMM (BN 128, 256, or 192 with B K-major; plain epilogue), launched as
-// clusters of two.
-int launch_bf16_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                     const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
+// clusters of two, or with mc = 2 (BN 256) as clusters of two pairs sharing B by multicast.
+int launch_bf16_pair(int bn, int mc, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                     const CUtensorMap& tc, const CUtensorMap& tc2, const Params& p, int grid, cudaStream_t s);
 // CTA pairs of the paired kernel that can be resident at once on the current device (0 if none).
 int pair_capacity();
+// Clusters of two pairs (the multicast form) that can be resident at once (0 if none).
+int mc_capacity();
 
 }  // namespace gemm
 }  // namespace xt

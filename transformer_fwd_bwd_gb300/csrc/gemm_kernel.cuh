@@ -135,6 +135,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// test_wait with acquire at cluster scope: pairs with a remote mbarrier.arrive.release.cluster
+// (the paired kernel's relayed stage arrivals).
+__device__ __forceinline__ bool mbar_test_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_spin_cl(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_test_wait_cl(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
 // Bounded wait that polls with the non-blocking test_wait: the waiting thread sees the phase
 // flip on its next poll instead of after a suspended try_wait wakes, for the MMA issuer's waits
 // on landed operand stages (a few per tile, each on the tensor core's critical path).
@@ -267,6 +289,17 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// Tile load multicast to the CTAs of `mask` (cluster ranks): the box lands at the same
+// shared-memory offset in each of them, and each one's mbarrier at the offset of `bar` receives
+// the bytes that landed in it.
+__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c0, int c1,
+                                               int c2, int c3, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(mask)
+      : "memory");
+}
 template <int CG>
 __device__ __forceinline__ void tmem_alloc_cg(uint32_t dst_smem, uint32_t ncols) {
   if constexpr (CG == 2)
@@ -288,11 +321,11 @@ __device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) 
     tmem_dealloc(taddr, ncols);
 }
 // Arrives on `bar` once this thread's earlier tcgen05 operations have completed: CG = 2 on the
-// barrier at that offset in both CTAs of the pair, CG = 1 on this CTA's barrier only.
+// barrier at that offset in each CTA of `mask` (cluster ranks; a pair's two CTAs by default),
+// CG = 1 on this CTA's barrier only.
 template <int CG>
-__device__ __forceinline__ void tc_commit_cg(uint32_t bar) {
+__device__ __forceinline__ void tc_commit_cg(uint32_t bar, uint16_t mask = 3) {
   if constexpr (CG == 2) {
-    const uint16_t mask = 3;
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(mask)
@@ -509,11 +542,22 @@ __device__ __forceinline__ void sk_fixup(uint32_t tacc, const Params& p, int fir
 // barrier of both CTAs and, per tile, on both CTAs' accumulator-full barriers; both CTAs'
 // epilogues (each draining its own 128 TMEM lanes) arrive on the even CTA's accumulator-empty
 // barrier.  Schedule units (Params::num_m tiles of 2·BM rows, stream-K shares) are pairs.
-template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0, int CG = 1>
+//
+// MC = 2 (clusters of four CTAs, two pairs; whole tiles of a plain schedule only): the two pairs
+// compute vertically adjacent tiles (pair i of the cluster the 2·BM rows of tile 2j + i of a
+// tile group), so both need the same B rows.  Each CTA loads half of its B rows and multicasts
+// it to the CTA at the same place in the other pair: every CTA's B stage is filled by two
+// loads, one from each pair, and a pair reads half the B bytes from L2 that it would alone.  A
+// stage of B in a pair's odd CTA completes on that CTA's own full barrier (a multicast signals
+// the barrier in each receiving CTA), and the odd CTA's warp 1 relays it to the even CTA's full
+// barrier, which then counts two arrivals; the MMAs' commits free a stage in all four CTAs
+// (each empty barrier counts one commit per pair).
+template <int KIND, int BN, bool A_MN, bool B_MN, int ACT = 0, int CG = 1, int MC = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2, const Params p) {
   static_assert(CG == 1 || (CG == 2 && ACT == 0 && BN % 32 == 0), "paired tiles: plain epilogue, BN / 2 whole atoms");
+  static_assert(MC == 1 || (MC == 2 && CG == 2 && BN == 256), "multicast pairs: 256-wide paired tiles");
   // The set-up below (barriers, tensor-map prefetch, TMEM) reads nothing a preceding kernel
   // writes, so it runs before the programmatic-launch wait.
   using C_ = Cfg<KIND, BN, CG>;
@@ -521,8 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t IDESC = instr_desc<KIND, BN, A_MN, B_MN, BM * CG>();
   constexpr uint32_t TCOLS = tmem_cols<BN>();
   constexpr int BNH = BN / CG;  // B rows staged by one CTA
-  const int rank = CG == 2 ? int(cluster_ctarank()) : 0;
-  const int unit = int(blockIdx.x) / CG, units = int(gridDim.x) / CG;
+  constexpr int CL = CG * MC;   // CTAs per cluster
+  // rank: this CTA's place in its pair; pidx: the pair's place in the cluster; leader: the
+  // cluster rank of the pair's even CTA
+  const int crank = CG == 2 ? int(cluster_ctarank()) : 0;
+  const int rank = crank & 1;
+  const int pidx = MC == 2 ? crank >> 1 : 0, leader = MC == 2 ? crank & ~1 : 0;
+  const int unit = int(blockIdx.x) / CL, units = int(gridDim.x) / CL;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -539,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&full[s]), MC == 2 && rank == 0 ? 2 : 1);  // + the odd CTA's relayed arrival
+      mbar_init(smem_u32(&empty[s]), MC);                            // one commit per pair
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -569,10 +618,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   if (p.prof_ts && threadIdx.x == 0) p.prof_ts[2 * blockIdx.x] = global_ns();
 
-  const int total = p.num_m * p.num_n * p.batches;
+  // schedule items: tiles, or with MC = 2 tile groups (two vertically adjacent tiles)
+  const int total = p.num_m * p.num_n * p.batches / MC;
 
   // ti.m0: this CTA's first row (tile row + rank·BM); ti.n0: the tile's first column.
   auto info = [&](int t, int kb0, int kb1) {
+    if constexpr (MC == 2) {  // group t → this pair's tile (m-groups fastest, as tiles are)
+      const int nmg = p.num_m / 2, per_g = nmg * p.num_n;
+      const int z = t / per_g, r = t - z * per_g;
+      const int nb = r / nmg, mg = r - nb * nmg;
+      t = z * (p.num_m * p.num_n) + nb * p.num_m + 2 * mg + pidx;
+    }
     TileInfo ti = tile_info<BK>(t, p);
     const int per = p.num_m * p.num_n;
     const int r = t - (t / per) * per;
@@ -612,9 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
           if (*abort_flag) break;
           if (!mbar_wait_spin(smem_u32(&empty[stage]), phase ^ 1, p.wait_ns)) { give_up(); break; }
-          uint32_t fb = smem_u32(&full[stage]);
-          if (rank == 0) mbar_expect_tx(fb, CG * C_::STAGE_BYTES);
-          if constexpr (CG == 2) fb = mapa_shared(fb, 0);
+          const uint32_t fb_own = smem_u32(&full[stage]);
+          uint32_t fb = fb_own;
+          if constexpr (MC == 2) mbar_expect_tx(fb_own, rank == 0 ? 2 * C_::A_BYTES + C_::B_BYTES : C_::B_BYTES);
+          else if (rank == 0) mbar_expect_tx(fb, CG * C_::STAGE_BYTES);
+          if constexpr (CG == 2) fb = mapa_shared(fb, leader);
           const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
           const uint32_t b_s = a_s + C_::A_BYTES;
           const int k0 = kb * BK;
@@ -626,7 +684,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < BM / ATOM; ++j)
               load(a_s + j * (BK * 128), &tmA, fb, ti.m0 + j * ATOM, k0, ti.ozi, ti.ozo);
           }
-          if constexpr (!B_MN) {
+          if constexpr (MC == 2) {
+            // this CTA's half of its B rows, to itself and to its place in the other pair
+            const uint16_t mask = uint16_t((1u << rank) | (1u << (rank + 2)));
+            if constexpr (!B_MN) {
+#pragma unroll
+              for (int c = 0; c < C_::KA; ++c)
+                tma_load_4d_mc(b_s + c * (BNH * 128) + pidx * (BNH / 2 * 128), &tmB, fb_own, k0 + c * ATOM,
+                               nb0 + pidx * (BNH / 2), ti.ozi, ti.ozo, mask);
+            } else {
+              static_assert(!B_MN || BNH == 2 * ATOM, "MN-major B: one atom-wide box per pair");
+              tma_load_4d_mc(b_s + pidx * (BK * 128), &tmB, fb_own, nb0 + pidx * ATOM, k0, ti.ozi, ti.ozo, mask);
+            }
+          } else if constexpr (!B_MN) {
 #pragma unroll
             for (int c = 0; c < C_::KA; ++c) load(b_s + c * (BNH * 128), &tmB, fb, k0 + c * ATOM, nb0, ti.ozi, ti.ozo);
           } else {
@@ -680,7 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tbase + uint32_t(ab * BN);
         bool ok = true;
         for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
-          if (*abort_flag || !mbar_wait_spin(smem_u32(&full[stage]), phase, p.wait_ns)) { ok = false; break; }
+          const bool landed = MC == 2 ? mbar_wait_spin_cl(smem_u32(&full[stage]), phase, p.wait_ns)
+                                      : mbar_wait_spin(smem_u32(&full[stage]), phase, p.wait_ns);
+          if (*abort_flag || !landed) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_s = smem_u32(smem + stage * C_::STAGE_BYTES);
           const uint32_t b_s = a_s + C_::A_BYTES;
@@ -695,19 +767,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma<KIND, CG>(d_tmem, ad, bd, IDESC, (kb > ti.kb_begin || kk > 0) ? 1u : 0u);
           }
           any = true;
-          tc_commit_cg<CG>(smem_u32(&empty[stage]));  // frees the smem slot(s) once these MMAs finish
+          // frees the smem slot(s) once these MMAs finish: a multicast stage in all four CTAs
+          tc_commit_cg<CG>(smem_u32(&empty[stage]), MC == 2 ? uint16_t(0xF) : uint16_t(3));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
           if (!fetched) fetch();
         }
         if (!ok) { give_up(); break; }
-        tc_commit_cg<CG>(smem_u32(&tfull[ab]));  // accumulator ready for the epilogue(s)
+        tc_commit_cg<CG>(smem_u32(&tfull[ab]), uint16_t(3u << leader));  // accumulator ready for the epilogue(s)
         if (++ab == 2) { ab = 0; aphase ^= 1; }
       }
       // every MMA issued has completed (also after a give-up) before TMEM is released
       if (any) {
-        tc_commit_cg<CG>(smem_u32(mma_done));  // (a pair's odd CTA receives an unused arrival)
+        tc_commit_cg<CG>(smem_u32(mma_done), uint16_t(3u << leader));  // (the odd CTA's arrival is unused)
         if (!mbar_wait(smem_u32(mma_done), 0)) give_up();
       }
+    } else if (MC == 2 && lane == 0 && rank == 1) {
+      // ------------------------------------------------ relay of the odd CTA's B stages
+      // The multicast halves of this CTA's B rows complete on its own full barrier; each
+      // completed stage is passed on to the even CTA's full barrier, where the MMA issuer waits.
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint32_t full_at = mapa_shared(smem_u32(&full[0]), leader);
+      Cursor cur = cursor_begin(p, unit, units);
+      int t, kb0, kb1;
+      bool ok = true;
+      while (ok && !*abort_flag && cursor_next(cur, p, total, units, t, kb0, kb1)) {
+        const TileInfo ti = info(t, kb0, kb1);
+        if (ti.skip) continue;
+        for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (*abort_flag || !mbar_wait_spin(smem_u32(&full[stage]), phase, p.wait_ns)) { ok = false; break; }
+          mbar_arrive_cluster(full_at + uint32_t(stage * 8));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) give_up();
     }
   } else {
     // -------------------------------------------------------------------- epilogue
@@ -718,10 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aphase = 0;
     uint32_t chunk = 0;  // staged stores issued by this warp (selects the staging buffer)
-    const int self = unit * CG + rank;  // this CTA's stream-K slot and flags
+    const int self = (unit * MC + pidx) * CG + rank;  // this CTA's stream-K slot and flags
     // this warp's share of freeing accumulator ab: a pair's barrier is in the even CTA
     const uint32_t tempty0 = smem_u32(&tempty[0]);
-    const uint32_t tempty_at = CG == 2 ? mapa_shared(tempty0, 0) : tempty0;
+    const uint32_t tempty_at = CG == 2 ? mapa_shared(tempty0, leader) : tempty0;
     auto release_acc = [&](int b) {
       if (CG == 2 && rank != 0) mbar_arrive_cluster(tempty_at + uint32_t(b * 8));
       else mbar_arrive(tempty0 + uint32_t(b * 8));

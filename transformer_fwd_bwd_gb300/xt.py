@@ -277,7 +277,8 @@ def gemm_set_schedule(mode: int):
 
 
 def gemm_set_pairing(mode: int):
-    """0 model's choice, 1 never the paired-CTA kernel, 2 the paired kernel wherever allowed."""
+    """0 model's choice, 1 never the paired-CTA kernel, 2 the paired kernel wherever allowed, 3 its
+    multicast form (two pairs of a cluster sharing B) wherever allowed."""
     call("xt_gemm_set_pairing", int(mode))
 
 
