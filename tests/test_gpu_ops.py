@@ -130,7 +130,8 @@ def test_sum(dtype, n):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("rows,cols", ROWS_COLS)
+# (8192, 768): the stack's size, every block's dγ partial carried over several rows per warp
+@pytest.mark.parametrize("rows,cols", ROWS_COLS + [(8192, 768)])
 def test_rms_norm(dtype, rows, cols):
     x = inputs((rows, cols), 7, dtype)
     gamma = inputs((cols,), 8, dtype, std=0.1, mean=1.0)
@@ -147,7 +148,8 @@ def test_rms_norm(dtype, rows, cols):
     DX, DG = empty((rows, cols), dtype), empty((cols,), "f32")
     xt.xt_rms_norm_bwd(Dd, X, G, IRo, DX, DG); sync()
     irr = np.float32(ir).astype(np.float64)
-    mag_dx = np.abs(irr[:, None] * d * gamma) + np.abs(x * (irr ** 3 / cols * np.sum(d * gamma * x, 1))[:, None])
+    # the row reduction Σ d·γ·x cancels: its rounding is relative to Σ|d·γ·x|, not to |Σ d·γ·x|
+    mag_dx = np.abs(irr[:, None] * d * gamma) + np.abs(x * (irr ** 3 / cols * np.sum(np.abs(d * gamma * x), 1))[:, None])
     check(host(DX), dx, dtype, "rms dx", mag=mag_dx)
     check_sum(host(DG), dg, np.abs(d * x * ir[:, None]).sum(0), "f32", "rms dgamma")
     # accumulate paths: dx += , dγ +=
@@ -160,8 +162,9 @@ def test_rms_norm(dtype, rows, cols):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 # (1500, 2048): a bf16 row of 2048 runs with 128 threads of two vectors, two rows per block, and
-# 1500 rows give each block two or three row pairs (the partials carried across rows)
-@pytest.mark.parametrize("rows,cols", ROWS_COLS + [(1500, 2048)])
+# 1500 rows give each block two or three row pairs (the partials carried across rows);
+# (8192, 768): the stack's size (304 blocks of eight row warps, three or four rows per warp)
+@pytest.mark.parametrize("rows,cols", ROWS_COLS + [(1500, 2048), (8192, 768)])
 def test_layernorm(dtype, rows, cols):
     x = inputs((rows, cols), 10, dtype, mean=0.3)
     gamma = inputs((cols,), 11, dtype, std=0.1, mean=1.0)
@@ -191,6 +194,31 @@ def test_layernorm(dtype, rows, cols):
     xh = (x - mu32[:, None]) * rs32[:, None]
     check_sum(host(DG), dg, np.abs(d * xh).sum(0), "f32", "ln dgamma")
     check_sum(host(DB), db, np.abs(d).sum(0), "f32", "ln dbeta")
+
+
+def test_layernorm_bwd_stack_form():
+    """LayerNorm backward as the 12-layer stack calls it at B 8 × S 1024, d 768: bf16 d, x and γ,
+    the float32 residual gradient accumulated (dh += dx), and float32 dγ / dβ accumulated."""
+    rows, cols = 8192, 768
+    x = inputs((rows, cols), 14, "bf16", mean=0.3)
+    gamma = inputs((cols,), 15, "bf16", std=0.1, mean=1.0)
+    d = inputs((rows, cols), 16, "bf16")
+    dh0 = inputs((rows, cols), 17, "f32")
+    dg0, db0 = inputs((cols,), 18, "f32"), inputs((cols,), 19, "f32")
+    _, mu, rstd = O.layernorm_fwd(x, gamma, np.zeros(cols), 1e-5)
+    mu32, rs32 = np.float32(mu).astype(np.float64), np.float32(rstd).astype(np.float64)
+    dx, dg, db = O.layernorm_bwd(d, x, gamma, mu32, rs32)
+    DH, DG, DB = dev(dh0, "f32"), dev(dg0, "f32"), dev(db0, "f32")
+    xt.xt_layernorm_bwd(dev(d, "bf16"), dev(x, "bf16"), dev(gamma, "bf16"), dev(mu32), dev(rs32), DH, DG, DB,
+                        acc_dx=1, acc_param=1); sync()
+    scale = np.max(np.abs(rs32[:, None] * d * gamma), axis=1, keepdims=True)
+    tol = 1e-5 * (np.abs(dh0) + np.maximum(np.abs(dx), 1e-3 * scale)) + 1e-6 * scale
+    g = host(DH)
+    assert np.all(np.abs(g - (dh0 + dx)) <= tol), f"dh max excess {np.max(np.abs(g - dh0 - dx) / tol):.3f}"
+    xh = (x - mu32[:, None]) * rs32[:, None]
+    check_sum(host(DG), dg0 + dg, np.abs(dg0) + np.abs(d * xh).sum(0), "f32", "ln dgamma acc")
+    check_sum(host(DB), db0 + db, np.abs(db0) + np.abs(d).sum(0), "f32", "ln dbeta acc")
+    assert xt.device_errors() == 0
 
 
 # ----------------------------------------------------------------------------- softmax
